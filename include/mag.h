@@ -1,0 +1,242 @@
+/*
+ * mag -- the single-token decode step of a GQA transformer with 4-bit
+ * group-quantised weights (W4A16) and a block-pooled KV cache in FP16, INT8
+ * or INT4, on one GB300 (sm_103a). C ABI.
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [Magnitude] "Magnitude: on-device AI-agent inference engine --
+ *               self-optimising scheduling and elastic memory pools"
+ *               (0539edu.com): 4.3 engine config and construction,
+ *               4.4 inference calls, 5.1 context overflow, 5.2 memory stats.
+ *   [Core]      "5. Core modules: format, runtime, scheduling, memory and
+ *               routing" (ai-infra.cypggs.com): 5.1 packager (W4A16, merged
+ *               QKV and gate-up, pre-generated RoPE table, shapes in the
+ *               package), 5.2 runtime (preallocated KV pool, static shapes,
+ *               allocation-free decode loop), 5.4 KV capacity planning.
+ *   [TFLite]    "TFLite memory planner" (pwwt.cn): 2.1-2.2 lifetime analysis
+ *               and greedy-by-size arena, 3.2 preserve-all debug mode and
+ *               externally owned I/O buffers.
+ *
+ * Conventions for every call:
+ *   - Ownership: the library owns every device allocation it makes (weights,
+ *     KV pool, block tables, RoPE table, activation arena, graphs). The caller
+ *     owns the CUDA stream and every input/output buffer it passes; those are
+ *     never placed in the arena ([TFLite] 3.2, external buffers).
+ *   - Ordering: calls are ordered on the context's stream (given at create);
+ *     except where stated they return without synchronising the host.
+ *   - Errors: every call returns mag_status. Argument and capacity errors are
+ *     found on the host before anything is launched and leave the context
+ *     unchanged (no partial append). mag_last_error() gives a message.
+ *   - Threads: one context is used by one host thread at a time.
+ *   - Pointers named *_dev are device pointers; *_host are host pointers.
+ */
+#ifndef MAG_H
+#define MAG_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MAG_OK = 0,
+  MAG_ERR_INVALID_ARG = 1,  /* bad shape, pointer, id, size or format */
+  MAG_ERR_OOM = 2,          /* a device or pinned-host allocation failed */
+  MAG_ERR_KV_FULL = 3,      /* the block pool has too few free blocks */
+  MAG_ERR_CONTEXT_FULL = 4, /* a session would pass max_context (never truncated) */
+  MAG_ERR_NOT_LOADED = 5,   /* a step was asked for before every weight was loaded */
+  MAG_ERR_CUDA = 6,         /* a CUDA runtime call failed (message says which) */
+  MAG_ERR_TIMEOUT = 7,      /* a bounded device-side wait gave up */
+  MAG_ERR_UNSUPPORTED = 8   /* a shape or mode this build does not handle */
+} mag_status;
+
+typedef enum { MAG_KV_FP16 = 0, MAG_KV_INT8 = 1, MAG_KV_INT4 = 2 } mag_kv_dtype;
+
+/* Flags. */
+#define MAG_FLAG_NO_GRAPH ((uint64_t)1)        /* launch kernels one by one instead of replaying a CUDA graph */
+#define MAG_FLAG_ARENA_NO_REUSE ((uint64_t)2)  /* give every arena tensor its own bytes ([TFLite] 3.2 preserve-all) */
+#define MAG_FLAG_NO_PDL ((uint64_t)4)          /* no programmatic dependent launch between kernels */
+
+/* Model shape and capacities ([Core] 5.1: the shape travels with the model;
+ * [Core] 5.2: everything sized once, up front; [Magnitude] 4.3: EngineConfig). */
+typedef struct mag_config {
+  int32_t n_layers;
+  int32_t hidden;     /* D */
+  int32_t n_heads;    /* Hq */
+  int32_t n_kv_heads; /* Hkv; Hq % Hkv == 0, query head h reads KV head h / (Hq/Hkv) */
+  int32_t head_dim;   /* d: 64 or 128 */
+  int32_t ffn;        /* F */
+  int32_t vocab;      /* V; 0 = no LM head, the step outputs the fp16 hidden state */
+  float rms_eps;
+  float rope_base;
+  int32_t kv_dtype;     /* mag_kv_dtype */
+  int32_t block_tokens; /* tokens per KV block; must be 16 */
+  int32_t pool_blocks;  /* P, blocks in the pool (each covers every layer) */
+  int32_t max_sessions;
+  int32_t max_batch;   /* sessions per decode step, 1..16 */
+  int32_t max_chunk;   /* tokens per prefill chunk; 0 = prefill not used */
+  int32_t max_context; /* tokens a session may hold */
+  const int32_t* pool_order_host; /* initial free-list order, a permutation of 0..P-1; NULL = 0,1,..,P-1 */
+  uint64_t flags;                 /* MAG_FLAG_* */
+} mag_config;
+
+typedef struct mag_ctx mag_ctx;
+
+/* Create a context: validates the shape, plans the activation arena
+ * ([TFLite] 2.1-2.2, 64-byte aligned offsets), allocates the weight region,
+ * the KV pool of pool_blocks blocks ([Core] 5.2) and the block tables, and
+ * builds the RoPE cos/sin table on the host in double, stored as fp32
+ * ([Core] 5.1, rope table pre-generation). `cuda_stream` is a cudaStream_t
+ * on which all work of the context is ordered (NULL: the context creates and
+ * owns a stream that synchronises with the legacy default stream).
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA; *out is NULL on error. */
+mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out);
+
+/* Free everything the context owns (synchronises its stream first). NULL is a no-op. */
+void mag_destroy(mag_ctx* ctx);
+
+/* Tensors of mag_load_weights. Projections are merged as [Core] 5.1 rewrites
+ * them: QKV rows [q (Hq*d); k (Hkv*d); v (Hkv*d)], gate-up rows [gate (F); up (F)]. */
+typedef enum {
+  MAG_W_QKV = 0,      /* [(Hq+2Hkv)d, D] */
+  MAG_W_O = 1,        /* [D, Hq*d] */
+  MAG_W_GATE_UP = 2,  /* [2F, D] */
+  MAG_W_DOWN = 3,     /* [D, F] */
+  MAG_NORM_ATTN = 4,  /* gain [D] before attention */
+  MAG_NORM_FFN = 5,   /* gain [D] before the FFN */
+  MAG_NORM_FINAL = 6, /* gain [D] before the LM head (layer ignored) */
+  MAG_LM_HEAD = 7     /* [V, D] fp16 (layer ignored) */
+} mag_tensor;
+
+/* Source formats. W4G32 is the packed 4-bit group-32 layout ([Core] 5.1
+ * W4A16; the byte layout is this library's): a matrix [N, K] has G =
+ * ceil(K/32) groups per row; its bytes are the codes u8 [N][16G] (byte j of a
+ * group holds code 2j in the low nibble and code 2j+1 in the high nibble,
+ * ragged last group padded with code 0) immediately followed by the fp16
+ * (scale, min) pairs [N][G][2]; element k of a row is scale*code + min. */
+typedef enum {
+  MAG_FMT_F32_DENSE = 0, /* fp32 row-major [N, K]; quantised to W4G32 on the device (projections only) */
+  MAG_FMT_W4G32 = 1,     /* already packed (projections only) */
+  MAG_FMT_F16 = 2        /* fp16 (norm gains, LM head) */
+} mag_format;
+
+/* Load one tensor from device memory `src_dev` of `bytes` bytes (which must
+ * equal the size the format and shape imply). FP32_DENSE is quantised on the
+ * device by the rule of mag_quantize_w4g32. Ordered on the stream; src_dev
+ * may be reused once the stream reaches this point.
+ * Errors: INVALID_ARG (id, layer, format, size), CUDA. */
+mag_status mag_load_weights(mag_ctx* ctx, int32_t tensor, int32_t layer, const void* src_dev, int32_t src_format,
+                            size_t bytes);
+
+/* Sessions: each holds its own block table and length. Close returns its
+ * blocks to the back of the free list. Errors: INVALID_ARG, and OOM-like
+ * MAG_ERR_INVALID_ARG when max_sessions are open. */
+mag_status mag_session_open(mag_ctx* ctx, int32_t* session_out);
+mag_status mag_session_close(mag_ctx* ctx, int32_t session);
+mag_status mag_session_length(mag_ctx* ctx, int32_t session, int32_t* length_out);
+
+/* Append n_tokens of already-rotated K and V to a session's cache, fp16
+ * [L][n_tokens][Hkv][d] each, quantised on store to the pool precision
+ * (INT8: one fp16 scale per token and head, s = fp16(max|x|/127), q =
+ * rint(x/s) clamped to +-127; INT4: the W4G32 rule along head_dim). Blocks
+ * are taken from the free list when a token index is a multiple of 16.
+ * Errors: INVALID_ARG, CONTEXT_FULL, KV_FULL (nothing is appended), CUDA. */
+mag_status mag_kv_append(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* k_dev, const void* v_dev);
+
+/* One decode step ([Magnitude] 4.4 infer, one token; [Core] 5.2 tight decode
+ * loop): for each of `batch` distinct sessions, take the fp16 hidden state
+ * hidden_in_dev[b][D] of its next token, run every layer (RMSNorm, W4 QKV,
+ * RoPE at the session's position, KV append, attention over the pool, W4 O +
+ * residual, RMSNorm, W4 gate-up + SwiGLU, W4 down + residual) and write
+ * out_dev[b][V] fp16 logits (or [b][D] fp16 hidden state when vocab == 0).
+ * The session's length grows by one. Replays a CUDA graph captured on the
+ * first step of each batch size. The residual stream is kept in fp32.
+ * Errors: INVALID_ARG, CONTEXT_FULL, KV_FULL, NOT_LOADED, CUDA. */
+mag_status mag_decode_step(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host, const void* hidden_in_dev,
+                           void* out_dev);
+
+/* The same step with HOST buffers: copies hidden_in_host to the device,
+ * runs the step, copies the output back into out_host and synchronises. */
+mag_status mag_decode_step_host(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host,
+                                const void* hidden_in_host, void* out_host);
+
+/* Chunked prefill: append n_tokens (<= max_chunk) of one session at its next
+ * positions with causal attention over the cache and the chunk, and write
+ * the fp16 output (logits, or hidden state when vocab == 0) of the last
+ * token to last_out_dev. hidden_in_dev is fp16 [n_tokens][D].
+ * Errors: INVALID_ARG, CONTEXT_FULL, KV_FULL, NOT_LOADED, UNSUPPORTED, CUDA. */
+mag_status mag_prefill_chunk(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
+                             void* last_out_dev);
+
+/* Wait for the context's stream and read the device error word
+ * (MAG_ERR_TIMEOUT if a bounded device wait gave up). */
+mag_status mag_sync(mag_ctx* ctx);
+
+typedef struct mag_memory_stats {
+  uint64_t weight_bytes;       /* packed W4 + scales + norm gains + LM head */
+  uint64_t kv_pool_bytes;      /* L * P * block bytes */
+  uint64_t kv_block_bytes;     /* bytes of one (layer, block) */
+  int32_t pool_blocks_total;
+  int32_t pool_blocks_free;
+  uint64_t arena_bytes;        /* planned activation arena */
+  uint64_t arena_unshared_bytes; /* sum of the arena tensors' sizes (no reuse) */
+  uint64_t other_device_bytes; /* block tables, RoPE table, counters, step arguments */
+  int32_t sessions_open;
+} mag_memory_stats;
+
+/* [Magnitude] 5.2 get_memory_stats: weights, pool, arena. */
+mag_status mag_get_memory_stats(mag_ctx* ctx, mag_memory_stats* out);
+
+/* Message of the last error on this context (never NULL; "" if none). */
+const char* mag_last_error(mag_ctx* ctx);
+
+/* [Core] 5.4 KV capacity planning: bytes one token adds to the pool over all
+ * layers, 2 * L * Hkv * d * bytes per value, plus this library's per-token
+ * scale metadata for INT8 (2 B per head) and INT4 (4 B per 32 values). */
+uint64_t mag_kv_bytes_per_token(const mag_config* cfg);
+
+/* Stateless quantiser ([Core] 5.1 W4A16 packing): fp32 [rows, cols] on the
+ * device -> codes u8 [rows][16G] and (scale, min) fp16 [rows][G][2], G =
+ * ceil(cols/32). Per group of 32 consecutive values: m = fp16(min), s =
+ * fp16((max - min)/15) (fp32 subtract, IEEE divide), code = clamp(rint((x -
+ * m)/s), 0, 15) in fp32 (0 when s == 0). Ordered on `cuda_stream`.
+ * Errors: INVALID_ARG, CUDA. */
+mag_status mag_quantize_w4g32(const void* src_dev, int64_t rows, int64_t cols, void* codes_dev, void* scale_min_dev,
+                              void* cuda_stream);
+
+/* ---- debug and test hooks ---- */
+
+/* Copy a loaded projection back in W4G32 bytes (codes then pairs) into dst_dev. */
+mag_status mag_debug_read_weights(mag_ctx* ctx, int32_t tensor, int32_t layer, void* dst_dev, size_t bytes);
+
+/* Byte offsets in the pool of token `token` of a session at `layer`, for KV
+ * head 0: out[0] K data, out[1] V data, out[2] K meta, out[3] V meta (meta =
+ * -1 for FP16); head h adds h * 16 * (bytes of one vector or its meta).
+ * out[4] is the physical block id. */
+mag_status mag_debug_kv_locate(mag_ctx* ctx, int32_t session, int32_t layer, int32_t token, int64_t out[5]);
+
+/* Device pointer and size of the KV pool, for reading stored bytes. */
+mag_status mag_debug_pool(mag_ctx* ctx, void** pool_dev, uint64_t* bytes);
+
+typedef struct mag_arena_tensor {
+  char name[24];
+  uint64_t size;   /* bytes */
+  int32_t first;   /* first op index (producer) */
+  int32_t last;    /* last op index (last consumer), closed interval */
+  uint64_t offset; /* planned offset, multiple of 64 */
+} mag_arena_tensor;
+
+/* The activation arena plan of phase 0 (decode step at max_batch) or 1
+ * (prefill chunk at max_chunk): up to `cap` tensors into out, their count into
+ * n_out and the arena size into arena_bytes. */
+mag_status mag_debug_arena_plan(mag_ctx* ctx, int32_t phase, mag_arena_tensor* out, int32_t cap, int32_t* n_out,
+                                uint64_t* arena_bytes);
+
+/* Kernel launches of the last decode step (0 if none ran yet). */
+int32_t mag_debug_last_step_launches(mag_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,239 @@
+"""Python binding of libmag (the GB300 decode-step library): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels; this module
+only converts Python/torch arguments into the C ABI of ``include/mag.h``. If
+the shared library is missing or cannot be loaded it raises -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmag.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_OOM, ERR_KV_FULL, ERR_CONTEXT_FULL, ERR_NOT_LOADED, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = \
+    range(9)
+STATUS_NAMES = ["OK", "INVALID_ARG", "OOM", "KV_FULL", "CONTEXT_FULL", "NOT_LOADED", "CUDA", "TIMEOUT", "UNSUPPORTED"]
+KV_FP16, KV_INT8, KV_INT4 = 0, 1, 2
+W_QKV, W_O, W_GATE_UP, W_DOWN, NORM_ATTN, NORM_FFN, NORM_FINAL, LM_HEAD = range(8)
+FMT_F32_DENSE, FMT_W4G32, FMT_F16 = 0, 1, 2
+FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL = 1, 2, 4
+
+EXPORTED = [
+    "mag_create", "mag_destroy", "mag_load_weights", "mag_session_open", "mag_session_close", "mag_session_length",
+    "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk", "mag_sync",
+    "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
+    "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
+    "mag_debug_last_step_launches",
+]
+
+
+class MagError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else status}: {msg}")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
+                ("kv_dtype", ctypes.c_int32), ("block_tokens", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
+                ("max_sessions", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("max_chunk", ctypes.c_int32),
+                ("max_context", ctypes.c_int32), ("pool_order_host", ctypes.POINTER(ctypes.c_int32)),
+                ("flags", ctypes.c_uint64)]
+
+
+class MemoryStats(ctypes.Structure):
+    _fields_ = [("weight_bytes", ctypes.c_uint64), ("kv_pool_bytes", ctypes.c_uint64),
+                ("kv_block_bytes", ctypes.c_uint64), ("pool_blocks_total", ctypes.c_int32),
+                ("pool_blocks_free", ctypes.c_int32), ("arena_bytes", ctypes.c_uint64),
+                ("arena_unshared_bytes", ctypes.c_uint64), ("other_device_bytes", ctypes.c_uint64),
+                ("sessions_open", ctypes.c_int32)]
+
+
+class ArenaTensor(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("size", ctypes.c_uint64), ("first", ctypes.c_int32),
+                ("last", ctypes.c_int32), ("offset", ctypes.c_uint64)]
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """Load libmag.so (raises if it is missing: build it with ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library must be built (quantized_decode_step_gb300."
+                                   "build()); there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+            P32 = ctypes.POINTER(ctypes.c_int32)
+            sig = {
+                "mag_create": ([ctypes.POINTER(Config), vp, ctypes.POINTER(vp)], i32),
+                "mag_destroy": ([vp], None),
+                "mag_load_weights": ([vp, i32, i32, vp, i32, sz], i32),
+                "mag_session_open": ([vp, P32], i32),
+                "mag_session_close": ([vp, i32], i32),
+                "mag_session_length": ([vp, i32, P32], i32),
+                "mag_kv_append": ([vp, i32, i32, vp, vp], i32),
+                "mag_decode_step": ([vp, i32, P32, vp, vp], i32),
+                "mag_decode_step_host": ([vp, i32, P32, vp, vp], i32),
+                "mag_prefill_chunk": ([vp, i32, i32, vp, vp], i32),
+                "mag_sync": ([vp], i32),
+                "mag_get_memory_stats": ([vp, ctypes.POINTER(MemoryStats)], i32),
+                "mag_last_error": ([vp], ctypes.c_char_p),
+                "mag_kv_bytes_per_token": ([ctypes.POINTER(Config)], u64),
+                "mag_quantize_w4g32": ([vp, i64, i64, vp, vp, vp], i32),
+                "mag_debug_read_weights": ([vp, i32, i32, vp, sz], i32),
+                "mag_debug_kv_locate": ([vp, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)], i32),
+                "mag_debug_pool": ([vp, ctypes.POINTER(vp), ctypes.POINTER(u64)], i32),
+                "mag_debug_arena_plan": ([vp, i32, ctypes.POINTER(ArenaTensor), i32, P32, ctypes.POINTER(u64)], i32),
+                "mag_debug_last_step_launches": ([vp], i32),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def _ptr(t) -> int:
+    """Device or host address of a torch tensor / numpy array / int."""
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data
+
+
+def make_config(shape, kv_dtype=KV_FP16, pool_blocks=64, max_sessions=4, max_batch=1, max_chunk=0, max_context=2048,
+                flags=0, pool_order=None) -> Config:
+    """A Config from any object with the shape fields (n_layers, hidden, ..., rms_eps, rope_base)."""
+    c = Config(shape.n_layers, shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn, shape.vocab,
+               shape.rms_eps, shape.rope_base, kv_dtype, 16, pool_blocks, max_sessions, max_batch, max_chunk,
+               max_context, None, flags)
+    if pool_order is not None:
+        import numpy as np
+        arr = np.ascontiguousarray(pool_order, dtype=np.int32)
+        c._order = arr  # keep alive
+        c.pool_order_host = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    return c
+
+
+def kv_bytes_per_token(cfg: Config) -> int:
+    return int(lib().mag_kv_bytes_per_token(ctypes.byref(cfg)))
+
+
+def quantize_w4g32(src, rows, cols, codes, scale_min, stream=0):
+    st = lib().mag_quantize_w4g32(_ptr(src), rows, cols, _ptr(codes), _ptr(scale_min), stream)
+    if st != OK:
+        raise MagError(st, "mag_quantize_w4g32")
+
+
+class Context:
+    """One mag_ctx. Methods mirror the C entry points of the same names."""
+
+    def __init__(self, cfg: Config, stream: int = 0):
+        self.cfg = cfg
+        h = ctypes.c_void_p()
+        st = lib().mag_create(ctypes.byref(cfg), stream, ctypes.byref(h))
+        if st != OK:
+            raise MagError(st, "mag_create failed (details on stderr)")
+        self.h = h
+
+    def _check(self, st, what):
+        if st != OK:
+            raise MagError(st, f"{what}: {lib().mag_last_error(self.h).decode()}")
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().mag_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def last_error(self) -> str:
+        return lib().mag_last_error(self.h).decode()
+
+    def load_weights(self, tensor, layer, src, fmt, nbytes):
+        self._check(lib().mag_load_weights(self.h, tensor, layer, _ptr(src), fmt, nbytes), "mag_load_weights")
+
+    def session_open(self) -> int:
+        sid = ctypes.c_int32()
+        self._check(lib().mag_session_open(self.h, ctypes.byref(sid)), "mag_session_open")
+        return sid.value
+
+    def session_close(self, sid):
+        self._check(lib().mag_session_close(self.h, sid), "mag_session_close")
+
+    def session_length(self, sid) -> int:
+        n = ctypes.c_int32()
+        self._check(lib().mag_session_length(self.h, sid, ctypes.byref(n)), "mag_session_length")
+        return n.value
+
+    def kv_append(self, sid, n_tokens, k, v):
+        self._check(lib().mag_kv_append(self.h, sid, n_tokens, _ptr(k), _ptr(v)), "mag_kv_append")
+
+    def decode_step(self, sessions, hidden_in, out):
+        ids = (ctypes.c_int32 * len(sessions))(*sessions)
+        self._check(lib().mag_decode_step(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out)), "mag_decode_step")
+
+    def decode_step_host(self, sessions, hidden_in_host, out_host):
+        ids = (ctypes.c_int32 * len(sessions))(*sessions)
+        self._check(lib().mag_decode_step_host(self.h, len(sessions), ids, _ptr(hidden_in_host), _ptr(out_host)),
+                    "mag_decode_step_host")
+
+    def prefill_chunk(self, sid, n_tokens, hidden_in, last_out):
+        self._check(lib().mag_prefill_chunk(self.h, sid, n_tokens, _ptr(hidden_in), _ptr(last_out)),
+                    "mag_prefill_chunk")
+
+    def sync(self):
+        self._check(lib().mag_sync(self.h), "mag_sync")
+
+    def memory_stats(self) -> dict:
+        s = MemoryStats()
+        self._check(lib().mag_get_memory_stats(self.h, ctypes.byref(s)), "mag_get_memory_stats")
+        return {n: getattr(s, n) for n, _ in MemoryStats._fields_}
+
+    def debug_read_weights(self, tensor, layer, dst, nbytes):
+        self._check(lib().mag_debug_read_weights(self.h, tensor, layer, _ptr(dst), nbytes), "mag_debug_read_weights")
+
+    def debug_kv_locate(self, sid, layer, token):
+        out = (ctypes.c_int64 * 5)()
+        self._check(lib().mag_debug_kv_locate(self.h, sid, layer, token, out), "mag_debug_kv_locate")
+        return list(out)
+
+    def debug_pool(self):
+        p, n = ctypes.c_void_p(), ctypes.c_uint64()
+        self._check(lib().mag_debug_pool(self.h, ctypes.byref(p), ctypes.byref(n)), "mag_debug_pool")
+        return p.value, n.value
+
+    def debug_arena_plan(self, phase=0):
+        n, total = ctypes.c_int32(), ctypes.c_uint64()
+        self._check(lib().mag_debug_arena_plan(self.h, phase, None, 0, ctypes.byref(n), ctypes.byref(total)),
+                    "mag_debug_arena_plan")
+        arr = (ArenaTensor * max(n.value, 1))()
+        self._check(lib().mag_debug_arena_plan(self.h, phase, arr, n.value, ctypes.byref(n), ctypes.byref(total)),
+                    "mag_debug_arena_plan")
+        return [dict(name=a.name.decode(), size=a.size, first=a.first, last=a.last, offset=a.offset)
+                for a in arr[:n.value]], total.value
+
+    def last_step_launches(self) -> int:
+        return int(lib().mag_debug_last_step_launches(self.h))

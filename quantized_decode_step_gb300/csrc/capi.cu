@@ -1,0 +1,905 @@
+// C ABI of the decode-step library: context, weights, KV block pool, arena
+// plan, CUDA-graph step and the debug hooks. See include/mag.h for the
+// contract of each call.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <string>
+#include <vector>
+
+#include "arena.h"
+#include "kernels.h"
+#include "mag.h"
+
+using namespace mag;
+
+namespace {
+
+constexpr int kRing = 8;
+
+struct Proj {
+  uint8_t* codes = nullptr;  // [N][16G] followed by (scale, min) [N][G]
+  __half2* sm = nullptr;
+  int N = 0, K = 0, G = 0;
+  size_t bytes = 0;
+};
+
+struct Session {
+  bool open = false;
+  int len = 0;
+  std::vector<int32_t> table;
+};
+
+struct GemvPlan {
+  int mpc, wk, ks, cpc;
+};
+
+}  // namespace
+
+struct mag_ctx {
+  mag_config cfg{};
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  int device = 0, n_sm = 0;
+  std::string err;
+  int L = 0, D = 0, Hq = 0, Hkv = 0, d = 0, F = 0, V = 0, R = 0, G = 0, B_max = 0;
+  int table_stride = 0;
+
+  // weights
+  uint8_t* wbase = nullptr;
+  size_t wbytes = 0;
+  std::vector<Proj> proj;  // [L][4]
+  std::vector<__half*> gamma1, gamma2;
+  __half* gamma_f = nullptr;
+  __half* lm_head = nullptr;
+  std::vector<uint8_t> loaded;  // [L][6] + final norm + lm head
+
+  // KV pool
+  uint8_t* pool = nullptr;
+  size_t pool_bytes = 0;
+  int64_t block_bytes = 0;
+  int data_bytes = 0, meta_bytes = 0;
+  std::deque<int32_t> free_list;
+  int32_t* d_tables = nullptr;
+  std::vector<Session> sessions;
+
+  // RoPE table
+  float* d_cos = nullptr;
+  float* d_sin = nullptr;
+
+  // activation arena (decode phase)
+  uint8_t* arena = nullptr;
+  uint64_t arena_bytes = 0, arena_unshared = 0;
+  std::vector<ArenaTensor> plan;
+  float* r = nullptr;
+  __half* qkv = nullptr;
+  __half* qrot = nullptr;
+  float* part_ml = nullptr;
+  float* part_o = nullptr;
+  __half* o = nullptr;
+  __half* act = nullptr;
+  float* gemv_part = nullptr;
+  int attn_split_max = 0;
+
+  // counters (zero between launches) and step arguments
+  uint32_t* d_counters = nullptr;
+  size_t n_counters = 0;
+  uint32_t* d_attn_counters = nullptr;
+  StepArgs* d_args = nullptr;
+  StepArgs* h_ring = nullptr;
+  cudaEvent_t ring_ev[kRing] = {};
+  int ring_pos = 0;
+
+  // staging for the host-buffer step
+  void* d_in_stage = nullptr;
+  void* d_out_stage = nullptr;
+
+  cudaGraphExec_t graphs[MAG_MAX_BATCH + 1] = {};
+  int graph_launches[MAG_MAX_BATCH + 1] = {};
+  int last_launches = 0;
+  uint64_t other_bytes = 0;
+};
+
+namespace {
+
+mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf;
+  return s;
+}
+
+#define CUDA_TRY(ctx, call)                                                                         \
+  do {                                                                                              \
+    cudaError_t e_ = (call);                                                                        \
+    if (e_ != cudaSuccess) return fail(ctx, MAG_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+int proj_index(int tensor) { return tensor; }  // QKV=0, O=1, GU=2, DOWN=3
+
+GemvPlan plan_gemv(int n_mtiles, int K, int B, bool f16w) {
+  GemvPlan p;
+  const int n_chunks = (K + 63) / 64;
+  if (B <= 8) {
+    if (f16w) {
+      p.mpc = 4;
+      p.wk = 2;
+    } else if (n_mtiles >= 1024) {
+      p.mpc = 2;
+      p.wk = 4;
+    } else {
+      p.mpc = 1;
+      p.wk = 8;
+    }
+  } else {
+    p.mpc = 8;
+    p.wk = 1;
+  }
+  const int max_cpc = std::max(1, (64 * 1024) / (B * 128) - 1);
+  p.ks = (n_chunks + max_cpc - 1) / max_cpc;
+  p.cpc = (n_chunks + p.ks - 1) / p.ks;
+  return p;
+}
+
+int attn_splits(const mag_ctx* c, int B) {
+  int s = (2 * c->n_sm + B * c->Hkv - 1) / (B * c->Hkv);
+  return std::max(1, std::min(s, 64));
+}
+
+int64_t kv_data_bytes(int d, int dt) { return dt == 0 ? 2 * d : (dt == 1 ? d : d / 2); }
+int64_t kv_meta_bytes(int d, int dt) { return dt == 0 ? 0 : (dt == 1 ? 2 : (d / 32) * 4); }
+
+PoolGeom pool_geom(const mag_ctx* c) {
+  PoolGeom g;
+  g.base = c->pool;
+  g.block_bytes = c->block_bytes;
+  g.pool_blocks = c->cfg.pool_blocks;
+  g.data_bytes = c->data_bytes;
+  g.meta_bytes = c->meta_bytes;
+  g.n_kv_heads = c->Hkv;
+  g.head_dim = c->d;
+  g.kv_dtype = c->cfg.kv_dtype;
+  g.tables = c->d_tables;
+  g.table_stride = c->table_stride;
+  return g;
+}
+
+bool all_loaded(const mag_ctx* c) {
+  for (int l = 0; l < c->L; ++l)
+    for (int i = 0; i < 6; ++i)
+      if (!c->loaded[l * 6 + i]) return false;
+  if (!c->loaded[c->L * 6]) return false;
+  if (c->V && !c->loaded[c->L * 6 + 1]) return false;
+  return true;
+}
+
+// Sizes of the decode-phase gemv partial buffer for batch B.
+size_t gemv_partial_floats(const mag_ctx* c, int B) {
+  size_t mx = 0;
+  const int nt = B > 8 ? 2 : 1;
+  auto one = [&](int n_mtiles, int K, bool f16) {
+    GemvPlan p = plan_gemv(n_mtiles, K, B, f16);
+    if (p.ks > 1) mx = std::max(mx, (size_t)p.ks * n_mtiles * 32 * 4 * nt);
+  };
+  one(c->R / 16, c->D, false);
+  one(c->D / 16, c->Hq * c->d, false);
+  one(c->F / 8, c->D, false);
+  one(c->D / 16, c->F, false);
+  if (c->V) one(c->V / 16, c->D, true);
+  return mx;
+}
+
+size_t gemv_grid_x(const mag_ctx* c, int B) {
+  size_t mx = 0;
+  auto one = [&](int n_mtiles, int K, bool f16) {
+    GemvPlan p = plan_gemv(n_mtiles, K, B, f16);
+    mx = std::max(mx, (size_t)((n_mtiles + p.mpc - 1) / p.mpc));
+  };
+  one(c->R / 16, c->D, false);
+  one(c->D / 16, c->Hq * c->d, false);
+  one(c->F / 8, c->D, false);
+  one(c->D / 16, c->F, false);
+  if (c->V) one(c->V / 16, c->D, true);
+  return mx;
+}
+
+// Decode-phase activation tensors at max_batch with their op lifetimes:
+// op 0 step begin, then per layer 1 QKV, 2 RoPE+append, 3 attention, 4 O,
+// 5 gate-up, 6 down (the one per-layer plan is reused by every layer), 7 output.
+void build_decode_plan(mag_ctx* c) {
+  const int B = c->B_max;
+  int S = 0;
+  for (int b = 1; b <= B; ++b) S = std::max(S, attn_splits(c, b) * b);
+  c->attn_split_max = S;  // splits x batch rows, the partial buffers' capacity
+  size_t part = 0;
+  for (int b = 1; b <= B; ++b) part = std::max(part, gemv_partial_floats(c, b));
+  auto T = [](const char* n, uint64_t sz, int f, int l) { return ArenaTensor{n, sz, f, l, 0}; };
+  c->plan.clear();
+  c->plan.push_back(T("residual", (uint64_t)B * c->D * 4, 0, 7));
+  c->plan.push_back(T("qkv", (uint64_t)B * c->R * 2, 1, 2));
+  c->plan.push_back(T("q_rot", (uint64_t)B * c->Hq * c->d * 2, 2, 3));
+  c->plan.push_back(T("attn_part_ml", (uint64_t)S * c->Hkv * c->G * 2 * 4, 3, 3));
+  c->plan.push_back(T("attn_part_o", (uint64_t)S * c->Hkv * c->G * c->d * 4, 3, 3));
+  c->plan.push_back(T("attn_out", (uint64_t)B * c->Hq * c->d * 2, 3, 4));
+  c->plan.push_back(T("ffn_act", (uint64_t)B * c->F * 2, 5, 6));
+  if (part) c->plan.push_back(T("gemv_partial", part * 4, 1, 7));
+  c->arena_unshared = 0;
+  for (auto& t : c->plan) c->arena_unshared += t.size;
+  c->arena_bytes = plan_arena(c->plan, 64, (c->cfg.flags & MAG_FLAG_ARENA_NO_REUSE) != 0);
+}
+
+void* arena_ptr(mag_ctx* c, const char* name) {
+  for (auto& t : c->plan)
+    if (t.name == name) return c->arena + t.offset;
+  return nullptr;
+}
+
+GemvArgs gemv_args(const mag_ctx* c, const Proj& p, int B, int n_mtiles, bool f16w) {
+  GemvArgs a = {};
+  GemvPlan pl = plan_gemv(n_mtiles, p.K, B, f16w);
+  a.w = p.codes;
+  a.sm = p.sm;
+  a.w_row_bytes = f16w ? (int64_t)p.K * 2 : (int64_t)p.G * 16;
+  a.sm_row = p.G;
+  a.n_mtiles = n_mtiles;
+  a.K = p.K;
+  a.n_chunks = (p.K + 63) / 64;
+  a.chunks_per_cta = pl.cpc;
+  a.ks = pl.ks;
+  a.mpc = pl.mpc;
+  a.wk = pl.wk;
+  a.batch = B;
+  a.eps = c->cfg.rms_eps;
+  a.partial = c->gemv_part;
+  a.counters = c->d_counters;
+  a.step = c->d_args;
+  return a;
+}
+
+// Enqueue the whole decode step for batch B (captured into a graph or run eagerly).
+cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
+  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL);
+  Launch L0{c->stream, false, n_launch};
+  Launch L{c->stream, pdl, n_launch};
+  cudaError_t e;
+  if ((e = launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B)) != cudaSuccess) return e;
+  const PoolGeom pg = pool_geom(c);
+  const int S = attn_splits(c, B);
+  for (int l = 0; l < c->L; ++l) {
+    const Proj* P = &c->proj[(size_t)l * 4];
+    {  // RMSNorm + QKV
+      GemvArgs a = gemv_args(c, P[0], B, c->R / 16, false);
+      a.r = c->r;
+      a.ldr = c->D;
+      a.gamma = c->gamma1[l];
+      a.out_h = c->qkv;
+      a.ldo = c->R;
+      if ((e = launch_gemv(L, a, W_W4, X_NORM, EPI_STORE)) != cudaSuccess) return e;
+    }
+    {  // RoPE + KV append
+      RopeAppendArgs a = {};
+      a.qkv = c->qkv;
+      a.q_out = c->qrot;
+      a.rope_cos = c->d_cos;
+      a.rope_sin = c->d_sin;
+      a.n_heads = c->Hq;
+      a.n_kv_heads = c->Hkv;
+      a.head_dim = c->d;
+      a.layer = l;
+      a.pool = pg;
+      a.step = c->d_args;
+      if ((e = launch_rope_append(L, a, B)) != cudaSuccess) return e;
+    }
+    {  // attention
+      AttnArgs a = {};
+      a.q = c->qrot;
+      a.o = c->o;
+      a.n_heads = c->Hq;
+      a.n_kv_heads = c->Hkv;
+      a.head_dim = c->d;
+      a.layer = l;
+      a.n_split = S;
+      a.part_ml = c->part_ml;
+      a.part_o = c->part_o;
+      a.counters = c->d_attn_counters;
+      a.pool = pg;
+      a.step = c->d_args;
+      if ((e = launch_attention(L, a, B)) != cudaSuccess) return e;
+    }
+    {  // O projection + residual
+      GemvArgs a = gemv_args(c, P[1], B, c->D / 16, false);
+      a.x = c->o;
+      a.ldx = c->Hq * c->d;
+      a.out_r = c->r;
+      a.ldo = c->D;
+      if ((e = launch_gemv(L, a, W_W4, X_F16, EPI_RESID)) != cudaSuccess) return e;
+    }
+    {  // RMSNorm + gate-up + SwiGLU
+      GemvArgs a = gemv_args(c, P[2], B, c->F / 8, false);
+      a.swiglu_f = c->F;
+      a.r = c->r;
+      a.ldr = c->D;
+      a.gamma = c->gamma2[l];
+      a.out_h = c->act;
+      a.ldo = c->F;
+      if ((e = launch_gemv(L, a, W_W4, X_NORM, EPI_SWIGLU)) != cudaSuccess) return e;
+    }
+    {  // down projection + residual
+      GemvArgs a = gemv_args(c, P[3], B, c->D / 16, false);
+      a.x = c->act;
+      a.ldx = c->F;
+      a.out_r = c->r;
+      a.ldo = c->D;
+      if ((e = launch_gemv(L, a, W_W4, X_F16, EPI_RESID)) != cudaSuccess) return e;
+    }
+  }
+  if (c->V) {
+    Proj lm;
+    lm.codes = reinterpret_cast<uint8_t*>(c->lm_head);
+    lm.N = c->V;
+    lm.K = c->D;
+    GemvArgs a = gemv_args(c, lm, B, c->V / 16, true);
+    a.r = c->r;
+    a.ldr = c->D;
+    a.gamma = c->gamma_f;
+    a.ldo = c->V;
+    if ((e = launch_gemv(L, a, W_F16, X_NORM, EPI_STORE_OUT)) != cudaSuccess) return e;
+  } else {
+    if ((e = launch_final_hidden(L, c->d_args, c->r, c->D, B)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+void free_ctx(mag_ctx* c) {
+  if (!c) return;
+  if (c->stream) cudaStreamSynchronize(c->stream);
+  for (auto& g : c->graphs)
+    if (g) cudaGraphExecDestroy(g);
+  for (auto& e : c->ring_ev)
+    if (e) cudaEventDestroy(e);
+  cudaFree(c->wbase);
+  cudaFree(c->pool);
+  cudaFree(c->d_tables);
+  cudaFree(c->d_cos);
+  cudaFree(c->d_sin);
+  cudaFree(c->arena);
+  cudaFree(c->d_counters);
+  cudaFree(c->d_attn_counters);
+  cudaFree(c->d_args);
+  cudaFree(c->d_in_stage);
+  cudaFree(c->d_out_stage);
+  if (c->h_ring) cudaFreeHost(c->h_ring);
+  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+  delete c;
+}
+
+mag_status check_cfg(const mag_config* g, std::string& why) {
+  char b[256];
+  auto bad = [&](const char* m) {
+    why = m;
+    return MAG_ERR_INVALID_ARG;
+  };
+  if (g->n_layers < 1 || g->hidden < 16 || g->n_heads < 1 || g->n_kv_heads < 1 || g->ffn < 8 || g->vocab < 0)
+    return bad("shape fields must be positive (vocab >= 0)");
+  if (g->n_heads % g->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+  if (g->n_heads / g->n_kv_heads > 8) return bad("more than 8 query heads per KV head");
+  if (g->head_dim != 64 && g->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (g->hidden % 16 || g->ffn % 8 || (g->n_heads * g->head_dim) % 16) return bad("hidden % 16, ffn % 8 required");
+  if (g->vocab % 16) return bad("vocab must be a multiple of 16");
+  if (g->block_tokens != 16) return bad("block_tokens must be 16");
+  if (g->kv_dtype < 0 || g->kv_dtype > 2) return bad("kv_dtype must be 0 (FP16), 1 (INT8) or 2 (INT4)");
+  if (g->pool_blocks < 1 || g->max_sessions < 1 || g->max_context < 1) return bad("pool, sessions, context > 0");
+  if (g->max_batch < 1 || g->max_batch > MAG_MAX_BATCH) return bad("max_batch must be 1..16");
+  if (g->max_chunk < 0) return bad("max_chunk must be >= 0");
+  if (!(g->rms_eps > 0) || !(g->rope_base > 0)) return bad("rms_eps and rope_base must be positive");
+  snprintf(b, sizeof b, "ok");
+  return MAG_OK;
+}
+
+}  // namespace
+
+// ============================================================================ API
+
+extern "C" {
+
+mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
+  if (!out) return MAG_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return MAG_ERR_INVALID_ARG;
+  std::string why;
+  if (check_cfg(cfg, why) != MAG_OK) {
+    fprintf(stderr, "mag_create: %s\n", why.c_str());
+    return MAG_ERR_INVALID_ARG;
+  }
+  mag_ctx* c = new mag_ctx();
+  c->cfg = *cfg;
+  c->cfg.pool_order_host = nullptr;
+  c->L = cfg->n_layers;
+  c->D = cfg->hidden;
+  c->Hq = cfg->n_heads;
+  c->Hkv = cfg->n_kv_heads;
+  c->d = cfg->head_dim;
+  c->F = cfg->ffn;
+  c->V = cfg->vocab;
+  c->G = c->Hq / c->Hkv;
+  c->R = (c->Hq + 2 * c->Hkv) * c->d;
+  c->B_max = cfg->max_batch;
+  c->table_stride = (cfg->max_context + 15) / 16;
+  auto bail = [&](mag_status s) {
+    fprintf(stderr, "mag_create: %s\n", c->err.c_str());
+    free_ctx(c);
+    return s;
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&c->device)) != cudaSuccess) {
+    fail(c, MAG_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    return bail(MAG_ERR_CUDA);
+  }
+  cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, c->device);
+  if (cuda_stream) {
+    c->stream = (cudaStream_t)cuda_stream;
+  } else {
+    if ((e = cudaStreamCreate(&c->stream)) != cudaSuccess) {
+      fail(c, MAG_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
+      return bail(MAG_ERR_CUDA);
+    }
+    c->own_stream = true;
+  }
+  // pool order
+  const int P = cfg->pool_blocks;
+  if (cfg->pool_order_host) {
+    std::vector<char> seen(P, 0);
+    for (int i = 0; i < P; ++i) {
+      int b = cfg->pool_order_host[i];
+      if (b < 0 || b >= P || seen[b]) {
+        fail(c, MAG_ERR_INVALID_ARG, "pool_order_host is not a permutation of 0..%d", P - 1);
+        return bail(MAG_ERR_INVALID_ARG);
+      }
+      seen[b] = 1;
+      c->free_list.push_back(b);
+    }
+  } else {
+    for (int i = 0; i < P; ++i) c->free_list.push_back(i);
+  }
+  c->sessions.resize(cfg->max_sessions);
+  c->loaded.assign((size_t)c->L * 6 + 2, 0);
+
+  // ---- weights region
+  size_t off = 0;
+  c->proj.resize((size_t)c->L * 4);
+  std::vector<size_t> offs;
+  const int shapes[4][2] = {{c->R, c->D}, {c->D, c->Hq * c->d}, {2 * c->F, c->D}, {c->D, c->F}};
+  for (int l = 0; l < c->L; ++l)
+    for (int i = 0; i < 4; ++i) {
+      Proj& p = c->proj[(size_t)l * 4 + i];
+      p.N = shapes[i][0];
+      p.K = shapes[i][1];
+      p.G = (p.K + 31) / 32;
+      p.bytes = (size_t)p.N * p.G * 16 + (size_t)p.N * p.G * 4;
+      offs.push_back(off);
+      off = align256(off + p.bytes);
+    }
+  std::vector<size_t> goffs;
+  for (int l = 0; l < c->L; ++l)
+    for (int i = 0; i < 2; ++i) {
+      goffs.push_back(off);
+      off = align256(off + (size_t)c->D * 2);
+    }
+  size_t gf_off = off;
+  off = align256(off + (size_t)c->D * 2);
+  size_t lm_off = off;
+  if (c->V) off = align256(off + (size_t)c->V * c->D * 2);
+  c->wbytes = off;
+  if ((e = cudaMalloc(&c->wbase, c->wbytes)) != cudaSuccess) {
+    fail(c, MAG_ERR_OOM, "weights: cudaMalloc(%zu): %s", c->wbytes, cudaGetErrorString(e));
+    return bail(MAG_ERR_OOM);
+  }
+  for (size_t i = 0; i < c->proj.size(); ++i) {
+    Proj& p = c->proj[i];
+    p.codes = c->wbase + offs[i];
+    p.sm = reinterpret_cast<__half2*>(p.codes + (size_t)p.N * p.G * 16);
+  }
+  for (int l = 0; l < c->L; ++l) {
+    c->gamma1.push_back(reinterpret_cast<__half*>(c->wbase + goffs[2 * l]));
+    c->gamma2.push_back(reinterpret_cast<__half*>(c->wbase + goffs[2 * l + 1]));
+  }
+  c->gamma_f = reinterpret_cast<__half*>(c->wbase + gf_off);
+  c->lm_head = c->V ? reinterpret_cast<__half*>(c->wbase + lm_off) : nullptr;
+
+  // ---- KV pool (zeroed: slots past a session's length read as finite zeros)
+  c->data_bytes = (int)kv_data_bytes(c->d, cfg->kv_dtype);
+  c->meta_bytes = (int)kv_meta_bytes(c->d, cfg->kv_dtype);
+  c->block_bytes = 2 * (int64_t)c->Hkv * 16 * (c->data_bytes + c->meta_bytes);
+  c->pool_bytes = (size_t)c->L * P * c->block_bytes;
+  if ((e = cudaMalloc(&c->pool, c->pool_bytes)) != cudaSuccess) {
+    fail(c, MAG_ERR_OOM, "KV pool: cudaMalloc(%zu): %s", c->pool_bytes, cudaGetErrorString(e));
+    return bail(MAG_ERR_OOM);
+  }
+  cudaMemsetAsync(c->pool, 0, c->pool_bytes, c->stream);
+  size_t tb = (size_t)cfg->max_sessions * c->table_stride * 4;
+  if ((e = cudaMalloc(&c->d_tables, tb)) != cudaSuccess) {
+    fail(c, MAG_ERR_OOM, "block tables: %s", cudaGetErrorString(e));
+    return bail(MAG_ERR_OOM);
+  }
+  cudaMemsetAsync(c->d_tables, 0, tb, c->stream);
+
+  // ---- RoPE table, built on the host in double, stored as fp32
+  {
+    const int half = c->d / 2;
+    const size_t rows = (size_t)cfg->max_context;
+    std::vector<float> cs(rows * half), sn(rows * half);
+    for (size_t p = 0; p < rows; ++p)
+      for (int i = 0; i < half; ++i) {
+        double theta = (double)p * std::pow((double)cfg->rope_base, -2.0 * i / c->d);
+        cs[p * half + i] = (float)std::cos(theta);
+        sn[p * half + i] = (float)std::sin(theta);
+      }
+    size_t bytes = rows * half * 4;
+    if (cudaMalloc(&c->d_cos, bytes) != cudaSuccess || cudaMalloc(&c->d_sin, bytes) != cudaSuccess) {
+      fail(c, MAG_ERR_OOM, "RoPE table");
+      return bail(MAG_ERR_OOM);
+    }
+    cudaMemcpy(c->d_cos, cs.data(), bytes, cudaMemcpyHostToDevice);
+    cudaMemcpy(c->d_sin, sn.data(), bytes, cudaMemcpyHostToDevice);
+    c->other_bytes += 2 * bytes + tb;
+  }
+
+  // ---- arena
+  build_decode_plan(c);
+  if ((e = cudaMalloc(&c->arena, std::max<uint64_t>(c->arena_bytes, 256))) != cudaSuccess) {
+    fail(c, MAG_ERR_OOM, "arena: %s", cudaGetErrorString(e));
+    return bail(MAG_ERR_OOM);
+  }
+  c->r = (float*)arena_ptr(c, "residual");
+  c->qkv = (__half*)arena_ptr(c, "qkv");
+  c->qrot = (__half*)arena_ptr(c, "q_rot");
+  c->part_ml = (float*)arena_ptr(c, "attn_part_ml");
+  c->part_o = (float*)arena_ptr(c, "attn_part_o");
+  c->o = (__half*)arena_ptr(c, "attn_out");
+  c->act = (__half*)arena_ptr(c, "ffn_act");
+  c->gemv_part = (float*)arena_ptr(c, "gemv_partial");
+
+  // ---- counters, step arguments, staging
+  size_t nc = 0;
+  for (int b = 1; b <= c->B_max; ++b) nc = std::max(nc, gemv_grid_x(c, b));
+  c->n_counters = nc;
+  size_t ac = (size_t)c->B_max * c->Hkv;
+  size_t stage_out = (size_t)c->B_max * (c->V ? c->V : c->D) * 2;
+  if (cudaMalloc(&c->d_counters, nc * 4) != cudaSuccess || cudaMalloc(&c->d_attn_counters, ac * 4) != cudaSuccess ||
+      cudaMalloc(&c->d_args, sizeof(StepArgs)) != cudaSuccess ||
+      cudaMalloc(&c->d_in_stage, (size_t)c->B_max * c->D * 2) != cudaSuccess ||
+      cudaMalloc(&c->d_out_stage, stage_out) != cudaSuccess ||
+      cudaMallocHost(&c->h_ring, sizeof(StepArgs) * kRing) != cudaSuccess) {
+    fail(c, MAG_ERR_OOM, "counters / step arguments");
+    return bail(MAG_ERR_OOM);
+  }
+  cudaMemsetAsync(c->d_counters, 0, nc * 4, c->stream);
+  cudaMemsetAsync(c->d_attn_counters, 0, ac * 4, c->stream);
+  for (auto& ev : c->ring_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  c->other_bytes += nc * 4 + ac * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
+  if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
+    fail(c, MAG_ERR_CUDA, "create: %s", cudaGetErrorString(e));
+    return bail(MAG_ERR_CUDA);
+  }
+  *out = c;
+  return MAG_OK;
+}
+
+void mag_destroy(mag_ctx* c) { free_ctx(c); }
+
+const char* mag_last_error(mag_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+uint64_t mag_kv_bytes_per_token(const mag_config* g) {
+  if (!g || g->head_dim <= 0) return 0;
+  return 2ull * g->n_layers * g->n_kv_heads *
+         (uint64_t)(kv_data_bytes(g->head_dim, g->kv_dtype) + kv_meta_bytes(g->head_dim, g->kv_dtype));
+}
+
+mag_status mag_quantize_w4g32(const void* src, int64_t rows, int64_t cols, void* codes, void* sm, void* stream) {
+  if (rows < 0 || cols <= 0 || (rows && (!src || !codes || !sm))) return MAG_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_w4g32((cudaStream_t)stream, (const float*)src, rows, cols, (uint8_t*)codes,
+                                        (__half2*)sm);
+  return e == cudaSuccess ? MAG_OK : MAG_ERR_CUDA;
+}
+
+mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const void* src, int32_t fmt, size_t bytes) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!src) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: null source");
+  const bool per_layer = tensor >= MAG_W_QKV && tensor <= MAG_NORM_FFN;
+  if (tensor < 0 || tensor > MAG_LM_HEAD) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: bad tensor %d", tensor);
+  if (per_layer && (layer < 0 || layer >= c->L))
+    return fail(c, MAG_ERR_INVALID_ARG, "load_weights: bad layer %d", layer);
+  if (tensor <= MAG_W_DOWN) {
+    Proj& p = c->proj[(size_t)layer * 4 + proj_index(tensor)];
+    if (fmt == MAG_FMT_F32_DENSE) {
+      if (bytes != (size_t)p.N * p.K * 4)
+        return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected fp32 [%d, %d]", bytes, p.N, p.K);
+      CUDA_TRY(c, launch_quantize_w4g32(c->stream, (const float*)src, p.N, p.K, p.codes, p.sm));
+    } else if (fmt == MAG_FMT_W4G32) {
+      if (bytes != p.bytes)
+        return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected W4G32 %zu", bytes, p.bytes);
+      CUDA_TRY(c, cudaMemcpyAsync(p.codes, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+    } else {
+      return fail(c, MAG_ERR_INVALID_ARG, "load_weights: projections take FP32_DENSE or W4G32");
+    }
+    c->loaded[(size_t)layer * 6 + tensor] = 1;
+    return MAG_OK;
+  }
+  if (fmt != MAG_FMT_F16) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: norms and LM head take F16");
+  if (tensor == MAG_LM_HEAD) {
+    if (!c->V) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: this model has no LM head");
+    if (bytes != (size_t)c->V * c->D * 2) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: LM head size");
+    CUDA_TRY(c, cudaMemcpyAsync(c->lm_head, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+    c->loaded[(size_t)c->L * 6 + 1] = 1;
+    return MAG_OK;
+  }
+  if (bytes != (size_t)c->D * 2) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: norm gain size");
+  __half* dst = tensor == MAG_NORM_ATTN ? c->gamma1[layer] : (tensor == MAG_NORM_FFN ? c->gamma2[layer] : c->gamma_f);
+  CUDA_TRY(c, cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  if (tensor == MAG_NORM_FINAL) c->loaded[(size_t)c->L * 6] = 1;
+  else c->loaded[(size_t)layer * 6 + tensor] = 1;
+  return MAG_OK;
+}
+
+mag_status mag_session_open(mag_ctx* c, int32_t* sid) {
+  if (!c || !sid) return MAG_ERR_INVALID_ARG;
+  for (size_t i = 0; i < c->sessions.size(); ++i)
+    if (!c->sessions[i].open) {
+      c->sessions[i].open = true;
+      c->sessions[i].len = 0;
+      c->sessions[i].table.clear();
+      *sid = (int32_t)i;
+      return MAG_OK;
+    }
+  return fail(c, MAG_ERR_INVALID_ARG, "session_open: all %d sessions are open", (int)c->sessions.size());
+}
+
+mag_status mag_session_close(mag_ctx* c, int32_t sid) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "session_close: session %d is not open", sid);
+  for (int32_t b : c->sessions[sid].table) c->free_list.push_back(b);
+  c->sessions[sid] = Session();
+  return MAG_OK;
+}
+
+mag_status mag_session_length(mag_ctx* c, int32_t sid, int32_t* len) {
+  if (!c || !len) return MAG_ERR_INVALID_ARG;
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "session %d is not open", sid);
+  *len = c->sessions[sid].len;
+  return MAG_OK;
+}
+
+mag_status mag_kv_append(mag_ctx* c, int32_t sid, int32_t n, const void* k, const void* v) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "kv_append: session %d is not open", sid);
+  if (n < 0 || (n > 0 && (!k || !v))) return fail(c, MAG_ERR_INVALID_ARG, "kv_append: bad arguments");
+  Session& s = c->sessions[sid];
+  if ((int64_t)s.len + n > c->cfg.max_context)
+    return fail(c, MAG_ERR_CONTEXT_FULL, "kv_append: %d + %d tokens exceed max_context %d", s.len, n,
+                c->cfg.max_context);
+  const int nb_old = (s.len + 15) / 16, nb_new = (s.len + n + 15) / 16;
+  if (nb_new - nb_old > (int)c->free_list.size())
+    return fail(c, MAG_ERR_KV_FULL, "kv_append: needs %d blocks, %zu free", nb_new - nb_old, c->free_list.size());
+  if (n == 0) return MAG_OK;
+  for (int i = nb_old; i < nb_new; ++i) {
+    s.table.push_back(c->free_list.front());
+    c->free_list.pop_front();
+  }
+  int32_t* row = c->d_tables + (size_t)sid * c->table_stride;
+  if (nb_new > nb_old)
+    CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
+                                cudaMemcpyHostToDevice, c->stream));
+  KvStoreArgs a = {};
+  a.k = (const __half*)k;
+  a.v = (const __half*)v;
+  a.n_tok = n;
+  a.n_layers = c->L;
+  a.pos0 = s.len;
+  a.table = row;
+  a.pool = pool_geom(c);
+  Launch L{c->stream, false, nullptr};
+  // grid.x is the token count: split very long appends to respect the grid limit
+  for (int t0 = 0; t0 < n; t0 += 65535) {
+    KvStoreArgs b = a;
+    b.n_tok = std::min(65535, n - t0);
+    b.pos0 = s.len + t0;
+    // the source is [L][n][Hkv][d]: a slice of tokens is strided per layer, so
+    // slices go one layer at a time
+    for (int l = 0; l < c->L; ++l) {
+      KvStoreArgs bl = b;
+      bl.k = a.k + ((size_t)l * n + t0) * c->Hkv * c->d;
+      bl.v = a.v + ((size_t)l * n + t0) * c->Hkv * c->d;
+      bl.n_layers = 1;
+      bl.pool.base = c->pool + (size_t)l * c->cfg.pool_blocks * c->block_bytes;
+      CUDA_TRY(c, launch_kv_store(L, bl));
+    }
+  }
+  s.len += n;
+  return MAG_OK;
+}
+
+static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs& a) {
+  if (B < 1 || B > c->B_max) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: batch %d not in 1..%d", B, c->B_max);
+  if (!sids) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: null session ids");
+  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "decode_step: not every weight is loaded");
+  int need = 0;
+  for (int b = 0; b < B; ++b) {
+    int s = sids[b];
+    if (s < 0 || s >= (int)c->sessions.size() || !c->sessions[s].open)
+      return fail(c, MAG_ERR_INVALID_ARG, "decode_step: session %d is not open", s);
+    for (int j = 0; j < b; ++j)
+      if (sids[j] == s) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: session %d appears twice", s);
+    if (c->sessions[s].len + 1 > c->cfg.max_context)
+      return fail(c, MAG_ERR_CONTEXT_FULL, "decode_step: session %d is at max_context", s);
+    if (c->sessions[s].len % 16 == 0) ++need;
+  }
+  if (need > (int)c->free_list.size())
+    return fail(c, MAG_ERR_KV_FULL, "decode_step: needs %d blocks, %zu free", need, c->free_list.size());
+  a.batch = B;
+  a.n_upd = 0;
+  for (int b = 0; b < B; ++b) {
+    Session& s = c->sessions[sids[b]];
+    a.sess[b] = sids[b];
+    a.pos[b] = s.len;
+    if (s.len % 16 == 0) {
+      int blk = c->free_list.front();
+      c->free_list.pop_front();
+      s.table.push_back(blk);
+      a.upd_sess[a.n_upd] = sids[b];
+      a.upd_idx[a.n_upd] = s.len / 16;
+      a.upd_blk[a.n_upd] = blk;
+      ++a.n_upd;
+    }
+  }
+  return MAG_OK;
+}
+
+mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!in || !out) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: null buffer");
+  const int slot = c->ring_pos;
+  CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
+  StepArgs& a = c->h_ring[slot];
+  memset(&a, 0, sizeof a);
+  mag_status st = step_prepare(c, B, sids, a);
+  if (st != MAG_OK) return st;
+  a.hidden_in = (const __half*)in;
+  a.out = out;
+  CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
+  CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
+  c->ring_pos = (slot + 1) % kRing;
+  if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
+    int n = 0;
+    CUDA_TRY(c, record_step(c, B, &n));
+    c->last_launches = n;
+  } else {
+    if (!c->graphs[B]) {
+      cudaGraph_t g = nullptr;
+      int n = 0;
+      CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+      cudaError_t e = record_step(c, B, &n);
+      cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+      if (e != cudaSuccess || e2 != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return fail(c, MAG_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
+      }
+      cudaError_t e3 = cudaGraphInstantiate(&c->graphs[B], g, 0);
+      cudaGraphDestroy(g);
+      if (e3 != cudaSuccess) return fail(c, MAG_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e3));
+      c->graph_launches[B] = n;
+    }
+    CUDA_TRY(c, cudaGraphLaunch(c->graphs[B], c->stream));
+    c->last_launches = c->graph_launches[B];
+  }
+  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
+  return MAG_OK;
+}
+
+mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, const void* in_host, void* out_host) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!in_host || !out_host) return fail(c, MAG_ERR_INVALID_ARG, "decode_step_host: null buffer");
+  if (B < 1 || B > c->B_max) return fail(c, MAG_ERR_INVALID_ARG, "decode_step_host: batch %d", B);
+  const size_t in_b = (size_t)B * c->D * 2, out_b = (size_t)B * (c->V ? c->V : c->D) * 2;
+  CUDA_TRY(c, cudaMemcpyAsync(c->d_in_stage, in_host, in_b, cudaMemcpyHostToDevice, c->stream));
+  mag_status st = mag_decode_step(c, B, sids, c->d_in_stage, c->d_out_stage);
+  if (st != MAG_OK) return st;
+  CUDA_TRY(c, cudaMemcpyAsync(out_host, c->d_out_stage, out_b, cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return MAG_OK;
+}
+
+mag_status mag_prefill_chunk(mag_ctx* c, int32_t, int32_t, const void*, void*) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  return fail(c, MAG_ERR_UNSUPPORTED, "prefill_chunk: not available in this build");
+}
+
+mag_status mag_sync(mag_ctx* c) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return MAG_OK;
+}
+
+mag_status mag_get_memory_stats(mag_ctx* c, mag_memory_stats* s) {
+  if (!c || !s) return MAG_ERR_INVALID_ARG;
+  memset(s, 0, sizeof *s);
+  s->weight_bytes = c->wbytes;
+  s->kv_pool_bytes = c->pool_bytes;
+  s->kv_block_bytes = c->block_bytes;
+  s->pool_blocks_total = c->cfg.pool_blocks;
+  s->pool_blocks_free = (int32_t)c->free_list.size();
+  s->arena_bytes = c->arena_bytes;
+  s->arena_unshared_bytes = c->arena_unshared;
+  s->other_device_bytes = c->other_bytes;
+  int open = 0;
+  for (auto& x : c->sessions) open += x.open;
+  s->sessions_open = open;
+  return MAG_OK;
+}
+
+mag_status mag_debug_read_weights(mag_ctx* c, int32_t tensor, int32_t layer, void* dst, size_t bytes) {
+  if (!c || !dst) return MAG_ERR_INVALID_ARG;
+  if (tensor < MAG_W_QKV || tensor > MAG_W_DOWN || layer < 0 || layer >= c->L)
+    return fail(c, MAG_ERR_INVALID_ARG, "debug_read_weights: projections only");
+  Proj& p = c->proj[(size_t)layer * 4 + tensor];
+  if (bytes != p.bytes) return fail(c, MAG_ERR_INVALID_ARG, "debug_read_weights: expected %zu bytes", p.bytes);
+  CUDA_TRY(c, cudaMemcpyAsync(dst, p.codes, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  return MAG_OK;
+}
+
+mag_status mag_debug_kv_locate(mag_ctx* c, int32_t sid, int32_t layer, int32_t tok, int64_t out[5]) {
+  if (!c || !out) return MAG_ERR_INVALID_ARG;
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open || layer < 0 || layer >= c->L || tok < 0 ||
+      tok >= c->sessions[sid].len)
+    return fail(c, MAG_ERR_INVALID_ARG, "debug_kv_locate: bad session/layer/token");
+  const int blk = c->sessions[sid].table[tok / 16], slot = tok % 16;
+  const int64_t base = ((int64_t)layer * c->cfg.pool_blocks + blk) * c->block_bytes;
+  const int64_t vec = (int64_t)(0) * 16 + slot;
+  (void)vec;
+  const int64_t data_part = (int64_t)c->Hkv * 16 * c->data_bytes, meta_part = (int64_t)c->Hkv * 16 * c->meta_bytes;
+  // head 0; callers add head * 16 * bytes per vector
+  out[0] = base + (int64_t)slot * c->data_bytes;
+  out[1] = base + data_part + (int64_t)slot * c->data_bytes;
+  out[2] = c->meta_bytes ? base + 2 * data_part + (int64_t)slot * c->meta_bytes : -1;
+  out[3] = c->meta_bytes ? base + 2 * data_part + meta_part + (int64_t)slot * c->meta_bytes : -1;
+  out[4] = blk;
+  return MAG_OK;
+}
+
+mag_status mag_debug_pool(mag_ctx* c, void** p, uint64_t* bytes) {
+  if (!c || !p || !bytes) return MAG_ERR_INVALID_ARG;
+  *p = c->pool;
+  *bytes = c->pool_bytes;
+  return MAG_OK;
+}
+
+mag_status mag_debug_arena_plan(mag_ctx* c, int32_t phase, mag_arena_tensor* out, int32_t cap, int32_t* n_out,
+                                uint64_t* arena_bytes) {
+  if (!c || !n_out || !arena_bytes || cap < 0 || (cap && !out)) return MAG_ERR_INVALID_ARG;
+  if (phase != 0) return fail(c, MAG_ERR_UNSUPPORTED, "debug_arena_plan: only the decode phase is planned");
+  *n_out = (int32_t)c->plan.size();
+  *arena_bytes = c->arena_bytes;
+  for (int i = 0; i < (int)c->plan.size() && i < cap; ++i) {
+    memset(&out[i], 0, sizeof out[i]);
+    snprintf(out[i].name, sizeof out[i].name, "%s", c->plan[i].name.c_str());
+    out[i].size = c->plan[i].size;
+    out[i].first = c->plan[i].first;
+    out[i].last = c->plan[i].last;
+    out[i].offset = c->plan[i].offset;
+  }
+  return MAG_OK;
+}
+
+int32_t mag_debug_last_step_launches(mag_ctx* c) { return c ? c->last_launches : 0; }
+
+}  // extern "C"
