@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Decode-step benchmark on GB300: decode tokens/s and achieved HBM GB/s.
+
+Default workload: the 8B-shaped decode step, batch 1, FP16 KV at context 2048
+(32 layers, D 4096, 32/8 heads, d 128, F 14336, V 128256; W4 group-32 weights
+N(0, 0.02), FP16 LM head, KV N(0, 1), 16-token blocks). Every timed step runs
+on its own session holding exactly 2048 prior tokens, so each step is that
+workload. The inputs (5.4 GB of weights, 268 MB of KV per session) are far
+larger than the 126 MB L2, so no L2 flush is needed between steps.
+
+python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth.workloads import (DECODE_8B, LLAMA8B, LONG_FP16, LONG_INT4, LONG_INT8, KV_FP16, KV_INT4, KV_INT8,  # noqa
+                             Workload, agent_batch, shrink)
+
+METRIC = "decode tokens/s per GB300 and achieved HBM GB/s (% of peak) per decode step"
+UNIT = "tokens/s"
+CPU_SAMPLE_LAYERS = 2
+
+
+def workload_by_name(name: str, seed: int) -> Workload:
+    table = {w.name: w for w in (DECODE_8B, LONG_FP16, LONG_INT8, LONG_INT4)}
+    if name.startswith("8b-decode-b16-agent"):
+        return agent_batch(seed)
+    return table[name]
+
+
+def kv_token_bytes(shape, dt) -> int:
+    per_head = {KV_FP16: 2 * shape.head_dim, KV_INT8: shape.head_dim + 2,
+                KV_INT4: shape.head_dim // 2 + (shape.head_dim // 32) * 4}[dt]
+    return 2 * shape.n_layers * shape.n_kv_heads * per_head
+
+
+def weight_bytes(shape) -> dict:
+    """Algorithmic bytes of each projection (packed codes + fp16 scale/min) and of the fp16 LM head."""
+    D, F, R, Hd = shape.hidden, shape.ffn, shape.qkv_rows, shape.n_heads * shape.head_dim
+    w4 = lambda n, k: n * (-(-k // 32)) * (16 + 4)
+    return {"qkv": w4(R, D), "o_proj": w4(D, Hd), "gate_up": w4(2 * F, D), "down": w4(D, F),
+            "lm_head": shape.vocab * D * 2, "norms": (2 * shape.n_layers + 1) * D * 2}
+
+
+def step_bytes(wl: Workload) -> int:
+    """Bytes the step must move: every weight once, the live KV once, the appended KV once."""
+    s = wl.shape
+    wb = weight_bytes(s)
+    w = s.n_layers * (wb["qkv"] + wb["o_proj"] + wb["gate_up"] + wb["down"]) + wb["lm_head"] + wb["norms"]
+    kv = kv_token_bytes(s, wl.kv_dtype)
+    return w + sum(p * kv for p in wl.prior) + wl.batch * kv
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return None
+        sm = [float(r[1]) for r in self.rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in self.rows:
+            if len(r) > 8:
+                for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                   r[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_job(world, elapsed_s: float, units: float):
+    """Whole-job throughput: units summed over ranks / slowest rank's time (replicas, weak scaling)."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ============================================================================ oracle (CPU) leg
+
+def oracle_sample_setup(wl: Workload, seed: int, lm_head=None):
+    """The oracle on a bounded sample of the workload: the first CPU_SAMPLE_LAYERS layers (with their full
+    weights and KV) and, separately, the final norm + full LM head."""
+    import oracle
+    import synth
+    from tests.helpers import model_cfg, oracle_weights
+    s = wl.shape
+    part = shrink(s, n_layers=CPU_SAMPLE_LAYERS, vocab=0)
+    w_layers = oracle_weights(part, seed)
+    cfg_layers = model_cfg(part, wl.kv_dtype)
+    kvs = []
+    for i, p in enumerate(wl.prior):
+        kv = oracle.KV(cfg_layers, p + 1)
+        L, H, d = part.n_layers, s.n_kv_heads, s.head_dim
+        k = np.empty((L, p, H, d), np.float16)
+        v = np.empty((L, p, H, d), np.float16)
+        for l in range(L):
+            k[l] = synth.prior_kv_f16(seed, i, l, "K", p, H, d)
+            v[l] = synth.prior_kv_f16(seed, i, l, "V", p, H, d)
+        kv.append(k, v)
+        kvs.append(kv)
+    head = shrink(s, n_layers=0)
+    w_head = oracle.Weights(gamma_f=synth.norm_gain_f16(seed, "gf", s.hidden),
+                            lm_head=lm_head if lm_head is not None else synth.lm_head_f16(seed, s.vocab, s.hidden))
+    cfg_head = model_cfg(head, wl.kv_dtype)
+    rope = oracle.rope_table(max(wl.prior) + 64, s.head_dim, s.rope_base)
+    return dict(part=part, w_layers=w_layers, cfg_layers=cfg_layers, kvs=kvs, w_head=w_head, cfg_head=cfg_head,
+                rope=rope, head_kv=[oracle.KV(cfg_head, 1) for _ in wl.prior], prior=list(wl.prior))
+
+
+def oracle_sample_step(wl: Workload, st: dict, seed: int, step: int):
+    """Seconds of CPU for one full decode step, scaled from the sample: layers x (L / sample layers) + head."""
+    import oracle
+    from synth import driver
+    x = driver.step_inputs(wl, seed, step)
+    for kv, p in zip(st["kvs"], st["prior"]):  # every step sees exactly the workload's prior context
+        kv.truncate(p)
+    for kv in st["head_kv"]:
+        kv.truncate(0)
+    t0 = time.perf_counter()
+    oracle.forward(st["cfg_layers"], st["w_layers"], st["kvs"], [1] * wl.batch, x, *st["rope"])
+    t1 = time.perf_counter()
+    oracle.forward(st["cfg_head"], st["w_head"], st["head_kv"], [1] * wl.batch, x, *st["rope"])
+    t2 = time.perf_counter()
+    return (t1 - t0) * wl.shape.n_layers / CPU_SAMPLE_LAYERS + (t2 - t1)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def sample_text(wl):
+    return (f"{CPU_SAMPLE_LAYERS} of {wl.shape.n_layers} layers (full weights, full {'/'.join(map(str, wl.prior))}"
+            f"-token KV) timed and scaled x{wl.shape.n_layers // CPU_SAMPLE_LAYERS}, plus the final norm and full "
+            f"{wl.shape.vocab}-row LM head, per decode step of batch {wl.batch}")
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = workload_by_name(args.workload, args.seed)
+    st = oracle_sample_setup(wl, args.seed)
+    for i in range(args.warmup):
+        oracle_sample_step(wl, st, args.seed, i)
+    ts = [oracle_sample_step(wl, st, args.seed, args.warmup + i) for i in range(args.steps)]
+    total = sum(ts)
+    value = wl.batch * args.steps / total
+    cores = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) KV and inputs)",
+            "config": {"workload": wl.name, "batch": wl.batch, "context": list(wl.prior), "kv_dtype": wl.kv_dtype},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text(wl)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ============================================================================ GPU leg
+
+def traffic_from_profile(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+        src = os.path.join(ROOT, "quantized_decode_step_gb300", "csrc", prof["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        e = prof["kernels"][kernel_key]
+        return e["dram_bytes_per_launch"] if e.get("source_sha") == h else None
+    except Exception:
+        return None
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import quantized_decode_step_gb300 as mag
+    import synth
+    from synth import driver, hidden_f16, pool_order
+
+    torch.cuda.set_device(local)
+    mag.build()
+    wl = workload_by_name(args.workload, args.seed)
+    shape = wl.shape
+    n_runs = args.warmup + args.steps
+    e2e_steps = max(3, min(args.steps, 10))
+    prof_steps = 3
+    n_sets = n_runs + e2e_steps + prof_steps  # session sets: one fresh set per step
+    B = wl.batch
+    n_sess = n_sets * B
+    blocks = n_sets * sum(-(-(p + 1) // 16) for p in wl.prior)
+    stream = torch.cuda.Stream()
+    order = pool_order(args.seed, blocks) if wl.scattered_pool else None
+    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sess, max_batch=B,
+                          max_context=max(wl.prior) + 1, pool_order=order)
+    t_setup = time.time()
+    ctx = mag.Context(cfg, stream.cuda_stream)
+    lm_keep = {}
+    with torch.cuda.stream(stream):
+        driver.load_weights(ctx, shape, args.seed)
+        # prior KV: each session set holds the same seeded priors (drawn once per session of the batch)
+        sets = []
+        for s in range(n_sets):
+            sets.append([ctx.session_open() for _ in range(B)])
+        L, H, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
+        for i, p in enumerate(wl.prior):
+            for t0 in range(0, p, 4096):
+                n = min(4096, p - t0)
+                k = np.empty((L, n, H, d), np.float16)
+                v = np.empty((L, n, H, d), np.float16)
+                for l in range(L):
+                    k[l] = synth.prior_kv_f16(args.seed, i, l, "K", n, H, d, tok0=t0)
+                    v[l] = synth.prior_kv_f16(args.seed, i, l, "V", n, H, d, tok0=t0)
+                kt, vt = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
+                for s in range(n_sets):
+                    ctx.kv_append(sets[s][i], n, kt, vt)
+                stream.synchronize()
+                del kt, vt
+        x = torch.from_numpy(hidden_f16(args.seed, B, shape.hidden, tag="x.step0")).cuda()
+        width = shape.vocab or shape.hidden
+        out = torch.empty((B, width), dtype=torch.float16, device="cuda")
+    stream.synchronize()
+    t_setup = time.time() - t_setup
+
+    # ---- timed region: K steps, each on a fresh session set
+    for i in range(args.warmup):
+        ctx.decode_step(sets[i], x, out)
+    stream.synchronize()
+    launches_per_step = ctx.last_step_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            ctx.decode_step(sets[args.warmup + i], x, out)
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+    elapsed_s = ev0.elapsed_time(ev1) / 1e3
+    job_s, job_units = reduce_job(world, elapsed_s, B * args.steps)
+    value = job_units / job_s
+    ms_per_step = 1e3 * elapsed_s / args.steps
+
+    # ---- end to end: host buffers through the C ABI, copies inside the timed region
+    x_host = hidden_f16(args.seed, B, shape.hidden, tag="x.step0")
+    out_host = np.empty((B, width), np.float16)
+    base = n_runs
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        ctx.decode_step_host(sets[base + i], x_host, out_host)
+    e2e_s = time.perf_counter() - t0
+    e2e_job_s, e2e_units = reduce_job(world, e2e_s, B * e2e_steps)
+
+    # ---- per-kernel device times (instrumented replay of the same step on fresh sessions)
+    per_kind = {}
+    for i in range(prof_steps):
+        for kind, ms in ctx.profile_step(sets[base + e2e_steps + i], x, out):
+            per_kind.setdefault(kind, []).append(ms)
+    stream.synchronize()
+
+    if rank != 0:
+        return
+    hbm, tc, peak_src = measured_peaks()
+    sb = step_bytes(wl)
+    wb = weight_bytes(shape)
+    kernel_bytes = {"gate_up": wb["gate_up"], "qkv": wb["qkv"], "o_proj": wb["o_proj"], "down": wb["down"],
+                    "lm_head": wb["lm_head"]}
+    kern_rows = {}
+    for kind, v in per_kind.items():
+        per_launch = statistics.mean(v)
+        row = {"launches_per_step": len(v) // prof_steps, "ms_per_launch": per_launch,
+               "ms_per_step": sum(v) / prof_steps}
+        if kind in kernel_bytes:
+            row["gbs"] = kernel_bytes[kind] / (per_launch / 1e3) / 1e9
+        kern_rows[kind] = row
+    dom = "gate_up"
+    dom_ms = kern_rows[dom]["ms_per_launch"]
+    achieved = kernel_bytes[dom] / (dom_ms / 1e3) / 1e9
+    clocks = clk.summary()
+    cores = cpu_cores()
+    # ---- CPU baseline: the oracle on a bounded sample of this workload (rank 0, N = 1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        st = oracle_sample_setup(wl, args.seed)
+        oracle_sample_step(wl, st, args.seed, 0)
+        t_cpu = oracle_sample_step(wl, st, args.seed, 1)
+        cpu = {"value": B / t_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text(wl),
+               "s_per_step": t_cpu}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic: seeded N(0,0.02) weights quantised to W4 g32, fp16 LM head, N(0,1) KV and inputs",
+        "config": {"workload": wl.name, "batch": B, "context": list(wl.prior), "kv_dtype": wl.kv_dtype,
+                   "layers": shape.n_layers, "hidden": shape.hidden, "heads": [shape.n_heads, shape.n_kv_heads],
+                   "head_dim": shape.head_dim, "ffn": shape.ffn, "vocab": shape.vocab,
+                   "l2": "inputs larger than L2 (5.4 GB weights + KV per step), no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "step_bytes": sb, "hbm_gbs_step": sb / (ms_per_step / 1e3) / 1e9,
+        "hbm_frac_step": sb / (ms_per_step / 1e3) / 1e9 / hbm,
+        "roofline": {"bound": "hbm", "kernel": "W4 gate-up GEMV (RMSNorm + SwiGLU fused), 28672x4096",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": peak_src, "algorithmic_bytes_per_launch": kernel_bytes[dom],
+                     "traffic": traffic_from_profile(dom)},
+        "kernels": kern_rows,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_units / e2e_job_s, "unit": UNIT, "h2d_bytes_per_step": B * shape.hidden * 2,
+                "d2h_bytes_per_step": B * width * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "setup_s": t_setup,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default=DECODE_8B.name)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

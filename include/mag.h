@@ -236,6 +236,28 @@ mag_status mag_debug_arena_plan(mag_ctx* ctx, int32_t phase, mag_arena_tensor* o
 /* Kernel launches of the last decode step (0 if none ran yet). */
 int32_t mag_debug_last_step_launches(mag_ctx* ctx);
 
+/* Kinds of kernel launch reported by mag_debug_profile_step. */
+typedef enum {
+  MAG_OP_STEP_BEGIN = 0,   /* block-table writes, fp16 input -> fp32 residual */
+  MAG_OP_QKV = 1,          /* RMSNorm + W4 QKV GEMV */
+  MAG_OP_ROPE_APPEND = 2,  /* RoPE of q and k, K/V store into the pool */
+  MAG_OP_ATTENTION = 3,    /* split-K attention over the pool + split merge */
+  MAG_OP_O = 4,            /* W4 O GEMV + residual */
+  MAG_OP_GATE_UP = 5,      /* RMSNorm + W4 gate-up GEMV + SwiGLU */
+  MAG_OP_DOWN = 6,         /* W4 down GEMV + residual */
+  MAG_OP_LM_HEAD = 7,      /* final RMSNorm + fp16 LM head GEMV */
+  MAG_OP_FINAL_HIDDEN = 8  /* fp16 hidden-state output (no LM head) */
+} mag_op;
+
+/* One decode step like mag_decode_step but launched kernel by kernel (no
+ * graph, no programmatic dependent launch) with a CUDA event pair around each
+ * launch on the context's stream; synchronises, then writes the launch count
+ * to n_out and, for the first `cap` launches, kinds[i] (mag_op) and ms[i]
+ * (device time between the pair). The session lengths advance as in a step. */
+mag_status mag_debug_profile_step(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host,
+                                  const void* hidden_in_dev, void* out_dev, int32_t* kinds, float* ms, int32_t cap,
+                                  int32_t* n_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -85,6 +85,7 @@ def lib():
                 "orc_kv_create": ([ctypes.POINTER(Cfg), i32], vp),
                 "orc_kv_destroy": ([vp], None),
                 "orc_kv_len": ([vp], i32),
+                "orc_kv_truncate": ([vp, i32], None),
                 "orc_kv_append": ([vp, i32, vp, vp], i32),
                 "orc_kv_read": ([vp, i32, i32, i32, i32, vp], None),
                 "orc_kv_stored": ([vp, i32, i32, i32, i32, vp, vp], i64),
@@ -373,6 +374,9 @@ class KV:
 
     def __len__(self):
         return int(lib().orc_kv_len(self.h))
+
+    def truncate(self, n: int):
+        lib().orc_kv_truncate(self.h, n)
 
     def append(self, k_f16, v_f16):
         """k, v: fp16 [L, n, Hkv, d] (already rotated)."""

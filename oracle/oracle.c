@@ -415,6 +415,11 @@ void orc_kv_destroy(orc_kv* kv) {
 
 int orc_kv_len(const orc_kv* kv) { return kv->len; }
 
+/* Forget every token from position len on (bookkeeping only). */
+void orc_kv_truncate(orc_kv* kv, int len) {
+  if (len >= 0 && len <= kv->len) kv->len = len;
+}
+
 /* Store one fp16 vector of head_dim values in the configured KV precision. */
 static void kv_store_vec(orc_kv* kv, int layer, int which, int tok, int head, const uint16_t* x) {
   int H = kv->cfg.n_kv_heads, d = kv->cfg.head_dim, dt = kv->cfg.kv_dtype;
@@ -437,6 +442,7 @@ static void kv_store_vec(orc_kv* kv, int layer, int which, int tok, int head, co
 int orc_kv_append(orc_kv* kv, int n_tok, const uint16_t* k, const uint16_t* v) {
   int L = kv->cfg.n_layers, H = kv->cfg.n_kv_heads, d = kv->cfg.head_dim;
   if (kv->len + n_tok > kv->cap) return -1;
+#pragma omp parallel for schedule(static)
   for (int l = 0; l < L; ++l)
     for (int t = 0; t < n_tok; ++t)
       for (int h = 0; h < H; ++h) {

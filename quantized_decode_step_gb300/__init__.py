@@ -29,8 +29,9 @@ EXPORTED = [
     "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk", "mag_sync",
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
-    "mag_debug_last_step_launches",
+    "mag_debug_last_step_launches", "mag_debug_profile_step",
 ]
+OP_NAMES = ["step_begin", "qkv", "rope_append", "attention", "o_proj", "gate_up", "down", "lm_head", "final_hidden"]
 
 
 class MagError(RuntimeError):
@@ -99,6 +100,8 @@ def lib():
                 "mag_debug_pool": ([vp, ctypes.POINTER(vp), ctypes.POINTER(u64)], i32),
                 "mag_debug_arena_plan": ([vp, i32, ctypes.POINTER(ArenaTensor), i32, P32, ctypes.POINTER(u64)], i32),
                 "mag_debug_last_step_launches": ([vp], i32),
+                "mag_debug_profile_step": ([vp, i32, P32, vp, vp, P32, ctypes.POINTER(ctypes.c_float), i32, P32],
+                                           i32),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -237,3 +240,13 @@ class Context:
 
     def last_step_launches(self) -> int:
         return int(lib().mag_debug_last_step_launches(self.h))
+
+    def profile_step(self, sessions, hidden_in, out, cap=4096):
+        """Instrumented step: list of (op name, device ms) per kernel launch."""
+        ids = (ctypes.c_int32 * len(sessions))(*sessions)
+        kinds = (ctypes.c_int32 * cap)()
+        ms = (ctypes.c_float * cap)()
+        n = ctypes.c_int32()
+        self._check(lib().mag_debug_profile_step(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out), kinds, ms,
+                                                 cap, ctypes.byref(n)), "mag_debug_profile_step")
+        return [(OP_NAMES[kinds[i]], float(ms[i])) for i in range(min(n.value, cap))]

@@ -37,6 +37,31 @@ struct GemvPlan {
   int mpc, wk, ks, cpc;
 };
 
+// Event pairs around each launch of an instrumented (eager) step.
+struct Profiler {
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int> kinds;
+  cudaError_t begin(cudaStream_t s) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) return r;
+    start.push_back(e);
+    return cudaEventRecord(e, s);
+  }
+  cudaError_t end(cudaStream_t s, int kind) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) return r;
+    stop.push_back(e);
+    kinds.push_back(kind);
+    return cudaEventRecord(e, s);
+  }
+  ~Profiler() {
+    for (auto e : start) cudaEventDestroy(e);
+    for (auto e : stop) cudaEventDestroy(e);
+  }
+};
+
 }  // namespace
 
 struct mag_ctx {
@@ -265,12 +290,19 @@ GemvArgs gemv_args(const mag_ctx* c, const Proj& p, int B, int n_mtiles, bool f1
 }
 
 // Enqueue the whole decode step for batch B (captured into a graph or run eagerly).
-cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
-  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL);
+cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullptr) {
+  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof;
   Launch L0{c->stream, false, n_launch};
   Launch L{c->stream, pdl, n_launch};
   cudaError_t e;
-  if ((e = launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B)) != cudaSuccess) return e;
+  // every launch goes through MAG_RUN, which brackets it with events when profiling
+#define MAG_RUN(kind, call)                                                   \
+  do {                                                                       \
+    if (prof && (e = prof->begin(c->stream)) != cudaSuccess) return e;       \
+    if ((e = (call)) != cudaSuccess) return e;                               \
+    if (prof && (e = prof->end(c->stream, (kind))) != cudaSuccess) return e; \
+  } while (0)
+  MAG_RUN(MAG_OP_STEP_BEGIN, launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B));
   const PoolGeom pg = pool_geom(c);
   const int S = attn_splits(c, B);
   for (int l = 0; l < c->L; ++l) {
@@ -282,7 +314,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
       a.gamma = c->gamma1[l];
       a.out_h = c->qkv;
       a.ldo = c->R;
-      if ((e = launch_gemv(L, a, W_W4, X_NORM, EPI_STORE)) != cudaSuccess) return e;
+      MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, X_NORM, EPI_STORE));
     }
     {  // RoPE + KV append
       RopeAppendArgs a = {};
@@ -296,7 +328,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
       a.layer = l;
       a.pool = pg;
       a.step = c->d_args;
-      if ((e = launch_rope_append(L, a, B)) != cudaSuccess) return e;
+      MAG_RUN(MAG_OP_ROPE_APPEND, launch_rope_append(L, a, B));
     }
     {  // attention
       AttnArgs a = {};
@@ -312,7 +344,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
       a.counters = c->d_attn_counters;
       a.pool = pg;
       a.step = c->d_args;
-      if ((e = launch_attention(L, a, B)) != cudaSuccess) return e;
+      MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
     {  // O projection + residual
       GemvArgs a = gemv_args(c, P[1], B, c->D / 16, false);
@@ -320,7 +352,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
       a.ldx = c->Hq * c->d;
       a.out_r = c->r;
       a.ldo = c->D;
-      if ((e = launch_gemv(L, a, W_W4, X_F16, EPI_RESID)) != cudaSuccess) return e;
+      MAG_RUN(MAG_OP_O, launch_gemv(L, a, W_W4, X_F16, EPI_RESID));
     }
     {  // RMSNorm + gate-up + SwiGLU
       GemvArgs a = gemv_args(c, P[2], B, c->F / 8, false);
@@ -330,7 +362,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
       a.gamma = c->gamma2[l];
       a.out_h = c->act;
       a.ldo = c->F;
-      if ((e = launch_gemv(L, a, W_W4, X_NORM, EPI_SWIGLU)) != cudaSuccess) return e;
+      MAG_RUN(MAG_OP_GATE_UP, launch_gemv(L, a, W_W4, X_NORM, EPI_SWIGLU));
     }
     {  // down projection + residual
       GemvArgs a = gemv_args(c, P[3], B, c->D / 16, false);
@@ -338,7 +370,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
       a.ldx = c->F;
       a.out_r = c->r;
       a.ldo = c->D;
-      if ((e = launch_gemv(L, a, W_W4, X_F16, EPI_RESID)) != cudaSuccess) return e;
+      MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, X_F16, EPI_RESID));
     }
   }
   if (c->V) {
@@ -351,10 +383,11 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch) {
     a.ldr = c->D;
     a.gamma = c->gamma_f;
     a.ldo = c->V;
-    if ((e = launch_gemv(L, a, W_F16, X_NORM, EPI_STORE_OUT)) != cudaSuccess) return e;
+    MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, X_NORM, EPI_STORE_OUT));
   } else {
-    if ((e = launch_final_hidden(L, c->d_args, c->r, c->D, B)) != cudaSuccess) return e;
+    MAG_RUN(MAG_OP_FINAL_HIDDEN, launch_final_hidden(L, c->d_args, c->r, c->D, B));
   }
+#undef MAG_RUN
   return cudaSuccess;
 }
 
@@ -765,8 +798,7 @@ static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs&
   return MAG_OK;
 }
 
-mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out) {
-  if (!c) return MAG_ERR_INVALID_ARG;
+static mag_status step_upload(mag_ctx* c, int B, const int32_t* sids, const void* in, void* out) {
   if (!in || !out) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: null buffer");
   const int slot = c->ring_pos;
   CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
@@ -779,6 +811,13 @@ mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const voi
   CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
   CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
   c->ring_pos = (slot + 1) % kRing;
+  return MAG_OK;
+}
+
+mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  mag_status st = step_upload(c, B, sids, in, out);
+  if (st != MAG_OK) return st;
   if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
     int n = 0;
     CUDA_TRY(c, record_step(c, B, &n));
@@ -803,6 +842,25 @@ mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const voi
     c->last_launches = c->graph_launches[B];
   }
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
+  return MAG_OK;
+}
+
+mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out,
+                                  int32_t* kinds, float* ms, int32_t cap, int32_t* n_out) {
+  if (!c || !n_out || cap < 0 || (cap && (!kinds || !ms))) return MAG_ERR_INVALID_ARG;
+  mag_status st = step_upload(c, B, sids, in, out);
+  if (st != MAG_OK) return st;
+  Profiler prof;
+  int n = 0;
+  CUDA_TRY(c, record_step(c, B, &n, &prof));
+  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  *n_out = (int32_t)prof.kinds.size();
+  for (int i = 0; i < (int)prof.kinds.size() && i < cap; ++i) {
+    kinds[i] = prof.kinds[i];
+    CUDA_TRY(c, cudaEventElapsedTime(&ms[i], prof.start[i], prof.stop[i]));
+  }
+  c->last_launches = n;
   return MAG_OK;
 }
 

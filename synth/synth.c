@@ -47,16 +47,6 @@ uint64_t synth_draw(uint64_t key, uint64_t i) { return mix64(key + (i + 1) * SYN
 
 static double to_unit(uint64_t x) { return ((double)(x >> 11) + 0.5) * (1.0 / 9007199254740992.0); }
 
-/* One standard normal: element i of the stream keyed by `key`. */
-static double normal_at(uint64_t key, uint64_t i) {
-  uint64_t j = i >> 1;
-  double u1 = to_unit(synth_draw(key, 2 * j));
-  double u2 = to_unit(synth_draw(key, 2 * j + 1));
-  double r = sqrt(-2.0 * log(u1));
-  double a = 6.283185307179586476925286766559 * u2;
-  return (i & 1) ? r * sin(a) : r * cos(a);
-}
-
 void synth_uniform_f64(uint64_t seed, const char* tag, int64_t n, double* out) {
   uint64_t key = synth_key(seed, tag);
 #pragma omp parallel for schedule(static)
@@ -69,34 +59,50 @@ void synth_u64(uint64_t seed, const char* tag, int64_t n, uint64_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = synth_draw(key, (uint64_t)i);
 }
 
-/* Normals starting at stream element `offset`, so that a large tensor can be
- * produced in slices that concatenate to the same values. */
+/* Normals for stream elements [offset, offset + n), so that a large tensor can
+ * be produced in slices that concatenate to the same values; each Box-Muller
+ * pair is computed once and both of its values are used. */
+#define SYNTH_NORMAL_LOOP(STORE)                                                   \
+  uint64_t key = synth_key(seed, tag);                                             \
+  int64_t j0 = offset >> 1, j1 = (offset + n + 1) >> 1;                            \
+  _Pragma("omp parallel for schedule(static)")                                     \
+  for (int64_t j = j0; j < j1; ++j) {                                              \
+    double u1 = to_unit(synth_draw(key, 2 * (uint64_t)j));                         \
+    double u2 = to_unit(synth_draw(key, 2 * (uint64_t)j + 1));                     \
+    double r = sqrt(-2.0 * log(u1));                                               \
+    double a = 6.283185307179586476925286766559 * u2;                              \
+    double v0 = mean + std * (r * cos(a)), v1 = mean + std * (r * sin(a));         \
+    int64_t i0 = 2 * j - offset, i1 = i0 + 1;                                       \
+    if (i0 >= 0 && i0 < n) STORE(i0, v0);                                          \
+    if (i1 >= 0 && i1 < n) STORE(i1, v1);                                          \
+  }
+
 void synth_normal_f64(uint64_t seed, const char* tag, int64_t offset, int64_t n, double mean, double std,
                       double* out) {
-  uint64_t key = synth_key(seed, tag);
-#pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < n; ++i) out[i] = mean + std * normal_at(key, (uint64_t)(offset + i));
+#define ST64(i, v) out[i] = (v)
+  SYNTH_NORMAL_LOOP(ST64)
+#undef ST64
 }
 
 void synth_normal_f32(uint64_t seed, const char* tag, int64_t offset, int64_t n, double mean, double std,
                       float* out) {
-  uint64_t key = synth_key(seed, tag);
-#pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < n; ++i) out[i] = (float)(mean + std * normal_at(key, (uint64_t)(offset + i)));
+#define ST32(i, v) out[i] = (float)(v)
+  SYNTH_NORMAL_LOOP(ST32)
+#undef ST32
 }
 
 /* Storage as IEEE binary16 bits; the compiler's _Float16 conversion rounds
  * to nearest even from double in one step. */
+static void store_f16(uint16_t* out, int64_t i, double v) {
+  _Float16 h = (_Float16)v;
+  memcpy(out + i, &h, 2);
+}
+
 void synth_normal_f16(uint64_t seed, const char* tag, int64_t offset, int64_t n, double mean, double std,
                       uint16_t* out) {
-  uint64_t key = synth_key(seed, tag);
-#pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < n; ++i) {
-    _Float16 h = (_Float16)(mean + std * normal_at(key, (uint64_t)(offset + i)));
-    uint16_t bits;
-    memcpy(&bits, &h, 2);
-    out[i] = bits;
-  }
+#define ST16(i, v) store_f16(out, i, v)
+  SYNTH_NORMAL_LOOP(ST16)
+#undef ST16
 }
 
 /* Uniform on [lo, hi) rounded to fp32. */

@@ -182,7 +182,7 @@ def test_kv_append_bytes_and_placement_bit_exact(dt):
 def _device_bytes(ptr, nbytes):
     """A uint8 CUDA tensor copy of `nbytes` at device address `ptr` (read through the CUDA array interface)."""
     class _Arr:
-        __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, True), "version": 3}
+        __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
     return torch.as_tensor(_Arr(), device="cuda").clone()
 
 
