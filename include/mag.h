@@ -238,15 +238,13 @@ int32_t mag_debug_last_step_launches(mag_ctx* ctx);
 
 /* Kinds of kernel launch reported by mag_debug_profile_step. */
 typedef enum {
-  MAG_OP_STEP_BEGIN = 0,   /* block-table writes, fp16 input -> fp32 residual */
-  MAG_OP_QKV = 1,          /* RMSNorm + W4 QKV GEMV */
-  MAG_OP_ROPE_APPEND = 2,  /* RoPE of q and k, K/V store into the pool */
-  MAG_OP_ATTENTION = 3,    /* split-K attention over the pool + split merge */
-  MAG_OP_O = 4,            /* W4 O GEMV + residual */
-  MAG_OP_GATE_UP = 5,      /* RMSNorm + W4 gate-up GEMV + SwiGLU */
-  MAG_OP_DOWN = 6,         /* W4 down GEMV + residual */
-  MAG_OP_LM_HEAD = 7,      /* final RMSNorm + fp16 LM head GEMV */
-  MAG_OP_FINAL_HIDDEN = 8  /* fp16 hidden-state output (no LM head) */
+  MAG_OP_STEP_BEGIN = 0, /* block-table writes, fp16 input -> fp32 residual, RMSNorm of layer 0 */
+  MAG_OP_QKV = 1,        /* W4 QKV GEMV + RoPE of q and k */
+  MAG_OP_ATTENTION = 2,  /* K/V append into the pool + split-K attention + split merge */
+  MAG_OP_O = 3,          /* W4 O GEMV + residual + RMSNorm (last block) */
+  MAG_OP_GATE_UP = 4,    /* W4 gate-up GEMV + SwiGLU */
+  MAG_OP_DOWN = 5,       /* W4 down GEMV + residual + next RMSNorm or output (last block) */
+  MAG_OP_LM_HEAD = 6     /* fp16 LM head GEMV */
 } mag_op;
 
 /* One decode step like mag_decode_step but launched kernel by kernel (no

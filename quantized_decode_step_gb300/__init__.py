@@ -31,7 +31,7 @@ EXPORTED = [
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
     "mag_debug_last_step_launches", "mag_debug_profile_step",
 ]
-OP_NAMES = ["step_begin", "qkv", "rope_append", "attention", "o_proj", "gate_up", "down", "lm_head", "final_hidden"]
+OP_NAMES = ["step_begin", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head"]
 
 
 class MagError(RuntimeError):

@@ -100,12 +100,16 @@ struct mag_ctx {
   uint64_t arena_bytes = 0, arena_unshared = 0;
   std::vector<ArenaTensor> plan;
   float* r = nullptr;
+  __half* xn = nullptr;
+  float* xn_sum = nullptr;
   __half* qkv = nullptr;
-  __half* qrot = nullptr;
   float* part_ml = nullptr;
   float* part_o = nullptr;
   __half* o = nullptr;
+  float* o_sum = nullptr;
+  float* ss_part = nullptr;
   __half* act = nullptr;
+  float* act_sum = nullptr;
   float* gemv_part = nullptr;
   int attn_split_max = 0;
 
@@ -150,24 +154,29 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 int proj_index(int tensor) { return tensor; }  // QKV=0, O=1, GU=2, DOWN=3
 
-GemvPlan plan_gemv(int n_mtiles, int K, int B, bool f16w) {
+// Launch shape of one projection at batch B. Up to 4 tokens the activations
+// are read straight from global memory (L1/L2 resident); above that they are
+// staged in shared memory per block, which then covers 8 tiles, and the
+// k-range is split so the staged slice fits in 64 KB.
+int gemv_xmode(int B) { return B <= 4 ? X_DIRECT : X_SMEM; }
+
+GemvPlan plan_gemv(int n_mtiles, int K, int B, bool f16w, bool swiglu) {
   GemvPlan p;
   const int n_chunks = (K + 63) / 64;
-  if (B <= 8) {
-    if (f16w) {
+  if (gemv_xmode(B) == X_DIRECT) {
+    if (f16w || swiglu || n_mtiles >= 1024) {
       p.mpc = 4;
       p.wk = 2;
-    } else if (n_mtiles >= 1024) {
-      p.mpc = 2;
-      p.wk = 4;
     } else {
       p.mpc = 1;
       p.wk = 8;
     }
-  } else {
-    p.mpc = 8;
-    p.wk = 1;
+    p.ks = 1;
+    p.cpc = n_chunks;
+    return p;
   }
+  p.mpc = 8;
+  p.wk = 1;
   const int max_cpc = std::max(1, (64 * 1024) / (B * 128) - 1);
   p.ks = (n_chunks + max_cpc - 1) / max_cpc;
   p.cpc = (n_chunks + p.ks - 1) / p.ks;
@@ -206,39 +215,43 @@ bool all_loaded(const mag_ctx* c) {
   return true;
 }
 
-// Sizes of the decode-phase gemv partial buffer for batch B.
+// The decode step's projections: (m-tiles, K, fp16 weights, SwiGLU)
+struct ProjShape {
+  int n_mtiles, K;
+  bool f16, swiglu;
+};
+std::vector<ProjShape> proj_shapes(const mag_ctx* c) {
+  std::vector<ProjShape> v = {{c->R / 16, c->D, false, false},
+                              {c->D / 16, c->Hq * c->d, false, false},
+                              {c->F / 8, c->D, false, true},
+                              {c->D / 16, c->F, false, false}};
+  if (c->V) v.push_back({c->V / 16, c->D, true, false});
+  return v;
+}
+
+// Floats of the k-split partial buffer for batch B.
 size_t gemv_partial_floats(const mag_ctx* c, int B) {
   size_t mx = 0;
   const int nt = B > 8 ? 2 : 1;
-  auto one = [&](int n_mtiles, int K, bool f16) {
-    GemvPlan p = plan_gemv(n_mtiles, K, B, f16);
-    if (p.ks > 1) mx = std::max(mx, (size_t)p.ks * n_mtiles * 32 * 4 * nt);
-  };
-  one(c->R / 16, c->D, false);
-  one(c->D / 16, c->Hq * c->d, false);
-  one(c->F / 8, c->D, false);
-  one(c->D / 16, c->F, false);
-  if (c->V) one(c->V / 16, c->D, true);
+  for (auto& ps : proj_shapes(c)) {
+    GemvPlan p = plan_gemv(ps.n_mtiles, ps.K, B, ps.f16, ps.swiglu);
+    if (p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
+  }
   return mx;
 }
 
 size_t gemv_grid_x(const mag_ctx* c, int B) {
   size_t mx = 0;
-  auto one = [&](int n_mtiles, int K, bool f16) {
-    GemvPlan p = plan_gemv(n_mtiles, K, B, f16);
-    mx = std::max(mx, (size_t)((n_mtiles + p.mpc - 1) / p.mpc));
-  };
-  one(c->R / 16, c->D, false);
-  one(c->D / 16, c->Hq * c->d, false);
-  one(c->F / 8, c->D, false);
-  one(c->D / 16, c->F, false);
-  if (c->V) one(c->V / 16, c->D, true);
+  for (auto& ps : proj_shapes(c)) {
+    GemvPlan p = plan_gemv(ps.n_mtiles, ps.K, B, ps.f16, ps.swiglu);
+    mx = std::max(mx, (size_t)((ps.n_mtiles + p.mpc - 1) / p.mpc));
+  }
   return mx;
 }
 
-// Decode-phase activation tensors at max_batch with their op lifetimes:
-// op 0 step begin, then per layer 1 QKV, 2 RoPE+append, 3 attention, 4 O,
-// 5 gate-up, 6 down (the one per-layer plan is reused by every layer), 7 output.
+// Decode-phase activation tensors at max_batch with their op lifetimes: op 0
+// step begin; per layer 1 QKV, 2 attention, 3 O, 4 gate-up, 5 down (one plan,
+// reused by every layer); 6 LM head.
 void build_decode_plan(mag_ctx* c) {
   const int B = c->B_max;
   int S = 0;
@@ -246,16 +259,21 @@ void build_decode_plan(mag_ctx* c) {
   c->attn_split_max = S;  // splits x batch rows, the partial buffers' capacity
   size_t part = 0;
   for (int b = 1; b <= B; ++b) part = std::max(part, gemv_partial_floats(c, b));
+  const int Gd = c->D / 32, Go = c->Hq * c->d / 32, Gf = (c->F + 31) / 32;
   auto T = [](const char* n, uint64_t sz, int f, int l) { return ArenaTensor{n, sz, f, l, 0}; };
   c->plan.clear();
-  c->plan.push_back(T("residual", (uint64_t)B * c->D * 4, 0, 7));
+  c->plan.push_back(T("residual", (uint64_t)B * c->D * 4, 0, 6));
+  c->plan.push_back(T("norm_out", (uint64_t)B * c->D * 2, 0, 6));
+  c->plan.push_back(T("norm_out_sum", (uint64_t)B * Gd * 4, 0, 6));
   c->plan.push_back(T("qkv", (uint64_t)B * c->R * 2, 1, 2));
-  c->plan.push_back(T("q_rot", (uint64_t)B * c->Hq * c->d * 2, 2, 3));
-  c->plan.push_back(T("attn_part_ml", (uint64_t)S * c->Hkv * c->G * 2 * 4, 3, 3));
-  c->plan.push_back(T("attn_part_o", (uint64_t)S * c->Hkv * c->G * c->d * 4, 3, 3));
-  c->plan.push_back(T("attn_out", (uint64_t)B * c->Hq * c->d * 2, 3, 4));
-  c->plan.push_back(T("ffn_act", (uint64_t)B * c->F * 2, 5, 6));
-  if (part) c->plan.push_back(T("gemv_partial", part * 4, 1, 7));
+  c->plan.push_back(T("attn_part_ml", (uint64_t)S * c->Hkv * c->G * 2 * 4, 2, 2));
+  c->plan.push_back(T("attn_part_o", (uint64_t)S * c->Hkv * c->G * c->d * 4, 2, 2));
+  c->plan.push_back(T("attn_out", (uint64_t)B * c->Hq * c->d * 2, 2, 3));
+  c->plan.push_back(T("attn_out_sum", (uint64_t)B * Go * 4, 2, 3));
+  c->plan.push_back(T("sumsq_part", (uint64_t)(c->D / 16) * MAG_MAX_BATCH * 4, 3, 5));
+  c->plan.push_back(T("ffn_act", (uint64_t)B * c->F * 2, 4, 5));
+  c->plan.push_back(T("ffn_act_sum", (uint64_t)B * Gf * 4, 4, 5));
+  if (part) c->plan.push_back(T("gemv_partial", part * 4, 1, 6));
   c->arena_unshared = 0;
   for (auto& t : c->plan) c->arena_unshared += t.size;
   c->arena_bytes = plan_arena(c->plan, 64, (c->cfg.flags & MAG_FLAG_ARENA_NO_REUSE) != 0);
@@ -267,9 +285,9 @@ void* arena_ptr(mag_ctx* c, const char* name) {
   return nullptr;
 }
 
-GemvArgs gemv_args(const mag_ctx* c, const Proj& p, int B, int n_mtiles, bool f16w) {
+GemvArgs gemv_args(const mag_ctx* c, const Proj& p, int B, int n_mtiles, bool f16w, bool swiglu) {
   GemvArgs a = {};
-  GemvPlan pl = plan_gemv(n_mtiles, p.K, B, f16w);
+  GemvPlan pl = plan_gemv(n_mtiles, p.K, B, f16w, swiglu);
   a.w = p.codes;
   a.sm = p.sm;
   a.w_row_bytes = f16w ? (int64_t)p.K * 2 : (int64_t)p.G * 16;
@@ -295,6 +313,8 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
   Launch L0{c->stream, false, n_launch};
   Launch L{c->stream, pdl, n_launch};
   cudaError_t e;
+  const int xm = gemv_xmode(B);
+  const int Gd = c->D / 32, Go = c->Hq * c->d / 32, Gf = (c->F + 31) / 32;
   // every launch goes through MAG_RUN, which brackets it with events when profiling
 #define MAG_RUN(kind, call)                                                   \
   do {                                                                       \
@@ -302,38 +322,34 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
     if ((e = (call)) != cudaSuccess) return e;                               \
     if (prof && (e = prof->end(c->stream, (kind))) != cudaSuccess) return e; \
   } while (0)
-  MAG_RUN(MAG_OP_STEP_BEGIN, launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B));
+  MAG_RUN(MAG_OP_STEP_BEGIN, launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B,
+                                               c->gamma1[0], c->cfg.rms_eps, c->xn, c->xn_sum));
   const PoolGeom pg = pool_geom(c);
   const int S = attn_splits(c, B);
   for (int l = 0; l < c->L; ++l) {
     const Proj* P = &c->proj[(size_t)l * 4];
-    {  // RMSNorm + QKV
-      GemvArgs a = gemv_args(c, P[0], B, c->R / 16, false);
-      a.r = c->r;
-      a.ldr = c->D;
-      a.gamma = c->gamma1[l];
+    {  // QKV (+ RoPE of q and k)
+      GemvArgs a = gemv_args(c, P[0], B, c->R / 16, false, false);
+      a.x = c->xn;
+      a.ldx = c->D;
+      a.xsum = c->xn_sum;
+      a.ldxs = Gd;
       a.out_h = c->qkv;
       a.ldo = c->R;
-      MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, X_NORM, EPI_STORE));
-    }
-    {  // RoPE + KV append
-      RopeAppendArgs a = {};
-      a.qkv = c->qkv;
-      a.q_out = c->qrot;
+      a.head_dim = c->d;
+      a.n_rot_heads = c->Hq + c->Hkv;
       a.rope_cos = c->d_cos;
       a.rope_sin = c->d_sin;
-      a.n_heads = c->Hq;
-      a.n_kv_heads = c->Hkv;
-      a.head_dim = c->d;
-      a.layer = l;
-      a.pool = pg;
-      a.step = c->d_args;
-      MAG_RUN(MAG_OP_ROPE_APPEND, launch_rope_append(L, a, B));
+      MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, xm, EPI_QKV));
     }
-    {  // attention
+    {  // KV append + attention
       AttnArgs a = {};
-      a.q = c->qrot;
+      a.qkv = c->qkv;
+      a.qkv_ld = c->R;
       a.o = c->o;
+      a.ldo = c->Hq * c->d;
+      a.osum = c->o_sum;
+      a.ldos = Go;
       a.n_heads = c->Hq;
       a.n_kv_heads = c->Hkv;
       a.head_dim = c->d;
@@ -346,31 +362,63 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
       a.step = c->d_args;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
-    {  // O projection + residual
-      GemvArgs a = gemv_args(c, P[1], B, c->D / 16, false);
+    {  // O projection + residual, then RMSNorm for the FFN
+      GemvArgs a = gemv_args(c, P[1], B, c->D / 16, false, false);
       a.x = c->o;
       a.ldx = c->Hq * c->d;
-      a.out_r = c->r;
-      a.ldo = c->D;
-      MAG_RUN(MAG_OP_O, launch_gemv(L, a, W_W4, X_F16, EPI_RESID));
-    }
-    {  // RMSNorm + gate-up + SwiGLU
-      GemvArgs a = gemv_args(c, P[2], B, c->F / 8, false);
-      a.swiglu_f = c->F;
+      a.xsum = c->o_sum;
+      a.ldxs = Go;
       a.r = c->r;
       a.ldr = c->D;
+      a.ss_part = c->ss_part;
+      a.tail = TAIL_NORM;
       a.gamma = c->gamma2[l];
+      a.xn = c->xn;
+      a.ldxn = c->D;
+      a.xn_permuted = 1;
+      a.xn_sum = c->xn_sum;
+      a.ldxns = Gd;
+      MAG_RUN(MAG_OP_O, launch_gemv(L, a, W_W4, xm, EPI_RESID));
+    }
+    {  // gate-up + SwiGLU
+      GemvArgs a = gemv_args(c, P[2], B, c->F / 8, false, true);
+      a.swiglu_f = c->F;
+      a.x = c->xn;
+      a.ldx = c->D;
+      a.xsum = c->xn_sum;
+      a.ldxs = Gd;
       a.out_h = c->act;
       a.ldo = c->F;
-      MAG_RUN(MAG_OP_GATE_UP, launch_gemv(L, a, W_W4, X_NORM, EPI_SWIGLU));
+      a.out_sum = c->act_sum;
+      a.ldos = Gf;
+      MAG_RUN(MAG_OP_GATE_UP, launch_gemv(L, a, W_W4, xm, EPI_SWIGLU));
     }
-    {  // down projection + residual
-      GemvArgs a = gemv_args(c, P[3], B, c->D / 16, false);
+    {  // down projection + residual, then the next RMSNorm (or the output)
+      GemvArgs a = gemv_args(c, P[3], B, c->D / 16, false, false);
       a.x = c->act;
       a.ldx = c->F;
-      a.out_r = c->r;
-      a.ldo = c->D;
-      MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, X_F16, EPI_RESID));
+      a.xsum = c->act_sum;
+      a.ldxs = Gf;
+      a.r = c->r;
+      a.ldr = c->D;
+      a.ss_part = c->ss_part;
+      a.xn = c->xn;
+      a.ldxn = c->D;
+      if (l + 1 < c->L) {
+        a.tail = TAIL_NORM;
+        a.gamma = c->gamma1[l + 1];
+        a.xn_permuted = 1;
+        a.xn_sum = c->xn_sum;
+        a.ldxns = Gd;
+      } else if (c->V) {
+        a.tail = TAIL_NORM;  // final norm, natural order for the fp16 LM head
+        a.gamma = c->gamma_f;
+        a.xn_permuted = 0;
+        a.xn_sum = nullptr;
+      } else {
+        a.tail = TAIL_HIDDEN;
+      }
+      MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, xm, EPI_RESID));
     }
   }
   if (c->V) {
@@ -378,14 +426,11 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
     lm.codes = reinterpret_cast<uint8_t*>(c->lm_head);
     lm.N = c->V;
     lm.K = c->D;
-    GemvArgs a = gemv_args(c, lm, B, c->V / 16, true);
-    a.r = c->r;
-    a.ldr = c->D;
-    a.gamma = c->gamma_f;
+    GemvArgs a = gemv_args(c, lm, B, c->V / 16, true, false);
+    a.x = c->xn;
+    a.ldx = c->D;
     a.ldo = c->V;
-    MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, X_NORM, EPI_STORE_OUT));
-  } else {
-    MAG_RUN(MAG_OP_FINAL_HIDDEN, launch_final_hidden(L, c->d_args, c->r, c->D, B));
+    MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, xm, EPI_STORE_OUT));
   }
 #undef MAG_RUN
   return cudaSuccess;
@@ -592,17 +637,22 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     return bail(MAG_ERR_OOM);
   }
   c->r = (float*)arena_ptr(c, "residual");
+  c->xn = (__half*)arena_ptr(c, "norm_out");
+  c->xn_sum = (float*)arena_ptr(c, "norm_out_sum");
   c->qkv = (__half*)arena_ptr(c, "qkv");
-  c->qrot = (__half*)arena_ptr(c, "q_rot");
   c->part_ml = (float*)arena_ptr(c, "attn_part_ml");
   c->part_o = (float*)arena_ptr(c, "attn_part_o");
   c->o = (__half*)arena_ptr(c, "attn_out");
+  c->o_sum = (float*)arena_ptr(c, "attn_out_sum");
+  c->ss_part = (float*)arena_ptr(c, "sumsq_part");
   c->act = (__half*)arena_ptr(c, "ffn_act");
+  c->act_sum = (float*)arena_ptr(c, "ffn_act_sum");
   c->gemv_part = (float*)arena_ptr(c, "gemv_partial");
 
   // ---- counters, step arguments, staging
   size_t nc = 0;
   for (int b = 1; b <= c->B_max; ++b) nc = std::max(nc, gemv_grid_x(c, b));
+  nc += 1;  // one more: the whole-grid counter of the residual projections' tail
   c->n_counters = nc;
   size_t ac = (size_t)c->B_max * c->Hkv;
   size_t stage_out = (size_t)c->B_max * (c->V ? c->V : c->D) * 2;

@@ -24,98 +24,66 @@ namespace mag {
 namespace {
 
 // ---------------------------------------------------------------- store of one (token, head) vector
-// x: the d fp16 values in shared memory; executed by d threads (thread i owns
-// element i; warp w owns elements 32w..32w+31, i.e. one INT4 group). The
-// quantisers take their decisions in fp32 with IEEE division and
-// round-half-even, group minima and maxima in index order, so the stored
-// bytes are fixed by the rule alone.
+// x: the d fp16 values in shared memory. Called by every thread of the block;
+// thread i < d owns element i and warp w < d/32 owns elements 32w..32w+31
+// (one INT4 group). The quantisers take their decisions in fp32 with IEEE
+// division and round-half-even, group minima and maxima in index order, so
+// the stored bytes are fixed by the rule alone.
 __device__ void store_vec(const PoolGeom& P, int layer, int blk, int slot, int head, int which, const __half* x,
                           float* red) {
   const int i = threadIdx.x, lane = i & 31, w = i >> 5, d = P.head_dim;
+  const bool act = i < d;  // whole warps: d % 32 == 0
   uint8_t* data = pool_vec(P, layer, blk, which, head, slot);
-  float xi = __half2float(x[i]);
+  const float xi = act ? __half2float(x[i]) : 0.f;
   if (P.kv_dtype == 0) {
-    reinterpret_cast<__half*>(data)[i] = x[i];
+    if (act) reinterpret_cast<__half*>(data)[i] = x[i];
   } else if (P.kv_dtype == 1) {
-    float a = warp_max(fabsf(xi));
-    if (lane == 0) red[w] = a;
-    __syncthreads();
-    float amax = red[0];
-    for (int j = 1; j < d / 32; ++j) amax = fmaxf(amax, red[j]);
-    __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
-    float s = __half2float(s16);
-    int q = 0;
-    if (s != 0.0f) {
-      q = (int)rintf(__fdiv_rn(xi, s));
-      q = max(-127, min(127, q));
+    if (act) {
+      const float a = warp_max(fabsf(xi));
+      if (lane == 0) red[w] = a;
     }
-    reinterpret_cast<int8_t*>(data)[i] = (int8_t)q;
-    if (i == 0) *reinterpret_cast<__half*>(pool_vec(P, layer, blk, 2 + which, head, slot)) = s16;
+    __syncthreads();
+    if (act) {
+      float amax = red[0];
+      for (int j = 1; j < d / 32; ++j) amax = fmaxf(amax, red[j]);
+      const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+      const float s = __half2float(s16);
+      int q = 0;
+      if (s != 0.0f) {
+        q = (int)rintf(__fdiv_rn(xi, s));
+        q = max(-127, min(127, q));
+      }
+      reinterpret_cast<int8_t*>(data)[i] = (int8_t)q;
+      if (i == 0) *reinterpret_cast<__half*>(pool_vec(P, layer, blk, 2 + which, head, slot)) = s16;
+    }
     __syncthreads();  // red reused by the next call
-  } else {
+  } else if (act) {
     float lo = 0.f, hi = 0.f;
     if (lane == 0) {
       lo = hi = __half2float(x[32 * w]);
       for (int j = 1; j < 32; ++j) {
-        float v = __half2float(x[32 * w + j]);
+        const float v = __half2float(x[32 * w + j]);
         if (v < lo) lo = v;
         if (v > hi) hi = v;
       }
     }
     lo = __shfl_sync(0xffffffffu, lo, 0);
     hi = __shfl_sync(0xffffffffu, hi, 0);
-    __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
-    __half m16 = __float2half_rn(lo);
-    float s = __half2float(s16), m = __half2float(m16);
+    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+    const __half m16 = __float2half_rn(lo);
+    const float s = __half2float(s16), m = __half2float(m16);
     int q = 0;
     if (s != 0.0f) {
       q = (int)rintf(__fdiv_rn(__fsub_rn(xi, m), s));
       q = max(0, min(15, q));
     }
-    int qn = __shfl_down_sync(0xffffffffu, q, 1);
+    const int qn = __shfl_down_sync(0xffffffffu, q, 1);
     if ((lane & 1) == 0) data[i >> 1] = (uint8_t)(q | (qn << 4));
     if (lane == 0) {
       __half2* meta = reinterpret_cast<__half2*>(pool_vec(P, layer, blk, 2 + which, head, slot));
       meta[w] = __halves2half2(s16, m16);
     }
   }
-}
-
-// ---------------------------------------------------------------- RoPE + append (one block per (token, KV head))
-__global__ void rope_append_kernel(const RopeAppendArgs a) {
-  __shared__ __half xk[128], xv[128];
-  __shared__ float red[8];
-  pdl_wait();
-  pdl_trigger();
-  const int b = blockIdx.x, g = blockIdx.y, i = threadIdx.x, d = a.head_dim, half = d / 2;
-  const int G = a.n_heads / a.n_kv_heads;
-  const int pos = a.step->pos[b], sess = a.step->sess[b];
-  const int R = (a.n_heads + 2 * a.n_kv_heads) * d;
-  const __half* row = a.qkv + (int64_t)b * R;
-  const float* cs = a.rope_cos + (int64_t)pos * half;
-  const float* sn = a.rope_sin + (int64_t)pos * half;
-  // query heads of this group: rotate pairs (j, j + d/2)
-  for (int idx = i; idx < G * half; idx += d) {
-    int h = g * G + idx / half, j = idx % half;
-    float x0 = __half2float(row[h * d + j]), x1 = __half2float(row[h * d + j + half]);
-    float c = cs[j], s = sn[j];
-    a.q_out[(int64_t)b * a.n_heads * d + h * d + j] = __float2half_rn(x0 * c - x1 * s);
-    a.q_out[(int64_t)b * a.n_heads * d + h * d + j + half] = __float2half_rn(x0 * s + x1 * c);
-  }
-  // key head g rotated, value head g as is
-  const __half* kr = row + (a.n_heads + g) * d;
-  const __half* vr = row + (a.n_heads + a.n_kv_heads + g) * d;
-  if (i < half) {
-    float x0 = __half2float(kr[i]), x1 = __half2float(kr[i + half]);
-    float c = cs[i], s = sn[i];
-    xk[i] = __float2half_rn(x0 * c - x1 * s);
-    xk[i + half] = __float2half_rn(x0 * s + x1 * c);
-  }
-  xv[i] = vr[i];
-  __syncthreads();
-  const int blk = a.pool.tables[(int64_t)sess * a.pool.table_stride + (pos >> 4)];
-  store_vec(a.pool, a.layer, blk, pos & 15, g, 0, xk, red);
-  store_vec(a.pool, a.layer, blk, pos & 15, g, 1, xv, red);
 }
 
 // ---------------------------------------------------------------- bulk store of given (rotated) K/V
@@ -226,18 +194,38 @@ __device__ __forceinline__ uint32_t pair_tokens(const uint32_t* ra, const uint32
   return __byte_perm(ra[n >> 1], rb[n >> 1], (n & 1) ? 0x7632 : 0x5410);
 }
 
+// 8 codes of a word as exact fp16 integers in (k0,k4) (k1,k5) (k2,k6) (k3,k7) order.
+__device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
+  const __half2 k1024 = __float2half2_rn(1024.0f);
+  const __half2 k1_16 = __float2half2_rn(0.0625f);
+  const __half2 km64 = __float2half2_rn(-64.0f);
+  const uint32_t w2 = w >> 8;
+  uint4 o;
+  o.x = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w, 0x000F000Fu, 0x64006400u)), k1024));
+  o.y = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w, 0x00F000F0u, 0x64006400u)), k1_16, km64));
+  o.z = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w2, 0x000F000Fu, 0x64006400u)), k1024));
+  o.w = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w2, 0x00F000F0u, 0x64006400u)), k1_16, km64));
+  return o;
+}
+
+// position of element e (0..7) of an 8-wide unit in the order the W4 projections read activations
+__device__ __forceinline__ int unit_pos8(int e) { return e < 4 ? 2 * e : 2 * (e - 4) + 1; }
+
 template <int D, int DT>
 __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
-  constexpr int NS = D / 32;  // 32-dim slabs of K
+  constexpr int NS = D / 32;  // 32-dim slabs of K (one INT4 group each)
   constexpr int NV = D / 8;   // V n-tiles
-  constexpr int NW = D / 16;  // words per V row
+  constexpr int NW = D / 16;  // words per V row of a lane
   __shared__ float s_m[4][8], s_l[4][8];
   __shared__ float s_acc[4][8][D];
+  __shared__ __half s_kv[2][D];
+  __shared__ float s_red[8];
+  __shared__ float s_cm[64][8], s_cl[64][8];
   __shared__ int s_last;
 
   const int split = blockIdx.x, gk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, t = lane & 3;
-  const int Hkv = a.n_kv_heads, G = a.n_heads / Hkv;
+  const int Hq = a.n_heads, Hkv = a.n_kv_heads, G = Hq / Hkv;
   pdl_wait();
   pdl_trigger();
   const int pos = a.step->pos[b], sess = a.step->sess[b];
@@ -247,17 +235,42 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   const int bps = (n_blocks + s_eff - 1) / s_eff;
   const int blk0 = split * bps, blk1 = min(blk0 + bps, n_blocks);
   const int32_t* table = a.pool.tables + (int64_t)sess * a.pool.table_stride;
+  const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
   const int64_t pbase = (((int64_t)b * Hkv + gk) * a.n_split + split) * G;
 
+  // the block that holds the new token first appends its K (rotated) and V to the pool
+  if (blk0 <= (pos >> 4) && (pos >> 4) < blk1) {
+    if (tid < D) {
+      s_kv[0][tid] = qkv[(int64_t)(Hq + gk) * D + tid];
+      s_kv[1][tid] = qkv[(int64_t)(Hq + Hkv + gk) * D + tid];
+    }
+    __syncthreads();
+    const int phys = table[pos >> 4];
+    store_vec(a.pool, a.layer, phys, pos & 15, gk, 0, s_kv[0], s_red);
+    store_vec(a.pool, a.layer, phys, pos & 15, gk, 1, s_kv[1], s_red);
+    __threadfence_block();
+    __syncthreads();
+  }
+
   if (blk0 < blk1) {
-    // query fragments (rows = heads of the group, padded to 16 with zeros)
+    // query fragments: rows = the G heads of this KV head, padded to 16 with zeros
     uint32_t qa[2 * NS][2];
+    float qsum[NS];  // INT4: per 32-dim slab, the sum of this row's query values
     const bool hv = gi < G;
-    const __half* qrow = a.q + (int64_t)b * a.n_heads * D + (int64_t)(gk * G + (hv ? gi : 0)) * D;
+    const __half* qrow = qkv + (int64_t)(gk * G + (hv ? gi : 0)) * D;
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
       uint4 v = hv ? *reinterpret_cast<const uint4*>(qrow + 32 * s + 8 * t) : make_uint4(0, 0, 0, 0);
-      if (DT == 2) v = perm_k0k4(v);
+      if (DT == 2) {
+        const __half* h = reinterpret_cast<const __half*>(&v);
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum += __half2float(h[e]);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        qsum[s] = sum;
+        v = perm_k0k4(v);
+      }
       qa[2 * s][0] = v.x;
       qa[2 * s][1] = v.y;
       qa[2 * s + 1][0] = v.z;
@@ -271,28 +284,49 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
 
     for (int blk = blk0 + warp; blk < blk1; blk += 4) {
       const int phys = table[blk];
-      // ---- scores S[head][token] for the block's 16 tokens (two n-tiles of 8)
+      // ---- scores S[head][token] of the block's 16 tokens (two n-tiles of 8)
       float sfr[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
-        const int tok = gi + 8 * nt;
-        const uint8_t* krow = pool_vec(a.pool, a.layer, phys, 0, gk, tok);
-        const uint8_t* kmeta = DT == 2 ? pool_vec(a.pool, a.layer, phys, 2, gk, tok) : nullptr;
+        const uint8_t* krow = pool_vec(a.pool, a.layer, phys, 0, gk, gi + 8 * nt);
+        if (DT == 2) {
+          const uint8_t* kmeta0 = pool_vec(a.pool, a.layer, phys, 2, gk, 8 * nt + 2 * t);
 #pragma unroll
-        for (int s = 0; s < NS; ++s) {
-          uint4 kb = load_k_slab<DT>(a.pool, krow, kmeta, s, t);
-          mma_16816(sfr[nt], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
-          mma_16816(sfr[nt], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
+          for (int s = 0; s < NS; ++s) {
+            const uint4 kq = u4x8_codes(*reinterpret_cast<const uint32_t*>(krow + 16 * s + 4 * t));
+            float as[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(as, qa[2 * s][0], 0u, qa[2 * s][1], 0u, kq.x, kq.y);
+            mma_16816(as, qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kq.z, kq.w);
+            // per (token, group): score += s * (q . codes) + m * sum(q)
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + 4 * s));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + a.pool.meta_bytes + 4 * s));
+            sfr[nt][0] = fmaf(f0.x, as[0], fmaf(f0.y, qsum[s], sfr[nt][0]));
+            sfr[nt][1] = fmaf(f1.x, as[1], fmaf(f1.y, qsum[s], sfr[nt][1]));
+          }
+        } else {
+#pragma unroll
+          for (int s = 0; s < NS; ++s) {
+            uint4 kb;
+            if (DT == 0) {
+              kb = *reinterpret_cast<const uint4*>(krow + (32 * s + 8 * t) * 2);
+            } else {
+              const uint2 w = *reinterpret_cast<const uint2*>(krow + 32 * s + 8 * t);
+              i8x4_to_h2(w.x, kb.x, kb.y);
+              i8x4_to_h2(w.y, kb.z, kb.w);
+            }
+            mma_16816(sfr[nt], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
+            mma_16816(sfr[nt], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
+          }
         }
       }
-      // this lane's tokens: (nt, j) -> 16*blk + 8nt + 2t + j
+      // this lane's tokens: (nt, j) -> 16 blk + 8 nt + 2 t + j
       float ks[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
       if (DT == 1) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          __half2 k2 = *reinterpret_cast<const __half2*>(pool_vec(a.pool, a.layer, phys, 2, gk, 8 * nt + 2 * t));
-          __half2 v2 = *reinterpret_cast<const __half2*>(pool_vec(a.pool, a.layer, phys, 3, gk, 8 * nt + 2 * t));
+          const __half2 k2 = *reinterpret_cast<const __half2*>(pool_vec(a.pool, a.layer, phys, 2, gk, 8 * nt + 2 * t));
+          const __half2 v2 = *reinterpret_cast<const __half2*>(pool_vec(a.pool, a.layer, phys, 3, gk, 8 * nt + 2 * t));
           ks[nt][0] = __low2float(k2);
           ks[nt][1] = __high2float(k2);
           vsc[nt][0] = __low2float(v2);
@@ -304,7 +338,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          int tok = blk * 16 + 8 * nt + 2 * t + j;
+          const int tok = blk * 16 + 8 * nt + 2 * t + j;
           float v = sfr[nt][j] * ks[nt][j] * sc;
           v = tok < n_keys ? v : -INFINITY;
           sfr[nt][j] = v;
@@ -330,9 +364,19 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
         acc[n][0] *= corr;
         acc[n][1] *= corr;
       }
-      // P as the A operand: a0 = tokens (2t, 2t+1), a2 = tokens (8+2t, 9+2t)
-      uint32_t pa0 = h2_as_u32(__floats2half2_rn(p[0][0] * vsc[0][0], p[0][1] * vsc[0][1]));
-      uint32_t pa2 = h2_as_u32(__floats2half2_rn(p[1][0] * vsc[1][0], p[1][1] * vsc[1][1]));
+      // P (times the INT8 value scale) as the A operand, split into fp16 hi + lo so the
+      // product carries no fp16 rounding of the probabilities: a0 = tokens (2t, 2t+1),
+      // a2 = tokens (8+2t, 9+2t)
+      float pv[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) pv[nt][j] = p[nt][j] * vsc[nt][j];
+      const __half2 h0 = __floats2half2_rn(pv[0][0], pv[0][1]), h2 = __floats2half2_rn(pv[1][0], pv[1][1]);
+      const float2 f0 = __half22float2(h0), f2 = __half22float2(h2);
+      const uint32_t pa0 = h2_as_u32(h0), pa2 = h2_as_u32(h2);
+      const uint32_t pl0 = h2_as_u32(__floats2half2_rn(pv[0][0] - f0.x, pv[0][1] - f0.y));
+      const uint32_t pl2 = h2_as_u32(__floats2half2_rn(pv[1][0] - f2.x, pv[1][1] - f2.y));
       // ---- V rows of tokens 2t, 2t+1, 8+2t, 9+2t
       uint32_t v0[NW], v1[NW], v8[NW], v9[NW];
       load_v_row<D, DT>(pool_vec(a.pool, a.layer, phys, 1, gk, 2 * t),
@@ -345,8 +389,9 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
                         DT == 2 ? pool_vec(a.pool, a.layer, phys, 3, gk, 9 + 2 * t) : nullptr, gi, v9);
 #pragma unroll
       for (int n = 0; n < NV; ++n) {
-        uint32_t b0 = pair_tokens(v0, v1, n), b1 = pair_tokens(v8, v9, n);
+        const uint32_t b0 = pair_tokens(v0, v1, n), b1 = pair_tokens(v8, v9, n);
         mma_16816(acc[n], pa0, 0u, pa2, 0u, b0, b1);
+        mma_16816(acc[n], pl0, 0u, pl2, 0u, b0, b1);
       }
     }
     // ---- merge the 4 warps of this block
@@ -373,7 +418,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
       float o = 0.f, l = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        float e = exp2f(s_m[w][h] - mm);  // warps without blocks: m = -inf -> 0
+        const float e = exp2f(s_m[w][h] - mm);  // warps without blocks: m = -inf -> 0
         o += s_acc[w][h][dim] * e;
         l += s_l[w][h] * e;
       }
@@ -387,27 +432,39 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // ---- the last block of this (session, KV head) merges the splits in order
   __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    unsigned prev = atomicAdd(a.counters + (int64_t)b * Hkv + gk, 1u);
-    s_last = prev == (unsigned)(a.n_split - 1);
-  }
+  if (tid == 0) s_last = atomicAdd(a.counters + (int64_t)b * Hkv + gk, 1u) == (unsigned)(a.n_split - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  const int n_valid = (n_blocks + bps - 1) / bps;  // splits that hold blocks
   const int64_t base0 = (((int64_t)b * Hkv + gk) * a.n_split) * G;
+  for (int i = tid; i < n_valid * G; i += blockDim.x) {
+    const int s = i / G, h = i - s * G;
+    s_cm[s][h] = __ldcg(a.part_ml + (base0 + i) * 2);
+    s_cl[s][h] = __ldcg(a.part_ml + (base0 + i) * 2 + 1);
+  }
+  __syncthreads();
+  if (tid < G) {
+    float mm = -INFINITY;
+    for (int s = 0; s < n_valid; ++s) mm = fmaxf(mm, s_cm[s][tid]);
+    float l = 0.f;
+    for (int s = 0; s < n_valid; ++s) l += s_cl[s][tid] * exp2f(s_cm[s][tid] - mm);
+    const float inv = 1.0f / l;
+    for (int s = 0; s < n_valid; ++s) s_cm[s][tid] = exp2f(s_cm[s][tid] - mm) * inv;  // split weights
+  }
+  __syncthreads();
+  // 32 consecutive threads cover 32 consecutive dims of one head: one group of the O projection
   for (int idx = tid; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, dim = idx - h * D;
-    float mm = -INFINITY;
-    for (int s = 0; s < a.n_split && s * bps < n_blocks; ++s)
-      mm = fmaxf(mm, __ldcg(a.part_ml + (base0 + (int64_t)s * G + h) * 2));
-    float o = 0.f, l = 0.f;
-    for (int s = 0; s < a.n_split && s * bps < n_blocks; ++s) {
-      const int64_t pi = base0 + (int64_t)s * G + h;
-      float e = exp2f(__ldcg(a.part_ml + pi * 2) - mm);
-      o += __ldcg(a.part_o + pi * D + dim) * e;
-      l += __ldcg(a.part_ml + pi * 2 + 1) * e;
-    }
-    a.o[(int64_t)b * a.n_heads * D + (int64_t)(gk * G + h) * D + dim] = __float2half_rn(o / l);
+    const float* po = a.part_o + (base0 + h) * D + dim;
+    float o = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < n_valid; ++s) o += __ldcg(po + (int64_t)s * G * D) * s_cm[s][h];
+    const __half oh = __float2half_rn(o);
+    const int e = (gk * G + h) * D + dim;  // element of the [Hq * d] attention output
+    a.o[(int64_t)b * a.ldo + (e & ~7) + unit_pos8(e & 7)] = oh;
+    const float gs = warp_sum(__half2float(oh));
+    if (lane == 0) a.osum[(int64_t)b * a.ldos + e / 32] = gs;
   }
   if (tid == 0) a.counters[(int64_t)b * Hkv + gk] = 0;
 }
@@ -429,10 +486,6 @@ cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, size_t sme
 }
 
 }  // namespace
-
-cudaError_t launch_rope_append(const Launch& L, const RopeAppendArgs& a, int batch) {
-  return launch_ex(L, rope_append_kernel, dim3(batch, a.n_kv_heads), dim3(a.head_dim), 0, a);
-}
 
 cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a) {
   if (a.n_tok == 0) return cudaSuccess;

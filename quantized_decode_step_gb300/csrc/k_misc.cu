@@ -1,4 +1,4 @@
-// Load-time W4 quantiser, step prologue and the no-LM-head output.
+// Load-time W4 quantiser and the decode-step prologue.
 #include "kernels.h"
 
 namespace mag {
@@ -43,26 +43,66 @@ __global__ void quantize_w4g32_kernel(const float* __restrict__ src, int64_t row
   sm[r * groups + g] = __halves2half2(s16, m16);
 }
 
-// Step prologue: write this step's block-table entries and load the fp16
-// hidden inputs into the fp32 residual stream.
+// Step prologue (one block per token): write this step's block-table entries,
+// load the fp16 hidden input into the fp32 residual stream, and RMSNorm it for
+// the first layer's QKV projection ("5. Core modules" 5.1, pre-norm): xn in
+// the W4 activation unit order (x0,x4,x1,x5,x2,x6,x3,x7) plus its 32-value
+// group sums.
 __global__ void step_begin_kernel(const StepArgs* __restrict__ st, float* __restrict__ r, int D,
-                                  int32_t* __restrict__ tables, int table_stride) {
+                                  int32_t* __restrict__ tables, int table_stride, const __half* __restrict__ gamma,
+                                  float eps, __half* __restrict__ xn, float* __restrict__ xn_sum) {
+  __shared__ float s_red[32];
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x;
-  if (b == 0 && threadIdx.x < st->n_upd)
-    tables[(int64_t)st->upd_sess[threadIdx.x] * table_stride + st->upd_idx[threadIdx.x]] = st->upd_blk[threadIdx.x];
-  for (int i = threadIdx.x; i < D; i += blockDim.x)
-    r[(int64_t)b * D + i] = __half2float(st->hidden_in[(int64_t)b * D + i]);
-}
-
-// No LM head: the output is the fp16 hidden state.
-__global__ void final_hidden_kernel(const StepArgs* __restrict__ st, const float* __restrict__ r, int D) {
-  pdl_wait();
-  pdl_trigger();
-  const int b = blockIdx.x;
-  __half* out = reinterpret_cast<__half*>(st->out);
-  for (int i = threadIdx.x; i < D; i += blockDim.x) out[(int64_t)b * D + i] = __float2half_rn(r[(int64_t)b * D + i]);
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (b == 0 && tid < st->n_upd)
+    tables[(int64_t)st->upd_sess[tid] * table_stride + st->upd_idx[tid]] = st->upd_blk[tid];
+  const __half* hin = st->hidden_in + (int64_t)b * D;
+  const int units = D / 8;
+  float ss = 0.f;
+  for (int u = tid; u < units; u += blockDim.x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(hin + 8 * u);
+    const __half* h = reinterpret_cast<const __half*>(&v);
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      f[e] = __half2float(h[e]);
+      ss += f[e] * f[e];
+    }
+    *reinterpret_cast<float4*>(r + (int64_t)b * D + 8 * u) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4*>(r + (int64_t)b * D + 8 * u + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) s_red[warp] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_red[w];
+    s_red[0] = 1.0f / sqrtf(tot / (float)D + eps);
+  }
+  __syncthreads();
+  const float inv = s_red[0];
+  for (int base = 0; base < units; base += blockDim.x) {  // warp-uniform trips: quads share a group
+    const int u = base + tid;
+    float s = 0.f;
+    if (u < units) {
+      const uint4 v = *reinterpret_cast<const uint4*>(hin + 8 * u);
+      const uint4 gg = *reinterpret_cast<const uint4*>(gamma + 8 * u);
+      const __half* h = reinterpret_cast<const __half*>(&v);
+      const __half* gh = reinterpret_cast<const __half*>(&gg);
+      __half o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __half x = __float2half_rn(__half2float(h[e]) * inv * __half2float(gh[e]));
+        o[e < 4 ? 2 * e : 2 * (e - 4) + 1] = x;
+        s += __half2float(x);
+      }
+      *reinterpret_cast<uint4*>(xn + (int64_t)b * D + 8 * u) = *reinterpret_cast<uint4*>(o);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if (u < units && (u & 3) == 0) xn_sum[(int64_t)b * (D / 32) + u / 4] = s;
+  }
 }
 
 template <typename K, typename... Args>
@@ -95,12 +135,10 @@ cudaError_t launch_quantize_w4g32(cudaStream_t s, const float* src, int64_t rows
 }
 
 cudaError_t launch_step_begin(const Launch& L, const StepArgs* step, float* r, int D, int32_t* tables,
-                              int table_stride, int batch) {
-  return launch_plain(L, step_begin_kernel, dim3(batch), dim3(256), step, r, D, tables, table_stride);
-}
-
-cudaError_t launch_final_hidden(const Launch& L, const StepArgs* step, const float* r, int D, int batch) {
-  return launch_plain(L, final_hidden_kernel, dim3(batch), dim3(256), step, r, D);
+                              int table_stride, int batch, const __half* gamma, float eps, __half* xn,
+                              float* xn_sum) {
+  return launch_plain(L, step_begin_kernel, dim3(batch), dim3(256), step, r, D, tables, table_stride, gamma, eps,
+                      xn, xn_sum);
 }
 
 }  // namespace mag

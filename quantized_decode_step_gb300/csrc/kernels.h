@@ -18,58 +18,63 @@ struct Launch {
 
 // ---------------------------------------------------------------- W4 / fp16 GEMV (mma.sync)
 enum WeightFmt { W_W4 = 0, W_F16 = 1 };
-enum XMode { X_F16 = 0, X_NORM = 1 };
-enum Epilogue { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_STORE_OUT = 3 };
+enum XMode { X_DIRECT = 0, X_SMEM = 1 };
+enum Epilogue { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_STORE_OUT = 3 };
+enum Tail { TAIL_NONE = 0, TAIL_NORM = 1, TAIL_HIDDEN = 2 };
 
 struct GemvArgs {
   const uint8_t* w;       // W4 codes [N][w_row_bytes] or fp16 [N][K]
   const __half2* sm;      // W4 (scale, min) pairs [N][sm_row]
   int64_t w_row_bytes;
   int32_t sm_row;         // groups per row (W4)
-  int32_t n_mtiles;       // m-tiles of 16 output rows (SwiGLU: 8 gate + 8 up rows)
-  int32_t swiglu_f;       // SwiGLU: F (up rows start at F)
+  int32_t n_mtiles;       // 16-row tiles (SwiGLU: 8 gate + 8 up rows; QKV: rows i..i+7 and i+d/2.. of a head)
   int32_t K;              // reduction length
   int32_t n_chunks;       // ceil(K / 64)
   int32_t chunks_per_cta; // k-range of one block, in 64-wide chunks
   int32_t ks;             // k-splits (grid.y)
   int32_t mpc;            // m-tiles per block
   int32_t wk;             // warps sharing one m-tile's k-range
-  const __half* x;        // X_F16: [B][ldx]
+  const __half* x;        // activations [B][ldx]: W4 unit order (x0,x4,x1,x5,x2,x6,x3,x7) / natural (fp16 W)
   int32_t ldx;
-  const float* r;         // X_NORM: residual [B][ldr] and gain [K]
-  int32_t ldr;
-  const __half* gamma;
-  float eps;
+  const float* xsum;      // W4: group sums of x [B][ldxs]
+  int32_t ldxs;
   int32_t batch;
-  __half* out_h;          // EPI_STORE / EPI_SWIGLU: [B][ldo]
-  float* out_r;           // EPI_RESID: [B][ldo] (+=)
+  // EPI_QKV
+  int32_t head_dim, n_rot_heads;
+  const float* rope_cos;
+  const float* rope_sin;
+  // EPI_QKV / EPI_SWIGLU: fp16 out [B][ldo]; EPI_SWIGLU group sums [B][ldos]
+  __half* out_h;
   int32_t ldo;
+  int32_t swiglu_f;
+  float* out_sum;
+  int32_t ldos;
+  // EPI_RESID: residual [B][ldr] += y, per-tile sums of squares [n_mtiles][16], tail
+  float* r;
+  int32_t ldr;
+  float* ss_part;
+  int32_t tail;           // Tail
+  const __half* gamma;    // TAIL_NORM gain
+  float eps;
+  __half* xn;             // TAIL_NORM output [B][ldxn]
+  int32_t ldxn;
+  int32_t xn_permuted;    // 1: W4 unit order
+  float* xn_sum;          // group sums of xn (or null) [B][ldxns]
+  int32_t ldxns;
   float* partial;         // ks > 1: [ks][n_mtiles][32][4 * n_tiles]
-  uint32_t* counters;     // ks > 1: [grid.x], zero between launches
-  const StepArgs* step;   // EPI_STORE_OUT: output pointer of the step
+  uint32_t* counters;     // [grid.x + 1], zero between launches
+  const StepArgs* step;
 };
 
-size_t gemv_smem_bytes(const GemvArgs& a, int n_tok_tiles);
+size_t gemv_smem_bytes(const GemvArgs& a, int xmode);
 cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xmode, int epi);
 
 // ---------------------------------------------------------------- step prologue
+// block-table writes, fp16 input -> fp32 residual, RMSNorm of layer 0 into xn (W4 unit order) + group sums
 cudaError_t launch_step_begin(const Launch& L, const StepArgs* step, float* r, int D, int32_t* tables,
-                              int table_stride, int batch);
-cudaError_t launch_final_hidden(const Launch& L, const StepArgs* step, const float* r, int D, int batch);
+                              int table_stride, int batch, const __half* gamma, float eps, __half* xn, float* xn_sum);
 
-// ---------------------------------------------------------------- RoPE + KV append, bulk KV store
-struct RopeAppendArgs {
-  const __half* qkv;  // [B][(Hq+2Hkv)d]
-  __half* q_out;      // [B][Hq d] rotated
-  const float* rope_cos;  // [max_pos][d/2]
-  const float* rope_sin;
-  int32_t n_heads, n_kv_heads, head_dim;
-  int32_t layer;
-  PoolGeom pool;
-  const StepArgs* step;
-};
-cudaError_t launch_rope_append(const Launch& L, const RopeAppendArgs& a, int batch);
-
+// ---------------------------------------------------------------- bulk KV store
 struct KvStoreArgs {
   const __half* k;  // [L][n][Hkv][d]
   const __half* v;
@@ -82,11 +87,15 @@ cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a);
 
 // ---------------------------------------------------------------- split-K flash-decode attention
 struct AttnArgs {
-  const __half* q;  // [B][Hq d] rotated
-  __half* o;        // [B][Hq d]
+  const __half* qkv;  // [B][qkv_ld]: q (rotated) [Hq d], k (rotated) [Hkv d], v [Hkv d]
+  int32_t qkv_ld;
+  __half* o;          // [B][ldo] attention output, W4 unit order
+  int32_t ldo;
+  float* osum;        // [B][ldos] group sums of o (32 dims)
+  int32_t ldos;
   int32_t n_heads, n_kv_heads, head_dim;
   int32_t layer;
-  int32_t n_split;  // grid.x
+  int32_t n_split;  // grid.x (<= 64)
   float* part_ml;   // [B][Hkv][n_split][G][2]
   float* part_o;    // [B][Hkv][n_split][G][d]
   uint32_t* counters;  // [B][Hkv]
