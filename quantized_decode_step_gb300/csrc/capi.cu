@@ -21,10 +21,11 @@ namespace {
 constexpr int kRing = 8;
 
 struct Proj {
-  uint8_t* codes = nullptr;  // [N][16G] followed by (scale, min) [N][G]
-  __half2* sm = nullptr;
+  uint8_t* tiles = nullptr;  // [N/16][ceil(K/64)][640 B]
   int N = 0, K = 0, G = 0;
-  size_t bytes = 0;
+  int map = 0, map_arg = 0;  // tile row map (TileMap) and its argument
+  size_t canon_bytes = 0;    // W4G32 bytes: N * G * 20
+  size_t tile_bytes = 0;
 };
 
 struct Session {
@@ -34,7 +35,7 @@ struct Session {
 };
 
 struct GemvPlan {
-  int mpc, wk, ks, cpc;
+  int streamk_blocks, ks, cpc;
 };
 
 // Event pairs around each launch of an instrumented (eager) step.
@@ -100,17 +101,14 @@ struct mag_ctx {
   uint64_t arena_bytes = 0, arena_unshared = 0;
   std::vector<ArenaTensor> plan;
   float* r = nullptr;
-  __half* xn = nullptr;
-  float* xn_sum = nullptr;
   __half* qkv = nullptr;
   float* part_ml = nullptr;
   float* part_o = nullptr;
   __half* o = nullptr;
-  float* o_sum = nullptr;
   float* ss_part = nullptr;
   __half* act = nullptr;
-  float* act_sum = nullptr;
   float* gemv_part = nullptr;
+  int sk_blocks[5][5] = {};  // Stream-K blocks per projection kind (QKV, O, GU, DOWN, LM) and batch 1..4
   int attn_split_max = 0;
 
   // counters (zero between launches) and step arguments
@@ -152,32 +150,24 @@ mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...) {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-int proj_index(int tensor) { return tensor; }  // QKV=0, O=1, GU=2, DOWN=3
+// Launch shape of one projection at batch B: up to 4 tokens a Stream-K grid
+// of sk_blocks (the GPU filled to its occupancy, activations for the whole K
+// staged per block); above that a k-split grid whose staged activation slice
+// fits in 64 KB of shared memory.
+constexpr int kStreamKMaxBatch = 4;
 
-// Launch shape of one projection at batch B. Up to 4 tokens the activations
-// are read straight from global memory (L1/L2 resident); above that they are
-// staged in shared memory per block, which then covers 8 tiles, and the
-// k-range is split so the staged slice fits in 64 KB.
-int gemv_xmode(int B) { return B <= 4 ? X_DIRECT : X_SMEM; }
-
-GemvPlan plan_gemv(int n_mtiles, int K, int B, bool f16w, bool swiglu) {
+GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
   GemvPlan p;
   const int n_chunks = (K + 63) / 64;
-  if (gemv_xmode(B) == X_DIRECT) {
-    if (f16w || swiglu || n_mtiles >= 1024) {
-      p.mpc = 4;
-      p.wk = 2;
-    } else {
-      p.mpc = 1;
-      p.wk = 8;
-    }
+  if (B <= kStreamKMaxBatch) {
+    p.streamk_blocks = c->sk_blocks[kind][B];
     p.ks = 1;
     p.cpc = n_chunks;
     return p;
   }
-  p.mpc = 8;
-  p.wk = 1;
-  const int max_cpc = std::max(1, (64 * 1024) / (B * 128) - 1);
+  (void)n_mtiles;
+  p.streamk_blocks = 0;
+  const int max_cpc = std::max(1, (64 * 1024) / (B * 136) - 1);
   p.ks = (n_chunks + max_cpc - 1) / max_cpc;
   p.cpc = (n_chunks + p.ks - 1) / p.ks;
   return p;
@@ -215,38 +205,51 @@ bool all_loaded(const mag_ctx* c) {
   return true;
 }
 
-// The decode step's projections: (m-tiles, K, fp16 weights, SwiGLU)
+// The decode step's projections: kind (0 QKV, 1 O, 2 gate-up, 3 down, 4 LM head), tiles, K, launch variant
 struct ProjShape {
-  int n_mtiles, K;
-  bool f16, swiglu;
+  int kind, n_mtiles, K, wfmt, xsrc, epi;
 };
 std::vector<ProjShape> proj_shapes(const mag_ctx* c) {
-  std::vector<ProjShape> v = {{c->R / 16, c->D, false, false},
-                              {c->D / 16, c->Hq * c->d, false, false},
-                              {c->F / 8, c->D, false, true},
-                              {c->D / 16, c->F, false, false}};
-  if (c->V) v.push_back({c->V / 16, c->D, true, false});
+  std::vector<ProjShape> v = {{0, c->R / 16, c->D, W_W4, XSRC_RESID, EPI_QKV},
+                              {1, c->D / 16, c->Hq * c->d, W_W4, XSRC_F16, EPI_RESID},
+                              {2, c->F / 8, c->D, W_W4, XSRC_RESID, EPI_SWIGLU},
+                              {3, c->D / 16, c->F, W_W4, XSRC_F16, EPI_RESID}};
+  if (c->V) v.push_back({4, c->V / 16, c->D, W_F16, XSRC_RESID, EPI_STORE_OUT});
   return v;
 }
 
-// Floats of the k-split partial buffer for batch B.
+// Floats of the partial-sum buffer for batch B (Stream-K parts or k-split slices).
 size_t gemv_partial_floats(const mag_ctx* c, int B) {
   size_t mx = 0;
   const int nt = B > 8 ? 2 : 1;
   for (auto& ps : proj_shapes(c)) {
-    GemvPlan p = plan_gemv(ps.n_mtiles, ps.K, B, ps.f16, ps.swiglu);
-    if (p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
+    GemvPlan p = plan_gemv(c, ps.kind, ps.n_mtiles, ps.K, B);
+    if (p.streamk_blocks > 0) mx = std::max(mx, (size_t)p.streamk_blocks * 8 * 2 * 32 * 4);
+    else if (p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
   }
   return mx;
 }
 
-size_t gemv_grid_x(const mag_ctx* c, int B) {
-  size_t mx = 0;
-  for (auto& ps : proj_shapes(c)) {
-    GemvPlan p = plan_gemv(ps.n_mtiles, ps.K, B, ps.f16, ps.swiglu);
-    mx = std::max(mx, (size_t)((ps.n_mtiles + p.mpc - 1) / p.mpc));
-  }
+// Counter slots: one per tile (Stream-K) or per block column (k-split).
+size_t gemv_counters(const mag_ctx* c) {
+  size_t mx = 1;
+  for (auto& ps : proj_shapes(c)) mx = std::max(mx, (size_t)ps.n_mtiles);
   return mx;
+}
+
+// Stream-K grid per projection kind and batch: SMs x resident blocks.
+void plan_streamk(mag_ctx* c) {
+  for (auto& ps : proj_shapes(c))
+    for (int B = 1; B <= std::min(kStreamKMaxBatch, c->B_max); ++B) {
+      GemvArgs a = {};
+      a.batch = B;
+      a.n_chunks = (ps.K + 63) / 64;
+      a.streamk_blocks = 1;
+      const size_t smem = gemv_smem_bytes(a);
+      const int per_sm = std::max(1, gemv_blocks_per_sm(ps.wfmt, ps.xsrc, ps.epi, smem));
+      const int tiles_chunks = ps.n_mtiles * a.n_chunks;
+      c->sk_blocks[ps.kind][B] = std::max(1, std::min(c->n_sm * per_sm, (tiles_chunks + 7) / 8));
+    }
 }
 
 // Decode-phase activation tensors at max_batch with their op lifetimes: op 0
@@ -259,20 +262,15 @@ void build_decode_plan(mag_ctx* c) {
   c->attn_split_max = S;  // splits x batch rows, the partial buffers' capacity
   size_t part = 0;
   for (int b = 1; b <= B; ++b) part = std::max(part, gemv_partial_floats(c, b));
-  const int Gd = c->D / 32, Go = c->Hq * c->d / 32, Gf = (c->F + 31) / 32;
   auto T = [](const char* n, uint64_t sz, int f, int l) { return ArenaTensor{n, sz, f, l, 0}; };
   c->plan.clear();
   c->plan.push_back(T("residual", (uint64_t)B * c->D * 4, 0, 6));
-  c->plan.push_back(T("norm_out", (uint64_t)B * c->D * 2, 0, 6));
-  c->plan.push_back(T("norm_out_sum", (uint64_t)B * Gd * 4, 0, 6));
+  c->plan.push_back(T("sumsq_part", (uint64_t)(c->D / 16) * MAG_MAX_BATCH * 4, 0, 6));
   c->plan.push_back(T("qkv", (uint64_t)B * c->R * 2, 1, 2));
   c->plan.push_back(T("attn_part_ml", (uint64_t)S * c->Hkv * c->G * 2 * 4, 2, 2));
   c->plan.push_back(T("attn_part_o", (uint64_t)S * c->Hkv * c->G * c->d * 4, 2, 2));
   c->plan.push_back(T("attn_out", (uint64_t)B * c->Hq * c->d * 2, 2, 3));
-  c->plan.push_back(T("attn_out_sum", (uint64_t)B * Go * 4, 2, 3));
-  c->plan.push_back(T("sumsq_part", (uint64_t)(c->D / 16) * MAG_MAX_BATCH * 4, 3, 5));
   c->plan.push_back(T("ffn_act", (uint64_t)B * c->F * 2, 4, 5));
-  c->plan.push_back(T("ffn_act_sum", (uint64_t)B * Gf * 4, 4, 5));
   if (part) c->plan.push_back(T("gemv_partial", part * 4, 1, 6));
   c->arena_unshared = 0;
   for (auto& t : c->plan) c->arena_unshared += t.size;
@@ -285,22 +283,23 @@ void* arena_ptr(mag_ctx* c, const char* name) {
   return nullptr;
 }
 
-GemvArgs gemv_args(const mag_ctx* c, const Proj& p, int B, int n_mtiles, bool f16w, bool swiglu) {
+GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, int K, int B) {
   GemvArgs a = {};
-  GemvPlan pl = plan_gemv(n_mtiles, p.K, B, f16w, swiglu);
-  a.w = p.codes;
-  a.sm = p.sm;
-  a.w_row_bytes = f16w ? (int64_t)p.K * 2 : (int64_t)p.G * 16;
-  a.sm_row = p.G;
+  GemvPlan pl = plan_gemv(c, kind, n_mtiles, K, B);
+  a.w = w;
+  a.w_row_bytes = (int64_t)K * 2;
   a.n_mtiles = n_mtiles;
-  a.K = p.K;
-  a.n_chunks = (p.K + 63) / 64;
+  a.K = K;
+  a.n_chunks = (K + 63) / 64;
+  a.streamk_blocks = pl.streamk_blocks;
   a.chunks_per_cta = pl.cpc;
   a.ks = pl.ks;
-  a.mpc = pl.mpc;
-  a.wk = pl.wk;
   a.batch = B;
   a.eps = c->cfg.rms_eps;
+  a.r = c->r;
+  a.ldr = c->D;
+  a.ss_part = c->ss_part;
+  a.n_ss = c->D / 16;
   a.partial = c->gemv_part;
   a.counters = c->d_counters;
   a.step = c->d_args;
@@ -313,8 +312,6 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
   Launch L0{c->stream, false, n_launch};
   Launch L{c->stream, pdl, n_launch};
   cudaError_t e;
-  const int xm = gemv_xmode(B);
-  const int Gd = c->D / 32, Go = c->Hq * c->d / 32, Gf = (c->F + 31) / 32;
   // every launch goes through MAG_RUN, which brackets it with events when profiling
 #define MAG_RUN(kind, call)                                                   \
   do {                                                                       \
@@ -322,25 +319,23 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
     if ((e = (call)) != cudaSuccess) return e;                               \
     if (prof && (e = prof->end(c->stream, (kind))) != cudaSuccess) return e; \
   } while (0)
-  MAG_RUN(MAG_OP_STEP_BEGIN, launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B,
-                                               c->gamma1[0], c->cfg.rms_eps, c->xn, c->xn_sum));
+  MAG_RUN(MAG_OP_STEP_BEGIN,
+          launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B, c->ss_part));
   const PoolGeom pg = pool_geom(c);
   const int S = attn_splits(c, B);
   for (int l = 0; l < c->L; ++l) {
     const Proj* P = &c->proj[(size_t)l * 4];
-    {  // QKV (+ RoPE of q and k)
-      GemvArgs a = gemv_args(c, P[0], B, c->R / 16, false, false);
-      a.x = c->xn;
-      a.ldx = c->D;
-      a.xsum = c->xn_sum;
-      a.ldxs = Gd;
+    {  // RMSNorm + QKV + RoPE of q and k
+      GemvArgs a = gemv_args(c, 0, P[0].tiles, c->R / 16, c->D, B);
+      a.n_ss = l == 0 ? 1 : c->D / 16;  // the step prologue leaves one sum per token
+      a.gamma = c->gamma1[l];
       a.out_h = c->qkv;
       a.ldo = c->R;
       a.head_dim = c->d;
       a.n_rot_heads = c->Hq + c->Hkv;
       a.rope_cos = c->d_cos;
       a.rope_sin = c->d_sin;
-      MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, xm, EPI_QKV));
+      MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, XSRC_RESID, EPI_QKV));
     }
     {  // KV append + attention
       AttnArgs a = {};
@@ -348,8 +343,6 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
       a.qkv_ld = c->R;
       a.o = c->o;
       a.ldo = c->Hq * c->d;
-      a.osum = c->o_sum;
-      a.ldos = Go;
       a.n_heads = c->Hq;
       a.n_kv_heads = c->Hkv;
       a.head_dim = c->d;
@@ -362,75 +355,33 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
       a.step = c->d_args;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
-    {  // O projection + residual, then RMSNorm for the FFN
-      GemvArgs a = gemv_args(c, P[1], B, c->D / 16, false, false);
+    {  // O projection + residual
+      GemvArgs a = gemv_args(c, 1, P[1].tiles, c->D / 16, c->Hq * c->d, B);
       a.x = c->o;
       a.ldx = c->Hq * c->d;
-      a.xsum = c->o_sum;
-      a.ldxs = Go;
-      a.r = c->r;
-      a.ldr = c->D;
-      a.ss_part = c->ss_part;
-      a.tail = TAIL_NORM;
-      a.gamma = c->gamma2[l];
-      a.xn = c->xn;
-      a.ldxn = c->D;
-      a.xn_permuted = 1;
-      a.xn_sum = c->xn_sum;
-      a.ldxns = Gd;
-      MAG_RUN(MAG_OP_O, launch_gemv(L, a, W_W4, xm, EPI_RESID));
+      MAG_RUN(MAG_OP_O, launch_gemv(L, a, W_W4, XSRC_F16, EPI_RESID));
     }
-    {  // gate-up + SwiGLU
-      GemvArgs a = gemv_args(c, P[2], B, c->F / 8, false, true);
-      a.swiglu_f = c->F;
-      a.x = c->xn;
-      a.ldx = c->D;
-      a.xsum = c->xn_sum;
-      a.ldxs = Gd;
+    {  // RMSNorm + gate-up + SwiGLU
+      GemvArgs a = gemv_args(c, 2, P[2].tiles, c->F / 8, c->D, B);
+      a.gamma = c->gamma2[l];
       a.out_h = c->act;
       a.ldo = c->F;
-      a.out_sum = c->act_sum;
-      a.ldos = Gf;
-      MAG_RUN(MAG_OP_GATE_UP, launch_gemv(L, a, W_W4, xm, EPI_SWIGLU));
+      MAG_RUN(MAG_OP_GATE_UP, launch_gemv(L, a, W_W4, XSRC_RESID, EPI_SWIGLU));
     }
-    {  // down projection + residual, then the next RMSNorm (or the output)
-      GemvArgs a = gemv_args(c, P[3], B, c->D / 16, false, false);
+    {  // down projection + residual
+      GemvArgs a = gemv_args(c, 3, P[3].tiles, c->D / 16, c->F, B);
       a.x = c->act;
       a.ldx = c->F;
-      a.xsum = c->act_sum;
-      a.ldxs = Gf;
-      a.r = c->r;
-      a.ldr = c->D;
-      a.ss_part = c->ss_part;
-      a.xn = c->xn;
-      a.ldxn = c->D;
-      if (l + 1 < c->L) {
-        a.tail = TAIL_NORM;
-        a.gamma = c->gamma1[l + 1];
-        a.xn_permuted = 1;
-        a.xn_sum = c->xn_sum;
-        a.ldxns = Gd;
-      } else if (c->V) {
-        a.tail = TAIL_NORM;  // final norm, natural order for the fp16 LM head
-        a.gamma = c->gamma_f;
-        a.xn_permuted = 0;
-        a.xn_sum = nullptr;
-      } else {
-        a.tail = TAIL_HIDDEN;
-      }
-      MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, xm, EPI_RESID));
+      MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, XSRC_F16, EPI_RESID));
     }
   }
-  if (c->V) {
-    Proj lm;
-    lm.codes = reinterpret_cast<uint8_t*>(c->lm_head);
-    lm.N = c->V;
-    lm.K = c->D;
-    GemvArgs a = gemv_args(c, lm, B, c->V / 16, true, false);
-    a.x = c->xn;
-    a.ldx = c->D;
+  if (c->V) {  // final RMSNorm + LM head
+    GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, c->D, B);
+    a.gamma = c->gamma_f;
     a.ldo = c->V;
-    MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, xm, EPI_STORE_OUT));
+    MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, XSRC_RESID, EPI_STORE_OUT));
+  } else {
+    MAG_RUN(MAG_OP_LM_HEAD, launch_final_hidden(L, c->d_args, c->r, c->D, B));
   }
 #undef MAG_RUN
   return cudaSuccess;
@@ -550,20 +501,24 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   c->sessions.resize(cfg->max_sessions);
   c->loaded.assign((size_t)c->L * 6 + 2, 0);
 
-  // ---- weights region
+  // ---- weights region: W4 projections as 640-byte tiles, fp16 gains, fp16 LM head
   size_t off = 0;
   c->proj.resize((size_t)c->L * 4);
   std::vector<size_t> offs;
   const int shapes[4][2] = {{c->R, c->D}, {c->D, c->Hq * c->d}, {2 * c->F, c->D}, {c->D, c->F}};
+  const int maps[4][2] = {{MAP_QKV, c->d}, {MAP_PLAIN, 0}, {MAP_SWIGLU, c->F}, {MAP_PLAIN, 0}};
   for (int l = 0; l < c->L; ++l)
     for (int i = 0; i < 4; ++i) {
       Proj& p = c->proj[(size_t)l * 4 + i];
       p.N = shapes[i][0];
       p.K = shapes[i][1];
       p.G = (p.K + 31) / 32;
-      p.bytes = (size_t)p.N * p.G * 16 + (size_t)p.N * p.G * 4;
+      p.map = maps[i][0];
+      p.map_arg = maps[i][1];
+      p.canon_bytes = (size_t)p.N * p.G * 20;
+      p.tile_bytes = (size_t)(p.N / 16) * ((p.K + 63) / 64) * kTileBytes;
       offs.push_back(off);
-      off = align256(off + p.bytes);
+      off = align256(off + p.tile_bytes);
     }
   std::vector<size_t> goffs;
   for (int l = 0; l < c->L; ++l)
@@ -580,11 +535,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     fail(c, MAG_ERR_OOM, "weights: cudaMalloc(%zu): %s", c->wbytes, cudaGetErrorString(e));
     return bail(MAG_ERR_OOM);
   }
-  for (size_t i = 0; i < c->proj.size(); ++i) {
-    Proj& p = c->proj[i];
-    p.codes = c->wbase + offs[i];
-    p.sm = reinterpret_cast<__half2*>(p.codes + (size_t)p.N * p.G * 16);
-  }
+  for (size_t i = 0; i < c->proj.size(); ++i) c->proj[i].tiles = c->wbase + offs[i];
   for (int l = 0; l < c->L; ++l) {
     c->gamma1.push_back(reinterpret_cast<__half*>(c->wbase + goffs[2 * l]));
     c->gamma2.push_back(reinterpret_cast<__half*>(c->wbase + goffs[2 * l + 1]));
@@ -630,29 +581,24 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     c->other_bytes += 2 * bytes + tb;
   }
 
-  // ---- arena
+  // ---- launch plans and arena
+  plan_streamk(c);
   build_decode_plan(c);
   if ((e = cudaMalloc(&c->arena, std::max<uint64_t>(c->arena_bytes, 256))) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "arena: %s", cudaGetErrorString(e));
     return bail(MAG_ERR_OOM);
   }
   c->r = (float*)arena_ptr(c, "residual");
-  c->xn = (__half*)arena_ptr(c, "norm_out");
-  c->xn_sum = (float*)arena_ptr(c, "norm_out_sum");
+  c->ss_part = (float*)arena_ptr(c, "sumsq_part");
   c->qkv = (__half*)arena_ptr(c, "qkv");
   c->part_ml = (float*)arena_ptr(c, "attn_part_ml");
   c->part_o = (float*)arena_ptr(c, "attn_part_o");
   c->o = (__half*)arena_ptr(c, "attn_out");
-  c->o_sum = (float*)arena_ptr(c, "attn_out_sum");
-  c->ss_part = (float*)arena_ptr(c, "sumsq_part");
   c->act = (__half*)arena_ptr(c, "ffn_act");
-  c->act_sum = (float*)arena_ptr(c, "ffn_act_sum");
   c->gemv_part = (float*)arena_ptr(c, "gemv_partial");
 
   // ---- counters, step arguments, staging
-  size_t nc = 0;
-  for (int b = 1; b <= c->B_max; ++b) nc = std::max(nc, gemv_grid_x(c, b));
-  nc += 1;  // one more: the whole-grid counter of the residual projections' tail
+  size_t nc = gemv_counters(c);
   c->n_counters = nc;
   size_t ac = (size_t)c->B_max * c->Hkv;
   size_t stage_out = (size_t)c->B_max * (c->V ? c->V : c->D) * 2;
@@ -701,15 +647,24 @@ mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const voi
   if (per_layer && (layer < 0 || layer >= c->L))
     return fail(c, MAG_ERR_INVALID_ARG, "load_weights: bad layer %d", layer);
   if (tensor <= MAG_W_DOWN) {
-    Proj& p = c->proj[(size_t)layer * 4 + proj_index(tensor)];
+    Proj& p = c->proj[(size_t)layer * 4 + tensor];
     if (fmt == MAG_FMT_F32_DENSE) {
       if (bytes != (size_t)p.N * p.K * 4)
         return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected fp32 [%d, %d]", bytes, p.N, p.K);
-      CUDA_TRY(c, launch_quantize_w4g32(c->stream, (const float*)src, p.N, p.K, p.codes, p.sm));
+      // quantise into a stream-ordered scratch copy in W4G32 bytes, then tile it
+      uint8_t* canon = nullptr;
+      CUDA_TRY(c, cudaMallocAsync(reinterpret_cast<void**>(&canon), p.canon_bytes, c->stream));
+      cudaError_t e1 = launch_quantize_w4g32(c->stream, (const float*)src, p.N, p.K, canon,
+                                             reinterpret_cast<__half2*>(canon + (size_t)p.N * p.G * 16));
+      cudaError_t e2 = e1 == cudaSuccess ? launch_w4_to_tiles(c->stream, canon, p.N, p.K, p.map, p.map_arg, p.tiles)
+                                         : e1;
+      cudaError_t e3 = cudaFreeAsync(canon, c->stream);
+      if (e2 != cudaSuccess || e3 != cudaSuccess)
+        return fail(c, MAG_ERR_CUDA, "load_weights: %s", cudaGetErrorString(e2 != cudaSuccess ? e2 : e3));
     } else if (fmt == MAG_FMT_W4G32) {
-      if (bytes != p.bytes)
-        return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected W4G32 %zu", bytes, p.bytes);
-      CUDA_TRY(c, cudaMemcpyAsync(p.codes, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+      if (bytes != p.canon_bytes)
+        return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected W4G32 %zu", bytes, p.canon_bytes);
+      CUDA_TRY(c, launch_w4_to_tiles(c->stream, (const uint8_t*)src, p.N, p.K, p.map, p.map_arg, p.tiles));
     } else {
       return fail(c, MAG_ERR_INVALID_ARG, "load_weights: projections take FP32_DENSE or W4G32");
     }
@@ -960,8 +915,9 @@ mag_status mag_debug_read_weights(mag_ctx* c, int32_t tensor, int32_t layer, voi
   if (tensor < MAG_W_QKV || tensor > MAG_W_DOWN || layer < 0 || layer >= c->L)
     return fail(c, MAG_ERR_INVALID_ARG, "debug_read_weights: projections only");
   Proj& p = c->proj[(size_t)layer * 4 + tensor];
-  if (bytes != p.bytes) return fail(c, MAG_ERR_INVALID_ARG, "debug_read_weights: expected %zu bytes", p.bytes);
-  CUDA_TRY(c, cudaMemcpyAsync(dst, p.codes, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  if (bytes != p.canon_bytes)
+    return fail(c, MAG_ERR_INVALID_ARG, "debug_read_weights: expected %zu bytes", p.canon_bytes);
+  CUDA_TRY(c, launch_w4_from_tiles(c->stream, p.tiles, p.N, p.K, p.map, p.map_arg, (uint8_t*)dst));
   return MAG_OK;
 }
 

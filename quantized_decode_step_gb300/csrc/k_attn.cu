@@ -208,9 +208,6 @@ __device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
   return o;
 }
 
-// position of element e (0..7) of an 8-wide unit in the order the W4 projections read activations
-__device__ __forceinline__ int unit_pos8(int e) { return e < 4 ? 2 * e : 2 * (e - 4) + 1; }
-
 template <int D, int DT>
 __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   constexpr int NS = D / 32;  // 32-dim slabs of K (one INT4 group each)
@@ -453,18 +450,13 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     for (int s = 0; s < n_valid; ++s) s_cm[s][tid] = exp2f(s_cm[s][tid] - mm) * inv;  // split weights
   }
   __syncthreads();
-  // 32 consecutive threads cover 32 consecutive dims of one head: one group of the O projection
   for (int idx = tid; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, dim = idx - h * D;
     const float* po = a.part_o + (base0 + h) * D + dim;
     float o = 0.f;
 #pragma unroll 8
     for (int s = 0; s < n_valid; ++s) o += __ldcg(po + (int64_t)s * G * D) * s_cm[s][h];
-    const __half oh = __float2half_rn(o);
-    const int e = (gk * G + h) * D + dim;  // element of the [Hq * d] attention output
-    a.o[(int64_t)b * a.ldo + (e & ~7) + unit_pos8(e & 7)] = oh;
-    const float gs = warp_sum(__half2float(oh));
-    if (lane == 0) a.osum[(int64_t)b * a.ldos + e / 32] = gs;
+    a.o[(int64_t)b * a.ldo + (int64_t)(gk * G + h) * D + dim] = __float2half_rn(o);
   }
   if (tid == 0) a.counters[(int64_t)b * Hkv + gk] = 0;
 }

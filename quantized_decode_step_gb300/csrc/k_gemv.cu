@@ -1,32 +1,39 @@
 // W4A16 (and fp16) matrix-vector products of the decode step on mma.sync.
 //
 // y[b][n] = sum_k deq(W)[n][k] x[b][k] for a handful of tokens b, with the
-// weights streamed once from HBM in the packed 4-bit group-32 layout the
-// library takes at load time ("5. Core modules" 5.1: 4-bit weights, FP16
-// activations). No repacking. Per 64-wide k-chunk a lane reads, for rows g
-// and g+8 of its 16-row tile, one 32-bit word of each of the chunk's two
-// groups, turns its 8 nibbles into exact small integers in fp16 with a LOP3
-// into the mantissa of 1024 (the int4-to-fp16 conversion of Kim et al., "Who
-// Says Elephants Can't Run", 2022) and feeds m16n8k16 tensor-core MMAs with
-// fp32 accumulators, one fresh accumulator per group. Scale and min are
-// applied per group in fp32:
+// weights streamed once from HBM ("5. Core modules" 5.1: 4-bit weights, FP16
+// activations). At load time each projection is repacked into 640-byte tiles
+// (16 rows x 64 k: 512 bytes of codes in lane order, then 128 bytes of fp16
+// (scale, min) pairs), so a warp's per-chunk loads are two fully coalesced
+// 128-bit loads per lane. A lane turns its 8-nibble words into exact small
+// integers in fp16 with a LOP3 into the mantissa of 1024 (the int4-to-fp16
+// conversion of Kim et al., "Who Says Elephants Can't Run", 2022) and feeds
+// m16n8k16 tensor-core MMAs with fp32 accumulators, one fresh accumulator per
+// 32-wide group; scale and min are applied per group in fp32:
 //     sum_k (s q_k + m) x_k = s * sum_k q_k x_k + m * X_g,   X_g = sum_{k in g} x_k,
-// so the result carries no rounding of the dequantised weights; the group
-// sums X_g come with the activations from their producer. The activations are
-// stored in 8-wide units in the order (x0,x4,x1,x5,x2,x6,x3,x7), which is the
-// k order the nibble pairs come out in, so a lane's B fragments for one group
-// are one 128-bit load.
+// so the product carries no rounding of the dequantised weights.
 //
-// Epilogues fused around the product:
-//   QKV      fp16 q/k/v, q and k rotated (RoPE, pre-generated table) -- the
-//            tile's rows g and g+8 are the pair (i, i + d/2) of one head;
-//   RESID    fp32 residual add, per-tile sums of squares, and in the last
-//            block to finish the RMSNorm of the new residual for the next
-//            projection (or the fp16 hidden-state output);
-//   SWIGLU   silu(gate) * up of interleaved gate/up rows, with group sums;
-//   OUT      fp16 logits into the caller's buffer.
-// Weight loads for the first chunks are issued before the programmatic-
-// dependent-launch wait, so they overlap the previous kernel's tail.
+// The activations are staged once per block in shared memory, in 8-wide
+// units ordered (x0,x4,x1,x5,x2,x6,x3,x7) -- the k order the nibble pairs come
+// out in -- together with their group sums X_g. For the projections that
+// follow an RMSNorm ("5. Core modules" 5.1, pre-norm) the staging computes the
+// norm itself from the fp32 residual and the producer's per-tile sums of
+// squares.
+//
+// Schedules:
+//   Stream-K (up to 4 tokens): the (tile, chunk) pairs of the whole matrix are
+//   cut into equal contiguous runs, one per warp of a grid sized to the GPU; a
+//   tile split between warps is finished by the last of them to arrive, which
+//   adds the parts in warp order (deterministic).
+//   K-split (more tokens): a block owns 8 tiles over a k-range whose
+//   activations fit in shared memory; k-ranges are merged in order by the last
+//   block of the group.
+// Epilogues (per tile, one warp): QKV (fp16, q and k rotated by the
+// pre-generated RoPE table; the tile's rows g and g+8 are the pair (i, i+d/2)
+// of one head), RESID (fp32 residual add + per-tile sums of squares), SWIGLU
+// (silu(gate) * up of interleaved gate/up rows), OUT (fp16 logits into the
+// caller's buffer). Weight loads for the first chunks are issued before the
+// programmatic-dependent-launch wait, so they overlap the previous kernel.
 #include "kernels.h"
 
 namespace mag {
@@ -34,15 +41,15 @@ namespace mag {
 namespace {
 
 constexpr int kStages = 4;
+constexpr int kWarps = 8;  // warps per block
 
 struct W4Stage {
-  uint32_t wg0, wg1, wv0, wv1;  // row g / g+8, group 0 / 1 of the chunk: word t
-  uint2 sg, sv;                 // (scale, min) of groups 0 and 1, rows g and g+8
+  uint4 code;  // row g: group 0 word t, group 1 word t; row g+8: the same
+  uint4 sm;    // (scale, min): row g group 0, group 1; row g+8 group 0, group 1
 };
 struct F16Stage {
   uint4 g0, g1, h0, h1;
 };
-
 template <int WFMT>
 struct StageT;
 template <>
@@ -54,45 +61,21 @@ struct StageT<W_F16> {
   using type = F16Stage;
 };
 
-__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
+__device__ __forceinline__ void load_stage(W4Stage& st, const GemvArgs& a, int mt, int c, int lane) {
+  const uint8_t* tile = a.w + ((int64_t)mt * a.n_chunks + c) * kTileBytes;
+  st.code = ldg_stream_u4(tile + lane * 16);
+  st.sm = ldg_stream_u4(tile + 512 + (lane >> 2) * 16);
 }
 
-__device__ __forceinline__ void load_stage(W4Stage& st, const GemvArgs& a, int row_g, int row_g8, int c, int t) {
-  const uint8_t* pg = a.w + (int64_t)row_g * a.w_row_bytes + c * 32 + t * 4;
-  const uint8_t* pv = a.w + (int64_t)row_g8 * a.w_row_bytes + c * 32 + t * 4;
-  const bool g1 = 2 * c + 1 < a.sm_row;  // the chunk's second group exists
-  st.wg0 = ldg_stream_u32(pg);
-  st.wv0 = ldg_stream_u32(pv);
-  st.wg1 = g1 ? ldg_stream_u32(pg + 16) : 0u;
-  st.wv1 = g1 ? ldg_stream_u32(pv + 16) : 0u;
-  const __half2* sg = a.sm + (int64_t)row_g * a.sm_row + 2 * c;
-  const __half2* sv = a.sm + (int64_t)row_g8 * a.sm_row + 2 * c;
-  if (g1) {
-    st.sg = ldg_nc_u2(sg);
-    st.sv = ldg_nc_u2(sv);
-  } else {
-    st.sg = make_uint2(ldg_nc_u32(sg), 0u);
-    st.sv = make_uint2(ldg_nc_u32(sv), 0u);
-  }
-}
-
-__device__ __forceinline__ void load_stage(F16Stage& st, const GemvArgs& a, int row_g, int row_g8, int c, int t) {
-  int k = c * 64 + t * 16;
+__device__ __forceinline__ void load_stage(F16Stage& st, const GemvArgs& a, int mt, int c, int lane) {
+  const int g = lane >> 2, t = lane & 3, k = c * 64 + t * 16;
   if (k < a.K) {
-    const uint8_t* pg = a.w + (int64_t)row_g * a.w_row_bytes + (int64_t)k * 2;
-    const uint8_t* pg8 = a.w + (int64_t)row_g8 * a.w_row_bytes + (int64_t)k * 2;
+    const uint8_t* pg = a.w + (int64_t)(mt * 16 + g) * a.w_row_bytes + (int64_t)k * 2;
+    const uint8_t* ph = pg + 8 * a.w_row_bytes;
     st.g0 = ldg_stream_u4(pg);
     st.g1 = ldg_stream_u4(pg + 16);
-    st.h0 = ldg_stream_u4(pg8);
-    st.h1 = ldg_stream_u4(pg8 + 16);
+    st.h0 = ldg_stream_u4(ph);
+    st.h1 = ldg_stream_u4(ph + 16);
   } else {
     st.g0 = st.g1 = st.h0 = st.h1 = make_uint4(0, 0, 0, 0);
   }
@@ -107,7 +90,7 @@ __device__ __forceinline__ Q4 codes_word(uint32_t w) {
   const __half2 k1024 = __float2half2_rn(1024.0f);
   const __half2 k1_16 = __float2half2_rn(0.0625f);
   const __half2 km64 = __float2half2_rn(-64.0f);
-  uint32_t w2 = w >> 8;
+  const uint32_t w2 = w >> 8;
   Q4 q;
   q.e0 = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w, 0x000F000Fu, 0x64006400u)), k1024));
   q.e1 = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w, 0x00F000F0u, 0x64006400u)), k1_16, km64));
@@ -116,18 +99,19 @@ __device__ __forceinline__ Q4 codes_word(uint32_t w) {
   return q;
 }
 
-// Activation fragments of one chunk for one 8-token n-tile: W4 -> units 8c+t
-// (group 0) and 8c+4+t (group 1); fp16 weights -> units 8c+2t, 8c+2t+1.
-struct XFrag {
-  uint4 u0, u1;
-  float2 s_lo, s_hi;  // W4: group sums (groups 0, 1) of tokens 2t and 2t+1 of the n-tile
+// Shared-memory staging of one block: B token rows of `xrow` halves (the
+// block's k-range in W4 unit order or natural order) followed by the group
+// sums [B][grow] (W4 only).
+struct Staged {
+  const __half* x;
+  const float* xs;
+  int xrow, grow, c0;  // c0: first chunk of the staged range
 };
 
 // acc += scale * (q . x) + min * X_g for rows g (acc[0..1]) and g + 8 (acc[2..3]).
-__device__ __forceinline__ void gemv_fma_group(float (&acc)[4], const float (&aq)[4], uint32_t sm_g, uint32_t sm_g8,
-                                               float x_lo, float x_hi, bool one_tok) {
+__device__ __forceinline__ void fma_group(float (&acc)[4], const float (&aq)[4], uint32_t sm_g, uint32_t sm_g8,
+                                          float x_lo, float x_hi, bool one_tok) {
   const float2 fg = __half22float2(u32_as_h2(sm_g)), fv = __half22float2(u32_as_h2(sm_g8));
-  // fg = (scale, min) of row g, fv of row g + 8; columns: tokens 2t (lo) and 2t+1 (hi)
   acc[0] = fmaf(fg.x, aq[0], fmaf(fg.y, x_lo, acc[0]));
   acc[2] = fmaf(fv.x, aq[2], fmaf(fv.y, x_lo, acc[2]));
   if (!one_tok) {
@@ -137,231 +121,312 @@ __device__ __forceinline__ void gemv_fma_group(float (&acc)[4], const float (&aq
 }
 
 template <int NT>
-__device__ __forceinline__ void compute_stage(const W4Stage& st, float (&acc)[2][4], const XFrag (&xf)[2],
-                                              bool one_tok) {
+__device__ __forceinline__ void compute_chunk(const W4Stage& st, float (&acc)[2][4], const Staged& S, int B, int c,
+                                              int g, int t) {
+  const int cl = c - S.c0;
 #pragma unroll
   for (int grp = 0; grp < 2; ++grp) {
-    const Q4 qg = codes_word(grp ? st.wg1 : st.wg0);
-    const Q4 qv = codes_word(grp ? st.wv1 : st.wv0);
-    const uint32_t smg = grp ? st.sg.y : st.sg.x, smv = grp ? st.sv.y : st.sv.x;
+    const Q4 qg = codes_word(grp ? st.code.y : st.code.x);
+    const Q4 qv = codes_word(grp ? st.code.w : st.code.z);
+    const uint32_t smg = grp ? st.sm.y : st.sm.x, smv = grp ? st.sm.w : st.sm.z;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const uint4 xb = grp ? xf[nt].u1 : xf[nt].u0;
+      const int tok = g + 8 * nt;
+      uint4 xb = make_uint4(0, 0, 0, 0);
+      if (tok < B) xb = reinterpret_cast<const uint4*>(S.x + (size_t)tok * S.xrow)[8 * cl + 4 * grp + t];
       float aq[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16816(aq, qg.e0, qv.e0, qg.e1, qv.e1, xb.x, xb.y);
       mma_16816(aq, qg.e2, qv.e2, qg.e3, qv.e3, xb.z, xb.w);
-      const float2 xs = grp ? xf[nt].s_hi : xf[nt].s_lo;  // .x token 2t, .y token 2t+1
-      gemv_fma_group(acc[nt], aq, smg, smv, xs.x, xs.y, NT == 1 && one_tok);
+      const int t0 = 8 * nt + 2 * t;  // this lane's C columns: tokens t0, t0 + 1
+      const float xlo = t0 < B ? S.xs[(size_t)t0 * S.grow + 2 * cl + grp] : 0.f;
+      const float xhi = t0 + 1 < B ? S.xs[(size_t)(t0 + 1) * S.grow + 2 * cl + grp] : 0.f;
+      fma_group(acc[nt], aq, smg, smv, xlo, xhi, B == 1);
     }
   }
 }
 
 template <int NT>
-__device__ __forceinline__ void compute_stage(const F16Stage& st, float (&acc)[2][4], const XFrag (&xf)[2], bool) {
+__device__ __forceinline__ void compute_chunk(const F16Stage& st, float (&acc)[2][4], const Staged& S, int B, int c,
+                                              int g, int t) {
+  const int cl = c - S.c0;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    mma_16816(acc[nt], st.g0.x, st.h0.x, st.g0.y, st.h0.y, xf[nt].u0.x, xf[nt].u0.y);
-    mma_16816(acc[nt], st.g0.z, st.h0.z, st.g0.w, st.h0.w, xf[nt].u0.z, xf[nt].u0.w);
-    mma_16816(acc[nt], st.g1.x, st.h1.x, st.g1.y, st.h1.y, xf[nt].u1.x, xf[nt].u1.y);
-    mma_16816(acc[nt], st.g1.z, st.h1.z, st.g1.w, st.h1.w, xf[nt].u1.z, xf[nt].u1.w);
+    const int tok = g + 8 * nt;
+    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+    if (tok < B) {
+      const uint4* p = reinterpret_cast<const uint4*>(S.x + (size_t)tok * S.xrow);
+      x0 = p[8 * cl + 2 * t];
+      x1 = p[8 * cl + 2 * t + 1];
+    }
+    mma_16816(acc[nt], st.g0.x, st.h0.x, st.g0.y, st.h0.y, x0.x, x0.y);
+    mma_16816(acc[nt], st.g0.z, st.h0.z, st.g0.w, st.h0.w, x0.z, x0.w);
+    mma_16816(acc[nt], st.g1.x, st.h1.x, st.g1.y, st.h1.y, x1.x, x1.y);
+    mma_16816(acc[nt], st.g1.z, st.h1.z, st.g1.w, st.h1.w, x1.z, x1.w);
   }
 }
 
 // position of element e (0..7) of a unit in the W4 activation order
 __device__ __forceinline__ int unit_pos(int e) { return e < 4 ? 2 * e : 2 * (e - 4) + 1; }
 
-template <int NT, int WFMT, int XMODE>
-__device__ __forceinline__ void load_x(XFrag (&xf)[2], const GemvArgs& a, const __half* xs_smem, int xrow, int c,
-                                       int c_begin, int g, int t) {
-  const int B = a.batch;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int tok = g + 8 * nt;
-    const int ua = WFMT == W_W4 ? 8 * c + t : 8 * c + 2 * t;
-    const int ub = WFMT == W_W4 ? 8 * c + 4 + t : 8 * c + 2 * t + 1;
-    uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
-    if (tok < B) {
-      if (XMODE == X_SMEM) {
-        const uint4* p = reinterpret_cast<const uint4*>(xs_smem + (size_t)tok * xrow);
-        u0 = p[ua - 8 * c_begin];
-        u1 = p[ub - 8 * c_begin];
-      } else {
-        const uint4* p = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * a.ldx);
-        if (8 * ua < a.K) u0 = __ldg(p + ua);
-        if (8 * ub < a.K) u1 = __ldg(p + ub);
-      }
+// Stage chunks [c0, c1) of the activations into shared memory (and their group
+// sums for W4). XSRC_RESID: xn = fp16(r / sqrt(mean(r^2) + eps) * gamma), the
+// mean from the producer's n_ss partial sums of squares per token.
+template <int WFMT, int XSRC>
+__device__ Staged stage_x(const GemvArgs& a, uint8_t* smem, float* s_inv, int c0, int c1) {
+  const int tid = threadIdx.x, B = a.batch;
+  Staged S;
+  S.c0 = c0;
+  S.xrow = (c1 - c0) * 64 + 8;
+  S.grow = 2 * (c1 - c0) + 2;
+  __half* xw = reinterpret_cast<__half*>(smem);
+  float* xsw = reinterpret_cast<float*>(smem + (((size_t)B * S.xrow * 2 + 15) & ~(size_t)15));
+  S.x = xw;
+  S.xs = xsw;
+  if (XSRC == XSRC_RESID) {
+    // inv[b] from the producer's partial sums of squares (all threads share the loads)
+    float part[MAG_MAX_BATCH];
+    for (int b = 0; b < B; ++b) part[b] = 0.f;
+    for (int i = tid; i < a.n_ss; i += blockDim.x)
+      for (int b = 0; b < B; ++b) part[b] += __ldcg(a.ss_part + (int64_t)i * MAG_MAX_BATCH + b);
+    for (int b = 0; b < B; ++b) {
+      const float v = warp_sum(part[b]);
+      if ((tid & 31) == 0) s_inv[(tid >> 5) * MAG_MAX_BATCH + b] = v;
     }
-    xf[nt].u0 = u0;
-    xf[nt].u1 = u1;
-    if (WFMT == W_W4) {
-      // group sums for this lane's two C columns (tokens 2t, 2t+1 of the n-tile)
-      const int t0 = 8 * nt + 2 * t, t1 = t0 + 1;
-      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-      const bool g1 = 2 * c + 1 < a.sm_row;
-      if (t0 < B) {
-        const float* p = a.xsum + (int64_t)t0 * a.ldxs + 2 * c;
-        a0 = g1 ? __ldg(reinterpret_cast<const float2*>(p)) : make_float2(__ldg(p), 0.f);
-      }
-      if (t1 < B) {
-        const float* p = a.xsum + (int64_t)t1 * a.ldxs + 2 * c;
-        a1 = g1 ? __ldg(reinterpret_cast<const float2*>(p)) : make_float2(__ldg(p), 0.f);
-      }
-      xf[nt].s_lo = make_float2(a0.x, a1.x);  // group 0: tokens 2t, 2t+1
-      xf[nt].s_hi = make_float2(a0.y, a1.y);  // group 1
+    __syncthreads();
+    if (tid < B) {
+      float tot = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_inv[w * MAG_MAX_BATCH + tid];
+      s_inv[kWarps * MAG_MAX_BATCH + tid] = 1.0f / sqrtf(tot / (float)a.K + a.eps);
     }
+    __syncthreads();
   }
-}
-
-__device__ __forceinline__ float silu_mul(float gte, float up) { return gte / (1.0f + expf(-gte)) * up; }
-
-// Last block of a residual projection: RMSNorm of the new residual into the
-// next projection's fp16 activations (W4 unit order or natural) and their
-// group sums, or the fp16 hidden-state output.
-__device__ void residual_tail(const GemvArgs& a, float* sm_inv) {
-  const int B = a.batch, D = a.n_mtiles * 16, tid = threadIdx.x;
-  if (a.tail == TAIL_HIDDEN) {
-    __half* out = reinterpret_cast<__half*>(a.step->out);
-    for (int i = tid; i < B * D; i += blockDim.x) {
-      const int b = i / D, k = i - b * D;
-      out[(int64_t)b * D + k] = __float2half_rn(__ldcg(a.r + (int64_t)b * a.ldr + k));
-    }
-    return;
-  }
-  if (tid < B) {
-    float tot = 0.f;
-    for (int m = 0; m < a.n_mtiles; ++m) tot += __ldcg(a.ss_part + (int64_t)m * MAG_MAX_BATCH + tid);
-    sm_inv[tid] = 1.0f / sqrtf(tot / (float)D + a.eps);
-  }
-  __syncthreads();
-  const int units = D / 8;  // D % 32 == 0: the 4 units of a group sit in one quad of lanes
+  const int units = (c1 - c0) * 8;  // multiple of 4: the 4 units of a group sit in one quad of lanes
   for (int base = 0; base < B * units; base += blockDim.x) {
     const int i = base + tid;
     const bool live = i < B * units;
     const int b = live ? i / units : 0, u = live ? i - b * units : 0;
+    const int k = (c0 * 8 + u) * 8;
     float s = 0.f;
     if (live) {
-      const float inv = sm_inv[b];
-      const float4 r0 = __ldcg(reinterpret_cast<const float4*>(a.r + (int64_t)b * a.ldr + 8 * u));
-      const float4 r1 = __ldcg(reinterpret_cast<const float4*>(a.r + (int64_t)b * a.ldr + 8 * u + 4));
-      const uint4 gg = *reinterpret_cast<const uint4*>(a.gamma + 8 * u);
-      const __half* gh = reinterpret_cast<const __half*>(&gg);
-      const float f[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-      __half h[8], o[8];
+      __half h[8];
+      if (k >= a.K) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(0.f);
+      } else if (XSRC == XSRC_F16) {
+        *reinterpret_cast<uint4*>(h) = *reinterpret_cast<const uint4*>(a.x + (int64_t)b * a.ldx + k);
+      } else {
+        const float inv = s_inv[kWarps * MAG_MAX_BATCH + b];
+        const float4 r0 = __ldcg(reinterpret_cast<const float4*>(a.r + (int64_t)b * a.ldr + k));
+        const float4 r1 = __ldcg(reinterpret_cast<const float4*>(a.r + (int64_t)b * a.ldr + k + 4));
+        const uint4 gg = *reinterpret_cast<const uint4*>(a.gamma + k);
+        const __half* gh = reinterpret_cast<const __half*>(&gg);
+        const float f[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(f[e] * inv * __half2float(gh[e]));
+      }
+      __half o[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        h[e] = __float2half_rn(f[e] * inv * __half2float(gh[e]));
+        o[WFMT == W_W4 ? unit_pos(e) : e] = h[e];
         s += __half2float(h[e]);
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[a.xn_permuted ? unit_pos(e) : e] = h[e];
-      *reinterpret_cast<uint4*>(a.xn + (int64_t)b * a.ldxn + 8 * u) = *reinterpret_cast<uint4*>(o);
+      *reinterpret_cast<uint4*>(xw + (size_t)b * S.xrow + 8 * u) = *reinterpret_cast<uint4*>(o);
     }
-    if (a.xn_sum) {
+    if (WFMT == W_W4) {
       s += __shfl_xor_sync(0xffffffffu, s, 1);
       s += __shfl_xor_sync(0xffffffffu, s, 2);
-      if (live && (u & 3) == 0) a.xn_sum[(int64_t)b * a.ldxns + u / 4] = s;
+      if (live && (u & 3) == 0) xsw[(size_t)b * S.grow + u / 4] = s;
     }
   }
+  __syncthreads();
+  return S;
 }
 
-template <int NT, int WFMT, int XMODE, int EPI>
-__global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs a) {
+__device__ __forceinline__ float silu_mul(float gte, float up) { return gte / (1.0f + expf(-gte)) * up; }
+
+// Per-tile epilogue, one warp. acc[nt][0..1]: row g, tokens 8nt+2t, +1; acc[nt][2..3]: row g+8.
+template <int NT, int EPI>
+__device__ void epilogue_tile(const GemvArgs& a, int mt, const float (&acc)[2][4], int lane) {
+  const int g = lane >> 2, t = lane & 3, B = a.batch;
+  if (EPI == EPI_RESID) {
+    float ssq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int tok = nt * 8 + 2 * t + jj;
+        if (tok < B) {
+          float* o = a.r + (int64_t)tok * a.ldr + mt * 16 + g;
+          const float n0 = o[0] + acc[nt][jj], n1 = o[8] + acc[nt][jj + 2];
+          o[0] = n0;
+          o[8] = n1;
+          ssq[nt][jj] = n0 * n0 + n1 * n1;
+        }
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        float v = ssq[nt][jj];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        const int tok = nt * 8 + 2 * t + jj;
+        if (g == 0 && tok < B) a.ss_part[(int64_t)mt * MAG_MAX_BATCH + tok] = v;
+      }
+    return;
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int tok = nt * 8 + 2 * t + jj;
+      if (tok >= B) continue;
+      const float lo = acc[nt][jj], hi = acc[nt][jj + 2];  // rows g and g + 8 of the tile
+      if (EPI == EPI_SWIGLU) {
+        a.out_h[(int64_t)tok * a.ldo + mt * 8 + g] = __float2half_rn(silu_mul(lo, hi));
+      } else if (EPI == EPI_QKV) {
+        const int tiles_per_head = a.head_dim / 16, head = mt / tiles_per_head;
+        const int i = 8 * (mt - head * tiles_per_head) + g;  // pair (i, i + d/2) of the head
+        const int row = head * a.head_dim + i, row8 = row + a.head_dim / 2;
+        __half* o = a.out_h + (int64_t)tok * a.ldo;
+        if (head < a.n_rot_heads) {
+          // round as the fp16 projection output, then rotate
+          const float x0 = __half2float(__float2half_rn(lo)), x1 = __half2float(__float2half_rn(hi));
+          const int pos = a.step->pos[tok], hd = a.head_dim / 2;
+          const float cs = a.rope_cos[(int64_t)pos * hd + i], sn = a.rope_sin[(int64_t)pos * hd + i];
+          o[row] = __float2half_rn(x0 * cs - x1 * sn);
+          o[row8] = __float2half_rn(x0 * sn + x1 * cs);
+        } else {
+          o[row] = __float2half_rn(lo);
+          o[row8] = __float2half_rn(hi);
+        }
+      } else {
+        __half* o = reinterpret_cast<__half*>(a.step->out) + (int64_t)tok * a.ldo + mt * 16 + g;
+        o[0] = __float2half_rn(lo);
+        o[8] = __float2half_rn(hi);
+      }
+    }
+}
+
+// ------------------------------------------------------------------ Stream-K schedule (B <= 4)
+template <int WFMT, int XSRC, int EPI>
+__global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
   using Stage = typename StageT<WFMT>::type;
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ float s_misc[4 * 8 * MAG_MAX_BATCH + MAG_MAX_BATCH];
-  __shared__ int s_last;
+  __shared__ float s_inv[(kWarps + 1) * MAG_MAX_BATCH];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int mt_local = warp % a.mpc, kw = warp / a.mpc;
-  const int mt = blockIdx.x * a.mpc + mt_local;
-  const bool mt_ok = mt < a.n_mtiles;
-  const int c_begin = blockIdx.y * a.chunks_per_cta;
-  const int c_end = min(c_begin + a.chunks_per_cta, a.n_chunks);
-  const int n_cc = c_end - c_begin;
-  const int B = a.batch;
-  const bool one_tok = B == 1;
+  const int C = a.n_chunks;
+  const int64_t P = (int64_t)a.n_mtiles * C;
+  const int64_t W = (int64_t)gridDim.x * kWarps;
+  const int64_t Q = (P + W - 1) / W;
+  const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t p0 = min(w * Q, P), p1 = min(p0 + Q, P);
+  const int n = (int)(p1 - p0);
 
-  int row_g, row_g8;
-  if (EPI == EPI_SWIGLU) {
-    row_g = mt * 8 + g;
-    row_g8 = a.swiglu_f + mt * 8 + g;
-  } else if (EPI == EPI_QKV) {
-    const int tiles_per_head = a.head_dim / 16, head = mt / tiles_per_head, j = mt - head * tiles_per_head;
-    row_g = head * a.head_dim + 8 * j + g;
-    row_g8 = row_g + a.head_dim / 2;
-  } else {
-    row_g = mt * 16 + g;
-    row_g8 = row_g + 8;
-  }
-
-  const int n_my = (mt_ok && kw < n_cc) ? (n_cc - kw + a.wk - 1) / a.wk : 0;
   Stage st[kStages];
 #pragma unroll
   for (int u = 0; u < kStages; ++u)
-    if (u < n_my) load_stage(st[u], a, row_g, row_g8, c_begin + kw + u * a.wk, t);
+    if (u < n) load_stage(st[u], a, (int)((p0 + u) / C), (int)((p0 + u) % C), lane);
 
   pdl_wait();
   pdl_trigger();
+  const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, 0, C);
 
-  const int xrow = n_cc * 64 + 8;  // X_SMEM: halves per staged token row
-  const __half* xs = reinterpret_cast<const __half*>(smem);
-  if (XMODE == X_SMEM) {
-    __half* xw = reinterpret_cast<__half*>(smem);
-    const int units = n_cc * 8;
-    for (int i = tid; i < units * B; i += blockDim.x) {
-      const int b = i / units, u = i - b * units, k = (c_begin * 8 + u) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (k < a.K) v = *reinterpret_cast<const uint4*>(a.x + (int64_t)b * a.ldx + k);
-      *reinterpret_cast<uint4*>(xw + (size_t)b * xrow + u * 8) = v;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  int mt = (int)(p0 / C), c = (int)(p0 % C);
+  int64_t seg0 = p0;
+  // finish the tile mt with this warp's part [seg0, seg1) of its pairs
+  auto finish = [&](int64_t seg1) {
+    const int64_t t0 = (int64_t)mt * C, t1 = t0 + C;
+    if (seg0 == t0 && seg1 == t1) {
+      epilogue_tile<1, EPI>(a, mt, acc, lane);
+      return;
     }
-    __syncthreads();
-  }
+    // part of a tile: publish it; the last warp of the tile adds the parts in warp order
+    const int slot = p0 >= t0 ? 0 : 1;
+    float* part = a.partial + ((w * 2 + slot) * 32 + lane) * 4;
+    *reinterpret_cast<float4*>(part) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    __threadfence();
+    __syncwarp();
+    const int64_t w_first = t0 / Q, w_last = (t1 - 1) / Q;
+    unsigned prev = 0;
+    if (lane == 0) prev = atomicAdd(a.counters + mt, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev != (unsigned)(w_last - w_first)) return;
+    __threadfence();
+    float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int64_t v = w_first; v <= w_last; ++v) {
+      const int sl = v * Q >= t0 ? 0 : 1;
+      const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partial + ((v * 2 + sl) * 32 + lane) * 4));
+      sum[0][0] += p.x;
+      sum[0][1] += p.y;
+      sum[0][2] += p.z;
+      sum[0][3] += p.w;
+    }
+    epilogue_tile<1, EPI>(a, mt, sum, lane);
+    if (lane == 0) a.counters[mt] = 0;
+  };
 
-  float acc[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-
-  for (int i = 0; i < n_my; i += kStages) {
+  for (int i = 0; i < n; i += kStages) {
 #pragma unroll
     for (int u = 0; u < kStages; ++u) {
-      if (i + u < n_my) {
+      if (i + u < n) {
         const Stage cur = st[u];
-        const int c = c_begin + kw + (i + u) * a.wk;
-        if (i + u + kStages < n_my) load_stage(st[u], a, row_g, row_g8, c + kStages * a.wk, t);
-        XFrag xf[2];
-        load_x<NT, WFMT, XMODE>(xf, a, xs, xrow, c, c_begin, g, t);
-        compute_stage<NT>(cur, acc, xf, one_tok);
+        if (i + u + kStages < n) {
+          const int64_t q = p0 + i + u + kStages;
+          load_stage(st[u], a, (int)(q / C), (int)(q % C), lane);
+        }
+        compute_chunk<1>(cur, acc, S, a.batch, c, g, t);
+        if (++c == C) {  // end of a tile
+          finish(p0 + i + u + 1);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[0][j] = 0.f;
+          ++mt;
+          c = 0;
+          seg0 = p0 + i + u + 1;
+        }
       }
     }
   }
+  if (seg0 < p1) finish(p1);  // this warp's run ends inside a tile
+}
 
-  // ---- reduce the wk warps of each m-tile
-  if (a.wk > 1) {
-    __syncthreads();
-    float* red = reinterpret_cast<float*>(smem);
-    if (kw > 0 && mt_ok) {
-      float* p = red + (((size_t)(kw - 1) * a.mpc + mt_local) * 32 + lane) * 8;
+// ------------------------------------------------------------------ K-split schedule (B > 4)
+template <int NT, int WFMT, int XSRC, int EPI>
+__global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
+  using Stage = typename StageT<WFMT>::type;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float s_inv[(kWarps + 1) * MAG_MAX_BATCH];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int mt = blockIdx.x * kWarps + warp;
+  const bool mt_ok = mt < a.n_mtiles;
+  const int c0 = blockIdx.y * a.chunks_per_cta, c1 = min(c0 + a.chunks_per_cta, a.n_chunks);
+  const int n = mt_ok ? c1 - c0 : 0;
+
+  Stage st[kStages];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+  for (int u = 0; u < kStages; ++u)
+    if (u < n) load_stage(st[u], a, mt, c0 + u, lane);
+
+  pdl_wait();
+  pdl_trigger();
+  const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, c0, c1);
+
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int i = 0; i < n; i += kStages) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[nt * 4 + i] = acc[nt][i];
-    }
-    __syncthreads();
-    if (kw == 0 && mt_ok) {
-      for (int w = 1; w < a.wk; ++w) {
-        const float* p = red + (((size_t)(w - 1) * a.mpc + mt_local) * 32 + lane) * 8;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[nt][i] += p[nt * 4 + i];
+    for (int u = 0; u < kStages; ++u) {
+      if (i + u < n) {
+        const Stage cur = st[u];
+        if (i + u + kStages < n) load_stage(st[u], a, mt, c0 + i + u + kStages, lane);
+        compute_chunk<NT>(cur, acc, S, a.batch, c0 + i + u, g, t);
       }
     }
   }
-
-  // ---- reduce across k-split blocks: the last block of the group sums in split order
   if (a.ks > 1) {
-    if (kw == 0 && mt_ok) {
+    if (mt_ok) {
       float* p = a.partial + (((size_t)blockIdx.y * a.n_mtiles + mt) * 32 + lane) * (4 * NT);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -373,11 +438,11 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (kw == 0 && mt_ok) {
+    if (mt_ok) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
       for (int s = 0; s < a.ks; ++s) {
         const float* p = a.partial + (((size_t)s * a.n_mtiles + mt) * 32 + lane) * (4 * NT);
 #pragma unroll
@@ -392,148 +457,18 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs a) {
     }
     if (tid == 0) a.counters[blockIdx.x] = 0;
   }
-
-  // ---- epilogue
-  const bool ep = kw == 0 && mt_ok;
-  if (EPI == EPI_SWIGLU) {
-    // act = silu(gate) * up for rows j = 8 mt + g, stored in W4 unit order, plus group sums
-    float gsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    if (ep) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int tok = nt * 8 + 2 * t + jj;
-          if (tok < B) {
-            const __half h = __float2half_rn(silu_mul(acc[nt][jj], acc[nt][jj + 2]));
-            a.out_h[(int64_t)tok * a.ldo + 8 * mt + unit_pos(g)] = h;
-            gsum[nt][jj] = __half2float(h);
-          }
-        }
-    }
-    // sum over the 8 rows of the tile (lanes with equal t), then over the 4 tiles of a group
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        float v = gsum[nt][jj];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        gsum[nt][jj] = v;
-      }
-    if (kw == 0 && g == 0) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) s_misc[mt_local * MAG_MAX_BATCH + nt * 8 + 2 * t + jj] = gsum[nt][jj];
-    }
-    __syncthreads();
-    // one thread per (group of 4 tiles, token)
-    const int n_groups_cta = (a.mpc + 3) / 4;
-    for (int i = tid; i < n_groups_cta * B; i += blockDim.x) {
-      const int gi = i / B, tok = i - gi * B;
-      const int mt0 = blockIdx.x * a.mpc + 4 * gi;
-      float s = 0.f;
-      for (int m = 0; m < 4; ++m)
-        if (4 * gi + m < a.mpc && mt0 + m < a.n_mtiles) s += s_misc[(4 * gi + m) * MAG_MAX_BATCH + tok];
-      if (mt0 < a.n_mtiles) a.out_sum[(int64_t)tok * a.ldos + mt0 / 4] = s;
-    }
-    return;
-  }
-  if (EPI == EPI_RESID) {
-    float ssq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    if (ep) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int tok = nt * 8 + 2 * t + jj;
-          if (tok < B) {
-            float* o = a.r + (int64_t)tok * a.ldr + mt * 16 + g;
-            const float n0 = o[0] + acc[nt][jj], n1 = o[8] + acc[nt][jj + 2];
-            o[0] = n0;
-            o[8] = n1;
-            ssq[nt][jj] = n0 * n0 + n1 * n1;
-          }
-        }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        float v = ssq[nt][jj];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        ssq[nt][jj] = v;
-      }
-    if (ep && g == 0) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int tok = nt * 8 + 2 * t + jj;
-          if (tok < B) a.ss_part[(int64_t)mt * MAG_MAX_BATCH + tok] = ssq[nt][jj];
-        }
-    }
-    if (a.tail == TAIL_NONE) return;
-    // the last block to finish runs the tail over the whole residual
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(a.counters + gridDim.x, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    residual_tail(a, s_misc);
-    if (tid == 0) a.counters[gridDim.x] = 0;
-    return;
-  }
-  if (!ep) return;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      const int tok = nt * 8 + 2 * t + jj;
-      if (tok >= B) continue;
-      const float lo = acc[nt][jj], hi = acc[nt][jj + 2];  // rows g and g + 8
-      if (EPI == EPI_QKV) {
-        // round as the fp16 projection output, then rotate q and k heads: pair (i, i + d/2)
-        const float x0 = __half2float(__float2half_rn(lo)), x1 = __half2float(__float2half_rn(hi));
-        const int head = row_g / a.head_dim, i = row_g - head * a.head_dim;
-        __half* o = a.out_h + (int64_t)tok * a.ldo;
-        if (head < a.n_rot_heads) {
-          const int pos = a.step->pos[tok], hd = a.head_dim / 2;
-          const float c = a.rope_cos[(int64_t)pos * hd + i], s = a.rope_sin[(int64_t)pos * hd + i];
-          o[row_g] = __float2half_rn(x0 * c - x1 * s);
-          o[row_g8] = __float2half_rn(x0 * s + x1 * c);
-        } else {
-          o[row_g] = __float2half_rn(lo);
-          o[row_g8] = __float2half_rn(hi);
-        }
-      } else {
-        __half* o = (EPI == EPI_STORE_OUT ? reinterpret_cast<__half*>(a.step->out) : a.out_h) +
-                    (int64_t)tok * a.ldo + mt * 16 + g;
-        o[0] = __float2half_rn(lo);
-        o[8] = __float2half_rn(hi);
-      }
-    }
-  }
+  if (mt_ok) epilogue_tile<NT, EPI>(a, mt, acc, lane);
 }
 
-template <int NT, int WFMT, int XMODE, int EPI>
-cudaError_t launch_t(const Launch& L, const GemvArgs& a) {
-  dim3 grid((a.n_mtiles + a.mpc - 1) / a.mpc, a.ks);
-  dim3 block(32 * a.mpc * a.wk);
-  size_t smem = gemv_smem_bytes(a, XMODE);
-  auto kern = gemv_kernel<NT, WFMT, XMODE, EPI>;
+template <typename K>
+cudaError_t launch_k(const Launch& L, K kern, dim3 grid, size_t smem, const GemvArgs& a) {
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = block;
+  cfg.blockDim = dim3(32 * kWarps);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
@@ -545,27 +480,46 @@ cudaError_t launch_t(const Launch& L, const GemvArgs& a) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-}  // namespace
-
-size_t gemv_smem_bytes(const GemvArgs& a, int xmode) {
-  size_t xs = xmode == X_SMEM ? (size_t)a.batch * (a.chunks_per_cta * 64 + 8) * 2 : 0;
-  size_t red = a.wk > 1 ? (size_t)(a.wk - 1) * a.mpc * 32 * 8 * 4 : 0;
-  size_t body = xs > red ? xs : red;
-  return ((body + 15) / 16) * 16;
+template <int WFMT, int XSRC, int EPI>
+cudaError_t launch_sched(const Launch& L, const GemvArgs& a) {
+  const size_t smem = gemv_smem_bytes(a);
+  if (a.streamk_blocks > 0)
+    return launch_k(L, gemv_streamk_kernel<WFMT, XSRC, EPI>, dim3(a.streamk_blocks), smem, a);
+  const dim3 grid((a.n_mtiles + kWarps - 1) / kWarps, a.ks);
+  if (a.batch > 8) return launch_k(L, gemv_ksplit_kernel<2, WFMT, XSRC, EPI>, grid, smem, a);
+  return launch_k(L, gemv_ksplit_kernel<1, WFMT, XSRC, EPI>, grid, smem, a);
 }
 
-cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xmode, int epi) {
-  const bool two = a.batch > 8;
-#define MAG_GEMV_CASE(NT_, W_, X_, E_) \
-  if ((NT_ == 2) == two && wfmt == W_ && xmode == X_ && epi == E_) return launch_t<NT_, W_, X_, E_>(L, a);
-#define MAG_GEMV_NT(W_, X_, E_) MAG_GEMV_CASE(1, W_, X_, E_) MAG_GEMV_CASE(2, W_, X_, E_)
-#define MAG_GEMV_X(W_, E_) MAG_GEMV_CASE(1, W_, X_DIRECT, E_) MAG_GEMV_NT(W_, X_SMEM, E_)
-  MAG_GEMV_X(W_W4, EPI_QKV)
-  MAG_GEMV_X(W_W4, EPI_RESID)
-  MAG_GEMV_X(W_W4, EPI_SWIGLU)
-  MAG_GEMV_X(W_F16, EPI_STORE_OUT)
-#undef MAG_GEMV_X
-#undef MAG_GEMV_NT
+}  // namespace
+
+size_t gemv_smem_bytes(const GemvArgs& a) {
+  const int nch = a.streamk_blocks > 0 ? a.n_chunks : a.chunks_per_cta;
+  return (((size_t)a.batch * (nch * 64 + 8) * 2 + 15) & ~(size_t)15) + (size_t)a.batch * (2 * nch + 2) * 4;
+}
+
+int gemv_blocks_per_sm(int wfmt, int xsrc, int epi, size_t smem) {
+  int n = 0;
+#define MAG_OCC(W_, X_, E_)                                                                                   \
+  if (wfmt == W_ && xsrc == X_ && epi == E_) {                                                               \
+    auto k = gemv_streamk_kernel<W_, X_, E_>;                                                                \
+    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, 32 * kWarps, smem);                                \
+  }
+  MAG_OCC(W_W4, XSRC_RESID, EPI_QKV)
+  MAG_OCC(W_W4, XSRC_F16, EPI_RESID)
+  MAG_OCC(W_W4, XSRC_RESID, EPI_SWIGLU)
+  MAG_OCC(W_F16, XSRC_RESID, EPI_STORE_OUT)
+#undef MAG_OCC
+  return n;
+}
+
+cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi) {
+#define MAG_GEMV_CASE(W_, X_, E_) \
+  if (wfmt == W_ && xsrc == X_ && epi == E_) return launch_sched<W_, X_, E_>(L, a);
+  MAG_GEMV_CASE(W_W4, XSRC_RESID, EPI_QKV)
+  MAG_GEMV_CASE(W_W4, XSRC_F16, EPI_RESID)
+  MAG_GEMV_CASE(W_W4, XSRC_RESID, EPI_SWIGLU)
+  MAG_GEMV_CASE(W_F16, XSRC_RESID, EPI_STORE_OUT)
 #undef MAG_GEMV_CASE
   return cudaErrorInvalidValue;
 }

@@ -44,13 +44,10 @@ __global__ void quantize_w4g32_kernel(const float* __restrict__ src, int64_t row
 }
 
 // Step prologue (one block per token): write this step's block-table entries,
-// load the fp16 hidden input into the fp32 residual stream, and RMSNorm it for
-// the first layer's QKV projection ("5. Core modules" 5.1, pre-norm): xn in
-// the W4 activation unit order (x0,x4,x1,x5,x2,x6,x3,x7) plus its 32-value
-// group sums.
+// load the fp16 hidden input into the fp32 residual stream and store its sum
+// of squares in ss_part[0][b] for the first layer's RMSNorm.
 __global__ void step_begin_kernel(const StepArgs* __restrict__ st, float* __restrict__ r, int D,
-                                  int32_t* __restrict__ tables, int table_stride, const __half* __restrict__ gamma,
-                                  float eps, __half* __restrict__ xn, float* __restrict__ xn_sum) {
+                                  int32_t* __restrict__ tables, int table_stride, float* __restrict__ ss_part) {
   __shared__ float s_red[32];
   pdl_wait();
   pdl_trigger();
@@ -58,9 +55,8 @@ __global__ void step_begin_kernel(const StepArgs* __restrict__ st, float* __rest
   if (b == 0 && tid < st->n_upd)
     tables[(int64_t)st->upd_sess[tid] * table_stride + st->upd_idx[tid]] = st->upd_blk[tid];
   const __half* hin = st->hidden_in + (int64_t)b * D;
-  const int units = D / 8;
   float ss = 0.f;
-  for (int u = tid; u < units; u += blockDim.x) {
+  for (int u = tid; u < D / 8; u += blockDim.x) {
     const uint4 v = *reinterpret_cast<const uint4*>(hin + 8 * u);
     const __half* h = reinterpret_cast<const __half*>(&v);
     float f[8];
@@ -78,30 +74,72 @@ __global__ void step_begin_kernel(const StepArgs* __restrict__ st, float* __rest
   if (tid == 0) {
     float tot = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_red[w];
-    s_red[0] = 1.0f / sqrtf(tot / (float)D + eps);
+    ss_part[b] = tot;  // entry 0 of token b (row stride MAG_MAX_BATCH)
   }
-  __syncthreads();
-  const float inv = s_red[0];
-  for (int base = 0; base < units; base += blockDim.x) {  // warp-uniform trips: quads share a group
-    const int u = base + tid;
-    float s = 0.f;
-    if (u < units) {
-      const uint4 v = *reinterpret_cast<const uint4*>(hin + 8 * u);
-      const uint4 gg = *reinterpret_cast<const uint4*>(gamma + 8 * u);
-      const __half* h = reinterpret_cast<const __half*>(&v);
-      const __half* gh = reinterpret_cast<const __half*>(&gg);
-      __half o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const __half x = __float2half_rn(__half2float(h[e]) * inv * __half2float(gh[e]));
-        o[e < 4 ? 2 * e : 2 * (e - 4) + 1] = x;
-        s += __half2float(x);
+}
+
+// No LM head: the output is the fp16 hidden state.
+__global__ void final_hidden_kernel(const StepArgs* __restrict__ st, const float* __restrict__ r, int D) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x;
+  __half* out = reinterpret_cast<__half*>(st->out);
+  for (int i = threadIdx.x; i < D; i += blockDim.x) out[(int64_t)b * D + i] = __float2half_rn(r[(int64_t)b * D + i]);
+}
+
+// Row pair (r_g, r_g8) of slot g of tile mt under a tile map.
+__device__ __forceinline__ void tile_rows(int map, int map_arg, int mt, int g, int& rg, int& rg8) {
+  if (map == MAP_SWIGLU) {
+    rg = mt * 8 + g;
+    rg8 = map_arg + mt * 8 + g;
+  } else if (map == MAP_QKV) {
+    const int tph = map_arg / 16, head = mt / tph;
+    rg = head * map_arg + 8 * (mt - head * tph) + g;
+    rg8 = rg + map_arg / 2;
+  } else {
+    rg = mt * 16 + g;
+    rg8 = rg + 8;
+  }
+}
+
+// One thread per (tile, chunk, lane): the lane's 16 bytes of codes, and for
+// t == 0 the 16 bytes of (scale, min) of its row pair. dir 0: canonical ->
+// tiles, 1: tiles -> canonical.
+__global__ void w4_tiles_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int N, int K, int map,
+                                int map_arg, int dir) {
+  const int G = (K + 31) / 32, C = (K + 63) / 64, n_mt = N / 16;
+  const int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (id >= (int64_t)n_mt * C * 32) return;
+  const int lane = (int)(id & 31), g = lane >> 2, t = lane & 3;
+  const int64_t tc = id >> 5;
+  const int mt = (int)(tc / C), c = (int)(tc - (int64_t)mt * C);
+  int rg, rg8;
+  tile_rows(map, map_arg, mt, g, rg, rg8);
+  const int64_t code_bytes = (int64_t)N * G * 16;
+  uint8_t* tile = (dir == 0 ? dst : const_cast<uint8_t*>(src)) + tc * kTileBytes;
+  const int rows[2] = {rg, rg8};
+  for (int h = 0; h < 2; ++h)
+    for (int q = 0; q < 2; ++q) {
+      const int grp = 2 * c + q;
+      uint32_t* tw = reinterpret_cast<uint32_t*>(tile + lane * 16) + 2 * h + q;
+      if (dir == 0) {
+        *tw = grp < G ? *reinterpret_cast<const uint32_t*>(src + (int64_t)rows[h] * G * 16 + grp * 16 + 4 * t) : 0u;
+      } else if (grp < G) {
+        *reinterpret_cast<uint32_t*>(dst + (int64_t)rows[h] * G * 16 + grp * 16 + 4 * t) = *tw;
       }
-      *reinterpret_cast<uint4*>(xn + (int64_t)b * D + 8 * u) = *reinterpret_cast<uint4*>(o);
     }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    if (u < units && (u & 3) == 0) xn_sum[(int64_t)b * (D / 32) + u / 4] = s;
+  if (t == 0) {
+    for (int h = 0; h < 2; ++h)
+      for (int q = 0; q < 2; ++q) {
+        const int grp = 2 * c + q;
+        uint32_t* ts = reinterpret_cast<uint32_t*>(tile + 512 + g * 16) + 2 * h + q;
+        const int64_t ci = code_bytes + ((int64_t)rows[h] * G + grp) * 4;
+        if (dir == 0) {
+          *ts = grp < G ? *reinterpret_cast<const uint32_t*>(src + ci) : 0u;
+        } else if (grp < G) {
+          *reinterpret_cast<uint32_t*>(dst + ci) = *ts;
+        }
+      }
   }
 }
 
@@ -135,10 +173,30 @@ cudaError_t launch_quantize_w4g32(cudaStream_t s, const float* src, int64_t rows
 }
 
 cudaError_t launch_step_begin(const Launch& L, const StepArgs* step, float* r, int D, int32_t* tables,
-                              int table_stride, int batch, const __half* gamma, float eps, __half* xn,
-                              float* xn_sum) {
-  return launch_plain(L, step_begin_kernel, dim3(batch), dim3(256), step, r, D, tables, table_stride, gamma, eps,
-                      xn, xn_sum);
+                              int table_stride, int batch, float* ss_part) {
+  return launch_plain(L, step_begin_kernel, dim3(batch), dim3(256), step, r, D, tables, table_stride, ss_part);
+}
+
+cudaError_t launch_final_hidden(const Launch& L, const StepArgs* step, const float* r, int D, int batch) {
+  return launch_plain(L, final_hidden_kernel, dim3(batch), dim3(256), step, r, D);
+}
+
+static cudaError_t launch_tiles(cudaStream_t s, const uint8_t* src, uint8_t* dst, int N, int K, int map, int map_arg,
+                                int dir) {
+  const int64_t n = (int64_t)(N / 16) * ((K + 63) / 64) * 32;
+  if (n == 0) return cudaSuccess;
+  w4_tiles_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, dst, N, K, map, map_arg, dir);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w4_to_tiles(cudaStream_t s, const uint8_t* canon, int N, int K, int map, int map_arg,
+                               uint8_t* tiles) {
+  return launch_tiles(s, canon, tiles, N, K, map, map_arg, 0);
+}
+
+cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, int K, int map, int map_arg,
+                                 uint8_t* canon) {
+  return launch_tiles(s, tiles, canon, N, K, map, map_arg, 1);
 }
 
 }  // namespace mag

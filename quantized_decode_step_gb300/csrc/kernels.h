@@ -18,61 +18,60 @@ struct Launch {
 
 // ---------------------------------------------------------------- W4 / fp16 GEMV (mma.sync)
 enum WeightFmt { W_W4 = 0, W_F16 = 1 };
-enum XMode { X_DIRECT = 0, X_SMEM = 1 };
+enum XSource { XSRC_F16 = 0, XSRC_RESID = 1 };
 enum Epilogue { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_STORE_OUT = 3 };
-enum Tail { TAIL_NONE = 0, TAIL_NORM = 1, TAIL_HIDDEN = 2 };
+enum TileMap { MAP_PLAIN = 0, MAP_QKV = 1, MAP_SWIGLU = 2 };
+constexpr int kTileBytes = 640;  // one 16-row x 64-k tile: 512 B of codes + 128 B of (scale, min)
 
 struct GemvArgs {
-  const uint8_t* w;       // W4 codes [N][w_row_bytes] or fp16 [N][K]
-  const __half2* sm;      // W4 (scale, min) pairs [N][sm_row]
-  int64_t w_row_bytes;
-  int32_t sm_row;         // groups per row (W4)
-  int32_t n_mtiles;       // 16-row tiles (SwiGLU: 8 gate + 8 up rows; QKV: rows i..i+7 and i+d/2.. of a head)
+  const uint8_t* w;       // W4: tiles [n_mtiles][n_chunks][640 B]; fp16: row-major [N][K]
+  int64_t w_row_bytes;    // fp16 weights: 2K
+  int32_t n_mtiles;       // 16-row tiles
   int32_t K;              // reduction length
   int32_t n_chunks;       // ceil(K / 64)
-  int32_t chunks_per_cta; // k-range of one block, in 64-wide chunks
-  int32_t ks;             // k-splits (grid.y)
-  int32_t mpc;            // m-tiles per block
-  int32_t wk;             // warps sharing one m-tile's k-range
-  const __half* x;        // activations [B][ldx]: W4 unit order (x0,x4,x1,x5,x2,x6,x3,x7) / natural (fp16 W)
-  int32_t ldx;
-  const float* xsum;      // W4: group sums of x [B][ldxs]
-  int32_t ldxs;
+  int32_t streamk_blocks; // > 0: Stream-K over that many blocks; 0: k-split grid
+  int32_t chunks_per_cta; // k-split: k-range of one block, in chunks
+  int32_t ks;             // k-split: splits (grid.y)
   int32_t batch;
-  // EPI_QKV
-  int32_t head_dim, n_rot_heads;
+  // activations: XSRC_F16 fp16 [B][ldx]; XSRC_RESID RMSNorm of the fp32 residual
+  const __half* x;
+  int32_t ldx;
+  float* r;               // fp32 residual [B][ldr] (read by XSRC_RESID, updated by EPI_RESID)
+  int32_t ldr;
+  float* ss_part;         // per-tile sums of squares [n][16]: written by EPI_RESID, read by XSRC_RESID
+  int32_t n_ss;           // XSRC_RESID: entries of ss_part to add up
+  const __half* gamma;    // XSRC_RESID gain
+  float eps;
+  // epilogues
+  __half* out_h;          // EPI_QKV [B][ldo] natural, EPI_SWIGLU [B][ldo]
+  int32_t ldo;
+  int32_t head_dim, n_rot_heads;  // EPI_QKV: heads below n_rot_heads get RoPE
   const float* rope_cos;
   const float* rope_sin;
-  // EPI_QKV / EPI_SWIGLU: fp16 out [B][ldo]; EPI_SWIGLU group sums [B][ldos]
-  __half* out_h;
-  int32_t ldo;
-  int32_t swiglu_f;
-  float* out_sum;
-  int32_t ldos;
-  // EPI_RESID: residual [B][ldr] += y, per-tile sums of squares [n_mtiles][16], tail
-  float* r;
-  int32_t ldr;
-  float* ss_part;
-  int32_t tail;           // Tail
-  const __half* gamma;    // TAIL_NORM gain
-  float eps;
-  __half* xn;             // TAIL_NORM output [B][ldxn]
-  int32_t ldxn;
-  int32_t xn_permuted;    // 1: W4 unit order
-  float* xn_sum;          // group sums of xn (or null) [B][ldxns]
-  int32_t ldxns;
-  float* partial;         // ks > 1: [ks][n_mtiles][32][4 * n_tiles]
-  uint32_t* counters;     // [grid.x + 1], zero between launches
+  float* partial;         // Stream-K: [warps][2][32][4]; k-split: [ks][n_mtiles][32][4 * n_tiles]
+  uint32_t* counters;     // zero between launches
   const StepArgs* step;
 };
 
-size_t gemv_smem_bytes(const GemvArgs& a, int xmode);
-cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xmode, int epi);
+size_t gemv_smem_bytes(const GemvArgs& a);
+int gemv_blocks_per_sm(int wfmt, int xsrc, int epi, size_t smem);
+cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi);
+
+// Load-time repack of a W4G32 matrix [N, K] (codes [N][16G] then (scale, min)
+// [N][G]) into 640-byte tiles, and back. Tile (mt, c) holds rows
+// (r_g, r_g8) for g = 0..7 by `map`: MAP_PLAIN 16 mt + g / +8; MAP_QKV the
+// RoPE pair (i, i + d/2) of one head; MAP_SWIGLU gate row 8 mt + g and up row
+// F + 8 mt + g.
+cudaError_t launch_w4_to_tiles(cudaStream_t s, const uint8_t* canon, int N, int K, int map, int map_arg,
+                               uint8_t* tiles);
+cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, int K, int map, int map_arg,
+                                 uint8_t* canon);
 
 // ---------------------------------------------------------------- step prologue
-// block-table writes, fp16 input -> fp32 residual, RMSNorm of layer 0 into xn (W4 unit order) + group sums
+// block-table writes, fp16 input -> fp32 residual and its sum of squares (ss_part[0][b])
 cudaError_t launch_step_begin(const Launch& L, const StepArgs* step, float* r, int D, int32_t* tables,
-                              int table_stride, int batch, const __half* gamma, float eps, __half* xn, float* xn_sum);
+                              int table_stride, int batch, float* ss_part);
+cudaError_t launch_final_hidden(const Launch& L, const StepArgs* step, const float* r, int D, int batch);
 
 // ---------------------------------------------------------------- bulk KV store
 struct KvStoreArgs {
@@ -89,10 +88,8 @@ cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a);
 struct AttnArgs {
   const __half* qkv;  // [B][qkv_ld]: q (rotated) [Hq d], k (rotated) [Hkv d], v [Hkv d]
   int32_t qkv_ld;
-  __half* o;          // [B][ldo] attention output, W4 unit order
+  __half* o;          // [B][ldo] attention output
   int32_t ldo;
-  float* osum;        // [B][ldos] group sums of o (32 dims)
-  int32_t ldos;
   int32_t n_heads, n_kv_heads, head_dim;
   int32_t layer;
   int32_t n_split;  // grid.x (<= 64)

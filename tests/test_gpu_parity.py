@@ -120,7 +120,7 @@ def _run_decode(wl: Workload, seed, n_steps=1, random_gain=False, flags=0, weigh
 def test_tiny_decode_matches_oracle(dt):
     wl = Workload(f"tiny-{dt}", TINY, dt, 1, (128,))
     ctx, res = _run_decode(wl, 11, n_steps=3, random_gain=True, weights_check=True)
-    assert ctx.last_step_launches() >= 8
+    assert ctx.last_step_launches() == 1 + 5 * TINY.n_layers + 1
 
 
 @pytest.mark.parametrize("flags", [mag.FLAG_NO_GRAPH, mag.FLAG_NO_PDL, mag.FLAG_ARENA_NO_REUSE])
