@@ -107,7 +107,6 @@ def _clone_kvs(cfg, kvs, wl, seed=SEED):
     out = []
     for i, p in enumerate(wl.prior):
         kv = oracle.KV(cfg, p + 8)
-        driver_kv = []
         L, H, d = wl.shape.n_layers, wl.shape.n_kv_heads, wl.shape.head_dim
         for t0 in range(0, p, 4096):
             n = min(4096, p - t0)
@@ -149,8 +148,6 @@ def _steps(ctx, w, wl, sids, kvs, cfg, n_steps, seed=SEED, floor_check=False):
             if ref[b, top[1]] - ref[b, top[0]] > 2 * TOL_MAX_ABS:
                 assert int(np.argmax(got[b])) == int(top[1])
         res.append((ma, rl))
-        if floor_check:
-            floor_check = step == 0 and False
     return res
 
 
