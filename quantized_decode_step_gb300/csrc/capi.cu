@@ -245,7 +245,7 @@ void plan_streamk(mag_ctx* c) {
       a.batch = B;
       a.n_chunks = (ps.K + 63) / 64;
       a.streamk_blocks = 1;
-      const size_t smem = gemv_smem_bytes(a);
+      const size_t smem = gemv_smem_bytes(a, ps.wfmt);
       const int per_sm = std::max(1, gemv_blocks_per_sm(ps.wfmt, ps.xsrc, ps.epi, smem));
       const int tiles_chunks = ps.n_mtiles * a.n_chunks;
       c->sk_blocks[ps.kind][B] = std::max(1, std::min(c->n_sm * per_sm, (tiles_chunks + 7) / 8));

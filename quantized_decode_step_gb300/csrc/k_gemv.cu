@@ -32,16 +32,69 @@
 // pre-generated RoPE table; the tile's rows g and g+8 are the pair (i, i+d/2)
 // of one head), RESID (fp32 residual add + per-tile sums of squares), SWIGLU
 // (silu(gate) * up of interleaved gate/up rows), OUT (fp16 logits into the
-// caller's buffer). Weight loads for the first chunks are issued before the
-// programmatic-dependent-launch wait, so they overlap the previous kernel.
+// caller's buffer).
+//
+// Weights reach shared memory through a per-warp ring of cp.async copies
+// (16 bytes per lane, L2 only), 12 chunks deep for W4 tiles and 4 for fp16
+// rows, so a warp keeps ~8 KB of HBM reads in flight without holding them in
+// registers; the ring is filled before the programmatic-dependent-launch wait,
+// so the first reads overlap the previous kernel.
 #include "kernels.h"
 
 namespace mag {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kWarps = 8;  // warps per block
+
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Per-warp ring of weight chunks in shared memory.
+template <int WFMT>
+struct Ring;
+
+template <>
+struct Ring<W_W4> {
+  static constexpr int kSlots = 12;
+  static constexpr int kSlotBytes = kTileBytes;  // 512 B codes (lane order) + 128 B (scale, min)
+  // copy chunk (mt, c) into `slot`: every lane its 16 B of codes, lanes 0-7 the (scale, min) rows
+  static __device__ __forceinline__ void issue(uint8_t* slot, const GemvArgs& a, int mt, int c, int lane) {
+    const uint8_t* tile = a.w + ((int64_t)mt * a.n_chunks + c) * kTileBytes;
+    cp_async16(slot + lane * 16, tile + lane * 16);
+    if (lane < 8) cp_async16(slot + 512 + lane * 16, tile + 512 + lane * 16);
+  }
+};
+
+template <>
+struct Ring<W_F16> {
+  static constexpr int kSlots = 4;
+  static constexpr int kSlotBytes = 2048;  // 16 rows x 64 k fp16; lane L: 64 B at 64 L
+  static __device__ __forceinline__ void issue(uint8_t* slot, const GemvArgs& a, int mt, int c, int lane) {
+    const int g = lane >> 2, t = lane & 3, k = c * 64 + t * 16;
+    uint8_t* d = slot + lane * 64;
+    if (k < a.K) {
+      const uint8_t* pg = a.w + (int64_t)(mt * 16 + g) * a.w_row_bytes + (int64_t)k * 2;
+      const uint8_t* ph = pg + 8 * a.w_row_bytes;
+      cp_async16(d, pg);
+      cp_async16(d + 16, pg + 16);
+      cp_async16(d + 32, ph);
+      cp_async16(d + 48, ph + 16);
+    } else {
+      *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(d + 16) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(d + 32) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(d + 48) = make_uint4(0, 0, 0, 0);
+    }
+  }
+};
 
 struct W4Stage {
   uint4 code;  // row g: group 0 word t, group 1 word t; row g+8: the same
@@ -50,6 +103,17 @@ struct W4Stage {
 struct F16Stage {
   uint4 g0, g1, h0, h1;
 };
+__device__ __forceinline__ void read_slot(W4Stage& st, const uint8_t* slot, int lane) {
+  st.code = *reinterpret_cast<const uint4*>(slot + lane * 16);
+  st.sm = *reinterpret_cast<const uint4*>(slot + 512 + (lane >> 2) * 16);
+}
+__device__ __forceinline__ void read_slot(F16Stage& st, const uint8_t* slot, int lane) {
+  const uint4* p = reinterpret_cast<const uint4*>(slot + lane * 64);
+  st.g0 = p[0];
+  st.g1 = p[1];
+  st.h0 = p[2];
+  st.h1 = p[3];
+}
 template <int WFMT>
 struct StageT;
 template <>
@@ -60,26 +124,6 @@ template <>
 struct StageT<W_F16> {
   using type = F16Stage;
 };
-
-__device__ __forceinline__ void load_stage(W4Stage& st, const GemvArgs& a, int mt, int c, int lane) {
-  const uint8_t* tile = a.w + ((int64_t)mt * a.n_chunks + c) * kTileBytes;
-  st.code = ldg_stream_u4(tile + lane * 16);
-  st.sm = ldg_stream_u4(tile + 512 + (lane >> 2) * 16);
-}
-
-__device__ __forceinline__ void load_stage(F16Stage& st, const GemvArgs& a, int mt, int c, int lane) {
-  const int g = lane >> 2, t = lane & 3, k = c * 64 + t * 16;
-  if (k < a.K) {
-    const uint8_t* pg = a.w + (int64_t)(mt * 16 + g) * a.w_row_bytes + (int64_t)k * 2;
-    const uint8_t* ph = pg + 8 * a.w_row_bytes;
-    st.g0 = ldg_stream_u4(pg);
-    st.g1 = ldg_stream_u4(pg + 16);
-    st.h0 = ldg_stream_u4(ph);
-    st.h1 = ldg_stream_u4(ph + 16);
-  } else {
-    st.g0 = st.g1 = st.h0 = st.h1 = make_uint4(0, 0, 0, 0);
-  }
-}
 
 // The 8 codes of a word (k0 in bits 0-3 ... k7 in bits 28-31) as exact fp16
 // integers, paired (k0,k4) (k1,k5) (k2,k6) (k3,k7).
@@ -171,6 +215,11 @@ __device__ __forceinline__ int unit_pos(int e) { return e < 4 ? 2 * e : 2 * (e -
 // Stage chunks [c0, c1) of the activations into shared memory (and their group
 // sums for W4). XSRC_RESID: xn = fp16(r / sqrt(mean(r^2) + eps) * gamma), the
 // mean from the producer's n_ss partial sums of squares per token.
+__host__ __device__ __forceinline__ size_t staged_bytes(int B, int nch) {
+  return ((((size_t)B * (nch * 64 + 8) * 2 + 15) & ~(size_t)15) + (size_t)B * (2 * nch + 2) * 4 + 127) &
+         ~(size_t)127;
+}
+
 template <int WFMT, int XSRC>
 __device__ Staged stage_x(const GemvArgs& a, uint8_t* smem, float* s_inv, int c0, int c1) {
   const int tid = threadIdx.x, B = a.batch;
@@ -313,7 +362,8 @@ __device__ void epilogue_tile(const GemvArgs& a, int mt, const float (&acc)[2][4
 template <int WFMT, int XSRC, int EPI>
 __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
   using Stage = typename StageT<WFMT>::type;
-  extern __shared__ __align__(16) uint8_t smem[];
+  using R = Ring<WFMT>;
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_inv[(kWarps + 1) * MAG_MAX_BATCH];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int C = a.n_chunks;
@@ -323,11 +373,13 @@ __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
   const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
   const int64_t p0 = min(w * Q, P), p1 = min(p0 + Q, P);
   const int n = (int)(p1 - p0);
+  uint8_t* ring = smem + staged_bytes(a.batch, C) + (size_t)warp * R::kSlots * R::kSlotBytes;
 
-  Stage st[kStages];
 #pragma unroll
-  for (int u = 0; u < kStages; ++u)
-    if (u < n) load_stage(st[u], a, (int)((p0 + u) / C), (int)((p0 + u) % C), lane);
+  for (int u = 0; u < R::kSlots; ++u) {
+    if (u < n) R::issue(ring + u * R::kSlotBytes, a, (int)((p0 + u) / C), (int)((p0 + u) % C), lane);
+    cp_async_commit();
+  }
 
   pdl_wait();
   pdl_trigger();
@@ -358,45 +410,48 @@ __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
     float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int64_t v = w_first; v <= w_last; ++v) {
       const int sl = v * Q >= t0 ? 0 : 1;
-      const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partial + ((v * 2 + sl) * 32 + lane) * 4));
-      sum[0][0] += p.x;
-      sum[0][1] += p.y;
-      sum[0][2] += p.z;
-      sum[0][3] += p.w;
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(a.partial + ((v * 2 + sl) * 32 + lane) * 4));
+      sum[0][0] += q.x;
+      sum[0][1] += q.y;
+      sum[0][2] += q.z;
+      sum[0][3] += q.w;
     }
     epilogue_tile<1, EPI>(a, mt, sum, lane);
     if (lane == 0) a.counters[mt] = 0;
   };
 
-  for (int i = 0; i < n; i += kStages) {
+  for (int i = 0; i < n; ++i) {
+    uint8_t* slot = ring + (i % R::kSlots) * R::kSlotBytes;
+    cp_async_wait<R::kSlots - 1>();
+    __syncwarp();
+    Stage cur;
+    read_slot(cur, slot, lane);
+    __syncwarp();
+    if (i + R::kSlots < n) {
+      const int64_t q = p0 + i + R::kSlots;
+      R::issue(slot, a, (int)(q / C), (int)(q % C), lane);
+    }
+    cp_async_commit();
+    compute_chunk<1>(cur, acc, S, a.batch, c, g, t);
+    if (++c == C) {  // end of a tile
+      finish(p0 + i + 1);
 #pragma unroll
-    for (int u = 0; u < kStages; ++u) {
-      if (i + u < n) {
-        const Stage cur = st[u];
-        if (i + u + kStages < n) {
-          const int64_t q = p0 + i + u + kStages;
-          load_stage(st[u], a, (int)(q / C), (int)(q % C), lane);
-        }
-        compute_chunk<1>(cur, acc, S, a.batch, c, g, t);
-        if (++c == C) {  // end of a tile
-          finish(p0 + i + u + 1);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[0][j] = 0.f;
-          ++mt;
-          c = 0;
-          seg0 = p0 + i + u + 1;
-        }
-      }
+      for (int j = 0; j < 4; ++j) acc[0][j] = 0.f;
+      ++mt;
+      c = 0;
+      seg0 = p0 + i + 1;
     }
   }
   if (seg0 < p1) finish(p1);  // this warp's run ends inside a tile
+  cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ K-split schedule (B > 4)
 template <int NT, int WFMT, int XSRC, int EPI>
 __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   using Stage = typename StageT<WFMT>::type;
-  extern __shared__ __align__(16) uint8_t smem[];
+  using R = Ring<WFMT>;
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_inv[(kWarps + 1) * MAG_MAX_BATCH];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -404,27 +459,31 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   const bool mt_ok = mt < a.n_mtiles;
   const int c0 = blockIdx.y * a.chunks_per_cta, c1 = min(c0 + a.chunks_per_cta, a.n_chunks);
   const int n = mt_ok ? c1 - c0 : 0;
+  uint8_t* ring = smem + staged_bytes(a.batch, a.chunks_per_cta) + (size_t)warp * R::kSlots * R::kSlotBytes;
 
-  Stage st[kStages];
 #pragma unroll
-  for (int u = 0; u < kStages; ++u)
-    if (u < n) load_stage(st[u], a, mt, c0 + u, lane);
+  for (int u = 0; u < R::kSlots; ++u) {
+    if (u < n) R::issue(ring + u * R::kSlotBytes, a, mt, c0 + u, lane);
+    cp_async_commit();
+  }
 
   pdl_wait();
   pdl_trigger();
   const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, c0, c1);
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  for (int i = 0; i < n; i += kStages) {
-#pragma unroll
-    for (int u = 0; u < kStages; ++u) {
-      if (i + u < n) {
-        const Stage cur = st[u];
-        if (i + u + kStages < n) load_stage(st[u], a, mt, c0 + i + u + kStages, lane);
-        compute_chunk<NT>(cur, acc, S, a.batch, c0 + i + u, g, t);
-      }
-    }
+  for (int i = 0; i < n; ++i) {
+    uint8_t* slot = ring + (i % R::kSlots) * R::kSlotBytes;
+    cp_async_wait<R::kSlots - 1>();
+    __syncwarp();
+    Stage cur;
+    read_slot(cur, slot, lane);
+    __syncwarp();
+    if (i + R::kSlots < n) R::issue(slot, a, mt, c0 + i + R::kSlots, lane);
+    cp_async_commit();
+    compute_chunk<NT>(cur, acc, S, a.batch, c0 + i, g, t);
   }
+  cp_async_wait<0>();
   if (a.ks > 1) {
     if (mt_ok) {
       float* p = a.partial + (((size_t)blockIdx.y * a.n_mtiles + mt) * 32 + lane) * (4 * NT);
@@ -482,7 +541,7 @@ cudaError_t launch_k(const Launch& L, K kern, dim3 grid, size_t smem, const Gemv
 
 template <int WFMT, int XSRC, int EPI>
 cudaError_t launch_sched(const Launch& L, const GemvArgs& a) {
-  const size_t smem = gemv_smem_bytes(a);
+  const size_t smem = gemv_smem_bytes(a, WFMT);
   if (a.streamk_blocks > 0)
     return launch_k(L, gemv_streamk_kernel<WFMT, XSRC, EPI>, dim3(a.streamk_blocks), smem, a);
   const dim3 grid((a.n_mtiles + kWarps - 1) / kWarps, a.ks);
@@ -492,9 +551,11 @@ cudaError_t launch_sched(const Launch& L, const GemvArgs& a) {
 
 }  // namespace
 
-size_t gemv_smem_bytes(const GemvArgs& a) {
+size_t gemv_smem_bytes(const GemvArgs& a, int wfmt) {
   const int nch = a.streamk_blocks > 0 ? a.n_chunks : a.chunks_per_cta;
-  return (((size_t)a.batch * (nch * 64 + 8) * 2 + 15) & ~(size_t)15) + (size_t)a.batch * (2 * nch + 2) * 4;
+  const size_t ring = wfmt == W_W4 ? (size_t)Ring<W_W4>::kSlots * Ring<W_W4>::kSlotBytes
+                                   : (size_t)Ring<W_F16>::kSlots * Ring<W_F16>::kSlotBytes;
+  return staged_bytes(a.batch, nch) + kWarps * ring;
 }
 
 int gemv_blocks_per_sm(int wfmt, int xsrc, int epi, size_t smem) {

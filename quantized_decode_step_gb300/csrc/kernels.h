@@ -53,7 +53,7 @@ struct GemvArgs {
   const StepArgs* step;
 };
 
-size_t gemv_smem_bytes(const GemvArgs& a);
+size_t gemv_smem_bytes(const GemvArgs& a, int wfmt);
 int gemv_blocks_per_sm(int wfmt, int xsrc, int epi, size_t smem);
 cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi);
 

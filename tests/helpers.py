@@ -69,12 +69,13 @@ FLOOR_FACTOR = 1.25
 
 
 def one_ulp_floor(run_oracle, x_f16, n=3):
-    """Mean rel-L2 change of the oracle's output when one input element moves by one fp16 ulp."""
+    """Mean rel-L2 change of the oracle's output when one input element of every token row moves by one
+    fp16 ulp (each row is an independent sequence, so each gets its own perturbation)."""
     base = run_oracle(x_f16)
     vals = []
     for i in range(n):
-        x2 = x_f16.copy()
-        flat = x2.reshape(-1).view(np.uint16)
-        flat[(977 * i + 101) % flat.size] += 1
-        vals.append(rel_l2(run_oracle(x2), base))
+        x2 = np.array(x_f16, copy=True).reshape(-1, x_f16.shape[-1])
+        rows = x2.view(np.uint16)
+        rows[:, (977 * i + 101) % rows.shape[1]] += 1
+        vals.append(rel_l2(run_oracle(x2.reshape(x_f16.shape)), base))
     return float(np.mean(vals)), base
