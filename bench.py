@@ -268,6 +268,9 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(local)
     mag.build()
     wl = workload_by_name(args.workload, args.seed)
+    if args.layers:
+        from dataclasses import replace as _replace
+        wl = _replace(wl, name=wl.name + f"-{args.layers}layers", shape=shrink(wl.shape, n_layers=args.layers))
     shape = wl.shape
     n_runs = args.warmup + args.steps
     e2e_steps = max(3, min(args.steps, 10))
@@ -411,6 +414,8 @@ def main():
     ap.add_argument("--workload", default=DECODE_8B.name)
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: the same per-layer shapes with fewer layers (not a bench configuration)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     world, rank, local = dist_setup()
