@@ -375,9 +375,17 @@ __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
   const int n = (int)(p1 - p0);
   uint8_t* ring = smem + staged_bytes(a.batch, C) + (size_t)warp * R::kSlots * R::kSlotBytes;
 
+  // (imt, ic): the next pair to copy into the ring, advanced incrementally
+  int imt = (int)(p0 / C), ic = (int)(p0 - (int64_t)imt * C);
 #pragma unroll
   for (int u = 0; u < R::kSlots; ++u) {
-    if (u < n) R::issue(ring + u * R::kSlotBytes, a, (int)((p0 + u) / C), (int)((p0 + u) % C), lane);
+    if (u < n) {
+      R::issue(ring + u * R::kSlotBytes, a, imt, ic, lane);
+      if (++ic == C) {
+        ic = 0;
+        ++imt;
+      }
+    }
     cp_async_commit();
   }
 
@@ -420,16 +428,21 @@ __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
     if (lane == 0) a.counters[mt] = 0;
   };
 
+  int si = 0;  // ring slot of chunk i
   for (int i = 0; i < n; ++i) {
-    uint8_t* slot = ring + (i % R::kSlots) * R::kSlotBytes;
+    uint8_t* slot = ring + si * R::kSlotBytes;
+    if (++si == R::kSlots) si = 0;
     cp_async_wait<R::kSlots - 1>();
     __syncwarp();
     Stage cur;
     read_slot(cur, slot, lane);
     __syncwarp();
     if (i + R::kSlots < n) {
-      const int64_t q = p0 + i + R::kSlots;
-      R::issue(slot, a, (int)(q / C), (int)(q % C), lane);
+      R::issue(slot, a, imt, ic, lane);
+      if (++ic == C) {
+        ic = 0;
+        ++imt;
+      }
     }
     cp_async_commit();
     compute_chunk<1>(cur, acc, S, a.batch, c, g, t);
@@ -472,8 +485,10 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, c0, c1);
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  int si = 0;
   for (int i = 0; i < n; ++i) {
-    uint8_t* slot = ring + (i % R::kSlots) * R::kSlotBytes;
+    uint8_t* slot = ring + si * R::kSlotBytes;
+    if (++si == R::kSlots) si = 0;
     cp_async_wait<R::kSlots - 1>();
     __syncwarp();
     Stage cur;
