@@ -126,22 +126,22 @@ struct StageT<W_F16> {
 };
 
 // The 8 codes of a word (k0 in bits 0-3 ... k7 in bits 28-31) as exact fp16
-// integers, paired (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+// values code * 2^-20, paired (k0,k4) (k1,k5) (k2,k6) (k3,k7): each pair is the
+// word masked so that its two nibbles land in bits 4-7 and 20-23, i.e. in the
+// mantissa of an fp16 subnormal (16 * code <= 240 units of 2^-24). Integer
+// shifts and masks only; the tensor cores take the subnormals as they are.
 struct Q4 {
   uint32_t e0, e1, e2, e3;
 };
 __device__ __forceinline__ Q4 codes_word(uint32_t w) {
-  const __half2 k1024 = __float2half2_rn(1024.0f);
-  const __half2 k1_16 = __float2half2_rn(0.0625f);
-  const __half2 km64 = __float2half2_rn(-64.0f);
-  const uint32_t w2 = w >> 8;
   Q4 q;
-  q.e0 = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w, 0x000F000Fu, 0x64006400u)), k1024));
-  q.e1 = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w, 0x00F000F0u, 0x64006400u)), k1_16, km64));
-  q.e2 = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w2, 0x000F000Fu, 0x64006400u)), k1024));
-  q.e3 = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w2, 0x00F000F0u, 0x64006400u)), k1_16, km64));
+  q.e0 = (w << 4) & 0x00F000F0u;
+  q.e1 = w & 0x00F000F0u;
+  q.e2 = (w >> 4) & 0x00F000F0u;
+  q.e3 = (w >> 8) & 0x00F000F0u;
   return q;
 }
+constexpr float kCodeUnit = 1048576.0f;  // 2^20: undoes the code scaling of codes_word
 
 // Shared-memory staging of one block: B token rows of `xrow` halves (the
 // block's k-range in W4 unit order or natural order) followed by the group
@@ -152,56 +152,61 @@ struct Staged {
   int xrow, grow, c0;  // c0: first chunk of the staged range
 };
 
-// acc += scale * (q . x) + min * X_g for rows g (acc[0..1]) and g + 8 (acc[2..3]).
-__device__ __forceinline__ void fma_group(float (&acc)[4], const float (&aq)[4], uint32_t sm_g, uint32_t sm_g8,
-                                          float x_lo, float x_hi, bool one_tok) {
-  const float2 fg = __half22float2(u32_as_h2(sm_g)), fv = __half22float2(u32_as_h2(sm_g8));
-  acc[0] = fmaf(fg.x, aq[0], fmaf(fg.y, x_lo, acc[0]));
-  acc[2] = fmaf(fv.x, aq[2], fmaf(fv.y, x_lo, acc[2]));
-  if (!one_tok) {
-    acc[1] = fmaf(fg.x, aq[1], fmaf(fg.y, x_hi, acc[1]));
-    acc[3] = fmaf(fv.x, aq[3], fmaf(fv.y, x_hi, acc[3]));
-  }
-}
-
+// Per lane and n-tile: acc[0..3] collects scale * (codes . x) (in units of
+// 2^-20) and acc[4..7] min * X_g, for (row g, token 2t), (row g, 2t+1),
+// (row g+8, 2t), (row g+8, 2t+1).
 template <int NT>
-__device__ __forceinline__ void compute_chunk(const W4Stage& st, float (&acc)[2][4], const Staged& S, int B, int c,
-                                              int g, int t) {
-  const int cl = c - S.c0;
-#pragma unroll
-  for (int grp = 0; grp < 2; ++grp) {
-    const Q4 qg = codes_word(grp ? st.code.y : st.code.x);
-    const Q4 qv = codes_word(grp ? st.code.w : st.code.z);
-    const uint32_t smg = grp ? st.sm.y : st.sm.x, smv = grp ? st.sm.w : st.sm.z;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int tok = g + 8 * nt;
-      uint4 xb = make_uint4(0, 0, 0, 0);
-      if (tok < B) xb = reinterpret_cast<const uint4*>(S.x + (size_t)tok * S.xrow)[8 * cl + 4 * grp + t];
-      float aq[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(aq, qg.e0, qv.e0, qg.e1, qv.e1, xb.x, xb.y);
-      mma_16816(aq, qg.e2, qv.e2, qg.e3, qv.e3, xb.z, xb.w);
-      const int t0 = 8 * nt + 2 * t;  // this lane's C columns: tokens t0, t0 + 1
-      const float xlo = t0 < B ? S.xs[(size_t)t0 * S.grow + 2 * cl + grp] : 0.f;
-      const float xhi = t0 + 1 < B ? S.xs[(size_t)(t0 + 1) * S.grow + 2 * cl + grp] : 0.f;
-      fma_group(acc[nt], aq, smg, smv, xlo, xhi, B == 1);
-    }
-  }
-}
-
-template <int NT>
-__device__ __forceinline__ void compute_chunk(const F16Stage& st, float (&acc)[2][4], const Staged& S, int B, int c,
+__device__ __forceinline__ void compute_chunk(const W4Stage& st, float (&acc)[2][8], const Staged& S, int B, int c,
                                               int g, int t) {
   const int cl = c - S.c0;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int tok = g + 8 * nt;
-    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-    if (tok < B) {
-      const uint4* p = reinterpret_cast<const uint4*>(S.x + (size_t)tok * S.xrow);
-      x0 = p[8 * cl + 2 * t];
-      x1 = p[8 * cl + 2 * t + 1];
+    // columns past the batch read a valid row and are discarded
+    const int tok = min(g + 8 * nt, B - 1);
+    const int t0 = min(8 * nt + 2 * t, B - 1), t1 = min(8 * nt + 2 * t + 1, B - 1);
+    const uint4* xr = reinterpret_cast<const uint4*>(S.x + (size_t)tok * S.xrow) + 8 * cl + t;
+    const float2 X0 = reinterpret_cast<const float2*>(S.xs + (size_t)t0 * S.grow)[cl];
+    const float2 X1 = reinterpret_cast<const float2*>(S.xs + (size_t)t1 * S.grow)[cl];
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const Q4 qg = codes_word(grp ? st.code.y : st.code.x);
+      const Q4 qv = codes_word(grp ? st.code.w : st.code.z);
+      const uint4 xb = xr[4 * grp];
+      float aq[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816(aq, qg.e0, qv.e0, qg.e1, qv.e1, xb.x, xb.y);
+      mma_16816(aq, qg.e2, qv.e2, qg.e3, qv.e3, xb.z, xb.w);
+      const float2 fg = __half22float2(u32_as_h2(grp ? st.sm.y : st.sm.x));
+      const float2 fv = __half22float2(u32_as_h2(grp ? st.sm.w : st.sm.z));
+      const float xs0 = grp ? X0.y : X0.x, xs1 = grp ? X1.y : X1.x;
+      acc[nt][0] = fmaf(fg.x, aq[0], acc[nt][0]);
+      acc[nt][4] = fmaf(fg.y, xs0, acc[nt][4]);
+      acc[nt][2] = fmaf(fv.x, aq[2], acc[nt][2]);
+      acc[nt][6] = fmaf(fv.y, xs0, acc[nt][6]);
+      if (B > 1) {
+        acc[nt][1] = fmaf(fg.x, aq[1], acc[nt][1]);
+        acc[nt][5] = fmaf(fg.y, xs1, acc[nt][5]);
+        acc[nt][3] = fmaf(fv.x, aq[3], acc[nt][3]);
+        acc[nt][7] = fmaf(fv.y, xs1, acc[nt][7]);
+      }
     }
+  }
+}
+
+// The four results of an n-tile: W4 parts combined (2^20 undoes the code scaling).
+__device__ __forceinline__ void tile_result(const float (&a)[8], float (&r)[4], int wfmt) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[i] = wfmt == W_W4 ? fmaf(a[i], kCodeUnit, a[i + 4]) : a[i];
+}
+
+template <int NT>
+__device__ __forceinline__ void compute_chunk(const F16Stage& st, float (&acc)[2][8], const Staged& S, int B, int c,
+                                              int g, int t) {
+  const int cl = c - S.c0;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int tok = min(g + 8 * nt, B - 1);  // columns past the batch read a valid row and are discarded
+    const uint4* p = reinterpret_cast<const uint4*>(S.x + (size_t)tok * S.xrow);
+    const uint4 x0 = p[8 * cl + 2 * t], x1 = p[8 * cl + 2 * t + 1];
     mma_16816(acc[nt], st.g0.x, st.h0.x, st.g0.y, st.h0.y, x0.x, x0.y);
     mma_16816(acc[nt], st.g0.z, st.h0.z, st.g0.w, st.h0.w, x0.z, x0.w);
     mma_16816(acc[nt], st.g1.x, st.h1.x, st.g1.y, st.h1.y, x1.x, x1.y);
@@ -393,20 +398,22 @@ __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
   pdl_trigger();
   const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, 0, C);
 
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float acc[2][8] = {};
   int mt = (int)(p0 / C), c = (int)(p0 % C);
   int64_t seg0 = p0;
   // finish the tile mt with this warp's part [seg0, seg1) of its pairs
   auto finish = [&](int64_t seg1) {
     const int64_t t0 = (int64_t)mt * C, t1 = t0 + C;
+    float res[2][4];
+    tile_result(acc[0], res[0], WFMT);
     if (seg0 == t0 && seg1 == t1) {
-      epilogue_tile<1, EPI>(a, mt, acc, lane);
+      epilogue_tile<1, EPI>(a, mt, res, lane);
       return;
     }
     // part of a tile: publish it; the last warp of the tile adds the parts in warp order
     const int slot = p0 >= t0 ? 0 : 1;
     float* part = a.partial + ((w * 2 + slot) * 32 + lane) * 4;
-    *reinterpret_cast<float4*>(part) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    *reinterpret_cast<float4*>(part) = make_float4(res[0][0], res[0][1], res[0][2], res[0][3]);
     __threadfence();
     __syncwarp();
     const int64_t w_first = t0 / Q, w_last = (t1 - 1) / Q;
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
     if (++c == C) {  // end of a tile
       finish(p0 + i + 1);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[0][j] = 0.f;
+      for (int j = 0; j < 8; ++j) acc[0][j] = 0.f;
       ++mt;
       c = 0;
       seg0 = p0 + i + 1;
@@ -484,7 +491,7 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   pdl_trigger();
   const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, c0, c1);
 
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float acc8[2][8] = {};
   int si = 0;
   for (int i = 0; i < n; ++i) {
     uint8_t* slot = ring + si * R::kSlotBytes;
@@ -496,9 +503,12 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
     __syncwarp();
     if (i + R::kSlots < n) R::issue(slot, a, mt, c0 + i + R::kSlots, lane);
     cp_async_commit();
-    compute_chunk<NT>(cur, acc, S, a.batch, c0 + i, g, t);
+    compute_chunk<NT>(cur, acc8, S, a.batch, c0 + i, g, t);
   }
   cp_async_wait<0>();
+  float acc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) tile_result(acc8[nt], acc[nt], WFMT);
   if (a.ks > 1) {
     if (mt_ok) {
       float* p = a.partial + (((size_t)blockIdx.y * a.n_mtiles + mt) * 32 + lane) * (4 * NT);
