@@ -70,6 +70,7 @@ struct mag_ctx {
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   int device = 0, n_sm = 0;
+  int attn_cluster_max = 1;
   std::string err;
   int L = 0, D = 0, Hq = 0, Hkv = 0, d = 0, F = 0, V = 0, R = 0, G = 0, B_max = 0;
   int table_stride = 0;
@@ -102,19 +103,15 @@ struct mag_ctx {
   std::vector<ArenaTensor> plan;
   float* r = nullptr;
   __half* qkv = nullptr;
-  float* part_ml = nullptr;
-  float* part_o = nullptr;
   __half* o = nullptr;
   float* ss_part = nullptr;
   __half* act = nullptr;
   float* gemv_part = nullptr;
   int sk_blocks[5][5] = {};  // Stream-K blocks per projection kind (QKV, O, GU, DOWN, LM) and batch 1..4
-  int attn_split_max = 0;
 
   // counters (zero between launches) and step arguments
   uint32_t* d_counters = nullptr;
   size_t n_counters = 0;
-  uint32_t* d_attn_counters = nullptr;
   StepArgs* d_args = nullptr;
   StepArgs* h_ring = nullptr;
   cudaEvent_t ring_ev[kRing] = {};
@@ -173,9 +170,11 @@ GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
   return p;
 }
 
+// Splits of one (session, KV head): the blocks of one thread-block cluster, so at
+// most the largest cluster the device co-schedules (16 on a full GPU).
 int attn_splits(const mag_ctx* c, int B) {
   int s = (2 * c->n_sm + B * c->Hkv - 1) / (B * c->Hkv);
-  return std::max(1, std::min(s, 64));
+  return std::max(1, std::min(s, c->attn_cluster_max));
 }
 
 int64_t kv_data_bytes(int d, int dt) { return dt == 0 ? 2 * d : (dt == 1 ? d : d / 2); }
@@ -257,9 +256,6 @@ void plan_streamk(mag_ctx* c) {
 // reused by every layer); 6 LM head.
 void build_decode_plan(mag_ctx* c) {
   const int B = c->B_max;
-  int S = 0;
-  for (int b = 1; b <= B; ++b) S = std::max(S, attn_splits(c, b) * b);
-  c->attn_split_max = S;  // splits x batch rows, the partial buffers' capacity
   size_t part = 0;
   for (int b = 1; b <= B; ++b) part = std::max(part, gemv_partial_floats(c, b));
   auto T = [](const char* n, uint64_t sz, int f, int l) { return ArenaTensor{n, sz, f, l, 0}; };
@@ -267,8 +263,6 @@ void build_decode_plan(mag_ctx* c) {
   c->plan.push_back(T("residual", (uint64_t)B * c->D * 4, 0, 6));
   c->plan.push_back(T("sumsq_part", (uint64_t)(c->D / 16) * MAG_MAX_BATCH * 4, 0, 6));
   c->plan.push_back(T("qkv", (uint64_t)B * c->R * 2, 1, 2));
-  c->plan.push_back(T("attn_part_ml", (uint64_t)S * c->Hkv * c->G * 2 * 4, 2, 2));
-  c->plan.push_back(T("attn_part_o", (uint64_t)S * c->Hkv * c->G * c->d * 4, 2, 2));
   c->plan.push_back(T("attn_out", (uint64_t)B * c->Hq * c->d * 2, 2, 3));
   c->plan.push_back(T("ffn_act", (uint64_t)B * c->F * 2, 4, 5));
   if (part) c->plan.push_back(T("gemv_partial", part * 4, 1, 6));
@@ -348,9 +342,6 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
       a.head_dim = c->d;
       a.layer = l;
       a.n_split = S;
-      a.part_ml = c->part_ml;
-      a.part_o = c->part_o;
-      a.counters = c->d_attn_counters;
       a.pool = pg;
       a.step = c->d_args;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
@@ -401,7 +392,6 @@ void free_ctx(mag_ctx* c) {
   cudaFree(c->d_sin);
   cudaFree(c->arena);
   cudaFree(c->d_counters);
-  cudaFree(c->d_attn_counters);
   cudaFree(c->d_args);
   cudaFree(c->d_in_stage);
   cudaFree(c->d_out_stage);
@@ -473,6 +463,10 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     return bail(MAG_ERR_CUDA);
   }
   cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, c->device);
+  if ((e = attention_max_cluster(cfg->head_dim, cfg->kv_dtype, &c->attn_cluster_max)) != cudaSuccess) {
+    fail(c, MAG_ERR_CUDA, "attention cluster query: %s", cudaGetErrorString(e));
+    return bail(MAG_ERR_CUDA);
+  }
   if (cuda_stream) {
     c->stream = (cudaStream_t)cuda_stream;
   } else {
@@ -591,8 +585,6 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   c->r = (float*)arena_ptr(c, "residual");
   c->ss_part = (float*)arena_ptr(c, "sumsq_part");
   c->qkv = (__half*)arena_ptr(c, "qkv");
-  c->part_ml = (float*)arena_ptr(c, "attn_part_ml");
-  c->part_o = (float*)arena_ptr(c, "attn_part_o");
   c->o = (__half*)arena_ptr(c, "attn_out");
   c->act = (__half*)arena_ptr(c, "ffn_act");
   c->gemv_part = (float*)arena_ptr(c, "gemv_partial");
@@ -600,9 +592,8 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   // ---- counters, step arguments, staging
   size_t nc = gemv_counters(c);
   c->n_counters = nc;
-  size_t ac = (size_t)c->B_max * c->Hkv;
   size_t stage_out = (size_t)c->B_max * (c->V ? c->V : c->D) * 2;
-  if (cudaMalloc(&c->d_counters, nc * 4) != cudaSuccess || cudaMalloc(&c->d_attn_counters, ac * 4) != cudaSuccess ||
+  if (cudaMalloc(&c->d_counters, nc * 4) != cudaSuccess ||
       cudaMalloc(&c->d_args, sizeof(StepArgs)) != cudaSuccess ||
       cudaMalloc(&c->d_in_stage, (size_t)c->B_max * c->D * 2) != cudaSuccess ||
       cudaMalloc(&c->d_out_stage, stage_out) != cudaSuccess ||
@@ -611,9 +602,8 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     return bail(MAG_ERR_OOM);
   }
   cudaMemsetAsync(c->d_counters, 0, nc * 4, c->stream);
-  cudaMemsetAsync(c->d_attn_counters, 0, ac * 4, c->stream);
   for (auto& ev : c->ring_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-  c->other_bytes += nc * 4 + ac * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
+  c->other_bytes += nc * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
   if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
     fail(c, MAG_ERR_CUDA, "create: %s", cudaGetErrorString(e));
     return bail(MAG_ERR_CUDA);

@@ -15,8 +15,12 @@
 // are exact small integers whose scale is folded into the scores and the
 // probabilities; INT4 codes are dequantised with scale and min). The softmax
 // is the online (running-max) form, in exp2 with log2(e) folded into the
-// score scale. Split partials (m, l, o) are merged in split order by the
-// last block of each (session, KV head) to arrive.
+// score scale. The blocks of one (session, KV head) form a thread-block
+// cluster; each streams its share of the pool blocks through a per-warp
+// cp.async ring in shared memory, and the cluster merges its split partials
+// (m, l, o) through distributed shared memory.
+#include <cooperative_groups.h>
+
 #include "kernels.h"
 
 namespace mag {
@@ -142,20 +146,48 @@ __device__ __forceinline__ int v_slot_dim(int n) {
   return (n & 8) + ((n & 7) >> 1) + 4 * (n & 1);
 }
 
-// K slab (32 dims) of one token for lane t: 4 half2 = b0/b1 of k-steps 2s and 2s+1.
-template <int DT>
-__device__ __forceinline__ uint4 load_k_slab(const PoolGeom& P, const uint8_t* row, const uint8_t* meta, int s, int t) {
-  if (DT == 0) return *reinterpret_cast<const uint4*>(row + (32 * s + 8 * t) * 2);
-  if (DT == 1) {
-    uint2 w = *reinterpret_cast<const uint2*>(row + 32 * s + 8 * t);
-    uint4 o;
-    i8x4_to_h2(w.x, o.x, o.y);
-    i8x4_to_h2(w.y, o.z, o.w);
-    return o;
+// ---------------------------------------------------------------- attention
+// Shared-memory image of one (block, KV head): K data [16][db], V data [16][db],
+// K meta [16][mb], V meta [16][mb], each region 16-byte aligned.
+template <int D, int DT>
+struct SlotGeom {
+  static constexpr int kDb = DT == 0 ? 2 * D : (DT == 1 ? D : D / 2);     // bytes per K or V vector
+  static constexpr int kMb = DT == 0 ? 0 : (DT == 1 ? 2 : (D / 32) * 4);  // meta bytes per vector
+  static constexpr int kData = 16 * kDb;
+  static constexpr int kMeta = ((16 * kMb) + 15) / 16 * 16;
+  static constexpr int kBytes = 2 * kData + 2 * kMeta;
+};
+
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Copy one (block, KV head) of the pool into a slot (the 32 lanes of a warp, 16 bytes each).
+template <int D, int DT>
+__device__ __forceinline__ void issue_block(uint8_t* slot, const PoolGeom& P, int layer, int phys, int gk, int lane) {
+  using SG = SlotGeom<D, DT>;
+  const uint8_t* kd = pool_vec(P, layer, phys, 0, gk, 0);
+  const uint8_t* vd = pool_vec(P, layer, phys, 1, gk, 0);
+#pragma unroll
+  for (int o = lane * 16; o < SG::kData; o += 512) {
+    cp_async16(slot + o, kd + o);
+    cp_async16(slot + SG::kData + o, vd + o);
   }
-  uint32_t w = *reinterpret_cast<const uint32_t*>(row + 16 * s + 4 * t);
-  __half2 sm = *reinterpret_cast<const __half2*>(meta + 4 * s);
-  return u4x8_to_h2(w, sm);
+  if (DT != 0) {
+    const uint8_t* km = pool_vec(P, layer, phys, 2, gk, 0);
+    const uint8_t* vm = pool_vec(P, layer, phys, 3, gk, 0);
+    constexpr int mbytes = 16 * SG::kMb;
+    for (int o = lane * 16; o < mbytes; o += 512) {
+      cp_async16(slot + 2 * SG::kData + o, km + o);
+      cp_async16(slot + 2 * SG::kData + SG::kMeta + o, vm + o);
+    }
+  }
 }
 
 // V dims of lane group gi for one token: NV halves as NV/2 words, slot order.
@@ -166,7 +198,7 @@ __device__ __forceinline__ void load_v_row(const uint8_t* row, const uint8_t* me
     const uint4* p = reinterpret_cast<const uint4*>(row + gi * NV * 2);
 #pragma unroll
     for (int j = 0; j < NV / 8; ++j) {
-      uint4 v = p[j];
+      const uint4 v = p[j];
       out[4 * j + 0] = v.x;
       out[4 * j + 1] = v.y;
       out[4 * j + 2] = v.z;
@@ -178,10 +210,10 @@ __device__ __forceinline__ void load_v_row(const uint8_t* row, const uint8_t* me
     for (int j = 0; j < NV / 4; ++j) i8x4_to_h2(p[j], out[2 * j], out[2 * j + 1]);
   } else {
     const uint32_t* p = reinterpret_cast<const uint32_t*>(row + gi * NV / 2);
-    __half2 sm = *reinterpret_cast<const __half2*>(meta + 4 * ((gi * NV) / 32));
+    const __half2 sm = *reinterpret_cast<const __half2*>(meta + 4 * ((gi * NV) / 32));
 #pragma unroll
     for (int j = 0; j < NV / 8; ++j) {
-      uint4 o = u4x8_to_h2(p[j], sm);
+      const uint4 o = u4x8_to_h2(p[j], sm);
       out[4 * j + 0] = o.x;
       out[4 * j + 1] = o.y;
       out[4 * j + 2] = o.z;
@@ -208,273 +240,360 @@ __device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
   return o;
 }
 
+constexpr int kAttnSlots = 2;  // per-warp ring depth, in (block, KV head) units
+
+template <int D, int DT>
+__host__ __device__ constexpr size_t attn_smem_bytes() {
+  return (size_t)4 * kAttnSlots * SlotGeom<D, DT>::kBytes;
+}
+
+// One block of the grid per (split, KV head, session); the blocks of a
+// (session, KV head) form a thread-block cluster and merge their splits
+// through distributed shared memory.
 template <int D, int DT>
 __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
+  namespace cg = cooperative_groups;
+  using SG = SlotGeom<D, DT>;
   constexpr int NS = D / 32;  // 32-dim slabs of K (one INT4 group each)
   constexpr int NV = D / 8;   // V n-tiles
   constexpr int NW = D / 16;  // words per V row of a lane
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_m[4][8], s_l[4][8];
   __shared__ float s_acc[4][8][D];
+  __shared__ float s_pm[8], s_pl[8];  // this block's partial (m, l) per head
   __shared__ __half s_kv[2][D];
   __shared__ float s_red[8];
-  __shared__ float s_cm[64][8], s_cl[64][8];
-  __shared__ int s_last;
+  __shared__ float s_w[16][8];  // merge weights of the cluster's splits
 
+  cg::cluster_group cluster = cg::this_cluster();
   const int split = blockIdx.x, gk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, t = lane & 3;
   const int Hq = a.n_heads, Hkv = a.n_kv_heads, G = Hq / Hkv;
-  pdl_wait();
-  pdl_trigger();
+  const int S = a.n_split;  // == cluster size
+  // The step's arguments were copied before the step's first kernel and the
+  // pool blocks before the new token's were written and mapped by earlier
+  // steps, so their fetch starts before waiting for the QKV projection.
   const int pos = a.step->pos[b], sess = a.step->sess[b];
-  const int n_keys = pos + 1;
-  const int n_blocks = (n_keys + 15) >> 4;
-  const int s_eff = max(1, min(a.n_split, (n_blocks + 3) >> 2));
-  const int bps = (n_blocks + s_eff - 1) / s_eff;
+  const int n_keys = pos + 1, new_blk = pos >> 4;
+  const int n_blocks = new_blk + 1;
+  const int bps = (n_blocks + S - 1) / S;
   const int blk0 = split * bps, blk1 = min(blk0 + bps, n_blocks);
   const int32_t* table = a.pool.tables + (int64_t)sess * a.pool.table_stride;
+  // this warp's blocks: blk0 + warp + 4 j; the new token's block, if it is one
+  // of them, is the last
+  const int nb = blk0 + warp < blk1 ? (blk1 - blk0 - warp + 3) / 4 : 0;
+  uint8_t* ring = smem + (size_t)warp * kAttnSlots * SG::kBytes;
+  int issued = 0;
+  for (; issued < min(nb, kAttnSlots); ++issued) {
+    const int blk = blk0 + warp + 4 * issued;
+    if (blk == new_blk) break;
+    issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, table[blk], gk, lane);
+    cp_async_commit();
+  }
+  pdl_wait();
+  pdl_trigger();
   const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
-  const int64_t pbase = (((int64_t)b * Hkv + gk) * a.n_split + split) * G;
 
-  // the block that holds the new token first appends its K (rotated) and V to the pool
-  if (blk0 <= (pos >> 4) && (pos >> 4) < blk1) {
+  // the block that holds the new token appends its K (rotated) and V to the pool
+  if (blk0 <= new_blk && new_blk < blk1) {
     if (tid < D) {
       s_kv[0][tid] = qkv[(int64_t)(Hq + gk) * D + tid];
       s_kv[1][tid] = qkv[(int64_t)(Hq + Hkv + gk) * D + tid];
     }
     __syncthreads();
-    const int phys = table[pos >> 4];
+    const int phys = table[new_blk];
     store_vec(a.pool, a.layer, phys, pos & 15, gk, 0, s_kv[0], s_red);
     store_vec(a.pool, a.layer, phys, pos & 15, gk, 1, s_kv[1], s_red);
     __threadfence_block();
     __syncthreads();
-  }
-
-  if (blk0 < blk1) {
-    // query fragments: rows = the G heads of this KV head, padded to 16 with zeros
-    uint32_t qa[2 * NS][2];
-    float qsum[NS];  // INT4: per 32-dim slab, the sum of this row's query values
-    const bool hv = gi < G;
-    const __half* qrow = qkv + (int64_t)(gk * G + (hv ? gi : 0)) * D;
-#pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      uint4 v = hv ? *reinterpret_cast<const uint4*>(qrow + 32 * s + 8 * t) : make_uint4(0, 0, 0, 0);
-      if (DT == 2) {
-        const __half* h = reinterpret_cast<const __half*>(&v);
-        float sum = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sum += __half2float(h[e]);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        qsum[s] = sum;
-        v = perm_k0k4(v);
-      }
-      qa[2 * s][0] = v.x;
-      qa[2 * s][1] = v.y;
-      qa[2 * s + 1][0] = v.z;
-      qa[2 * s + 1][1] = v.w;
+    if (issued < min(nb, kAttnSlots)) {  // this warp's deferred fetch of the new token's block
+      issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, table[new_blk], gk, lane);
+      cp_async_commit();
+      ++issued;
     }
-    const float sc = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
-    float m_run = -INFINITY, l_part = 0.f;
-    float acc[NV][4];
-#pragma unroll
-    for (int n = 0; n < NV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  }
+  for (; issued < kAttnSlots; ++issued) cp_async_commit();  // one group per ring slot
 
-    for (int blk = blk0 + warp; blk < blk1; blk += 4) {
-      const int phys = table[blk];
-      // ---- scores S[head][token] of the block's 16 tokens (two n-tiles of 8)
-      float sfr[2][4];
+  // query fragments: rows = the G heads of this KV head, padded to 16 with zeros
+  uint32_t qa[2 * NS][2];
+  float qsum[NS];  // INT4: per 32-dim slab, the sum of this row's query values
+  const bool hv = gi < G;
+  const __half* qrow = qkv + (int64_t)(gk * G + (hv ? gi : 0)) * D;
+#pragma unroll
+  for (int s = 0; s < NS; ++s) {
+    uint4 v = hv ? *reinterpret_cast<const uint4*>(qrow + 32 * s + 8 * t) : make_uint4(0, 0, 0, 0);
+    if (DT == 2) {
+      const __half* h = reinterpret_cast<const __half*>(&v);
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += __half2float(h[e]);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      qsum[s] = sum;
+      v = perm_k0k4(v);
+    }
+    qa[2 * s][0] = v.x;
+    qa[2 * s][1] = v.y;
+    qa[2 * s + 1][0] = v.z;
+    qa[2 * s + 1][1] = v.w;
+  }
+  const float sc = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
+  float m_run = -INFINITY, l_part = 0.f;
+  float acc[NV][4];
+#pragma unroll
+  for (int n = 0; n < NV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+  for (int j = 0; j < nb; ++j) {
+    const int blk = blk0 + warp + 4 * j;
+    uint8_t* slot = ring + (j & (kAttnSlots - 1)) * SG::kBytes;
+    cp_async_wait<kAttnSlots - 1>();
+    __syncwarp();
+    const uint8_t* kd = slot;
+    const uint8_t* vd = slot + SG::kData;
+    const uint8_t* km = slot + 2 * SG::kData;
+    const uint8_t* vm = km + SG::kMeta;
+    // ---- scores S[head][token] of the block's 16 tokens (two n-tiles of 8)
+    float sfr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+      const uint8_t* krow = kd + (gi + 8 * nt) * SG::kDb;
+      if (DT == 2) {
+        const uint8_t* kmeta0 = km + (8 * nt + 2 * t) * SG::kMb;
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+          const uint4 kq = u4x8_codes(*reinterpret_cast<const uint32_t*>(krow + 16 * s + 4 * t));
+          float as[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_16816(as, qa[2 * s][0], 0u, qa[2 * s][1], 0u, kq.x, kq.y);
+          mma_16816(as, qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kq.z, kq.w);
+          // per (token, group): score += s * (q . codes) + m * sum(q)
+          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + 4 * s));
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + SG::kMb + 4 * s));
+          sfr[nt][0] = fmaf(f0.x, as[0], fmaf(f0.y, qsum[s], sfr[nt][0]));
+          sfr[nt][1] = fmaf(f1.x, as[1], fmaf(f1.y, qsum[s], sfr[nt][1]));
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+          uint4 kb;
+          if (DT == 0) {
+            kb = *reinterpret_cast<const uint4*>(krow + (32 * s + 8 * t) * 2);
+          } else {
+            const uint2 w = *reinterpret_cast<const uint2*>(krow + 32 * s + 8 * t);
+            i8x4_to_h2(w.x, kb.x, kb.y);
+            i8x4_to_h2(w.y, kb.z, kb.w);
+          }
+          mma_16816(sfr[nt], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
+          mma_16816(sfr[nt], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
+        }
+      }
+    }
+    // this lane's tokens: (nt, jj) -> 16 blk + 8 nt + 2 t + jj
+    float ks[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+    if (DT == 1) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
-        const uint8_t* krow = pool_vec(a.pool, a.layer, phys, 0, gk, gi + 8 * nt);
-        if (DT == 2) {
-          const uint8_t* kmeta0 = pool_vec(a.pool, a.layer, phys, 2, gk, 8 * nt + 2 * t);
-#pragma unroll
-          for (int s = 0; s < NS; ++s) {
-            const uint4 kq = u4x8_codes(*reinterpret_cast<const uint32_t*>(krow + 16 * s + 4 * t));
-            float as[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_16816(as, qa[2 * s][0], 0u, qa[2 * s][1], 0u, kq.x, kq.y);
-            mma_16816(as, qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kq.z, kq.w);
-            // per (token, group): score += s * (q . codes) + m * sum(q)
-            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + 4 * s));
-            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + a.pool.meta_bytes + 4 * s));
-            sfr[nt][0] = fmaf(f0.x, as[0], fmaf(f0.y, qsum[s], sfr[nt][0]));
-            sfr[nt][1] = fmaf(f1.x, as[1], fmaf(f1.y, qsum[s], sfr[nt][1]));
-          }
-        } else {
-#pragma unroll
-          for (int s = 0; s < NS; ++s) {
-            uint4 kb;
-            if (DT == 0) {
-              kb = *reinterpret_cast<const uint4*>(krow + (32 * s + 8 * t) * 2);
-            } else {
-              const uint2 w = *reinterpret_cast<const uint2*>(krow + 32 * s + 8 * t);
-              i8x4_to_h2(w.x, kb.x, kb.y);
-              i8x4_to_h2(w.y, kb.z, kb.w);
-            }
-            mma_16816(sfr[nt], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
-            mma_16816(sfr[nt], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
-          }
-        }
-      }
-      // this lane's tokens: (nt, j) -> 16 blk + 8 nt + 2 t + j
-      float ks[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
-      if (DT == 1) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const __half2 k2 = *reinterpret_cast<const __half2*>(pool_vec(a.pool, a.layer, phys, 2, gk, 8 * nt + 2 * t));
-          const __half2 v2 = *reinterpret_cast<const __half2*>(pool_vec(a.pool, a.layer, phys, 3, gk, 8 * nt + 2 * t));
-          ks[nt][0] = __low2float(k2);
-          ks[nt][1] = __high2float(k2);
-          vsc[nt][0] = __low2float(v2);
-          vsc[nt][1] = __high2float(v2);
-        }
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int tok = blk * 16 + 8 * nt + 2 * t + j;
-          float v = sfr[nt][j] * ks[nt][j] * sc;
-          v = tok < n_keys ? v : -INFINITY;
-          sfr[nt][j] = v;
-          mx = fmaxf(mx, v);
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float corr = exp2f(m_run - m_new);
-      m_run = m_new;
-      float p[2][2];
-      float psum = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          p[nt][j] = exp2f(sfr[nt][j] - m_new);
-          psum += p[nt][j];
-        }
-      l_part = l_part * corr + psum;
-#pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        acc[n][0] *= corr;
-        acc[n][1] *= corr;
-      }
-      // P (times the INT8 value scale) as the A operand, split into fp16 hi + lo so the
-      // product carries no fp16 rounding of the probabilities: a0 = tokens (2t, 2t+1),
-      // a2 = tokens (8+2t, 9+2t)
-      float pv[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) pv[nt][j] = p[nt][j] * vsc[nt][j];
-      const __half2 h0 = __floats2half2_rn(pv[0][0], pv[0][1]), h2 = __floats2half2_rn(pv[1][0], pv[1][1]);
-      const float2 f0 = __half22float2(h0), f2 = __half22float2(h2);
-      const uint32_t pa0 = h2_as_u32(h0), pa2 = h2_as_u32(h2);
-      const uint32_t pl0 = h2_as_u32(__floats2half2_rn(pv[0][0] - f0.x, pv[0][1] - f0.y));
-      const uint32_t pl2 = h2_as_u32(__floats2half2_rn(pv[1][0] - f2.x, pv[1][1] - f2.y));
-      // ---- V rows of tokens 2t, 2t+1, 8+2t, 9+2t
-      uint32_t v0[NW], v1[NW], v8[NW], v9[NW];
-      load_v_row<D, DT>(pool_vec(a.pool, a.layer, phys, 1, gk, 2 * t),
-                        DT == 2 ? pool_vec(a.pool, a.layer, phys, 3, gk, 2 * t) : nullptr, gi, v0);
-      load_v_row<D, DT>(pool_vec(a.pool, a.layer, phys, 1, gk, 2 * t + 1),
-                        DT == 2 ? pool_vec(a.pool, a.layer, phys, 3, gk, 2 * t + 1) : nullptr, gi, v1);
-      load_v_row<D, DT>(pool_vec(a.pool, a.layer, phys, 1, gk, 8 + 2 * t),
-                        DT == 2 ? pool_vec(a.pool, a.layer, phys, 3, gk, 8 + 2 * t) : nullptr, gi, v8);
-      load_v_row<D, DT>(pool_vec(a.pool, a.layer, phys, 1, gk, 9 + 2 * t),
-                        DT == 2 ? pool_vec(a.pool, a.layer, phys, 3, gk, 9 + 2 * t) : nullptr, gi, v9);
-#pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        const uint32_t b0 = pair_tokens(v0, v1, n), b1 = pair_tokens(v8, v9, n);
-        mma_16816(acc[n], pa0, 0u, pa2, 0u, b0, b1);
-        mma_16816(acc[n], pl0, 0u, pl2, 0u, b0, b1);
+        const __half2 k2 = *reinterpret_cast<const __half2*>(km + (8 * nt + 2 * t) * 2);
+        const __half2 v2 = *reinterpret_cast<const __half2*>(vm + (8 * nt + 2 * t) * 2);
+        ks[nt][0] = __low2float(k2);
+        ks[nt][1] = __high2float(k2);
+        vsc[nt][0] = __low2float(v2);
+        vsc[nt][1] = __high2float(v2);
       }
     }
-    // ---- merge the 4 warps of this block
-    float l_tot = l_part;
-    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
-    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-    if (hv) {
-      if (t == 0) {
-        s_m[warp][gi] = m_run;
-        s_l[warp][gi] = l_tot;
-      }
+    float mx = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        s_acc[warp][gi][(2 * t) * NV + v_slot_dim<DT>(n)] = acc[n][0];
-        s_acc[warp][gi][(2 * t + 1) * NV + v_slot_dim<DT>(n)] = acc[n][1];
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int tok = blk * 16 + 8 * nt + 2 * t + jj;
+        float v = sfr[nt][jj] * ks[nt][jj] * sc;
+        v = tok < n_keys ? v : -INFINITY;
+        sfr[nt][jj] = v;
+        mx = fmaxf(mx, v);
       }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = exp2f(m_run - m_new);
+    m_run = m_new;
+    float p[2][2];
+    float psum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        p[nt][jj] = exp2f(sfr[nt][jj] - m_new);
+        psum += p[nt][jj];
+      }
+    l_part = l_part * corr + psum;
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+      acc[n][0] *= corr;
+      acc[n][1] *= corr;
     }
-    __syncthreads();
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
-      const int h = idx / D, dim = idx - h * D;
-      float mm = -INFINITY;
+    // P (times the INT8 value scale) as the A operand, split into fp16 hi + lo so the
+    // product carries no fp16 rounding of the probabilities: a0 = tokens (2t, 2t+1),
+    // a2 = tokens (8+2t, 9+2t)
+    float pv[2][2];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) mm = fmaxf(mm, s_m[w][h]);
-      float o = 0.f, l = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float e = exp2f(s_m[w][h] - mm);  // warps without blocks: m = -inf -> 0
-        o += s_acc[w][h][dim] * e;
-        l += s_l[w][h] * e;
-      }
-      a.part_o[(pbase + h) * D + dim] = o;
-      if (dim == 0) {
-        a.part_ml[(pbase + h) * 2 + 0] = mm;
-        a.part_ml[(pbase + h) * 2 + 1] = l;
-      }
+      for (int jj = 0; jj < 2; ++jj) pv[nt][jj] = p[nt][jj] * vsc[nt][jj];
+    const __half2 h0 = __floats2half2_rn(pv[0][0], pv[0][1]), h2 = __floats2half2_rn(pv[1][0], pv[1][1]);
+    const float2 f0 = __half22float2(h0), f2 = __half22float2(h2);
+    const uint32_t pa0 = h2_as_u32(h0), pa2 = h2_as_u32(h2);
+    const uint32_t pl0 = h2_as_u32(__floats2half2_rn(pv[0][0] - f0.x, pv[0][1] - f0.y));
+    const uint32_t pl2 = h2_as_u32(__floats2half2_rn(pv[1][0] - f2.x, pv[1][1] - f2.y));
+    // ---- V rows of tokens 2t, 2t+1, 8+2t, 9+2t
+    uint32_t v0[NW], v1[NW], v8[NW], v9[NW];
+    load_v_row<D, DT>(vd + (2 * t) * SG::kDb, vm + (2 * t) * SG::kMb, gi, v0);
+    load_v_row<D, DT>(vd + (2 * t + 1) * SG::kDb, vm + (2 * t + 1) * SG::kMb, gi, v1);
+    load_v_row<D, DT>(vd + (8 + 2 * t) * SG::kDb, vm + (8 + 2 * t) * SG::kMb, gi, v8);
+    load_v_row<D, DT>(vd + (9 + 2 * t) * SG::kDb, vm + (9 + 2 * t) * SG::kMb, gi, v9);
+    __syncwarp();
+    // the slot is free: fetch the block after next into it
+    if (j + kAttnSlots < nb)
+      issue_block<D, DT>(slot, a.pool, a.layer, table[blk + 4 * kAttnSlots], gk, lane);
+    cp_async_commit();
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+      const uint32_t b0 = pair_tokens(v0, v1, n), b1 = pair_tokens(v8, v9, n);
+      mma_16816(acc[n], pa0, 0u, pa2, 0u, b0, b1);
+      mma_16816(acc[n], pl0, 0u, pl2, 0u, b0, b1);
     }
   }
-  // ---- the last block of this (session, KV head) merges the splits in order
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.counters + (int64_t)b * Hkv + gk, 1u) == (unsigned)(a.n_split - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int n_valid = (n_blocks + bps - 1) / bps;  // splits that hold blocks
-  const int64_t base0 = (((int64_t)b * Hkv + gk) * a.n_split) * G;
-  for (int i = tid; i < n_valid * G; i += blockDim.x) {
-    const int s = i / G, h = i - s * G;
-    s_cm[s][h] = __ldcg(a.part_ml + (base0 + i) * 2);
-    s_cl[s][h] = __ldcg(a.part_ml + (base0 + i) * 2 + 1);
+  cp_async_wait<0>();
+
+  // ---- merge the 4 warps of this block into the block's partial (m, l, o)
+  float l_tot = l_part;
+  l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+  l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+  if (hv) {
+    if (t == 0) {
+      s_m[warp][gi] = m_run;
+      s_l[warp][gi] = l_tot;
+    }
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+      s_acc[warp][gi][(2 * t) * NV + v_slot_dim<DT>(n)] = acc[n][0];
+      s_acc[warp][gi][(2 * t + 1) * NV + v_slot_dim<DT>(n)] = acc[n][1];
+    }
   }
   __syncthreads();
   if (tid < G) {
     float mm = -INFINITY;
-    for (int s = 0; s < n_valid; ++s) mm = fmaxf(mm, s_cm[s][tid]);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mm = fmaxf(mm, s_m[w][tid]);
     float l = 0.f;
-    for (int s = 0; s < n_valid; ++s) l += s_cl[s][tid] * exp2f(s_cm[s][tid] - mm);
-    const float inv = 1.0f / l;
-    for (int s = 0; s < n_valid; ++s) s_cm[s][tid] = exp2f(s_cm[s][tid] - mm) * inv;  // split weights
+#pragma unroll
+    for (int w = 0; w < 4; ++w) l += s_l[w][tid] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][tid] - mm));
+    s_pm[tid] = mm;  // -inf for a block without keys
+    s_pl[tid] = l;
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, dim = idx - h * D;
-    const float* po = a.part_o + (base0 + h) * D + dim;
+    const float mm = s_pm[h];
     float o = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < n_valid; ++s) o += __ldcg(po + (int64_t)s * G * D) * s_cm[s][h];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) o += s_acc[w][h][dim] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][h] - mm));
+    s_acc[0][h][dim] = o;  // row 0 of s_acc now holds the block's partial o
+  }
+  // ---- merge the cluster's splits through distributed shared memory
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  if (tid < G) {
+    float mm = -INFINITY;
+    for (int q = 0; q < S; ++q) mm = fmaxf(mm, *cluster.map_shared_rank(&s_pm[tid], q));
+    float l = 0.f;
+    for (int q = 0; q < S; ++q) {
+      const float mq = *cluster.map_shared_rank(&s_pm[tid], q);
+      const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
+      s_w[q][tid] = e;
+      l += *cluster.map_shared_rank(&s_pl[tid], q) * e;
+    }
+    for (int q = 0; q < S; ++q) s_w[q][tid] /= l;
+  }
+  __syncthreads();
+  const int per = (G * D + S - 1) / S;  // this rank's share of the outputs
+  for (int idx = rank * per + tid; idx < min((rank + 1) * per, G * D); idx += blockDim.x) {
+    const int h = idx / D, dim = idx - h * D;
+    float o = 0.f;
+    for (int q = 0; q < S; ++q) o += *cluster.map_shared_rank(&s_acc[0][h][dim], q) * s_w[q][h];
     a.o[(int64_t)b * a.ldo + (int64_t)(gk * G + h) * D + dim] = __float2half_rn(o);
   }
-  if (tid == 0) a.counters[(int64_t)b * Hkv + gk] = 0;
+  cluster.sync();  // keep this block's shared memory alive until every rank has read it
 }
 
 template <typename K, typename Args>
-cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, size_t smem, const Args& a) {
+cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, size_t smem, const Args& a,
+                      int cluster_x = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+  int n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   if (L.counter) ++*L.counter;
   return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int D, int DT>
+cudaError_t attn_prepare() {
+  auto kern = attn_kernel<D, DT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes<D, DT>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+template <int D, int DT>
+cudaError_t launch_attn_t(const Launch& L, const AttnArgs& a, int batch) {
+  cudaError_t e = attn_prepare<D, DT>();
+  if (e != cudaSuccess) return e;
+  return launch_ex(L, attn_kernel<D, DT>, dim3(a.n_split, a.n_kv_heads, batch), dim3(128), attn_smem_bytes<D, DT>(),
+                   a, a.n_split);
+}
+
+// Largest cluster size (16, 8, 4, 2, 1) of which at least one cluster fits on the device.
+template <int D, int DT>
+cudaError_t attn_max_cluster_t(int* out) {
+  cudaError_t e = attn_prepare<D, DT>();
+  if (e != cudaSuccess) return e;
+  for (int s = 16; s >= 1; s /= 2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s, 1, 1);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = attn_smem_bytes<D, DT>();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = s;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, attn_kernel<D, DT>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n >= 1) {
+      *out = s;
+      return cudaSuccess;
+    }
+  }
+  *out = 0;
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace
@@ -484,18 +603,32 @@ cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a) {
   return launch_ex(L, kv_store_kernel, dim3(a.n_tok, a.pool.n_kv_heads, a.n_layers), dim3(a.pool.head_dim), 0, a);
 }
 
+cudaError_t attention_max_cluster(int head_dim, int kv_dtype, int* out) {
+  if (head_dim == 128) {
+    if (kv_dtype == 0) return attn_max_cluster_t<128, 0>(out);
+    if (kv_dtype == 1) return attn_max_cluster_t<128, 1>(out);
+    return attn_max_cluster_t<128, 2>(out);
+  }
+  if (head_dim == 64) {
+    if (kv_dtype == 0) return attn_max_cluster_t<64, 0>(out);
+    if (kv_dtype == 1) return attn_max_cluster_t<64, 1>(out);
+    return attn_max_cluster_t<64, 2>(out);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch) {
-  dim3 grid(a.n_split, a.n_kv_heads, batch), block(128);
   const int dt = a.pool.kv_dtype;
+  if (a.n_split < 1 || a.n_split > 16) return cudaErrorInvalidValue;
   if (a.head_dim == 128) {
-    if (dt == 0) return launch_ex(L, attn_kernel<128, 0>, grid, block, 0, a);
-    if (dt == 1) return launch_ex(L, attn_kernel<128, 1>, grid, block, 0, a);
-    return launch_ex(L, attn_kernel<128, 2>, grid, block, 0, a);
+    if (dt == 0) return launch_attn_t<128, 0>(L, a, batch);
+    if (dt == 1) return launch_attn_t<128, 1>(L, a, batch);
+    return launch_attn_t<128, 2>(L, a, batch);
   }
   if (a.head_dim == 64) {
-    if (dt == 0) return launch_ex(L, attn_kernel<64, 0>, grid, block, 0, a);
-    if (dt == 1) return launch_ex(L, attn_kernel<64, 1>, grid, block, 0, a);
-    return launch_ex(L, attn_kernel<64, 2>, grid, block, 0, a);
+    if (dt == 0) return launch_attn_t<64, 0>(L, a, batch);
+    if (dt == 1) return launch_attn_t<64, 1>(L, a, batch);
+    return launch_attn_t<64, 2>(L, a, batch);
   }
   return cudaErrorInvalidValue;
 }

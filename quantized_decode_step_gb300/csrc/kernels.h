@@ -92,14 +92,13 @@ struct AttnArgs {
   int32_t ldo;
   int32_t n_heads, n_kv_heads, head_dim;
   int32_t layer;
-  int32_t n_split;  // grid.x (<= 64)
-  float* part_ml;   // [B][Hkv][n_split][G][2]
-  float* part_o;    // [B][Hkv][n_split][G][d]
-  uint32_t* counters;  // [B][Hkv]
+  int32_t n_split;  // grid.x = cluster size (<= 16)
   PoolGeom pool;
   const StepArgs* step;
 };
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch);
+// Largest split count (cluster size) the device can co-schedule for this head size and KV type.
+cudaError_t attention_max_cluster(int head_dim, int kv_dtype, int* out);
 
 // ---------------------------------------------------------------- W4 quantiser (load time)
 cudaError_t launch_quantize_w4g32(cudaStream_t s, const float* src, int64_t rows, int64_t cols, uint8_t* codes,
