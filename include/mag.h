@@ -129,6 +129,28 @@ typedef enum {
 mag_status mag_load_weights(mag_ctx* ctx, int32_t tensor, int32_t layer, const void* src_dev, int32_t src_format,
                             size_t bytes);
 
+/* Load one fp32 projection (MAG_W_QKV..MAG_W_DOWN; [N, K] row-major, bytes =
+ * N*K*4, device memory) like mag_load_weights with MAG_FMT_F32_DENSE, to the
+ * same bytes, but without allocating device memory. The pages have no
+ * counterpart: it is for callers that cannot allocate at load time -- a
+ * process whose KV pool was sized to take the HBM left after the weights, or
+ * one that forbids device allocation after start-up -- where the ordinary
+ * path's transient W4G32 copy of the whole projection (up to N*K*5/8 bytes)
+ * would fail. The projection goes through one 4 MiB scratch buffer that is part
+ * of the library image, one per device, in slabs of whole 16-row tiles
+ * (QKV: whole heads); nothing in the scratch needs to start at zero.
+ * A tile of rows of K values takes 16 * ceil(K/32) * 20 bytes: a projection
+ * whose smallest slab (one tile; QKV: one head of d/16 tiles) exceeds 4 MiB
+ * -- K above 419,424; QKV K above 52,416 (d = 128) or 104,816 (d = 64) -- is
+ * rejected with INVALID_ARG. The context's device must be current. The first call on each
+ * device looks the scratch's address up; make it before any stream capture
+ * begins. Ordered on the context's stream; src_dev may be reused once the
+ * stream reaches this point. Calls that overlap in time on one device (other
+ * streams, threads or contexts) race on the shared scratch: order them.
+ * Errors: INVALID_ARG (id, layer, size, scratch limit, device), CUDA. */
+mag_status mag_load_weights_f32_noalloc(mag_ctx* ctx, int32_t tensor, int32_t layer, const void* src_dev,
+                                        size_t bytes);
+
 /* Sessions: each holds its own block table and length. Close returns its
  * blocks to the back of the free list. Errors: INVALID_ARG, and OOM-like
  * MAG_ERR_INVALID_ARG when max_sessions are open. */

@@ -25,7 +25,7 @@ FMT_F32_DENSE, FMT_W4G32, FMT_F16 = 0, 1, 2
 FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL = 1, 2, 4
 
 EXPORTED = [
-    "mag_create", "mag_destroy", "mag_load_weights", "mag_session_open", "mag_session_close", "mag_session_length",
+    "mag_create", "mag_destroy", "mag_load_weights", "mag_load_weights_f32_noalloc", "mag_session_open", "mag_session_close", "mag_session_length",
     "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk", "mag_sync",
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
@@ -83,6 +83,7 @@ def lib():
                 "mag_create": ([ctypes.POINTER(Config), vp, ctypes.POINTER(vp)], i32),
                 "mag_destroy": ([vp], None),
                 "mag_load_weights": ([vp, i32, i32, vp, i32, sz], i32),
+                "mag_load_weights_f32_noalloc": ([vp, i32, i32, vp, sz], i32),
                 "mag_session_open": ([vp, P32], i32),
                 "mag_session_close": ([vp, i32], i32),
                 "mag_session_length": ([vp, i32, P32], i32),
@@ -177,6 +178,11 @@ class Context:
 
     def load_weights(self, tensor, layer, src, fmt, nbytes):
         self._check(lib().mag_load_weights(self.h, tensor, layer, _ptr(src), fmt, nbytes), "mag_load_weights")
+
+    def load_weights_f32_noalloc(self, tensor, layer, src, nbytes):
+        """fp32 projection load through the library's fixed per-device scratch (no device allocation)."""
+        self._check(lib().mag_load_weights_f32_noalloc(self.h, tensor, layer, _ptr(src), nbytes),
+                    "mag_load_weights_f32_noalloc")
 
     def session_open(self) -> int:
         sid = ctypes.c_int32()

@@ -12,6 +12,7 @@
 
 #include "arena.h"
 #include "kernels.h"
+#include "noalloc.h"
 #include "mag.h"
 
 using namespace mag;
@@ -674,6 +675,30 @@ mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const voi
   CUDA_TRY(c, cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
   if (tensor == MAG_NORM_FINAL) c->loaded[(size_t)c->L * 6] = 1;
   else c->loaded[(size_t)layer * 6 + tensor] = 1;
+  return MAG_OK;
+}
+
+mag_status mag_load_weights_f32_noalloc(mag_ctx* c, int32_t tensor, int32_t layer, const void* src, size_t bytes) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!src) return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: null source");
+  if (tensor < MAG_W_QKV || tensor > MAG_W_DOWN)
+    return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: tensor %d is not a projection", tensor);
+  if (layer < 0 || layer >= c->L) return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: bad layer %d", layer);
+  Proj& p = c->proj[(size_t)layer * 4 + tensor];
+  if (bytes != (size_t)p.N * p.K * 4)
+    return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: %zu bytes, expected fp32 [%d, %d]", bytes, p.N,
+                p.K);
+  if (noalloc_slab_tiles(p.K, p.map, p.map_arg) == 0)
+    return fail(c, MAG_ERR_INVALID_ARG,
+                "load_weights_f32_noalloc: rows of %d values need more than the %zu-byte scratch per slab", p.K,
+                kNoAllocScratchBytes);
+  int dev = -1;
+  CUDA_TRY(c, cudaGetDevice(&dev));
+  if (dev != c->device)
+    return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: make the context's device %d current (not %d)",
+                c->device, dev);
+  CUDA_TRY(c, load_f32_noalloc(c->stream, (const float*)src, p.N, p.K, p.map, p.map_arg, p.tiles));
+  c->loaded[(size_t)layer * 6 + tensor] = 1;
   return MAG_OK;
 }
 
