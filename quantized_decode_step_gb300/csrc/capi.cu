@@ -36,7 +36,9 @@ struct Session {
 };
 
 struct GemvPlan {
-  int streamk_blocks, ks, cpc;
+  int n_cta, stages, t_max;  // pipelined kernel (batch <= kPipeMaxBatch); n_cta = 0 otherwise
+  int ks, cpc;               // k-split kernel
+  size_t smem;
 };
 
 // Event pairs around each launch of an instrumented (eager) step.
@@ -108,10 +110,11 @@ struct mag_ctx {
   float* ss_part = nullptr;
   __half* act = nullptr;
   float* gemv_part = nullptr;
-  int sk_blocks[5][5] = {};  // Stream-K blocks per projection kind (QKV, O, GU, DOWN, LM) and batch 1..4
 
   // counters (zero between launches) and step arguments
   uint32_t* d_counters = nullptr;
+  uint32_t* h_err = nullptr;  // mapped pinned word: kernels set bits when a bounded wait gives up
+  uint32_t* d_err = nullptr;
   size_t n_counters = 0;
   StepArgs* d_args = nullptr;
   StepArgs* h_ring = nullptr;
@@ -148,23 +151,38 @@ mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...) {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Launch shape of one projection at batch B: up to 4 tokens a Stream-K grid
-// of sk_blocks (the GPU filled to its occupancy, activations for the whole K
-// staged per block); above that a k-split grid whose staged activation slice
-// fits in 64 KB of shared memory.
-constexpr int kStreamKMaxBatch = 4;
+// After a synchronisation: a kernel whose bounded wait gave up left a bit in the error word.
+mag_status check_err(mag_ctx* c) {
+  const uint32_t e = *reinterpret_cast<volatile uint32_t*>(c->h_err);
+  if (e == 0) return MAG_OK;
+  *reinterpret_cast<volatile uint32_t*>(c->h_err) = 0;
+  return fail(c, MAG_ERR_TIMEOUT, "a kernel's pipeline wait gave up (code 0x%x)", e);
+}
+
+// Launch shape of one projection at batch B. Up to kPipeMaxBatch tokens: the
+// pipelined kernel, one block per SM over contiguous tile ranges, its per-warp
+// rings as deep as a shared-memory budget allows. Above that a k-split grid
+// whose staged activation slice fits in 64 KB of shared memory.
+constexpr size_t kPipeBudget = 200 * 1024, kSmemMax = 227 * 1024;
 
 GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
-  GemvPlan p;
+  GemvPlan p = {};
   const int n_chunks = (K + 63) / 64;
-  if (B <= kStreamKMaxBatch) {
-    p.streamk_blocks = c->sk_blocks[kind][B];
+  if (B <= kPipeMaxBatch) {
+    const int wfmt = kind == 4 ? W_F16 : W_W4;
+    p.n_cta = std::max(1, std::min(c->n_sm, n_mtiles));
+    p.t_max = (n_mtiles + p.n_cta - 1) / p.n_cta;
+    const size_t base = gemv_pipe_smem_bytes(wfmt, B, n_chunks, 0, p.t_max);
+    const size_t stage = gemv_pipe_slot_bytes(wfmt);
+    const size_t budget = kPipeBudget;
+    const int fit = budget > base ? (int)((budget - base) / stage) : 0;
+    p.stages = std::max(2, std::min(gemv_pipe_max_stages(), fit));
+    p.smem = gemv_pipe_smem_bytes(wfmt, B, n_chunks, p.stages, p.t_max);
     p.ks = 1;
     p.cpc = n_chunks;
     return p;
   }
   (void)n_mtiles;
-  p.streamk_blocks = 0;
   const int max_cpc = std::max(1, (64 * 1024) / (B * 136) - 1);
   p.ks = (n_chunks + max_cpc - 1) / max_cpc;
   p.cpc = (n_chunks + p.ks - 1) / p.ks;
@@ -218,38 +236,38 @@ std::vector<ProjShape> proj_shapes(const mag_ctx* c) {
   return v;
 }
 
-// Floats of the partial-sum buffer for batch B (Stream-K parts or k-split slices).
+// Floats of the partial-sum buffer for batch B (k-split slices).
 size_t gemv_partial_floats(const mag_ctx* c, int B) {
   size_t mx = 0;
   const int nt = B > 8 ? 2 : 1;
   for (auto& ps : proj_shapes(c)) {
     GemvPlan p = plan_gemv(c, ps.kind, ps.n_mtiles, ps.K, B);
-    if (p.streamk_blocks > 0) mx = std::max(mx, (size_t)p.streamk_blocks * 8 * 2 * 32 * 4);
-    else if (p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
+    if (p.n_cta == 0 && p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
   }
   return mx;
 }
 
-// Counter slots: one per tile (Stream-K) or per block column (k-split).
+// Shared memory of the pipelined kernel for every projection and batch must fit one block.
+bool gemv_plans_fit(const mag_ctx* c, std::string& why) {
+  for (auto& ps : proj_shapes(c))
+    for (int B = 1; B <= std::min(kPipeMaxBatch, c->B_max); ++B) {
+      const GemvPlan p = plan_gemv(c, ps.kind, ps.n_mtiles, ps.K, B);
+      if (p.smem > kSmemMax) {
+        char b[160];
+        snprintf(b, sizeof b, "projection %d (K = %d) at batch %d needs %zu bytes of shared memory (limit %zu)",
+                 ps.kind, ps.K, B, p.smem, kSmemMax);
+        why = b;
+        return false;
+      }
+    }
+  return true;
+}
+
+// Counter slots: one per block column (k-split).
 size_t gemv_counters(const mag_ctx* c) {
   size_t mx = 1;
   for (auto& ps : proj_shapes(c)) mx = std::max(mx, (size_t)ps.n_mtiles);
   return mx;
-}
-
-// Stream-K grid per projection kind and batch: SMs x resident blocks.
-void plan_streamk(mag_ctx* c) {
-  for (auto& ps : proj_shapes(c))
-    for (int B = 1; B <= std::min(kStreamKMaxBatch, c->B_max); ++B) {
-      GemvArgs a = {};
-      a.batch = B;
-      a.n_chunks = (ps.K + 63) / 64;
-      a.streamk_blocks = 1;
-      const size_t smem = gemv_smem_bytes(a, ps.wfmt);
-      const int per_sm = std::max(1, gemv_blocks_per_sm(ps.wfmt, ps.xsrc, ps.epi, smem));
-      const int tiles_chunks = ps.n_mtiles * a.n_chunks;
-      c->sk_blocks[ps.kind][B] = std::max(1, std::min(c->n_sm * per_sm, (tiles_chunks + 7) / 8));
-    }
 }
 
 // Decode-phase activation tensors at max_batch with their op lifetimes: op 0
@@ -282,11 +300,13 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
   GemvArgs a = {};
   GemvPlan pl = plan_gemv(c, kind, n_mtiles, K, B);
   a.w = w;
-  a.w_row_bytes = (int64_t)K * 2;
   a.n_mtiles = n_mtiles;
   a.K = K;
   a.n_chunks = (K + 63) / 64;
-  a.streamk_blocks = pl.streamk_blocks;
+  a.n_cta = pl.n_cta;
+  a.stages = pl.stages;
+  a.t_max = pl.t_max;
+  a.err = c->d_err;
   a.chunks_per_cta = pl.cpc;
   a.ks = pl.ks;
   a.batch = B;
@@ -397,6 +417,7 @@ void free_ctx(mag_ctx* c) {
   cudaFree(c->d_in_stage);
   cudaFree(c->d_out_stage);
   if (c->h_ring) cudaFreeHost(c->h_ring);
+  if (c->h_err) cudaFreeHost(c->h_err);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   delete c;
 }
@@ -524,7 +545,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   size_t gf_off = off;
   off = align256(off + (size_t)c->D * 2);
   size_t lm_off = off;
-  if (c->V) off = align256(off + (size_t)c->V * c->D * 2);
+  if (c->V) off = align256(off + (size_t)(c->V / 16) * ((c->D + 63) / 64) * 2048);  // fp16 tiles, ragged k zeroed
   c->wbytes = off;
   if ((e = cudaMalloc(&c->wbase, c->wbytes)) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "weights: cudaMalloc(%zu): %s", c->wbytes, cudaGetErrorString(e));
@@ -577,7 +598,13 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   }
 
   // ---- launch plans and arena
-  plan_streamk(c);
+  {
+    std::string why;
+    if (!gemv_plans_fit(c, why)) {
+      fail(c, MAG_ERR_INVALID_ARG, "create: %s", why.c_str());
+      return bail(MAG_ERR_INVALID_ARG);
+    }
+  }
   build_decode_plan(c);
   if ((e = cudaMalloc(&c->arena, std::max<uint64_t>(c->arena_bytes, 256))) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "arena: %s", cudaGetErrorString(e));
@@ -598,10 +625,13 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
       cudaMalloc(&c->d_args, sizeof(StepArgs)) != cudaSuccess ||
       cudaMalloc(&c->d_in_stage, (size_t)c->B_max * c->D * 2) != cudaSuccess ||
       cudaMalloc(&c->d_out_stage, stage_out) != cudaSuccess ||
-      cudaMallocHost(&c->h_ring, sizeof(StepArgs) * kRing) != cudaSuccess) {
+      cudaMallocHost(&c->h_ring, sizeof(StepArgs) * kRing) != cudaSuccess ||
+      cudaHostAlloc(&c->h_err, sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess ||
+      cudaHostGetDevicePointer(&c->d_err, c->h_err, 0) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "counters / step arguments");
     return bail(MAG_ERR_OOM);
   }
+  *c->h_err = 0;
   cudaMemsetAsync(c->d_counters, 0, nc * 4, c->stream);
   for (auto& ev : c->ring_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
   c->other_bytes += nc * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
@@ -666,7 +696,7 @@ mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const voi
   if (tensor == MAG_LM_HEAD) {
     if (!c->V) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: this model has no LM head");
     if (bytes != (size_t)c->V * c->D * 2) return fail(c, MAG_ERR_INVALID_ARG, "load_weights: LM head size");
-    CUDA_TRY(c, cudaMemcpyAsync(c->lm_head, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+    CUDA_TRY(c, launch_f16_to_tiles(c->stream, (const __half*)src, c->V, c->D, reinterpret_cast<uint8_t*>(c->lm_head)));
     c->loaded[(size_t)c->L * 6 + 1] = 1;
     return MAG_OK;
   }
@@ -894,7 +924,7 @@ mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, cons
   if (st != MAG_OK) return st;
   CUDA_TRY(c, cudaMemcpyAsync(out_host, c->d_out_stage, out_b, cudaMemcpyDeviceToHost, c->stream));
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  return MAG_OK;
+  return check_err(c);
 }
 
 mag_status mag_prefill_chunk(mag_ctx* c, int32_t, int32_t, const void*, void*) {
@@ -905,7 +935,7 @@ mag_status mag_prefill_chunk(mag_ctx* c, int32_t, int32_t, const void*, void*) {
 mag_status mag_sync(mag_ctx* c) {
   if (!c) return MAG_ERR_INVALID_ARG;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  return MAG_OK;
+  return check_err(c);
 }
 
 mag_status mag_get_memory_stats(mag_ctx* c, mag_memory_stats* s) {

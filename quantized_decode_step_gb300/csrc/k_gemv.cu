@@ -76,23 +76,14 @@ struct Ring<W_W4> {
 template <>
 struct Ring<W_F16> {
   static constexpr int kSlots = 4;
-  static constexpr int kSlotBytes = 2048;  // 16 rows x 64 k fp16; lane L: 64 B at 64 L
+  static constexpr int kSlotBytes = 2048;  // 16 rows x 64 k fp16 tile, lane order: lane L's 64 B at 64 L
   static __device__ __forceinline__ void issue(uint8_t* slot, const GemvArgs& a, int mt, int c, int lane) {
-    const int g = lane >> 2, t = lane & 3, k = c * 64 + t * 16;
+    const uint8_t* src = a.w + ((int64_t)mt * a.n_chunks + c) * kSlotBytes + lane * 64;
     uint8_t* d = slot + lane * 64;
-    if (k < a.K) {
-      const uint8_t* pg = a.w + (int64_t)(mt * 16 + g) * a.w_row_bytes + (int64_t)k * 2;
-      const uint8_t* ph = pg + 8 * a.w_row_bytes;
-      cp_async16(d, pg);
-      cp_async16(d + 16, pg + 16);
-      cp_async16(d + 32, ph);
-      cp_async16(d + 48, ph + 16);
-    } else {
-      *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(d + 16) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(d + 32) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(d + 48) = make_uint4(0, 0, 0, 0);
-    }
+    cp_async16(d, src);
+    cp_async16(d + 16, src + 16);
+    cp_async16(d + 32, src + 32);
+    cp_async16(d + 48, src + 48);
   }
 };
 
@@ -363,109 +354,6 @@ __device__ void epilogue_tile(const GemvArgs& a, int mt, const float (&acc)[2][4
     }
 }
 
-// ------------------------------------------------------------------ Stream-K schedule (B <= 4)
-template <int WFMT, int XSRC, int EPI>
-__global__ void __launch_bounds__(256) gemv_streamk_kernel(const GemvArgs a) {
-  using Stage = typename StageT<WFMT>::type;
-  using R = Ring<WFMT>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_inv[(kWarps + 1) * MAG_MAX_BATCH];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int C = a.n_chunks;
-  const int64_t P = (int64_t)a.n_mtiles * C;
-  const int64_t W = (int64_t)gridDim.x * kWarps;
-  const int64_t Q = (P + W - 1) / W;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
-  const int64_t p0 = min(w * Q, P), p1 = min(p0 + Q, P);
-  const int n = (int)(p1 - p0);
-  uint8_t* ring = smem + staged_bytes(a.batch, C) + (size_t)warp * R::kSlots * R::kSlotBytes;
-
-  // (imt, ic): the next pair to copy into the ring, advanced incrementally
-  int imt = (int)(p0 / C), ic = (int)(p0 - (int64_t)imt * C);
-#pragma unroll
-  for (int u = 0; u < R::kSlots; ++u) {
-    if (u < n) {
-      R::issue(ring + u * R::kSlotBytes, a, imt, ic, lane);
-      if (++ic == C) {
-        ic = 0;
-        ++imt;
-      }
-    }
-    cp_async_commit();
-  }
-
-  pdl_wait();
-  pdl_trigger();
-  const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, 0, C);
-
-  float acc[2][8] = {};
-  int mt = (int)(p0 / C), c = (int)(p0 % C);
-  int64_t seg0 = p0;
-  // finish the tile mt with this warp's part [seg0, seg1) of its pairs
-  auto finish = [&](int64_t seg1) {
-    const int64_t t0 = (int64_t)mt * C, t1 = t0 + C;
-    float res[2][4];
-    tile_result(acc[0], res[0], WFMT);
-    if (seg0 == t0 && seg1 == t1) {
-      epilogue_tile<1, EPI>(a, mt, res, lane);
-      return;
-    }
-    // part of a tile: publish it; the last warp of the tile adds the parts in warp order
-    const int slot = p0 >= t0 ? 0 : 1;
-    float* part = a.partial + ((w * 2 + slot) * 32 + lane) * 4;
-    *reinterpret_cast<float4*>(part) = make_float4(res[0][0], res[0][1], res[0][2], res[0][3]);
-    __threadfence();
-    __syncwarp();
-    const int64_t w_first = t0 / Q, w_last = (t1 - 1) / Q;
-    unsigned prev = 0;
-    if (lane == 0) prev = atomicAdd(a.counters + mt, 1u);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev != (unsigned)(w_last - w_first)) return;
-    __threadfence();
-    float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int64_t v = w_first; v <= w_last; ++v) {
-      const int sl = v * Q >= t0 ? 0 : 1;
-      const float4 q = __ldcg(reinterpret_cast<const float4*>(a.partial + ((v * 2 + sl) * 32 + lane) * 4));
-      sum[0][0] += q.x;
-      sum[0][1] += q.y;
-      sum[0][2] += q.z;
-      sum[0][3] += q.w;
-    }
-    epilogue_tile<1, EPI>(a, mt, sum, lane);
-    if (lane == 0) a.counters[mt] = 0;
-  };
-
-  int si = 0;  // ring slot of chunk i
-  for (int i = 0; i < n; ++i) {
-    uint8_t* slot = ring + si * R::kSlotBytes;
-    if (++si == R::kSlots) si = 0;
-    cp_async_wait<R::kSlots - 1>();
-    __syncwarp();
-    Stage cur;
-    read_slot(cur, slot, lane);
-    __syncwarp();
-    if (i + R::kSlots < n) {
-      R::issue(slot, a, imt, ic, lane);
-      if (++ic == C) {
-        ic = 0;
-        ++imt;
-      }
-    }
-    cp_async_commit();
-    compute_chunk<1>(cur, acc, S, a.batch, c, g, t);
-    if (++c == C) {  // end of a tile
-      finish(p0 + i + 1);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[0][j] = 0.f;
-      ++mt;
-      c = 0;
-      seg0 = p0 + i + 1;
-    }
-  }
-  if (seg0 < p1) finish(p1);  // this warp's run ends inside a tile
-  cp_async_wait<0>();
-}
-
 // ------------------------------------------------------------------ K-split schedule (B > 4)
 template <int NT, int WFMT, int XSRC, int EPI>
 __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
@@ -567,8 +455,6 @@ cudaError_t launch_k(const Launch& L, K kern, dim3 grid, size_t smem, const Gemv
 template <int WFMT, int XSRC, int EPI>
 cudaError_t launch_sched(const Launch& L, const GemvArgs& a) {
   const size_t smem = gemv_smem_bytes(a, WFMT);
-  if (a.streamk_blocks > 0)
-    return launch_k(L, gemv_streamk_kernel<WFMT, XSRC, EPI>, dim3(a.streamk_blocks), smem, a);
   const dim3 grid((a.n_mtiles + kWarps - 1) / kWarps, a.ks);
   if (a.batch > 8) return launch_k(L, gemv_ksplit_kernel<2, WFMT, XSRC, EPI>, grid, smem, a);
   return launch_k(L, gemv_ksplit_kernel<1, WFMT, XSRC, EPI>, grid, smem, a);
@@ -577,29 +463,14 @@ cudaError_t launch_sched(const Launch& L, const GemvArgs& a) {
 }  // namespace
 
 size_t gemv_smem_bytes(const GemvArgs& a, int wfmt) {
-  const int nch = a.streamk_blocks > 0 ? a.n_chunks : a.chunks_per_cta;
+  const int nch = a.chunks_per_cta;
   const size_t ring = wfmt == W_W4 ? (size_t)Ring<W_W4>::kSlots * Ring<W_W4>::kSlotBytes
                                    : (size_t)Ring<W_F16>::kSlots * Ring<W_F16>::kSlotBytes;
   return staged_bytes(a.batch, nch) + kWarps * ring;
 }
 
-int gemv_blocks_per_sm(int wfmt, int xsrc, int epi, size_t smem) {
-  int n = 0;
-#define MAG_OCC(W_, X_, E_)                                                                                   \
-  if (wfmt == W_ && xsrc == X_ && epi == E_) {                                                               \
-    auto k = gemv_streamk_kernel<W_, X_, E_>;                                                                \
-    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, 32 * kWarps, smem);                                \
-  }
-  MAG_OCC(W_W4, XSRC_RESID, EPI_QKV)
-  MAG_OCC(W_W4, XSRC_F16, EPI_RESID)
-  MAG_OCC(W_W4, XSRC_RESID, EPI_SWIGLU)
-  MAG_OCC(W_F16, XSRC_RESID, EPI_STORE_OUT)
-#undef MAG_OCC
-  return n;
-}
-
 cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi) {
+  if (a.n_cta > 0) return launch_gemv_pipe(L, a, wfmt, xsrc, epi);
 #define MAG_GEMV_CASE(W_, X_, E_) \
   if (wfmt == W_ && xsrc == X_ && epi == E_) return launch_sched<W_, X_, E_>(L, a);
   MAG_GEMV_CASE(W_W4, XSRC_RESID, EPI_QKV)

@@ -143,6 +143,24 @@ __global__ void w4_tiles_kernel(const uint8_t* __restrict__ src, uint8_t* __rest
   }
 }
 
+// One thread per (tile, chunk, lane, row half): 16 fp16 values of row g (or g+8).
+__global__ void f16_tiles_kernel(const __half* __restrict__ src, int N, int K, uint8_t* __restrict__ dst) {
+  const int C = (K + 63) / 64, n_mt = N / 16;
+  const int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (id >= (int64_t)n_mt * C * 64) return;
+  const int h = (int)(id & 1), lane = (int)((id >> 1) & 31), g = lane >> 2, t = lane & 3;
+  const int64_t tc = id >> 6;
+  const int mt = (int)(tc / C), c = (int)(tc - (int64_t)mt * C);
+  const int64_t row = (int64_t)mt * 16 + g + 8 * h;
+  const int k0 = c * 64 + t * 16;
+  __half v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = k0 + j < K ? src[row * K + k0 + j] : __float2half_rn(0.f);
+  uint4* o = reinterpret_cast<uint4*>(dst + tc * 2048 + lane * 64 + h * 32);
+  o[0] = *reinterpret_cast<uint4*>(v);
+  o[1] = *reinterpret_cast<uint4*>(v + 8);
+}
+
 template <typename K, typename... Args>
 cudaError_t launch_plain(const Launch& L, K kern, dim3 grid, dim3 block, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -199,4 +217,13 @@ cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, in
   return launch_tiles(s, tiles, canon, N, K, map, map_arg, 1);
 }
 
+}  // namespace mag
+
+namespace mag {
+cudaError_t launch_f16_to_tiles(cudaStream_t s, const __half* src, int N, int K, uint8_t* tiles) {
+  const int64_t n = (int64_t)(N / 16) * ((K + 63) / 64) * 64;
+  if (n == 0) return cudaSuccess;
+  f16_tiles_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, N, K, tiles);
+  return cudaGetLastError();
+}
 }  // namespace mag

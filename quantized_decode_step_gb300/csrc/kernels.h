@@ -24,12 +24,10 @@ enum TileMap { MAP_PLAIN = 0, MAP_QKV = 1, MAP_SWIGLU = 2 };
 constexpr int kTileBytes = 640;  // one 16-row x 64-k tile: 512 B of codes + 128 B of (scale, min)
 
 struct GemvArgs {
-  const uint8_t* w;       // W4: tiles [n_mtiles][n_chunks][640 B]; fp16: row-major [N][K]
-  int64_t w_row_bytes;    // fp16 weights: 2K
+  const uint8_t* w;       // tiles [n_mtiles][n_chunks]: W4 640 B, fp16 2048 B each
   int32_t n_mtiles;       // 16-row tiles
   int32_t K;              // reduction length
   int32_t n_chunks;       // ceil(K / 64)
-  int32_t streamk_blocks; // > 0: Stream-K over that many blocks; 0: k-split grid
   int32_t chunks_per_cta; // k-split: k-range of one block, in chunks
   int32_t ks;             // k-split: splits (grid.y)
   int32_t batch;
@@ -48,13 +46,23 @@ struct GemvArgs {
   int32_t head_dim, n_rot_heads;  // EPI_QKV: heads below n_rot_heads get RoPE
   const float* rope_cos;
   const float* rope_sin;
-  float* partial;         // Stream-K: [warps][2][32][4]; k-split: [ks][n_mtiles][32][4 * n_tiles]
+  float* partial;         // k-split: [ks][n_mtiles][32][4 * n_tiles]
   uint32_t* counters;     // zero between launches
   const StepArgs* step;
+  // pipelined kernel (batch <= kPipeMaxBatch): one block per SM
+  int32_t n_cta;          // blocks; block i owns tiles [i n_mtiles / n_cta, (i+1) n_mtiles / n_cta)
+  int32_t stages;         // ring slots per warp (2..8)
+  int32_t t_max;          // most tiles of one block
+  uint32_t* err;          // set (bit or) when a pipeline wait gives up
 };
 
+constexpr int kPipeMaxBatch = 4;
+size_t gemv_pipe_smem_bytes(int wfmt, int batch, int n_chunks, int stages, int t_max);
+int gemv_pipe_max_stages();
+size_t gemv_pipe_slot_bytes(int wfmt);  // ring bytes of one slot across the block's warps
+cudaError_t launch_gemv_pipe(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi);
+
 size_t gemv_smem_bytes(const GemvArgs& a, int wfmt);
-int gemv_blocks_per_sm(int wfmt, int xsrc, int epi, size_t smem);
 cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi);
 
 // Load-time repack of a W4G32 matrix [N, K] (codes [N][16G] then (scale, min)
@@ -66,6 +74,10 @@ cudaError_t launch_w4_to_tiles(cudaStream_t s, const uint8_t* canon, int N, int 
                                uint8_t* tiles);
 cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, int K, int map, int map_arg,
                                  uint8_t* canon);
+// Load-time repack of an fp16 matrix [N, K] (row-major, N % 16 == 0) into
+// 2048-byte tiles [N/16][ceil(K/64)]: lane L = (g, t) of a tile holds rows
+// g and g+8 at k = 64c + 16t .. 16t+15 (32 bytes each); k >= K is zero.
+cudaError_t launch_f16_to_tiles(cudaStream_t s, const __half* src, int N, int K, uint8_t* tiles);
 
 // ---------------------------------------------------------------- step prologue
 // block-table writes, fp16 input -> fp32 residual and its sum of squares (ss_part[0][b])

@@ -134,6 +134,13 @@ def test_tiny_batch_ragged_contexts():
     _run_decode(wl, 13, n_steps=2)
 
 
+@pytest.mark.parametrize("B", [2, 3, 4])
+def test_tiny_small_batches(B):
+    """Batches of 2-4 sessions (the multi-token path of the one-block-per-SM GEMV), ragged contexts."""
+    wl = Workload(f"tiny-b{B}", TINY, KV_INT8, B, tuple(range(5, 5 + 37 * B, 37)), scattered_pool=True)
+    _run_decode(wl, 15 + B, n_steps=2)
+
+
 def test_tiny_batch16():
     wl = Workload("tiny-b16", TINY, KV_FP16, 16, tuple(range(3, 3 + 16 * 9, 9)), scattered_pool=True)
     _run_decode(wl, 14, n_steps=1)
