@@ -183,11 +183,17 @@ mag_status mag_decode_step(mag_ctx* ctx, int32_t batch, const int32_t* session_i
 mag_status mag_decode_step_host(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host,
                                 const void* hidden_in_host, void* out_host);
 
-/* Chunked prefill: append n_tokens (<= max_chunk) of one session at its next
- * positions with causal attention over the cache and the chunk, and write
- * the fp16 output (logits, or hidden state when vocab == 0) of the last
- * token to last_out_dev. hidden_in_dev is fp16 [n_tokens][D].
- * Errors: INVALID_ARG, CONTEXT_FULL, KV_FULL, NOT_LOADED, UNSUPPORTED, CUDA. */
+/* Chunked prefill ("5. Core modules" 5.1 W4A16 model, 5.2 block pool): append
+ * n_tokens (1..max_chunk) of one session at its next positions, with causal
+ * attention over the session's cache and the chunk itself, and write the fp16
+ * output (logits, or the hidden state when vocab == 0) of the chunk's last
+ * token to last_out_dev. hidden_in_dev is fp16 [n_tokens][D]; the chunk's K/V
+ * are stored in the pool like mag_kv_append's (the same quantisers). The
+ * projections run as tensor-core GEMMs over an exact two-term fp16 copy of
+ * every W4 matrix (hi + lo = s q + m), made at load time when max_chunk > 0
+ * (4 bytes per weight; mag_get_memory_stats reports it). Stream-ordered.
+ * Errors: INVALID_ARG, CONTEXT_FULL, KV_FULL, NOT_LOADED, UNSUPPORTED (created
+ * with max_chunk = 0), CUDA. */
 mag_status mag_prefill_chunk(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
                              void* last_out_dev);
 
@@ -205,6 +211,8 @@ typedef struct mag_memory_stats {
   uint64_t arena_unshared_bytes; /* sum of the arena tensors' sizes (no reuse) */
   uint64_t other_device_bytes; /* block tables, RoPE table, counters, step arguments */
   int32_t sessions_open;
+  uint64_t prefill_weight_bytes; /* exact two-term fp16 weight copies of the prefill GEMM (max_chunk > 0) */
+  uint64_t prefill_arena_bytes;  /* planned prefill activation arena (max_chunk rows) */
 } mag_memory_stats;
 
 /* [Magnitude] 5.2 get_memory_stats: weights, pool, arena. */

@@ -55,7 +55,8 @@ class MemoryStats(ctypes.Structure):
                 ("kv_block_bytes", ctypes.c_uint64), ("pool_blocks_total", ctypes.c_int32),
                 ("pool_blocks_free", ctypes.c_int32), ("arena_bytes", ctypes.c_uint64),
                 ("arena_unshared_bytes", ctypes.c_uint64), ("other_device_bytes", ctypes.c_uint64),
-                ("sessions_open", ctypes.c_int32)]
+                ("sessions_open", ctypes.c_int32), ("prefill_weight_bytes", ctypes.c_uint64),
+                ("prefill_arena_bytes", ctypes.c_uint64)]
 
 
 class ArenaTensor(ctypes.Structure):

@@ -129,6 +129,28 @@ struct mag_ctx {
   int graph_launches[MAG_MAX_BATCH + 1] = {};
   int last_launches = 0;
   uint64_t other_bytes = 0;
+  // chunked prefill (max_chunk > 0): exact two-term fp16 weight copies, their TMA maps, planned buffers
+  struct PrefillProj {
+    __half* hi = nullptr;
+    __half* lo = nullptr;
+    int rows = 0;  // copy rows: a multiple of 128
+    alignas(64) uint8_t map_hi[128];
+    alignas(64) uint8_t map_lo[128];
+  };
+  std::vector<PrefillProj> pproj;  // [L][4]
+  uint8_t* pf_w = nullptr;
+  size_t pf_wbytes = 0;
+  uint8_t* pf_arena = nullptr;
+  uint64_t pf_arena_bytes = 0;
+  std::vector<ArenaTensor> pf_plan;
+  float* pf_r = nullptr;
+  __half* pf_xn = nullptr;
+  __half* pf_qkv = nullptr;
+  __half* pf_o = nullptr;
+  __half* pf_act = nullptr;
+  alignas(64) uint8_t map_xn[128];
+  alignas(64) uint8_t map_o[128];
+  alignas(64) uint8_t map_act[128];
 };
 
 namespace {
@@ -418,6 +440,8 @@ void free_ctx(mag_ctx* c) {
   cudaFree(c->d_out_stage);
   if (c->h_ring) cudaFreeHost(c->h_ring);
   if (c->h_err) cudaFreeHost(c->h_err);
+  cudaFree(c->pf_w);
+  cudaFree(c->pf_arena);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   delete c;
 }
@@ -443,6 +467,84 @@ mag_status check_cfg(const mag_config* g, std::string& why) {
   if (!(g->rms_eps > 0) || !(g->rope_base > 0)) return bad("rms_eps and rope_base must be positive");
   snprintf(b, sizeof b, "ok");
   return MAG_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// ---------------------------------------------------------------- chunked prefill set-up
+// Copy rows of projection kind i: a multiple of the GEMM tile; gate-up interleaves gate and up in blocks of 64.
+int prefill_rows(const mag_ctx* c, int i) {
+  const int t = tc_gemm_rows_multiple();
+  if (i == 2) return (c->F + 63) / 64 * 128;
+  const int n = i == 0 ? c->R : c->D;
+  return (n + t - 1) / t * t;
+}
+
+// Prefill activation tensors at max_chunk rows with their op lifetimes: 0 input, per layer 1 norm,
+// 2 QKV, 3 KV store + attention, 4 O, 5 norm, 6 gate-up, 7 down (one plan for every layer); 8 LM head.
+void build_prefill_plan(mag_ctx* c) {
+  const uint64_t T = c->cfg.max_chunk;
+  auto Tn = [](const char* n, uint64_t sz, int f, int l) { return ArenaTensor{n, sz, f, l, 0}; };
+  c->pf_plan.clear();
+  c->pf_plan.push_back(Tn("pf_residual", T * c->D * 4, 0, 8));
+  c->pf_plan.push_back(Tn("pf_norm", T * c->D * 2, 1, 6));
+  c->pf_plan.push_back(Tn("pf_qkv", T * c->R * 2, 2, 3));
+  c->pf_plan.push_back(Tn("pf_attn_out", T * c->Hq * c->d * 2, 3, 4));
+  c->pf_plan.push_back(Tn("pf_ffn_act", T * c->F * 2, 6, 7));
+  c->pf_arena_bytes = plan_arena(c->pf_plan, 64, (c->cfg.flags & MAG_FLAG_ARENA_NO_REUSE) != 0);
+}
+
+mag_status setup_prefill(mag_ctx* c) {
+  const int Ks[4] = {c->D, c->Hq * c->d, c->D, c->F};
+  size_t total = 0;
+  std::vector<size_t> offs;
+  for (int l = 0; l < c->L; ++l)
+    for (int i = 0; i < 4; ++i) {
+      offs.push_back(total);
+      total = align256(total + (size_t)prefill_rows(c, i) * Ks[i] * 2 * 2);
+    }
+  cudaError_t e = cudaMalloc(&c->pf_w, std::max<size_t>(total, 256));
+  if (e != cudaSuccess) return fail(c, MAG_ERR_OOM, "prefill weights: cudaMalloc(%zu): %s", total, cudaGetErrorString(e));
+  c->pf_wbytes = total;
+  cudaMemsetAsync(c->pf_w, 0, total, c->stream);  // padding rows stay zero
+  c->pproj.resize((size_t)c->L * 4);
+  for (int l = 0; l < c->L; ++l)
+    for (int i = 0; i < 4; ++i) {
+      auto& pp = c->pproj[(size_t)l * 4 + i];
+      pp.rows = prefill_rows(c, i);
+      pp.hi = reinterpret_cast<__half*>(c->pf_w + offs[(size_t)l * 4 + i]);
+      pp.lo = pp.hi + (size_t)pp.rows * Ks[i];
+      if (!make_tmap_2d(pp.map_hi, pp.hi, pp.rows, Ks[i]) || !make_tmap_2d(pp.map_lo, pp.lo, pp.rows, Ks[i]))
+        return fail(c, MAG_ERR_CUDA, "prefill: tensor map encoding failed (layer %d, projection %d)", l, i);
+    }
+  build_prefill_plan(c);
+  if ((e = cudaMalloc(&c->pf_arena, std::max<uint64_t>(c->pf_arena_bytes, 256))) != cudaSuccess)
+    return fail(c, MAG_ERR_OOM, "prefill arena: %s", cudaGetErrorString(e));
+  auto at = [&](const char* n) -> uint8_t* {
+    for (auto& t : c->pf_plan)
+      if (t.name == n) return c->pf_arena + t.offset;
+    return nullptr;
+  };
+  c->pf_r = reinterpret_cast<float*>(at("pf_residual"));
+  c->pf_xn = reinterpret_cast<__half*>(at("pf_norm"));
+  c->pf_qkv = reinterpret_cast<__half*>(at("pf_qkv"));
+  c->pf_o = reinterpret_cast<__half*>(at("pf_attn_out"));
+  c->pf_act = reinterpret_cast<__half*>(at("pf_ffn_act"));
+  const int T = c->cfg.max_chunk;
+  if (!make_tmap_2d(c->map_xn, c->pf_xn, T, c->D) || !make_tmap_2d(c->map_o, c->pf_o, T, (int64_t)c->Hq * c->d) ||
+      !make_tmap_2d(c->map_act, c->pf_act, T, c->F))
+    return fail(c, MAG_ERR_CUDA, "prefill: activation tensor maps");
+  return MAG_OK;
+}
+
+// After a projection's tiles are written: its two-term copy for the prefill GEMM.
+cudaError_t refresh_prefill_copy(mag_ctx* c, int layer, int tensor) {
+  if (c->cfg.max_chunk <= 0) return cudaSuccess;
+  const Proj& p = c->proj[(size_t)layer * 4 + tensor];
+  auto& pp = c->pproj[(size_t)layer * 4 + tensor];
+  return launch_w4_tiles_to_hilo(c->stream, p.tiles, p.N, p.K, p.map, p.map_arg, pp.hi, pp.lo);
 }
 
 }  // namespace
@@ -632,6 +734,10 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     return bail(MAG_ERR_OOM);
   }
   *c->h_err = 0;
+  if (cfg->max_chunk > 0) {
+    mag_status ps = setup_prefill(c);
+    if (ps != MAG_OK) return bail(ps);
+  }
   cudaMemsetAsync(c->d_counters, 0, nc * 4, c->stream);
   for (auto& ev : c->ring_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
   c->other_bytes += nc * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
@@ -682,10 +788,12 @@ mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const voi
       cudaError_t e3 = cudaFreeAsync(canon, c->stream);
       if (e2 != cudaSuccess || e3 != cudaSuccess)
         return fail(c, MAG_ERR_CUDA, "load_weights: %s", cudaGetErrorString(e2 != cudaSuccess ? e2 : e3));
+      CUDA_TRY(c, refresh_prefill_copy(c, layer, tensor));
     } else if (fmt == MAG_FMT_W4G32) {
       if (bytes != p.canon_bytes)
         return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected W4G32 %zu", bytes, p.canon_bytes);
       CUDA_TRY(c, launch_w4_to_tiles(c->stream, (const uint8_t*)src, p.N, p.K, p.map, p.map_arg, p.tiles));
+      CUDA_TRY(c, refresh_prefill_copy(c, layer, tensor));
     } else {
       return fail(c, MAG_ERR_INVALID_ARG, "load_weights: projections take FP32_DENSE or W4G32");
     }
@@ -728,6 +836,7 @@ mag_status mag_load_weights_f32_noalloc(mag_ctx* c, int32_t tensor, int32_t laye
     return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: make the context's device %d current (not %d)",
                 c->device, dev);
   CUDA_TRY(c, load_f32_noalloc(c->stream, (const float*)src, p.N, p.K, p.map, p.map_arg, p.tiles));
+  CUDA_TRY(c, refresh_prefill_copy(c, layer, tensor));
   c->loaded[(size_t)layer * 6 + tensor] = 1;
   return MAG_OK;
 }
@@ -927,9 +1036,133 @@ mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, cons
   return check_err(c);
 }
 
-mag_status mag_prefill_chunk(mag_ctx* c, int32_t, int32_t, const void*, void*) {
+mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out) {
   if (!c) return MAG_ERR_INVALID_ARG;
-  return fail(c, MAG_ERR_UNSUPPORTED, "prefill_chunk: not available in this build");
+  if (c->cfg.max_chunk <= 0) return fail(c, MAG_ERR_UNSUPPORTED, "prefill_chunk: created with max_chunk = 0");
+  if (!in || !last_out) return fail(c, MAG_ERR_INVALID_ARG, "prefill_chunk: null buffer");
+  if (T < 1 || T > c->cfg.max_chunk)
+    return fail(c, MAG_ERR_INVALID_ARG, "prefill_chunk: %d tokens not in 1..%d", T, c->cfg.max_chunk);
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "prefill_chunk: session %d is not open", sid);
+  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "prefill_chunk: not every weight is loaded");
+  Session& s = c->sessions[sid];
+  if ((int64_t)s.len + T > c->cfg.max_context)
+    return fail(c, MAG_ERR_CONTEXT_FULL, "prefill_chunk: %d + %d tokens exceed max_context %d", s.len, T,
+                c->cfg.max_context);
+  const int nb_old = (s.len + 15) / 16, nb_new = (s.len + T + 15) / 16;
+  if (nb_new - nb_old > (int)c->free_list.size())
+    return fail(c, MAG_ERR_KV_FULL, "prefill_chunk: needs %d blocks, %zu free", nb_new - nb_old, c->free_list.size());
+  // step arguments of the last token's LM head (or final hidden state)
+  const int slot = c->ring_pos;
+  CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
+  StepArgs& sa = c->h_ring[slot];
+  memset(&sa, 0, sizeof sa);
+  sa.batch = 1;
+  sa.sess[0] = sid;
+  sa.pos[0] = s.len + T - 1;
+  sa.out = last_out;
+  for (int i = nb_old; i < nb_new; ++i) {
+    s.table.push_back(c->free_list.front());
+    c->free_list.pop_front();
+  }
+  int32_t* row = c->d_tables + (size_t)sid * c->table_stride;
+  if (nb_new > nb_old)
+    CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
+                                cudaMemcpyHostToDevice, c->stream));
+  CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &sa, sizeof sa, cudaMemcpyHostToDevice, c->stream));
+  CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
+  c->ring_pos = (slot + 1) % kRing;
+
+  int n = 0;
+  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL);
+  Launch L{c->stream, pdl, &n};
+  const int p0 = s.len, D = c->D, HD = c->Hq * c->d;
+  const PoolGeom pg = pool_geom(c);
+  CUDA_TRY(c, launch_rows_to_resid(L, (const __half*)in, c->pf_r, T, D));
+  for (int l = 0; l < c->L; ++l) {
+    const auto* pp = &c->pproj[(size_t)l * 4];
+    TcGemmArgs g = {};
+    g.M = T;
+    g.err = c->d_err;
+    // RMSNorm + QKV (+ RoPE of q and k)
+    CUDA_TRY(c, launch_rmsnorm_rows(L, c->pf_r, c->gamma1[l], c->cfg.rms_eps, T, D, c->pf_xn));
+    TcGemmArgs gq = g;
+    gq.N = pp[0].rows;
+    gq.K = D;
+    gq.n_valid = c->R;
+    gq.out = c->pf_qkv;
+    gq.ldo = c->R;
+    gq.head_dim = c->d;
+    gq.n_rot_heads = c->Hq + c->Hkv;
+    gq.pos0 = p0;
+    gq.rope_cos = c->d_cos;
+    gq.rope_sin = c->d_sin;
+    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_xn, pp[0].map_hi, pp[0].map_lo}, gq, EPI_QKV));
+    // the chunk's k, v into the pool, then causal attention over the pool
+    KvChunkArgs kc = {};
+    kc.qkv = c->pf_qkv;
+    kc.qkv_ld = c->R;
+    kc.n_heads = c->Hq;
+    kc.n_tok = T;
+    kc.pos0 = p0;
+    kc.layer = l;
+    kc.table = row;
+    kc.pool = pg;
+    CUDA_TRY(c, launch_kv_store_chunk(L, kc));
+    PrefillAttnArgs pa = {};
+    pa.qkv = c->pf_qkv;
+    pa.qkv_ld = c->R;
+    pa.o = c->pf_o;
+    pa.ldo = HD;
+    pa.n_tok = T;
+    pa.pos0 = p0;
+    pa.n_heads = c->Hq;
+    pa.n_kv_heads = c->Hkv;
+    pa.head_dim = c->d;
+    pa.layer = l;
+    pa.table = row;
+    pa.pool = pg;
+    CUDA_TRY(c, launch_prefill_attention(L, pa));
+    // O projection + residual
+    TcGemmArgs go = g;
+    go.N = pp[1].rows;
+    go.K = HD;
+    go.n_valid = D;
+    go.r = c->pf_r;
+    go.ldr = D;
+    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_o, pp[1].map_hi, pp[1].map_lo}, go, EPI_RESID));
+    // RMSNorm + gate-up + SwiGLU
+    CUDA_TRY(c, launch_rmsnorm_rows(L, c->pf_r, c->gamma2[l], c->cfg.rms_eps, T, D, c->pf_xn));
+    TcGemmArgs gg = g;
+    gg.N = pp[2].rows;
+    gg.K = D;
+    gg.n_valid = c->F;
+    gg.out = c->pf_act;
+    gg.ldo = c->F;
+    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_xn, pp[2].map_hi, pp[2].map_lo}, gg, EPI_SWIGLU));
+    // down projection + residual
+    TcGemmArgs gd = g;
+    gd.N = pp[3].rows;
+    gd.K = c->F;
+    gd.n_valid = D;
+    gd.r = c->pf_r;
+    gd.ldr = D;
+    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_act, pp[3].map_hi, pp[3].map_lo}, gd, EPI_RESID));
+  }
+  float* r_last = c->pf_r + (size_t)(T - 1) * D;
+  if (c->V) {  // final RMSNorm + LM head of the last token
+    GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, D, 1);
+    a.r = r_last;
+    a.ldr = D;
+    a.gamma = c->gamma_f;
+    a.ldo = c->V;
+    CUDA_TRY(c, launch_gemv(L, a, W_F16, XSRC_RESID, EPI_STORE_OUT));
+  } else {
+    CUDA_TRY(c, launch_final_hidden(L, c->d_args, r_last, D, 1));
+  }
+  c->last_launches = n;
+  s.len += T;
+  return MAG_OK;
 }
 
 mag_status mag_sync(mag_ctx* c) {
@@ -949,6 +1182,8 @@ mag_status mag_get_memory_stats(mag_ctx* c, mag_memory_stats* s) {
   s->arena_bytes = c->arena_bytes;
   s->arena_unshared_bytes = c->arena_unshared;
   s->other_device_bytes = c->other_bytes;
+  s->prefill_weight_bytes = c->pf_wbytes;
+  s->prefill_arena_bytes = c->pf_arena_bytes;
   int open = 0;
   for (auto& x : c->sessions) open += x.open;
   s->sessions_open = open;

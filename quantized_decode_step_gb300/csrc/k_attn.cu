@@ -526,6 +526,178 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   cluster.sync();  // keep this block's shared memory alive until every rank has read it
 }
 
+// ---------------------------------------------------------------- chunked prefill
+// One block per (chunk token, KV head): its rotated k and v from the QKV output into the pool.
+__global__ void kv_store_chunk_kernel(const KvChunkArgs a) {
+  __shared__ __half xk[128], xv[128];
+  __shared__ float red[8];
+  const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+  const int d = a.pool.head_dim, Hkv = a.pool.n_kv_heads;
+  pdl_wait();  // the QKV projection's output
+  pdl_trigger();
+  const __half* row = a.qkv + (int64_t)t * a.qkv_ld;
+  xk[i] = row[(int64_t)(a.n_heads + h) * d + i];
+  xv[i] = row[(int64_t)(a.n_heads + Hkv + h) * d + i];
+  __syncthreads();
+  const int pos = a.pos0 + t;
+  const int blk = a.table[pos >> 4];
+  store_vec(a.pool, a.layer, blk, pos & 15, h, 0, xk, red);
+  store_vec(a.pool, a.layer, blk, pos & 15, h, 1, xv, red);
+}
+
+// pool value (which 0 = K, 1 = V) of (block, slot, head), element i, widened to fp16
+__device__ __forceinline__ __half pool_value(const PoolGeom& P, int layer, int blk, int which, int head, int slot,
+                                             int i) {
+  const uint8_t* data = pool_vec(P, layer, blk, which, head, slot);
+  if (P.kv_dtype == 0) return reinterpret_cast<const __half*>(data)[i];
+  const uint8_t* meta = pool_vec(P, layer, blk, which + 2, head, slot);
+  if (P.kv_dtype == 1) {
+    const float s = __half2float(*reinterpret_cast<const __half*>(meta));
+    return __float2half_rn(s * (float)reinterpret_cast<const int8_t*>(data)[i]);
+  }
+  const __half2 sm = reinterpret_cast<const __half2*>(meta)[i >> 5];
+  const int q = (data[i >> 1] >> (4 * (i & 1))) & 15;
+  return __float2half_rn(__fadd_rn(__fmul_rn(__low2float(sm), (float)q), __high2float(sm)));
+}
+
+// Block: one KV head and 4 warps x 16 MMA rows; a row is (token, query head of the group), 16/G tokens per
+// warp. The pool blocks up to the block's last position are widened into shared memory one at a time (K
+// row-major, V transposed) and shared by the warps; each warp runs QK^T, the causal mask, the online
+// softmax and PV (probabilities split into fp16 hi + lo) on m16n8k16 MMAs.
+template <int D>
+__global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs a) {
+  constexpr int KS = D / 16;  // k-steps of QK^T
+  constexpr int NV = D / 8;   // n-tiles of PV
+  __shared__ __align__(16) __half sk[16][D + 8];
+  __shared__ __align__(16) __half svt[D][16 + 8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int G = a.n_heads / a.n_kv_heads, gk = blockIdx.y;
+  const int tpw = 16 / G;  // tokens per warp
+  const int t_blk = blockIdx.x * 4 * tpw, t_warp = t_blk + warp * tpw;
+  pdl_wait();
+  pdl_trigger();
+  // the rows of this lane: r0 = g, r1 = g + 8
+  int tok[2], hq[2];
+  bool live[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = g + 8 * h, tl = r / G;
+    tok[h] = t_warp + tl;
+    hq[h] = gk * G + (r - tl * G);
+    live[h] = tl < tpw && tok[h] < a.n_tok;
+  }
+  uint32_t qa[KS][4];
+#pragma unroll
+  for (int s = 0; s < KS; ++s)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half* q = a.qkv + (int64_t)(live[h] ? tok[h] : 0) * a.qkv_ld + (int64_t)hq[h] * D + 16 * s + 2 * t;
+      qa[s][h] = live[h] ? *reinterpret_cast<const uint32_t*>(q) : 0u;
+      qa[s][2 + h] = live[h] ? *reinterpret_cast<const uint32_t*>(q + 8) : 0u;
+    }
+  const float sc = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
+  float m_run[2] = {-1e30f, -1e30f}, l_run[2] = {0.f, 0.f};
+  float acc[NV][4];
+#pragma unroll
+  for (int n = 0; n < NV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  const int last_tok = min(a.n_tok, t_blk + 4 * tpw) - 1;
+  const int n_blocks = (a.pos0 + last_tok) / 16 + 1;
+  const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
+  for (int b = 0; b < n_blocks; ++b) {
+    const int phys = a.table[b];
+    for (int e = threadIdx.x; e < 16 * D; e += blockDim.x) {
+      const int slot = e / D, i = e - slot * D;
+      sk[slot][i] = pool_value(a.pool, a.layer, phys, 0, gk, slot, i);
+      svt[i][slot] = pool_value(a.pool, a.layer, phys, 1, gk, slot, i);
+    }
+    __syncthreads();
+    if (warp_last >= t_warp && 16 * b <= a.pos0 + warp_last) {
+      float sfr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&sk[8 * nt + g][16 * s + 2 * t]);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&sk[8 * nt + g][16 * s + 2 * t + 8]);
+          mma_16816(sfr[nt], qa[s][0], qa[s][1], qa[s][2], qa[s][3], b0, b1);
+        }
+      }
+      // causal mask and online softmax; fragment (nt, j): row g + 8 (j >> 1), key 16 b + 8 nt + 2 t + (j & 1)
+      float mx[2] = {-1e30f, -1e30f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int h = j >> 1, kp = 16 * b + 8 * nt + 2 * t + (j & 1);
+          const bool ok = live[h] && kp <= a.pos0 + tok[h];
+          const float v = ok ? sfr[nt][j] * sc : -INFINITY;
+          sfr[nt][j] = v;
+          mx[h] = fmaxf(mx[h], v);
+        }
+      float corr[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float mn = fmaxf(m_run[h], mx[h]);
+        corr[h] = exp2f(m_run[h] - mn);
+        m_run[h] = mn;
+      }
+      float p[2][4], ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int h = j >> 1;
+          p[nt][j] = exp2f(sfr[nt][j] - m_run[h]);  // masked: exp2(-inf) = 0
+          ps[h] += p[nt][j];
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * corr[h] + ps[h];
+#pragma unroll
+      for (int n = 0; n < NV; ++n) {
+        acc[n][0] *= corr[0];
+        acc[n][1] *= corr[0];
+        acc[n][2] *= corr[1];
+        acc[n][3] *= corr[1];
+      }
+      // P as the A operand in fp16 hi + lo: a0 row g keys 2t,2t+1; a1 row g+8; a2/a3 keys 8+2t, 9+2t
+      uint32_t ph[4], pl[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int nt = i >> 1, h = i & 1;
+        const float x0 = p[nt][2 * h], x1 = p[nt][2 * h + 1];
+        const __half2 hh = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(hh);
+        ph[i] = h2_as_u32(hh);
+        pl[i] = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+      }
+#pragma unroll
+      for (int n = 0; n < NV; ++n) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&svt[8 * n + g][2 * t]);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&svt[8 * n + g][2 * t + 8]);
+        mma_16816(acc[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
+        mma_16816(acc[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      }
+    }
+    __syncthreads();
+  }
+  // normalise and store: acc[n][2h + j] = (row g + 8h, dim 8n + 2t + j)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float l = l_run[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (!live[h]) continue;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    __half* o = a.o + (int64_t)tok[h] * a.ldo + (int64_t)hq[h] * D;
+#pragma unroll
+    for (int n = 0; n < NV; ++n)
+      *reinterpret_cast<__half2*>(o + 8 * n + 2 * t) = __floats2half2_rn(acc[n][2 * h] * inv, acc[n][2 * h + 1] * inv);
+  }
+}
+
 template <typename K, typename Args>
 cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, size_t smem, const Args& a,
                       int cluster_x = 0) {
@@ -601,6 +773,22 @@ cudaError_t attn_max_cluster_t(int* out) {
 cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a) {
   if (a.n_tok == 0) return cudaSuccess;
   return launch_ex(L, kv_store_kernel, dim3(a.n_tok, a.pool.n_kv_heads, a.n_layers), dim3(a.pool.head_dim), 0, a);
+}
+
+cudaError_t launch_kv_store_chunk(const Launch& L, const KvChunkArgs& a) {
+  if (a.n_tok == 0) return cudaSuccess;
+  return launch_ex(L, kv_store_chunk_kernel, dim3(a.n_tok, a.pool.n_kv_heads), dim3(a.pool.head_dim), 0, a);
+}
+
+cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a) {
+  if (a.n_tok == 0) return cudaSuccess;
+  const int G = a.n_heads / a.n_kv_heads;
+  if (G < 1 || G > 16) return cudaErrorInvalidValue;
+  const int per_block = 4 * (16 / G);
+  const dim3 grid((a.n_tok + per_block - 1) / per_block, a.n_kv_heads);
+  if (a.head_dim == 128) return launch_ex(L, prefill_attn_kernel<128>, grid, dim3(128), 0, a);
+  if (a.head_dim == 64) return launch_ex(L, prefill_attn_kernel<64>, grid, dim3(128), 0, a);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t attention_max_cluster(int head_dim, int kv_dtype, int* out) {

@@ -78,6 +78,39 @@ cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, in
 // 2048-byte tiles [N/16][ceil(K/64)]: lane L = (g, t) of a tile holds rows
 // g and g+8 at k = 64c + 16t .. 16t+15 (32 bytes each); k >= K is zero.
 cudaError_t launch_f16_to_tiles(cudaStream_t s, const __half* src, int N, int K, uint8_t* tiles);
+// Exact two-term fp16 copy (hi + lo = s q + m) of a tiled W4 matrix for the prefill GEMM, rows
+// in canonical order except MAP_SWIGLU (gate / up interleaved in blocks of 64). hi, lo: [N][K].
+cudaError_t launch_w4_tiles_to_hilo(cudaStream_t s, const uint8_t* tiles, int N, int K, int map, int map_arg,
+                                    __half* hi, __half* lo);
+
+// ---------------------------------------------------------------- chunked prefill (tcgen05)
+// Y = X W^T over an exact two-term weight copy, 128 x 128 tiles. M: tokens, N: copy rows (a multiple
+// of 128), K. Epilogues: EPI_QKV (fp16 out, q and k rotated at position pos0 + row), EPI_RESID
+// (r[row][n] += y), EPI_SWIGLU (out[row][j] = fp16(silu(gate) up) from interleaved copy rows).
+struct TcGemmArgs {
+  int32_t M, N, K;
+  int32_t n_valid;  // output columns that exist (RESID: N of the matrix; SWIGLU: F)
+  float* r;
+  int32_t ldr;
+  __half* out;
+  int32_t ldo;
+  int32_t head_dim, n_rot_heads, pos0;
+  const float* rope_cos;
+  const float* rope_sin;
+  uint32_t* err;
+};
+struct TcMaps {
+  const void* a;  // 128-byte tensor maps: activations [M][K], weight hi [N][K], weight lo [N][K]
+  const void* hi;
+  const void* lo;
+};
+// A 2-D fp16 tensor map over row-major [rows][cols] with 64 x 128 boxes and 128-byte swizzle.
+bool make_tmap_2d(void* map_out, const void* base, int64_t rows, int64_t cols);
+int tc_gemm_rows_multiple();
+cudaError_t launch_tc_gemm(const Launch& L, const TcMaps& m, const TcGemmArgs& a, int epi);
+cudaError_t launch_rows_to_resid(const Launch& L, const __half* x, float* r, int T, int D);
+cudaError_t launch_rmsnorm_rows(const Launch& L, const float* r, const __half* gamma, float eps, int T, int D,
+                                __half* xn);
 
 // ---------------------------------------------------------------- step prologue
 // block-table writes, fp16 input -> fp32 residual and its sum of squares (ss_part[0][b])
@@ -95,6 +128,32 @@ struct KvStoreArgs {
   PoolGeom pool;
 };
 cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a);
+
+// Chunked prefill: the rotated k and v of n_tok chunk tokens (rows of the QKV output) stored at
+// positions pos0.. of one layer, by the same quantisers.
+struct KvChunkArgs {
+  const __half* qkv;  // [n_tok][qkv_ld]: q [Hq d], k [Hkv d], v [Hkv d]
+  int32_t qkv_ld, n_heads;
+  int32_t n_tok, pos0, layer;
+  const int32_t* table;
+  PoolGeom pool;
+};
+cudaError_t launch_kv_store_chunk(const Launch& L, const KvChunkArgs& a);
+
+// Chunked prefill: causal GQA attention of the chunk's queries (token t at position pos0 + t) over the
+// pool positions 0 .. pos0 + t (the chunk's own keys stored first). Pool values are widened to fp16 in
+// shared memory (exact for FP16 storage).
+struct PrefillAttnArgs {
+  const __half* qkv;  // [n_tok][qkv_ld]
+  int32_t qkv_ld;
+  __half* o;          // [n_tok][ldo]
+  int32_t ldo;
+  int32_t n_tok, pos0;
+  int32_t n_heads, n_kv_heads, head_dim, layer;
+  const int32_t* table;
+  PoolGeom pool;
+};
+cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a);
 
 // ---------------------------------------------------------------- split-K flash-decode attention
 struct AttnArgs {

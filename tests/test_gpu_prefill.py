@@ -1,0 +1,144 @@
+"""GPU parity of the chunked prefill (mag_prefill_chunk).
+
+* Tiny layer (FFN 688: ragged K and a ragged gate-up tile; G = 2; d = 64) with
+  FP16 / INT8 / INT4 KV: two chunks (37 tokens, one partial 128-row tile; 150
+  tokens, two tiles) on a 128-token cache, then one decode step. The output
+  of each chunk's last token and of the decode step (which reads every key the
+  chunks stored) against the oracle's causal forward pass.
+* A chunk on an empty cache (position 0 onwards).
+* Two 8B-shaped layers with the full vocabulary: a 64-token chunk on an
+  800-token FP16 cache against the oracle.
+* The 8B chunked-prefill configuration at full size (32 layers, a 512-token
+  chunk on an 800-token FP16 cache): the oracle can not run it in a test, so
+  the chunk's last logits are compared with the same 512 tokens decoded one by
+  one on the GPU (a property of any correct prefill). The bar there is the
+  sum of the two paths' own distance to the oracle at 32 layers (each about
+  2e-3 rel-L2, the oracle's one-ulp input sensitivity at that depth).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_decode_step_gb300 as mag
+import synth
+from synth import driver
+from synth.workloads import KV_FP16, KV_INT4, KV_INT8, LLAMA8B, PREFILL_8B, TINY, Workload, shrink
+from tests.helpers import TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, oracle_weights, prior_kv, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mag.build()
+    assert torch.cuda.is_available()
+
+
+def _compare(got, ref, what, bar=TOL_REL_L2):
+    a, b = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(a)), what
+    ma, rl = max_abs(a, b), rel_l2(a, b)
+    print(f"{what}: max-abs {ma:.3e} rel-L2 {rl:.3e}")
+    assert ma <= TOL_MAX_ABS and rl <= bar, f"{what}: max-abs {ma:.3e}, rel-L2 {rl:.3e}"
+
+
+def _run(wl: Workload, seed: int, chunks, decode_after=1, random_gain=True):
+    shape = wl.shape
+    total = sum(chunks) + decode_after
+    ctx, sids = driver.setup(wl, seed, random_gain=random_gain, extra_tokens=total)
+    sid = sids[0]
+    w = oracle_weights(shape, seed, random_gain)
+    cfg = model_cfg(shape, wl.kv_dtype)
+    p = wl.prior[0]
+    kv = oracle.KV(cfg, p + total + 8)
+    if p:
+        k, v = prior_kv(shape, seed, 0, p)
+        kv.append(k, v)
+    c, s = oracle.rope_table(p + total + 2, shape.head_dim, shape.rope_base)
+    width = shape.vocab or shape.hidden
+    pos = p
+    for i, T in enumerate(chunks):
+        x = synth.hidden_f16(seed, T, shape.hidden, tag=f"chunk{i}")
+        out = torch.empty(width, dtype=torch.float16, device="cuda")
+        ctx.prefill_chunk(sid, T, torch.from_numpy(x).cuda(), out)
+        ctx.sync()
+        pos += T
+        assert ctx.session_length(sid) == pos
+        ref = oracle.forward(cfg, w, [kv], [T], x, c, s)[0]
+        _compare(out.cpu().numpy(), ref, f"{wl.name} chunk {i} ({T} tokens)")
+    for j in range(decode_after):
+        x = synth.hidden_f16(seed, 1, shape.hidden, tag=f"after{j}")
+        out = torch.empty((1, width), dtype=torch.float16, device="cuda")
+        ctx.decode_step([sid], torch.from_numpy(x).cuda(), out)
+        ctx.sync()
+        ref = oracle.forward(cfg, w, [kv], [1], x, c, s)
+        _compare(out.cpu().numpy(), ref, f"{wl.name} decode after the chunks")
+    return ctx
+
+
+@pytest.mark.parametrize("dt", [KV_FP16, KV_INT8, KV_INT4])
+def test_tiny_prefill_chunks_then_decode(dt):
+    wl = Workload(f"tiny-prefill-kv{dt}", TINY, dt, 1, (128,), chunk=160)
+    ctx = _run(wl, 21 + dt, (37, 150))
+    st = ctx.memory_stats()
+    assert st["prefill_weight_bytes"] > 0 and st["prefill_arena_bytes"] > 0
+
+
+def test_tiny_prefill_on_empty_cache():
+    wl = Workload("tiny-prefill-empty", TINY, KV_FP16, 1, (0,), chunk=40)
+    _run(wl, 25, (40,), decode_after=2)
+
+
+def test_prefill_unsupported_without_max_chunk():
+    wl = Workload("tiny-no-chunk", TINY, KV_FP16, 1, (16,))
+    ctx, sids = driver.setup(wl, 26)
+    assert ctx.memory_stats()["prefill_weight_bytes"] == 0
+    x = torch.zeros((4, TINY.hidden), dtype=torch.float16, device="cuda")
+    out = torch.empty(TINY.hidden, dtype=torch.float16, device="cuda")
+    with pytest.raises(mag.MagError) as e:
+        ctx.prefill_chunk(sids[0], 4, x, out)
+    assert e.value.status == mag.ERR_UNSUPPORTED
+    assert ctx.session_length(sids[0]) == 16
+
+
+@pytest.mark.slow
+def test_8b_two_layers_prefill_chunk():
+    shape = shrink(LLAMA8B, n_layers=2)
+    wl = Workload("8b2L-prefill-64-on-800", shape, KV_FP16, 1, (800,), chunk=64)
+    _run(wl, 27, (64,), decode_after=0, random_gain=False)
+
+
+@pytest.mark.slow
+def test_8b_prefill_512_on_800_matches_token_by_token_decode():
+    wl = PREFILL_8B
+    shape, T, p = wl.shape, wl.chunk, wl.prior[0]
+    seed = 28
+    x = synth.hidden_f16(seed, T, shape.hidden, tag="chunk0")
+    width = shape.vocab
+    # the chunk at once
+    ctx, sids = driver.setup(wl, seed, extra_tokens=T)
+    out_p = torch.empty(width, dtype=torch.float16, device="cuda")
+    ctx.prefill_chunk(sids[0], T, torch.from_numpy(x).cuda(), out_p)
+    ctx.sync()
+    assert ctx.session_length(sids[0]) == p + T
+    got_p = out_p.cpu().numpy().astype(np.float64)
+    ctx.close()
+    torch.cuda.empty_cache()
+    # the same tokens one decode step at a time
+    wl_d = Workload(wl.name + "-decode", shape, wl.kv_dtype, 1, wl.prior)
+    ctx, sids = driver.setup(wl_d, seed, extra_tokens=T)
+    xd = torch.from_numpy(x).cuda()
+    out_d = torch.empty((1, width), dtype=torch.float16, device="cuda")
+    for t in range(T):
+        ctx.decode_step([sids[0]], xd[t:t + 1], out_d)
+    ctx.sync()
+    got_d = out_d.cpu().numpy()[0].astype(np.float64)
+    ctx.close()
+    assert np.all(np.isfinite(got_p)) and np.all(np.isfinite(got_d))
+    ma, rl = max_abs(got_p, got_d), rel_l2(got_p, got_d)
+    print(f"{wl.name}: prefill vs token-by-token decode: max-abs {ma:.3e} rel-L2 {rl:.3e}")
+    assert ma <= TOL_MAX_ABS and rl <= 5e-3
+    top = np.argsort(got_d)[-2:]
+    if got_d[top[1]] - got_d[top[0]] > 2 * TOL_MAX_ABS:
+        assert int(np.argmax(got_p)) == int(top[1])
