@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from synth.workloads import (DECODE_8B, LLAMA8B, LONG_FP16, LONG_INT4, LONG_INT8, KV_FP16, KV_INT4, KV_INT8,  # noqa
+                             PREFILL_8B,
                              Workload, agent_batch, shrink)
 
 METRIC = "decode tokens/s per GB300 and achieved HBM GB/s (% of peak) per decode step"
@@ -402,7 +403,83 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks,
         "setup_s": t_setup,
     }
+    if not args.no_prefill:
+        ctx.close()
+        del ctx
+        torch.cuda.empty_cache()
+        line["prefill"] = run_prefill(args, tc)
     print(json.dumps(line), flush=True)
+
+
+def prefill_flops(shape, prior: int, T: int) -> float:
+    """Algorithmic FLOPs of one chunk: 2 T N K over the projections, QK^T and PV over the causal key
+    ranges, and the last token's LM head (the two-term weight copy's second pass is not counted)."""
+    D, F, d = shape.hidden, shape.ffn, shape.head_dim
+    per_layer = shape.qkv_rows * D + D * shape.n_heads * d + 2 * F * D + D * F
+    keys = T * (prior + 1) + T * (T - 1) // 2
+    attn = 4 * shape.n_heads * d * keys
+    return shape.n_layers * (2.0 * T * per_layer + attn) + 2.0 * shape.vocab * D
+
+
+def run_prefill(args, tc_peak):
+    """The chunked-prefill configuration: T-token chunks on fresh sessions holding the prior cache."""
+    import torch
+    import quantized_decode_step_gb300 as mag
+    import synth
+    from synth import driver, hidden_f16
+
+    wl = PREFILL_8B
+    if args.layers:
+        from dataclasses import replace as _replace
+        wl = _replace(wl, name=wl.name + f"-{args.layers}layers", shape=shrink(wl.shape, n_layers=args.layers))
+    shape, T, p = wl.shape, wl.chunk, wl.prior[0]
+    warm, runs = 2, 3
+    n_sets = warm + runs
+    blocks = n_sets * -(-(p + T) // 16)
+    stream = torch.cuda.Stream()
+    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sets, max_batch=1,
+                          max_chunk=T, max_context=p + T)
+    t_setup = time.time()
+    ctx = mag.Context(cfg, stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        driver.load_weights(ctx, shape, args.seed)
+        sids = [ctx.session_open() for _ in range(n_sets)]
+        L, H, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
+        k = np.empty((L, p, H, d), np.float16)
+        v = np.empty((L, p, H, d), np.float16)
+        for l in range(L):
+            k[l] = synth.prior_kv_f16(args.seed, 0, l, "K", p, H, d)
+            v[l] = synth.prior_kv_f16(args.seed, 0, l, "V", p, H, d)
+        kt, vt = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
+        for sid in sids:
+            ctx.kv_append(sid, p, kt, vt)
+        x = torch.from_numpy(hidden_f16(args.seed, T, shape.hidden, tag="chunk0")).cuda()
+        out = torch.empty(shape.vocab or shape.hidden, dtype=torch.float16, device="cuda")
+    stream.synchronize()
+    t_setup = time.time() - t_setup
+    for i in range(warm):
+        ctx.prefill_chunk(sids[i], T, x, out)
+    stream.synchronize()
+    launches = ctx.last_step_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(runs):
+        ctx.prefill_chunk(sids[warm + i], T, x, out)
+    ev1.record(stream)
+    ev1.synchronize()
+    s_chunk = ev0.elapsed_time(ev1) / 1e3 / runs
+    fl = prefill_flops(shape, p, T)
+    st = ctx.memory_stats()
+    ctx.close()
+    achieved = fl / s_chunk / 1e12
+    return {"workload": wl.name, "chunk": T, "prior": p, "ms_per_chunk": s_chunk * 1e3,
+            "tokens_per_s": T / s_chunk, "algorithmic_tflop_per_chunk": fl / 1e12,
+            "roofline": {"bound": "tensor", "scope": "whole chunk", "achieved": achieved, "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                         "note": "fp16 kind::f16 at the measured bf16 rate; the exact two-term weights double "
+                                 "the tensor work, which is not counted as achieved"},
+            "launches_per_chunk": launches, "prefill_weight_bytes": st["prefill_weight_bytes"],
+            "setup_s": t_setup}
 
 
 def main():
@@ -414,6 +491,7 @@ def main():
     ap.add_argument("--workload", default=DECODE_8B.name)
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill leg")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: the same per-layer shapes with fewer layers (not a bench configuration)")
     args = ap.parse_args()

@@ -545,19 +545,48 @@ __global__ void kv_store_chunk_kernel(const KvChunkArgs a) {
   store_vec(a.pool, a.layer, blk, pos & 15, h, 1, xv, red);
 }
 
-// pool value (which 0 = K, 1 = V) of (block, slot, head), element i, widened to fp16
-__device__ __forceinline__ __half pool_value(const PoolGeom& P, int layer, int blk, int which, int head, int slot,
-                                             int i) {
+// 8 consecutive values (dims c8 .. c8+7) of one pool vector in raw form: fp16 16 B, INT8 8 B + the
+// vector's scale, INT4 4 B + the (scale, min) of their group.
+struct RawUnit {
+  uint4 d;
+  uint32_t meta;
+};
+__device__ __forceinline__ RawUnit load_unit(const PoolGeom& P, int layer, int blk, int which, int head, int slot,
+                                             int c8) {
+  RawUnit r;
+  r.meta = 0;
   const uint8_t* data = pool_vec(P, layer, blk, which, head, slot);
-  if (P.kv_dtype == 0) return reinterpret_cast<const __half*>(data)[i];
-  const uint8_t* meta = pool_vec(P, layer, blk, which + 2, head, slot);
-  if (P.kv_dtype == 1) {
-    const float s = __half2float(*reinterpret_cast<const __half*>(meta));
-    return __float2half_rn(s * (float)reinterpret_cast<const int8_t*>(data)[i]);
+  if (P.kv_dtype == 0) {
+    r.d = *reinterpret_cast<const uint4*>(data + c8 * 2);
+  } else {
+    const uint8_t* meta = pool_vec(P, layer, blk, which + 2, head, slot);
+    if (P.kv_dtype == 1) {
+      const uint2 v = *reinterpret_cast<const uint2*>(data + c8);
+      r.d = make_uint4(v.x, v.y, 0, 0);
+      r.meta = *reinterpret_cast<const uint16_t*>(meta);
+    } else {
+      r.d = make_uint4(*reinterpret_cast<const uint32_t*>(data + c8 / 2), 0, 0, 0);
+      r.meta = reinterpret_cast<const uint32_t*>(meta)[c8 >> 5];
+    }
   }
-  const __half2 sm = reinterpret_cast<const __half2*>(meta)[i >> 5];
-  const int q = (data[i >> 1] >> (4 * (i & 1))) & 15;
-  return __float2half_rn(__fadd_rn(__fmul_rn(__low2float(sm), (float)q), __high2float(sm)));
+  return r;
+}
+// the unit as 8 fp16 values (INT8: s q; INT4: s q + m, in fp32 then rounded; FP16 as stored)
+__device__ __forceinline__ void widen_unit(int dt, const RawUnit& r, __half (&h)[8]) {
+  if (dt == 0) {
+    *reinterpret_cast<uint4*>(h) = r.d;
+  } else if (dt == 1) {
+    const float s = __half2float(__ushort_as_half((unsigned short)r.meta));
+    const int8_t* q = reinterpret_cast<const int8_t*>(&r.d);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(s * (float)q[e]);
+  } else {
+    const __half2 sm = u32_as_h2(r.meta);
+    const float s = __low2float(sm), mn = __high2float(sm);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      h[e] = __float2half_rn(__fadd_rn(__fmul_rn(s, (float)((r.d.x >> (4 * e)) & 15u)), mn));
+  }
 }
 
 // Block: one KV head and 4 warps x 16 MMA rows; a row is (token, query head of the group), 16/G tokens per
@@ -603,14 +632,34 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   const int last_tok = min(a.n_tok, t_blk + 4 * tpw) - 1;
   const int n_blocks = (a.pos0 + last_tok) / 16 + 1;
   const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
-  for (int b = 0; b < n_blocks; ++b) {
+  // each thread moves kUnits (vector, 8-dim) units of K and of V per pool block; the next block's raw bytes are
+  // loaded while the current one is computed
+  constexpr int kUnits = 16 * D / 8 / 128;
+  const int dt = a.pool.kv_dtype;
+  RawUnit nk[kUnits], nv[kUnits];
+  auto fetch = [&](int b) {
     const int phys = a.table[b];
-    for (int e = threadIdx.x; e < 16 * D; e += blockDim.x) {
-      const int slot = e / D, i = e - slot * D;
-      sk[slot][i] = pool_value(a.pool, a.layer, phys, 0, gk, slot, i);
-      svt[i][slot] = pool_value(a.pool, a.layer, phys, 1, gk, slot, i);
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+      const int u = threadIdx.x + 128 * j, slot = u / (D / 8), c8 = (u - slot * (D / 8)) * 8;
+      nk[j] = load_unit(a.pool, a.layer, phys, 0, gk, slot, c8);
+      nv[j] = load_unit(a.pool, a.layer, phys, 1, gk, slot, c8);
+    }
+  };
+  if (n_blocks > 0) fetch(0);
+  for (int b = 0; b < n_blocks; ++b) {
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+      const int u = threadIdx.x + 128 * j, slot = u / (D / 8), c8 = (u - slot * (D / 8)) * 8;
+      __half h[8];
+      widen_unit(dt, nk[j], h);
+      *reinterpret_cast<uint4*>(&sk[slot][c8]) = *reinterpret_cast<uint4*>(h);
+      widen_unit(dt, nv[j], h);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) svt[c8 + e][slot] = h[e];
     }
     __syncthreads();
+    if (b + 1 < n_blocks) fetch(b + 1);
     if (warp_last >= t_warp && 16 * b <= a.pos0 + warp_last) {
       float sfr[2][4];
 #pragma unroll
