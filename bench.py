@@ -283,7 +283,8 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.Stream()
     order = pool_order(args.seed, blocks) if wl.scattered_pool else None
     cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sess, max_batch=B,
-                          max_context=max(wl.prior) + 1, pool_order=order)
+                          max_context=max(wl.prior) + 1, pool_order=order,
+                          flags=mag.FLAG_NO_GRAPH if args.eager else 0)
     t_setup = time.time()
     ctx = mag.Context(cfg, stream.cuda_stream)
     lm_keep = {}
@@ -492,6 +493,8 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill leg")
+    ap.add_argument("--eager", action="store_true",
+                    help="profiling aid: launch the step's kernels one by one instead of replaying a CUDA graph")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: the same per-layer shapes with fewer layers (not a bench configuration)")
     args = ap.parse_args()

@@ -110,7 +110,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* acc_full = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  // the token tiles of one weight tile are neighbours in launch order, so the weights come from HBM once
+  // and from L2 for the other token tiles
+  const int n0 = blockIdx.y * BN, m0 = blockIdx.x * BM;
   const int nk = (a.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -306,7 +308,7 @@ cudaError_t launch_tc_t(const Launch& L, const TcMaps& m, const TcGemmArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
+  cfg.gridDim = dim3((a.M + BM - 1) / BM, (a.N + BN - 1) / BN);
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
