@@ -503,24 +503,27 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // ---- merge the cluster's splits through distributed shared memory
   cluster.sync();
   const int rank = (int)cluster.block_rank();
-  if (tid < G) {
-    float mm = -INFINITY;
-    for (int q = 0; q < S; ++q) mm = fmaxf(mm, *cluster.map_shared_rank(&s_pm[tid], q));
-    float l = 0.f;
-    for (int q = 0; q < S; ++q) {
-      const float mq = *cluster.map_shared_rank(&s_pm[tid], q);
-      const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
-      s_w[q][tid] = e;
-      l += *cluster.map_shared_rank(&s_pl[tid], q) * e;
-    }
-    for (int q = 0; q < S; ++q) s_w[q][tid] /= l;
+  // weights of the splits: warp w merges heads w, w + 4, ..., lane q reads rank q (one remote round trip)
+  for (int h = warp; h < G; h += 4) {
+    const float mq = lane < S ? *cluster.map_shared_rank(&s_pm[h], lane) : -INFINITY;
+    const float lq = lane < S ? *cluster.map_shared_rank(&s_pl[h], lane) : 0.f;
+    float mm = mq;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
+    const float l = warp_sum(lq * e);
+    if (lane < S) s_w[lane][h] = e / l;
   }
   __syncthreads();
   const int per = (G * D + S - 1) / S;  // this rank's share of the outputs
   for (int idx = rank * per + tid; idx < min((rank + 1) * per, G * D); idx += blockDim.x) {
     const int h = idx / D, dim = idx - h * D;
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = q < S ? *cluster.map_shared_rank(&s_acc[0][h][dim], q) : 0.f;
     float o = 0.f;
-    for (int q = 0; q < S; ++q) o += *cluster.map_shared_rank(&s_acc[0][h][dim], q) * s_w[q][h];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) o = q < S ? fmaf(v[q], s_w[q][h], o) : o;
     a.o[(int64_t)b * a.ldo + (int64_t)(gk * G + h) * D + dim] = __float2half_rn(o);
   }
   cluster.sync();  // keep this block's shared memory alive until every rank has read it
