@@ -240,11 +240,27 @@ __device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
   return o;
 }
 
-constexpr int kAttnSlots = 2;  // per-warp ring depth, in (block, KV head) units
+constexpr int kAttnSlots = 3;  // per-warp ring depth, in (block, KV head) units
+
+// Shared-memory image of the four warps' partial outputs, [warp][head row][t][jj][n] with the t and head
+// strides padded so that the float4 stores of a quarter-warp fall into distinct banks. n is the PV
+// n-tile, (2t + jj) the column within it: dim = (2t + jj) NV + v_slot_dim(n). It and the block's
+// merged partial o [head][dim] reuse the rings' shared memory once every warp has left its loop.
+template <int D>
+struct AccGeom {
+  static constexpr int kNV = D / 8;
+  static constexpr int kTS = 2 * kNV + 4;                         // floats per t
+  static constexpr int kRow = (4 * kTS + 16 + 31) / 32 * 32 + 16;  // floats per head row, = 16 mod 32
+  static constexpr int kWarp = 8 * kRow;
+  static constexpr size_t kAccBytes = (size_t)4 * kWarp * 4;
+  static constexpr size_t kBytes = kAccBytes + (size_t)8 * D * 4;  // + the partial o
+};
 
 template <int D, int DT>
 __host__ __device__ constexpr size_t attn_smem_bytes() {
-  return (size_t)4 * kAttnSlots * SlotGeom<D, DT>::kBytes;
+  return (size_t)4 * kAttnSlots * SlotGeom<D, DT>::kBytes > AccGeom<D>::kBytes
+             ? (size_t)4 * kAttnSlots * SlotGeom<D, DT>::kBytes
+             : AccGeom<D>::kBytes;
 }
 
 // One block of the grid per (split, KV head, session); the blocks of a
@@ -254,16 +270,17 @@ template <int D, int DT>
 __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   namespace cg = cooperative_groups;
   using SG = SlotGeom<D, DT>;
+  using AG = AccGeom<D>;
   constexpr int NS = D / 32;  // 32-dim slabs of K (one INT4 group each)
   constexpr int NV = D / 8;   // V n-tiles
   constexpr int NW = D / 16;  // words per V row of a lane
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_m[4][8], s_l[4][8];
-  __shared__ float s_acc[4][8][D];
+  float* s_acc = reinterpret_cast<float*>(smem);                    // after the loops
+  float* s_po = reinterpret_cast<float*>(smem + AG::kAccBytes);      // this block's partial o [head][dim]
   __shared__ float s_pm[8], s_pl[8];  // this block's partial (m, l) per head
   __shared__ __half s_kv[2][D];
   __shared__ float s_red[8];
-  __shared__ float s_w[16][8];  // merge weights of the cluster's splits
 
   cg::cluster_group cluster = cg::this_cluster();
   const int split = blockIdx.x, gk = blockIdx.y, b = blockIdx.z;
@@ -282,12 +299,15 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // this warp's blocks: blk0 + warp + 4 j; the new token's block, if it is one
   // of them, is the last
   const int nb = blk0 + warp < blk1 ? (blk1 - blk0 - warp + 3) / 4 : 0;
+  // physical ids of the warp's first 32 blocks, one lane each (one round trip for all of them)
+  const int phys_l = lane < nb ? table[blk0 + warp + 4 * lane] : 0;
+  auto phys_of = [&](int j) { return j < 32 ? __shfl_sync(0xffffffffu, phys_l, j) : table[blk0 + warp + 4 * j]; };
   uint8_t* ring = smem + (size_t)warp * kAttnSlots * SG::kBytes;
   int issued = 0;
   for (; issued < min(nb, kAttnSlots); ++issued) {
     const int blk = blk0 + warp + 4 * issued;
     if (blk == new_blk) break;
-    issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, table[blk], gk, lane);
+    issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys_of(issued), gk, lane);
     cp_async_commit();
   }
   pdl_wait();
@@ -307,7 +327,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     __threadfence_block();
     __syncthreads();
     if (issued < min(nb, kAttnSlots)) {  // this warp's deferred fetch of the new token's block
-      issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, table[new_blk], gk, lane);
+      issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys, gk, lane);
       cp_async_commit();
       ++issued;
     }
@@ -343,20 +363,22 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
 #pragma unroll
   for (int n = 0; n < NV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
+  int slot_i = 0;
   for (int j = 0; j < nb; ++j) {
     const int blk = blk0 + warp + 4 * j;
-    uint8_t* slot = ring + (j & (kAttnSlots - 1)) * SG::kBytes;
+    uint8_t* slot = ring + slot_i * SG::kBytes;
     cp_async_wait<kAttnSlots - 1>();
     __syncwarp();
     const uint8_t* kd = slot;
     const uint8_t* vd = slot + SG::kData;
     const uint8_t* km = slot + 2 * SG::kData;
     const uint8_t* vm = km + SG::kMeta;
-    // ---- scores S[head][token] of the block's 16 tokens (two n-tiles of 8)
+    // ---- scores S[head][token] of the block's 16 tokens (two n-tiles of 8), the slabs in two
+    // independent accumulation chains
     float sfr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+      float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const uint8_t* krow = kd + (gi + 8 * nt) * SG::kDb;
       if (DT == 2) {
         const uint8_t* kmeta0 = km + (8 * nt + 2 * t) * SG::kMb;
@@ -369,8 +391,8 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
           // per (token, group): score += s * (q . codes) + m * sum(q)
           const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + 4 * s));
           const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + SG::kMb + 4 * s));
-          sfr[nt][0] = fmaf(f0.x, as[0], fmaf(f0.y, qsum[s], sfr[nt][0]));
-          sfr[nt][1] = fmaf(f1.x, as[1], fmaf(f1.y, qsum[s], sfr[nt][1]));
+          s2[s & 1][0] = fmaf(f0.x, as[0], fmaf(f0.y, qsum[s], s2[s & 1][0]));
+          s2[s & 1][1] = fmaf(f1.x, as[1], fmaf(f1.y, qsum[s], s2[s & 1][1]));
         }
       } else {
 #pragma unroll
@@ -383,10 +405,12 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
             i8x4_to_h2(w.x, kb.x, kb.y);
             i8x4_to_h2(w.y, kb.z, kb.w);
           }
-          mma_16816(sfr[nt], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
-          mma_16816(sfr[nt], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
+          mma_16816(s2[s & 1], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
+          mma_16816(s2[s & 1], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sfr[nt][e] = s2[0][e] + s2[1][e];
     }
     // this lane's tokens: (nt, jj) -> 16 blk + 8 nt + 2 t + jj
     float ks[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
@@ -452,10 +476,10 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     load_v_row<D, DT>(vd + (8 + 2 * t) * SG::kDb, vm + (8 + 2 * t) * SG::kMb, gi, v8);
     load_v_row<D, DT>(vd + (9 + 2 * t) * SG::kDb, vm + (9 + 2 * t) * SG::kMb, gi, v9);
     __syncwarp();
-    // the slot is free: fetch the block after next into it
-    if (j + kAttnSlots < nb)
-      issue_block<D, DT>(slot, a.pool, a.layer, table[blk + 4 * kAttnSlots], gk, lane);
+    // the slot is free: fetch the block kAttnSlots ahead into it
+    if (j + kAttnSlots < nb) issue_block<D, DT>(slot, a.pool, a.layer, phys_of(j + kAttnSlots), gk, lane);
     cp_async_commit();
+    slot_i = slot_i + 1 == kAttnSlots ? 0 : slot_i + 1;
 #pragma unroll
     for (int n = 0; n < NV; ++n) {
       const uint32_t b0 = pair_tokens(v0, v1, n), b1 = pair_tokens(v8, v9, n);
@@ -465,66 +489,71 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   }
   cp_async_wait<0>();
 
-  // ---- merge the 4 warps of this block into the block's partial (m, l, o)
+  // ---- merge the 4 warps of this block into the block's partial (m, l, o); the barrier below also
+  // ends every warp's use of its ring, whose memory the merge reuses
   float l_tot = l_part;
   l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
   l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-  if (hv) {
-    if (t == 0) {
-      s_m[warp][gi] = m_run;
-      s_l[warp][gi] = l_tot;
-    }
-#pragma unroll
-    for (int n = 0; n < NV; ++n) {
-      s_acc[warp][gi][(2 * t) * NV + v_slot_dim<DT>(n)] = acc[n][0];
-      s_acc[warp][gi][(2 * t + 1) * NV + v_slot_dim<DT>(n)] = acc[n][1];
-    }
+  if (hv && t == 0) {
+    s_m[warp][gi] = m_run;
+    s_l[warp][gi] = l_tot;
   }
   __syncthreads();
-  if (tid < G) {
-    float mm = -INFINITY;
+  if (hv) {
+    // this warp's share, rescaled to the block's running maximum of the head
+    float mm = s_m[0][gi];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) mm = fmaxf(mm, s_m[w][tid]);
-    float l = 0.f;
+    for (int w = 1; w < 4; ++w) mm = fmaxf(mm, s_m[w][gi]);
+    const float e = mm == -INFINITY ? 0.f : exp2f(m_run - mm);
+    float* dst = s_acc + warp * AG::kWarp + gi * AG::kRow + t * AG::kTS;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) l += s_l[w][tid] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][tid] - mm));
-    s_pm[tid] = mm;  // -inf for a block without keys
-    s_pl[tid] = l;
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int q = 0; q < NV / 4; ++q)
+        *reinterpret_cast<float4*>(dst + jj * NV + 4 * q) =
+            make_float4(acc[4 * q][jj] * e, acc[4 * q + 1][jj] * e, acc[4 * q + 2][jj] * e, acc[4 * q + 3][jj] * e);
+    if (warp == 0 && t == 0) {
+      float l = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) l += s_l[w][gi] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][gi] - mm));
+      s_pm[gi] = mm;  // -inf for a block without keys
+      s_pl[gi] = l;
+    }
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, dim = idx - h * D;
-    const float mm = s_pm[h];
-    float o = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) o += s_acc[w][h][dim] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][h] - mm));
-    s_acc[0][h][dim] = o;  // row 0 of s_acc now holds the block's partial o
+    const int c = dim / NV, r = dim - c * NV;  // column 2t + jj of n-tile v_slot_dim^-1(r)
+    int n = r;
+    if (DT == 2) n = (r & 8) + ((r & 3) << 1) + ((r >> 2) & 1);
+    const int off = h * AG::kRow + (c >> 1) * AG::kTS + (c & 1) * NV + n;
+    s_po[idx] = s_acc[off] + s_acc[AG::kWarp + off] + s_acc[2 * AG::kWarp + off] + s_acc[3 * AG::kWarp + off];
   }
-  // ---- merge the cluster's splits through distributed shared memory
+  // ---- merge the cluster's splits through distributed shared memory: every output reads the S
+  // partials (m, l, o) in one round trip
   cluster.sync();
   const int rank = (int)cluster.block_rank();
-  // weights of the splits: warp w merges heads w, w + 4, ..., lane q reads rank q (one remote round trip)
-  for (int h = warp; h < G; h += 4) {
-    const float mq = lane < S ? *cluster.map_shared_rank(&s_pm[h], lane) : -INFINITY;
-    const float lq = lane < S ? *cluster.map_shared_rank(&s_pl[h], lane) : 0.f;
-    float mm = mq;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-    const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
-    const float l = warp_sum(lq * e);
-    if (lane < S) s_w[lane][h] = e / l;
-  }
-  __syncthreads();
   const int per = (G * D + S - 1) / S;  // this rank's share of the outputs
   for (int idx = rank * per + tid; idx < min((rank + 1) * per, G * D); idx += blockDim.x) {
-    const int h = idx / D, dim = idx - h * D;
-    float v[16];
+    const int h = idx / D;
+    float mq[16], lq[16], oq[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = q < S ? *cluster.map_shared_rank(&s_acc[0][h][dim], q) : 0.f;
-    float o = 0.f;
+    for (int q = 0; q < 16; ++q) {
+      mq[q] = q < S ? *cluster.map_shared_rank(&s_pm[h], q) : -INFINITY;
+      lq[q] = q < S ? *cluster.map_shared_rank(&s_pl[h], q) : 0.f;
+      oq[q] = q < S ? *cluster.map_shared_rank(&s_po[idx], q) : 0.f;
+    }
+    float mm = mq[0];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) o = q < S ? fmaf(v[q], s_w[q][h], o) : o;
-    a.o[(int64_t)b * a.ldo + (int64_t)(gk * G + h) * D + dim] = __float2half_rn(o);
+    for (int q = 1; q < 16; ++q) mm = fmaxf(mm, mq[q]);
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float e = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mm);
+      l = fmaf(lq[q], e, l);
+      o = fmaf(oq[q], e, o);
+    }
+    a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
   }
   cluster.sync();  // keep this block's shared memory alive until every rank has read it
 }
