@@ -252,8 +252,11 @@ def traffic_from_profile(kernel_key: str):
     try:
         with open(path) as f:
             prof = json.load(f)
-        src = os.path.join(ROOT, "quantized_decode_step_gb300", "csrc", prof["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        srcs = prof["sources"] if "sources" in prof else [prof["source"]]
+        hs = hashlib.sha256()
+        for name in srcs:
+            hs.update(open(os.path.join(ROOT, "quantized_decode_step_gb300", "csrc", name), "rb").read())
+        h = hs.hexdigest()[:16]
         e = prof["kernels"][kernel_key]
         return e["dram_bytes_per_launch"] if e.get("source_sha") == h else None
     except Exception:

@@ -9,8 +9,9 @@
 // own ring of shared-memory slots with cp.async.bulk, one slot per copy,
 // completing on the slot's mbarrier, and refills a slot as soon as it holds
 // the slot in registers, so no warp ever waits on another to issue copies.
-// The first copies are issued before the wait on the previous kernel, whose
-// outputs they do not touch. A tile split between warps leaves each warp's partial in shared
+// The first two copies of every warp are issued before the wait on the
+// previous kernel, whose outputs they do not touch, the rest once the
+// activations are staged. A tile split between warps leaves each warp's partial in shared
 // memory; the last warp to finish it adds the parts in warp order
 // (deterministic) and runs the epilogue.
 //
@@ -38,6 +39,8 @@ using namespace pipe;
 // WIN: batch 1, W4, K a multiple of 256 (the host checks): warps take whole 4-chunk windows (one ring
 // slot each) and use the 8 MMA columns for the window's 8 groups rather than for tokens. Only that loop
 // is compiled into such a kernel, which keeps its code (and instruction-cache footprint) small.
+constexpr int kPreFills = 2;  // ring slots per warp filled before the wait on the previous kernel
+
 template <int WFMT, int XSRC, int EPI, int B, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1) gemv_pipe_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -69,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pipe_kernel(const GemvArgs a
     for (int i = 0; i < NS; ++i) mbar_init(full + i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the weights do not depend on earlier kernels: start streaming before waiting for them
-    for (int f = 0; f < min(NS, nf); ++f) issue(f);
+    for (int f = 0; f < min(kPreFills, nf); ++f) issue(f);
   }
   for (int i = tid; i < a.t_max; i += kThreads) reinterpret_cast<uint32_t*>(smem + L.tcnt)[i] = 0;
   int* bounds = reinterpret_cast<int*>(smem + L.bounds);
@@ -82,6 +85,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pipe_kernel(const GemvArgs a
   __half* xw = reinterpret_cast<__half*>(smem + L.x);
   float* xsw = reinterpret_cast<float*>(smem + L.xs);
   stage_x<WFMT, XSRC, B>(a, xw, xsw, reinterpret_cast<float*>(smem + L.red), xrow, grow, [] {});
+  // the rest of the ring is filled once the activations are in: their loads must not queue behind it
+  if (lane == 0)
+    for (int f = kPreFills; f < min(NS, nf); ++f) issue(f);
 
   const uint4* xrow_l = reinterpret_cast<const uint4*>(xw + (size_t)min(g, B - 1) * xrow);
   const float2* X0p = reinterpret_cast<const float2*>(xsw + (size_t)min(2 * t, B - 1) * grow);
