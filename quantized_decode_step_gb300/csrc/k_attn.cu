@@ -299,9 +299,15 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // this warp's blocks: blk0 + warp + 4 j; the new token's block, if it is one
   // of them, is the last
   const int nb = blk0 + warp < blk1 ? (blk1 - blk0 - warp + 3) / 4 : 0;
-  // physical ids of the warp's first 32 blocks, one lane each (one round trip for all of them)
+  // physical ids of the warp's first 32 blocks, one lane each (one round trip for all of them); the
+  // new token's block may have been mapped by this step's prologue, so its id is read after the wait
   const int phys_l = lane < nb ? table[blk0 + warp + 4 * lane] : 0;
-  auto phys_of = [&](int j) { return j < 32 ? __shfl_sync(0xffffffffu, phys_l, j) : table[blk0 + warp + 4 * j]; };
+  int phys_new = -1;
+  auto phys_of = [&](int j) {
+    const int blk = blk0 + warp + 4 * j;
+    const int p = j < 32 ? __shfl_sync(0xffffffffu, phys_l, j) : table[blk];
+    return blk == new_blk ? phys_new : p;
+  };
   uint8_t* ring = smem + (size_t)warp * kAttnSlots * SG::kBytes;
   int issued = 0;
   for (; issued < min(nb, kAttnSlots); ++issued) {
@@ -312,6 +318,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   }
   pdl_wait();
   pdl_trigger();
+  phys_new = table[new_blk];
   const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
 
   // the block that holds the new token appends its K (rotated) and V to the pool
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
       s_kv[1][tid] = qkv[(int64_t)(Hq + Hkv + gk) * D + tid];
     }
     __syncthreads();
-    const int phys = table[new_blk];
+    const int phys = phys_new;
     store_vec(a.pool, a.layer, phys, pos & 15, gk, 0, s_kv[0], s_red);
     store_vec(a.pool, a.layer, phys, pos & 15, gk, 1, s_kv[1], s_red);
     __threadfence_block();

@@ -42,7 +42,7 @@ using namespace pipe;
 constexpr int kPreFills = 2;  // ring slots per warp filled before the wait on the previous kernel
 
 template <int WFMT, int XSRC, int EPI, int B, bool WIN>
-__global__ void __launch_bounds__(kThreads, 1) gemv_pipe_kernel(const GemvArgs a) {
+__device__ __forceinline__ void gemv_pipe_body(const GemvArgs& a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int CB = ChunkFmt<WFMT>::kBytes, SC = ChunkFmt<WFMT>::kPerSlot;
   constexpr uint32_t SB = SC * CB;
@@ -286,9 +286,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pipe_kernel(const GemvArgs a
   }
 }
 
+template <int WFMT, int XSRC, int EPI, int B>
+__global__ void __launch_bounds__(kThreads, 1) gemv_pipe_kernel(const GemvArgs a) {
+  gemv_pipe_body<WFMT, XSRC, EPI, B, false>(a);
+}
+
+// The window kernels need no more than 80 registers a thread.
+template <int WFMT, int XSRC, int EPI>
+__global__ void __maxnreg__(80) gemv_win_kernel(const GemvArgs a) {
+  gemv_pipe_body<WFMT, XSRC, EPI, 1, true>(a);
+}
+
 template <int WFMT, int XSRC, int EPI, int B, bool WIN>
 cudaError_t launch_pipe_b(const Launch& L, const GemvArgs& a) {
-  auto kern = gemv_pipe_kernel<WFMT, XSRC, EPI, B, WIN>;
+  void (*kern)(const GemvArgs);
+  if constexpr (WIN)
+    kern = gemv_win_kernel<WFMT, XSRC, EPI>;
+  else
+    kern = gemv_pipe_kernel<WFMT, XSRC, EPI, B>;
   const PipeSmem sl = pipe_smem(WFMT, B, a.n_chunks, a.stages, a.t_max);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.total);
   if (e != cudaSuccess) return e;
