@@ -628,20 +628,78 @@ __device__ __forceinline__ void widen_unit(int dt, const RawUnit& r, __half (&h)
   }
 }
 
+// ---------------------------------------------------------------- prefill attention
 // Block: one KV head and 4 warps x 16 MMA rows; a row is (token, query head of the group), 16/G tokens per
-// warp. The pool blocks up to the block's last position are widened into shared memory one at a time (K
-// row-major, V transposed) and shared by the warps; each warp runs QK^T, the causal mask, the online
-// softmax and PV (probabilities split into fp16 hi + lo) on m16n8k16 MMAs.
+// warp. Keys go through shared memory in tiles of 64 (four pool blocks), K and V row-major as fp16 with
+// padded rows, double-buffered: FP16 pools are copied with cp.async while the previous tile is computed,
+// INT8 / INT4 pools are widened into the tile (s q, s q + m in fp32, rounded). Each warp runs QK^T
+// (B fragments by ldmatrix), the causal mask, the online softmax and PV (B fragments by ldmatrix.trans,
+// probabilities split into fp16 hi + lo) on m16n8k16 MMAs. Keys past the chunk's last token are zeros.
+constexpr int kPfKeys = 64;  // keys per tile
+
+template <int D>
+struct PfGeom {
+  static constexpr int kRow = D + 8;               // halves per shared-memory row (ldmatrix rows on distinct banks)
+  static constexpr int kTile = kPfKeys * kRow;     // halves per K or V tile
+  static constexpr size_t kBytes = (size_t)4 * kTile * 2;  // K and V, two buffers
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
 template <int D>
 __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs a) {
+  using PG = PfGeom<D>;
   constexpr int KS = D / 16;  // k-steps of QK^T
   constexpr int NV = D / 8;   // n-tiles of PV
-  __shared__ __align__(16) __half sk[16][D + 8];
-  __shared__ __align__(16) __half svt[D][16 + 8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  constexpr int NT = kPfKeys / 8;  // n-tiles of QK^T per key tile
+  extern __shared__ __align__(128) uint8_t smem[];
+  __half* tiles = reinterpret_cast<__half*>(smem);  // [buf][K, V][kPfKeys][kRow]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int G = a.n_heads / a.n_kv_heads, gk = blockIdx.y;
   const int tpw = 16 / G;  // tokens per warp
   const int t_blk = blockIdx.x * 4 * tpw, t_warp = t_blk + warp * tpw;
+  const int dt = a.pool.kv_dtype;
+  const int n_valid = a.pos0 + a.n_tok;  // keys in the pool after the chunk's store
+  const int last_tok = min(a.n_tok, t_blk + 4 * tpw) - 1;
+  const int n_keys = a.pos0 + last_tok + 1;  // keys this block reads
+  const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
+  const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
+
+  // key tile i into buffer bf: FP16 by cp.async (committed as one group), others widened synchronously
+  auto stage = [&](int i, int bf) {
+    __half* kt = tiles + (size_t)bf * 2 * PG::kTile;
+    __half* vt = kt + PG::kTile;
+    constexpr int kChunks = kPfKeys * D / 8;  // 16-byte chunks per K or V tile
+    for (int c = tid; c < 2 * kChunks; c += 128) {
+      const int which = c >= kChunks, cc = which ? c - kChunks : c;
+      const int row = cc / (D / 8), c8 = (cc - row * (D / 8)) * 8;
+      const int kp = i * kPfKeys + row;
+      __half* dst = (which ? vt : kt) + row * PG::kRow + c8;
+      if (kp >= n_valid) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const int phys = a.table[kp >> 4];
+      if (dt == 0) {
+        cp_async16(dst, pool_vec(a.pool, a.layer, phys, which, gk, kp & 15) + c8 * 2);
+      } else {
+        __half h[8];
+        widen_unit(dt, load_unit(a.pool, a.layer, phys, which, gk, kp & 15, c8), h);
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
+      }
+    }
+    cp_async_commit();
+  };
+
   pdl_wait();
   pdl_trigger();
   // the rows of this lane: r0 = g, r1 = g + 8
@@ -654,6 +712,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     hq[h] = gk * G + (r - tl * G);
     live[h] = tl < tpw && tok[h] < a.n_tok;
   }
+  if (n_tiles > 0) stage(0, 0);
   uint32_t qa[KS][4];
 #pragma unroll
   for (int s = 0; s < KS; ++s)
@@ -668,108 +727,94 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   float acc[NV][4];
 #pragma unroll
   for (int n = 0; n < NV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  const int last_tok = min(a.n_tok, t_blk + 4 * tpw) - 1;
-  const int n_blocks = (a.pos0 + last_tok) / 16 + 1;
-  const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
-  // each thread moves kUnits (vector, 8-dim) units of K and of V per pool block; the next block's raw bytes are
-  // loaded while the current one is computed
-  constexpr int kUnits = 16 * D / 8 / 128;
-  const int dt = a.pool.kv_dtype;
-  RawUnit nk[kUnits], nv[kUnits];
-  auto fetch = [&](int b) {
-    const int phys = a.table[b];
+
+  for (int i = 0; i < n_tiles; ++i) {
+    const int bf = i & 1;
+    cp_async_wait<0>();
+    __syncthreads();  // tile i is in; every warp is done with tile i - 1, whose buffer the next stage reuses
+    if (i + 1 < n_tiles) stage(i + 1, bf ^ 1);
+    const __half* kt = tiles + (size_t)bf * 2 * PG::kTile;
+    const __half* vt = kt + PG::kTile;
+    if (warp_last < t_warp || i * kPfKeys > a.pos0 + warp_last) continue;  // no key of this tile is visible
+    // ---- S = Q K^T over the tile's 64 keys: n-tile nt = keys 8 nt .. 8 nt + 7
+    float sfr[NT][4];
 #pragma unroll
-    for (int j = 0; j < kUnits; ++j) {
-      const int u = threadIdx.x + 128 * j, slot = u / (D / 8), c8 = (u - slot * (D / 8)) * 8;
-      nk[j] = load_unit(a.pool, a.layer, phys, 0, gk, slot, c8);
-      nv[j] = load_unit(a.pool, a.layer, phys, 1, gk, slot, c8);
+    for (int nt = 0; nt < NT; ++nt) {
+      sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < KS; s += 2) {
+        // matrices: (k-step s, dims lo), (s, hi), (s + 1, lo), (s + 1, hi) of keys 8 nt ..
+        const int m = lane >> 3;
+        uint32_t kb[4];
+        ldsm_x4(kb, kt + (8 * nt + (lane & 7)) * PG::kRow + 16 * (s + (m >> 1)) + 8 * (m & 1));
+        mma_16816(sfr[nt], qa[s][0], qa[s][1], qa[s][2], qa[s][3], kb[0], kb[1]);
+        mma_16816(sfr[nt], qa[s + 1][0], qa[s + 1][1], qa[s + 1][2], qa[s + 1][3], kb[2], kb[3]);
+      }
     }
-  };
-  if (n_blocks > 0) fetch(0);
-  for (int b = 0; b < n_blocks; ++b) {
+    // causal mask and online softmax; fragment (nt, j): row g + 8 (j >> 1), key 64 i + 8 nt + 2 t + (j & 1)
+    float mx[2] = {-1e30f, -1e30f};
 #pragma unroll
-    for (int j = 0; j < kUnits; ++j) {
-      const int u = threadIdx.x + 128 * j, slot = u / (D / 8), c8 = (u - slot * (D / 8)) * 8;
-      __half h[8];
-      widen_unit(dt, nk[j], h);
-      *reinterpret_cast<uint4*>(&sk[slot][c8]) = *reinterpret_cast<uint4*>(h);
-      widen_unit(dt, nv[j], h);
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) svt[c8 + e][slot] = h[e];
+      for (int j = 0; j < 4; ++j) {
+        const int h = j >> 1, kp = i * kPfKeys + 8 * nt + 2 * t + (j & 1);
+        const bool ok = live[h] && kp <= a.pos0 + tok[h];
+        const float v = ok ? sfr[nt][j] * sc : -INFINITY;
+        sfr[nt][j] = v;
+        mx[h] = fmaxf(mx[h], v);
+      }
+    float corr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+      const float mn = fmaxf(m_run[h], mx[h]);
+      corr[h] = exp2f(m_run[h] - mn);
+      m_run[h] = mn;
     }
-    __syncthreads();
-    if (b + 1 < n_blocks) fetch(b + 1);
-    if (warp_last >= t_warp && 16 * b <= a.pos0 + warp_last) {
-      float sfr[2][4];
+    float ps[2] = {0.f, 0.f};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int s = 0; s < KS; ++s) {
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&sk[8 * nt + g][16 * s + 2 * t]);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&sk[8 * nt + g][16 * s + 2 * t + 8]);
-          mma_16816(sfr[nt], qa[s][0], qa[s][1], qa[s][2], qa[s][3], b0, b1);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const int h = j >> 1;
+        sfr[nt][j] = exp2f(sfr[nt][j] - m_run[h]);  // masked: exp2(-inf) = 0
+        ps[h] += sfr[nt][j];
       }
-      // causal mask and online softmax; fragment (nt, j): row g + 8 (j >> 1), key 16 b + 8 nt + 2 t + (j & 1)
-      float mx[2] = {-1e30f, -1e30f};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * corr[h] + ps[h];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int h = j >> 1, kp = 16 * b + 8 * nt + 2 * t + (j & 1);
-          const bool ok = live[h] && kp <= a.pos0 + tok[h];
-          const float v = ok ? sfr[nt][j] * sc : -INFINITY;
-          sfr[nt][j] = v;
-          mx[h] = fmaxf(mx[h], v);
-        }
-      float corr[2];
+    for (int n = 0; n < NV; ++n) {
+      acc[n][0] *= corr[0];
+      acc[n][1] *= corr[0];
+      acc[n][2] *= corr[1];
+      acc[n][3] *= corr[1];
+    }
+    // ---- O += P V, k-step j = keys 16 j .. 16 j + 15: P of n-tiles 2j, 2j+1 as the A operand, fp16 hi + lo
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-        const float mn = fmaxf(m_run[h], mx[h]);
-        corr[h] = exp2f(m_run[h] - mn);
-        m_run[h] = mn;
-      }
-      float p[2][4], ps[2] = {0.f, 0.f};
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int h = j >> 1;
-          p[nt][j] = exp2f(sfr[nt][j] - m_run[h]);  // masked: exp2(-inf) = 0
-          ps[h] += p[nt][j];
-        }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * corr[h] + ps[h];
-#pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        acc[n][0] *= corr[0];
-        acc[n][1] *= corr[0];
-        acc[n][2] *= corr[1];
-        acc[n][3] *= corr[1];
-      }
-      // P as the A operand in fp16 hi + lo: a0 row g keys 2t,2t+1; a1 row g+8; a2/a3 keys 8+2t, 9+2t
+    for (int j = 0; j < NT / 2; ++j) {
       uint32_t ph[4], pl[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int nt = i >> 1, h = i & 1;
-        const float x0 = p[nt][2 * h], x1 = p[nt][2 * h + 1];
+      for (int q = 0; q < 4; ++q) {
+        const int nt = 2 * j + (q >> 1), h = q & 1;
+        const float x0 = sfr[nt][2 * h], x1 = sfr[nt][2 * h + 1];
         const __half2 hh = __floats2half2_rn(x0, x1);
         const float2 hf = __half22float2(hh);
-        ph[i] = h2_as_u32(hh);
-        pl[i] = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+        ph[q] = h2_as_u32(hh);
+        pl[q] = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
       }
 #pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&svt[8 * n + g][2 * t]);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&svt[8 * n + g][2 * t + 8]);
-        mma_16816(acc[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
-        mma_16816(acc[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      for (int n = 0; n < NV; n += 2) {
+        // matrices: (dims 8n, keys lo), (8n, keys hi), (8n + 8, lo), (8n + 8, hi), transposed
+        const int m = lane >> 3;
+        uint32_t vb[4];
+        ldsm_x4_t(vb, vt + (16 * j + 8 * (m & 1) + (lane & 7)) * PG::kRow + 8 * (n + (m >> 1)));
+        mma_16816(acc[n], ph[0], ph[1], ph[2], ph[3], vb[0], vb[1]);
+        mma_16816(acc[n], pl[0], pl[1], pl[2], pl[3], vb[0], vb[1]);
+        mma_16816(acc[n + 1], ph[0], ph[1], ph[2], ph[3], vb[2], vb[3]);
+        mma_16816(acc[n + 1], pl[0], pl[1], pl[2], pl[3], vb[2], vb[3]);
       }
     }
-    __syncthreads();
   }
   // normalise and store: acc[n][2h + j] = (row g + 8h, dim 8n + 2t + j)
 #pragma unroll
@@ -874,8 +919,12 @@ cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a) 
   if (G < 1 || G > 16) return cudaErrorInvalidValue;
   const int per_block = 4 * (16 / G);
   const dim3 grid((a.n_tok + per_block - 1) / per_block, a.n_kv_heads);
-  if (a.head_dim == 128) return launch_ex(L, prefill_attn_kernel<128>, grid, dim3(128), 0, a);
-  if (a.head_dim == 64) return launch_ex(L, prefill_attn_kernel<64>, grid, dim3(128), 0, a);
+  auto run = [&](auto kern, size_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return e != cudaSuccess ? e : launch_ex(L, kern, grid, dim3(128), smem, a);
+  };
+  if (a.head_dim == 128) return run(prefill_attn_kernel<128>, PfGeom<128>::kBytes);
+  if (a.head_dim == 64) return run(prefill_attn_kernel<64>, PfGeom<64>::kBytes);
   return cudaErrorInvalidValue;
 }
 
