@@ -264,25 +264,58 @@ __global__ void rows_to_resid_kernel(const __half* __restrict__ x, float* __rest
 }
 
 // One block per token row: xn = fp16(r / sqrt(mean(r^2) + eps) * gamma) ("5. Core modules" 5.1, pre-norm).
-__global__ void rmsnorm_rows_kernel(const float* __restrict__ r, const __half* __restrict__ gamma, float eps, int D,
-                                    __half* __restrict__ xn) {
-  __shared__ float red[32];
-  __shared__ float s_inv;
+// D % 4 == 0: each thread keeps its float4 units of the row in registers (one pass over memory) when the
+// row fits kRegUnits units a thread, else reads them twice.
+constexpr int kNormThreads = 256, kRegUnits = 8;
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(const float* __restrict__ r,
+                                                                    const __half* __restrict__ gamma, float eps,
+                                                                    int D, __half* __restrict__ xn) {
+  __shared__ float red[kNormThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.x;
-  const float* rr = r + row * D;
+  const float4* rr = reinterpret_cast<const float4*>(r + row * D);
+  const int U = D / 4;
+  const bool in_regs = U <= kRegUnits * kNormThreads;
+  float4 v[kRegUnits];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) ss = fmaf(rr[i], rr[i], ss);
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < kRegUnits; ++j) {
+      const int u = threadIdx.x + j * kNormThreads;
+      v[j] = u < U ? rr[u] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
+    }
+  } else {
+    for (int u = threadIdx.x; u < U; u += kNormThreads) {
+      const float4 x = rr[u];
+      ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
+    }
+  }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-    s_inv = 1.0f / sqrtf(t / (float)D + eps);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)D + eps);
+  auto put = [&](int u, const float4 x) {
+    const uint2 gh = *reinterpret_cast<const uint2*>(gamma + 4 * u);
+    const float2 g0 = __half22float2(u32_as_h2(gh.x)), g1 = __half22float2(u32_as_h2(gh.y));
+    uint2 o;
+    o.x = h2_as_u32(__floats2half2_rn(x.x * inv * g0.x, x.y * inv * g0.y));
+    o.y = h2_as_u32(__floats2half2_rn(x.z * inv * g1.x, x.w * inv * g1.y));
+    *reinterpret_cast<uint2*>(xn + row * D + 4 * u) = o;
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < kRegUnits; ++j) {
+      const int u = threadIdx.x + j * kNormThreads;
+      if (u < U) put(u, v[j]);
+    }
+  } else {
+    for (int u = threadIdx.x; u < U; u += kNormThreads) put(u, rr[u]);
   }
-  __syncthreads();
-  const float inv = s_inv;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) xn[row * D + i] = __float2half_rn(rr[i] * inv * __half2float(gamma[i]));
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -358,9 +391,18 @@ cudaError_t launch_rows_to_resid(const Launch& L, const __half* x, float* r, int
 cudaError_t launch_rmsnorm_rows(const Launch& L, const float* r, const __half* gamma, float eps, int T, int D,
                                 __half* xn) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_rows_kernel<<<T, 256, 0, L.stream>>>(r, gamma, eps, D, xn);
+  if (D % 4) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(kNormThreads);
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (L.counter) ++*L.counter;
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, rmsnorm_rows_kernel, r, gamma, eps, D, xn);
 }
 
 }  // namespace mag
