@@ -185,26 +185,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (ok) mma_commit(acc_full);
     }
   } else {
-    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 = rows of the tile
+    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 = rows of the tile. A thread holds one row;
+    // the warp passes each 32-column slice through a padded shared-memory square (the ring is free once
+    // the accumulator is complete) so that global memory sees whole 16-byte runs of a row.
     pdl_wait();
     pdl_trigger();
     const int q = warp & 3, m = m0 + q * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    constexpr int SQ = 36;  // floats per staged row: 16-byte aligned, float4 stores of a quarter-warp on distinct banks
+    float* sq = reinterpret_cast<float*>(smem) + q * 2 * 32 * SQ;  // two 32 x 32 squares per warp
+    // this lane's row of square k <- v (32 values)
+    auto put_row = [&](int k, const float (&v)[32]) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(sq + k * 32 * SQ + lane * SQ + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    };
+    // row rr, columns 4 c4 .. 4 c4 + 3 of square k
+    auto get4 = [&](int k, int rr, int c4) { return *reinterpret_cast<const float4*>(sq + k * 32 * SQ + rr * SQ + 4 * c4); };
     if (!mb_wait(acc_full, 0)) {
       atomicOr(a.err, 32u);
     } else {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const bool live = m < a.M;
+      const int row0 = m0 + q * 32;  // first row of this warp's slice
       if (EPI == EPI_RESID) {
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tmem_ld32(trow + c0, v);
-          if (live) {
-            float* o = a.r + (int64_t)m * a.ldr + n0 + c0;
+          put_row(0, v);
+          __syncwarp();
+          // 32 rows x 8 float4: lane takes float4 (lane & 7) of rows lane / 8 + 4 i; all loads first
+          const int c4 = lane & 7, col = n0 + c0 + 4 * c4;
+          float4 y[8];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n0 + c0 + j < a.n_valid) o[j] += v[j];
+          for (int i = 0; i < 8; ++i) {
+            const int rr = (lane >> 3) + 4 * i;
+            y[i] = (row0 + rr < a.M && col < a.n_valid)
+                       ? *reinterpret_cast<const float4*>(a.r + (int64_t)(row0 + rr) * a.ldr + col)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
           }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = (lane >> 3) + 4 * i;
+            if (row0 + rr < a.M && col < a.n_valid) {
+              const float4 x = get4(0, rr, c4);
+              *reinterpret_cast<float4*>(a.r + (int64_t)(row0 + rr) * a.ldr + col) =
+                  make_float4(y[i].x + x.x, y[i].y + x.y, y[i].z + x.z, y[i].w + x.w);
+            }
+          }
+          __syncwarp();
         }
       } else if (EPI == EPI_SWIGLU) {
         // tile columns [0, 64) are gate rows 64 (n0/128) + c, [64, 128) the matching up rows
@@ -212,13 +240,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float g[32], u[32];
           tmem_ld32(trow + c0, g);
           tmem_ld32(trow + c0 + BN / 2, u);
-          const int j0 = (n0 / BN) * (BN / 2) + c0;
-          if (live) {
-            __half* o = a.out + (int64_t)m * a.ldo + j0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j0 + j < a.n_valid) o[j] = __float2half_rn(silu_mul(g[j], u[j]));
+          for (int j = 0; j < 32; ++j) g[j] = silu_mul(g[j], u[j]);
+          put_row(0, g);
+          __syncwarp();
+          const int j0 = (n0 / BN) * (BN / 2) + c0;
+          // 32 rows x 4 runs of 8 halves: lane takes run (lane & 3) of rows lane / 4 + 8 i
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i, c8 = lane & 3, col = j0 + 8 * c8;
+            if (row0 + rr < a.M && col < a.n_valid) {
+              const float4 x0 = get4(0, rr, 2 * c8), x1 = get4(0, rr, 2 * c8 + 1);
+              uint4 h;
+              h.x = h2_as_u32(__floats2half2_rn(x0.x, x0.y));
+              h.y = h2_as_u32(__floats2half2_rn(x0.z, x0.w));
+              h.z = h2_as_u32(__floats2half2_rn(x1.x, x1.y));
+              h.w = h2_as_u32(__floats2half2_rn(x1.z, x1.w));
+              *reinterpret_cast<uint4*>(a.out + (int64_t)(row0 + rr) * a.ldo + col) = h;
+            }
           }
+          __syncwarp();
         }
       } else {  // EPI_QKV: fp16 q, k, v; q and k rotated at position pos0 + m (pairs (i, i + d/2) of a head)
         const int d = a.head_dim, hd = d / 2;
@@ -229,24 +270,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float x0[32], x1[32];
           tmem_ld32(trow + c0, x0);
           tmem_ld32(trow + c0 + hd, x1);
-          if (!live) continue;
-          __half* o = a.out + (int64_t)m * a.ldo + n0 + c0;
           if (head < a.n_rot_heads) {
-            const float* cs = a.rope_cos + (int64_t)pos * hd + i0;
-            const float* sn = a.rope_sin + (int64_t)pos * hd + i0;
+            const float4* cs = reinterpret_cast<const float4*>(a.rope_cos + (int64_t)min(pos, a.pos0 + a.M - 1) * hd + i0);
+            const float4* sn = reinterpret_cast<const float4*>(a.rope_sin + (int64_t)min(pos, a.pos0 + a.M - 1) * hd + i0);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float a0 = __half2float(__float2half_rn(x0[j])), a1 = __half2float(__float2half_rn(x1[j]));
-              o[j] = __float2half_rn(a0 * cs[j] - a1 * sn[j]);
-              o[j + hd] = __float2half_rn(a0 * sn[j] + a1 * cs[j]);
-            }
-          } else {
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 c = cs[j4], sv = sn[j4];
+              const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              o[j] = __float2half_rn(x0[j]);
-              o[j + hd] = __float2half_rn(x1[j]);
+              for (int e = 0; e < 4; ++e) {
+                // round as the fp16 projection output, then rotate
+                const int j = 4 * j4 + e;
+                const float a0 = __half2float(__float2half_rn(x0[j])), a1 = __half2float(__float2half_rn(x1[j]));
+                x0[j] = a0 * cc[e] - a1 * ss[e];
+                x1[j] = a0 * ss[e] + a1 * cc[e];
+              }
             }
           }
+          put_row(0, x0);
+          put_row(1, x1);
+          __syncwarp();
+          // squares 0 (columns c0 ..) and 1 (columns c0 + hd ..): 32 rows x 4 runs of 8 halves each
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = i >> 2, rr = (lane >> 2) + 8 * (i & 3), c8 = lane & 3;
+            const int col = n0 + c0 + k * hd + 8 * c8;
+            if (row0 + rr < a.M) {
+              const float4 y0 = get4(k, rr, 2 * c8), y1 = get4(k, rr, 2 * c8 + 1);
+              uint4 h;
+              h.x = h2_as_u32(__floats2half2_rn(y0.x, y0.y));
+              h.y = h2_as_u32(__floats2half2_rn(y0.z, y0.w));
+              h.z = h2_as_u32(__floats2half2_rn(y1.x, y1.y));
+              h.w = h2_as_u32(__floats2half2_rn(y1.z, y1.w));
+              *reinterpret_cast<uint4*>(a.out + (int64_t)(row0 + rr) * a.ldo + col) = h;
+            }
+          }
+          __syncwarp();
         }
       }
     }
