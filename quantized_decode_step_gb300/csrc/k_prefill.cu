@@ -11,12 +11,15 @@
 // is exact in fp32), and the GEMM accumulates X hi^T + X lo^T in one fp32
 // accumulator: twice the tensor work, no rounding of the weights.
 //
-// GEMM block: a 128 x 128 output tile, K in steps of 64. Warp 0 issues the TMA
-// loads (A, hi, lo; 128-byte swizzle) into a 4-stage ring; one thread of warp 1
-// issues tcgen05.mma (M 128, N 128, K 16; fp16 in, fp32 out in 128 TMEM columns)
-// and commits each stage back to the producer; warps 2-5 read the accumulator
-// with tcgen05.ld (each warp its 32 TMEM lanes = 32 rows) and apply the epilogue.
+// GEMM block (persistent, one per SM): 128 x 128 output tiles, K in steps of 64.
+// Warp 0 issues the TMA loads (A, hi, lo; 128-byte swizzle) into a 4-stage ring;
+// one thread of warp 1 issues tcgen05.mma (M 128, N 128, K 16; fp16 in, fp32 out
+// in one of two 128-column TMEM accumulators) and commits each stage back to the
+// producer; warps 2-5 read the accumulator with tcgen05.ld (each warp its 32 TMEM
+// lanes = 32 rows) and apply the epilogue while the next tile accumulates.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "kernels.h"
 
@@ -99,20 +102,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 __device__ __forceinline__ float silu_mul(float gte, float up) { return gte / (1.0f + expf(-gte)) * up; }
 
+constexpr int kSq = 36;                              // floats per staged row (see the epilogue)
+constexpr int kStageSqBytes = 32 * kSq * 4;          // one warp's 32 x 32 staging square
+constexpr int kGemmSmem = STAGES * STAGE_BYTES + 4 * kStageSqBytes + 256 + 1024;
+
+// Persistent: one block per SM takes output tiles tile = blockIdx.x + i gridDim.x, the token tiles of a
+// weight tile next to each other (they run at the same time and share its bytes through L2). The ring
+// of stages runs on across tiles, and the accumulator is double-buffered in tensor memory, so the
+// epilogue of tile i overlaps the MMAs of tile i + 1.
 template <int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_hi,
                    const __grid_constant__ CUtensorMap map_lo, const TcGemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  float* stage_sq = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + 4 * kStageSqBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = empty + STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the token tiles of one weight tile are neighbours in launch order, so the weights come from HBM once
-  // and from L2 for the other token tiles
-  const int n0 = blockIdx.y * BN, m0 = blockIdx.x * BM;
+  const int n_m = (a.M + BM - 1) / BM, n_tiles = n_m * (a.N / BN);
   const int nk = (a.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -120,12 +131,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mb_init(full + s, 1);
       mb_init(empty + s, 1);
     }
-    mb_init(acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mb_init(acc_full + i, 1);
+      mb_init(acc_empty + i, 4);  // one arrival per epilogue warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                 "n"(BN)
+                 "n"(2 * BN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -135,83 +149,123 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- TMA producer: the first stages' weights before waiting for the previous kernel (they do not
-    // depend on it), then the activations
-    if (lane == 0) {
+    // ---- TMA producer: the first tile's first stages of weights before waiting for the previous kernel
+    // (they do not depend on it), then everything in ring order
+    if (lane == 0 && (int)blockIdx.x < n_tiles) {
       const int pre = min(STAGES, nk);
-      for (int kb = 0; kb < pre; ++kb) {
-        uint8_t* st = smem + kb * STAGE_BYTES;
-        mb_expect(full + kb, STAGE_BYTES);
-        tma_2d(st + TILE_A, &map_hi, kb * BK, n0, full + kb);
-        tma_2d(st + TILE_A + TILE_B, &map_lo, kb * BK, n0, full + kb);
-      }
-      pdl_wait();
-      for (int kb = 0; kb < pre; ++kb) tma_2d(smem + kb * STAGE_BYTES, &map_a, kb * BK, m0, full + kb);
-      for (int kb = pre; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        if (!mb_wait(empty + s, ((kb / STAGES) - 1) & 1)) {
-          atomicOr(a.err, 8u);
-          break;
+      {
+        const int n0 = ((int)blockIdx.x / n_m) * BN;
+        for (int kb = 0; kb < pre; ++kb) {
+          uint8_t* st = smem + kb * STAGE_BYTES;
+          mb_expect(full + kb, STAGE_BYTES);
+          tma_2d(st + TILE_A, &map_hi, kb * BK, n0, full + kb);
+          tma_2d(st + TILE_A + TILE_B, &map_lo, kb * BK, n0, full + kb);
         }
-        uint8_t* st = smem + s * STAGE_BYTES;
-        mb_expect(full + s, STAGE_BYTES);
-        tma_2d(st + TILE_A, &map_hi, kb * BK, n0, full + s);
-        tma_2d(st + TILE_A + TILE_B, &map_lo, kb * BK, n0, full + s);
-        tma_2d(st, &map_a, kb * BK, m0, full + s);
+        pdl_wait();
+        const int m0 = ((int)blockIdx.x % n_m) * BM;
+        for (int kb = 0; kb < pre; ++kb) tma_2d(smem + kb * STAGE_BYTES, &map_a, kb * BK, m0, full + kb);
+      }
+      int g = 0;  // stages issued so far, over all tiles
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % n_m) * BM, n0 = (tile / n_m) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          if (g < pre) continue;  // issued above
+          const int s = g % STAGES;
+          if (!mb_wait(empty + s, ((g / STAGES) - 1) & 1)) {
+            atomicOr(a.err, 8u);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * STAGE_BYTES;
+          mb_expect(full + s, STAGE_BYTES);
+          tma_2d(st + TILE_A, &map_hi, kb * BK, n0, full + s);
+          tma_2d(st + TILE_A + TILE_B, &map_lo, kb * BK, n0, full + s);
+          tma_2d(st, &map_a, kb * BK, m0, full + s);
+        }
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer
+    // ---- MMA issuer: tile i into accumulator buffer i % 2, once the epilogue has drained it
     if (lane == 0) {
+      int g = 0;
       bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        if (!mb_wait(full + s, (kb / STAGES) & 1)) {
-          atomicOr(a.err, 16u);
-          ok = false;
+      for (int tile = blockIdx.x, it = 0; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+        const int ab = it & 1;
+        if (it >= 2 && !mb_wait(acc_empty + ab, ((it >> 1) - 1) & 1)) {
+          atomicOr(a.err, 64u);
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        uint8_t* st = smem + s * STAGE_BYTES;
-        const uint64_t da = smem_desc(st), dh = smem_desc(st + TILE_A), dl = smem_desc(st + TILE_A + TILE_B);
+        const uint32_t d = tmem + (uint32_t)(ab * BN);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % STAGES;
+          if (!mb_wait(full + s, (g / STAGES) & 1)) {
+            atomicOr(a.err, 16u);
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          uint8_t* st = smem + s * STAGE_BYTES;
+          const uint64_t da = smem_desc(st), dh = smem_desc(st + TILE_A), dl = smem_desc(st + TILE_A + TILE_B);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t off = (uint64_t)(k * 32) >> 4;  // 16 fp16 further along K
-          mma_f16(tmem, da + off, dh + off, (kb | k) != 0);
-          mma_f16(tmem, da + off, dl + off, 1);
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t off = (uint64_t)(k * 32) >> 4;  // 16 fp16 further along K
+            mma_f16(d, da + off, dh + off, (kb | k) != 0);
+            mma_f16(d, da + off, dl + off, 1);
+          }
+          mma_commit(empty + s);
         }
-        mma_commit(empty + s);
+        if (ok) mma_commit(acc_full + ab);
       }
-      if (ok) mma_commit(acc_full);
     }
   } else {
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 = rows of the tile. A thread holds one row;
-    // the warp passes each 32-column slice through a padded shared-memory square (the ring is free once
-    // the accumulator is complete) so that global memory sees whole 16-byte runs of a row.
+    // the warp passes each 32-column slice through its own padded shared-memory square so that global
+    // memory sees whole 16-byte runs of a row.
     pdl_wait();
     pdl_trigger();
-    const int q = warp & 3, m = m0 + q * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    constexpr int SQ = 36;  // floats per staged row: 16-byte aligned, float4 stores of a quarter-warp on distinct banks
-    float* sq = reinterpret_cast<float*>(smem) + q * 2 * 32 * SQ;  // two 32 x 32 squares per warp
-    // this lane's row of square k <- v (32 values)
-    auto put_row = [&](int k, const float (&v)[32]) {
+    const int q = warp & 3;
+    float* sq = stage_sq + q * 32 * kSq;
+    // this lane's row of the square <- v (32 values); float4 stores of a quarter-warp on distinct banks
+    auto put_row = [&](const float (&v)[32]) {
 #pragma unroll
       for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(sq + k * 32 * SQ + lane * SQ + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        *reinterpret_cast<float4*>(sq + lane * kSq + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     };
-    // row rr, columns 4 c4 .. 4 c4 + 3 of square k
-    auto get4 = [&](int k, int rr, int c4) { return *reinterpret_cast<const float4*>(sq + k * 32 * SQ + rr * SQ + 4 * c4); };
-    if (!mb_wait(acc_full, 0)) {
-      atomicOr(a.err, 32u);
-    } else {
+    // row rr, columns 4 c4 .. 4 c4 + 3 of the square
+    auto get4 = [&](int rr, int c4) { return *reinterpret_cast<const float4*>(sq + rr * kSq + 4 * c4); };
+    // the square's 32 rows x 32 columns as fp16 at out (row stride ldo), rows from row0, valid rows < M
+    auto store_f16 = [&](__half* out, int row0, int ld, bool col_ok) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = (lane >> 2) + 8 * i, c8 = lane & 3;
+        if (row0 + rr < a.M && col_ok) {
+          const float4 y0 = get4(rr, 2 * c8), y1 = get4(rr, 2 * c8 + 1);
+          uint4 h;
+          h.x = h2_as_u32(__floats2half2_rn(y0.x, y0.y));
+          h.y = h2_as_u32(__floats2half2_rn(y0.z, y0.w));
+          h.z = h2_as_u32(__floats2half2_rn(y1.x, y1.y));
+          h.w = h2_as_u32(__floats2half2_rn(y1.z, y1.w));
+          *reinterpret_cast<uint4*>(out + (int64_t)(row0 + rr) * ld + 8 * c8) = h;
+        }
+      }
+    };
+    for (int tile = blockIdx.x, it = 0; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int ab = it & 1;
+      const int m0 = (tile % n_m) * BM, n0 = (tile / n_m) * BN;
+      const int m = m0 + q * 32 + lane, row0 = m0 + q * 32;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN);
+      if (!mb_wait(acc_full + ab, (it >> 1) & 1)) {
+        atomicOr(a.err, 32u);
+        break;
+      }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int row0 = m0 + q * 32;  // first row of this warp's slice
       if (EPI == EPI_RESID) {
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tmem_ld32(trow + c0, v);
-          put_row(0, v);
+          put_row(v);
           __syncwarp();
           // 32 rows x 8 float4: lane takes float4 (lane & 7) of rows lane / 8 + 4 i; all loads first
           const int c4 = lane & 7, col = n0 + c0 + 4 * c4;
@@ -227,7 +281,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int i = 0; i < 8; ++i) {
             const int rr = (lane >> 3) + 4 * i;
             if (row0 + rr < a.M && col < a.n_valid) {
-              const float4 x = get4(0, rr, c4);
+              const float4 x = get4(rr, c4);
               *reinterpret_cast<float4*>(a.r + (int64_t)(row0 + rr) * a.ldr + col) =
                   make_float4(y[i].x + x.x, y[i].y + x.y, y[i].z + x.z, y[i].w + x.w);
             }
@@ -242,28 +296,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld32(trow + c0 + BN / 2, u);
 #pragma unroll
           for (int j = 0; j < 32; ++j) g[j] = silu_mul(g[j], u[j]);
-          put_row(0, g);
+          put_row(g);
           __syncwarp();
           const int j0 = (n0 / BN) * (BN / 2) + c0;
-          // 32 rows x 4 runs of 8 halves: lane takes run (lane & 3) of rows lane / 4 + 8 i
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = (lane >> 2) + 8 * i, c8 = lane & 3, col = j0 + 8 * c8;
-            if (row0 + rr < a.M && col < a.n_valid) {
-              const float4 x0 = get4(0, rr, 2 * c8), x1 = get4(0, rr, 2 * c8 + 1);
-              uint4 h;
-              h.x = h2_as_u32(__floats2half2_rn(x0.x, x0.y));
-              h.y = h2_as_u32(__floats2half2_rn(x0.z, x0.w));
-              h.z = h2_as_u32(__floats2half2_rn(x1.x, x1.y));
-              h.w = h2_as_u32(__floats2half2_rn(x1.z, x1.w));
-              *reinterpret_cast<uint4*>(a.out + (int64_t)(row0 + rr) * a.ldo + col) = h;
-            }
-          }
+          store_f16(a.out + j0, row0, a.ldo, j0 + 8 * (lane & 3) < a.n_valid);
           __syncwarp();
         }
       } else {  // EPI_QKV: fp16 q, k, v; q and k rotated at position pos0 + m (pairs (i, i + d/2) of a head)
         const int d = a.head_dim, hd = d / 2;
-        const int pos = a.pos0 + m;
+        const int pos = min(a.pos0 + m, a.pos0 + a.M - 1);  // rows past the chunk compute, but store nothing
         for (int c0 = 0; c0 < BN; c0 += 32) {
           const int head = (n0 + c0) / d, i0 = (n0 + c0) - head * d;
           if (i0 >= hd) continue;  // the second half of a head comes with the first
@@ -271,8 +312,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld32(trow + c0, x0);
           tmem_ld32(trow + c0 + hd, x1);
           if (head < a.n_rot_heads) {
-            const float4* cs = reinterpret_cast<const float4*>(a.rope_cos + (int64_t)min(pos, a.pos0 + a.M - 1) * hd + i0);
-            const float4* sn = reinterpret_cast<const float4*>(a.rope_sin + (int64_t)min(pos, a.pos0 + a.M - 1) * hd + i0);
+            const float4* cs = reinterpret_cast<const float4*>(a.rope_cos + (int64_t)pos * hd + i0);
+            const float4* sn = reinterpret_cast<const float4*>(a.rope_sin + (int64_t)pos * hd + i0);
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
               const float4 c = cs[j4], sv = sn[j4];
@@ -287,32 +328,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
           }
-          put_row(0, x0);
-          put_row(1, x1);
+          put_row(x0);
           __syncwarp();
-          // squares 0 (columns c0 ..) and 1 (columns c0 + hd ..): 32 rows x 4 runs of 8 halves each
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int k = i >> 2, rr = (lane >> 2) + 8 * (i & 3), c8 = lane & 3;
-            const int col = n0 + c0 + k * hd + 8 * c8;
-            if (row0 + rr < a.M) {
-              const float4 y0 = get4(k, rr, 2 * c8), y1 = get4(k, rr, 2 * c8 + 1);
-              uint4 h;
-              h.x = h2_as_u32(__floats2half2_rn(y0.x, y0.y));
-              h.y = h2_as_u32(__floats2half2_rn(y0.z, y0.w));
-              h.z = h2_as_u32(__floats2half2_rn(y1.x, y1.y));
-              h.w = h2_as_u32(__floats2half2_rn(y1.z, y1.w));
-              *reinterpret_cast<uint4*>(a.out + (int64_t)(row0 + rr) * a.ldo + col) = h;
-            }
-          }
+          store_f16(a.out + n0 + c0, row0, a.ldo, true);
+          __syncwarp();
+          put_row(x1);
+          __syncwarp();
+          store_f16(a.out + n0 + c0 + hd, row0, a.ldo, true);
           __syncwarp();
         }
       }
+      // the accumulator buffer is drained: the MMA warp may reuse it
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(acc_empty + ab)) : "memory");
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(BN) : "memory");
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(2 * BN) : "memory");
 }
 
 // ---------------------------------------------------------------- row kernels
@@ -396,11 +431,18 @@ EncodeTiledFn encode_fn() {
 template <int EPI>
 cudaError_t launch_tc_t(const Launch& L, const TcMaps& m, const TcGemmArgs& a) {
   auto kern = tc_gemm_kernel<EPI>;
-  const int smem = STAGES * STAGE_BYTES + 1024 + 256;
+  const int smem = kGemmSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  }
+  const int n_tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.M + BM - 1) / BM, (a.N + BN - 1) / BN);
+  cfg.gridDim = dim3(std::min(n_tiles, n_sm));
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
