@@ -674,26 +674,49 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
   const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
 
-  // key tile i into buffer bf: FP16 by cp.async (committed as one group), others widened synchronously
+  // key tile i into buffer bf: FP16 by cp.async (committed as one group), others widened synchronously.
+  // Keys past the chunk's last stored token are zeros.
   auto stage = [&](int i, int bf) {
     __half* kt = tiles + (size_t)bf * 2 * PG::kTile;
     __half* vt = kt + PG::kTile;
-    constexpr int kChunks = kPfKeys * D / 8;  // 16-byte chunks per K or V tile
-    for (int c = tid; c < 2 * kChunks; c += 128) {
-      const int which = c >= kChunks, cc = which ? c - kChunks : c;
-      const int row = cc / (D / 8), c8 = (cc - row * (D / 8)) * 8;
-      const int kp = i * kPfKeys + row;
-      __half* dst = (which ? vt : kt) + row * PG::kRow + c8;
-      if (kp >= n_valid) {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-        continue;
+    const int n_rows = max(0, min(kPfKeys, n_valid - i * kPfKeys));  // rows that exist in the pool
+    if (dt == 0) {
+      // a thread keeps one 16-byte column c8 of the rows r0 + kRpp j; the four pool blocks' row-0 addresses
+      // are computed once
+      constexpr int kCpr = D / 8, kRpp = 128 / kCpr;  // 16-byte chunks per row, rows per pass
+      const int c8 = (tid % kCpr) * 8, r0 = tid / kCpr;
+      const uint8_t* bp[2][4];
+#pragma unroll
+      for (int pb = 0; pb < 4; ++pb) {
+        const int blk = i * 4 + pb;
+        const int phys = blk * 16 < n_valid ? a.table[blk] : 0;
+        bp[0][pb] = pool_vec(a.pool, a.layer, phys, 0, gk, 0) + c8 * 2;
+        bp[1][pb] = pool_vec(a.pool, a.layer, phys, 1, gk, 0) + c8 * 2;
       }
-      const int phys = a.table[kp >> 4];
-      if (dt == 0) {
-        cp_async16(dst, pool_vec(a.pool, a.layer, phys, which, gk, kp & 15) + c8 * 2);
-      } else {
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int j = 0; j < kPfKeys / kRpp; ++j) {
+          const int row = r0 + kRpp * j;
+          __half* dst = (w ? vt : kt) + row * PG::kRow + c8;
+          if (row < n_rows)
+            cp_async16(dst, bp[w][row >> 4] + (row & 15) * (2 * D));
+          else
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    } else {
+      constexpr int kChunks = kPfKeys * D / 8;  // 16-byte chunks per K or V tile
+      for (int c = tid; c < 2 * kChunks; c += 128) {
+        const int which = c >= kChunks, cc = which ? c - kChunks : c;
+        const int row = cc / (D / 8), c8 = (cc - row * (D / 8)) * 8;
+        const int kp = i * kPfKeys + row;
+        __half* dst = (which ? vt : kt) + row * PG::kRow + c8;
+        if (row >= n_rows) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+          continue;
+        }
         __half h[8];
-        widen_unit(dt, load_unit(a.pool, a.layer, phys, which, gk, kp & 15, c8), h);
+        widen_unit(dt, load_unit(a.pool, a.layer, a.table[kp >> 4], which, gk, kp & 15, c8), h);
         *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
       }
     }
