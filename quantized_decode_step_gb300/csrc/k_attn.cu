@@ -674,6 +674,9 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
   const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
 
+  // K data of (this layer, pool block 0, this KV head, slot 0); a block's V data is pool_v_off further
+  const uint8_t* pool_head0 = pool_vec(a.pool, a.layer, 0, 0, gk, 0);
+  const int64_t pool_v_off = pool_vec(a.pool, a.layer, 0, 1, gk, 0) - pool_head0;
   // key tile i into buffer bf: FP16 by cp.async (committed as one group), others widened synchronously.
   // Keys past the chunk's last stored token are zeros.
   auto stage = [&](int i, int bf) {
@@ -681,29 +684,29 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     __half* vt = kt + PG::kTile;
     const int n_rows = max(0, min(kPfKeys, n_valid - i * kPfKeys));  // rows that exist in the pool
     if (dt == 0) {
-      // a thread keeps one 16-byte column c8 of the rows r0 + kRpp j; the four pool blocks' row-0 addresses
-      // are computed once
+      // a thread keeps one 16-byte column c8 of slots r0 + kRpp jj of every pool block of the tile (kRpp
+      // rows per pass); only the block's base address changes from one pool block to the next
       constexpr int kCpr = D / 8, kRpp = 128 / kCpr;  // 16-byte chunks per row, rows per pass
       const int c8 = (tid % kCpr) * 8, r0 = tid / kCpr;
-      const uint8_t* bp[2][4];
 #pragma unroll
       for (int pb = 0; pb < 4; ++pb) {
         const int blk = i * 4 + pb;
-        const int phys = blk * 16 < n_valid ? a.table[blk] : 0;
-        bp[0][pb] = pool_vec(a.pool, a.layer, phys, 0, gk, 0) + c8 * 2;
-        bp[1][pb] = pool_vec(a.pool, a.layer, phys, 1, gk, 0) + c8 * 2;
-      }
+        const uint8_t* kb = pool_head0 + (int64_t)(blk * 16 < n_valid ? a.table[blk] : 0) * a.pool.block_bytes +
+                            r0 * (2 * D) + c8 * 2;
 #pragma unroll
-      for (int w = 0; w < 2; ++w)
-#pragma unroll
-        for (int j = 0; j < kPfKeys / kRpp; ++j) {
-          const int row = r0 + kRpp * j;
-          __half* dst = (w ? vt : kt) + row * PG::kRow + c8;
-          if (row < n_rows)
-            cp_async16(dst, bp[w][row >> 4] + (row & 15) * (2 * D));
-          else
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        for (int jj = 0; jj < 16 / kRpp; ++jj) {
+          const int row = pb * 16 + r0 + kRpp * jj;
+          __half* dk = kt + row * PG::kRow + c8;
+          __half* dv = vt + row * PG::kRow + c8;
+          if (row < n_rows) {
+            cp_async16(dk, kb + jj * kRpp * (2 * D));
+            cp_async16(dv, kb + pool_v_off + jj * kRpp * (2 * D));
+          } else {
+            *reinterpret_cast<uint4*>(dk) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dv) = make_uint4(0, 0, 0, 0);
+          }
         }
+      }
     } else {
       constexpr int kChunks = kPfKeys * D / 8;  // 16-byte chunks per K or V tile
       for (int c = tid; c < 2 * kChunks; c += 128) {
