@@ -611,28 +611,38 @@ __device__ __forceinline__ RawUnit load_unit(const PoolGeom& P, int layer, int b
   return r;
 }
 // the unit as 8 fp16 values (INT8: s q; INT4: s q + m, in fp32 then rounded; FP16 as stored)
-__device__ __forceinline__ void widen_unit(int dt, const RawUnit& r, __half (&h)[8]) {
-  if (dt == 0) {
-    *reinterpret_cast<uint4*>(h) = r.d;
-  } else if (dt == 1) {
+// the dequantised values of an INT8 / INT4 unit in fp32: s q (exact), s q + m (one rounding)
+__device__ __forceinline__ void dequant_unit(int dt, const RawUnit& r, float (&v)[8]) {
+  if (dt == 1) {
     const float s = __half2float(__ushort_as_half((unsigned short)r.meta));
     const int8_t* q = reinterpret_cast<const int8_t*>(&r.d);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(s * (float)q[e]);
+    for (int e = 0; e < 8; ++e) v[e] = s * (float)q[e];
   } else {
     const __half2 sm = u32_as_h2(r.meta);
     const float s = __low2float(sm), mn = __high2float(sm);
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      h[e] = __float2half_rn(__fadd_rn(__fmul_rn(s, (float)((r.d.x >> (4 * e)) & 15u)), mn));
+    for (int e = 0; e < 8; ++e) v[e] = __fadd_rn(__fmul_rn(s, (float)((r.d.x >> (4 * e)) & 15u)), mn);
   }
+}
+// the unit as 8 fp16 values (INT8 / INT4: the dequantised value rounded; FP16 as stored)
+__device__ __forceinline__ void widen_unit(int dt, const RawUnit& r, __half (&h)[8]) {
+  if (dt == 0) {
+    *reinterpret_cast<uint4*>(h) = r.d;
+    return;
+  }
+  float v[8];
+  dequant_unit(dt, r, v);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(v[e]);
 }
 
 // ---------------------------------------------------------------- prefill attention
 // Block: one KV head and 4 warps x 16 MMA rows; a row is (token, query head of the group), 16/G tokens per
 // warp. Keys go through shared memory in tiles of 64 (four pool blocks), K and V row-major as fp16 with
 // padded rows, double-buffered: FP16 pools are copied with cp.async while the previous tile is computed,
-// INT8 / INT4 pools are widened into the tile (s q, s q + m in fp32, rounded). Each warp runs QK^T
+// INT8 / INT4 pools are dequantised into the tile (s q, s q + m in fp32; keys as fp16 hi + lo, so QK^T sees
+// the fp32 value, values rounded to fp16). Each warp runs QK^T
 // (B fragments by ldmatrix), the causal mask, the online softmax and PV (B fragments by ldmatrix.trans,
 // probabilities split into fp16 hi + lo) on m16n8k16 MMAs. Keys past the chunk's last token are zeros.
 constexpr int kPfKeys = 64;  // keys per tile
@@ -642,6 +652,8 @@ struct PfGeom {
   static constexpr int kRow = D + 8;               // halves per shared-memory row (ldmatrix rows on distinct banks)
   static constexpr int kTile = kPfKeys * kRow;     // halves per K or V tile
   static constexpr size_t kBytes = (size_t)4 * kTile * 2;  // K and V, two buffers
+  // INT8 / INT4 pools also keep the keys' low parts (k - fp16(k)), one tile per buffer after those
+  static constexpr size_t kBytesQuant = (size_t)6 * kTile * 2;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
@@ -682,6 +694,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   auto stage = [&](int i, int bf) {
     __half* kt = tiles + (size_t)bf * 2 * PG::kTile;
     __half* vt = kt + PG::kTile;
+    __half* klo = tiles + (size_t)(4 + bf) * PG::kTile;  // INT8 / INT4 only
     const int n_rows = max(0, min(kPfKeys, n_valid - i * kPfKeys));  // rows that exist in the pool
     if (dt == 0) {
       // a thread keeps one 16-byte column c8 of slots r0 + kRpp jj of every pool block of the tile (kRpp
@@ -714,13 +727,22 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
         const int row = cc / (D / 8), c8 = (cc - row * (D / 8)) * 8;
         const int kp = i * kPfKeys + row;
         __half* dst = (which ? vt : kt) + row * PG::kRow + c8;
+        __half* dlo = klo + row * PG::kRow + c8;  // keys only
         if (row >= n_rows) {
           *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+          if (!which) *reinterpret_cast<uint4*>(dlo) = make_uint4(0, 0, 0, 0);
           continue;
         }
-        __half h[8];
-        widen_unit(dt, load_unit(a.pool, a.layer, a.table[kp >> 4], which, gk, kp & 15, c8), h);
+        float v[8];
+        dequant_unit(dt, load_unit(a.pool, a.layer, a.table[kp >> 4], which, gk, kp & 15, c8), v);
+        __half h[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          h[e] = __float2half_rn(v[e]);
+          lo[e] = __float2half_rn(v[e] - __half2float(h[e]));  // keys: hi + lo carries the fp32 value
+        }
         *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
+        if (!which) *reinterpret_cast<uint4*>(dlo) = *reinterpret_cast<uint4*>(lo);
       }
     }
     cp_async_commit();
@@ -761,6 +783,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     if (i + 1 < n_tiles) stage(i + 1, bf ^ 1);
     const __half* kt = tiles + (size_t)bf * 2 * PG::kTile;
     const __half* vt = kt + PG::kTile;
+    const __half* klo = tiles + (size_t)(4 + bf) * PG::kTile;
     if (warp_last < t_warp || i * kPfKeys > a.pos0 + warp_last) continue;  // no key of this tile is visible
     // ---- S = Q K^T over the tile's 64 keys: n-tile nt = keys 8 nt .. 8 nt + 7
     float sfr[NT][4];
@@ -772,9 +795,15 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
         // matrices: (k-step s, dims lo), (s, hi), (s + 1, lo), (s + 1, hi) of keys 8 nt ..
         const int m = lane >> 3;
         uint32_t kb[4];
-        ldsm_x4(kb, kt + (8 * nt + (lane & 7)) * PG::kRow + 16 * (s + (m >> 1)) + 8 * (m & 1));
+        const int off = (8 * nt + (lane & 7)) * PG::kRow + 16 * (s + (m >> 1)) + 8 * (m & 1);
+        ldsm_x4(kb, kt + off);
         mma_16816(sfr[nt], qa[s][0], qa[s][1], qa[s][2], qa[s][3], kb[0], kb[1]);
         mma_16816(sfr[nt], qa[s + 1][0], qa[s + 1][1], qa[s + 1][2], qa[s + 1][3], kb[2], kb[3]);
+        if (dt != 0) {  // the keys' low parts
+          ldsm_x4(kb, klo + off);
+          mma_16816(sfr[nt], qa[s][0], qa[s][1], qa[s][2], qa[s][3], kb[0], kb[1]);
+          mma_16816(sfr[nt], qa[s + 1][0], qa[s + 1][1], qa[s + 1][2], qa[s + 1][3], kb[2], kb[3]);
+        }
       }
     }
     // causal mask and online softmax; fragment (nt, j): row g + 8 (j >> 1), key 64 i + 8 nt + 2 t + (j & 1)
@@ -949,8 +978,9 @@ cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a) 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return e != cudaSuccess ? e : launch_ex(L, kern, grid, dim3(128), smem, a);
   };
-  if (a.head_dim == 128) return run(prefill_attn_kernel<128>, PfGeom<128>::kBytes);
-  if (a.head_dim == 64) return run(prefill_attn_kernel<64>, PfGeom<64>::kBytes);
+  const bool quant = a.pool.kv_dtype != 0;
+  if (a.head_dim == 128) return run(prefill_attn_kernel<128>, quant ? PfGeom<128>::kBytesQuant : PfGeom<128>::kBytes);
+  if (a.head_dim == 64) return run(prefill_attn_kernel<64>, quant ? PfGeom<64>::kBytesQuant : PfGeom<64>::kBytes);
   return cudaErrorInvalidValue;
 }
 

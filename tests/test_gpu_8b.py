@@ -5,7 +5,8 @@
   the oracle's quantiser, and the logits of two consecutive steps against the
   oracle's full 32-layer step.
 * Agent batch: 16 sessions, log-uniform contexts 20..2048, KV blocks
-  scattered through a shared pool.
+  scattered through a shared pool; the same with INT8 and INT4 KV on two
+  layers.
 * Long context, FP16 at 19,431 / INT8 at 38,863 / INT4 at 77,726 tokens (the
   capacities "5. Core modules" 5.4 prints): the full contexts and the full
   vocabulary, on 4 of the 32 layers (every layer runs the same launches).
@@ -166,6 +167,18 @@ def test_8b_agent_batch16_scattered_pool():
     ctx, w = _oracle_weights_and_ctx(wl)
     sids, kvs, cfg = _priors(ctx, wl)
     _steps(ctx, w, wl, sids, kvs, cfg, 1, floor_check=True)
+
+
+@pytest.mark.parametrize("dt", [KV_INT8, KV_INT4])
+def test_8b_agent_batch16_quantized_kv(dt):
+    """The agent batch (16 sessions, contexts 20..2048, scattered pool) with INT8 / INT4 KV, on two of the 32
+    layers with the full vocabulary (strict bar)."""
+    base = agent_batch(SEED)
+    wl = Workload(f"8b2L-b16-agent-kv{dt}", shrink(LLAMA8B, n_layers=2), dt, base.batch, base.prior,
+                  scattered_pool=True)
+    ctx, w = _oracle_weights_and_ctx(wl, check_bytes=False)
+    sids, kvs, cfg = _priors(ctx, wl)
+    _steps(ctx, w, wl, sids, kvs, cfg, 1)
 
 
 def test_8b_two_layers_strict():

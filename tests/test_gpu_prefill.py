@@ -7,7 +7,12 @@
   chunks stored) against the oracle's causal forward pass.
 * A chunk on an empty cache (position 0 onwards).
 * Two 8B-shaped layers with the full vocabulary: a 64-token chunk on an
-  800-token FP16 cache against the oracle.
+  800-token FP16 / INT8 / INT4 cache against the oracle (quantised pools then
+  also decode one token). With a quantised pool the chunk's own k and v go
+  through the quantiser, where one fp16 ulp upstream can move a code; there
+  the rel-L2 bar for the chunk and the step after it is 1.25 x the oracle's
+  own change under one ulp of one input value per token (measured in the
+  test), as for the 32-layer decode.
 * The 8B chunked-prefill configuration at full size (32 layers, a 512-token
   chunk on an 800-token FP16 cache): the oracle can not run it in a test, so
   the chunk's last logits are compared with the same 512 tokens decoded one by
@@ -24,7 +29,8 @@ import quantized_decode_step_gb300 as mag
 import synth
 from synth import driver
 from synth.workloads import KV_FP16, KV_INT4, KV_INT8, LLAMA8B, PREFILL_8B, TINY, Workload, shrink
-from tests.helpers import TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, oracle_weights, prior_kv, rel_l2
+from tests.helpers import (FLOOR_FACTOR, TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, one_ulp_floor, oracle_weights,
+                           prior_kv, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +49,7 @@ def _compare(got, ref, what, bar=TOL_REL_L2):
     assert ma <= TOL_MAX_ABS and rl <= bar, f"{what}: max-abs {ma:.3e}, rel-L2 {rl:.3e}"
 
 
-def _run(wl: Workload, seed: int, chunks, decode_after=1, random_gain=True):
+def _run(wl: Workload, seed: int, chunks, decode_after=1, random_gain=True, floor_check=False):
     shape = wl.shape
     total = sum(chunks) + decode_after
     ctx, sids = driver.setup(wl, seed, random_gain=random_gain, extra_tokens=total)
@@ -58,6 +64,7 @@ def _run(wl: Workload, seed: int, chunks, decode_after=1, random_gain=True):
     c, s = oracle.rope_table(p + total + 2, shape.head_dim, shape.rope_base)
     width = shape.vocab or shape.hidden
     pos = p
+    bar = TOL_REL_L2
     for i, T in enumerate(chunks):
         x = synth.hidden_f16(seed, T, shape.hidden, tag=f"chunk{i}")
         out = torch.empty(width, dtype=torch.float16, device="cuda")
@@ -65,15 +72,28 @@ def _run(wl: Workload, seed: int, chunks, decode_after=1, random_gain=True):
         ctx.sync()
         pos += T
         assert ctx.session_length(sid) == pos
+        if floor_check and i == 0:
+            # a quantised pool stores the chunk's own k and v through the quantiser, so one fp16 ulp of
+            # difference upstream can move a code: the bar is the oracle's own change under one ulp of one
+            # input value per token, from a store holding only the prior
+            def run(xx, T=T):
+                kv2 = oracle.KV(cfg, p + total + 8)
+                if p:
+                    kv2.append(k, v)
+                return oracle.forward(cfg, w, [kv2], [T], xx, c, s)[0]
+            floor, _ = one_ulp_floor(run, x)
+            bar = max(TOL_REL_L2, FLOOR_FACTOR * floor)
+            print(f"{wl.name}: one-ulp sensitivity of the oracle {floor:.3e} -> rel-L2 bar {bar:.3e}")
         ref = oracle.forward(cfg, w, [kv], [T], x, c, s)[0]
-        _compare(out.cpu().numpy(), ref, f"{wl.name} chunk {i} ({T} tokens)")
+        _compare(out.cpu().numpy(), ref, f"{wl.name} chunk {i} ({T} tokens)", bar)
     for j in range(decode_after):
         x = synth.hidden_f16(seed, 1, shape.hidden, tag=f"after{j}")
         out = torch.empty((1, width), dtype=torch.float16, device="cuda")
         ctx.decode_step([sid], torch.from_numpy(x).cuda(), out)
         ctx.sync()
         ref = oracle.forward(cfg, w, [kv], [1], x, c, s)
-        _compare(out.cpu().numpy(), ref, f"{wl.name} decode after the chunks")
+        # the step reads the chunk's stored keys and values: the same bar as the chunk
+        _compare(out.cpu().numpy(), ref, f"{wl.name} decode after the chunks", bar)
     return ctx
 
 
@@ -103,10 +123,11 @@ def test_prefill_unsupported_without_max_chunk():
 
 
 @pytest.mark.slow
-def test_8b_two_layers_prefill_chunk():
+@pytest.mark.parametrize("dt", [KV_FP16, KV_INT8, KV_INT4])
+def test_8b_two_layers_prefill_chunk(dt):
     shape = shrink(LLAMA8B, n_layers=2)
-    wl = Workload("8b2L-prefill-64-on-800", shape, KV_FP16, 1, (800,), chunk=64)
-    _run(wl, 27, (64,), decode_after=0, random_gain=False)
+    wl = Workload(f"8b2L-prefill-64-on-800-kv{dt}", shape, dt, 1, (800,), chunk=64)
+    _run(wl, 27, (64,), decode_after=1 if dt else 0, random_gain=False, floor_check=dt != KV_FP16)
 
 
 @pytest.mark.slow
