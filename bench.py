@@ -439,10 +439,11 @@ def run_prefill(args, tc_peak):
     shape, T, p = wl.shape, wl.chunk, wl.prior[0]
     warm, runs = 2, 3
     n_sets = warm + runs
-    blocks = n_sets * -(-(p + T) // 16)
+    n_draft = 4  # the verify leg: drafts checked in one call on a session after its chunk
+    blocks = n_sets * -(-(p + T + n_draft) // 16)
     stream = torch.cuda.Stream()
     cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sets, max_batch=1,
-                          max_chunk=T, max_context=p + T)
+                          max_chunk=T, max_context=p + T + n_draft)
     t_setup = time.time()
     ctx = mag.Context(cfg, stream.cuda_stream)
     with torch.cuda.stream(stream):
@@ -472,6 +473,24 @@ def run_prefill(args, tc_peak):
     ev1.record(stream)
     ev1.synchronize()
     s_chunk = ev0.elapsed_time(ev1) / 1e3 / runs
+    # verify leg: n_draft draft tokens in one call on a session holding p + T tokens, truncated back after
+    # each call so every call sees the same cache
+    sid_v = sids[0]
+    base_len = ctx.session_length(sid_v)
+    with torch.cuda.stream(stream):
+        xv = torch.from_numpy(hidden_f16(args.seed, n_draft, shape.hidden, tag="drafts")).cuda()
+        ov = torch.empty((n_draft, shape.vocab or shape.hidden), dtype=torch.float16, device="cuda")
+    for _ in range(3):
+        ctx.verify_tokens(sid_v, n_draft, xv, ov)
+        ctx.session_truncate(sid_v, base_len)
+    v_runs = 20
+    ev0.record(stream)
+    for _ in range(v_runs):
+        ctx.verify_tokens(sid_v, n_draft, xv, ov)
+        ctx.session_truncate(sid_v, base_len)
+    ev1.record(stream)
+    ev1.synchronize()
+    s_verify = ev0.elapsed_time(ev1) / 1e3 / v_runs
     fl = prefill_flops(shape, p, T)
     st = ctx.memory_stats()
     ctx.close()
@@ -483,6 +502,8 @@ def run_prefill(args, tc_peak):
                          "note": "fp16 kind::f16 at the measured bf16 rate; the exact two-term weights double "
                                  "the tensor work, which is not counted as achieved"},
             "launches_per_chunk": launches, "prefill_weight_bytes": st["prefill_weight_bytes"],
+            "verify": {"drafts": n_draft, "context": base_len, "ms_per_call": s_verify * 1e3,
+                       "tokens_per_s": n_draft / s_verify},
             "setup_s": t_setup}
 
 

@@ -158,6 +158,14 @@ mag_status mag_session_open(mag_ctx* ctx, int32_t* session_out);
 mag_status mag_session_close(mag_ctx* ctx, int32_t session);
 mag_status mag_session_length(mag_ctx* ctx, int32_t session, int32_t* length_out);
 
+/* Shorten a session to `length` tokens (0..its length), e.g. to drop draft
+ * tokens that mag_verify_tokens appended and the caller rejected. Blocks
+ * wholly past the new length go back to the free list; the tokens past it are
+ * never read again and the next append overwrites them. The pages have no
+ * counterpart (their speculative controller, [Core] 5.5, is out of scope;
+ * only this step of it is built). Host-only, no launch. Errors: INVALID_ARG. */
+mag_status mag_session_truncate(mag_ctx* ctx, int32_t session, int32_t length);
+
 /* Append n_tokens of already-rotated K and V to a session's cache, fp16
  * [L][n_tokens][Hkv][d] each, quantised on store to the pool precision
  * (INT8: one fp16 scale per token and head, s = fp16(max|x|/127), q =
@@ -196,6 +204,15 @@ mag_status mag_decode_step_host(mag_ctx* ctx, int32_t batch, const int32_t* sess
  * with max_chunk = 0), CUDA. */
 mag_status mag_prefill_chunk(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
                              void* last_out_dev);
+
+/* Multi-token verify step (draft tokens of speculative decoding checked in
+ * one pass): like mag_prefill_chunk with n_tokens = 1..4, but writing the fp16
+ * output of every token, out_dev[n_tokens][V] (or [n_tokens][D] when
+ * vocab == 0): token j attends causally to the session's cache and tokens
+ * 0..j. All n_tokens are appended; mag_session_truncate drops the rejected
+ * ones. Needs max_chunk >= n_tokens. Errors: as mag_prefill_chunk. */
+mag_status mag_verify_tokens(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
+                             void* out_dev);
 
 /* Wait for the context's stream and read the device error word
  * (MAG_ERR_TIMEOUT if a bounded device wait gave up). */

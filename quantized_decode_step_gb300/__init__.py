@@ -26,7 +26,8 @@ FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL = 1, 2, 4
 
 EXPORTED = [
     "mag_create", "mag_destroy", "mag_load_weights", "mag_load_weights_f32_noalloc", "mag_session_open", "mag_session_close", "mag_session_length",
-    "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk", "mag_sync",
+    "mag_session_truncate", "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk",
+    "mag_verify_tokens", "mag_sync",
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
     "mag_debug_last_step_launches", "mag_debug_profile_step",
@@ -88,10 +89,12 @@ def lib():
                 "mag_session_open": ([vp, P32], i32),
                 "mag_session_close": ([vp, i32], i32),
                 "mag_session_length": ([vp, i32, P32], i32),
+                "mag_session_truncate": ([vp, i32, i32], i32),
                 "mag_kv_append": ([vp, i32, i32, vp, vp], i32),
                 "mag_decode_step": ([vp, i32, P32, vp, vp], i32),
                 "mag_decode_step_host": ([vp, i32, P32, vp, vp], i32),
                 "mag_prefill_chunk": ([vp, i32, i32, vp, vp], i32),
+                "mag_verify_tokens": ([vp, i32, i32, vp, vp], i32),
                 "mag_sync": ([vp], i32),
                 "mag_get_memory_stats": ([vp, ctypes.POINTER(MemoryStats)], i32),
                 "mag_last_error": ([vp], ctypes.c_char_p),
@@ -198,6 +201,9 @@ class Context:
         self._check(lib().mag_session_length(self.h, sid, ctypes.byref(n)), "mag_session_length")
         return n.value
 
+    def session_truncate(self, sid, length):
+        self._check(lib().mag_session_truncate(self.h, sid, length), "mag_session_truncate")
+
     def kv_append(self, sid, n_tokens, k, v):
         self._check(lib().mag_kv_append(self.h, sid, n_tokens, _ptr(k), _ptr(v)), "mag_kv_append")
 
@@ -213,6 +219,9 @@ class Context:
     def prefill_chunk(self, sid, n_tokens, hidden_in, last_out):
         self._check(lib().mag_prefill_chunk(self.h, sid, n_tokens, _ptr(hidden_in), _ptr(last_out)),
                     "mag_prefill_chunk")
+
+    def verify_tokens(self, sid, n_tokens, hidden_in, out):
+        self._check(lib().mag_verify_tokens(self.h, sid, n_tokens, _ptr(hidden_in), _ptr(out)), "mag_verify_tokens")
 
     def sync(self):
         self._check(lib().mag_sync(self.h), "mag_sync")

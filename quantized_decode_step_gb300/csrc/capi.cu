@@ -1036,31 +1036,38 @@ mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, cons
   return check_err(c);
 }
 
-mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out) {
+namespace {
+
+// The chunk path of mag_prefill_chunk and mag_verify_tokens: T tokens of one session through every layer
+// (their k and v appended to the pool), then the final RMSNorm + LM head (or the final hidden state) of the
+// last out_rows tokens into out [out_rows][V or D].
+mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const void* in, void* out, int out_rows) {
   if (!c) return MAG_ERR_INVALID_ARG;
-  if (c->cfg.max_chunk <= 0) return fail(c, MAG_ERR_UNSUPPORTED, "prefill_chunk: created with max_chunk = 0");
-  if (!in || !last_out) return fail(c, MAG_ERR_INVALID_ARG, "prefill_chunk: null buffer");
+  if (c->cfg.max_chunk <= 0) return fail(c, MAG_ERR_UNSUPPORTED, "%s: created with max_chunk = 0", what);
+  if (!in || !out) return fail(c, MAG_ERR_INVALID_ARG, "%s: null buffer", what);
   if (T < 1 || T > c->cfg.max_chunk)
-    return fail(c, MAG_ERR_INVALID_ARG, "prefill_chunk: %d tokens not in 1..%d", T, c->cfg.max_chunk);
+    return fail(c, MAG_ERR_INVALID_ARG, "%s: %d tokens not in 1..%d", what, T, c->cfg.max_chunk);
   if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
-    return fail(c, MAG_ERR_INVALID_ARG, "prefill_chunk: session %d is not open", sid);
-  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "prefill_chunk: not every weight is loaded");
+    return fail(c, MAG_ERR_INVALID_ARG, "%s: session %d is not open", what, sid);
+  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "%s: not every weight is loaded", what);
   Session& s = c->sessions[sid];
   if ((int64_t)s.len + T > c->cfg.max_context)
-    return fail(c, MAG_ERR_CONTEXT_FULL, "prefill_chunk: %d + %d tokens exceed max_context %d", s.len, T,
+    return fail(c, MAG_ERR_CONTEXT_FULL, "%s: %d + %d tokens exceed max_context %d", what, s.len, T,
                 c->cfg.max_context);
   const int nb_old = (s.len + 15) / 16, nb_new = (s.len + T + 15) / 16;
   if (nb_new - nb_old > (int)c->free_list.size())
-    return fail(c, MAG_ERR_KV_FULL, "prefill_chunk: needs %d blocks, %zu free", nb_new - nb_old, c->free_list.size());
-  // step arguments of the last token's LM head (or final hidden state)
+    return fail(c, MAG_ERR_KV_FULL, "%s: needs %d blocks, %zu free", what, nb_new - nb_old, c->free_list.size());
+  // step arguments of the output rows' LM head (or final hidden state)
   const int slot = c->ring_pos;
   CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
   StepArgs& sa = c->h_ring[slot];
   memset(&sa, 0, sizeof sa);
-  sa.batch = 1;
-  sa.sess[0] = sid;
-  sa.pos[0] = s.len + T - 1;
-  sa.out = last_out;
+  sa.batch = out_rows;
+  for (int b = 0; b < out_rows; ++b) {
+    sa.sess[b] = sid;
+    sa.pos[b] = s.len + T - out_rows + b;
+  }
+  sa.out = out;
   for (int i = nb_old; i < nb_new; ++i) {
     s.table.push_back(c->free_list.front());
     c->free_list.pop_front();
@@ -1149,19 +1156,50 @@ mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in,
     gd.ldr = D;
     CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_act, pp[3].map_hi, pp[3].map_lo}, gd, EPI_RESID));
   }
-  float* r_last = c->pf_r + (size_t)(T - 1) * D;
-  if (c->V) {  // final RMSNorm + LM head of the last token
-    GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, D, 1);
-    a.r = r_last;
+  float* r_out = c->pf_r + (size_t)(T - out_rows) * D;
+  if (c->V) {  // final RMSNorm + LM head of the output rows
+    GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, D, out_rows);
+    a.r = r_out;
     a.ldr = D;
     a.gamma = c->gamma_f;
     a.ldo = c->V;
     CUDA_TRY(c, launch_gemv(L, a, W_F16, XSRC_RESID, EPI_STORE_OUT));
   } else {
-    CUDA_TRY(c, launch_final_hidden(L, c->d_args, r_last, D, 1));
+    CUDA_TRY(c, launch_final_hidden(L, c->d_args, r_out, D, out_rows));
   }
   c->last_launches = n;
   s.len += T;
+  return MAG_OK;
+}
+
+}  // namespace
+
+mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out) {
+  return run_chunk(c, "prefill_chunk", sid, T, in, last_out, 1);
+}
+
+mag_status mag_verify_tokens(mag_ctx* c, int32_t sid, int32_t n_tokens, const void* hidden_in, void* out) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (n_tokens < 1 || n_tokens > kPipeMaxBatch)
+    return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: %d tokens not in 1..%d", n_tokens, kPipeMaxBatch);
+  return run_chunk(c, "verify_tokens", sid, n_tokens, hidden_in, out, n_tokens);
+}
+
+mag_status mag_session_truncate(mag_ctx* c, int32_t sid, int32_t length) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "session_truncate: session %d is not open", sid);
+  Session& s = c->sessions[sid];
+  if (length < 0 || length > s.len)
+    return fail(c, MAG_ERR_INVALID_ARG, "session_truncate: length %d not in 0..%d", length, s.len);
+  // blocks wholly past the new length go back to the pool; the device table keeps stale entries past
+  // the length, which nothing reads, and a later append writes the new ids before they are used
+  const size_t nb = (size_t)(length + 15) / 16;
+  while (s.table.size() > nb) {
+    c->free_list.push_back(s.table.back());
+    s.table.pop_back();
+  }
+  s.len = length;
   return MAG_OK;
 }
 
