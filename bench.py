@@ -442,8 +442,9 @@ def run_prefill(args, tc_peak):
     n_draft = 4  # the verify leg: drafts checked in one call on a session after its chunk
     blocks = n_sets * -(-(p + T + n_draft) // 16)
     stream = torch.cuda.Stream()
-    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sets, max_batch=1,
-                          max_chunk=T, max_context=p + T + n_draft)
+    # max_batch = n_draft: the verify leg runs on the decode kernels, one row per draft
+    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sets,
+                          max_batch=n_draft, max_chunk=T, max_context=p + T + n_draft)
     t_setup = time.time()
     ctx = mag.Context(cfg, stream.cuda_stream)
     with torch.cuda.stream(stream):
@@ -483,6 +484,7 @@ def run_prefill(args, tc_peak):
     for _ in range(3):
         ctx.verify_tokens(sid_v, n_draft, xv, ov)
         ctx.session_truncate(sid_v, base_len)
+    v_launches = ctx.last_step_launches()
     v_runs = 20
     ev0.record(stream)
     for _ in range(v_runs):
@@ -503,7 +505,7 @@ def run_prefill(args, tc_peak):
                                  "the tensor work, which is not counted as achieved"},
             "launches_per_chunk": launches, "prefill_weight_bytes": st["prefill_weight_bytes"],
             "verify": {"drafts": n_draft, "context": base_len, "ms_per_call": s_verify * 1e3,
-                       "tokens_per_s": n_draft / s_verify},
+                       "tokens_per_s": n_draft / s_verify, "launches_per_call": v_launches},
             "setup_s": t_setup}
 
 

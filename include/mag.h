@@ -162,7 +162,7 @@ mag_status mag_session_length(mag_ctx* ctx, int32_t session, int32_t* length_out
  * tokens that mag_verify_tokens appended and the caller rejected. Blocks
  * wholly past the new length go back to the free list; the tokens past it are
  * never read again and the next append overwrites them. The pages have no
- * counterpart (their speculative controller, [Core] 5.5, is out of scope;
+ * counterpart (their speculative controller, [Core] 5.6, is out of scope;
  * only this step of it is built). Host-only, no launch. Errors: INVALID_ARG. */
 mag_status mag_session_truncate(mag_ctx* ctx, int32_t session, int32_t length);
 
@@ -206,11 +206,16 @@ mag_status mag_prefill_chunk(mag_ctx* ctx, int32_t session, int32_t n_tokens, co
                              void* last_out_dev);
 
 /* Multi-token verify step (draft tokens of speculative decoding checked in
- * one pass): like mag_prefill_chunk with n_tokens = 1..4, but writing the fp16
- * output of every token, out_dev[n_tokens][V] (or [n_tokens][D] when
- * vocab == 0): token j attends causally to the session's cache and tokens
- * 0..j. All n_tokens are appended; mag_session_truncate drops the rejected
- * ones. Needs max_chunk >= n_tokens. Errors: as mag_prefill_chunk. */
+ * one pass, [Core] 5.6): n_tokens tokens of one session at its next
+ * positions, writing the fp16 output of every token, out_dev[n_tokens][V] (or
+ * [n_tokens][D] when vocab == 0): token j attends causally to the session's
+ * cache and tokens 0..j. hidden_in_dev is fp16 [n_tokens][D]. All n_tokens
+ * are appended; mag_session_truncate drops the rejected ones. With
+ * n_tokens <= max_batch it runs as a decode step whose rows are the tokens
+ * (each W4 matrix read once for all of them; one captured graph per count);
+ * otherwise, with n_tokens <= min(4, max_chunk), through the prefill chunk
+ * path. Errors: INVALID_ARG (count outside both ranges, session, buffers),
+ * CONTEXT_FULL, KV_FULL, NOT_LOADED, CUDA. */
 mag_status mag_verify_tokens(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
                              void* out_dev);
 

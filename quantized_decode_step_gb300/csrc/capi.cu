@@ -127,6 +127,8 @@ struct mag_ctx {
 
   cudaGraphExec_t graphs[MAG_MAX_BATCH + 1] = {};
   int graph_launches[MAG_MAX_BATCH + 1] = {};
+  cudaGraphExec_t vgraphs[MAG_MAX_BATCH + 1] = {};  // verify steps, by draft count
+  int vgraph_launches[MAG_MAX_BATCH + 1] = {};
   int last_launches = 0;
   uint64_t other_bytes = 0;
   // chunked prefill (max_chunk > 0): exact two-term fp16 weight copies, their TMA maps, planned buffers
@@ -344,7 +346,10 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
 }
 
 // Enqueue the whole decode step for batch B (captured into a graph or run eagerly).
-cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullptr) {
+// The decode step's launches. With `verify` the B rows are B consecutive new tokens of one session: their
+// keys and values go into the pool in one store kernel after the QKV projection, and attention reads them
+// there (row b causally up to its own position) instead of each row appending its own.
+cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullptr, bool verify = false) {
   const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof;
   Launch L0{c->stream, false, n_launch};
   Launch L{c->stream, pdl, n_launch};
@@ -374,6 +379,17 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
       a.rope_sin = c->d_sin;
       MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, XSRC_RESID, EPI_QKV));
     }
+    if (verify) {  // the B tokens' k and v into the pool
+      KvChunkArgs kc = {};
+      kc.qkv = c->qkv;
+      kc.qkv_ld = c->R;
+      kc.n_heads = c->Hq;
+      kc.n_tok = B;
+      kc.layer = l;
+      kc.pool = pg;
+      kc.step = c->d_args;
+      MAG_RUN(MAG_OP_ATTENTION, launch_kv_store_chunk(L, kc));
+    }
     {  // KV append + attention
       AttnArgs a = {};
       a.qkv = c->qkv;
@@ -387,6 +403,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
       a.n_split = S;
       a.pool = pg;
       a.step = c->d_args;
+      a.stored = verify;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
     {  // O projection + residual
@@ -425,6 +442,8 @@ void free_ctx(mag_ctx* c) {
   if (!c) return;
   if (c->stream) cudaStreamSynchronize(c->stream);
   for (auto& g : c->graphs)
+    if (g) cudaGraphExecDestroy(g);
+  for (auto& g : c->vgraphs)
     if (g) cudaGraphExecDestroy(g);
   for (auto& e : c->ring_ev)
     if (e) cudaEventDestroy(e);
@@ -973,33 +992,43 @@ static mag_status step_upload(mag_ctx* c, int B, const int32_t* sids, const void
   return MAG_OK;
 }
 
+// Launches the step of B rows whose arguments were just uploaded: the captured graph of that shape
+// (captured on first use), or the kernels one by one under MAG_FLAG_NO_GRAPH.
+static mag_status launch_step(mag_ctx* c, int B, bool verify) {
+  if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
+    int n = 0;
+    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify));
+    c->last_launches = n;
+    return MAG_OK;
+  }
+  cudaGraphExec_t& ge = verify ? c->vgraphs[B] : c->graphs[B];
+  int& n_launch = verify ? c->vgraph_launches[B] : c->graph_launches[B];
+  if (!ge) {
+    cudaGraph_t g = nullptr;
+    int n = 0;
+    CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = record_step(c, B, &n, nullptr, verify);
+    cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+    if (e != cudaSuccess || e2 != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return fail(c, MAG_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
+    }
+    cudaError_t e3 = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (e3 != cudaSuccess) return fail(c, MAG_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e3));
+    n_launch = n;
+  }
+  CUDA_TRY(c, cudaGraphLaunch(ge, c->stream));
+  c->last_launches = n_launch;
+  return MAG_OK;
+}
+
 mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out) {
   if (!c) return MAG_ERR_INVALID_ARG;
   mag_status st = step_upload(c, B, sids, in, out);
   if (st != MAG_OK) return st;
-  if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
-    int n = 0;
-    CUDA_TRY(c, record_step(c, B, &n));
-    c->last_launches = n;
-  } else {
-    if (!c->graphs[B]) {
-      cudaGraph_t g = nullptr;
-      int n = 0;
-      CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-      cudaError_t e = record_step(c, B, &n);
-      cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
-      if (e != cudaSuccess || e2 != cudaSuccess) {
-        if (g) cudaGraphDestroy(g);
-        return fail(c, MAG_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
-      }
-      cudaError_t e3 = cudaGraphInstantiate(&c->graphs[B], g, 0);
-      cudaGraphDestroy(g);
-      if (e3 != cudaSuccess) return fail(c, MAG_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e3));
-      c->graph_launches[B] = n;
-    }
-    CUDA_TRY(c, cudaGraphLaunch(c->graphs[B], c->stream));
-    c->last_launches = c->graph_launches[B];
-  }
+  st = launch_step(c, B, false);
+  if (st != MAG_OK) return st;
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
   return MAG_OK;
 }
@@ -1178,11 +1207,61 @@ mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in,
   return run_chunk(c, "prefill_chunk", sid, T, in, last_out, 1);
 }
 
+// Verify step on the decode kernels: the n tokens are the n rows of a decode step of one session at
+// positions len .. len + n - 1, with their keys and values stored between the QKV projection and attention.
+static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void* in, void* out) {
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: session %d is not open", sid);
+  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "verify_tokens: not every weight is loaded");
+  Session& s = c->sessions[sid];
+  if ((int64_t)s.len + n > c->cfg.max_context)
+    return fail(c, MAG_ERR_CONTEXT_FULL, "verify_tokens: %d + %d tokens exceed max_context %d", s.len, n,
+                c->cfg.max_context);
+  // n <= 16 tokens reach at most one block past the session's last one
+  const int nb_old = (s.len + 15) / 16, nb_new = (s.len + n + 15) / 16;
+  if (nb_new - nb_old > (int)c->free_list.size())
+    return fail(c, MAG_ERR_KV_FULL, "verify_tokens: needs %d blocks, %zu free", nb_new - nb_old,
+                c->free_list.size());
+  const int slot = c->ring_pos;
+  CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
+  StepArgs& a = c->h_ring[slot];
+  memset(&a, 0, sizeof a);
+  a.batch = n;
+  for (int b = 0; b < n; ++b) {
+    a.sess[b] = sid;
+    a.pos[b] = s.len + b;
+  }
+  for (int i = nb_old; i < nb_new; ++i) {
+    const int blk = c->free_list.front();
+    c->free_list.pop_front();
+    s.table.push_back(blk);
+    a.upd_sess[a.n_upd] = sid;
+    a.upd_idx[a.n_upd] = i;
+    a.upd_blk[a.n_upd] = blk;
+    ++a.n_upd;
+  }
+  a.hidden_in = (const __half*)in;
+  a.out = out;
+  CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
+  CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
+  c->ring_pos = (slot + 1) % kRing;
+  mag_status st = launch_step(c, n, true);
+  if (st != MAG_OK) return st;
+  s.len += n;
+  return MAG_OK;
+}
+
 mag_status mag_verify_tokens(mag_ctx* c, int32_t sid, int32_t n_tokens, const void* hidden_in, void* out) {
   if (!c) return MAG_ERR_INVALID_ARG;
-  if (n_tokens < 1 || n_tokens > kPipeMaxBatch)
-    return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: %d tokens not in 1..%d", n_tokens, kPipeMaxBatch);
-  return run_chunk(c, "verify_tokens", sid, n_tokens, hidden_in, out, n_tokens);
+  if (!hidden_in || !out) return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: null buffer");
+  // up to max_batch tokens on the decode kernels (weights read once for all rows); beyond that, up to
+  // kPipeMaxBatch tokens through the prefill chunk path when the context has one
+  if (n_tokens >= 1 && n_tokens <= c->B_max) return verify_on_step(c, sid, n_tokens, hidden_in, out);
+  const int chunk_max = std::min(kPipeMaxBatch, c->cfg.max_chunk);
+  if (n_tokens >= 1 && n_tokens <= chunk_max)
+    return run_chunk(c, "verify_tokens", sid, n_tokens, hidden_in, out, n_tokens);
+  return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: %d tokens not in 1..%d", n_tokens,
+              std::max(c->B_max, chunk_max));
 }
 
 mag_status mag_session_truncate(mag_ctx* c, int32_t sid, int32_t length) {

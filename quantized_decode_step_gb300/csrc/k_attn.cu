@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // steps, so their fetch starts before waiting for the QKV projection.
   const int pos = a.step->pos[b], sess = a.step->sess[b];
   const int n_keys = pos + 1, new_blk = pos >> 4;
+  // blocks from fresh_blk on hold keys written in this step (the row's own, or with stored keys those of
+  // the session's earlier rows as well); they are mapped and fetched only after the wait
+  const int fresh_blk = a.stored ? a.step->pos[0] >> 4 : new_blk;
   const int n_blocks = new_blk + 1;
   const int bps = (n_blocks + S - 1) / S;
   const int blk0 = split * bps, blk1 = min(blk0 + bps, n_blocks);
@@ -299,20 +302,20 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // this warp's blocks: blk0 + warp + 4 j; the new token's block, if it is one
   // of them, is the last
   const int nb = blk0 + warp < blk1 ? (blk1 - blk0 - warp + 3) / 4 : 0;
-  // physical ids of the warp's first 32 blocks, one lane each (one round trip for all of them); the
-  // new token's block may have been mapped by this step's prologue, so its id is read after the wait
+  // physical ids of the warp's first 32 blocks, one lane each (one round trip for all of them); a block
+  // from fresh_blk on may have been mapped by this step's prologue, so its id is read after the wait
   const int phys_l = lane < nb ? table[blk0 + warp + 4 * lane] : 0;
   int phys_new = -1;
   auto phys_of = [&](int j) {
     const int blk = blk0 + warp + 4 * j;
     const int p = j < 32 ? __shfl_sync(0xffffffffu, phys_l, j) : table[blk];
-    return blk == new_blk ? phys_new : p;
+    return blk == new_blk ? phys_new : blk >= fresh_blk ? table[blk] : p;
   };
   uint8_t* ring = smem + (size_t)warp * kAttnSlots * SG::kBytes;
   int issued = 0;
   for (; issued < min(nb, kAttnSlots); ++issued) {
     const int blk = blk0 + warp + 4 * issued;
-    if (blk == new_blk) break;
+    if (blk >= fresh_blk) break;
     issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys_of(issued), gk, lane);
     cp_async_commit();
   }
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
 
   // the block that holds the new token appends its K (rotated) and V to the pool
-  if (blk0 <= new_blk && new_blk < blk1) {
+  if (!a.stored && blk0 <= new_blk && new_blk < blk1) {
     if (tid < D) {
       s_kv[0][tid] = qkv[(int64_t)(Hq + gk) * D + tid];
       s_kv[1][tid] = qkv[(int64_t)(Hq + Hkv + gk) * D + tid];
@@ -333,11 +336,11 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     store_vec(a.pool, a.layer, phys, pos & 15, gk, 1, s_kv[1], s_red);
     __threadfence_block();
     __syncthreads();
-    if (issued < min(nb, kAttnSlots)) {  // this warp's deferred fetch of the new token's block
-      issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys, gk, lane);
-      cp_async_commit();
-      ++issued;
-    }
+  }
+  // this warp's deferred fetches: the ring slots its blocks from fresh_blk on did not get before the wait
+  for (; issued < min(nb, kAttnSlots); ++issued) {
+    issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys_of(issued), gk, lane);
+    cp_async_commit();
   }
   for (; issued < kAttnSlots; ++issued) cp_async_commit();  // one group per ring slot
 
@@ -578,8 +581,9 @@ __global__ void kv_store_chunk_kernel(const KvChunkArgs a) {
   xk[i] = row[(int64_t)(a.n_heads + h) * d + i];
   xv[i] = row[(int64_t)(a.n_heads + Hkv + h) * d + i];
   __syncthreads();
-  const int pos = a.pos0 + t;
-  const int blk = a.table[pos >> 4];
+  const int pos = (a.step ? a.step->pos[0] : a.pos0) + t;
+  const int32_t* table = a.step ? a.pool.tables + (int64_t)a.step->sess[0] * a.pool.table_stride : a.table;
+  const int blk = table[pos >> 4];
   store_vec(a.pool, a.layer, blk, pos & 15, h, 0, xk, red);
   store_vec(a.pool, a.layer, blk, pos & 15, h, 1, xv, red);
 }

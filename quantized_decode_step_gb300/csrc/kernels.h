@@ -137,6 +137,9 @@ struct KvChunkArgs {
   int32_t n_tok, pos0, layer;
   const int32_t* table;
   PoolGeom pool;
+  // when set, pos0 and the table row are read on the device from the step arguments (session sess[0] from
+  // position pos[0]), so a captured graph serves any session and position
+  const StepArgs* step;
 };
 cudaError_t launch_kv_store_chunk(const Launch& L, const KvChunkArgs& a);
 
@@ -166,6 +169,10 @@ struct AttnArgs {
   int32_t n_split;  // grid.x = cluster size (<= 16)
   PoolGeom pool;
   const StepArgs* step;
+  // 0: row b appends its own token (position pos[b]) and attends to 0 .. pos[b].
+  // 1: the rows are consecutive new tokens of one session (pos[b] = pos[0] + b) whose keys and values an
+  //    earlier kernel stored; row b attends causally to 0 .. pos[b] and appends nothing.
+  int32_t stored;
 };
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch);
 // Largest split count (cluster size) the device can co-schedule for this head size and KV type.
