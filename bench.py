@@ -509,6 +509,43 @@ def run_prefill(args, tc_peak):
             "setup_s": t_setup}
 
 
+def run_plans(args):
+    """Measurement aid for the adaptive plans: decode step time (8B, one FP16 session) at short, medium and
+    long contexts under every split count the plans can take, each plan forced in turn. Prints one JSON
+    line {"plans": {splits: {context: ms per step}}, "presets": [...]} and exits."""
+    import torch
+    import quantized_decode_step_gb300 as mag
+    from synth import driver
+    mag.build()
+    lens = (40, 100, 300, 700, 2048, 8192)
+    steps = max(args.steps, 8)
+    wl = Workload("8b-plans", LLAMA8B, KV_FP16, len(lens), lens)
+    ctx, sids = driver.setup(wl, args.seed, extra_tokens=steps + args.warmup + 8)
+    x = torch.zeros((1, LLAMA8B.hidden), dtype=torch.float16, device="cuda")
+    out = torch.empty((1, LLAMA8B.vocab), dtype=torch.float16, device="cuda")
+    res = {}
+    for S in (1, 2, 4, 8, 16):
+        ctx.set_adaptive(True, force_plan=1, plan_splits=(S, S, S))
+        row = {}
+        for sid, n in zip(sids, lens):
+            for _ in range(args.warmup):
+                ctx.decode_step([sid], x, out)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                ctx.decode_step([sid], x, out)
+            e1.record()
+            e1.synchronize()
+            row[n] = round(e0.elapsed_time(e1) / steps, 4)
+            ctx.session_truncate(sid, n)
+        res[S] = row
+    a = mag.adapt_defaults()
+    print(json.dumps({"plans": res, "presets": list(a.plan_splits), "unit": "ms per decode step",
+                       "workload": "8b decode, 1 FP16 session, contexts " + "/".join(map(str, lens))}))
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,10 +558,15 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill leg")
     ap.add_argument("--eager", action="store_true",
                     help="profiling aid: launch the step's kernels one by one instead of replaying a CUDA graph")
+    ap.add_argument("--plans", action="store_true",
+                    help="measurement aid: decode step time per attention split count and context, then exit")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: the same per-layer shapes with fewer layers (not a bench configuration)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.plans:
+        run_plans(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -257,6 +257,68 @@ uint64_t mag_kv_bytes_per_token(const mag_config* cfg);
 mag_status mag_quantize_w4g32(const void* src_dev, int64_t rows, int64_t cols, void* codes_dev, void* scale_min_dev,
                               void* cuda_stream);
 
+/* ---- adaptive runtime: load profile, plan switching, hot pool size ----
+ * [Magnitude] 2.1-2.2, 3.1-3.3, 4.3 and 6.1-6.2: a profile of recent
+ * inferences (sliding window, sampled) whose P90 length picks one of three
+ * preset plans (short / medium / long sequences) and sizes the hot KV pool.
+ * Here an "inference" is one session row of a decode or verify step, and its
+ * length is the context that row attends to (its position + 1). A plan is a
+ * decode-attention split count (the thread-block cluster size over a
+ * session's keys); each plan has its own captured graphs, and a switch swaps
+ * which graphs the step launches. */
+typedef struct mag_adapt_config {
+  int32_t enable_adaptive;       /* 0: the profile and every policy are off (the default state) */
+  int32_t adaptive_window_size;  /* recorded inferences in the window; the pages' default 64 */
+  int32_t adaptive_sample_rate;  /* one inference in this many is recorded; default 4 */
+  int32_t plan_short_below;      /* P90 below this: short plan (0); default 128 */
+  int32_t plan_long_above;       /* P90 above this: long plan (2); between the two, medium (1); default 512 */
+  int32_t plan_splits[3];        /* attention splits of plans 0, 1, 2 for one session; a batch of B
+                                    uses min(this, the context's default for B), the default being
+                                    about 2 blocks per SM, at most the device's largest co-scheduled
+                                    cluster (16); 0 = the default */
+  int32_t force_plan;            /* -1: plans follow the profile; 0..2: that plan, always */
+  int32_t async_switch;          /* 1: a new plan's graphs are captured on a background thread and the
+                                    step keeps the old plan until they are ready */
+  float hot_pool_slack;          /* hot pool = slack x the blocks of the P90 length per open session;
+                                    default 1.2 */
+} mag_adapt_config;
+
+/* The pages' defaults (enable_adaptive = 1, window 64, rate 4, thresholds 128 / 512, no forced plan,
+ * no async switch, slack 1.2) and split counts 4 / 8 / 16 measured on GB300 for the three plans. */
+void mag_adapt_defaults(mag_adapt_config* out);
+
+/* Turn the adaptive runtime on (or off with enable_adaptive = 0) and reset its profile. The plan in use
+ * stays until the first decision. Errors: INVALID_ARG (window or rate < 1, thresholds out of order,
+ * split or plan out of range). */
+mag_status mag_set_adaptive(mag_ctx* ctx, const mag_adapt_config* cfg);
+
+typedef struct mag_profile {
+  int64_t seen;        /* inferences offered to the profile */
+  int32_t recorded;    /* in the window (<= adaptive_window_size) */
+  int32_t p50, p90, p99; /* nearest-rank quantiles of the window; -1 while it is empty */
+  int32_t plan;        /* plan the next step launches */
+  int32_t pending_plan; /* plan whose graphs a background capture is building; -1 if none */
+  int32_t plan_splits; /* attention split count of `plan` */
+  int32_t switches;    /* plan changes so far */
+  int64_t hot_blocks;  /* hot pool target from the last full window; -1 before one */
+} mag_profile;
+mag_status mag_get_profile(mag_ctx* ctx, mag_profile* out);
+
+/* The profile on its own (host only, no context or GPU), for callers that keep their own statistics:
+ * observe returns 1 when the value was recorded (the first observation, then every sample_every-th);
+ * quantile is nearest-rank over the window (the ceil(q n)-th smallest, q in (0, 1]; -1 if empty). */
+typedef struct mag_profiler mag_profiler;
+mag_status mag_profiler_create(int32_t window, int32_t sample_every, mag_profiler** out);
+void mag_profiler_destroy(mag_profiler* p);
+int32_t mag_profiler_observe(mag_profiler* p, int32_t length);
+mag_status mag_profiler_quantile(const mag_profiler* p, double q, int32_t* out);
+int32_t mag_profiler_count(const mag_profiler* p);
+/* The two policies as pure functions: plan of a P90 length (0 below short_below, 2 above long_above,
+ * else 1), and the hot pool in blocks, ceil(slack x n_sessions x ceil(p90 / 16)) with slack taken to
+ * six decimals (0 when p90 or n_sessions is not positive). */
+int32_t mag_plan_for(int32_t p90, int32_t short_below, int32_t long_above);
+int64_t mag_hot_pool_blocks(int32_t p90, int32_t n_sessions, float slack);
+
 /* ---- debug and test hooks ---- */
 
 /* Copy a loaded projection back in W4G32 bytes (codes then pairs) into dst_dev. */

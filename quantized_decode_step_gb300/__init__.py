@@ -31,6 +31,8 @@ EXPORTED = [
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
     "mag_debug_last_step_launches", "mag_debug_profile_step",
+    "mag_adapt_defaults", "mag_set_adaptive", "mag_get_profile", "mag_profiler_create", "mag_profiler_destroy",
+    "mag_profiler_observe", "mag_profiler_quantile", "mag_profiler_count", "mag_plan_for", "mag_hot_pool_blocks",
 ]
 OP_NAMES = ["step_begin", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head"]
 
@@ -63,6 +65,20 @@ class MemoryStats(ctypes.Structure):
 class ArenaTensor(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 24), ("size", ctypes.c_uint64), ("first", ctypes.c_int32),
                 ("last", ctypes.c_int32), ("offset", ctypes.c_uint64)]
+
+
+class AdaptConfig(ctypes.Structure):
+    _fields_ = [("enable_adaptive", ctypes.c_int32), ("adaptive_window_size", ctypes.c_int32),
+                ("adaptive_sample_rate", ctypes.c_int32), ("plan_short_below", ctypes.c_int32),
+                ("plan_long_above", ctypes.c_int32), ("plan_splits", ctypes.c_int32 * 3),
+                ("force_plan", ctypes.c_int32), ("async_switch", ctypes.c_int32), ("hot_pool_slack", ctypes.c_float)]
+
+
+class Profile(ctypes.Structure):
+    _fields_ = [("seen", ctypes.c_int64), ("recorded", ctypes.c_int32), ("p50", ctypes.c_int32),
+                ("p90", ctypes.c_int32), ("p99", ctypes.c_int32), ("plan", ctypes.c_int32),
+                ("pending_plan", ctypes.c_int32), ("plan_splits", ctypes.c_int32), ("switches", ctypes.c_int32),
+                ("hot_blocks", ctypes.c_int64)]
 
 
 def build(force: bool = False) -> str:
@@ -107,6 +123,16 @@ def lib():
                 "mag_debug_last_step_launches": ([vp], i32),
                 "mag_debug_profile_step": ([vp, i32, P32, vp, vp, P32, ctypes.POINTER(ctypes.c_float), i32, P32],
                                            i32),
+                "mag_adapt_defaults": ([ctypes.POINTER(AdaptConfig)], None),
+                "mag_set_adaptive": ([vp, ctypes.POINTER(AdaptConfig)], i32),
+                "mag_get_profile": ([vp, ctypes.POINTER(Profile)], i32),
+                "mag_profiler_create": ([i32, i32, ctypes.POINTER(vp)], i32),
+                "mag_profiler_destroy": ([vp], None),
+                "mag_profiler_observe": ([vp, i32], i32),
+                "mag_profiler_quantile": ([vp, ctypes.c_double, P32], i32),
+                "mag_profiler_count": ([vp], i32),
+                "mag_plan_for": ([i32, i32, i32], i32),
+                "mag_hot_pool_blocks": ([i32, i32, ctypes.c_float], i64),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -149,6 +175,55 @@ def quantize_w4g32(src, rows, cols, codes, scale_min, stream=0):
     st = lib().mag_quantize_w4g32(_ptr(src), rows, cols, _ptr(codes), _ptr(scale_min), stream)
     if st != OK:
         raise MagError(st, "mag_quantize_w4g32")
+
+
+def adapt_defaults() -> AdaptConfig:
+    a = AdaptConfig()
+    lib().mag_adapt_defaults(ctypes.byref(a))
+    return a
+
+
+class Profiler:
+    """The load profile on its own (host only): sliding window, sampled, nearest-rank quantiles."""
+
+    def __init__(self, window=64, sample_every=4):
+        h = ctypes.c_void_p()
+        st = lib().mag_profiler_create(window, sample_every, ctypes.byref(h))
+        if st != 0:
+            raise MagError(st, f"mag_profiler_create({window}, {sample_every})")
+        self.h = h
+
+    def observe(self, length) -> bool:
+        return bool(lib().mag_profiler_observe(self.h, int(length)))
+
+    def quantile(self, q) -> int:
+        out = ctypes.c_int32()
+        st = lib().mag_profiler_quantile(self.h, float(q), ctypes.byref(out))
+        if st != 0:
+            raise MagError(st, f"mag_profiler_quantile({q})")
+        return out.value
+
+    def count(self) -> int:
+        return int(lib().mag_profiler_count(self.h))
+
+    def close(self):
+        if self.h:
+            lib().mag_profiler_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def plan_for(p90, short_below=128, long_above=512) -> int:
+    return int(lib().mag_plan_for(p90, short_below, long_above))
+
+
+def hot_pool_blocks(p90, n_sessions, slack=1.2) -> int:
+    return int(lib().mag_hot_pool_blocks(p90, n_sessions, slack))
 
 
 class Context:
@@ -256,6 +331,23 @@ class Context:
 
     def last_step_launches(self) -> int:
         return int(lib().mag_debug_last_step_launches(self.h))
+
+    def set_adaptive(self, enable=True, **fields):
+        """Adaptive runtime from the library's defaults with the given fields replaced (plan_splits: a
+        3-sequence); enable=False turns it off."""
+        a = adapt_defaults()
+        a.enable_adaptive = 1 if enable else 0
+        for k, v in fields.items():
+            if k == "plan_splits":
+                a.plan_splits = (ctypes.c_int32 * 3)(*v)
+            else:
+                setattr(a, k, v)
+        self._check(lib().mag_set_adaptive(self.h, ctypes.byref(a)), "mag_set_adaptive")
+
+    def profile(self) -> dict:
+        p = Profile()
+        self._check(lib().mag_get_profile(self.h, ctypes.byref(p)), "mag_get_profile")
+        return {n: getattr(p, n) for n, _ in Profile._fields_}
 
     def profile_step(self, sessions, hidden_in, out, cap=4096):
         """Instrumented step: list of (op name, device ms) per kernel launch."""

@@ -2,14 +2,18 @@
 // plan, CUDA-graph step and the debug hooks. See include/mag.h for the
 // contract of each call.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <deque>
+#include <memory>
 #include <string>
+#include <thread>
 #include <vector>
 
+#include "adapt.h"
 #include "arena.h"
 #include "kernels.h"
 #include "noalloc.h"
@@ -125,11 +129,25 @@ struct mag_ctx {
   void* d_in_stage = nullptr;
   void* d_out_stage = nullptr;
 
-  cudaGraphExec_t graphs[MAG_MAX_BATCH + 1] = {};
-  int graph_launches[MAG_MAX_BATCH + 1] = {};
-  cudaGraphExec_t vgraphs[MAG_MAX_BATCH + 1] = {};  // verify steps, by draft count
-  int vgraph_launches[MAG_MAX_BATCH + 1] = {};
+  // captured step graphs by [verify][plan][batch]: a verify step's rows are the drafts of one session
+  struct StepGraph {
+    cudaGraphExec_t exec = nullptr;
+    int launches = 0;
+  };
+  StepGraph graphs[2][3][MAG_MAX_BATCH + 1];
   int last_launches = 0;
+
+  // adaptive runtime: load profile, plan in use, background capture of a new plan's graphs
+  mag_adapt_config adapt{};  // enable_adaptive = 0 until mag_set_adaptive
+  std::unique_ptr<LoadProfile> profile;
+  int cur_plan = 1;
+  int switches = 0;
+  int64_t hot_blocks = -1;
+  int pending_plan = -1;
+  std::thread cap_thread;
+  std::atomic<int> cap_state{0};  // 0 idle, 1 capturing, 2 done, 3 failed
+  std::string cap_err;
+  cudaStream_t cap_stream = nullptr;
   uint64_t other_bytes = 0;
   // chunked prefill (max_chunk > 0): exact two-term fp16 weight copies, their TMA maps, planned buffers
   struct PrefillProj {
@@ -349,22 +367,25 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
 // The decode step's launches. With `verify` the B rows are B consecutive new tokens of one session: their
 // keys and values go into the pool in one store kernel after the QKV projection, and attention reads them
 // there (row b causally up to its own position) instead of each row appending its own.
-cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullptr, bool verify = false) {
+// `splits` is the attention split count of the plan in use; `st` the stream the launches go to (the
+// context's, or a capture stream).
+cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool verify, int splits,
+                        cudaStream_t st) {
   const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof;
-  Launch L0{c->stream, false, n_launch};
-  Launch L{c->stream, pdl, n_launch};
+  Launch L0{st, false, n_launch};
+  Launch L{st, pdl, n_launch};
   cudaError_t e;
   // every launch goes through MAG_RUN, which brackets it with events when profiling
-#define MAG_RUN(kind, call)                                                   \
-  do {                                                                       \
-    if (prof && (e = prof->begin(c->stream)) != cudaSuccess) return e;       \
-    if ((e = (call)) != cudaSuccess) return e;                               \
-    if (prof && (e = prof->end(c->stream, (kind))) != cudaSuccess) return e; \
+#define MAG_RUN(kind, call)                                            \
+  do {                                                                \
+    if (prof && (e = prof->begin(st)) != cudaSuccess) return e;       \
+    if ((e = (call)) != cudaSuccess) return e;                        \
+    if (prof && (e = prof->end(st, (kind))) != cudaSuccess) return e; \
   } while (0)
   MAG_RUN(MAG_OP_STEP_BEGIN,
           launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B, c->ss_part));
   const PoolGeom pg = pool_geom(c);
-  const int S = attn_splits(c, B);
+  const int S = splits;
   for (int l = 0; l < c->L; ++l) {
     const Proj* P = &c->proj[(size_t)l * 4];
     {  // RMSNorm + QKV + RoPE of q and k
@@ -441,10 +462,12 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof = nullp
 void free_ctx(mag_ctx* c) {
   if (!c) return;
   if (c->stream) cudaStreamSynchronize(c->stream);
-  for (auto& g : c->graphs)
-    if (g) cudaGraphExecDestroy(g);
-  for (auto& g : c->vgraphs)
-    if (g) cudaGraphExecDestroy(g);
+  if (c->cap_thread.joinable()) c->cap_thread.join();
+  for (auto& gv : c->graphs)
+    for (auto& gp : gv)
+      for (auto& g : gp)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
   for (auto& e : c->ring_ev)
     if (e) cudaEventDestroy(e);
   cudaFree(c->wbase);
@@ -992,44 +1015,120 @@ static mag_status step_upload(mag_ctx* c, int B, const int32_t* sids, const void
   return MAG_OK;
 }
 
+// Attention split count of plan p at batch B: the plan's count (a single-session figure), capped by the
+// context's default for B (which shrinks as the batch fills the GPU); 0 = the default.
+static int plan_splits(const mag_ctx* c, int p, int B) {
+  const int s = c->adapt.enable_adaptive ? c->adapt.plan_splits[p] : 0;
+  return s > 0 ? std::min(s, attn_splits(c, B)) : attn_splits(c, B);
+}
+
+// Capture and instantiate the step graph of (verify, plan p, batch B) on stream st: the context's
+// stream, or the capture stream of a background switch.
+static cudaError_t capture_graph(mag_ctx* c, bool verify, int p, int B, cudaStream_t st,
+                                 mag_ctx::StepGraph& out) {
+  cudaGraph_t g = nullptr;
+  int n = 0;
+  cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return e;
+  e = record_step(c, B, &n, nullptr, verify, plan_splits(c, p, B), st);
+  const cudaError_t e2 = cudaStreamEndCapture(st, &g);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&out.exec, g, 0);
+  if (g) cudaGraphDestroy(g);
+  if (e == cudaSuccess) out.launches = n;
+  return e;
+}
+
+// A background capture that has finished: switch to its plan, or report why it failed.
+static mag_status poll_capture(mag_ctx* c) {
+  const int s = c->cap_state.load(std::memory_order_acquire);
+  if (s != 2 && s != 3) return MAG_OK;
+  c->cap_thread.join();
+  c->cap_state.store(0);
+  const int p = c->pending_plan;
+  c->pending_plan = -1;
+  if (s == 3) return fail(c, MAG_ERR_CUDA, "capture of plan %d: %s", p, c->cap_err.c_str());
+  c->cur_plan = p;
+  ++c->switches;
+  return MAG_OK;
+}
+
+// Wait for a background capture (before the graphs or the configuration change under it).
+static mag_status finish_capture(mag_ctx* c) {
+  if (c->cap_thread.joinable()) c->cap_thread.join();
+  return poll_capture(c);
+}
+
+// Switch to plan p: at once (its graphs are captured on first use by the step), or, with async_switch,
+// after a background thread has captured p's graphs for every shape the current plan has captured.
+static void switch_plan(mag_ctx* c, int p) {
+  std::vector<std::pair<int, int>> shapes;
+  if (c->adapt.async_switch && !(c->cfg.flags & MAG_FLAG_NO_GRAPH))
+    for (int v = 0; v < 2; ++v)
+      for (int b = 1; b <= MAG_MAX_BATCH; ++b)
+        if (c->graphs[v][c->cur_plan][b].exec && !c->graphs[v][p][b].exec) shapes.emplace_back(v, b);
+  if (shapes.empty()) {
+    c->cur_plan = p;
+    ++c->switches;
+    return;
+  }
+  c->pending_plan = p;
+  c->cap_state.store(1);
+  c->cap_thread = std::thread([c, p, shapes]() {
+    cudaError_t e = cudaSetDevice(c->device);
+    for (const auto& sh : shapes) {
+      if (e != cudaSuccess) break;
+      e = capture_graph(c, sh.first != 0, p, sh.second, c->cap_stream, c->graphs[sh.first][p][sh.second]);
+    }
+    if (e != cudaSuccess) c->cap_err = cudaGetErrorString(e);
+    c->cap_state.store(e == cudaSuccess ? 2 : 3, std::memory_order_release);
+  });
+}
+
+// Offer a finished step's rows (the context length each attended) to the load profile; on a recorded
+// sample with the window full, update the hot pool target and pick the plan of the window's P90.
+static void adapt_after_step(mag_ctx* c, int B, const int32_t* lens) {
+  if (!c->adapt.enable_adaptive) return;
+  bool rec = false;
+  for (int b = 0; b < B; ++b) rec |= c->profile->observe(lens[b]);
+  if (!rec || !c->profile->full()) return;
+  const int32_t p90 = c->profile->quantile(0.9);
+  int open = 0;
+  for (const Session& s : c->sessions) open += s.open;
+  c->hot_blocks = hot_pool_blocks(p90, open, c->adapt.hot_pool_slack, 16);
+  if (c->adapt.force_plan >= 0 || c->pending_plan >= 0) return;
+  const int want = plan_for(p90, c->adapt.plan_short_below, c->adapt.plan_long_above);
+  if (want != c->cur_plan) switch_plan(c, want);
+}
+
 // Launches the step of B rows whose arguments were just uploaded: the captured graph of that shape
-// (captured on first use), or the kernels one by one under MAG_FLAG_NO_GRAPH.
+// under the plan in use (captured on first use), or the kernels one by one under MAG_FLAG_NO_GRAPH.
 static mag_status launch_step(mag_ctx* c, int B, bool verify) {
+  const int S = plan_splits(c, c->cur_plan, B);
   if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
     int n = 0;
-    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify));
+    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify, S, c->stream));
     c->last_launches = n;
     return MAG_OK;
   }
-  cudaGraphExec_t& ge = verify ? c->vgraphs[B] : c->graphs[B];
-  int& n_launch = verify ? c->vgraph_launches[B] : c->graph_launches[B];
-  if (!ge) {
-    cudaGraph_t g = nullptr;
-    int n = 0;
-    CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = record_step(c, B, &n, nullptr, verify);
-    cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
-    if (e != cudaSuccess || e2 != cudaSuccess) {
-      if (g) cudaGraphDestroy(g);
-      return fail(c, MAG_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
-    }
-    cudaError_t e3 = cudaGraphInstantiate(&ge, g, 0);
-    cudaGraphDestroy(g);
-    if (e3 != cudaSuccess) return fail(c, MAG_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e3));
-    n_launch = n;
-  }
-  CUDA_TRY(c, cudaGraphLaunch(ge, c->stream));
-  c->last_launches = n_launch;
+  mag_ctx::StepGraph& g = c->graphs[verify][c->cur_plan][B];
+  if (!g.exec) CUDA_TRY(c, capture_graph(c, verify, c->cur_plan, B, c->stream, g));
+  CUDA_TRY(c, cudaGraphLaunch(g.exec, c->stream));
+  c->last_launches = g.launches;
   return MAG_OK;
 }
 
 mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out) {
   if (!c) return MAG_ERR_INVALID_ARG;
-  mag_status st = step_upload(c, B, sids, in, out);
+  mag_status st = poll_capture(c);
+  if (st != MAG_OK) return st;
+  st = step_upload(c, B, sids, in, out);
   if (st != MAG_OK) return st;
   st = launch_step(c, B, false);
   if (st != MAG_OK) return st;
-  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
+  int32_t lens[MAG_MAX_BATCH];
+  for (int b = 0; b < B; ++b) lens[b] = ++c->sessions[sids[b]].len;
+  adapt_after_step(c, B, lens);
   return MAG_OK;
 }
 
@@ -1040,7 +1139,7 @@ mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, co
   if (st != MAG_OK) return st;
   Profiler prof;
   int n = 0;
-  CUDA_TRY(c, record_step(c, B, &n, &prof));
+  CUDA_TRY(c, record_step(c, B, &n, &prof, false, plan_splits(c, c->cur_plan, B), c->stream));
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   *n_out = (int32_t)prof.kinds.size();
@@ -1210,6 +1309,8 @@ mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in,
 // Verify step on the decode kernels: the n tokens are the n rows of a decode step of one session at
 // positions len .. len + n - 1, with their keys and values stored between the QKV projection and attention.
 static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void* in, void* out) {
+  mag_status st = poll_capture(c);
+  if (st != MAG_OK) return st;
   if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
     return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: session %d is not open", sid);
   if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "verify_tokens: not every weight is loaded");
@@ -1245,9 +1346,12 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
   CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
   CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
   c->ring_pos = (slot + 1) % kRing;
-  mag_status st = launch_step(c, n, true);
+  st = launch_step(c, n, true);
   if (st != MAG_OK) return st;
+  int32_t lens[MAG_MAX_BATCH];
+  for (int b = 0; b < n; ++b) lens[b] = s.len + b + 1;
   s.len += n;
+  adapt_after_step(c, n, lens);
   return MAG_OK;
 }
 
@@ -1279,6 +1383,94 @@ mag_status mag_session_truncate(mag_ctx* c, int32_t sid, int32_t length) {
     s.table.pop_back();
   }
   s.len = length;
+  return MAG_OK;
+}
+
+void mag_adapt_defaults(mag_adapt_config* a) {
+  if (!a) return;
+  *a = mag_adapt_config{};
+  a->enable_adaptive = 1;
+  a->adaptive_window_size = 64;
+  a->adaptive_sample_rate = 4;
+  a->plan_short_below = 128;
+  a->plan_long_above = 512;
+  // measured on GB300 (8B shape, one session): 4 splits are fastest below ~128 keys, 8 to ~300, 16 above
+  a->plan_splits[0] = 4;
+  a->plan_splits[1] = 8;
+  a->plan_splits[2] = 16;
+  a->force_plan = -1;
+  a->async_switch = 0;
+  a->hot_pool_slack = 1.2f;
+}
+
+mag_status mag_set_adaptive(mag_ctx* c, const mag_adapt_config* a) {
+  if (!c || !a) return MAG_ERR_INVALID_ARG;
+  if (a->enable_adaptive) {
+    if (a->adaptive_window_size < 1 || a->adaptive_sample_rate < 1)
+      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: window %d and sample rate %d must be >= 1",
+                  a->adaptive_window_size, a->adaptive_sample_rate);
+    if (a->plan_short_below > a->plan_long_above + 1)
+      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: short_below %d above long_above %d",
+                  a->plan_short_below, a->plan_long_above);
+    for (int i = 0; i < 3; ++i)
+      if (a->plan_splits[i] < 0 || a->plan_splits[i] > 16)
+        return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: plan %d splits %d not in 0..16", i, a->plan_splits[i]);
+    if (a->force_plan < -1 || a->force_plan > 2)
+      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: force_plan %d not in -1..2", a->force_plan);
+    if (!(a->hot_pool_slack >= 1.0f && a->hot_pool_slack <= 16.0f))
+      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: hot_pool_slack %g not in 1..16", a->hot_pool_slack);
+  }
+  mag_status st = finish_capture(c);
+  if (st != MAG_OK) return st;
+  if (a->enable_adaptive && a->async_switch && !c->cap_stream)
+    CUDA_TRY(c, cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+  // graphs captured under other split counts are dropped; the ones that stay valid are kept
+  mag_adapt_config next = a->enable_adaptive ? *a : mag_adapt_config{};
+  for (int p = 0; p < 3; ++p) {
+    for (int b = 1; b <= MAG_MAX_BATCH; ++b) {
+      const int s_old = plan_splits(c, p, b);
+      std::swap(c->adapt, next);
+      const int s_new = plan_splits(c, p, b);
+      std::swap(c->adapt, next);
+      if (s_old == s_new) continue;
+      for (int v = 0; v < 2; ++v) {
+        mag_ctx::StepGraph& g = c->graphs[v][p][b];
+        if (g.exec) {
+          CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+          CUDA_TRY(c, cudaGraphExecDestroy(g.exec));
+          g = mag_ctx::StepGraph{};
+        }
+      }
+    }
+  }
+  c->adapt = next;
+  c->profile.reset();
+  if (next.enable_adaptive)
+    c->profile = std::make_unique<LoadProfile>(next.adaptive_window_size, next.adaptive_sample_rate);
+  c->hot_blocks = -1;
+  if (next.enable_adaptive && next.force_plan >= 0) {
+    if (next.force_plan != c->cur_plan) ++c->switches;
+    c->cur_plan = next.force_plan;
+  }
+  if (!next.enable_adaptive) c->cur_plan = 1;
+  return MAG_OK;
+}
+
+mag_status mag_get_profile(mag_ctx* c, mag_profile* out) {
+  if (!c || !out) return MAG_ERR_INVALID_ARG;
+  mag_status st = poll_capture(c);
+  if (st != MAG_OK) return st;
+  *out = mag_profile{};
+  out->seen = c->profile ? c->profile->seen() : 0;
+  out->recorded = c->profile ? c->profile->count() : 0;
+  out->p50 = c->profile ? c->profile->quantile(0.5) : -1;
+  out->p90 = c->profile ? c->profile->quantile(0.9) : -1;
+  out->p99 = c->profile ? c->profile->quantile(0.99) : -1;
+  out->plan = c->cur_plan;
+  out->pending_plan = c->pending_plan;
+  out->plan_splits = plan_splits(c, c->cur_plan, 1);
+  out->switches = c->switches;
+  out->hot_blocks = c->hot_blocks;
   return MAG_OK;
 }
 
