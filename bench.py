@@ -546,6 +546,66 @@ def run_plans(args):
     ctx.close()
 
 
+def run_elastic(args):
+    """Measurement aid for the elastic KV pool: the 8B decode step (one FP16 session, context 2048) with a
+    fixed and with an elastic pool, and the elastic pool's own costs: an append that maps a new group
+    (one 2 MiB page per layer), and the close that gives groups back. Host wall times around synchronised
+    calls. Prints one JSON line and exits."""
+    import torch
+    import quantized_decode_step_gb300 as mag
+    from synth import driver
+    mag.build()
+    shape, ctx_len, steps = LLAMA8B, 2048, max(args.steps, 8)
+    L, H, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
+    res = {}
+    for name, flags in (("fixed", 0), ("elastic", mag.FLAG_ELASTIC_POOL)):
+        cfg = mag.make_config(shape, kv_dtype=KV_FP16, pool_blocks=4 * 8192 // 16, max_sessions=4, max_batch=1,
+                              max_context=8192, flags=flags)
+        stream = torch.cuda.current_stream()
+        ctx = mag.Context(cfg, stream.cuda_stream)
+        driver.load_weights(ctx, shape, args.seed)
+        sid = ctx.session_open()
+        driver.append_prior(ctx, sid, shape, args.seed, 0, ctx_len)
+        x = torch.zeros((1, shape.hidden), dtype=torch.float16, device="cuda")
+        out = torch.empty((1, shape.vocab), dtype=torch.float16, device="cuda")
+        for _ in range(args.warmup):
+            ctx.decode_step([sid], x, out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            ctx.decode_step([sid], x, out)
+        e1.record()
+        e1.synchronize()
+        r = {"ms_per_step": e0.elapsed_time(e1) / steps}
+        # appends of 2048 tokens into a second session: every 512 tokens need one more 32-block group
+        k = torch.zeros((L, 512, H, d), dtype=torch.float16, device="cuda")
+        sid2 = ctx.session_open()
+        times = []
+        for _ in range(4):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            ctx.kv_append(sid2, 512, k, k)
+            torch.cuda.synchronize()
+            times.append((time.perf_counter() - t0) * 1e3)
+        r["append_512_ms"] = [round(t, 3) for t in times]
+        st = ctx.memory_stats()
+        r["mapped_mb_before_close"] = st["kv_pool_mapped_bytes"] / 2**20
+        t0 = time.perf_counter()
+        ctx.session_close(sid2)
+        torch.cuda.synchronize()
+        ctx.session_close(ctx.session_open())  # the trim that unmaps what the stream has passed
+        r["close_and_release_ms"] = round((time.perf_counter() - t0) * 1e3, 3)
+        r["mapped_mb_after_close"] = ctx.memory_stats()["kv_pool_mapped_bytes"] / 2**20
+        r["group_blocks"] = st["pool_group_blocks"]
+        res[name] = r
+        ctx.close()
+        del k
+        torch.cuda.empty_cache()
+    print(json.dumps({"elastic_pool": res, "workload": "8b decode, 1 FP16 session, context 2048; appends of "
+                      "512 tokens (one 32-block group each) into a second session", "steps": steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -560,12 +620,17 @@ def main():
                     help="profiling aid: launch the step's kernels one by one instead of replaying a CUDA graph")
     ap.add_argument("--plans", action="store_true",
                     help="measurement aid: decode step time per attention split count and context, then exit")
+    ap.add_argument("--elastic", action="store_true",
+                    help="measurement aid: decode step and map / release costs of the elastic KV pool, then exit")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: the same per-layer shapes with fewer layers (not a bench configuration)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.plans:
         run_plans(args)
+        return
+    if args.elastic:
+        run_elastic(args)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -57,6 +57,13 @@ typedef enum { MAG_KV_FP16 = 0, MAG_KV_INT8 = 1, MAG_KV_INT4 = 2 } mag_kv_dtype;
 #define MAG_FLAG_NO_GRAPH ((uint64_t)1)        /* launch kernels one by one instead of replaying a CUDA graph */
 #define MAG_FLAG_ARENA_NO_REUSE ((uint64_t)2)  /* give every arena tensor its own bytes ([TFLite] 3.2 preserve-all) */
 #define MAG_FLAG_NO_PDL ((uint64_t)4)          /* no programmatic dependent launch between kernels */
+/* Elastic KV pool ([Magnitude] 2.2 layer 1, 3.2 hot / cold pool): pool_blocks becomes a reserved virtual
+ * range (rounded up to whole mapping groups); device memory is mapped a group at a time (zeroed), the
+ * lowest groups up to the hot size stay mapped, a group above it is mapped when the free blocks run out
+ * and returned to the device once wholly free (after the stream has passed its last use). The hot size
+ * is one group, or, with the adaptive runtime on, hot_pool_slack x the P90 need (mag_set_adaptive).
+ * Free blocks go out lowest id first. pool_order_host must be NULL. */
+#define MAG_FLAG_ELASTIC_POOL ((uint64_t)8)
 
 /* Model shape and capacities ([Core] 5.1: the shape travels with the model;
  * [Core] 5.2: everything sized once, up front; [Magnitude] 4.3: EngineConfig). */
@@ -235,6 +242,12 @@ typedef struct mag_memory_stats {
   int32_t sessions_open;
   uint64_t prefill_weight_bytes; /* exact two-term fp16 weight copies of the prefill GEMM (max_chunk > 0) */
   uint64_t prefill_arena_bytes;  /* planned prefill activation arena (max_chunk rows) */
+  /* KV pool memory: a fixed pool has it all mapped; an elastic one (MAG_FLAG_ELASTIC_POOL) maps groups of
+   * pool_group_blocks blocks: the hot ones (pool_blocks_hot) stay, others come and go with demand */
+  uint64_t kv_pool_mapped_bytes;
+  int32_t pool_blocks_mapped;
+  int32_t pool_blocks_hot;
+  int32_t pool_group_blocks;
 } mag_memory_stats;
 
 /* [Magnitude] 5.2 get_memory_stats: weights, pool, arena. */

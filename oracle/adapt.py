@@ -65,3 +65,67 @@ def hot_pool_blocks(p90: int, n_sessions: int, slack="1.2", block_tokens: int = 
         return 0
     x = n_sessions * -(-p90 // block_tokens)
     return math.ceil(Fraction(str(slack)) * x)
+
+
+class ElasticPoolModel:
+    """3.2 (hot / cold pool) and 2.2 layer 1 (grow on demand, give idle memory back) on a block pool:
+    groups of G blocks; the lowest `hot` groups stay mapped; another group is mapped when the free
+    blocks run out (the lowest group not mapped) and unmapped once none of its blocks is in use; free
+    blocks go out lowest id first. Reading: the group is the unit of mapping (whole pages per layer),
+    the hot pool is at least one group."""
+
+    def __init__(self, n_blocks: int, group_blocks: int):
+        self.G = group_blocks
+        self.n_groups = -(-n_blocks // group_blocks)
+        self.P = self.n_groups * group_blocks
+        self.hot = 1
+        self.mapped: set[int] = set()
+        self.free: set[int] = set()
+        self.used = [0] * self.n_groups
+        self._map(0)
+
+    def _map(self, g):
+        self.mapped.add(g)
+        self.free.update(range(g * self.G, (g + 1) * self.G))
+
+    def _unmap(self, g):
+        self.mapped.discard(g)
+        self.free.difference_update(range(g * self.G, (g + 1) * self.G))
+
+    def available(self) -> int:
+        return len(self.free) + self.G * (self.n_groups - len(self.mapped))
+
+    def alloc(self, n: int):
+        """n blocks, or None (and no change) when the pool can not hold them."""
+        if n > self.available():
+            return None
+        g = 0
+        while len(self.free) < n:
+            if g not in self.mapped:
+                self._map(g)
+            g += 1
+        out = []
+        for _ in range(n):
+            b = min(self.free)
+            self.free.remove(b)
+            self.used[b // self.G] += 1
+            out.append(b)
+        return out
+
+    def release(self, blocks):
+        for b in blocks:
+            self.used[b // self.G] -= 1
+            self.free.add(b)
+        self.trim()
+
+    def trim(self):
+        for g in sorted(self.mapped):
+            if g >= self.hot and self.used[g] == 0:
+                self._unmap(g)
+
+    def set_hot(self, blocks: int):
+        self.hot = min(max(-(-blocks // self.G), 1), self.n_groups)
+        for g in range(self.hot):
+            if g not in self.mapped:
+                self._map(g)
+        self.trim()

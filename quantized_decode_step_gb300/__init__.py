@@ -22,7 +22,7 @@ STATUS_NAMES = ["OK", "INVALID_ARG", "OOM", "KV_FULL", "CONTEXT_FULL", "NOT_LOAD
 KV_FP16, KV_INT8, KV_INT4 = 0, 1, 2
 W_QKV, W_O, W_GATE_UP, W_DOWN, NORM_ATTN, NORM_FFN, NORM_FINAL, LM_HEAD = range(8)
 FMT_F32_DENSE, FMT_W4G32, FMT_F16 = 0, 1, 2
-FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL = 1, 2, 4
+FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL, FLAG_ELASTIC_POOL = 1, 2, 4, 8
 
 EXPORTED = [
     "mag_create", "mag_destroy", "mag_load_weights", "mag_load_weights_f32_noalloc", "mag_session_open", "mag_session_close", "mag_session_length",
@@ -59,7 +59,9 @@ class MemoryStats(ctypes.Structure):
                 ("pool_blocks_free", ctypes.c_int32), ("arena_bytes", ctypes.c_uint64),
                 ("arena_unshared_bytes", ctypes.c_uint64), ("other_device_bytes", ctypes.c_uint64),
                 ("sessions_open", ctypes.c_int32), ("prefill_weight_bytes", ctypes.c_uint64),
-                ("prefill_arena_bytes", ctypes.c_uint64)]
+                ("prefill_arena_bytes", ctypes.c_uint64), ("kv_pool_mapped_bytes", ctypes.c_uint64),
+                ("pool_blocks_mapped", ctypes.c_int32), ("pool_blocks_hot", ctypes.c_int32),
+                ("pool_group_blocks", ctypes.c_int32)]
 
 
 class ArenaTensor(ctypes.Structure):

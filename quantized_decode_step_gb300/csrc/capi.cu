@@ -16,6 +16,7 @@
 #include "adapt.h"
 #include "arena.h"
 #include "kernels.h"
+#include "kvpool.h"
 #include "noalloc.h"
 #include "mag.h"
 
@@ -92,11 +93,9 @@ struct mag_ctx {
   std::vector<uint8_t> loaded;  // [L][6] + final norm + lm head
 
   // KV pool
-  uint8_t* pool = nullptr;
-  size_t pool_bytes = 0;
+  KvPool kv;  // memory and free list (fixed, or elastic hot / cold groups)
   int64_t block_bytes = 0;
   int data_bytes = 0, meta_bytes = 0;
-  std::deque<int32_t> free_list;
   int32_t* d_tables = nullptr;
   std::vector<Session> sessions;
 
@@ -243,7 +242,7 @@ int64_t kv_meta_bytes(int d, int dt) { return dt == 0 ? 0 : (dt == 1 ? 2 : (d / 
 
 PoolGeom pool_geom(const mag_ctx* c) {
   PoolGeom g;
-  g.base = c->pool;
+  g.base = c->kv.base();
   g.block_bytes = c->block_bytes;
   g.pool_blocks = c->cfg.pool_blocks;
   g.data_bytes = c->data_bytes;
@@ -254,6 +253,32 @@ PoolGeom pool_geom(const mag_ctx* c) {
   g.tables = c->d_tables;
   g.table_stride = c->table_stride;
   return g;
+}
+
+// Make n pool blocks free and mapped; an error leaves the context unchanged.
+mag_status reserve_blocks(mag_ctx* c, const char* what, int64_t n) {
+  const mag_status st = c->kv.reserve(n, c->stream);
+  if (st == MAG_ERR_KV_FULL)
+    return fail(c, st, "%s: needs %lld blocks, %lld free", what, (long long)n, (long long)c->kv.available());
+  if (st != MAG_OK) return fail(c, st, "%s: %s", what, c->kv.err.c_str());
+  return MAG_OK;
+}
+
+// Whether an open session lists a block of group g of an elastic pool (checked before the group's release).
+bool group_referenced(const mag_ctx* c, int64_t g) {
+  const int64_t G = c->kv.group_blocks();
+  for (const Session& s : c->sessions)
+    if (s.open)
+      for (int32_t b : s.table)
+        if (b / G == g) return true;
+  return false;
+}
+
+// Elastic pool: release free groups above the hot size, unmap released ones the stream has passed.
+mag_status pool_trim(mag_ctx* c) {
+  if (!c->kv.elastic()) return MAG_OK;
+  const mag_status st = c->kv.trim(c->stream, [c](int64_t g) { return group_referenced(c, g); });
+  return st == MAG_OK ? st : fail(c, st, "%s", c->kv.err.c_str());
 }
 
 bool all_loaded(const mag_ctx* c) {
@@ -471,7 +496,6 @@ void free_ctx(mag_ctx* c) {
   for (auto& e : c->ring_ev)
     if (e) cudaEventDestroy(e);
   cudaFree(c->wbase);
-  cudaFree(c->pool);
   cudaFree(c->d_tables);
   cudaFree(c->d_cos);
   cudaFree(c->d_sin);
@@ -642,9 +666,13 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     }
     c->own_stream = true;
   }
-  // pool order
+  // pool order (a fixed pool only: an elastic one hands out the lowest free block)
   const int P = cfg->pool_blocks;
   if (cfg->pool_order_host) {
+    if (cfg->flags & MAG_FLAG_ELASTIC_POOL) {
+      fail(c, MAG_ERR_INVALID_ARG, "pool_order_host is not used with MAG_FLAG_ELASTIC_POOL");
+      return bail(MAG_ERR_INVALID_ARG);
+    }
     std::vector<char> seen(P, 0);
     for (int i = 0; i < P; ++i) {
       int b = cfg->pool_order_host[i];
@@ -653,10 +681,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
         return bail(MAG_ERR_INVALID_ARG);
       }
       seen[b] = 1;
-      c->free_list.push_back(b);
     }
-  } else {
-    for (int i = 0; i < P; ++i) c->free_list.push_back(i);
   }
   c->sessions.resize(cfg->max_sessions);
   c->loaded.assign((size_t)c->L * 6 + 2, 0);
@@ -707,12 +732,16 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   c->data_bytes = (int)kv_data_bytes(c->d, cfg->kv_dtype);
   c->meta_bytes = (int)kv_meta_bytes(c->d, cfg->kv_dtype);
   c->block_bytes = 2 * (int64_t)c->Hkv * 16 * (c->data_bytes + c->meta_bytes);
-  c->pool_bytes = (size_t)c->L * P * c->block_bytes;
-  if ((e = cudaMalloc(&c->pool, c->pool_bytes)) != cudaSuccess) {
-    fail(c, MAG_ERR_OOM, "KV pool: cudaMalloc(%zu): %s", c->pool_bytes, cudaGetErrorString(e));
-    return bail(MAG_ERR_OOM);
+  {
+    const mag_status st = (cfg->flags & MAG_FLAG_ELASTIC_POOL)
+                              ? c->kv.init_elastic(c->L, P, c->block_bytes, c->device, c->stream)
+                              : c->kv.init_fixed(c->L, P, c->block_bytes, cfg->pool_order_host, c->stream);
+    if (st != MAG_OK) {
+      fail(c, st, "%s", c->kv.err.c_str());
+      return bail(st);
+    }
+    c->cfg.pool_blocks = (int32_t)c->kv.blocks();  // elastic: rounded up to whole mapping groups
   }
-  cudaMemsetAsync(c->pool, 0, c->pool_bytes, c->stream);
   size_t tb = (size_t)cfg->max_sessions * c->table_stride * 4;
   if ((e = cudaMalloc(&c->d_tables, tb)) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "block tables: %s", cudaGetErrorString(e));
@@ -900,9 +929,9 @@ mag_status mag_session_close(mag_ctx* c, int32_t sid) {
   if (!c) return MAG_ERR_INVALID_ARG;
   if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
     return fail(c, MAG_ERR_INVALID_ARG, "session_close: session %d is not open", sid);
-  for (int32_t b : c->sessions[sid].table) c->free_list.push_back(b);
+  for (int32_t b : c->sessions[sid].table) c->kv.push(b);
   c->sessions[sid] = Session();
-  return MAG_OK;
+  return pool_trim(c);
 }
 
 mag_status mag_session_length(mag_ctx* c, int32_t sid, int32_t* len) {
@@ -923,13 +952,10 @@ mag_status mag_kv_append(mag_ctx* c, int32_t sid, int32_t n, const void* k, cons
     return fail(c, MAG_ERR_CONTEXT_FULL, "kv_append: %d + %d tokens exceed max_context %d", s.len, n,
                 c->cfg.max_context);
   const int nb_old = (s.len + 15) / 16, nb_new = (s.len + n + 15) / 16;
-  if (nb_new - nb_old > (int)c->free_list.size())
-    return fail(c, MAG_ERR_KV_FULL, "kv_append: needs %d blocks, %zu free", nb_new - nb_old, c->free_list.size());
   if (n == 0) return MAG_OK;
-  for (int i = nb_old; i < nb_new; ++i) {
-    s.table.push_back(c->free_list.front());
-    c->free_list.pop_front();
-  }
+  mag_status st = reserve_blocks(c, "kv_append", nb_new - nb_old);
+  if (st != MAG_OK) return st;
+  for (int i = nb_old; i < nb_new; ++i) s.table.push_back(c->kv.pop());
   int32_t* row = c->d_tables + (size_t)sid * c->table_stride;
   if (nb_new > nb_old)
     CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
@@ -955,7 +981,7 @@ mag_status mag_kv_append(mag_ctx* c, int32_t sid, int32_t n, const void* k, cons
       bl.k = a.k + ((size_t)l * n + t0) * c->Hkv * c->d;
       bl.v = a.v + ((size_t)l * n + t0) * c->Hkv * c->d;
       bl.n_layers = 1;
-      bl.pool.base = c->pool + (size_t)l * c->cfg.pool_blocks * c->block_bytes;
+      bl.pool.base = c->kv.base() + (size_t)l * c->cfg.pool_blocks * c->block_bytes;
       CUDA_TRY(c, launch_kv_store(L, bl));
     }
   }
@@ -978,8 +1004,8 @@ static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs&
       return fail(c, MAG_ERR_CONTEXT_FULL, "decode_step: session %d is at max_context", s);
     if (c->sessions[s].len % 16 == 0) ++need;
   }
-  if (need > (int)c->free_list.size())
-    return fail(c, MAG_ERR_KV_FULL, "decode_step: needs %d blocks, %zu free", need, c->free_list.size());
+  mag_status st = reserve_blocks(c, "decode_step", need);
+  if (st != MAG_OK) return st;
   a.batch = B;
   a.n_upd = 0;
   for (int b = 0; b < B; ++b) {
@@ -987,8 +1013,7 @@ static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs&
     a.sess[b] = sids[b];
     a.pos[b] = s.len;
     if (s.len % 16 == 0) {
-      int blk = c->free_list.front();
-      c->free_list.pop_front();
+      int blk = c->kv.pop();
       s.table.push_back(blk);
       a.upd_sess[a.n_upd] = sids[b];
       a.upd_idx[a.n_upd] = s.len / 16;
@@ -1096,6 +1121,9 @@ static void adapt_after_step(mag_ctx* c, int B, const int32_t* lens) {
   int open = 0;
   for (const Session& s : c->sessions) open += s.open;
   c->hot_blocks = hot_pool_blocks(p90, open, c->adapt.hot_pool_slack, 16);
+  if (c->kv.elastic() &&
+      c->kv.set_hot(c->hot_blocks, c->stream, [c](int64_t g) { return group_referenced(c, g); }) != MAG_OK)
+    fail(c, MAG_ERR_OOM, "hot pool resize (kept the old size): %s", c->kv.err.c_str());
   if (c->adapt.force_plan >= 0 || c->pending_plan >= 0) return;
   const int want = plan_for(p90, c->adapt.plan_short_below, c->adapt.plan_long_above);
   if (want != c->cur_plan) switch_plan(c, want);
@@ -1129,7 +1157,7 @@ mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const voi
   int32_t lens[MAG_MAX_BATCH];
   for (int b = 0; b < B; ++b) lens[b] = ++c->sessions[sids[b]].len;
   adapt_after_step(c, B, lens);
-  return MAG_OK;
+  return pool_trim(c);
 }
 
 mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out,
@@ -1183,8 +1211,8 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
     return fail(c, MAG_ERR_CONTEXT_FULL, "%s: %d + %d tokens exceed max_context %d", what, s.len, T,
                 c->cfg.max_context);
   const int nb_old = (s.len + 15) / 16, nb_new = (s.len + T + 15) / 16;
-  if (nb_new - nb_old > (int)c->free_list.size())
-    return fail(c, MAG_ERR_KV_FULL, "%s: needs %d blocks, %zu free", what, nb_new - nb_old, c->free_list.size());
+  mag_status rs = reserve_blocks(c, what, nb_new - nb_old);
+  if (rs != MAG_OK) return rs;
   // step arguments of the output rows' LM head (or final hidden state)
   const int slot = c->ring_pos;
   CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
@@ -1196,10 +1224,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
     sa.pos[b] = s.len + T - out_rows + b;
   }
   sa.out = out;
-  for (int i = nb_old; i < nb_new; ++i) {
-    s.table.push_back(c->free_list.front());
-    c->free_list.pop_front();
-  }
+  for (int i = nb_old; i < nb_new; ++i) s.table.push_back(c->kv.pop());
   int32_t* row = c->d_tables + (size_t)sid * c->table_stride;
   if (nb_new > nb_old)
     CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
@@ -1320,9 +1345,8 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
                 c->cfg.max_context);
   // n <= 16 tokens reach at most one block past the session's last one
   const int nb_old = (s.len + 15) / 16, nb_new = (s.len + n + 15) / 16;
-  if (nb_new - nb_old > (int)c->free_list.size())
-    return fail(c, MAG_ERR_KV_FULL, "verify_tokens: needs %d blocks, %zu free", nb_new - nb_old,
-                c->free_list.size());
+  st = reserve_blocks(c, "verify_tokens", nb_new - nb_old);
+  if (st != MAG_OK) return st;
   const int slot = c->ring_pos;
   CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
   StepArgs& a = c->h_ring[slot];
@@ -1333,8 +1357,7 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
     a.pos[b] = s.len + b;
   }
   for (int i = nb_old; i < nb_new; ++i) {
-    const int blk = c->free_list.front();
-    c->free_list.pop_front();
+    const int blk = c->kv.pop();
     s.table.push_back(blk);
     a.upd_sess[a.n_upd] = sid;
     a.upd_idx[a.n_upd] = i;
@@ -1352,7 +1375,7 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
   for (int b = 0; b < n; ++b) lens[b] = s.len + b + 1;
   s.len += n;
   adapt_after_step(c, n, lens);
-  return MAG_OK;
+  return pool_trim(c);
 }
 
 mag_status mag_verify_tokens(mag_ctx* c, int32_t sid, int32_t n_tokens, const void* hidden_in, void* out) {
@@ -1379,11 +1402,11 @@ mag_status mag_session_truncate(mag_ctx* c, int32_t sid, int32_t length) {
   // the length, which nothing reads, and a later append writes the new ids before they are used
   const size_t nb = (size_t)(length + 15) / 16;
   while (s.table.size() > nb) {
-    c->free_list.push_back(s.table.back());
+    c->kv.push(s.table.back());
     s.table.pop_back();
   }
   s.len = length;
-  return MAG_OK;
+  return pool_trim(c);
 }
 
 void mag_adapt_defaults(mag_adapt_config* a) {
@@ -1484,10 +1507,14 @@ mag_status mag_get_memory_stats(mag_ctx* c, mag_memory_stats* s) {
   if (!c || !s) return MAG_ERR_INVALID_ARG;
   memset(s, 0, sizeof *s);
   s->weight_bytes = c->wbytes;
-  s->kv_pool_bytes = c->pool_bytes;
+  s->kv_pool_bytes = c->kv.reserved_bytes();
   s->kv_block_bytes = c->block_bytes;
   s->pool_blocks_total = c->cfg.pool_blocks;
-  s->pool_blocks_free = (int32_t)c->free_list.size();
+  s->pool_blocks_free = (int32_t)c->kv.available();
+  s->kv_pool_mapped_bytes = c->kv.mapped_bytes();
+  s->pool_blocks_mapped = (int32_t)c->kv.mapped_blocks();
+  s->pool_blocks_hot = (int32_t)c->kv.hot_blocks();
+  s->pool_group_blocks = (int32_t)c->kv.group_blocks();
   s->arena_bytes = c->arena_bytes;
   s->arena_unshared_bytes = c->arena_unshared;
   s->other_device_bytes = c->other_bytes;
@@ -1531,8 +1558,8 @@ mag_status mag_debug_kv_locate(mag_ctx* c, int32_t sid, int32_t layer, int32_t t
 
 mag_status mag_debug_pool(mag_ctx* c, void** p, uint64_t* bytes) {
   if (!c || !p || !bytes) return MAG_ERR_INVALID_ARG;
-  *p = c->pool;
-  *bytes = c->pool_bytes;
+  *p = c->kv.base();
+  *bytes = c->kv.reserved_bytes();
   return MAG_OK;
 }
 

@@ -133,3 +133,41 @@ def test_library_policies_match_oracle(lib):
             for slack in ("1.0", "1.05", "1.1", "1.15", "1.2", "2.5"):
                 assert mag.hot_pool_blocks(p90, n, float(slack)) == adapt.hot_pool_blocks(p90, n, slack), \
                     (p90, n, slack)
+
+
+# ---------------------------------------------------------------- elastic pool model
+def test_elastic_model_hand_case():
+    # 600 blocks in groups of 256 -> 768; sessions of 188, 1 and 125 blocks fill group 0 and start group 1
+    m = adapt.ElasticPoolModel(600, 256)
+    assert (m.P, m.available(), sorted(m.mapped)) == (768, 768, [0])
+    a, c, b = m.alloc(188), m.alloc(1), m.alloc(125)
+    assert (a[0], a[-1], c, b[0], b[-1]) == (0, 187, [188], 189, 313)
+    assert sorted(m.mapped) == [0, 1]
+    m.release(b)  # group 1 wholly free again: given back
+    assert sorted(m.mapped) == [0] and m.available() == 768 - 189
+    assert m.alloc(1000) is None and sorted(m.mapped) == [0]
+
+
+def test_elastic_model_invariants_random():
+    rng = random.Random(5)
+    for G, n in ((4, 37), (16, 100), (256, 600)):
+        m = adapt.ElasticPoolModel(n, G)
+        held = []
+        for _ in range(2000):
+            op = rng.random()
+            if op < 0.45:
+                got = m.alloc(rng.randrange(1, 3 * G))
+                if got is not None:
+                    held.append(got)
+            elif op < 0.85 and held:
+                m.release(held.pop(rng.randrange(len(held))))
+            else:
+                m.set_hot(rng.randrange(0, m.P + 1))
+            in_use = [b for h in held for b in h]
+            assert len(in_use) == len(set(in_use))  # no block handed out twice
+            assert not (set(in_use) & m.free)
+            assert all(b // G in m.mapped for b in in_use)  # every block in use is mapped
+            # mapped = the hot groups and the groups with a block in use, nothing else
+            assert m.mapped == set(range(m.hot)) | {b // G for b in in_use}
+            assert m.free == {b for g in m.mapped for b in range(g * G, (g + 1) * G)} - set(in_use)
+            assert m.available() == m.P - len(in_use)
