@@ -493,6 +493,37 @@ def run_prefill(args, tc_peak):
     ev1.record(stream)
     ev1.synchronize()
     s_verify = ev0.elapsed_time(ev1) / 1e3 / v_runs
+    # batch leg: four sessions of the prior cache take 128 tokens each, in one mag_prefill_batch call and
+    # as four mag_prefill_chunk calls (the same 512 rows); sessions are truncated back after every call
+    n_b, t_b = 4, T // 4
+    bsids = sids[1:1 + n_b]
+    for sid in bsids:
+        ctx.session_truncate(sid, p)
+    with torch.cuda.stream(stream):
+        xb = torch.from_numpy(hidden_f16(args.seed, n_b * t_b, shape.hidden, tag="batch")).cuda()
+        ob = torch.empty((n_b, shape.vocab or shape.hidden), dtype=torch.float16, device="cuda")
+
+    def one_batch():
+        ctx.prefill_batch(bsids, [t_b] * n_b, xb, ob)
+        for sid in bsids:
+            ctx.session_truncate(sid, p)
+
+    def four_chunks():
+        for i, sid in enumerate(bsids):
+            ctx.prefill_chunk(sid, t_b, xb[i * t_b:(i + 1) * t_b], ob[i])
+        for sid in bsids:
+            ctx.session_truncate(sid, p)
+
+    legs = {}
+    for name, fn in (("one_call", one_batch), ("separate_calls", four_chunks)):
+        fn()
+        stream.synchronize()
+        ev0.record(stream)
+        for _ in range(runs):
+            fn()
+        ev1.record(stream)
+        ev1.synchronize()
+        legs[name] = ev0.elapsed_time(ev1) / runs
     fl = prefill_flops(shape, p, T)
     st = ctx.memory_stats()
     ctx.close()
@@ -506,6 +537,8 @@ def run_prefill(args, tc_peak):
             "launches_per_chunk": launches, "prefill_weight_bytes": st["prefill_weight_bytes"],
             "verify": {"drafts": n_draft, "context": base_len, "ms_per_call": s_verify * 1e3,
                        "tokens_per_s": n_draft / s_verify, "launches_per_call": v_launches},
+            "batch": {"sessions": n_b, "tokens_each": t_b, "prior": p, "ms_one_call": legs["one_call"],
+                      "ms_separate_calls": legs["separate_calls"]},
             "setup_s": t_setup}
 
 

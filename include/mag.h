@@ -212,6 +212,17 @@ mag_status mag_decode_step_host(mag_ctx* ctx, int32_t batch, const int32_t* sess
 mag_status mag_prefill_chunk(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
                              void* last_out_dev);
 
+/* Chunked prefill of several sessions in one pass (the batched form of mag_prefill_chunk): session
+ * session_ids_host[i] appends n_tokens_host[i] >= 1 tokens at its next positions; the sessions' rows
+ * follow each other in hidden_in_dev (fp16 [sum n_tokens][D], session 0's first), the total at most
+ * max_chunk, 1..16 distinct sessions. Each session's tokens attend causally to its own cache and to
+ * its own earlier tokens of the chunk; the projections run once over all rows. last_out_dev receives
+ * the fp16 output of every session's last token, [n_sessions][V] (or [n_sessions][D] when
+ * vocab == 0), in the order given. Errors: as mag_prefill_chunk, and INVALID_ARG for a repeated
+ * session; nothing is appended on error. */
+mag_status mag_prefill_batch(mag_ctx* ctx, int32_t n_sessions, const int32_t* session_ids_host,
+                             const int32_t* n_tokens_host, const void* hidden_in_dev, void* last_out_dev);
+
 /* Multi-token verify step (draft tokens of speculative decoding checked in
  * one pass, [Core] 5.6): n_tokens tokens of one session at its next
  * positions, writing the fp16 output of every token, out_dev[n_tokens][V] (or

@@ -27,7 +27,7 @@ FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL, FLAG_ELASTIC_POOL = 1, 2, 4, 8
 EXPORTED = [
     "mag_create", "mag_destroy", "mag_load_weights", "mag_load_weights_f32_noalloc", "mag_session_open", "mag_session_close", "mag_session_length",
     "mag_session_truncate", "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk",
-    "mag_verify_tokens", "mag_sync",
+    "mag_verify_tokens", "mag_prefill_batch", "mag_sync",
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
     "mag_debug_last_step_launches", "mag_debug_profile_step",
@@ -113,6 +113,7 @@ def lib():
                 "mag_decode_step_host": ([vp, i32, P32, vp, vp], i32),
                 "mag_prefill_chunk": ([vp, i32, i32, vp, vp], i32),
                 "mag_verify_tokens": ([vp, i32, i32, vp, vp], i32),
+                "mag_prefill_batch": ([vp, i32, P32, P32, vp, vp], i32),
                 "mag_sync": ([vp], i32),
                 "mag_get_memory_stats": ([vp, ctypes.POINTER(MemoryStats)], i32),
                 "mag_last_error": ([vp], ctypes.c_char_p),
@@ -296,6 +297,12 @@ class Context:
     def prefill_chunk(self, sid, n_tokens, hidden_in, last_out):
         self._check(lib().mag_prefill_chunk(self.h, sid, n_tokens, _ptr(hidden_in), _ptr(last_out)),
                     "mag_prefill_chunk")
+
+    def prefill_batch(self, sessions, n_tokens, hidden_in, last_out):
+        ids = (ctypes.c_int32 * len(sessions))(*sessions)
+        nt = (ctypes.c_int32 * len(n_tokens))(*n_tokens)
+        self._check(lib().mag_prefill_batch(self.h, len(sessions), ids, nt, _ptr(hidden_in), _ptr(last_out)),
+                    "mag_prefill_batch")
 
     def verify_tokens(self, sid, n_tokens, hidden_in, out):
         self._check(lib().mag_verify_tokens(self.h, sid, n_tokens, _ptr(hidden_in), _ptr(out)), "mag_verify_tokens")

@@ -167,6 +167,8 @@ struct mag_ctx {
   __half* pf_qkv = nullptr;
   __half* pf_o = nullptr;
   __half* pf_act = nullptr;
+  int32_t* pf_rows = nullptr;   // [2][max_chunk]: position and session of every row (several sessions)
+  float* pf_last_r = nullptr;   // [MAG_MAX_BATCH][D]: the sessions' last residual rows, gathered
   alignas(64) uint8_t map_xn[128];
   alignas(64) uint8_t map_o[128];
   alignas(64) uint8_t map_act[128];
@@ -508,6 +510,8 @@ void free_ctx(mag_ctx* c) {
   if (c->h_err) cudaFreeHost(c->h_err);
   cudaFree(c->pf_w);
   cudaFree(c->pf_arena);
+  cudaFree(c->pf_rows);
+  cudaFree(c->pf_last_r);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   delete c;
 }
@@ -602,6 +606,11 @@ mag_status setup_prefill(mag_ctx* c) {
   if (!make_tmap_2d(c->map_xn, c->pf_xn, T, c->D) || !make_tmap_2d(c->map_o, c->pf_o, T, (int64_t)c->Hq * c->d) ||
       !make_tmap_2d(c->map_act, c->pf_act, T, c->F))
     return fail(c, MAG_ERR_CUDA, "prefill: activation tensor maps");
+  // several sessions in one chunk: per-row positions and sessions, and the gathered last rows
+  if ((e = cudaMalloc(&c->pf_rows, (size_t)2 * T * 4)) != cudaSuccess ||
+      (e = cudaMalloc(&c->pf_last_r, (size_t)MAG_MAX_BATCH * c->D * 4)) != cudaSuccess)
+    return fail(c, MAG_ERR_OOM, "prefill row tables: %s", cudaGetErrorString(e));
+  c->other_bytes += (size_t)2 * T * 4 + (size_t)MAG_MAX_BATCH * c->D * 4;
   return MAG_OK;
 }
 
@@ -1197,21 +1206,39 @@ namespace {
 // The chunk path of mag_prefill_chunk and mag_verify_tokens: T tokens of one session through every layer
 // (their k and v appended to the pool), then the final RMSNorm + LM head (or the final hidden state) of the
 // last out_rows tokens into out [out_rows][V or D].
-mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const void* in, void* out, int out_rows) {
+// One prefill chunk of n_seg sessions: session sids[i] appends ntok[i] tokens, the rows of the sessions
+// following each other in `in` ([sum ntok][D]); each session's tokens attend causally to its own cache.
+// Output: with all_rows (one session), every row; otherwise the last row of every session, in order.
+mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sids, const int32_t* ntok,
+                     const void* in, void* out, bool all_rows) {
   if (!c) return MAG_ERR_INVALID_ARG;
   if (c->cfg.max_chunk <= 0) return fail(c, MAG_ERR_UNSUPPORTED, "%s: created with max_chunk = 0", what);
-  if (!in || !out) return fail(c, MAG_ERR_INVALID_ARG, "%s: null buffer", what);
-  if (T < 1 || T > c->cfg.max_chunk)
-    return fail(c, MAG_ERR_INVALID_ARG, "%s: %d tokens not in 1..%d", what, T, c->cfg.max_chunk);
-  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
-    return fail(c, MAG_ERR_INVALID_ARG, "%s: session %d is not open", what, sid);
+  if (!in || !out || !sids || !ntok) return fail(c, MAG_ERR_INVALID_ARG, "%s: null buffer", what);
+  if (n_seg < 1 || n_seg > MAG_MAX_BATCH)
+    return fail(c, MAG_ERR_INVALID_ARG, "%s: %d sessions not in 1..%d", what, n_seg, MAG_MAX_BATCH);
   if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "%s: not every weight is loaded", what);
-  Session& s = c->sessions[sid];
-  if ((int64_t)s.len + T > c->cfg.max_context)
-    return fail(c, MAG_ERR_CONTEXT_FULL, "%s: %d + %d tokens exceed max_context %d", what, s.len, T,
-                c->cfg.max_context);
-  const int nb_old = (s.len + 15) / 16, nb_new = (s.len + T + 15) / 16;
-  mag_status rs = reserve_blocks(c, what, nb_new - nb_old);
+  int T = 0, need = 0;
+  for (int i = 0; i < n_seg; ++i) {
+    const int sid = sids[i];
+    if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+      return fail(c, MAG_ERR_INVALID_ARG, "%s: session %d is not open", what, sid);
+    for (int j = 0; j < i; ++j)
+      if (sids[j] == sid) return fail(c, MAG_ERR_INVALID_ARG, "%s: session %d appears twice", what, sid);
+    if (ntok[i] < 1 || ntok[i] > c->cfg.max_chunk - T)
+      return fail(c, MAG_ERR_INVALID_ARG, "%s: %d + %d tokens exceed max_chunk %d", what, T, ntok[i],
+                  c->cfg.max_chunk);
+    const Session& s = c->sessions[sid];
+    if ((int64_t)s.len + ntok[i] > c->cfg.max_context)
+      return fail(c, MAG_ERR_CONTEXT_FULL, "%s: %d + %d tokens exceed max_context %d", what, s.len, ntok[i],
+                  c->cfg.max_context);
+    T += ntok[i];
+    need += (s.len + ntok[i] + 15) / 16 - (s.len + 15) / 16;
+  }
+  const int out_rows = all_rows ? T : n_seg;
+  if (all_rows && (n_seg != 1 || T > kPipeMaxBatch))
+    return fail(c, MAG_ERR_INVALID_ARG, "%s: every row's output needs one session of 1..%d tokens", what,
+                kPipeMaxBatch);
+  mag_status rs = reserve_blocks(c, what, need);
   if (rs != MAG_OK) return rs;
   // step arguments of the output rows' LM head (or final hidden state)
   const int slot = c->ring_pos;
@@ -1219,24 +1246,47 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
   StepArgs& sa = c->h_ring[slot];
   memset(&sa, 0, sizeof sa);
   sa.batch = out_rows;
-  for (int b = 0; b < out_rows; ++b) {
-    sa.sess[b] = sid;
-    sa.pos[b] = s.len + T - out_rows + b;
-  }
   sa.out = out;
-  for (int i = nb_old; i < nb_new; ++i) s.table.push_back(c->kv.pop());
-  int32_t* row = c->d_tables + (size_t)sid * c->table_stride;
-  if (nb_new > nb_old)
-    CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
-                                cudaMemcpyHostToDevice, c->stream));
+  PrefillAttnArgs pa = {};
+  pa.n_seg = n_seg;
+  RowList last = {};
+  last.n = n_seg;
+  std::vector<int32_t> rows;  // [2][T]: position and session of every row, several sessions only
+  if (n_seg > 1) rows.resize((size_t)2 * T);
+  for (int i = 0, row0 = 0; i < n_seg; row0 += ntok[i], ++i) {
+    Session& s = c->sessions[sids[i]];
+    pa.seg[i] = PfSeg{row0, ntok[i], s.len, sids[i]};
+    last.row[i] = row0 + ntok[i] - 1;
+    if (n_seg > 1)
+      for (int t = 0; t < ntok[i]; ++t) {
+        rows[row0 + t] = s.len + t;
+        rows[(size_t)T + row0 + t] = sids[i];
+      }
+    const int nb_old = (s.len + 15) / 16, nb_new = (s.len + ntok[i] + 15) / 16;
+    for (int b = nb_old; b < nb_new; ++b) s.table.push_back(c->kv.pop());
+    int32_t* row = c->d_tables + (size_t)sids[i] * c->table_stride;
+    if (nb_new > nb_old)
+      CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
+                                  cudaMemcpyHostToDevice, c->stream));
+  }
+  for (int b = 0; b < out_rows; ++b) {
+    sa.sess[b] = all_rows ? sids[0] : sids[b];
+    sa.pos[b] = all_rows ? c->sessions[sids[0]].len + b : c->sessions[sids[b]].len + ntok[b] - 1;
+  }
+  if (n_seg > 1)  // pageable source: the copy has taken the bytes when the call returns
+    CUDA_TRY(c, cudaMemcpyAsync(c->pf_rows, rows.data(), rows.size() * 4, cudaMemcpyHostToDevice, c->stream));
   CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &sa, sizeof sa, cudaMemcpyHostToDevice, c->stream));
   CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
   c->ring_pos = (slot + 1) % kRing;
+  const int32_t* row_pos = n_seg > 1 ? c->pf_rows : nullptr;
+  const int32_t* row_sess = n_seg > 1 ? c->pf_rows + T : nullptr;
+  const int p0 = c->sessions[sids[0]].len;  // one session: positions p0 + row
+  int32_t* row = c->d_tables + (size_t)sids[0] * c->table_stride;
 
   int n = 0;
   const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL);
   Launch L{c->stream, pdl, &n};
-  const int p0 = s.len, D = c->D, HD = c->Hq * c->d;
+  const int D = c->D, HD = c->Hq * c->d;
   const PoolGeom pg = pool_geom(c);
   CUDA_TRY(c, launch_rows_to_resid(L, (const __half*)in, c->pf_r, T, D));
   for (int l = 0; l < c->L; ++l) {
@@ -1255,6 +1305,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
     gq.head_dim = c->d;
     gq.n_rot_heads = c->Hq + c->Hkv;
     gq.pos0 = p0;
+    gq.row_pos = row_pos;
     gq.rope_cos = c->d_cos;
     gq.rope_sin = c->d_sin;
     CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_xn, pp[0].map_hi, pp[0].map_lo}, gq, EPI_QKV));
@@ -1268,19 +1319,17 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
     kc.layer = l;
     kc.table = row;
     kc.pool = pg;
+    kc.row_pos = row_pos;
+    kc.row_sess = row_sess;
     CUDA_TRY(c, launch_kv_store_chunk(L, kc));
-    PrefillAttnArgs pa = {};
     pa.qkv = c->pf_qkv;
     pa.qkv_ld = c->R;
     pa.o = c->pf_o;
     pa.ldo = HD;
-    pa.n_tok = T;
-    pa.pos0 = p0;
     pa.n_heads = c->Hq;
     pa.n_kv_heads = c->Hkv;
     pa.head_dim = c->d;
     pa.layer = l;
-    pa.table = row;
     pa.pool = pg;
     CUDA_TRY(c, launch_prefill_attention(L, pa));
     // O projection + residual
@@ -1309,7 +1358,12 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
     gd.ldr = D;
     CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_act, pp[3].map_hi, pp[3].map_lo}, gd, EPI_RESID));
   }
+  // the output rows: contiguous for one session, else each session's last row gathered
   float* r_out = c->pf_r + (size_t)(T - out_rows) * D;
+  if (n_seg > 1) {
+    CUDA_TRY(c, launch_gather_rows(L, c->pf_r, D, last, c->pf_last_r));
+    r_out = c->pf_last_r;
+  }
   if (c->V) {  // final RMSNorm + LM head of the output rows
     GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, D, out_rows);
     a.r = r_out;
@@ -1321,14 +1375,19 @@ mag_status run_chunk(mag_ctx* c, const char* what, int32_t sid, int32_t T, const
     CUDA_TRY(c, launch_final_hidden(L, c->d_args, r_out, D, out_rows));
   }
   c->last_launches = n;
-  s.len += T;
+  for (int i = 0; i < n_seg; ++i) c->sessions[sids[i]].len += ntok[i];
   return MAG_OK;
 }
 
 }  // namespace
 
 mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out) {
-  return run_chunk(c, "prefill_chunk", sid, T, in, last_out, 1);
+  return run_chunk(c, "prefill_chunk", 1, &sid, &T, in, last_out, false);
+}
+
+mag_status mag_prefill_batch(mag_ctx* c, int32_t n_sessions, const int32_t* sids, const int32_t* n_tokens,
+                             const void* in, void* last_out) {
+  return run_chunk(c, "prefill_batch", n_sessions, sids, n_tokens, in, last_out, false);
 }
 
 // Verify step on the decode kernels: the n tokens are the n rows of a decode step of one session at
@@ -1386,7 +1445,7 @@ mag_status mag_verify_tokens(mag_ctx* c, int32_t sid, int32_t n_tokens, const vo
   if (n_tokens >= 1 && n_tokens <= c->B_max) return verify_on_step(c, sid, n_tokens, hidden_in, out);
   const int chunk_max = std::min(kPipeMaxBatch, c->cfg.max_chunk);
   if (n_tokens >= 1 && n_tokens <= chunk_max)
-    return run_chunk(c, "verify_tokens", sid, n_tokens, hidden_in, out, n_tokens);
+    return run_chunk(c, "verify_tokens", 1, &sid, &n_tokens, hidden_in, out, true);
   return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: %d tokens not in 1..%d", n_tokens,
               std::max(c->B_max, chunk_max));
 }

@@ -581,8 +581,9 @@ __global__ void kv_store_chunk_kernel(const KvChunkArgs a) {
   xk[i] = row[(int64_t)(a.n_heads + h) * d + i];
   xv[i] = row[(int64_t)(a.n_heads + Hkv + h) * d + i];
   __syncthreads();
-  const int pos = (a.step ? a.step->pos[0] : a.pos0) + t;
-  const int32_t* table = a.step ? a.pool.tables + (int64_t)a.step->sess[0] * a.pool.table_stride : a.table;
+  const int pos = a.row_pos ? a.row_pos[t] : (a.step ? a.step->pos[0] : a.pos0) + t;
+  const int sess = a.row_sess ? a.row_sess[t] : (a.step ? a.step->sess[0] : -1);
+  const int32_t* table = sess >= 0 ? a.pool.tables + (int64_t)sess * a.pool.table_stride : a.table;
   const int blk = table[pos >> 4];
   store_vec(a.pool, a.layer, blk, pos & 15, h, 0, xk, red);
   store_vec(a.pool, a.layer, blk, pos & 15, h, 1, xv, red);
@@ -683,12 +684,19 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   const int G = a.n_heads / a.n_kv_heads, gk = blockIdx.y;
   const int tpw = 16 / G;  // tokens per warp
   const int t_blk = blockIdx.x * 4 * tpw, t_warp = t_blk + warp * tpw;
+  // this block's session: its rows of the QKV output and of o, its positions and block table
+  const PfSeg sg = a.seg[blockIdx.z];
+  if (t_blk >= sg.n_tok) return;  // past this session's tokens (grid.x covers the longest)
+  const int n_tok = sg.n_tok, pos0 = sg.pos0;
+  const int32_t* table = a.pool.tables + (int64_t)sg.sess * a.pool.table_stride;
+  const __half* qkv = a.qkv + (int64_t)sg.row0 * a.qkv_ld;
+  __half* o_rows = a.o + (int64_t)sg.row0 * a.ldo;
   const int dt = a.pool.kv_dtype;
-  const int n_valid = a.pos0 + a.n_tok;  // keys in the pool after the chunk's store
-  const int last_tok = min(a.n_tok, t_blk + 4 * tpw) - 1;
-  const int n_keys = a.pos0 + last_tok + 1;  // keys this block reads
+  const int n_valid = pos0 + n_tok;  // keys in the pool after the chunk's store
+  const int last_tok = min(n_tok, t_blk + 4 * tpw) - 1;
+  const int n_keys = pos0 + last_tok + 1;  // keys this block reads
   const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
-  const int warp_last = min(a.n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
+  const int warp_last = min(n_tok, t_warp + tpw) - 1;  // this warp's last token (may be < t_warp)
 
   // K data of (this layer, pool block 0, this KV head, slot 0); a block's V data is pool_v_off further
   const uint8_t* pool_head0 = pool_vec(a.pool, a.layer, 0, 0, gk, 0);
@@ -708,7 +716,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
 #pragma unroll
       for (int pb = 0; pb < 4; ++pb) {
         const int blk = i * 4 + pb;
-        const uint8_t* kb = pool_head0 + (int64_t)(blk * 16 < n_valid ? a.table[blk] : 0) * a.pool.block_bytes +
+        const uint8_t* kb = pool_head0 + (int64_t)(blk * 16 < n_valid ? table[blk] : 0) * a.pool.block_bytes +
                             r0 * (2 * D) + c8 * 2;
 #pragma unroll
         for (int jj = 0; jj < 16 / kRpp; ++jj) {
@@ -738,7 +746,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
           continue;
         }
         float v[8];
-        dequant_unit(dt, load_unit(a.pool, a.layer, a.table[kp >> 4], which, gk, kp & 15, c8), v);
+        dequant_unit(dt, load_unit(a.pool, a.layer, table[kp >> 4], which, gk, kp & 15, c8), v);
         __half h[8], lo[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -762,7 +770,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     const int r = g + 8 * h, tl = r / G;
     tok[h] = t_warp + tl;
     hq[h] = gk * G + (r - tl * G);
-    live[h] = tl < tpw && tok[h] < a.n_tok;
+    live[h] = tl < tpw && tok[h] < n_tok;
   }
   if (n_tiles > 0) stage(0, 0);
   uint32_t qa[KS][4];
@@ -770,7 +778,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
   for (int s = 0; s < KS; ++s)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const __half* q = a.qkv + (int64_t)(live[h] ? tok[h] : 0) * a.qkv_ld + (int64_t)hq[h] * D + 16 * s + 2 * t;
+      const __half* q = qkv + (int64_t)(live[h] ? tok[h] : 0) * a.qkv_ld + (int64_t)hq[h] * D + 16 * s + 2 * t;
       qa[s][h] = live[h] ? *reinterpret_cast<const uint32_t*>(q) : 0u;
       qa[s][2 + h] = live[h] ? *reinterpret_cast<const uint32_t*>(q + 8) : 0u;
     }
@@ -788,7 +796,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     const __half* kt = tiles + (size_t)bf * 2 * PG::kTile;
     const __half* vt = kt + PG::kTile;
     const __half* klo = tiles + (size_t)(4 + bf) * PG::kTile;
-    if (warp_last < t_warp || i * kPfKeys > a.pos0 + warp_last) continue;  // no key of this tile is visible
+    if (warp_last < t_warp || i * kPfKeys > pos0 + warp_last) continue;  // no key of this tile is visible
     // ---- S = Q K^T over the tile's 64 keys: n-tile nt = keys 8 nt .. 8 nt + 7
     float sfr[NT][4];
 #pragma unroll
@@ -817,7 +825,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int h = j >> 1, kp = i * kPfKeys + 8 * nt + 2 * t + (j & 1);
-        const bool ok = live[h] && kp <= a.pos0 + tok[h];
+        const bool ok = live[h] && kp <= pos0 + tok[h];
         const float v = ok ? sfr[nt][j] * sc : -INFINITY;
         sfr[nt][j] = v;
         mx[h] = fmaxf(mx[h], v);
@@ -883,7 +891,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     if (!live[h]) continue;
     const float inv = l > 0.f ? 1.0f / l : 0.f;
-    __half* o = a.o + (int64_t)tok[h] * a.ldo + (int64_t)hq[h] * D;
+    __half* o = o_rows + (int64_t)tok[h] * a.ldo + (int64_t)hq[h] * D;
 #pragma unroll
     for (int n = 0; n < NV; ++n)
       *reinterpret_cast<__half2*>(o + 8 * n + 2 * t) = __floats2half2_rn(acc[n][2 * h] * inv, acc[n][2 * h + 1] * inv);
@@ -973,11 +981,14 @@ cudaError_t launch_kv_store_chunk(const Launch& L, const KvChunkArgs& a) {
 }
 
 cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a) {
-  if (a.n_tok == 0) return cudaSuccess;
+  if (a.n_seg < 1 || a.n_seg > MAG_MAX_BATCH) return cudaErrorInvalidValue;
   const int G = a.n_heads / a.n_kv_heads;
   if (G < 1 || G > 16) return cudaErrorInvalidValue;
   const int per_block = 4 * (16 / G);
-  const dim3 grid((a.n_tok + per_block - 1) / per_block, a.n_kv_heads);
+  int longest = 0;
+  for (int i = 0; i < a.n_seg; ++i) longest = a.seg[i].n_tok > longest ? a.seg[i].n_tok : longest;
+  if (longest == 0) return cudaSuccess;
+  const dim3 grid((longest + per_block - 1) / per_block, a.n_kv_heads, a.n_seg);
   auto run = [&](auto kern, size_t smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return e != cudaSuccess ? e : launch_ex(L, kern, grid, dim3(128), smem, a);

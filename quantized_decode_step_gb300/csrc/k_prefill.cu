@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else {  // EPI_QKV: fp16 q, k, v; q and k rotated at position pos0 + m (pairs (i, i + d/2) of a head)
         const int d = a.head_dim, hd = d / 2;
-        const int pos = min(a.pos0 + m, a.pos0 + a.M - 1);  // rows past the chunk compute, but store nothing
+        const int mm = min(m, a.M - 1);  // rows past the chunk compute, but store nothing
+        const int pos = a.row_pos ? a.row_pos[mm] : a.pos0 + mm;
         for (int c0 = 0; c0 < BN; c0 += 32) {
           const int head = (n0 + c0) / d, i0 = (n0 + c0) - head * d;
           if (i0 >= hd) continue;  // the second half of a head comes with the first
@@ -355,6 +356,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 __global__ void rows_to_resid_kernel(const __half* __restrict__ x, float* __restrict__ r, int D) {
   const int64_t row = blockIdx.x;
   for (int i = threadIdx.x; i < D; i += blockDim.x) r[row * D + i] = __half2float(x[row * D + i]);
+}
+
+// One block per listed row: dst row i = src row rows.row[i] (the last rows of several sessions' chunks).
+__global__ void gather_rows_kernel(const float* __restrict__ src, int D, const RowList rows, float* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t from = rows.row[blockIdx.x];
+  for (int i = threadIdx.x; i < D; i += blockDim.x) dst[(int64_t)blockIdx.x * D + i] = src[from * D + i];
 }
 
 // One block per token row: xn = fp16(r / sqrt(mean(r^2) + eps) * gamma) ("5. Core modules" 5.1, pre-norm).
@@ -487,6 +496,21 @@ cudaError_t launch_rows_to_resid(const Launch& L, const __half* x, float* r, int
   rows_to_resid_kernel<<<T, 256, 0, L.stream>>>(x, r, D);
   if (L.counter) ++*L.counter;
   return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const Launch& L, const float* src, int D, const RowList& rows, float* dst) {
+  if (rows.n < 1 || rows.n > MAG_MAX_BATCH) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows.n);
+  cfg.blockDim = dim3(256);
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L.counter) ++*L.counter;
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, src, D, rows, dst);
 }
 
 cudaError_t launch_rmsnorm_rows(const Launch& L, const float* r, const __half* gamma, float eps, int T, int D,

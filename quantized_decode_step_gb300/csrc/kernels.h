@@ -95,6 +95,7 @@ struct TcGemmArgs {
   __half* out;
   int32_t ldo;
   int32_t head_dim, n_rot_heads, pos0;
+  const int32_t* row_pos;  // when set, row m is rotated at row_pos[m] instead of pos0 + m
   const float* rope_cos;
   const float* rope_sin;
   uint32_t* err;
@@ -111,6 +112,12 @@ cudaError_t launch_tc_gemm(const Launch& L, const TcMaps& m, const TcGemmArgs& a
 cudaError_t launch_rows_to_resid(const Launch& L, const __half* x, float* r, int T, int D);
 cudaError_t launch_rmsnorm_rows(const Launch& L, const float* r, const __half* gamma, float eps, int T, int D,
                                 __half* xn);
+// Rows rows.row[0 .. n) of the fp32 [*][D] src into dst [n][D].
+struct RowList {
+  int32_t n;
+  int32_t row[MAG_MAX_BATCH];
+};
+cudaError_t launch_gather_rows(const Launch& L, const float* src, int D, const RowList& rows, float* dst);
 
 // ---------------------------------------------------------------- step prologue
 // block-table writes, fp16 input -> fp32 residual and its sum of squares (ss_part[0][b])
@@ -140,21 +147,28 @@ struct KvChunkArgs {
   // when set, pos0 and the table row are read on the device from the step arguments (session sess[0] from
   // position pos[0]), so a captured graph serves any session and position
   const StepArgs* step;
+  // when set (several sessions in one chunk), token t goes to session row_sess[t] at position row_pos[t]
+  const int32_t* row_pos;
+  const int32_t* row_sess;
 };
 cudaError_t launch_kv_store_chunk(const Launch& L, const KvChunkArgs& a);
 
 // Chunked prefill: causal GQA attention of the chunk's queries (token t at position pos0 + t) over the
 // pool positions 0 .. pos0 + t (the chunk's own keys stored first). Pool values are widened to fp16 in
 // shared memory (exact for FP16 storage).
+// One session's tokens in a chunk: rows row0 .. row0 + n_tok - 1 of the QKV output, at positions pos0 ..
+struct PfSeg {
+  int32_t row0, n_tok, pos0, sess;
+};
 struct PrefillAttnArgs {
-  const __half* qkv;  // [n_tok][qkv_ld]
+  const __half* qkv;  // [rows][qkv_ld]
   int32_t qkv_ld;
-  __half* o;          // [n_tok][ldo]
+  __half* o;          // [rows][ldo]
   int32_t ldo;
-  int32_t n_tok, pos0;
   int32_t n_heads, n_kv_heads, head_dim, layer;
-  const int32_t* table;
-  PoolGeom pool;
+  PoolGeom pool;      // block tables of the sessions in pool.tables
+  int32_t n_seg;      // grid.z
+  PfSeg seg[MAG_MAX_BATCH];
 };
 cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a);
 

@@ -163,3 +163,65 @@ def test_8b_prefill_512_on_800_matches_token_by_token_decode():
     top = np.argsort(got_d)[-2:]
     if got_d[top[1]] - got_d[top[0]] > 2 * TOL_MAX_ABS:
         assert int(np.argmax(got_p)) == int(top[1])
+
+
+def _run_batch(wl: Workload, seed: int, ntok, random_gain=True, decode_after=True, bar=TOL_REL_L2):
+    """Several sessions' chunks in one mag_prefill_batch call, then one decode step of all of them."""
+    shape = wl.shape
+    ctx, sids = driver.setup(wl, seed, random_gain=random_gain, extra_tokens=max(ntok) + 2)
+    w = oracle_weights(shape, seed, random_gain)
+    cfg = model_cfg(shape, wl.kv_dtype)
+    kvs = []
+    for i, p in enumerate(wl.prior):
+        kv = oracle.KV(cfg, p + max(ntok) + 8)
+        if p:
+            kv.append(*prior_kv(shape, seed, i, p))
+        kvs.append(kv)
+    c, s = oracle.rope_table(max(wl.prior) + max(ntok) + 4, shape.head_dim, shape.rope_base)
+    width = shape.vocab or shape.hidden
+    xs = [synth.hidden_f16(seed, n, shape.hidden, tag=f"batch{i}") for i, n in enumerate(ntok)]
+    out = torch.empty((len(sids), width), dtype=torch.float16, device="cuda")
+    ctx.prefill_batch(sids, list(ntok), torch.from_numpy(np.concatenate(xs)).cuda(), out)
+    ctx.sync()
+    got = out.cpu().numpy()
+    for i, (sid, p, n) in enumerate(zip(sids, wl.prior, ntok)):
+        assert ctx.session_length(sid) == p + n
+        ref = oracle.forward(cfg, w, [kvs[i]], [n], xs[i], c, s)[0]
+        _compare(got[i], ref, f"{wl.name} session {i} ({p} + {n} tokens)", bar)
+    if decode_after:
+        x = synth.hidden_f16(seed, len(sids), shape.hidden, tag="after")
+        od = torch.empty((len(sids), width), dtype=torch.float16, device="cuda")
+        ctx.decode_step(sids, torch.from_numpy(x).cuda(), od)
+        ctx.sync()
+        ref = oracle.forward(cfg, w, kvs, [1] * len(sids), x, c, s)
+        _compare(od.cpu().numpy(), ref, f"{wl.name} decode of every session after the batch", bar)
+    return ctx, sids
+
+
+@pytest.mark.parametrize("dt", [KV_FP16, KV_INT8, KV_INT4])
+def test_tiny_prefill_batch_of_sessions(dt):
+    # three sessions (128-token cache, empty, 37-token cache) with 37, 20 and 64 new tokens: ragged tiles,
+    # a session from position 0, one that crosses blocks
+    wl = Workload(f"tiny-prefill-batch-kv{dt}", TINY, dt, 3, (128, 0, 37), chunk=160)
+    _run_batch(wl, 91 + dt, (37, 20, 64))
+
+
+def test_tiny_prefill_batch_errors_change_nothing():
+    wl = Workload("tiny-prefill-batch-args", TINY, KV_FP16, 2, (10, 20), chunk=16)
+    ctx, sids = driver.setup(wl, 95, extra_tokens=16)
+    x = torch.zeros((16, TINY.hidden), dtype=torch.float16, device="cuda")
+    out = torch.empty((2, TINY.hidden), dtype=torch.float16, device="cuda")
+    free0 = ctx.memory_stats()["pool_blocks_free"]
+    for ids, nt in (([sids[0], sids[0]], [4, 4]), (sids, [10, 7]), (sids, [4, 0]), ([sids[0], 99], [4, 4])):
+        with pytest.raises(mag.MagError) as e:
+            ctx.prefill_batch(ids, nt, x, out)
+        assert e.value.status == mag.ERR_INVALID_ARG, (ids, nt)
+    assert [ctx.session_length(s) for s in sids] == [10, 20]
+    assert ctx.memory_stats()["pool_blocks_free"] == free0
+
+
+@pytest.mark.slow
+def test_8b_two_layers_prefill_batch():
+    shape = shrink(LLAMA8B, n_layers=2)
+    wl = Workload("8b2L-prefill-batch", shape, KV_FP16, 2, (800, 300), chunk=128)
+    _run_batch(wl, 97, (64, 40), random_gain=False)
