@@ -543,40 +543,49 @@ def run_prefill(args, tc_peak):
 
 
 def run_plans(args):
-    """Measurement aid for the adaptive plans: decode step time (8B, one FP16 session) at short, medium and
-    long contexts under every split count the plans can take, each plan forced in turn. Prints one JSON
-    line {"plans": {splits: {context: ms per step}}, "presets": [...]} and exits."""
+    """Measurement aid for the adaptive plans: decode step time (8B, one session) at short, medium and long
+    contexts under every attention launch shape a plan can take (split count x 4-warp or wide blocks),
+    each forced in turn; FP16 at 40 .. 19,431 keys, INT8 at 38,863 and INT4 at 77,726. Prints one JSON
+    line {"plans": {kv: {shape: {context: ms per step}}}, "presets": ...} and exits."""
     import torch
     import quantized_decode_step_gb300 as mag
     from synth import driver
     mag.build()
-    lens = (40, 100, 300, 700, 2048, 8192)
     steps = max(args.steps, 8)
-    wl = Workload("8b-plans", LLAMA8B, KV_FP16, len(lens), lens)
-    ctx, sids = driver.setup(wl, args.seed, extra_tokens=steps + args.warmup + 8)
-    x = torch.zeros((1, LLAMA8B.hidden), dtype=torch.float16, device="cuda")
-    out = torch.empty((1, LLAMA8B.vocab), dtype=torch.float16, device="cuda")
+    runs = ((KV_FP16, (40, 100, 300, 700, 2048, 8192, 19431)), (KV_INT8, (38863,)), (KV_INT4, (77726,)))
     res = {}
-    for S in (1, 2, 4, 8, 16):
-        ctx.set_adaptive(True, force_plan=1, plan_splits=(S, S, S))
-        row = {}
-        for sid, n in zip(sids, lens):
-            for _ in range(args.warmup):
-                ctx.decode_step([sid], x, out)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(steps):
-                ctx.decode_step([sid], x, out)
-            e1.record()
-            e1.synchronize()
-            row[n] = round(e0.elapsed_time(e1) / steps, 4)
-            ctx.session_truncate(sid, n)
-        res[S] = row
+    for dt, lens in runs:
+        wl = Workload(f"8b-plans-kv{dt}", LLAMA8B, dt, len(lens), lens)
+        ctx, sids = driver.setup(wl, args.seed, extra_tokens=steps + args.warmup + 8)
+        x = torch.zeros((1, LLAMA8B.hidden), dtype=torch.float16, device="cuda")
+        out = torch.empty((1, LLAMA8B.vocab), dtype=torch.float16, device="cuda")
+        table = {}
+        for S in (1, 2, 4, 8, 16, 32, 48, 64):
+            for wide in (0, 1):
+                if (dt != KV_FP16 and S < 8) or (wide and S >= 16):
+                    continue  # long contexts: few splits are far off; wide clusters of 16 queue
+                ctx.set_adaptive(True, force_plan=1, plan_splits=(S, S, S), plan_wide=(wide,) * 3)
+                row = {}
+                for sid, n in zip(sids, lens):
+                    for _ in range(args.warmup):
+                        ctx.decode_step([sid], x, out)
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(steps):
+                        ctx.decode_step([sid], x, out)
+                    e1.record()
+                    e1.synchronize()
+                    row[n] = round(e0.elapsed_time(e1) / steps, 4)
+                    ctx.session_truncate(sid, n)
+                table[f"S{S}{'w' if wide else ''}"] = row
+                print(f"kv{dt} S{S} wide{wide}", row, file=sys.stderr, flush=True)
+        res[f"kv{dt}"] = table
+        ctx.close()
+        torch.cuda.empty_cache()
     a = mag.adapt_defaults()
-    print(json.dumps({"plans": res, "presets": list(a.plan_splits), "unit": "ms per decode step",
-                       "workload": "8b decode, 1 FP16 session, contexts " + "/".join(map(str, lens))}))
-    ctx.close()
+    print(json.dumps({"plans": res, "presets": {"splits": list(a.plan_splits), "wide": list(a.plan_wide)},
+                      "unit": "ms per decode step", "workload": "8b decode, 1 session; contexts per KV type"}))
 
 
 def run_elastic(args):

@@ -296,10 +296,13 @@ typedef struct mag_adapt_config {
   int32_t adaptive_sample_rate;  /* one inference in this many is recorded; default 4 */
   int32_t plan_short_below;      /* P90 below this: short plan (0); default 128 */
   int32_t plan_long_above;       /* P90 above this: long plan (2); between the two, medium (1); default 512 */
-  int32_t plan_splits[3];        /* attention splits of plans 0, 1, 2 for one session; a batch of B
-                                    uses min(this, the context's default for B), the default being
-                                    about 2 blocks per SM, at most the device's largest co-scheduled
-                                    cluster (16); 0 = the default */
+  int32_t plan_splits[3];        /* attention splits of plans 0, 1, 2 for one session, 0..64 (0 = the
+                                    default: about 2 blocks per SM, at most one cluster of 16); a
+                                    batch of B is capped at 4 x SMs / (B x Hkv); more splits than the
+                                    device's largest co-scheduled cluster run as up to 8 clusters of 8
+                                    whose outputs the last block to finish merges */
+  int32_t plan_wide[3];          /* 1: plan p runs the wide attention blocks (8 warps at head_dim 128,
+                                    16 at 64; one block per SM) instead of 4-warp blocks */
   int32_t force_plan;            /* -1: plans follow the profile; 0..2: that plan, always */
   int32_t async_switch;          /* 1: a new plan's graphs are captured on a background thread and the
                                     step keeps the old plan until they are ready */
@@ -323,6 +326,7 @@ typedef struct mag_profile {
   int32_t plan;        /* plan the next step launches */
   int32_t pending_plan; /* plan whose graphs a background capture is building; -1 if none */
   int32_t plan_splits; /* attention split count of `plan` */
+  int32_t plan_wide;   /* whether `plan` runs the wide attention blocks */
   int32_t switches;    /* plan changes so far */
   int64_t hot_blocks;  /* hot pool target from the last full window; -1 before one */
 } mag_profile;

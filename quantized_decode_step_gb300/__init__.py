@@ -73,13 +73,14 @@ class AdaptConfig(ctypes.Structure):
     _fields_ = [("enable_adaptive", ctypes.c_int32), ("adaptive_window_size", ctypes.c_int32),
                 ("adaptive_sample_rate", ctypes.c_int32), ("plan_short_below", ctypes.c_int32),
                 ("plan_long_above", ctypes.c_int32), ("plan_splits", ctypes.c_int32 * 3),
-                ("force_plan", ctypes.c_int32), ("async_switch", ctypes.c_int32), ("hot_pool_slack", ctypes.c_float)]
+                ("plan_wide", ctypes.c_int32 * 3), ("force_plan", ctypes.c_int32), ("async_switch", ctypes.c_int32), ("hot_pool_slack", ctypes.c_float)]
 
 
 class Profile(ctypes.Structure):
     _fields_ = [("seen", ctypes.c_int64), ("recorded", ctypes.c_int32), ("p50", ctypes.c_int32),
                 ("p90", ctypes.c_int32), ("p99", ctypes.c_int32), ("plan", ctypes.c_int32),
-                ("pending_plan", ctypes.c_int32), ("plan_splits", ctypes.c_int32), ("switches", ctypes.c_int32),
+                ("pending_plan", ctypes.c_int32), ("plan_splits", ctypes.c_int32), ("plan_wide", ctypes.c_int32),
+                ("switches", ctypes.c_int32),
                 ("hot_blocks", ctypes.c_int64)]
 
 
@@ -347,8 +348,8 @@ class Context:
         a = adapt_defaults()
         a.enable_adaptive = 1 if enable else 0
         for k, v in fields.items():
-            if k == "plan_splits":
-                a.plan_splits = (ctypes.c_int32 * 3)(*v)
+            if k in ("plan_splits", "plan_wide"):
+                setattr(a, k, (ctypes.c_int32 * 3)(*v))
             else:
                 setattr(a, k, v)
         self._check(lib().mag_set_adaptive(self.h, ctypes.byref(a)), "mag_set_adaptive")

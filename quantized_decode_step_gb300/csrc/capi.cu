@@ -78,7 +78,10 @@ struct mag_ctx {
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   int device = 0, n_sm = 0;
-  int attn_cluster_max = 1;
+  int attn_cluster_max = 1;       // largest co-scheduled attention cluster, 4-warp blocks
+  int attn_cluster_max_wide = 1;  // the same for the wide (16- or 8-warp) blocks
+  float* attn_part = nullptr;       // clusters' partial outputs when a (session, KV head) spans several
+  uint32_t* attn_arrivals = nullptr;
   std::string err;
   int L = 0, D = 0, Hq = 0, Hkv = 0, d = 0, F = 0, V = 0, R = 0, G = 0, B_max = 0;
   int table_stride = 0;
@@ -234,9 +237,9 @@ GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
 
 // Splits of one (session, KV head): the blocks of one thread-block cluster, so at
 // most the largest cluster the device co-schedules (16 on a full GPU).
-int attn_splits(const mag_ctx* c, int B) {
+int attn_splits(const mag_ctx* c, int B, bool wide = false) {
   int s = (2 * c->n_sm + B * c->Hkv - 1) / (B * c->Hkv);
-  return std::max(1, std::min(s, c->attn_cluster_max));
+  return std::max(1, std::min(s, wide ? c->attn_cluster_max_wide : c->attn_cluster_max));
 }
 
 int64_t kv_data_bytes(int d, int dt) { return dt == 0 ? 2 * d : (dt == 1 ? d : d / 2); }
@@ -396,7 +399,7 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
 // there (row b causally up to its own position) instead of each row appending its own.
 // `splits` is the attention split count of the plan in use; `st` the stream the launches go to (the
 // context's, or a capture stream).
-cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool verify, int splits,
+cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool verify, int splits, bool wide,
                         cudaStream_t st) {
   const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof;
   Launch L0{st, false, n_launch};
@@ -448,10 +451,18 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
       a.n_kv_heads = c->Hkv;
       a.head_dim = c->d;
       a.layer = l;
-      a.n_split = S;
       a.pool = pg;
       a.step = c->d_args;
       a.stored = verify;
+      a.wide = wide;
+      // more splits than one cluster holds: clusters of at most 8 (which co-schedule more readily than
+      // clusters of 16), merged by the last block to finish
+      const int cmax = wide ? c->attn_cluster_max_wide : c->attn_cluster_max;
+      const int csz = S <= cmax ? cmax : std::min(cmax, 8);
+      a.n_groups = std::min(kAttnMaxGroups, (S + csz - 1) / csz);
+      a.n_split = std::min(csz, (S + a.n_groups - 1) / a.n_groups);
+      a.part = c->attn_part;
+      a.arrivals = c->attn_arrivals;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
     {  // O projection + residual
@@ -503,6 +514,8 @@ void free_ctx(mag_ctx* c) {
   cudaFree(c->d_sin);
   cudaFree(c->arena);
   cudaFree(c->d_counters);
+  cudaFree(c->attn_part);
+  cudaFree(c->attn_arrivals);
   cudaFree(c->d_args);
   cudaFree(c->d_in_stage);
   cudaFree(c->d_out_stage);
@@ -662,7 +675,8 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     return bail(MAG_ERR_CUDA);
   }
   cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, c->device);
-  if ((e = attention_max_cluster(cfg->head_dim, cfg->kv_dtype, &c->attn_cluster_max)) != cudaSuccess) {
+  if ((e = attention_max_cluster(cfg->head_dim, cfg->kv_dtype, false, &c->attn_cluster_max)) != cudaSuccess ||
+      (e = attention_max_cluster(cfg->head_dim, cfg->kv_dtype, true, &c->attn_cluster_max_wide)) != cudaSuccess) {
     fail(c, MAG_ERR_CUDA, "attention cluster query: %s", cudaGetErrorString(e));
     return bail(MAG_ERR_CUDA);
   }
@@ -803,7 +817,11 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   size_t nc = gemv_counters(c);
   c->n_counters = nc;
   size_t stage_out = (size_t)c->B_max * (c->V ? c->V : c->D) * 2;
+  const size_t part_bytes = (size_t)c->B_max * c->Hkv * kAttnMaxGroups * 3 * c->Hq / c->Hkv * c->d * 4;
+  const size_t arrival_bytes = (size_t)c->B_max * c->Hkv * 4;
   if (cudaMalloc(&c->d_counters, nc * 4) != cudaSuccess ||
+      cudaMalloc(&c->attn_part, part_bytes) != cudaSuccess ||
+      cudaMalloc(&c->attn_arrivals, arrival_bytes) != cudaSuccess ||
       cudaMalloc(&c->d_args, sizeof(StepArgs)) != cudaSuccess ||
       cudaMalloc(&c->d_in_stage, (size_t)c->B_max * c->D * 2) != cudaSuccess ||
       cudaMalloc(&c->d_out_stage, stage_out) != cudaSuccess ||
@@ -819,6 +837,8 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     if (ps != MAG_OK) return bail(ps);
   }
   cudaMemsetAsync(c->d_counters, 0, nc * 4, c->stream);
+  cudaMemsetAsync(c->attn_arrivals, 0, arrival_bytes, c->stream);
+  c->other_bytes += part_bytes + arrival_bytes;
   for (auto& ev : c->ring_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
   c->other_bytes += nc * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
   if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
@@ -1049,11 +1069,16 @@ static mag_status step_upload(mag_ctx* c, int B, const int32_t* sids, const void
   return MAG_OK;
 }
 
-// Attention split count of plan p at batch B: the plan's count (a single-session figure), capped by the
-// context's default for B (which shrinks as the batch fills the GPU); 0 = the default.
+// Whether plan p runs the wide attention blocks.
+static bool plan_wide(const mag_ctx* c, int p) { return c->adapt.enable_adaptive && c->adapt.plan_wide[p]; }
+
+// Attention split count of plan p at batch B: the plan's count (a single-session figure), capped at about
+// 4 blocks per SM over the batch's (session, KV head) pairs; 0 = the context's default (at most one
+// cluster).
 static int plan_splits(const mag_ctx* c, int p, int B) {
   const int s = c->adapt.enable_adaptive ? c->adapt.plan_splits[p] : 0;
-  return s > 0 ? std::min(s, attn_splits(c, B)) : attn_splits(c, B);
+  if (s == 0) return attn_splits(c, B, plan_wide(c, p));
+  return std::max(1, std::min(s, 4 * c->n_sm / (B * c->Hkv)));
 }
 
 // Capture and instantiate the step graph of (verify, plan p, batch B) on stream st: the context's
@@ -1064,7 +1089,7 @@ static cudaError_t capture_graph(mag_ctx* c, bool verify, int p, int B, cudaStre
   int n = 0;
   cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return e;
-  e = record_step(c, B, &n, nullptr, verify, plan_splits(c, p, B), st);
+  e = record_step(c, B, &n, nullptr, verify, plan_splits(c, p, B), plan_wide(c, p), st);
   const cudaError_t e2 = cudaStreamEndCapture(st, &g);
   if (e == cudaSuccess) e = e2;
   if (e == cudaSuccess) e = cudaGraphInstantiate(&out.exec, g, 0);
@@ -1144,7 +1169,7 @@ static mag_status launch_step(mag_ctx* c, int B, bool verify) {
   const int S = plan_splits(c, c->cur_plan, B);
   if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
     int n = 0;
-    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify, S, c->stream));
+    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify, S, plan_wide(c, c->cur_plan), c->stream));
     c->last_launches = n;
     return MAG_OK;
   }
@@ -1176,7 +1201,8 @@ mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, co
   if (st != MAG_OK) return st;
   Profiler prof;
   int n = 0;
-  CUDA_TRY(c, record_step(c, B, &n, &prof, false, plan_splits(c, c->cur_plan, B), c->stream));
+  CUDA_TRY(c, record_step(c, B, &n, &prof, false, plan_splits(c, c->cur_plan, B), plan_wide(c, c->cur_plan),
+                          c->stream));
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   *n_out = (int32_t)prof.kinds.size();
@@ -1494,9 +1520,13 @@ mag_status mag_set_adaptive(mag_ctx* c, const mag_adapt_config* a) {
     if (a->plan_short_below > a->plan_long_above + 1)
       return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: short_below %d above long_above %d",
                   a->plan_short_below, a->plan_long_above);
-    for (int i = 0; i < 3; ++i)
-      if (a->plan_splits[i] < 0 || a->plan_splits[i] > 16)
-        return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: plan %d splits %d not in 0..16", i, a->plan_splits[i]);
+    for (int i = 0; i < 3; ++i) {
+      if (a->plan_splits[i] < 0 || a->plan_splits[i] > 8 * kAttnMaxGroups)
+        return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: plan %d splits %d not in 0..%d", i, a->plan_splits[i],
+                    8 * kAttnMaxGroups);
+      if (a->plan_wide[i] != 0 && a->plan_wide[i] != 1)
+        return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: plan %d wide %d not 0 or 1", i, a->plan_wide[i]);
+    }
     if (a->force_plan < -1 || a->force_plan > 2)
       return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: force_plan %d not in -1..2", a->force_plan);
     if (!(a->hot_pool_slack >= 1.0f && a->hot_pool_slack <= 16.0f))
@@ -1510,9 +1540,9 @@ mag_status mag_set_adaptive(mag_ctx* c, const mag_adapt_config* a) {
   mag_adapt_config next = a->enable_adaptive ? *a : mag_adapt_config{};
   for (int p = 0; p < 3; ++p) {
     for (int b = 1; b <= MAG_MAX_BATCH; ++b) {
-      const int s_old = plan_splits(c, p, b);
+      const int s_old = plan_splits(c, p, b) * 2 + plan_wide(c, p);
       std::swap(c->adapt, next);
-      const int s_new = plan_splits(c, p, b);
+      const int s_new = plan_splits(c, p, b) * 2 + plan_wide(c, p);
       std::swap(c->adapt, next);
       if (s_old == s_new) continue;
       for (int v = 0; v < 2; ++v) {
@@ -1551,6 +1581,7 @@ mag_status mag_get_profile(mag_ctx* c, mag_profile* out) {
   out->plan = c->cur_plan;
   out->pending_plan = c->pending_plan;
   out->plan_splits = plan_splits(c, c->cur_plan, 1);
+  out->plan_wide = plan_wide(c, c->cur_plan);
   out->switches = c->switches;
   out->hot_blocks = c->hot_blocks;
   return MAG_OK;

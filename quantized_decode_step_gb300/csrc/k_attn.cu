@@ -242,40 +242,49 @@ __device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
 
 constexpr int kAttnSlots = 3;  // per-warp ring depth, in (block, KV head) units
 
-// Shared-memory image of the four warps' partial outputs, [warp][head row][t][jj][n] with the t and head
+// Shared-memory image of the NW warps' partial outputs, [warp][head row][t][jj][n] with the t and head
 // strides padded so that the float4 stores of a quarter-warp fall into distinct banks. n is the PV
 // n-tile, (2t + jj) the column within it: dim = (2t + jj) NV + v_slot_dim(n). It and the block's
 // merged partial o [head][dim] reuse the rings' shared memory once every warp has left its loop.
-template <int D>
+template <int D, int NW>
 struct AccGeom {
   static constexpr int kNV = D / 8;
   static constexpr int kTS = 2 * kNV + 4;                         // floats per t
   static constexpr int kRow = (4 * kTS + 16 + 31) / 32 * 32 + 16;  // floats per head row, = 16 mod 32
   static constexpr int kWarp = 8 * kRow;
-  static constexpr size_t kAccBytes = (size_t)4 * kWarp * 4;
+  static constexpr size_t kAccBytes = (size_t)NW * kWarp * 4;
   static constexpr size_t kBytes = kAccBytes + (size_t)8 * D * 4;  // + the partial o
 };
 
-template <int D, int DT>
+template <int D, int DT, int NW>
 __host__ __device__ constexpr size_t attn_smem_bytes() {
-  return (size_t)4 * kAttnSlots * SlotGeom<D, DT>::kBytes > AccGeom<D>::kBytes
-             ? (size_t)4 * kAttnSlots * SlotGeom<D, DT>::kBytes
-             : AccGeom<D>::kBytes;
+  return (size_t)NW * kAttnSlots * SlotGeom<D, DT>::kBytes > AccGeom<D, NW>::kBytes
+             ? (size_t)NW * kAttnSlots * SlotGeom<D, DT>::kBytes
+             : AccGeom<D, NW>::kBytes;
+}
+
+// Warps per block of the wide variant (long contexts: more warps per SM to hide the per-block chain).
+// At head_dim 128 a lane holds ~185 registers, so 4-warp blocks stop at two per SM (8 warps) and 16-warp
+// blocks would spill under the 128-register cap: 8 warps, one block per SM on every SM of the grid.
+// At head_dim 64, 16 warps where their rings fit one SM's shared memory.
+template <int D, int DT>
+constexpr int attn_wide_warps() {
+  return D > 64 ? 8 : ((size_t)16 * kAttnSlots * SlotGeom<D, DT>::kBytes <= 220 * 1024 ? 16 : 8);
 }
 
 // One block of the grid per (split, KV head, session); the blocks of a
 // (session, KV head) form a thread-block cluster and merge their splits
-// through distributed shared memory.
-template <int D, int DT>
-__global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
+// through distributed shared memory. NWARP warps per block.
+template <int D, int DT, int NWARP>
+__global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   namespace cg = cooperative_groups;
   using SG = SlotGeom<D, DT>;
-  using AG = AccGeom<D>;
+  using AG = AccGeom<D, NWARP>;
   constexpr int NS = D / 32;  // 32-dim slabs of K (one INT4 group each)
   constexpr int NV = D / 8;   // V n-tiles
   constexpr int NW = D / 16;  // words per V row of a lane
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_m[4][8], s_l[4][8];
+  __shared__ float s_m[NWARP][8], s_l[NWARP][8];
   float* s_acc = reinterpret_cast<float*>(smem);                    // after the loops
   float* s_po = reinterpret_cast<float*>(smem + AG::kAccBytes);      // this block's partial o [head][dim]
   __shared__ float s_pm[8], s_pl[8];  // this block's partial (m, l) per head
@@ -287,6 +296,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, t = lane & 3;
   const int Hq = a.n_heads, Hkv = a.n_kv_heads, G = Hq / Hkv;
   const int S = a.n_split;  // == cluster size
+  const int K = a.n_groups;  // clusters per (session, KV head); S K splits in all, blockIdx.x = split
   // The step's arguments were copied before the step's first kernel and the
   // pool blocks before the new token's were written and mapped by earlier
   // steps, so their fetch starts before waiting for the QKV projection.
@@ -296,25 +306,25 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   // the session's earlier rows as well); they are mapped and fetched only after the wait
   const int fresh_blk = a.stored ? a.step->pos[0] >> 4 : new_blk;
   const int n_blocks = new_blk + 1;
-  const int bps = (n_blocks + S - 1) / S;
+  const int bps = (n_blocks + S * K - 1) / (S * K);
   const int blk0 = split * bps, blk1 = min(blk0 + bps, n_blocks);
   const int32_t* table = a.pool.tables + (int64_t)sess * a.pool.table_stride;
-  // this warp's blocks: blk0 + warp + 4 j; the new token's block, if it is one
+  // this warp's blocks: blk0 + warp + NWARP j; the new token's block, if it is one
   // of them, is the last
-  const int nb = blk0 + warp < blk1 ? (blk1 - blk0 - warp + 3) / 4 : 0;
+  const int nb = blk0 + warp < blk1 ? (blk1 - blk0 - warp + NWARP - 1) / NWARP : 0;
   // physical ids of the warp's first 32 blocks, one lane each (one round trip for all of them); a block
   // from fresh_blk on may have been mapped by this step's prologue, so its id is read after the wait
-  const int phys_l = lane < nb ? table[blk0 + warp + 4 * lane] : 0;
+  const int phys_l = lane < nb ? table[blk0 + warp + NWARP * lane] : 0;
   int phys_new = -1;
   auto phys_of = [&](int j) {
-    const int blk = blk0 + warp + 4 * j;
+    const int blk = blk0 + warp + NWARP * j;
     const int p = j < 32 ? __shfl_sync(0xffffffffu, phys_l, j) : table[blk];
     return blk == new_blk ? phys_new : blk >= fresh_blk ? table[blk] : p;
   };
   uint8_t* ring = smem + (size_t)warp * kAttnSlots * SG::kBytes;
   int issued = 0;
   for (; issued < min(nb, kAttnSlots); ++issued) {
-    const int blk = blk0 + warp + 4 * issued;
+    const int blk = blk0 + warp + NWARP * issued;
     if (blk >= fresh_blk) break;
     issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys_of(issued), gk, lane);
     cp_async_commit();
@@ -375,7 +385,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
 
   int slot_i = 0;
   for (int j = 0; j < nb; ++j) {
-    const int blk = blk0 + warp + 4 * j;
+    const int blk = blk0 + warp + NWARP * j;
     uint8_t* slot = ring + slot_i * SG::kBytes;
     cp_async_wait<kAttnSlots - 1>();
     __syncwarp();
@@ -499,7 +509,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
   }
   cp_async_wait<0>();
 
-  // ---- merge the 4 warps of this block into the block's partial (m, l, o); the barrier below also
+  // ---- merge the NWARP warps of this block into the block's partial (m, l, o); the barrier below also
   // ends every warp's use of its ring, whose memory the merge reuses
   float l_tot = l_part;
   l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
@@ -513,7 +523,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     // this warp's share, rescaled to the block's running maximum of the head
     float mm = s_m[0][gi];
 #pragma unroll
-    for (int w = 1; w < 4; ++w) mm = fmaxf(mm, s_m[w][gi]);
+    for (int w = 1; w < NWARP; ++w) mm = fmaxf(mm, s_m[w][gi]);
     const float e = mm == -INFINITY ? 0.f : exp2f(m_run - mm);
     float* dst = s_acc + warp * AG::kWarp + gi * AG::kRow + t * AG::kTS;
 #pragma unroll
@@ -525,7 +535,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     if (warp == 0 && t == 0) {
       float l = 0.f;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) l += s_l[w][gi] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][gi] - mm));
+      for (int w = 0; w < NWARP; ++w) l += s_l[w][gi] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][gi] - mm));
       s_pm[gi] = mm;  // -inf for a block without keys
       s_pl[gi] = l;
     }
@@ -537,7 +547,10 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
     int n = r;
     if (DT == 2) n = (r & 8) + ((r & 3) << 1) + ((r >> 2) & 1);
     const int off = h * AG::kRow + (c >> 1) * AG::kTS + (c & 1) * NV + n;
-    s_po[idx] = s_acc[off] + s_acc[AG::kWarp + off] + s_acc[2 * AG::kWarp + off] + s_acc[3 * AG::kWarp + off];
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) sum += s_acc[w * AG::kWarp + off];
+    s_po[idx] = sum;
   }
   // ---- merge the cluster's splits through distributed shared memory: every output reads the S
   // partials (m, l, o) in one round trip
@@ -563,7 +576,43 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnArgs a) {
       l = fmaf(lq[q], e, l);
       o = fmaf(oq[q], e, o);
     }
-    a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
+    if (K == 1) {
+      a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
+    } else {  // this cluster's (m, l, o) of the output, for the merge of the K clusters
+      float* pp = a.part + ((((int64_t)b * Hkv + gk) * K + split / S) * 3) * G * D;
+      pp[idx] = mm;  // -inf when none of the cluster's splits has a key
+      pp[G * D + idx] = l;
+      pp[2 * G * D + idx] = o;
+    }
+  }
+  if (K > 1) {
+    // the last block of the S K to arrive merges the K clusters' parts in cluster order (no waiting)
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned int n = atomicAdd(a.arrivals + (int64_t)b * Hkv + gk, 1u);
+      s_last = n == (unsigned int)(S * K - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const float* pb = a.part + (((int64_t)b * Hkv + gk) * K) * 3 * G * D;
+      for (int idx = tid; idx < G * D; idx += blockDim.x) {
+        float mm = -INFINITY;
+        for (int q = 0; q < K; ++q) mm = fmaxf(mm, __ldcg(pb + (int64_t)q * 3 * G * D + idx));
+        float l = 0.f, o = 0.f;
+        for (int q = 0; q < K; ++q) {
+          const float* pq = pb + (int64_t)q * 3 * G * D;
+          const float mq = __ldcg(pq + idx);
+          const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
+          l = fmaf(__ldcg(pq + G * D + idx), e, l);
+          o = fmaf(__ldcg(pq + 2 * G * D + idx), e, o);
+        }
+        a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
+      }
+      if (tid == 0) a.arrivals[(int64_t)b * Hkv + gk] = 0u;  // ready for the next launch
+    }
   }
   cluster.sync();  // keep this block's shared memory alive until every rank has read it
 }
@@ -923,32 +972,38 @@ cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int D, int DT>
+template <int D, int DT, int NW>
 cudaError_t attn_prepare() {
-  auto kern = attn_kernel<D, DT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes<D, DT>());
+  auto kern = attn_kernel<D, DT, NW>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes<D, DT, NW>());
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
+template <int D, int DT, int NW>
+cudaError_t launch_attn_nw(const Launch& L, const AttnArgs& a, int batch) {
+  cudaError_t e = attn_prepare<D, DT, NW>();
+  if (e != cudaSuccess) return e;
+  return launch_ex(L, attn_kernel<D, DT, NW>, dim3(a.n_split * a.n_groups, a.n_kv_heads, batch), dim3(32 * NW),
+                   attn_smem_bytes<D, DT, NW>(), a, a.n_split);
+}
+
 template <int D, int DT>
 cudaError_t launch_attn_t(const Launch& L, const AttnArgs& a, int batch) {
-  cudaError_t e = attn_prepare<D, DT>();
-  if (e != cudaSuccess) return e;
-  return launch_ex(L, attn_kernel<D, DT>, dim3(a.n_split, a.n_kv_heads, batch), dim3(128), attn_smem_bytes<D, DT>(),
-                   a, a.n_split);
+  return a.wide ? launch_attn_nw<D, DT, attn_wide_warps<D, DT>()>(L, a, batch) : launch_attn_nw<D, DT, 4>(L, a, batch);
 }
 
 // Largest cluster size (16, 8, 4, 2, 1) of which at least one cluster fits on the device.
-template <int D, int DT>
-cudaError_t attn_max_cluster_t(int* out) {
-  cudaError_t e = attn_prepare<D, DT>();
+template <int D, int DT, int NW>
+cudaError_t attn_max_cluster_nw(int* out) {
+  cudaError_t e = attn_prepare<D, DT, NW>();
   if (e != cudaSuccess) return e;
   for (int s = 16; s >= 1; s /= 2) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(s, 1, 1);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = attn_smem_bytes<D, DT>();
+    cfg.blockDim = dim3(32 * NW);
+    cfg.dynamicSmemBytes = attn_smem_bytes<D, DT, NW>();
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = s;
@@ -957,7 +1012,7 @@ cudaError_t attn_max_cluster_t(int* out) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, attn_kernel<D, DT>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, attn_kernel<D, DT, NW>, &cfg);
     if (e != cudaSuccess) return e;
     if (n >= 1) {
       *out = s;
@@ -999,23 +1054,30 @@ cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a) 
   return cudaErrorInvalidValue;
 }
 
-cudaError_t attention_max_cluster(int head_dim, int kv_dtype, int* out) {
+template <int D, int DT>
+cudaError_t attn_max_cluster_t(int* out, bool wide) {
+  return wide ? attn_max_cluster_nw<D, DT, attn_wide_warps<D, DT>()>(out) : attn_max_cluster_nw<D, DT, 4>(out);
+}
+
+cudaError_t attention_max_cluster(int head_dim, int kv_dtype, bool wide, int* out) {
   if (head_dim == 128) {
-    if (kv_dtype == 0) return attn_max_cluster_t<128, 0>(out);
-    if (kv_dtype == 1) return attn_max_cluster_t<128, 1>(out);
-    return attn_max_cluster_t<128, 2>(out);
+    if (kv_dtype == 0) return attn_max_cluster_t<128, 0>(out, wide);
+    if (kv_dtype == 1) return attn_max_cluster_t<128, 1>(out, wide);
+    return attn_max_cluster_t<128, 2>(out, wide);
   }
   if (head_dim == 64) {
-    if (kv_dtype == 0) return attn_max_cluster_t<64, 0>(out);
-    if (kv_dtype == 1) return attn_max_cluster_t<64, 1>(out);
-    return attn_max_cluster_t<64, 2>(out);
+    if (kv_dtype == 0) return attn_max_cluster_t<64, 0>(out, wide);
+    if (kv_dtype == 1) return attn_max_cluster_t<64, 1>(out, wide);
+    return attn_max_cluster_t<64, 2>(out, wide);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch) {
   const int dt = a.pool.kv_dtype;
-  if (a.n_split < 1 || a.n_split > 16) return cudaErrorInvalidValue;
+  if (a.n_split < 1 || a.n_split > 16 || a.n_groups < 1 || a.n_groups > kAttnMaxGroups ||
+      (a.n_groups > 1 && (!a.part || !a.arrivals)))
+    return cudaErrorInvalidValue;
   if (a.head_dim == 128) {
     if (dt == 0) return launch_attn_t<128, 0>(L, a, batch);
     if (dt == 1) return launch_attn_t<128, 1>(L, a, batch);

@@ -180,17 +180,27 @@ struct AttnArgs {
   int32_t ldo;
   int32_t n_heads, n_kv_heads, head_dim;
   int32_t layer;
-  int32_t n_split;  // grid.x = cluster size (<= 16)
+  int32_t n_split;   // cluster size (<= 16)
+  int32_t n_groups;  // clusters per (session, KV head), 1..kAttnMaxGroups: grid.x = n_split * n_groups
+  // n_groups > 1: per (session, KV head, cluster) the cluster's (m, l, o) of the G d outputs, fp32
+  // [B][Hkv][n_groups][3][G d], and per (session, KV head) a counter of arrived blocks (zero between
+  // launches: the last block to arrive merges and resets it)
+  float* part;
+  uint32_t* arrivals;
   PoolGeom pool;
   const StepArgs* step;
   // 0: row b appends its own token (position pos[b]) and attends to 0 .. pos[b].
   // 1: the rows are consecutive new tokens of one session (pos[b] = pos[0] + b) whose keys and values an
   //    earlier kernel stored; row b attends causally to 0 .. pos[b] and appends nothing.
   int32_t stored;
+  // 0: 4 warps per block (two blocks per SM); 1: the wide variant, 8 warps per block at head_dim 128
+  // (16 at 64), one block per SM, for long contexts
+  int32_t wide;
 };
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch);
-// Largest split count (cluster size) the device can co-schedule for this head size and KV type.
-cudaError_t attention_max_cluster(int head_dim, int kv_dtype, int* out);
+constexpr int kAttnMaxGroups = 8;
+// Largest split count (cluster size) the device can co-schedule for this head size, KV type and variant.
+cudaError_t attention_max_cluster(int head_dim, int kv_dtype, bool wide, int* out);
 
 // ---------------------------------------------------------------- W4 quantiser (load time)
 cudaError_t launch_quantize_w4g32(cudaStream_t s, const float* src, int64_t rows, int64_t cols, uint8_t* codes,

@@ -9,7 +9,9 @@
   layers.
 * Long context, FP16 at 19,431 / INT8 at 38,863 / INT4 at 77,726 tokens (the
   capacities "5. Core modules" 5.4 prints): the full contexts and the full
-  vocabulary, on 4 of the 32 layers (every layer runs the same launches).
+  vocabulary, on 4 of the 32 layers (every layer runs the same launches); one
+  token with the default attention blocks, the next with the wide ones over
+  two clusters per KV head.
 Tolerance on fp16 logits: max-abs <= 2e-2 and rel-L2 <= 1e-3 -- except that
 after 32 random layers rel-L2 is bounded by 1.25 x the oracle's own change
 under a one-ulp change of one input value (measured in the test, about 2e-3):
@@ -194,6 +196,11 @@ def test_8b_two_layers_strict():
 def test_8b_long_context_kv_precision(dt, ctx_len):
     shape = shrink(LLAMA8B, n_layers=4)
     wl = Workload(f"8b4L-ctx{ctx_len}-kv{dt}", shape, dt, 1, (ctx_len,))
-    ctx, w = _oracle_weights_and_ctx(wl, check_bytes=False)
+    ctx, w = _oracle_weights_and_ctx(wl, check_bytes=False, extra_tokens=2)
     sids, kvs, cfg = _priors(ctx, wl)
+    _steps(ctx, w, wl, sids, kvs, cfg, 1)
+    # the next token through the long plan's wide attention blocks (8 warps per block), 32 splits as two
+    # clusters merged by the last block to finish
+    ctx.set_adaptive(True, force_plan=2, plan_splits=(4, 8, 32), plan_wide=(0, 0, 1))
+    assert ctx.profile()["plan_wide"] == 1 and ctx.profile()["plan_splits"] == 32
     _steps(ctx, w, wl, sids, kvs, cfg, 1)

@@ -2,7 +2,8 @@
 set of captured graphs each), the load profile that picks them, and the hot pool target.
 
 * Every plan forced in turn on a 3-session ragged batch (FP16 and INT4 pools), decode and verify
-  steps against the oracle: a plan changes only how attention splits the keys.
+  steps against the oracle: a plan changes only how attention splits the keys and how many warps a
+  block has (4, or the wide blocks).
 * Plans chosen by the profile (window 8, every step recorded): short-context steps switch to the short
   plan once the window is full, long-context ones to the long plan; the switch points, the profile's
   quantiles and the hot pool target agree with the oracle's window fed the same lengths; outputs
@@ -84,12 +85,13 @@ class _Run:
 def test_forced_plans_match_oracle(dt):
     wl = Workload(f"tiny-plans-kv{dt}", TINY, dt, 3, (40, 300, 1000))
     run = _Run(wl, 51 + dt, extra=20)
-    splits = (1, 3, 16)
+    # plan 2 spreads each (session, KV head) over 3 clusters of 16 (48 splits), merged by the last block
+    splits, wide = (1, 3, 48), (0, 1, 1)
     for p in (0, 1, 2, 0):
-        run.ctx.set_adaptive(True, force_plan=p, plan_splits=splits)
+        run.ctx.set_adaptive(True, force_plan=p, plan_splits=splits, plan_wide=wide)
         prof = run.ctx.profile()
-        # 16 is clamped to the device's largest co-scheduled cluster
-        assert prof["plan"] == p and (prof["plan_splits"] == splits[p] or (p == 2 and prof["plan_splits"] >= 8))
+        assert prof["plan"] == p and prof["plan_splits"] == splits[p]
+        assert prof["plan_wide"] == wide[p]
         run.decode([0, 1, 2], f"{wl.name} plan {p} decode")
         run.verify(1, 3, f"{wl.name} plan {p} verify")
     # off again: the default plan
@@ -151,7 +153,7 @@ def test_set_adaptive_argument_errors():
     wl = Workload("tiny-adapt-args", TINY, KV_FP16, 1, (10,))
     ctx, _ = driver.setup(wl, 71)
     bad = [dict(adaptive_window_size=0), dict(adaptive_sample_rate=0), dict(plan_short_below=600, plan_long_above=500),
-           dict(plan_splits=(0, 17, 0)), dict(plan_splits=(-1, 0, 0)), dict(force_plan=3),
+           dict(plan_splits=(0, 65, 0)), dict(plan_splits=(-1, 0, 0)), dict(force_plan=3),
            dict(hot_pool_slack=0.5)]
     for kw in bad:
         with pytest.raises(mag.MagError) as e:
