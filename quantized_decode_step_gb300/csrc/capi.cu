@@ -42,7 +42,7 @@ struct Session {
 
 struct GemvPlan {
   int n_cta, stages, t_max;  // pipelined kernel (batch <= kPipeMaxBatch); n_cta = 0 otherwise
-  int ks, cpc;               // k-split kernel
+  int ks, cpc, tpw;          // k-split kernel
   size_t smem;
 };
 
@@ -228,10 +228,14 @@ GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
     p.cpc = n_chunks;
     return p;
   }
-  (void)n_mtiles;
   const int max_cpc = std::max(1, (64 * 1024) / (B * 136) - 1);
   p.ks = (n_chunks + max_cpc - 1) / max_cpc;
   p.cpc = (n_chunks + p.ks - 1) / p.ks;
+  // tiles per warp: the fewest that keep the grid within one wave of two blocks per SM (each block
+  // stages its k-range of activations once for all its tiles)
+  const int groups = (n_mtiles + 7) / 8;
+  p.tpw = 1;
+  while (p.tpw < 4 && (int64_t)((groups + p.tpw - 1) / p.tpw) * p.ks > 2 * c->n_sm) p.tpw *= 2;
   return p;
 }
 
@@ -381,6 +385,7 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
   a.err = c->d_err;
   a.chunks_per_cta = pl.cpc;
   a.ks = pl.ks;
+  a.tpw = pl.tpw;
   a.batch = B;
   a.eps = c->cfg.rms_eps;
   a.r = c->r;

@@ -355,7 +355,9 @@ __device__ void epilogue_tile(const GemvArgs& a, int mt, const float (&acc)[2][4
 }
 
 // ------------------------------------------------------------------ K-split schedule (B > 4)
-template <int NT, int WFMT, int XSRC, int EPI>
+// Block: kWarps x TPW tiles over one k-range; warp w takes tiles mt0 + kWarps i (i < TPW) one after the
+// other, its ring running on across them, so the block's activation staging serves TPW tiles per warp.
+template <int NT, int TPW, int WFMT, int XSRC, int EPI>
 __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   using Stage = typename StageT<WFMT>::type;
   using R = Ring<WFMT>;
@@ -363,15 +365,18 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   __shared__ float s_inv[(kWarps + 1) * MAG_MAX_BATCH];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int mt = blockIdx.x * kWarps + warp;
-  const bool mt_ok = mt < a.n_mtiles;
+  const int mt0 = blockIdx.x * kWarps * TPW + warp;
+  int nv = 0;  // this warp's tiles that exist (a prefix of its TPW)
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) nv += mt0 + kWarps * i < a.n_mtiles;
   const int c0 = blockIdx.y * a.chunks_per_cta, c1 = min(c0 + a.chunks_per_cta, a.n_chunks);
-  const int n = mt_ok ? c1 - c0 : 0;
+  const int n = c1 - c0;        // chunks per tile
+  const int total = nv * n;     // (tile, chunk) pairs of this warp, tile-major
   uint8_t* ring = smem + staged_bytes(a.batch, a.chunks_per_cta) + (size_t)warp * R::kSlots * R::kSlotBytes;
 
 #pragma unroll
   for (int u = 0; u < R::kSlots; ++u) {
-    if (u < n) R::issue(ring + u * R::kSlotBytes, a, mt, c0 + u, lane);
+    if (u < total) R::issue(ring + u * R::kSlotBytes, a, mt0 + kWarps * (u / n), c0 + u % n, lane);
     cp_async_commit();
   }
 
@@ -380,8 +385,11 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
   const Staged S = stage_x<WFMT, XSRC>(a, smem, s_inv, c0, c1);
 
   float acc8[2][8] = {};
-  int si = 0;
-  for (int i = 0; i < n; ++i) {
+  float accs[TPW][2][4];
+  int si = 0, ti = 0, ci = 0;  // ring slot; tile and chunk of pair p
+  // tile and chunk of the pair kSlots ahead (the next copy), advanced without divisions
+  int qt = TPW == 1 ? 0 : R::kSlots / n, qc = TPW == 1 ? R::kSlots : R::kSlots - qt * n;
+  for (int p = 0; p < total; ++p) {
     uint8_t* slot = ring + si * R::kSlotBytes;
     if (++si == R::kSlots) si = 0;
     cp_async_wait<R::kSlots - 1>();
@@ -389,20 +397,45 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
     Stage cur;
     read_slot(cur, slot, lane);
     __syncwarp();
-    if (i + R::kSlots < n) R::issue(slot, a, mt, c0 + i + R::kSlots, lane);
+    if (p + R::kSlots < total) R::issue(slot, a, mt0 + kWarps * qt, c0 + qc, lane);
     cp_async_commit();
-    compute_chunk<NT>(cur, acc8, S, a.batch, c0 + i, g, t);
+    if (TPW > 1 && ++qc == n) {
+      qc = 0;
+      ++qt;
+    } else if (TPW == 1) {
+      ++qc;
+    }
+    compute_chunk<NT>(cur, acc8, S, a.batch, c0 + ci, g, t);
+    if (++ci == n) {  // tile ti complete
+      float acc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) tile_result(acc8[nt], acc[nt], WFMT);
+#pragma unroll
+      for (int i = 0; i < TPW; ++i)
+        if (i == ti)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) accs[i][nt][j] = acc[nt][j];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc8[nt][j] = 0.f;
+      ci = 0;
+      ++ti;
+    }
   }
   cp_async_wait<0>();
-  float acc[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) tile_result(acc8[nt], acc[nt], WFMT);
   if (a.ks > 1) {
-    if (mt_ok) {
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+      if (i >= nv) break;
+      const int mt = mt0 + kWarps * i;
       float* p = a.partial + (((size_t)blockIdx.y * a.n_mtiles + mt) * 32 + lane) * (4 * NT);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
-        *reinterpret_cast<float4*>(p + nt * 4) = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+        *reinterpret_cast<float4*>(p + nt * 4) =
+            make_float4(accs[i][nt][0], accs[i][nt][1], accs[i][nt][2], accs[i][nt][3]);
     }
     __threadfence();
     __syncthreads();
@@ -410,26 +443,33 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (mt_ok) {
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+      if (i >= nv) break;
+      const int mt = mt0 + kWarps * i;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
+        for (int j = 0; j < 4; ++j) accs[i][nt][j] = 0.f;
       for (int s = 0; s < a.ks; ++s) {
         const float* p = a.partial + (((size_t)s * a.n_mtiles + mt) * 32 + lane) * (4 * NT);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float4 v = __ldcg(reinterpret_cast<const float4*>(p + nt * 4));
-          acc[nt][0] += v.x;
-          acc[nt][1] += v.y;
-          acc[nt][2] += v.z;
-          acc[nt][3] += v.w;
+          accs[i][nt][0] += v.x;
+          accs[i][nt][1] += v.y;
+          accs[i][nt][2] += v.z;
+          accs[i][nt][3] += v.w;
         }
       }
     }
     if (tid == 0) a.counters[blockIdx.x] = 0;
   }
-  if (mt_ok) epilogue_tile<NT, EPI>(a, mt, acc, lane);
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) {
+    if (i >= nv) break;
+    epilogue_tile<NT, EPI>(a, mt0 + kWarps * i, accs[i], lane);
+  }
 }
 
 template <typename K>
@@ -455,9 +495,16 @@ cudaError_t launch_k(const Launch& L, K kern, dim3 grid, size_t smem, const Gemv
 template <int WFMT, int XSRC, int EPI>
 cudaError_t launch_sched(const Launch& L, const GemvArgs& a) {
   const size_t smem = gemv_smem_bytes(a, WFMT);
-  const dim3 grid((a.n_mtiles + kWarps - 1) / kWarps, a.ks);
-  if (a.batch > 8) return launch_k(L, gemv_ksplit_kernel<2, WFMT, XSRC, EPI>, grid, smem, a);
-  return launch_k(L, gemv_ksplit_kernel<1, WFMT, XSRC, EPI>, grid, smem, a);
+  const int tpw = a.tpw == 4 ? 4 : (a.tpw == 2 ? 2 : 1);
+  const dim3 grid((a.n_mtiles + kWarps * tpw - 1) / (kWarps * tpw), a.ks);
+  if (a.batch > 8) {
+    if (tpw == 4) return launch_k(L, gemv_ksplit_kernel<2, 4, WFMT, XSRC, EPI>, grid, smem, a);
+    if (tpw == 2) return launch_k(L, gemv_ksplit_kernel<2, 2, WFMT, XSRC, EPI>, grid, smem, a);
+    return launch_k(L, gemv_ksplit_kernel<2, 1, WFMT, XSRC, EPI>, grid, smem, a);
+  }
+  if (tpw == 4) return launch_k(L, gemv_ksplit_kernel<1, 4, WFMT, XSRC, EPI>, grid, smem, a);
+  if (tpw == 2) return launch_k(L, gemv_ksplit_kernel<1, 2, WFMT, XSRC, EPI>, grid, smem, a);
+  return launch_k(L, gemv_ksplit_kernel<1, 1, WFMT, XSRC, EPI>, grid, smem, a);
 }
 
 }  // namespace

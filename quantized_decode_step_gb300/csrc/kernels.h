@@ -30,6 +30,7 @@ struct GemvArgs {
   int32_t n_chunks;       // ceil(K / 64)
   int32_t chunks_per_cta; // k-split: k-range of one block, in chunks
   int32_t ks;             // k-split: splits (grid.y)
+  int32_t tpw;            // k-split: tiles per warp (1, 2 or 4); a block covers 8 tpw tiles
   int32_t batch;
   // activations: XSRC_F16 fp16 [B][ldx]; XSRC_RESID RMSNorm of the fp32 residual
   const __half* x;

@@ -183,6 +183,19 @@ def test_8b_agent_batch16_quantized_kv(dt):
     _steps(ctx, w, wl, sids, kvs, cfg, 1)
 
 
+@pytest.mark.parametrize("n", [8, 6])
+def test_8b_two_layers_agent_batch_k_split(n):
+    """8 and 6 sessions of the agent batch on two layers (FP16, strict bar): the k-split GEMVs with one
+    token n-tile; at 8 the gate-up takes two tiles per warp over 2 k-ranges, and at both the LM head four
+    tiles per warp with a ragged last block."""
+    base = agent_batch(SEED)
+    wl = Workload(f"8b2L-b{n}-agent-fp16", shrink(LLAMA8B, n_layers=2), KV_FP16, n, base.prior[:n],
+                  scattered_pool=True)
+    ctx, w = _oracle_weights_and_ctx(wl, check_bytes=False)
+    sids, kvs, cfg = _priors(ctx, wl)
+    _steps(ctx, w, wl, sids, kvs, cfg, 1)
+
+
 def test_8b_two_layers_strict():
     """Two of the 32 layers with the full vocabulary: the strict bar holds at this depth."""
     shape = shrink(LLAMA8B, n_layers=2)
