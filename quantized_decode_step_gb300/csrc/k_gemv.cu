@@ -405,8 +405,8 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
     } else if (TPW == 1) {
       ++qc;
     }
-    compute_chunk<NT>(cur, acc8, S, a.batch, c0 + ci, g, t);
-    if (++ci == n) {  // tile ti complete
+    compute_chunk<NT>(cur, acc8, S, a.batch, c0 + (TPW == 1 ? p : ci), g, t);
+    if (TPW > 1 && ++ci == n) {  // tile ti complete
       float acc[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) tile_result(acc8[nt], acc[nt], WFMT);
@@ -424,6 +424,15 @@ __global__ void __launch_bounds__(256) gemv_ksplit_kernel(const GemvArgs a) {
       ci = 0;
       ++ti;
     }
+  }
+  if (TPW == 1 && nv) {  // one tile: its result once the loop is done
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) tile_result(acc8[nt], acc[nt], WFMT);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) accs[0][nt][j] = acc[nt][j];
   }
   cp_async_wait<0>();
   if (a.ks > 1) {
