@@ -66,3 +66,32 @@ def test_create_without_device_reports_cuda_error(lib):
     h = ctypes.c_void_p()
     assert lib.mag_create(ctypes.byref(cfg), None, ctypes.byref(h)) == mag.ERR_CUDA
     assert not h.value
+
+
+def _c_layout(struct, fields):
+    """sizeof and offsetof of a struct of include/mag.h, from a host C program built with gcc."""
+    import subprocess
+    import tempfile
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "mag.h"', 'int main(void) {',
+             f'  printf("%zu\\n", sizeof({struct}));']
+    lines += [f'  printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    lines += ['  return 0;', '}']
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        with open(src, "w") as f:
+            f.write("\n".join(lines) + "\n")
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
+    return int(out[0]), [int(x) for x in out[1:]]
+
+
+@pytest.mark.parametrize("struct,cls", [("mag_config", "Config"), ("mag_memory_stats", "MemoryStats"),
+                                        ("mag_adapt_config", "AdaptConfig"), ("mag_profile", "Profile"),
+                                        ("mag_arena_tensor", "ArenaTensor")])
+def test_binding_structs_match_the_header(struct, cls):
+    """The ctypes mirrors of the header's structs have the C compiler's size and field offsets."""
+    c = getattr(mag, cls)
+    fields = [f for f, _ in c._fields_]
+    size, offs = _c_layout(struct, fields)
+    assert ctypes.sizeof(c) == size, (struct, ctypes.sizeof(c), size)
+    assert [getattr(c, f).offset for f in fields] == offs, struct
