@@ -91,6 +91,9 @@ def lib():
                 "orc_kv_stored": ([vp, i32, i32, i32, i32, vp, vp], i64),
                 "orc_attention": ([ctypes.POINTER(Cfg), vp, i32, i32, vp, i32, vp], None),
                 "orc_forward": ([ctypes.POINTER(Cfg), ctypes.POINTER(_Weights), i32, vp, vp, vp, vp, vp, i32, vp], i32),
+                "orc_layer": ([ctypes.POINTER(Cfg), ctypes.POINTER(_Weights), i32, i32, vp, vp, vp, vp, vp, i32, vp],
+                              i32),
+                "orc_output": ([ctypes.POINTER(Cfg), ctypes.POINTER(_Weights), vp, vp], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -421,4 +424,38 @@ def forward(cfg: ModelCfg, weights: Weights, kvs, n_tok, x_f16, rope_cos, rope_s
     del keep
     if rc != 0:
         raise RuntimeError("oracle forward: KV store full or RoPE table too short")
+    return out.view(np.float16)
+
+
+def layer(cfg: ModelCfg, weights: Weights, l: int, kvs, n_tok, r_in, rope_cos, rope_sin):
+    """Layer l alone, from the residual r_in (float64 [T, hidden], the tokens of the sequences in order) to
+    the residual after it (float64 [T, hidden]). The tokens' k and v are stored at layer l of each store at
+    positions len .. len + n_tok - 1; the stores' lengths do not change."""
+    c = cfg.c()
+    w, keep = weights.c()
+    n_seq = len(kvs)
+    hs = (ctypes.c_void_p * n_seq)(*[k.h for k in kvs])
+    nt = _c(n_tok, np.int32)
+    r = _c(r_in, np.float64)
+    out = np.empty_like(r)
+    rc_, rs_ = _c(rope_cos, np.float32), _c(rope_sin, np.float32)
+    rc = lib().orc_layer(ctypes.byref(c), ctypes.byref(w), l, n_seq, ctypes.cast(hs, ctypes.c_void_p), _p(nt),
+                         _p(r), _p(rc_), _p(rs_), rc_.shape[0], _p(out))
+    del keep
+    if rc != 0:
+        raise RuntimeError("oracle layer: KV store full or RoPE table too short")
+    return out
+
+
+def output(cfg: ModelCfg, weights: Weights, r):
+    """The output of each row of the final residual r (float64 [n, hidden]): fp16 logits [n, vocab], or the
+    fp16 hidden state [n, hidden] without an LM head."""
+    c = cfg.c()
+    w, keep = weights.c()
+    r = _c(np.atleast_2d(r), np.float64)
+    width = cfg.vocab if cfg.vocab else cfg.hidden
+    out = np.empty((r.shape[0], width), dtype=np.uint16)
+    for i in range(r.shape[0]):
+        lib().orc_output(ctypes.byref(c), ctypes.byref(w), _p(r[i]), _p(out[i]))
+    del keep
     return out.view(np.float16)

@@ -515,116 +515,146 @@ void orc_attention(const orc_cfg* cfg, const orc_kv* kv, int layer, int kv_head,
 
 /* ========================================================================== whole step */
 
-/* One pass of the pre-norm GQA decoder ([Core] 5.1: pre-norm, merged QKV,
+/* Positions of the T tokens of a pass: sequence s appends n_tok[s] tokens at
+ * len_s .. len_s + n_tok[s] - 1 (tokens ordered sequence by sequence).
+ * Returns T, or -1 if a store or the RoPE table is too short. */
+static int token_positions(int n_seq, orc_kv* const* kv, const int* n_tok, int rope_rows, int** seq_of, int** pos) {
+  int T = 0;
+  for (int s = 0; s < n_seq; ++s) {
+    if (kv[s]->len + n_tok[s] > kv[s]->cap || kv[s]->len + n_tok[s] > rope_rows) return -1;
+    T += n_tok[s];
+  }
+  *seq_of = (int*)malloc(sizeof(int) * (T > 0 ? T : 1));
+  *pos = (int*)malloc(sizeof(int) * (T > 0 ? T : 1));
+  for (int s = 0, t = 0; s < n_seq; ++s)
+    for (int i = 0; i < n_tok[s]; ++i, ++t) {
+      (*seq_of)[t] = s;
+      (*pos)[t] = kv[s]->len + i;
+    }
+  return T;
+}
+
+/* One layer of the pre-norm GQA decoder ([Core] 5.1: pre-norm, merged QKV,
  * merged gate-up, precomputed RoPE table; [Core] 5.2: KV pool written in
  * place) for n_seq sequences, sequence s appending n_tok[s] tokens at
- * positions len_s .. len_s + n_tok[s] - 1 with causal attention. n_tok = 1
- * for every sequence is the decode step; one sequence with n_tok = T is a
- * prefill chunk. Per layer, for every token:
+ * positions len_s .. len_s + n_tok[s] - 1 with causal attention. For every
+ * token, from its residual r (double):
  *   xn = rmsnorm(r, gamma1)                          fp16
  *   [q; k; v] = W_qkv xn                             fp16
  *   q, k rotated at the token's position             fp16
- *   k, v stored in the KV store (quantised there)
+ *   k, v stored in the KV store at this layer (quantised there)
  *   o_h = attention(q_h, keys 0..p of KV head h/G)   fp16   (h/G: contiguous grouping)
  *   r += W_o o
  *   xn2 = rmsnorm(r, gamma2)                         fp16
  *   [g; u] = W_gu xn2,  a = silu(g) * u              fp16
  *   r += W_down a
- * The residual r starts as the fp16 input and is carried unrounded. Output,
- * for the last token of each sequence: fp16(W_lm rmsnorm(r, gamma_f)), or
- * fp16(r) when there is no LM head. Returns 0, or -1 if a store is full or
- * the RoPE table is too short. */
-int orc_forward(const orc_cfg* cfg, const orc_weights* w, int n_seq, orc_kv* const* kv, const int* n_tok,
-                const uint16_t* x_f16, const float* rope_cos, const float* rope_sin, int rope_rows,
-                uint16_t* out_f16) {
-  int L = cfg->n_layers, D = cfg->hidden, Hq = cfg->n_heads, Hkv = cfg->n_kv_heads, d = cfg->head_dim;
-  int F = cfg->ffn, V = cfg->vocab, G = Hq / Hkv, half = d / 2;
+ * r_in and r_out are [T][D] (they may be the same array); the stores'
+ * lengths are not advanced (the pass's last layer is followed by that).
+ * Returns 0, or -1 if a store is full or the RoPE table is too short. */
+int orc_layer(const orc_cfg* cfg, const orc_weights* w, int l, int n_seq, orc_kv* const* kv, const int* n_tok,
+              const double* r_in, const float* rope_cos, const float* rope_sin, int rope_rows, double* r_out) {
+  int D = cfg->hidden, Hq = cfg->n_heads, Hkv = cfg->n_kv_heads, d = cfg->head_dim;
+  int F = cfg->ffn, G = Hq / Hkv, half = d / 2;
   int R = (Hq + 2 * Hkv) * d;
-  int T = 0;
-  for (int s = 0; s < n_seq; ++s) T += n_tok[s];
-  int* seq_of = (int*)malloc(sizeof(int) * T);
-  int* pos = (int*)malloc(sizeof(int) * T);
-  for (int s = 0, t = 0; s < n_seq; ++s) {
-    if (kv[s]->len + n_tok[s] > kv[s]->cap || kv[s]->len + n_tok[s] > rope_rows) {
-      free(seq_of);
-      free(pos);
-      return -1;
-    }
-    for (int i = 0; i < n_tok[s]; ++i, ++t) {
-      seq_of[t] = s;
-      pos[t] = kv[s]->len + i;
-    }
-  }
-  double* r = (double*)malloc(sizeof(double) * T * D);
-  for (int64_t i = 0; i < (int64_t)T * D; ++i) r[i] = h2d(x_f16[i]);
-  uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * T * (D > F ? D : F));
+  int *seq_of = NULL, *pos = NULL;
+  int T = token_positions(n_seq, kv, n_tok, rope_rows, &seq_of, &pos);
+  if (T < 0) return -1;
+  double* r = r_out;
+  if (r != r_in) memcpy(r, r_in, sizeof(double) * (size_t)T * D);
+  uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * T * D);
   double* y = (double*)malloc(sizeof(double) * (int64_t)T * (R > 2 * F ? R : 2 * F));
   uint16_t* qkv = (uint16_t*)malloc(sizeof(uint16_t) * (int64_t)T * R);
   uint16_t* o = (uint16_t*)malloc(sizeof(uint16_t) * (int64_t)T * Hq * d);
   uint16_t* a = (uint16_t*)malloc(sizeof(uint16_t) * (int64_t)T * F);
 
-  for (int l = 0; l < L; ++l) {
-    for (int t = 0; t < T; ++t) orc_rmsnorm(r + (int64_t)t * D, w->gamma1[l], D, cfg->rms_eps, xn + (int64_t)t * D);
-    orc_w4_gemv(w->wqkv[l], w->sqkv[l], R, D, T, xn, y);
-    for (int64_t i = 0; i < (int64_t)T * R; ++i) qkv[i] = orc_f64_to_f16(y[i]);
-    for (int t = 0; t < T; ++t) {
-      const float* c = rope_cos + (int64_t)pos[t] * half;
-      const float* sn = rope_sin + (int64_t)pos[t] * half;
-      uint16_t* row = qkv + (int64_t)t * R;
-      for (int h = 0; h < Hq + Hkv; ++h) orc_rope_apply(row + h * d, d, c, sn, row + h * d);
-      for (int h = 0; h < Hkv; ++h) {
-        kv_store_vec(kv[seq_of[t]], l, 0, pos[t], h, row + (Hq + h) * d);
-        kv_store_vec(kv[seq_of[t]], l, 1, pos[t], h, row + (Hq + Hkv + h) * d);
-      }
+  for (int t = 0; t < T; ++t) orc_rmsnorm(r + (int64_t)t * D, w->gamma1[l], D, cfg->rms_eps, xn + (int64_t)t * D);
+  orc_w4_gemv(w->wqkv[l], w->sqkv[l], R, D, T, xn, y);
+  for (int64_t i = 0; i < (int64_t)T * R; ++i) qkv[i] = orc_f64_to_f16(y[i]);
+  for (int t = 0; t < T; ++t) {
+    const float* c = rope_cos + (int64_t)pos[t] * half;
+    const float* sn = rope_sin + (int64_t)pos[t] * half;
+    uint16_t* row = qkv + (int64_t)t * R;
+    for (int h = 0; h < Hq + Hkv; ++h) orc_rope_apply(row + h * d, d, c, sn, row + h * d);
+    for (int h = 0; h < Hkv; ++h) {
+      kv_store_vec(kv[seq_of[t]], l, 0, pos[t], h, row + (Hq + h) * d);
+      kv_store_vec(kv[seq_of[t]], l, 1, pos[t], h, row + (Hq + Hkv + h) * d);
     }
+  }
 #pragma omp parallel for collapse(2) schedule(dynamic)
-    for (int t = 0; t < T; ++t)
-      for (int h = 0; h < Hq; ++h)
-        orc_attention(cfg, kv[seq_of[t]], l, h / G, qkv + (int64_t)t * R + h * d, pos[t] + 1,
-                      o + ((int64_t)t * Hq + h) * d);
-    orc_w4_gemv(w->wo[l], w->so[l], D, Hq * d, T, o, y);
-    for (int64_t i = 0; i < (int64_t)T * D; ++i) r[i] += y[i];
-    for (int t = 0; t < T; ++t) orc_rmsnorm(r + (int64_t)t * D, w->gamma2[l], D, cfg->rms_eps, xn + (int64_t)t * D);
-    orc_w4_gemv(w->wgu[l], w->sgu[l], 2 * F, D, T, xn, y);
-    for (int t = 0; t < T; ++t)
-      for (int j = 0; j < F; ++j) {
-        double g = y[(int64_t)t * 2 * F + j], u = y[(int64_t)t * 2 * F + F + j];
-        a[(int64_t)t * F + j] = orc_f64_to_f16(g / (1.0 + exp(-g)) * u);
-      }
-    orc_w4_gemv(w->wdown[l], w->sdown[l], D, F, T, a, y);
-    for (int64_t i = 0; i < (int64_t)T * D; ++i) r[i] += y[i];
-  }
-  for (int s = 0; s < n_seq; ++s) kv[s]->len += n_tok[s];
-
-  /* outputs of the last token of each sequence */
-  int t_last = -1;
-  for (int s = 0; s < n_seq; ++s) {
-    t_last += n_tok[s];
-    const double* rt = r + (int64_t)t_last * D;
-    if (V == 0) {
-      for (int i = 0; i < D; ++i) out_f16[(int64_t)s * D + i] = orc_f64_to_f16(rt[i]);
-      continue;
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < Hq; ++h)
+      orc_attention(cfg, kv[seq_of[t]], l, h / G, qkv + (int64_t)t * R + h * d, pos[t] + 1,
+                    o + ((int64_t)t * Hq + h) * d);
+  orc_w4_gemv(w->wo[l], w->so[l], D, Hq * d, T, o, y);
+  for (int64_t i = 0; i < (int64_t)T * D; ++i) r[i] += y[i];
+  for (int t = 0; t < T; ++t) orc_rmsnorm(r + (int64_t)t * D, w->gamma2[l], D, cfg->rms_eps, xn + (int64_t)t * D);
+  orc_w4_gemv(w->wgu[l], w->sgu[l], 2 * F, D, T, xn, y);
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < F; ++j) {
+      double g = y[(int64_t)t * 2 * F + j], u = y[(int64_t)t * 2 * F + F + j];
+      a[(int64_t)t * F + j] = orc_f64_to_f16(g / (1.0 + exp(-g)) * u);
     }
-    uint16_t* xf = xn;
-    orc_rmsnorm(rt, w->gamma_f, D, cfg->rms_eps, xf);
-    double* xd = (double*)malloc(sizeof(double) * D);
-    for (int i = 0; i < D; ++i) xd[i] = h2d(xf[i]);
-#pragma omp parallel for schedule(static)
-    for (int v = 0; v < V; ++v) {
-      const uint16_t* row = w->lm_head + (int64_t)v * D;
-      double acc = 0.0;
-      for (int i = 0; i < D; ++i) acc += h2d(row[i]) * xd[i];
-      out_f16[(int64_t)s * V + v] = orc_f64_to_f16(acc);
-    }
-    free(xd);
-  }
+  orc_w4_gemv(w->wdown[l], w->sdown[l], D, F, T, a, y);
+  for (int64_t i = 0; i < (int64_t)T * D; ++i) r[i] += y[i];
   free(seq_of);
   free(pos);
-  free(r);
   free(xn);
   free(y);
   free(qkv);
   free(o);
   free(a);
+  return 0;
+}
+
+/* Output of one token from its final residual r [D] (double): the fp16 logits
+ * W_lm xf with xf = rmsnorm(r, gamma_f) (fp16), accumulated in double and
+ * rounded once, [V]; or fp16(r) [D] when the model has no LM head. */
+void orc_output(const orc_cfg* cfg, const orc_weights* w, const double* r, uint16_t* out_f16) {
+  int D = cfg->hidden, V = cfg->vocab;
+  if (V == 0) {
+    for (int i = 0; i < D; ++i) out_f16[i] = orc_f64_to_f16(r[i]);
+    return;
+  }
+  uint16_t* xf = (uint16_t*)malloc(sizeof(uint16_t) * D);
+  orc_rmsnorm(r, w->gamma_f, D, cfg->rms_eps, xf);
+  double* xd = (double*)malloc(sizeof(double) * D);
+  for (int i = 0; i < D; ++i) xd[i] = h2d(xf[i]);
+#pragma omp parallel for schedule(static)
+  for (int v = 0; v < V; ++v) {
+    const uint16_t* row = w->lm_head + (int64_t)v * D;
+    double acc = 0.0;
+    for (int i = 0; i < D; ++i) acc += h2d(row[i]) * xd[i];
+    out_f16[v] = orc_f64_to_f16(acc);
+  }
+  free(xd);
+  free(xf);
+}
+
+/* The whole pass: the residual r of every token starts as its fp16 input and
+ * is carried unrounded through orc_layer for layers 0..L-1; then every store
+ * has grown by its n_tok, and the output of the last token of each sequence
+ * s goes to out_f16[s] (orc_output: [V], or [D] without an LM head). n_tok = 1
+ * for every sequence is the decode step; one sequence with n_tok = T is a
+ * prefill chunk. Returns 0, or -1 if a store is full or the RoPE table is too
+ * short (nothing is stored then). */
+int orc_forward(const orc_cfg* cfg, const orc_weights* w, int n_seq, orc_kv* const* kv, const int* n_tok,
+                const uint16_t* x_f16, const float* rope_cos, const float* rope_sin, int rope_rows,
+                uint16_t* out_f16) {
+  int D = cfg->hidden, V = cfg->vocab;
+  int *seq_of = NULL, *pos = NULL;
+  int T = token_positions(n_seq, kv, n_tok, rope_rows, &seq_of, &pos);
+  if (T < 0) return -1;
+  free(seq_of);
+  free(pos);
+  double* r = (double*)malloc(sizeof(double) * (size_t)T * D);
+  for (int64_t i = 0; i < (int64_t)T * D; ++i) r[i] = h2d(x_f16[i]);
+  for (int l = 0; l < cfg->n_layers; ++l) orc_layer(cfg, w, l, n_seq, kv, n_tok, r, rope_cos, rope_sin, rope_rows, r);
+  for (int s = 0; s < n_seq; ++s) kv[s]->len += n_tok[s];
+  int64_t width = V ? V : D;
+  for (int s = 0, t_last = -1; s < n_seq; ++s) {
+    t_last += n_tok[s];
+    orc_output(cfg, w, r + (int64_t)t_last * D, out_f16 + (int64_t)s * width);
+  }
+  free(r);
   return 0;
 }

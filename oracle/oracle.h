@@ -21,9 +21,11 @@
  * taken in fp32 with IEEE division and round-half-even, as the format defines.
  *
  * Parity pins: every function here is pinned by a test in tests/ against
- * closed forms, invariants, worked examples or library routines; the full
- * 32-layer step is a composition of pinned parts (its composition is pinned
- * on the one-layer shape against a model built from torch library routines).
+ * closed forms, invariants, worked examples or library routines. The step is
+ * orc_layer per layer then orc_output; its composition is pinned against
+ * models built from torch library routines: one layer, two chained layers
+ * with their own weights and caches, and the LM-head output; several
+ * sequences in one pass are pinned to the same sequences run one by one.
  */
 #ifndef MAG_ORACLE_H
 #define MAG_ORACLE_H
@@ -108,6 +110,9 @@ void orc_attention(const orc_cfg* cfg, const orc_kv* kv, int layer, int kv_head,
                    uint16_t* out_f16);
 
 /* ---- whole step ---- */
+int orc_layer(const orc_cfg* cfg, const orc_weights* w, int layer, int n_seq, orc_kv* const* kv, const int* n_tok,
+              const double* r_in, const float* rope_cos, const float* rope_sin, int rope_rows, double* r_out);
+void orc_output(const orc_cfg* cfg, const orc_weights* w, const double* r, uint16_t* out_f16);
 int orc_forward(const orc_cfg* cfg, const orc_weights* w, int n_seq, orc_kv* const* kv, const int* n_tok,
                 const uint16_t* x_f16, const float* rope_cos, const float* rope_sin, int rope_rows,
                 uint16_t* out_f16);

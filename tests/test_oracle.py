@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from synth.workloads import TINY
+from synth.workloads import TINY, shrink
 from tests.helpers import model_cfg, oracle_weights, prior_kv, rel_l2
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -369,17 +369,18 @@ def test_attention_special_cases():
 
 # ----------------------------------------------------------------------------- composition
 
-def _torch_layer_reference(shape, w, x, kprior, vprior, rope_c, rope_s):
-    """The tiny one-layer step composed from torch library routines (float64, fp16 cast points)."""
+def _torch_layer(shape, w, l, r, kprior, vprior, rope_c, rope_s):
+    """Layer l of the decode step for one token, from the float64 residual r [D], composed from torch library
+    routines (float64, fp16 cast points); kprior / vprior [p, Hkv, d] are that layer's cached keys and values.
+    Returns the float64 residual after the layer (unrounded)."""
     D, Hq, Hkv, d, F = shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn
     f16 = lambda t: t.to(torch.float16).to(torch.float64)
     deq = lambda p, sm, k: torch.from_numpy(oracle.w4g32_dequant(p, sm, k).astype(np.float64))
-    Wqkv, Wo, Wgu, Wd = (deq(w.wqkv[0], w.sqkv[0], D), deq(w.wo[0], w.so[0], Hq * d), deq(w.wgu[0], w.sgu[0], D),
-                         deq(w.wdown[0], w.sdown[0], F))
-    g1 = torch.from_numpy(w.gamma1[0].astype(np.float64))
-    g2 = torch.from_numpy(w.gamma2[0].astype(np.float64))
-    r = torch.from_numpy(x.astype(np.float64))[0]
-    p = kprior.shape[1]
+    Wqkv, Wo, Wgu, Wd = (deq(w.wqkv[l], w.sqkv[l], D), deq(w.wo[l], w.so[l], Hq * d), deq(w.wgu[l], w.sgu[l], D),
+                         deq(w.wdown[l], w.sdown[l], F))
+    g1 = torch.from_numpy(w.gamma1[l].astype(np.float64))
+    g2 = torch.from_numpy(w.gamma2[l].astype(np.float64))
+    p = kprior.shape[0]
     xn = f16(torch.nn.functional.rms_norm(r, (D,), g1, eps=shape.rms_eps))
     qkv = f16(Wqkv @ xn)
     q, k, v = qkv[:Hq * d].view(Hq, d), qkv[Hq * d:(Hq + Hkv) * d].view(Hkv, d), qkv[(Hq + Hkv) * d:].view(Hkv, d)
@@ -388,8 +389,8 @@ def _torch_layer_reference(shape, w, x, kprior, vprior, rope_c, rope_s):
     rot = lambda t: f16(torch.view_as_real(torch.complex(t[:, :d // 2], t[:, d // 2:]) *
                                            torch.complex(cos, sin)).permute(0, 2, 1).reshape(t.shape[0], d))
     q, k = rot(q), rot(k)
-    K = torch.cat([torch.from_numpy(kprior[0].astype(np.float64)), k[None]], 0)  # [p+1, Hkv, d]
-    V = torch.cat([torch.from_numpy(vprior[0].astype(np.float64)), v[None]], 0)
+    K = torch.cat([torch.from_numpy(kprior.astype(np.float64)), k[None]], 0)  # [p+1, Hkv, d]
+    V = torch.cat([torch.from_numpy(vprior.astype(np.float64)), v[None]], 0)
     Kh = K.permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)  # contiguous grouping: head h uses KV head h // G
     Vh = V.permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
     o = f16(torch.nn.functional.scaled_dot_product_attention(q[:, None, :], Kh, Vh)[:, 0, :]).reshape(-1)
@@ -397,8 +398,20 @@ def _torch_layer_reference(shape, w, x, kprior, vprior, rope_c, rope_s):
     xn2 = f16(torch.nn.functional.rms_norm(r, (D,), g2, eps=shape.rms_eps))
     gu = Wgu @ xn2
     a = f16(torch.nn.functional.silu(gu[:F]) * gu[F:])
-    r = r + Wd @ a
-    return r.to(torch.float16).numpy()
+    return r + Wd @ a
+
+
+def _torch_logits(shape, w, r):
+    """Final RMSNorm (gain gamma_f, fp16) and the fp16 LM head, float64 accumulation rounded once."""
+    gf = torch.from_numpy(w.gamma_f.astype(np.float64))
+    xf = torch.nn.functional.rms_norm(r, (shape.hidden,), gf, eps=shape.rms_eps).to(torch.float16)
+    return (torch.from_numpy(w.lm_head.astype(np.float64)) @ xf.to(torch.float64)).to(torch.float16).numpy()
+
+
+def _torch_layer_reference(shape, w, x, kprior, vprior, rope_c, rope_s):
+    """The tiny one-layer step composed from torch library routines: its fp16 output hidden state."""
+    r = torch.from_numpy(x.astype(np.float64))[0]
+    return _torch_layer(shape, w, 0, r, kprior[0], vprior[0], rope_c, rope_s).to(torch.float16).numpy()
 
 
 def test_tiny_layer_composition_matches_torch_library_model():
@@ -440,3 +453,137 @@ def test_prefill_equals_token_by_token_decode():
                 da, ma = a.stored(0, which, t, h)
                 db, mb = b.stored(0, which, t, h)
                 assert np.array_equal(da, db) and np.array_equal(ma, mb)
+
+
+def _fp16_ulps(a, b):
+    """Distance in fp16 steps between same-signed fp16 arrays (their bit patterns are ordered)."""
+    ai, bi = a.view(np.uint16).astype(np.int64), b.view(np.uint16).astype(np.int64)
+    ai = np.where(ai >= 0x8000, 0x8000 - ai, ai)
+    bi = np.where(bi >= 0x8000, 0x8000 - bi, bi)
+    return np.abs(ai - bi)
+
+
+def test_two_layer_chain_matches_torch_library_model():
+    """The layer loop: two layers, each with its own weights, gains and KV, against two torch layers chained
+    through the float64 residual ([Core] 5.1: pre-norm decoder layers in sequence)."""
+    shape = shrink(TINY, n_layers=2)
+    seed = 23
+    cfg = model_cfg(shape, oracle.KV_FP16)
+    w = oracle_weights(shape, seed, random_gain=True)
+    kp, vp = prior_kv(shape, seed, 0, 40)
+    kv = oracle.KV(cfg, 64)
+    kv.append(kp, vp)
+    x = synth.hidden_f16(seed, 1, shape.hidden)
+    c, s = oracle.rope_table(64, shape.head_dim, shape.rope_base)
+    out = oracle.forward(cfg, w, [kv], [1], x, c, s)
+    r = torch.from_numpy(x.astype(np.float64))[0]
+    for l in range(2):
+        r = _torch_layer(shape, w, l, r, kp[l], vp[l], c, s)
+    ref = r.to(torch.float16).numpy()
+    assert len(kv) == 41
+    assert rel_l2(out[0], ref) < 1e-4
+    assert np.max(np.abs(out[0].astype(np.float64) - ref.astype(np.float64))) < 4e-3
+    # a layer that read another layer's weights or cache would be far off: the second layer matters
+    r1 = _torch_layer(shape, w, 0, torch.from_numpy(x.astype(np.float64))[0], kp[0], vp[0], c, s)
+    assert rel_l2(out[0], r1.to(torch.float16).numpy()) > 1e-2
+
+
+def test_lm_head_branch_matches_torch_library_model():
+    """The output branch: logits = fp16(W_lm fp16(rmsnorm(r) gamma_f)) after two layers, against torch's
+    rms_norm and a float64 matmul; orc_output alone against the same on one residual."""
+    shape = shrink(TINY, n_layers=2, vocab=1024)
+    seed = 24
+    cfg = model_cfg(shape, oracle.KV_FP16)
+    w = oracle_weights(shape, seed, random_gain=True)
+    assert w.lm_head.shape == (1024, shape.hidden)
+    kp, vp = prior_kv(shape, seed, 0, 33)
+    kv = oracle.KV(cfg, 64)
+    kv.append(kp, vp)
+    x = synth.hidden_f16(seed, 1, shape.hidden)
+    c, s = oracle.rope_table(64, shape.head_dim, shape.rope_base)
+    out = oracle.forward(cfg, w, [kv], [1], x, c, s)[0]
+    r = torch.from_numpy(x.astype(np.float64))[0]
+    for l in range(2):
+        r = _torch_layer(shape, w, l, r, kp[l], vp[l], c, s)
+    ref = _torch_logits(shape, w, r)
+    assert out.shape == (1024,)
+    # two chained layers differ from torch's in a few fp16 roundings (rms_norm and SDPA sum in another
+    # order); those flips reach every logit, so this end-to-end bar is the tolerance's 1e-3
+    assert rel_l2(out, ref) < 1e-3
+    # the same final residual through orc_output: the logits agree to within one fp16 step (summation order)
+    got = oracle.output(cfg, w, r.numpy()[None])[0]
+    u = _fp16_ulps(got, ref)
+    assert u.max() <= 1 and np.mean(u == 0) > 0.99
+    # the gain is applied, and row v of the LM head gives logit v
+    w_plain = oracle.Weights(**{**w.__dict__, "gamma_f": np.ones(shape.hidden, np.float16)})
+    assert rel_l2(oracle.output(cfg, w_plain, r.numpy()[None])[0], ref) > 1e-2
+    w_rev = oracle.Weights(**{**w.__dict__, "lm_head": np.ascontiguousarray(w.lm_head[::-1])})
+    assert np.array_equal(oracle.output(cfg, w_rev, r.numpy()[None])[0].view(np.uint16),
+                          got[::-1].view(np.uint16))
+
+
+@pytest.mark.parametrize("dt", [oracle.KV_FP16, oracle.KV_INT4])
+def test_several_sequences_equal_separate_calls(dt):
+    """n_seq > 1: each sequence's output row and stored KV are those of the same sequence run alone, for
+    decode (one token each) and for a batched chunk (several tokens each)."""
+    shape = shrink(TINY, n_layers=2, vocab=64)
+    seed = 25
+    cfg = model_cfg(shape, dt)
+    w = oracle_weights(shape, seed)
+    priors = (5, 17, 33)
+    c, s = oracle.rope_table(64, shape.head_dim, shape.rope_base)
+    for n_tok in ((1, 1, 1), (3, 1, 2)):
+        x = synth.hidden_f16(seed, sum(n_tok), shape.hidden, tag=f"x{n_tok}")
+        together, alone = [], []
+        for i, p in enumerate(priors):
+            kp, vp = prior_kv(shape, seed, i, p)
+            for lst in (together, alone):
+                kv = oracle.KV(cfg, 64)
+                kv.append(kp, vp)
+                lst.append(kv)
+        out = oracle.forward(cfg, w, together, list(n_tok), x, c, s)
+        assert out.shape == (3, 64)
+        t0 = 0
+        for i, n in enumerate(n_tok):
+            ref = oracle.forward(cfg, w, [alone[i]], [n], x[t0:t0 + n], c, s)
+            assert np.array_equal(out[i].view(np.uint16), ref[0].view(np.uint16)), (n_tok, i)
+            assert len(together[i]) == len(alone[i]) == priors[i] + n
+            for t in range(priors[i] + n):
+                for l in range(2):
+                    for which in (0, 1):
+                        da, ma = together[i].stored(l, which, t, 1)
+                        db, mb = alone[i].stored(l, which, t, 1)
+                        assert np.array_equal(da, db) and np.array_equal(ma, mb)
+            t0 += n
+
+
+def test_forward_is_layers_then_output():
+    """orc_forward = orc_layer for each layer in turn on the carried residual, then orc_output of the last
+    token; orc_layer stores the tokens' KV at its own layer and leaves the lengths alone."""
+    shape = shrink(TINY, n_layers=2, vocab=256)
+    seed = 26
+    cfg = model_cfg(shape, oracle.KV_INT8)
+    w = oracle_weights(shape, seed, random_gain=True)
+    kp, vp = prior_kv(shape, seed, 0, 19)
+    a, b = oracle.KV(cfg, 64), oracle.KV(cfg, 64)
+    a.append(kp, vp)
+    b.append(kp, vp)
+    x = synth.hidden_f16(seed, 2, shape.hidden)
+    c, s = oracle.rope_table(64, shape.head_dim, shape.rope_base)
+    out = oracle.forward(cfg, w, [a], [2], x, c, s)
+    r = x.astype(np.float64)
+    r = oracle.layer(cfg, w, 0, [b], [2], r, c, s)
+    assert len(b) == 19
+    d0, _ = b.stored(0, 0, 19, 0)
+    d1, _ = b.stored(1, 0, 19, 0)
+    r = oracle.layer(cfg, w, 1, [b], [2], r, c, s)
+    got = oracle.output(cfg, w, r[-1:])
+    assert np.array_equal(got.view(np.uint16), out.view(np.uint16))
+    # the tokens are stored (read past the length, which was left behind)
+    for t in range(21):
+        for l in range(2):
+            for which in (0, 1):
+                da, ma = a.stored(l, which, t, 1)
+                db, mb = b.stored(l, which, t, 1)
+                assert np.array_equal(da, db) and np.array_equal(ma, mb)
+    assert not np.array_equal(d0, d1)  # each layer stored its own keys
