@@ -398,6 +398,24 @@ mag_status mag_debug_profile_step(mag_ctx* ctx, int32_t batch, const int32_t* se
                                   const void* hidden_in_dev, void* out_dev, int32_t* kinds, float* ms, int32_t cap,
                                   int32_t* n_out);
 
+/* One decode step like mag_decode_step, launched kernel by kernel (no graph, no programmatic dependent
+ * launch), that also copies the fp32 residual stream of every row into resid_dev (device memory, fp32
+ * [L+1][batch][D], caller-owned): row 0 is the input hidden state widened to fp32, row l+1 the residual
+ * after layer l (after its down projection). Lets a test check the step one layer at a time against a
+ * reference fed the same residual ([Core] 5.1: the pre-norm residual stream the layers share). The
+ * session lengths advance as in a step; synchronises the context's stream.
+ * Errors: as mag_decode_step; INVALID_ARG for a null resid_dev; TIMEOUT as mag_sync. */
+mag_status mag_debug_step_residuals(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host,
+                                    const void* hidden_in_dev, void* out_dev, void* resid_dev);
+
+/* A prefill chunk like mag_prefill_chunk, launched without programmatic dependent launch, that also copies
+ * the fp32 residual of all n_tokens rows into resid_dev (device memory, fp32 [L+1][n_tokens][D],
+ * caller-owned): row 0 the chunk's input widened to fp32, row l+1 the residuals after layer l. For checking
+ * the chunk one layer at a time against a reference ([Core] 5.1, 5.2). Synchronises the context's stream.
+ * Errors: as mag_prefill_chunk; INVALID_ARG for a null resid_dev; TIMEOUT as mag_sync. */
+mag_status mag_debug_prefill_residuals(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
+                                       void* last_out_dev, void* resid_dev);
+
 #ifdef __cplusplus
 }
 #endif

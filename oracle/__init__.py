@@ -64,6 +64,7 @@ def lib():
             L = ctypes.CDLL(_LIB)
             vp, i64, i32, f32, f64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
             sig = {
+                "orc_set_threads": ([i32], i32),
                 "orc_f64_to_f16": ([f64], ctypes.c_uint16),
                 "orc_f32_to_f16": ([f32], ctypes.c_uint16),
                 "orc_f16_to_f32": ([ctypes.c_uint16], f32),
@@ -86,6 +87,7 @@ def lib():
                 "orc_kv_destroy": ([vp], None),
                 "orc_kv_len": ([vp], i32),
                 "orc_kv_truncate": ([vp, i32], None),
+                "orc_kv_commit": ([vp, i32], i32),
                 "orc_kv_append": ([vp, i32, vp, vp], i32),
                 "orc_kv_read": ([vp, i32, i32, i32, i32, vp], None),
                 "orc_kv_stored": ([vp, i32, i32, i32, i32, vp, vp], i64),
@@ -113,6 +115,11 @@ def _c(a, dtype) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------- fp16
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's parallel loops (n < 1: every core); returns the count in use."""
+    return int(lib().orc_set_threads(int(n)))
+
 
 def f64_to_f16_bits(x: float) -> int:
     return int(lib().orc_f64_to_f16(float(x)))
@@ -380,6 +387,11 @@ class KV:
 
     def truncate(self, n: int):
         lib().orc_kv_truncate(self.h, n)
+
+    def commit(self, n: int):
+        """Make the n tokens that layer() stored past the length part of the store."""
+        if lib().orc_kv_commit(self.h, n) != 0:
+            raise RuntimeError("oracle KV: commit past the capacity")
 
     def append(self, k_f16, v_f16):
         """k, v: fp16 [L, n, Hkv, d] (already rotated)."""

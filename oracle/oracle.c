@@ -14,8 +14,17 @@
 #include "oracle.h"
 
 #include <math.h>
+#include <omp.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads of the parallel loops below (the row loops of the GEMVs and the
+ * LM head, the per-layer store loop, the per-head attention loop); n < 1
+ * restores every available core. Returns the count now in use. */
+int orc_set_threads(int n) {
+  omp_set_num_threads(n >= 1 ? n : omp_get_num_procs());
+  return omp_get_max_threads();
+}
 
 /* ========================================================================== fp16 */
 
@@ -418,6 +427,14 @@ int orc_kv_len(const orc_kv* kv) { return kv->len; }
 /* Forget every token from position len on (bookkeeping only). */
 void orc_kv_truncate(orc_kv* kv, int len) {
   if (len >= 0 && len <= kv->len) kv->len = len;
+}
+
+/* Tokens that orc_layer stored past the length (a pass run layer by layer)
+ * become part of the store: len += n. Returns 0, or -1 past the capacity. */
+int orc_kv_commit(orc_kv* kv, int n) {
+  if (n < 0 || kv->len + n > kv->cap) return -1;
+  kv->len += n;
+  return 0;
 }
 
 /* Store one fp16 vector of head_dim values in the configured KV precision. */

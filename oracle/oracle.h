@@ -64,6 +64,9 @@ typedef struct {
 
 typedef struct orc_kv orc_kv;
 
+/* ---- threads of the parallel loops (n < 1: every core); returns the count in use ---- */
+int orc_set_threads(int n);
+
 /* ---- fp16 ---- */
 uint16_t orc_f64_to_f16(double x);
 uint16_t orc_f32_to_f16(float x);
@@ -103,6 +106,7 @@ orc_kv* orc_kv_create(const orc_cfg* cfg, int capacity);
 void orc_kv_destroy(orc_kv* kv);
 int orc_kv_len(const orc_kv* kv);
 void orc_kv_truncate(orc_kv* kv, int len);
+int orc_kv_commit(orc_kv* kv, int n);
 int orc_kv_append(orc_kv* kv, int n_tok, const uint16_t* k_f16, const uint16_t* v_f16); /* [L][n][Hkv][d] */
 void orc_kv_read(const orc_kv* kv, int layer, int which, int tok, int head, float* out);
 int64_t orc_kv_stored(const orc_kv* kv, int layer, int which, int tok, int head, uint8_t* data, uint8_t* meta);

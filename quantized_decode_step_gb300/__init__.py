@@ -30,7 +30,8 @@ EXPORTED = [
     "mag_verify_tokens", "mag_prefill_batch", "mag_sync",
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
-    "mag_debug_last_step_launches", "mag_debug_profile_step",
+    "mag_debug_last_step_launches", "mag_debug_profile_step", "mag_debug_step_residuals",
+    "mag_debug_prefill_residuals",
     "mag_adapt_defaults", "mag_set_adaptive", "mag_get_profile", "mag_profiler_create", "mag_profiler_destroy",
     "mag_profiler_observe", "mag_profiler_quantile", "mag_profiler_count", "mag_plan_for", "mag_hot_pool_blocks",
 ]
@@ -127,6 +128,8 @@ def lib():
                 "mag_debug_last_step_launches": ([vp], i32),
                 "mag_debug_profile_step": ([vp, i32, P32, vp, vp, P32, ctypes.POINTER(ctypes.c_float), i32, P32],
                                            i32),
+                "mag_debug_step_residuals": ([vp, i32, P32, vp, vp, vp], i32),
+                "mag_debug_prefill_residuals": ([vp, i32, i32, vp, vp, vp], i32),
                 "mag_adapt_defaults": ([ctypes.POINTER(AdaptConfig)], None),
                 "mag_set_adaptive": ([vp, ctypes.POINTER(AdaptConfig)], i32),
                 "mag_get_profile": ([vp, ctypes.POINTER(Profile)], i32),
@@ -358,6 +361,18 @@ class Context:
         p = Profile()
         self._check(lib().mag_get_profile(self.h, ctypes.byref(p)), "mag_get_profile")
         return {n: getattr(p, n) for n, _ in Profile._fields_}
+
+    def step_residuals(self, sessions, hidden_in, out, resid):
+        """Eager step that also fills resid (device fp32 [L+1, batch, hidden]) with the residual stream:
+        row 0 the input, row l+1 after layer l."""
+        ids = (ctypes.c_int32 * len(sessions))(*sessions)
+        self._check(lib().mag_debug_step_residuals(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out),
+                                                   _ptr(resid)), "mag_debug_step_residuals")
+
+    def prefill_residuals(self, sid, n_tokens, hidden_in, last_out, resid):
+        """Prefill chunk that also fills resid (device fp32 [L+1, n_tokens, hidden]) with the residual stream."""
+        self._check(lib().mag_debug_prefill_residuals(self.h, sid, n_tokens, _ptr(hidden_in), _ptr(last_out),
+                                                      _ptr(resid)), "mag_debug_prefill_residuals")
 
     def profile_step(self, sessions, hidden_in, out, cap=4096):
         """Instrumented step: list of (op name, device ms) per kernel launch."""

@@ -403,10 +403,16 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
 // keys and values go into the pool in one store kernel after the QKV projection, and attention reads them
 // there (row b causally up to its own position) instead of each row appending its own.
 // `splits` is the attention split count of the plan in use; `st` the stream the launches go to (the
-// context's, or a capture stream).
+// context's, or a capture stream). With `resid_dump` (eager debug steps only) the fp32 residual of the B rows
+// is copied there after the step prologue and after every layer: [L+1][B][D].
 cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool verify, int splits, bool wide,
-                        cudaStream_t st) {
-  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof;
+                        cudaStream_t st, float* resid_dump = nullptr) {
+  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof && !resid_dump;
+  auto dump = [&](int row) {
+    return resid_dump ? cudaMemcpyAsync(resid_dump + (size_t)row * B * c->D, c->r, (size_t)B * c->D * 4,
+                                        cudaMemcpyDeviceToDevice, st)
+                      : cudaSuccess;
+  };
   Launch L0{st, false, n_launch};
   Launch L{st, pdl, n_launch};
   cudaError_t e;
@@ -419,6 +425,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
   } while (0)
   MAG_RUN(MAG_OP_STEP_BEGIN,
           launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B, c->ss_part));
+  if ((e = dump(0)) != cudaSuccess) return e;
   const PoolGeom pg = pool_geom(c);
   const int S = splits;
   for (int l = 0; l < c->L; ++l) {
@@ -489,6 +496,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
       a.ldx = c->F;
       MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, XSRC_F16, EPI_RESID));
     }
+    if ((e = dump(l + 1)) != cudaSuccess) return e;
   }
   if (c->V) {  // final RMSNorm + LM head
     GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, c->D, B);
@@ -1219,6 +1227,21 @@ mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, co
   return MAG_OK;
 }
 
+mag_status mag_debug_step_residuals(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out,
+                                    void* resid) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!resid) return fail(c, MAG_ERR_INVALID_ARG, "debug_step_residuals: null residual buffer");
+  mag_status st = step_upload(c, B, sids, in, out);
+  if (st != MAG_OK) return st;
+  int n = 0;
+  CUDA_TRY(c, record_step(c, B, &n, nullptr, false, plan_splits(c, c->cur_plan, B), plan_wide(c, c->cur_plan),
+                          c->stream, static_cast<float*>(resid)));
+  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  c->last_launches = n;
+  return check_err(c);
+}
+
 mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, const void* in_host, void* out_host) {
   if (!c) return MAG_ERR_INVALID_ARG;
   if (!in_host || !out_host) return fail(c, MAG_ERR_INVALID_ARG, "decode_step_host: null buffer");
@@ -1240,8 +1263,10 @@ namespace {
 // One prefill chunk of n_seg sessions: session sids[i] appends ntok[i] tokens, the rows of the sessions
 // following each other in `in` ([sum ntok][D]); each session's tokens attend causally to its own cache.
 // Output: with all_rows (one session), every row; otherwise the last row of every session, in order.
+// With resid_dump (debug) the launches run without programmatic dependent launch and the fp32 residual of
+// the T rows is copied there after the input and after every layer: [L+1][T][D].
 mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sids, const int32_t* ntok,
-                     const void* in, void* out, bool all_rows) {
+                     const void* in, void* out, bool all_rows, float* resid_dump = nullptr) {
   if (!c) return MAG_ERR_INVALID_ARG;
   if (c->cfg.max_chunk <= 0) return fail(c, MAG_ERR_UNSUPPORTED, "%s: created with max_chunk = 0", what);
   if (!in || !out || !sids || !ntok) return fail(c, MAG_ERR_INVALID_ARG, "%s: null buffer", what);
@@ -1315,11 +1340,17 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
   int32_t* row = c->d_tables + (size_t)sids[0] * c->table_stride;
 
   int n = 0;
-  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL);
+  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !resid_dump;
   Launch L{c->stream, pdl, &n};
   const int D = c->D, HD = c->Hq * c->d;
   const PoolGeom pg = pool_geom(c);
+  auto dump = [&](int i) {
+    return resid_dump ? cudaMemcpyAsync(resid_dump + (size_t)i * T * D, c->pf_r, (size_t)T * D * 4,
+                                        cudaMemcpyDeviceToDevice, c->stream)
+                      : cudaSuccess;
+  };
   CUDA_TRY(c, launch_rows_to_resid(L, (const __half*)in, c->pf_r, T, D));
+  CUDA_TRY(c, dump(0));
   for (int l = 0; l < c->L; ++l) {
     const auto* pp = &c->pproj[(size_t)l * 4];
     TcGemmArgs g = {};
@@ -1388,6 +1419,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
     gd.r = c->pf_r;
     gd.ldr = D;
     CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_act, pp[3].map_hi, pp[3].map_lo}, gd, EPI_RESID));
+    CUDA_TRY(c, dump(l + 1));
   }
   // the output rows: contiguous for one session, else each session's last row gathered
   float* r_out = c->pf_r + (size_t)(T - out_rows) * D;
@@ -1414,6 +1446,17 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
 
 mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out) {
   return run_chunk(c, "prefill_chunk", 1, &sid, &T, in, last_out, false);
+}
+
+mag_status mag_debug_prefill_residuals(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out,
+                                       void* resid) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!resid) return fail(c, MAG_ERR_INVALID_ARG, "debug_prefill_residuals: null residual buffer");
+  mag_status st = run_chunk(c, "debug_prefill_residuals", 1, &sid, &T, in, last_out, false,
+                            static_cast<float*>(resid));
+  if (st != MAG_OK) return st;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return check_err(c);
 }
 
 mag_status mag_prefill_batch(mag_ctx* c, int32_t n_sessions, const int32_t* sids, const int32_t* n_tokens,

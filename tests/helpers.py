@@ -79,3 +79,21 @@ def one_ulp_floor(run_oracle, x_f16, n=3):
         rows[:, (977 * i + 101) % rows.shape[1]] += 1
         vals.append(rel_l2(run_oracle(x2.reshape(x_f16.shape)), base))
     return float(np.mean(vals)), base
+
+
+def fp16_ulps(a, b):
+    """Distance in fp16 steps between fp16 arrays (sign-magnitude bit patterns mapped onto one ordered line)."""
+    ai = np.asarray(a, np.float16).view(np.uint16).astype(np.int64)
+    bi = np.asarray(b, np.float16).view(np.uint16).astype(np.int64)
+    ai = np.where(ai >= 0x8000, 0x8000 - ai, ai)
+    bi = np.where(bi >= 0x8000, 0x8000 - bi, bi)
+    return np.abs(ai - bi)
+
+
+def device_bytes(ptr, nbytes):
+    """A uint8 CUDA tensor copy of `nbytes` at device address `ptr` (read through the CUDA array interface)."""
+    import torch
+
+    class _Arr:
+        __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+    return torch.as_tensor(_Arr(), device="cuda").clone()

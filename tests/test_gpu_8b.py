@@ -8,15 +8,20 @@
   scattered through a shared pool; the same with INT8 and INT4 KV on two
   layers.
 * Long context, FP16 at 19,431 / INT8 at 38,863 / INT4 at 77,726 tokens (the
-  capacities "5. Core modules" 5.4 prints): the full contexts and the full
-  vocabulary, on 4 of the 32 layers (every layer runs the same launches); one
-  token with the default attention blocks, the next with the wide ones over
-  two clusters per KV head.
-Tolerance on fp16 logits: max-abs <= 2e-2 and rel-L2 <= 1e-3 -- except that
-after 32 random layers rel-L2 is bounded by 1.25 x the oracle's own change
-under a one-ulp change of one input value (measured in the test, about 2e-3):
-no implementation that differs from the oracle in a single fp16 rounding can
-do better than that floor.
+  capacities "5. Core modules" 5.4 prints): the full contexts, all 32 layers
+  and the full vocabulary; one token with the default attention blocks, the
+  next with the wide ones over two clusters per KV head.
+* Layer by layer (teacher forced): the step's fp32 residual after every layer
+  is read back (mag_debug_step_residuals) and the oracle runs each layer alone
+  from the GPU's residual at that layer's input; every layer's output hidden
+  state and its own contribution (output minus input), and the logits from the
+  GPU's final residual, are held to the strict bar. The graph-replayed step
+  the bench times gives the same logits, bit for bit, as that eager step.
+Tolerance on fp16 logits and hidden states: max-abs <= 2e-2 and rel-L2 <= 1e-3
+-- except that for the logits of the whole 32-layer step (not teacher forced)
+rel-L2 is bounded by 1.25 x the oracle's own change under a one-ulp change of
+one input value (measured in the test, about 2e-3): no implementation that
+differs from the oracle in a single fp16 rounding can do better than that floor.
 """
 import numpy as np
 import pytest
@@ -154,6 +159,65 @@ def _steps(ctx, w, wl, sids, kvs, cfg, n_steps, seed=SEED, floor_check=False):
     return res
 
 
+def _layerwise_step(ctx, w, wl, sids, kvs, cfg, step, seed=SEED, graph_check=True):
+    """One decode step through mag_debug_step_residuals, checked layer by layer against the oracle fed the
+    GPU's residual at each layer's input; then the logits from the GPU's final residual. With graph_check
+    the sessions are cut back and the same step is replayed through the captured graph (the bench's launch
+    path): its logits must equal the eager step's bit for bit."""
+    shape, B = wl.shape, wl.batch
+    L, D = shape.n_layers, shape.hidden
+    rows = max(wl.prior) + step + 2
+    c, s = oracle.rope_table(rows, shape.head_dim, shape.rope_base)
+    x = driver.step_inputs(wl, seed, step)
+    xt = torch.from_numpy(x).cuda()
+    out = torch.empty((B, shape.vocab), dtype=torch.float16, device="cuda")
+    resid = torch.empty((L + 1, B, D), dtype=torch.float32, device="cuda")
+    lens = [ctx.session_length(sid) for sid in sids]
+    ctx.step_residuals(sids, xt, out, resid)
+    R = resid.cpu().numpy().astype(np.float64)
+    got = out.cpu().numpy()
+    assert np.array_equal(R[0], x.astype(np.float64)), "row 0 is the fp16 input"
+    worst = [0.0, 0.0, 0.0]
+    for l in range(L):
+        ref = oracle.layer(cfg, w, l, kvs, [1] * B, R[l], c, s)
+        ma, rl = max_abs(R[l + 1], ref), rel_l2(R[l + 1], ref)
+        dl = rel_l2(R[l + 1] - R[l], ref - R[l])  # the layer's own contribution
+        worst = [max(worst[0], ma), max(worst[1], rl), max(worst[2], dl)]
+        assert ma <= TOL_MAX_ABS and rl <= TOL_REL_L2 and dl <= TOL_REL_L2, (wl.name, step, l, ma, rl, dl)
+    for kv in kvs:
+        kv.commit(1)
+    ref = oracle.output(cfg, w, R[L]).astype(np.float64)
+    ma, rl = max_abs(got, ref), rel_l2(got, ref)
+    print(f"{wl.name} step {step} layer by layer: hidden max-abs {worst[0]:.2e} rel-L2 {worst[1]:.2e}, "
+          f"layer contribution rel-L2 {worst[2]:.2e} (worst of {L}); logits max-abs {ma:.2e} rel-L2 {rl:.2e}")
+    assert ma <= TOL_MAX_ABS and rl <= TOL_REL_L2, (wl.name, step, "logits", ma, rl)
+    if graph_check:
+        for sid, n in zip(sids, lens):
+            ctx.session_truncate(sid, n)
+        out2 = torch.empty_like(out)
+        ctx.decode_step(sids, xt, out2)
+        ctx.sync()
+        assert torch.equal(out2.view(torch.int16), out.view(torch.int16)), "graph step differs from the eager step"
+    return worst, (ma, rl)
+
+
+def test_8b_layerwise_decode_b1_ctx2048_fp16():
+    """The bench's configuration, all 32 layers, teacher forced at the strict bar; two steps."""
+    wl = DECODE_8B
+    ctx, w = _oracle_weights_and_ctx(wl, extra_tokens=3)
+    sids, kvs, cfg = _priors(ctx, wl)
+    for step in range(2):
+        _layerwise_step(ctx, w, wl, sids, kvs, cfg, step)
+
+
+def test_8b_layerwise_agent_batch16():
+    """The agent batch (16 sessions, contexts 20..2048, scattered pool), all 32 layers, teacher forced."""
+    wl = agent_batch(SEED)
+    ctx, w = _oracle_weights_and_ctx(wl, extra_tokens=2)
+    sids, kvs, cfg = _priors(ctx, wl)
+    _layerwise_step(ctx, w, wl, sids, kvs, cfg, 0)
+
+
 def test_8b_decode_b1_ctx2048_fp16():
     wl = DECODE_8B
     ctx, w = _oracle_weights_and_ctx(wl, extra_tokens=2)
@@ -207,13 +271,13 @@ def test_8b_two_layers_strict():
 
 @pytest.mark.parametrize("dt,ctx_len", [(KV_FP16, 19431), (KV_INT8, 38863), (KV_INT4, 77726)])
 def test_8b_long_context_kv_precision(dt, ctx_len):
-    shape = shrink(LLAMA8B, n_layers=4)
-    wl = Workload(f"8b4L-ctx{ctx_len}-kv{dt}", shape, dt, 1, (ctx_len,))
+    """The long-context configurations at full size (32 layers, full vocabulary), teacher forced layer by
+    layer: one token with the default attention blocks, the next through the long plan's wide blocks with
+    32 splits as two clusters merged by the last block to finish."""
+    wl = Workload(f"8b-ctx{ctx_len}-kv{dt}", LLAMA8B, dt, 1, (ctx_len,))
     ctx, w = _oracle_weights_and_ctx(wl, check_bytes=False, extra_tokens=2)
     sids, kvs, cfg = _priors(ctx, wl)
-    _steps(ctx, w, wl, sids, kvs, cfg, 1)
-    # the next token through the long plan's wide attention blocks (8 warps per block), 32 splits as two
-    # clusters merged by the last block to finish
+    _layerwise_step(ctx, w, wl, sids, kvs, cfg, 0)
     ctx.set_adaptive(True, force_plan=2, plan_splits=(4, 8, 32), plan_wide=(0, 0, 1))
     assert ctx.profile()["plan_wide"] == 1 and ctx.profile()["plan_splits"] == 32
-    _steps(ctx, w, wl, sids, kvs, cfg, 1)
+    _layerwise_step(ctx, w, wl, sids, kvs, cfg, 1)

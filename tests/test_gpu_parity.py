@@ -12,7 +12,7 @@ import quantized_decode_step_gb300 as mag
 import synth
 from synth import driver
 from synth.workloads import KV_FP16, KV_INT4, KV_INT8, TINY, TINY_DECODE, Workload, shrink
-from tests.helpers import TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, rel_l2
+from tests.helpers import TOL_MAX_ABS, TOL_REL_L2, device_bytes, max_abs, model_cfg, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -166,7 +166,7 @@ def test_kv_append_bytes_and_placement_bit_exact(dt):
     ptr, nbytes = ctx.debug_pool()
     assert nbytes == 2 * P * oracle.kv_block_bytes(2, 64, dt)
     torch.cuda.synchronize()
-    host = _device_bytes(ptr, nbytes).cpu().numpy()
+    host = device_bytes(ptr, nbytes).cpu().numpy()
     H, d = 2, 64
     for sid, kv, n in kvs:
         for t in range(n):
@@ -184,13 +184,6 @@ def test_kv_append_bytes_and_placement_bit_exact(dt):
                             moff = oracle.kv_offset(H, d, dt, 16, P, l, blk, 2 + which, h, slot)
                             assert moff == loc[2 + which] + h * 16 * len(meta)
                             assert np.array_equal(host[moff:moff + len(meta)], meta), (sid, t, l, h, which)
-
-
-def _device_bytes(ptr, nbytes):
-    """A uint8 CUDA tensor copy of `nbytes` at device address `ptr` (read through the CUDA array interface)."""
-    class _Arr:
-        __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
-    return torch.as_tensor(_Arr(), device="cuda").clone()
 
 
 def test_arena_plan_offsets_match_oracle():

@@ -15,7 +15,7 @@ import torch
 import oracle
 import synth
 from synth.workloads import TINY, shrink
-from tests.helpers import model_cfg, oracle_weights, prior_kv, rel_l2
+from tests.helpers import fp16_ulps, model_cfg, oracle_weights, prior_kv, rel_l2
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -455,14 +455,6 @@ def test_prefill_equals_token_by_token_decode():
                 assert np.array_equal(da, db) and np.array_equal(ma, mb)
 
 
-def _fp16_ulps(a, b):
-    """Distance in fp16 steps between same-signed fp16 arrays (their bit patterns are ordered)."""
-    ai, bi = a.view(np.uint16).astype(np.int64), b.view(np.uint16).astype(np.int64)
-    ai = np.where(ai >= 0x8000, 0x8000 - ai, ai)
-    bi = np.where(bi >= 0x8000, 0x8000 - bi, bi)
-    return np.abs(ai - bi)
-
-
 def test_two_layer_chain_matches_torch_library_model():
     """The layer loop: two layers, each with its own weights, gains and KV, against two torch layers chained
     through the float64 residual ([Core] 5.1: pre-norm decoder layers in sequence)."""
@@ -512,7 +504,7 @@ def test_lm_head_branch_matches_torch_library_model():
     assert rel_l2(out, ref) < 1e-3
     # the same final residual through orc_output: the logits agree to within one fp16 step (summation order)
     got = oracle.output(cfg, w, r.numpy()[None])[0]
-    u = _fp16_ulps(got, ref)
+    u = fp16_ulps(got, ref)
     assert u.max() <= 1 and np.mean(u == 0) > 0.99
     # the gain is applied, and row v of the LM head gives logit v
     w_plain = oracle.Weights(**{**w.__dict__, "gamma_f": np.ones(shape.hidden, np.float16)})
@@ -587,3 +579,10 @@ def test_forward_is_layers_then_output():
                 db, mb = b.stored(l, which, t, 1)
                 assert np.array_equal(da, db) and np.array_equal(ma, mb)
     assert not np.array_equal(d0, d1)  # each layer stored its own keys
+    # committed, the layer-by-layer store continues like the forward's
+    b.commit(2)
+    assert len(b) == len(a) == 21
+    x1 = synth.hidden_f16(seed, 1, shape.hidden, tag="next")
+    o_a = oracle.forward(cfg, w, [a], [1], x1, c, s)
+    o_b = oracle.forward(cfg, w, [b], [1], x1, c, s)
+    assert np.array_equal(o_a.view(np.uint16), o_b.view(np.uint16))
