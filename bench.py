@@ -28,13 +28,13 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from synth import pool_order  # noqa: E402
 from synth.workloads import (DECODE_8B, LLAMA8B, LONG_FP16, LONG_INT4, LONG_INT8, KV_FP16, KV_INT4, KV_INT8,  # noqa
                              PREFILL_8B,
                              Workload, agent_batch, shrink)
 
 METRIC = "decode tokens/s per GB300 and achieved HBM GB/s (% of peak) per decode step"
 UNIT = "tokens/s"
-CPU_SAMPLE_LAYERS = 2
 
 
 def workload_by_name(name: str, seed: int) -> Workload:
@@ -163,74 +163,117 @@ def reduce_job(world, elapsed_s: float, units: float):
 
 # ============================================================================ oracle (CPU) leg
 
-def oracle_sample_setup(wl: Workload, seed: int, lm_head=None):
-    """The oracle on a bounded sample of the workload: the first CPU_SAMPLE_LAYERS layers (with their full
-    weights and KV) and, separately, the final norm + full LM head."""
-    import oracle
-    import synth
-    from tests.helpers import model_cfg, oracle_weights
-    s = wl.shape
-    part = shrink(s, n_layers=CPU_SAMPLE_LAYERS, vocab=0)
-    w_layers = oracle_weights(part, seed)
-    cfg_layers = model_cfg(part, wl.kv_dtype)
-    kvs = []
-    for i, p in enumerate(wl.prior):
-        kv = oracle.KV(cfg_layers, p + 1)
-        L, H, d = part.n_layers, s.n_kv_heads, s.head_dim
-        k = np.empty((L, p, H, d), np.float16)
-        v = np.empty((L, p, H, d), np.float16)
-        for l in range(L):
-            k[l] = synth.prior_kv_f16(seed, i, l, "K", p, H, d)
-            v[l] = synth.prior_kv_f16(seed, i, l, "V", p, H, d)
-        kv.append(k, v)
-        kvs.append(kv)
-    head = shrink(s, n_layers=0)
-    w_head = oracle.Weights(gamma_f=synth.norm_gain_f16(seed, "gf", s.hidden),
-                            lm_head=lm_head if lm_head is not None else synth.lm_head_f16(seed, s.vocab, s.hidden))
-    cfg_head = model_cfg(head, wl.kv_dtype)
-    rope = oracle.rope_table(max(wl.prior) + 64, s.head_dim, s.rope_base)
-    return dict(part=part, w_layers=w_layers, cfg_layers=cfg_layers, kvs=kvs, w_head=w_head, cfg_head=cfg_head,
-                rope=rope, head_kv=[oracle.KV(cfg_head, 1) for _ in wl.prior], prior=list(wl.prior))
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
-def oracle_sample_step(wl: Workload, st: dict, seed: int, step: int):
-    """Seconds of CPU for one full decode step, scaled from the sample: layers x (L / sample layers) + head."""
-    import oracle
-    from synth import driver
-    x = driver.step_inputs(wl, seed, step)
-    for kv, p in zip(st["kvs"], st["prior"]):  # every step sees exactly the workload's prior context
-        kv.truncate(p)
-    for kv in st["head_kv"]:
-        kv.truncate(0)
-    t0 = time.perf_counter()
-    oracle.forward(st["cfg_layers"], st["w_layers"], st["kvs"], [1] * wl.batch, x, *st["rope"])
-    t1 = time.perf_counter()
-    oracle.forward(st["cfg_head"], st["w_head"], st["head_kv"], [1] * wl.batch, x, *st["rope"])
-    t2 = time.perf_counter()
-    return (t1 - t0) * wl.shape.n_layers / CPU_SAMPLE_LAYERS + (t2 - t1)
+class OracleStep:
+    """The oracle running whole decode steps of a workload (every layer, the full LM head), on a chosen
+    number of host threads. Every step sees exactly the workload's prior context: the stores are cut back
+    to it before each step."""
+
+    def __init__(self, wl: Workload, seed: int):
+        import oracle
+        import synth
+        from tests.helpers import model_cfg, oracle_weights
+        self.wl, self.seed = wl, seed
+        s = wl.shape
+        t0 = time.perf_counter()
+        self.w = oracle_weights(s, seed)
+        self.cfg = model_cfg(s, wl.kv_dtype)
+        self.kvs = []
+        L, H, d = s.n_layers, s.n_kv_heads, s.head_dim
+        for i, p in enumerate(wl.prior):
+            kv = oracle.KV(self.cfg, p + 1)
+            for t0_ in range(0, p, 4096):
+                n = min(4096, p - t0_)
+                k = np.empty((L, n, H, d), np.float16)
+                v = np.empty((L, n, H, d), np.float16)
+                for l in range(L):
+                    k[l] = synth.prior_kv_f16(seed, i, l, "K", n, H, d, tok0=t0_)
+                    v[l] = synth.prior_kv_f16(seed, i, l, "V", n, H, d, tok0=t0_)
+                kv.append(k, v)
+            self.kvs.append(kv)
+        self.rope = oracle.rope_table(max(wl.prior) + 2, s.head_dim, s.rope_base)
+        self.setup_s = time.perf_counter() - t0
+
+    def step(self, step: int, threads: int = 0) -> float:
+        """Seconds of one whole step on `threads` threads (0: every core)."""
+        import oracle
+        from synth import driver
+        x = driver.step_inputs(self.wl, self.seed, step)
+        for kv, p in zip(self.kvs, self.wl.prior):
+            kv.truncate(p)
+        oracle.set_threads(threads)
+        try:
+            t0 = time.perf_counter()
+            oracle.forward(self.cfg, self.w, self.kvs, [1] * self.wl.batch, x, *self.rope)
+            return time.perf_counter() - t0
+        finally:
+            oracle.set_threads(0)
 
 
 def cpu_cores():
     try:
-        return len(os.sched_getaffinity(0))
+        import oracle
+        return oracle.set_threads(0)
     except Exception:
-        return os.cpu_count() or 1
+        try:
+            return len(os.sched_getaffinity(0))
+        except Exception:
+            return os.cpu_count() or 1
 
 
-def sample_text(wl):
-    return (f"{CPU_SAMPLE_LAYERS} of {wl.shape.n_layers} layers (full weights, full {'/'.join(map(str, wl.prior))}"
-            f"-token KV) timed and scaled x{wl.shape.n_layers // CPU_SAMPLE_LAYERS}, plus the final norm and full "
-            f"{wl.shape.vocab}-row LM head, per decode step of batch {wl.batch}")
+def cpu_baseline_leg(wl: Workload, seed: int, timed: int = 3) -> dict:
+    """The oracle as it stands on this host: whole steps of the workload on every core (one untimed, then
+    `timed` steps; the median is the value), and one whole step on a single thread; the same for the tiny
+    one-layer configuration."""
+    from synth.workloads import TINY_DECODE
+    st = OracleStep(wl, seed)
+    st.step(0)
+    ts = [st.step(1 + i) for i in range(timed)]
+    s_med = statistics.median(ts)
+    one = st.step(1 + timed, threads=1)
+    tiny = OracleStep(TINY_DECODE, seed)
+    tiny.step(0)
+    tiny_all = statistics.median([tiny.step(1 + i) for i in range(5)])
+    tiny_one = statistics.median([tiny.step(1 + i, threads=1) for i in range(5)])
+    cores = cpu_cores()
+    return {"value": wl.batch / s_med, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{timed} whole decode steps of {wl.name} ({wl.shape.n_layers} layers, full "
+                       f"{'/'.join(map(str, wl.prior))}-token KV, full {wl.shape.vocab}-row LM head), "
+                       f"median; not scaled"),
+            "s_per_step": s_med, "s_per_step_all": ts, "cpu_model": cpu_model(),
+            "one_thread": {"s_per_step": one, "value": wl.batch / one, "unit": UNIT},
+            "tiny": {"workload": TINY_DECODE.name, "us_per_step": tiny_all * 1e6, "cores": cores,
+                     "us_per_step_one_thread": tiny_one * 1e6},
+            "setup_s": st.setup_s}
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the oracle (the pages print no code to install), whole steps of the workload."""
     if rank != 0:
         return
     wl = workload_by_name(args.workload, args.seed)
-    st = oracle_sample_setup(wl, args.seed)
+    st = OracleStep(wl, args.seed)
     for i in range(args.warmup):
-        oracle_sample_step(wl, st, args.seed, i)
-    ts = [oracle_sample_step(wl, st, args.seed, args.warmup + i) for i in range(args.steps)]
+        st.step(i)
+    ts = [st.step(args.warmup + i) for i in range(args.steps)]
     total = sum(ts)
     value = wl.batch * args.steps / total
     cores = cpu_cores()
@@ -239,8 +282,12 @@ def run_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) KV and inputs)",
             "config": {"workload": wl.name, "batch": wl.batch, "context": list(wl.prior), "kv_dtype": wl.kv_dtype},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text(wl)},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} whole decode steps of {wl.name} (every layer, full KV and "
+                                       f"LM head), not scaled", "cpu_model": cpu_model(),
+                             "ms_per_step_median": 1e3 * statistics.median(ts)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "setup_s": st.setup_s}
     print(json.dumps(line), flush=True)
 
 
@@ -263,11 +310,104 @@ def traffic_from_profile(kernel_key: str):
         return None
 
 
-def run_gpu(args, world, rank, local):
+def pct(ms):
+    """Median, p10 and p90 of replay times (ms)."""
+    a = np.asarray(ms, np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "n": int(a.size)}
+
+
+def replay_times(ctx, stream, sids, lens, x, out, n):
+    """Device time of n graph-replayed decode steps, each bracketed by its own CUDA event pair on the
+    context's stream; the sessions are cut back to their prior lengths after every step, so each replay
+    is the same workload. Steps are enqueued back to back."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        ctx.decode_step(sids, x, out)
+        b.record(stream)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def open_with_priors(ctx, stream, wl: Workload, seed: int):
+    """Open one session per prior context of the workload and append its seeded prior K/V."""
+    import torch
+    from synth import driver
+    sids = []
+    with torch.cuda.stream(stream):
+        for i, p in enumerate(wl.prior):
+            sid = ctx.session_open()
+            driver.append_prior(ctx, sid, wl.shape, seed, i, p)
+            sids.append(sid)
+    stream.synchronize()
+    return sids
+
+
+def clone_weights(src, dst, shape, seed, stream):
+    """Load dst with src's weights: every W4 projection read back in W4G32 bytes and loaded packed (no
+    second draw and quantisation), the norm gains and the LM head drawn again from the same seed."""
     import torch
     import quantized_decode_step_gb300 as mag
     import synth
-    from synth import driver, hidden_f16, pool_order
+    from synth import driver
+    with torch.cuda.stream(stream):
+        for l in range(shape.n_layers):
+            for name, tid in driver.PROJ:
+                n, k = driver.proj_shape(shape, name)
+                nb = n * (-(-k // 32)) * 20
+                buf = torch.empty(nb, dtype=torch.uint8, device="cuda")
+                src.debug_read_weights(tid, l, buf, nb)
+                dst.load_weights(tid, l, buf, mag.FMT_W4G32, nb)
+                stream.synchronize()
+            for tag, tid in ((f"L{l}.g1", mag.NORM_ATTN), (f"L{l}.g2", mag.NORM_FFN)):
+                g = torch.from_numpy(synth.norm_gain_f16(seed, tag, shape.hidden)).cuda()
+                dst.load_weights(tid, l, g, mag.FMT_F16, g.numel() * 2)
+        g = torch.from_numpy(synth.norm_gain_f16(seed, "gf", shape.hidden)).cuda()
+        dst.load_weights(mag.NORM_FINAL, 0, g, mag.FMT_F16, g.numel() * 2)
+        if shape.vocab:
+            lm = torch.from_numpy(synth.lm_head_f16(seed, shape.vocab, shape.hidden)).cuda()
+            dst.load_weights(mag.LM_HEAD, 0, lm, mag.FMT_F16, lm.numel() * 2)
+    stream.synchronize()
+
+
+def decode_config(ctx, stream, wl: Workload, seed: int, hbm: float, n_replays: int, sids=None) -> dict:
+    """One decode configuration on a loaded context: median / p10 / p90 of graph replays, tokens/s and the
+    fraction of the measured HBM bandwidth the step's algorithmic bytes reach at the median."""
+    import torch
+    import synth
+    if sids is None:
+        sids = open_with_priors(ctx, stream, wl, seed)
+    B, shape = wl.batch, wl.shape
+    with torch.cuda.stream(stream):
+        x = torch.from_numpy(synth.hidden_f16(seed, B, shape.hidden, tag="x.step0")).cuda()
+        out = torch.empty((B, shape.vocab or shape.hidden), dtype=torch.float16, device="cuda")
+    lens = list(wl.prior)
+    replay_times(ctx, stream, sids, lens, x, out, 5)
+    ms = replay_times(ctx, stream, sids, lens, x, out, n_replays)
+    st = pct(ms)
+    sb = step_bytes(wl)
+    row = {"workload": wl.name, "batch": B, "kv_dtype": wl.kv_dtype, "replays": st,
+           "ms_per_step": st["median"], "tokens_per_s": B / (st["median"] / 1e3), "step_bytes": sb,
+           "hbm_gbs": sb / (st["median"] / 1e3) / 1e9, "hbm_frac": sb / (st["median"] / 1e3) / 1e9 / hbm,
+           "launches_per_step": ctx.last_step_launches()}
+    if wl.shape.vocab == 0:
+        row["us_per_step"] = st["median"] * 1e3
+    if B > 1 or len(set(wl.prior)) > 1:
+        row["context"] = list(wl.prior)
+    else:
+        row["context"] = wl.prior[0]
+    return row
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import quantized_decode_step_gb300 as mag
+    from synth import driver, hidden_f16
+    from synth.workloads import TINY_DECODE
 
     torch.cuda.set_device(local)
     mag.build()
@@ -276,50 +416,43 @@ def run_gpu(args, world, rank, local):
         from dataclasses import replace as _replace
         wl = _replace(wl, name=wl.name + f"-{args.layers}layers", shape=shrink(wl.shape, n_layers=args.layers))
     shape = wl.shape
-    n_runs = args.warmup + args.steps
+    hbm, tc, peak_src = measured_peaks()
     e2e_steps = max(3, min(args.steps, 10))
     prof_steps = 3
-    n_sets = n_runs + e2e_steps + prof_steps  # session sets: one fresh set per step
     B = wl.batch
-    n_sess = n_sets * B
-    blocks = n_sets * sum(-(-(p + 1) // 16) for p in wl.prior)
+    # the headline workload's sessions are reused: after every step they are cut back to their prior length
+    long_fp16 = None
+    if not args.no_configs and wl.name == DECODE_8B.name and not args.layers:
+        long_fp16 = LONG_FP16  # same weights, KV precision and pool order: shares the context
+    max_ctx = max(wl.prior) + 1 if long_fp16 is None else max(max(wl.prior), max(long_fp16.prior)) + 1
+    blocks = sum(-(-(p + 1) // 16) for p in wl.prior)
+    if long_fp16 is not None:
+        blocks += sum(-(-(p + 1) // 16) for p in long_fp16.prior)
     stream = torch.cuda.Stream()
     order = pool_order(args.seed, blocks) if wl.scattered_pool else None
-    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sess, max_batch=B,
-                          max_context=max(wl.prior) + 1, pool_order=order,
-                          flags=mag.FLAG_NO_GRAPH if args.eager else 0)
+    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=B + 1, max_batch=B,
+                          max_context=max_ctx, pool_order=order, flags=mag.FLAG_NO_GRAPH if args.eager else 0)
     t_setup = time.time()
     ctx = mag.Context(cfg, stream.cuda_stream)
-    lm_keep = {}
     with torch.cuda.stream(stream):
         driver.load_weights(ctx, shape, args.seed)
-        # prior KV: each session set holds the same seeded priors (drawn once per session of the batch)
-        sets = []
-        for s in range(n_sets):
-            sets.append([ctx.session_open() for _ in range(B)])
-        L, H, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
-        for i, p in enumerate(wl.prior):
-            for t0 in range(0, p, 4096):
-                n = min(4096, p - t0)
-                k = np.empty((L, n, H, d), np.float16)
-                v = np.empty((L, n, H, d), np.float16)
-                for l in range(L):
-                    k[l] = synth.prior_kv_f16(args.seed, i, l, "K", n, H, d, tok0=t0)
-                    v[l] = synth.prior_kv_f16(args.seed, i, l, "V", n, H, d, tok0=t0)
-                kt, vt = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
-                for s in range(n_sets):
-                    ctx.kv_append(sets[s][i], n, kt, vt)
-                stream.synchronize()
-                del kt, vt
+    sids = open_with_priors(ctx, stream, wl, args.seed)
+    lens = list(wl.prior)
+    with torch.cuda.stream(stream):
         x = torch.from_numpy(hidden_f16(args.seed, B, shape.hidden, tag="x.step0")).cuda()
         width = shape.vocab or shape.hidden
         out = torch.empty((B, width), dtype=torch.float16, device="cuda")
     stream.synchronize()
     t_setup = time.time() - t_setup
 
-    # ---- timed region: K steps, each on a fresh session set
-    for i in range(args.warmup):
-        ctx.decode_step(sets[i], x, out)
+    def one_step():
+        ctx.decode_step(sids, x, out)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
+
+    # ---- timed region: K steps of the workload
+    for _ in range(args.warmup):
+        one_step()
     stream.synchronize()
     launches_per_step = ctx.last_step_launches()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -327,12 +460,14 @@ def run_gpu(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize()
         ev0.record(stream)
-        for i in range(args.steps):
-            ctx.decode_step(sets[args.warmup + i], x, out)
+        for _ in range(args.steps):
+            one_step()
         ev1.record(stream)
         ev1.synchronize()
         torch.cuda.synchronize()
         barrier(world)
+        # the distribution over 100 graph replays, each bracketed by its own events
+        dist_ms = replay_times(ctx, stream, sids, lens, x, out, 100)
     elapsed_s = ev0.elapsed_time(ev1) / 1e3
     job_s, job_units = reduce_job(world, elapsed_s, B * args.steps)
     value = job_units / job_s
@@ -341,23 +476,34 @@ def run_gpu(args, world, rank, local):
     # ---- end to end: host buffers through the C ABI, copies inside the timed region
     x_host = hidden_f16(args.seed, B, shape.hidden, tag="x.step0")
     out_host = np.empty((B, width), np.float16)
-    base = n_runs
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        ctx.decode_step_host(sets[base + i], x_host, out_host)
+    for _ in range(e2e_steps):
+        ctx.decode_step_host(sids, x_host, out_host)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
     e2e_s = time.perf_counter() - t0
     e2e_job_s, e2e_units = reduce_job(world, e2e_s, B * e2e_steps)
 
-    # ---- per-kernel device times (instrumented replay of the same step on fresh sessions)
+    # ---- per-kernel device times: the same step launched kernel by kernel with an event pair per launch
     per_kind = {}
-    for i in range(prof_steps):
-        for kind, ms in ctx.profile_step(sets[base + e2e_steps + i], x, out):
+    for _ in range(prof_steps):
+        for kind, ms in ctx.profile_step(sids, x, out):
             per_kind.setdefault(kind, []).append(ms)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
     stream.synchronize()
 
+    configs = {}
+    if rank == 0 and long_fp16 is not None:
+        configs = run_configs(args, ctx, stream, hbm, tc)
+    prefill = None
+    if rank == 0 and not args.no_prefill:
+        prefill = run_prefill(args, tc, src=ctx if not args.layers else None)
+    ctx.close()
+    del ctx
+    torch.cuda.empty_cache()
     if rank != 0:
         return
-    hbm, tc, peak_src = measured_peaks()
     sb = step_bytes(wl)
     wb = weight_bytes(shape)
     kernel_bytes = {"gate_up": wb["gate_up"], "qkv": wb["qkv"], "o_proj": wb["o_proj"], "down": wb["down"],
@@ -374,15 +520,9 @@ def run_gpu(args, world, rank, local):
     dom_ms = kern_rows[dom]["ms_per_launch"]
     achieved = kernel_bytes[dom] / (dom_ms / 1e3) / 1e9
     clocks = clk.summary()
-    cores = cpu_cores()
-    # ---- CPU baseline: the oracle on a bounded sample of this workload (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        st = oracle_sample_setup(wl, args.seed)
-        oracle_sample_step(wl, st, args.seed, 0)
-        t_cpu = oracle_sample_step(wl, st, args.seed, 1)
-        cpu = {"value": B / t_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text(wl),
-               "s_per_step": t_cpu}
+        cpu = cpu_baseline_leg(wl, args.seed)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -395,9 +535,12 @@ def run_gpu(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "step_bytes": sb, "hbm_gbs_step": sb / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_step": sb / (ms_per_step / 1e3) / 1e9 / hbm,
+        "replays": pct(dist_ms),
         "roofline": {"bound": "hbm", "kernel": "W4 gate-up GEMV (RMSNorm + SwiGLU fused), 28672x4096",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": kernel_bytes[dom],
+                     "timing": "kernel by kernel (no graph, no programmatic launch), an event pair around each "
+                               "launch on the context's stream; mean over the step's 32 launches x 3 steps",
                      "traffic": traffic_from_profile(dom)},
         "kernels": kern_rows,
         "cpu_baseline": cpu,
@@ -407,12 +550,42 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks,
         "setup_s": t_setup,
     }
-    if not args.no_prefill:
+    if configs:
+        line["configs"] = configs
+    if prefill is not None:
+        line["prefill"] = prefill
+    print(json.dumps(line), flush=True)
+
+
+def run_configs(args, ctx_main, stream, hbm, tc) -> dict:
+    """Every other decode configuration, each with its own replay distribution: the long FP16 context on
+    the headline context; the agent batch (scattered pool), INT8 and INT4 long contexts on contexts loaded
+    with the headline context's weights; the tiny one-layer model (latency)."""
+    import torch
+    import quantized_decode_step_gb300 as mag
+    from synth import driver
+    from synth.workloads import TINY_DECODE
+    res = {}
+    t0 = time.time()
+    res["long_fp16"] = decode_config(ctx_main, stream, LONG_FP16, args.seed, hbm, 100)
+    for key, wl in (("agent_b16", agent_batch(args.seed)), ("long_int8", LONG_INT8), ("long_int4", LONG_INT4)):
+        blocks = sum(-(-(p + 1) // 16) for p in wl.prior)
+        order = pool_order(args.seed, blocks) if wl.scattered_pool else None
+        cfg = mag.make_config(wl.shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=wl.batch,
+                              max_batch=wl.batch, max_context=max(wl.prior) + 1, pool_order=order)
+        ctx = mag.Context(cfg, stream.cuda_stream)
+        clone_weights(ctx_main, ctx, wl.shape, args.seed, stream)
+        res[key] = decode_config(ctx, stream, wl, args.seed, hbm, 100)
         ctx.close()
         del ctx
         torch.cuda.empty_cache()
-        line["prefill"] = run_prefill(args, tc)
-    print(json.dumps(line), flush=True)
+    with torch.cuda.stream(stream):
+        ctx, sids = driver.setup(TINY_DECODE, args.seed, stream=stream.cuda_stream)
+    res["tiny"] = decode_config(ctx, stream, TINY_DECODE, args.seed, hbm, 200, sids=sids)
+    res["tiny"]["note"] = "L2-resident (0.52 MB): latency, not a bandwidth figure"
+    ctx.close()
+    res["setup_and_run_s"] = time.time() - t0
+    return res
 
 
 def prefill_flops(shape, prior: int, T: int) -> float:
@@ -425,11 +598,12 @@ def prefill_flops(shape, prior: int, T: int) -> float:
     return shape.n_layers * (2.0 * T * per_layer + attn) + 2.0 * shape.vocab * D
 
 
-def run_prefill(args, tc_peak):
-    """The chunked-prefill configuration: T-token chunks on fresh sessions holding the prior cache."""
+def run_prefill(args, tc_peak, src=None):
+    """The chunked-prefill configuration: 512-token chunks on a session holding the 800-token prior cache
+    (cut back to it after every chunk), timed per chunk with CUDA events; then the verify and batched
+    prefill legs. Weights come from `src` (the headline context) when given, else from the seed."""
     import torch
     import quantized_decode_step_gb300 as mag
-    import synth
     from synth import driver, hidden_f16
 
     wl = PREFILL_8B
@@ -437,46 +611,61 @@ def run_prefill(args, tc_peak):
         from dataclasses import replace as _replace
         wl = _replace(wl, name=wl.name + f"-{args.layers}layers", shape=shrink(wl.shape, n_layers=args.layers))
     shape, T, p = wl.shape, wl.chunk, wl.prior[0]
-    warm, runs = 2, 3
-    n_sets = warm + runs
+    warm, runs = 3, 20
     n_draft = 4  # the verify leg: drafts checked in one call on a session after its chunk
-    blocks = n_sets * -(-(p + T + n_draft) // 16)
+    n_sess = 5
+    blocks = n_sess * -(-(p + T + n_draft) // 16)
     stream = torch.cuda.Stream()
     # max_batch = n_draft: the verify leg runs on the decode kernels, one row per draft
-    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sets,
+    cfg = mag.make_config(shape, kv_dtype=wl.kv_dtype, pool_blocks=blocks, max_sessions=n_sess,
                           max_batch=n_draft, max_chunk=T, max_context=p + T + n_draft)
     t_setup = time.time()
     ctx = mag.Context(cfg, stream.cuda_stream)
+    if src is not None:
+        clone_weights(src, ctx, shape, args.seed, stream)
+    else:
+        with torch.cuda.stream(stream):
+            driver.load_weights(ctx, shape, args.seed)
+    prior = Workload(wl.name + "-prior", shape, wl.kv_dtype, n_sess, (p,) * n_sess)
     with torch.cuda.stream(stream):
-        driver.load_weights(ctx, shape, args.seed)
-        sids = [ctx.session_open() for _ in range(n_sets)]
+        sids = []
         L, H, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
         k = np.empty((L, p, H, d), np.float16)
         v = np.empty((L, p, H, d), np.float16)
+        import synth
         for l in range(L):
             k[l] = synth.prior_kv_f16(args.seed, 0, l, "K", p, H, d)
             v[l] = synth.prior_kv_f16(args.seed, 0, l, "V", p, H, d)
         kt, vt = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
-        for sid in sids:
+        for _ in range(prior.batch):
+            sid = ctx.session_open()
             ctx.kv_append(sid, p, kt, vt)
+            sids.append(sid)
         x = torch.from_numpy(hidden_f16(args.seed, T, shape.hidden, tag="chunk0")).cuda()
         out = torch.empty(shape.vocab or shape.hidden, dtype=torch.float16, device="cuda")
     stream.synchronize()
+    del kt, vt
     t_setup = time.time() - t_setup
-    for i in range(warm):
-        ctx.prefill_chunk(sids[i], T, x, out)
+    sid0 = sids[0]
+    for _ in range(warm):
+        ctx.prefill_chunk(sid0, T, x, out)
+        ctx.session_truncate(sid0, p)
     stream.synchronize()
     launches = ctx.last_step_launches()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+    for a, b in evs:
+        a.record(stream)
+        ctx.prefill_chunk(sid0, T, x, out)
+        b.record(stream)
+        ctx.session_truncate(sid0, p)
+    stream.synchronize()
+    ch = pct([a.elapsed_time(b) for a, b in evs])
+    s_chunk = ch["median"] / 1e3
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(runs):
-        ctx.prefill_chunk(sids[warm + i], T, x, out)
-    ev1.record(stream)
-    ev1.synchronize()
-    s_chunk = ev0.elapsed_time(ev1) / 1e3 / runs
     # verify leg: n_draft draft tokens in one call on a session holding p + T tokens, truncated back after
     # each call so every call sees the same cache
     sid_v = sids[0]
+    ctx.prefill_chunk(sid_v, T, x, out)
     base_len = ctx.session_length(sid_v)
     with torch.cuda.stream(stream):
         xv = torch.from_numpy(hidden_f16(args.seed, n_draft, shape.hidden, tag="drafts")).cuda()
@@ -497,8 +686,6 @@ def run_prefill(args, tc_peak):
     # as four mag_prefill_chunk calls (the same 512 rows); sessions are truncated back after every call
     n_b, t_b = 4, T // 4
     bsids = sids[1:1 + n_b]
-    for sid in bsids:
-        ctx.session_truncate(sid, p)
     with torch.cuda.stream(stream):
         xb = torch.from_numpy(hidden_f16(args.seed, n_b * t_b, shape.hidden, tag="batch")).cuda()
         ob = torch.empty((n_b, shape.vocab or shape.hidden), dtype=torch.float16, device="cuda")
@@ -519,21 +706,20 @@ def run_prefill(args, tc_peak):
         fn()
         stream.synchronize()
         ev0.record(stream)
-        for _ in range(runs):
+        for _ in range(5):
             fn()
         ev1.record(stream)
         ev1.synchronize()
-        legs[name] = ev0.elapsed_time(ev1) / runs
+        legs[name] = ev0.elapsed_time(ev1) / 5
     fl = prefill_flops(shape, p, T)
     st = ctx.memory_stats()
     ctx.close()
     achieved = fl / s_chunk / 1e12
-    return {"workload": wl.name, "chunk": T, "prior": p, "ms_per_chunk": s_chunk * 1e3,
+    return {"workload": wl.name, "chunk": T, "prior": p, "ms_per_chunk": s_chunk * 1e3, "chunks": ch,
             "tokens_per_s": T / s_chunk, "algorithmic_tflop_per_chunk": fl / 1e12,
-            "roofline": {"bound": "tensor", "scope": "whole chunk", "achieved": achieved, "peak": tc_peak,
-                         "unit": "TFLOP/s", "frac": achieved / tc_peak,
-                         "note": "fp16 kind::f16 at the measured bf16 rate; the exact two-term weights double "
-                                 "the tensor work, which is not counted as achieved"},
+            "roofline": {"bound": "tensor", "scope": "whole chunk (median of the timed chunks)",
+                         "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                         "note": "fp16 kind::f16 at the measured bf16 rate; algorithmic flops only"},
             "launches_per_chunk": launches, "prefill_weight_bytes": st["prefill_weight_bytes"],
             "verify": {"drafts": n_draft, "context": base_len, "ms_per_call": s_verify * 1e3,
                        "tokens_per_s": n_draft / s_verify, "launches_per_call": v_launches},
@@ -658,6 +844,8 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other decode configurations (agent batch, long contexts, tiny)")
     ap.add_argument("--eager", action="store_true",
                     help="profiling aid: launch the step's kernels one by one instead of replaying a CUDA graph")
     ap.add_argument("--plans", action="store_true",

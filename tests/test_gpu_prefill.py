@@ -13,12 +13,19 @@
   the rel-L2 bar for the chunk and the step after it is 1.25 x the oracle's
   own change under one ulp of one input value per token (measured in the
   test), as for the 32-layer decode.
-* The 8B chunked-prefill configuration at full size (32 layers, a 512-token
-  chunk on an 800-token FP16 cache): the oracle can not run it in a test, so
-  the chunk's last logits are compared with the same 512 tokens decoded one by
-  one on the GPU (a property of any correct prefill). The bar there is the
-  sum of the two paths' own distance to the oracle at 32 layers (each about
-  2e-3 rel-L2, the oracle's one-ulp input sensitivity at that depth).
+* The 8B chunked-prefill configuration's own chunk (512 tokens on an 800-token
+  FP16 cache, full vocabulary) on two layers against the oracle's forward
+  pass: the last token's logits, every stored key and value of the chunk at
+  both layers (within the tolerance), and the prior cache bit-exact.
+* The same configuration at full size (32 layers), teacher forced: the chunk's
+  fp32 residuals after every layer are read back (mag_debug_prefill_residuals);
+  the oracle runs sampled layers alone from the GPU's residual at their input
+  (all 512 tokens, causal over the cache and the chunk) and the final norm and
+  LM head from the GPU's last residual, all at the strict bar. (Each oracle
+  layer of 512 tokens costs several seconds of CPU, so not all 32 run.)
+* Also at full size: the chunk's last logits against the same 512 tokens
+  decoded one by one on the GPU (a property of any correct prefill; bar: the
+  two paths' own distance to the oracle at 32 layers, each about 2e-3).
 """
 import numpy as np
 import pytest
@@ -29,8 +36,8 @@ import quantized_decode_step_gb300 as mag
 import synth
 from synth import driver
 from synth.workloads import KV_FP16, KV_INT4, KV_INT8, LLAMA8B, PREFILL_8B, TINY, Workload, shrink
-from tests.helpers import (FLOOR_FACTOR, TOL_MAX_ABS, TOL_REL_L2, max_abs, model_cfg, one_ulp_floor, oracle_weights,
-                           prior_kv, rel_l2)
+from tests.helpers import (FLOOR_FACTOR, TOL_MAX_ABS, TOL_REL_L2, device_bytes, fp16_ulps, max_abs, model_cfg,
+                           one_ulp_floor, oracle_weights, prior_kv, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -128,6 +135,102 @@ def test_8b_two_layers_prefill_chunk(dt):
     shape = shrink(LLAMA8B, n_layers=2)
     wl = Workload(f"8b2L-prefill-64-on-800-kv{dt}", shape, dt, 1, (800,), chunk=64)
     _run(wl, 27, (64,), decode_after=1 if dt else 0, random_gain=False, floor_check=dt != KV_FP16)
+
+
+def _pool_host(ctx):
+    ptr, nbytes = ctx.debug_pool()
+    torch.cuda.synchronize()
+    return device_bytes(ptr, nbytes).cpu().numpy()
+
+
+def _stored_vec(host, ctx, sid, l, t, h, which, vec_bytes):
+    off = ctx.debug_kv_locate(sid, l, t)[which] + h * 16 * vec_bytes
+    return host[off:off + vec_bytes]
+
+
+@pytest.mark.slow
+def test_8b_prefill_512_on_800_two_layers_vs_oracle():
+    """The configuration's chunk (512 tokens at positions 800..1311, FP16 cache, full vocabulary) on two of
+    the 32 layers: four 128-row token tiles per weight tile, the 1312-key causal attention, and the chunk's
+    keys and values written into the pool ("5. Core modules" 5.2)."""
+    wl0 = PREFILL_8B
+    shape = shrink(wl0.shape, n_layers=2)
+    wl = Workload("8b2L-prefill-512-on-800", shape, KV_FP16, 1, wl0.prior, chunk=wl0.chunk)
+    seed, T, p = 29, wl.chunk, wl.prior[0]
+    ctx, sids = driver.setup(wl, seed, extra_tokens=T)
+    sid = sids[0]
+    x = synth.hidden_f16(seed, T, shape.hidden, tag="chunk0")
+    out = torch.empty(shape.vocab, dtype=torch.float16, device="cuda")
+    ctx.prefill_chunk(sid, T, torch.from_numpy(x).cuda(), out)
+    ctx.sync()
+    assert ctx.session_length(sid) == p + T
+    w = oracle_weights(shape, seed)
+    cfg = model_cfg(shape, KV_FP16)
+    kv = oracle.KV(cfg, p + T)
+    kv.append(*prior_kv(shape, seed, 0, p))
+    c, s = oracle.rope_table(p + T + 1, shape.head_dim, shape.rope_base)
+    ref = oracle.forward(cfg, w, [kv], [T], x, c, s)[0]
+    _compare(out.cpu().numpy(), ref, f"{wl.name} last-token logits")
+    host = _pool_host(ctx)
+    H, d, vb = shape.n_kv_heads, shape.head_dim, 2 * shape.head_dim
+    for t in range(0, p, 37):  # the prior cache, as appended
+        for l in range(2):
+            for h in range(H):
+                for which in (0, 1):
+                    assert np.array_equal(_stored_vec(host, ctx, sid, l, t, h, which, vb),
+                                          kv.stored(l, which, t, h)[0]), (t, l, h, which)
+    for l in range(2):
+        got = np.empty((T, H, 2, d), np.float16)
+        exp = np.empty_like(got)
+        for i in range(T):
+            for h in range(H):
+                for which in (0, 1):
+                    got[i, h, which] = _stored_vec(host, ctx, sid, l, p + i, h, which, vb).view(np.float16)
+                    exp[i, h, which] = kv.stored(l, which, p + i, h)[0].view(np.float16)
+        assert np.all(np.isfinite(got.astype(np.float32)))
+        # placement: a key or value read from the wrong block or slot would be unrelated N(0, 1)-scale
+        # data; the values themselves come out of an fp32 GEMM (the oracle's is double), are rounded to
+        # fp16, and keys are rotated and rounded again, so they are held to the tolerance
+        u = fp16_ulps(got, exp)
+        print(f"{wl.name} layer {l} stored K / V: {np.mean(u[:, :, 0] == 0):.4f} / {np.mean(u[:, :, 1] == 0):.4f} "
+              f"bit-identical")
+        _compare(got, exp, f"{wl.name} layer {l} stored K/V of the chunk")
+
+
+@pytest.mark.slow
+def test_8b_prefill_512_on_800_layerwise():
+    """The configuration at full size, 32 layers, teacher forced on sampled layers (see the module note)."""
+    wl = PREFILL_8B
+    shape, T, p = wl.shape, wl.chunk, wl.prior[0]
+    seed = 30
+    sample = (1, 16, 31)
+    ctx, sids = driver.setup(wl, seed, extra_tokens=T)
+    sid = sids[0]
+    x = synth.hidden_f16(seed, T, shape.hidden, tag="chunk0")
+    out = torch.empty(shape.vocab, dtype=torch.float16, device="cuda")
+    resid = torch.empty((shape.n_layers + 1, T, shape.hidden), dtype=torch.float32, device="cuda")
+    ctx.prefill_residuals(sid, T, torch.from_numpy(x).cuda(), out, resid)
+    R = resid.cpu().numpy().astype(np.float64)
+    got = out.cpu().numpy()
+    del resid
+    assert np.array_equal(R[0], x.astype(np.float64))
+    cfg = model_cfg(shape, KV_FP16)
+    w = oracle_weights(shape, seed, layers=sample)
+    # oracle weights of the sampled layers only: index them as layers 0..2 of a 3-layer model
+    c, s = oracle.rope_table(p + T + 1, shape.head_dim, shape.rope_base)
+    k_all, v_all = prior_kv(shape, seed, 0, p)
+    sub = shrink(shape, n_layers=len(sample))
+    scfg = model_cfg(sub, KV_FP16)
+    kv = oracle.KV(scfg, p + T)
+    kv.append(np.ascontiguousarray(k_all[list(sample)]), np.ascontiguousarray(v_all[list(sample)]))
+    for j, l in enumerate(sample):
+        ref = oracle.layer(scfg, w, j, [kv], [T], R[l], c, s)
+        ma, rl = max_abs(R[l + 1], ref), rel_l2(R[l + 1], ref)
+        dl = rel_l2(R[l + 1] - R[l], ref - R[l])
+        print(f"{wl.name} layer {l}: hidden max-abs {ma:.2e} rel-L2 {rl:.2e}, layer contribution rel-L2 {dl:.2e}")
+        assert ma <= TOL_MAX_ABS and rl <= TOL_REL_L2 and dl <= TOL_REL_L2, (l, ma, rl, dl)
+    ref = oracle.output(model_cfg(shape, KV_FP16), w, R[shape.n_layers][-1:])[0]
+    _compare(got, ref, f"{wl.name} logits from the final residual")
 
 
 @pytest.mark.slow
