@@ -148,10 +148,11 @@ mag_status mag_load_weights(mag_ctx* ctx, int32_t tensor, int32_t layer, const v
  * (QKV: whole heads); nothing in the scratch needs to start at zero.
  * A tile of rows of K values takes 16 * ceil(K/32) * 20 bytes: a projection
  * whose smallest slab (one tile; QKV: one head of d/16 tiles) exceeds 4 MiB
- * -- K above 419,424; QKV K above 52,416 (d = 128) or 104,816 (d = 64) -- is
+ * -- K above 419,424; QKV K above 52,416 (d = 128) or 104,832 (d = 64) -- is
  * rejected with INVALID_ARG. The context's device must be current. The first call on each
- * device looks the scratch's address up; make it before any stream capture
- * begins. Ordered on the context's stream; src_dev may be reused once the
+ * device looks the scratch's address up, and so does the first call after the
+ * device's context was replaced (a device reset); make those calls before any
+ * stream capture begins. Ordered on the context's stream; src_dev may be reused once the
  * stream reaches this point. Calls that overlap in time on one device (other
  * streams, threads or contexts) race on the shared scratch: order them.
  * Errors: INVALID_ARG (id, layer, size, scratch limit, device), CUDA. */
@@ -407,6 +408,24 @@ mag_status mag_debug_profile_step(mag_ctx* ctx, int32_t batch, const int32_t* se
  * Errors: as mag_decode_step; INVALID_ARG for a null resid_dev; TIMEOUT as mag_sync. */
 mag_status mag_debug_step_residuals(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host,
                                     const void* hidden_in_dev, void* out_dev, void* resid_dev);
+
+/* Failure injection for tests ([Magnitude] 5.1-5.2: the engine's error behaviour): the number of polls a
+ * decode GEMV's pipeline wait (for its weight copies to land in shared memory) makes before it gives up.
+ * polls < 0 restores the built-in limit (2^22); 0 makes every such wait give up at once, as if the copies
+ * were stuck: the kernel then sets its bit in the error word, waits (within the built-in limit) for the
+ * copies it has in flight, skips its arithmetic and returns, so the step's outputs are meaningless, the
+ * next mag_sync returns MAG_ERR_TIMEOUT and the context stays usable (drop the step's token with
+ * mag_session_truncate). Synchronises the stream; graphs captured under another limit are captured again.
+ * Errors: INVALID_ARG (null context), CUDA. */
+mag_status mag_debug_set_wait_limit(mag_ctx* ctx, int64_t polls);
+
+/* Failure injection for tests ([Magnitude] 5.2: memory errors): process-wide, the next `skip` allocations
+ * the library makes succeed and the `count` after them fail as if the device (or pinned host memory) were
+ * full: device and pinned-host allocations, the stream-ordered scratch of an fp32 load, and the physical
+ * memory of an elastic KV pool group. Each call that meets one returns MAG_ERR_OOM (an elastic pool that
+ * can map no new group: MAG_ERR_OOM from the call that needed it) with the context unchanged and usable;
+ * mag_create returns it with *out NULL, everything it had allocated freed. count <= 0 turns it off. */
+void mag_debug_fail_allocations(int32_t skip, int32_t count);
 
 /* A prefill chunk like mag_prefill_chunk, launched without programmatic dependent launch, that also copies
  * the fp32 residual of all n_tokens rows into resid_dev (device memory, fp32 [L+1][n_tokens][D],

@@ -31,11 +31,17 @@ EXPORTED = [
     "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
     "mag_debug_last_step_launches", "mag_debug_profile_step", "mag_debug_step_residuals",
-    "mag_debug_prefill_residuals",
+    "mag_debug_prefill_residuals", "mag_debug_set_wait_limit",
+    "mag_debug_fail_allocations",
     "mag_adapt_defaults", "mag_set_adaptive", "mag_get_profile", "mag_profiler_create", "mag_profiler_destroy",
     "mag_profiler_observe", "mag_profiler_quantile", "mag_profiler_count", "mag_plan_for", "mag_hot_pool_blocks",
 ]
 OP_NAMES = ["step_begin", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head"]
+
+
+def debug_fail_allocations(skip: int, count: int) -> None:
+    """Process-wide: the next `skip` library allocations succeed, the `count` after them fail (0: off)."""
+    lib().mag_debug_fail_allocations(int(skip), int(count))
 
 
 class MagError(RuntimeError):
@@ -130,6 +136,8 @@ def lib():
                                            i32),
                 "mag_debug_step_residuals": ([vp, i32, P32, vp, vp, vp], i32),
                 "mag_debug_prefill_residuals": ([vp, i32, i32, vp, vp, vp], i32),
+                "mag_debug_set_wait_limit": ([vp, i64], i32),
+                "mag_debug_fail_allocations": ([i32, i32], None),
                 "mag_adapt_defaults": ([ctypes.POINTER(AdaptConfig)], None),
                 "mag_set_adaptive": ([vp, ctypes.POINTER(AdaptConfig)], i32),
                 "mag_get_profile": ([vp, ctypes.POINTER(Profile)], i32),
@@ -368,6 +376,10 @@ class Context:
         ids = (ctypes.c_int32 * len(sessions))(*sessions)
         self._check(lib().mag_debug_step_residuals(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out),
                                                    _ptr(resid)), "mag_debug_step_residuals")
+
+    def set_wait_limit(self, polls: int):
+        """Polls of a GEMV pipeline wait before it gives up (< 0: the built-in limit; 0: at once)."""
+        self._check(lib().mag_debug_set_wait_limit(self.h, int(polls)), "mag_debug_set_wait_limit")
 
     def prefill_residuals(self, sid, n_tokens, hidden_in, last_out, resid):
         """Prefill chunk that also fills resid (device fp32 [L+1, n_tokens, hidden]) with the residual stream."""

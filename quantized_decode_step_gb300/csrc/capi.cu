@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "adapt.h"
+#include "alloc.h"
 #include "arena.h"
 #include "kernels.h"
 #include "kvpool.h"
@@ -120,6 +121,7 @@ struct mag_ctx {
   // counters (zero between launches) and step arguments
   uint32_t* d_counters = nullptr;
   uint32_t* h_err = nullptr;  // mapped pinned word: kernels set bits when a bounded wait gives up
+  uint32_t wait_limit = kWaitPolls;  // polls of a GEMV main-loop wait (mag_debug_set_wait_limit)
   uint32_t* d_err = nullptr;
   size_t n_counters = 0;
   StepArgs* d_args = nullptr;
@@ -383,6 +385,7 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
   a.stages = pl.stages;
   a.t_max = pl.t_max;
   a.err = c->d_err;
+  a.wait_limit = c->wait_limit;
   a.chunks_per_cta = pl.cpc;
   a.ks = pl.ks;
   a.tpw = pl.tpw;
@@ -601,8 +604,8 @@ mag_status setup_prefill(mag_ctx* c) {
       offs.push_back(total);
       total = align256(total + (size_t)prefill_rows(c, i) * Ks[i] * 2 * 2);
     }
-  cudaError_t e = cudaMalloc(&c->pf_w, std::max<size_t>(total, 256));
-  if (e != cudaSuccess) return fail(c, MAG_ERR_OOM, "prefill weights: cudaMalloc(%zu): %s", total, cudaGetErrorString(e));
+  cudaError_t e = dev_malloc(&c->pf_w, std::max<size_t>(total, 256));
+  if (e != cudaSuccess) return fail(c, MAG_ERR_OOM, "prefill weights: device allocation of %zu bytes: %s", total, cudaGetErrorString(e));
   c->pf_wbytes = total;
   cudaMemsetAsync(c->pf_w, 0, total, c->stream);  // padding rows stay zero
   c->pproj.resize((size_t)c->L * 4);
@@ -616,7 +619,7 @@ mag_status setup_prefill(mag_ctx* c) {
         return fail(c, MAG_ERR_CUDA, "prefill: tensor map encoding failed (layer %d, projection %d)", l, i);
     }
   build_prefill_plan(c);
-  if ((e = cudaMalloc(&c->pf_arena, std::max<uint64_t>(c->pf_arena_bytes, 256))) != cudaSuccess)
+  if ((e = dev_malloc(&c->pf_arena, std::max<uint64_t>(c->pf_arena_bytes, 256))) != cudaSuccess)
     return fail(c, MAG_ERR_OOM, "prefill arena: %s", cudaGetErrorString(e));
   auto at = [&](const char* n) -> uint8_t* {
     for (auto& t : c->pf_plan)
@@ -633,8 +636,8 @@ mag_status setup_prefill(mag_ctx* c) {
       !make_tmap_2d(c->map_act, c->pf_act, T, c->F))
     return fail(c, MAG_ERR_CUDA, "prefill: activation tensor maps");
   // several sessions in one chunk: per-row positions and sessions, and the gathered last rows
-  if ((e = cudaMalloc(&c->pf_rows, (size_t)2 * T * 4)) != cudaSuccess ||
-      (e = cudaMalloc(&c->pf_last_r, (size_t)MAG_MAX_BATCH * c->D * 4)) != cudaSuccess)
+  if ((e = dev_malloc(&c->pf_rows, (size_t)2 * T * 4)) != cudaSuccess ||
+      (e = dev_malloc(&c->pf_last_r, (size_t)MAG_MAX_BATCH * c->D * 4)) != cudaSuccess)
     return fail(c, MAG_ERR_OOM, "prefill row tables: %s", cudaGetErrorString(e));
   c->other_bytes += (size_t)2 * T * 4 + (size_t)MAG_MAX_BATCH * c->D * 4;
   return MAG_OK;
@@ -752,8 +755,8 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   size_t lm_off = off;
   if (c->V) off = align256(off + (size_t)(c->V / 16) * ((c->D + 63) / 64) * 2048);  // fp16 tiles, ragged k zeroed
   c->wbytes = off;
-  if ((e = cudaMalloc(&c->wbase, c->wbytes)) != cudaSuccess) {
-    fail(c, MAG_ERR_OOM, "weights: cudaMalloc(%zu): %s", c->wbytes, cudaGetErrorString(e));
+  if ((e = dev_malloc(&c->wbase, c->wbytes)) != cudaSuccess) {
+    fail(c, MAG_ERR_OOM, "weights: device allocation of %zu bytes: %s", c->wbytes, cudaGetErrorString(e));
     return bail(MAG_ERR_OOM);
   }
   for (size_t i = 0; i < c->proj.size(); ++i) c->proj[i].tiles = c->wbase + offs[i];
@@ -779,7 +782,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     c->cfg.pool_blocks = (int32_t)c->kv.blocks();  // elastic: rounded up to whole mapping groups
   }
   size_t tb = (size_t)cfg->max_sessions * c->table_stride * 4;
-  if ((e = cudaMalloc(&c->d_tables, tb)) != cudaSuccess) {
+  if ((e = dev_malloc(&c->d_tables, tb)) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "block tables: %s", cudaGetErrorString(e));
     return bail(MAG_ERR_OOM);
   }
@@ -797,7 +800,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
         sn[p * half + i] = (float)std::sin(theta);
       }
     size_t bytes = rows * half * 4;
-    if (cudaMalloc(&c->d_cos, bytes) != cudaSuccess || cudaMalloc(&c->d_sin, bytes) != cudaSuccess) {
+    if (dev_malloc(&c->d_cos, bytes) != cudaSuccess || dev_malloc(&c->d_sin, bytes) != cudaSuccess) {
       fail(c, MAG_ERR_OOM, "RoPE table");
       return bail(MAG_ERR_OOM);
     }
@@ -815,7 +818,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     }
   }
   build_decode_plan(c);
-  if ((e = cudaMalloc(&c->arena, std::max<uint64_t>(c->arena_bytes, 256))) != cudaSuccess) {
+  if ((e = dev_malloc(&c->arena, std::max<uint64_t>(c->arena_bytes, 256))) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "arena: %s", cudaGetErrorString(e));
     return bail(MAG_ERR_OOM);
   }
@@ -832,14 +835,14 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   size_t stage_out = (size_t)c->B_max * (c->V ? c->V : c->D) * 2;
   const size_t part_bytes = (size_t)c->B_max * c->Hkv * kAttnMaxGroups * 3 * c->Hq / c->Hkv * c->d * 4;
   const size_t arrival_bytes = (size_t)c->B_max * c->Hkv * 4;
-  if (cudaMalloc(&c->d_counters, nc * 4) != cudaSuccess ||
-      cudaMalloc(&c->attn_part, part_bytes) != cudaSuccess ||
-      cudaMalloc(&c->attn_arrivals, arrival_bytes) != cudaSuccess ||
-      cudaMalloc(&c->d_args, sizeof(StepArgs)) != cudaSuccess ||
-      cudaMalloc(&c->d_in_stage, (size_t)c->B_max * c->D * 2) != cudaSuccess ||
-      cudaMalloc(&c->d_out_stage, stage_out) != cudaSuccess ||
-      cudaMallocHost(&c->h_ring, sizeof(StepArgs) * kRing) != cudaSuccess ||
-      cudaHostAlloc(&c->h_err, sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess ||
+  if (dev_malloc(&c->d_counters, nc * 4) != cudaSuccess ||
+      dev_malloc(&c->attn_part, part_bytes) != cudaSuccess ||
+      dev_malloc(&c->attn_arrivals, arrival_bytes) != cudaSuccess ||
+      dev_malloc(&c->d_args, sizeof(StepArgs)) != cudaSuccess ||
+      dev_malloc(&c->d_in_stage, (size_t)c->B_max * c->D * 2) != cudaSuccess ||
+      dev_malloc(&c->d_out_stage, stage_out) != cudaSuccess ||
+      host_alloc(&c->h_ring, sizeof(StepArgs) * kRing, cudaHostAllocDefault) != cudaSuccess ||
+      host_alloc(&c->h_err, sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer(&c->d_err, c->h_err, 0) != cudaSuccess) {
     fail(c, MAG_ERR_OOM, "counters / step arguments");
     return bail(MAG_ERR_OOM);
@@ -893,7 +896,11 @@ mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const voi
         return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected fp32 [%d, %d]", bytes, p.N, p.K);
       // quantise into a stream-ordered scratch copy in W4G32 bytes, then tile it
       uint8_t* canon = nullptr;
-      CUDA_TRY(c, cudaMallocAsync(reinterpret_cast<void**>(&canon), p.canon_bytes, c->stream));
+      cudaError_t ea = dev_malloc_async(reinterpret_cast<void**>(&canon), p.canon_bytes, c->stream);
+      if (ea == cudaErrorMemoryAllocation)
+        return fail(c, MAG_ERR_OOM, "load_weights: %zu bytes of quantisation scratch: %s", p.canon_bytes,
+                    cudaGetErrorString(ea));
+      CUDA_TRY(c, ea);
       cudaError_t e1 = launch_quantize_w4g32(c->stream, (const float*)src, p.N, p.K, canon,
                                              reinterpret_cast<__half2*>(canon + (size_t)p.N * p.G * 16));
       cudaError_t e2 = e1 == cudaSuccess ? launch_w4_to_tiles(c->stream, canon, p.N, p.K, p.map, p.map_arg, p.tiles)
@@ -1240,6 +1247,25 @@ mag_status mag_debug_step_residuals(mag_ctx* c, int32_t B, const int32_t* sids, 
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   c->last_launches = n;
   return check_err(c);
+}
+
+mag_status mag_debug_set_wait_limit(mag_ctx* c, int64_t polls) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  mag_status st = finish_capture(c);
+  if (st != MAG_OK) return st;
+  const uint32_t v = polls < 0 ? kWaitPolls : (uint32_t)std::min<int64_t>(polls, 0xffffffffll);
+  if (v == c->wait_limit) return MAG_OK;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  // captured graphs hold the old limit in their kernel arguments: capture again on next use
+  for (auto& gv : c->graphs)
+    for (auto& gp : gv)
+      for (auto& g : gp)
+        if (g.exec) {
+          cudaGraphExecDestroy(g.exec);
+          g = mag_ctx::StepGraph{};
+        }
+  c->wait_limit = v;
+  return MAG_OK;
 }
 
 mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, const void* in_host, void* out_host) {

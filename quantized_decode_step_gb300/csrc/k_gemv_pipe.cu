@@ -159,7 +159,7 @@ __device__ __forceinline__ void gemv_pipe_body(const GemvArgs& a) {
     const uint4* zero4 = reinterpret_cast<const uint4*>(smem + L.zero);
     for (int f = 0; f < nf; ++f) {
       if (!dead) {
-        if (!__all_sync(0xffffffffu, mbar_wait(full + slot, round & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(full + slot, round & 1, a.wait_limit))) {
           if (lane == 0) atomicOr(a.err, 4u);
           dead = true;
         }
@@ -220,7 +220,7 @@ __device__ __forceinline__ void gemv_pipe_body(const GemvArgs& a) {
   } else {
   for (int f = 0; f < nf; ++f) {
     if (!dead) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(full + slot, round & 1));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(full + slot, round & 1, a.wait_limit));
       if (!ok) {
         if (lane == 0) atomicOr(a.err, 4u);
         dead = true;

@@ -55,8 +55,11 @@ struct GemvArgs {
   int32_t stages;         // ring slots per warp (2..8)
   int32_t t_max;          // most tiles of one block
   uint32_t* err;          // set (bit or) when a pipeline wait gives up
+  uint32_t wait_limit;    // polls of a main-loop pipeline wait before it gives up (0: at once)
 };
 
+// Polls of a bounded mbarrier wait before it is declared stuck (main-loop default; drain waits always).
+constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr int kPipeMaxBatch = 4;
 size_t gemv_pipe_smem_bytes(int wfmt, int batch, int n_chunks, int stages, int t_max);
 int gemv_pipe_max_stages();

@@ -1,6 +1,8 @@
 // KV block pool memory and free list; see kvpool.h.
 #include "kvpool.h"
 
+#include "alloc.h"
+
 #include <cuda.h>
 
 #include <algorithm>
@@ -82,7 +84,7 @@ mag_status KvPool::init_fixed(int layers, int64_t blocks, int64_t block_bytes, c
   P_ = blocks;
   bb_ = block_bytes;
   const size_t bytes = reserved_bytes();
-  cudaError_t e = cudaMalloc(&base_, bytes);
+  cudaError_t e = dev_malloc(&base_, bytes);
   if (e != cudaSuccess) {
     err = std::string("KV pool: cudaMalloc: ") + cudaGetErrorString(e);
     base_ = nullptr;
@@ -147,7 +149,7 @@ mag_status KvPool::map_group(int64_t g, cudaStream_t s) {
   for (int l = 0; l < L_; ++l) {
     const CUdeviceptr at = (CUdeviceptr)(base_ + ((size_t)l * P_ + (size_t)g * G_) * bb_);
     CUmemGenericAllocationHandle h = 0;
-    if (v.create(&h, gbytes, &prop, 0) != CUDA_SUCCESS) {
+    if (alloc_injected_failure() || v.create(&h, gbytes, &prop, 0) != CUDA_SUCCESS) {
       err = "KV pool: cuMemCreate failed (device memory)";
       unmap_group(g);
       return MAG_ERR_OOM;

@@ -9,6 +9,8 @@
 // part of the library image: quantise the slab's rows into the scratch, tile
 // them into place, next slab. The kernels are the ordinary load's, unchanged;
 // each slab is a self-contained smaller projection of the same tile map.
+#include <cuda.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -24,23 +26,55 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-uint8_t* g_scratch[kMaxDevices] = {};
+struct DeviceScratch {
+  unsigned long long ctx_id = 0;  // driver id of the context the address belongs to
+  uint8_t* ptr = nullptr;
+};
+DeviceScratch g_scratch[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (the first call on a device does it).
+// Driver id of the calling thread's current context (unique for the process's lifetime, so a primary
+// context created again after a device reset gets a new one); 0 when none is current or the driver
+// calls are unavailable.
+unsigned long long current_ctx_id() {
+  static decltype(&::cuCtxGetCurrent) get_current = nullptr;
+  static decltype(&::cuCtxGetId) get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", reinterpret_cast<void**>(&get_current), 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess || q != cudaDriverEntryPointSuccess)
+      get_current = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", reinterpret_cast<void**>(&get_id), 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess || q != cudaDriverEntryPointSuccess)
+      get_id = nullptr;
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch on the current device: looked up (cudaGetSymbolAddress, with the device
+// current) the first time a device's context is seen, and again if that context was replaced since (a
+// device reset reloads the library's module, possibly elsewhere). A cached address is only reused for the
+// context it was looked up in.
 cudaError_t scratch_on_current_device(uint8_t** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch[dev]) {
+  DeviceScratch& d = g_scratch[dev];
+  const unsigned long long id = current_ctx_id();
+  if (!d.ptr || id == 0 || id != d.ctx_id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, mag_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch[dev] = static_cast<uint8_t*>(p);
+    d.ptr = static_cast<uint8_t*>(p);
+    d.ctx_id = current_ctx_id();  // the lookup made the device's primary context current if none was
   }
-  *out = g_scratch[dev];
+  *out = d.ptr;
   return cudaSuccess;
 }
 

@@ -8,7 +8,7 @@ namespace pipe {
 constexpr int kCWarps = 16;                     // warps per block
 constexpr int kThreads = kCWarps * 32;
 constexpr int kMaxSlots = 8;                    // ring slots per warp
-constexpr uint32_t kSpinLimit = 1u << 22;       // mbarrier polls before a wait is declared stuck
+constexpr uint32_t kSpinLimit = kWaitPolls;     // mbarrier polls before a wait is declared stuck
 constexpr float kCodeUnit = 16777216.0f;        // 2^24
 
 template <int WFMT>
@@ -45,9 +45,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase of the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Bounded wait for the phase of the given parity to complete (at most `limit` polls).
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(b, parity)) return true;
   return false;
 }

@@ -95,3 +95,25 @@ def test_binding_structs_match_the_header(struct, cls):
     size, offs = _c_layout(struct, fields)
     assert ctypes.sizeof(c) == size, (struct, ctypes.sizeof(c), size)
     assert [getattr(c, f).offset for f in fields] == offs, struct
+
+
+def test_noalloc_documented_limits_follow_the_slab_rule():
+    """The K limits the header states for mag_load_weights_f32_noalloc follow from its slab rule: one slab of
+    whole 16-row tiles (QKV: one head, d/16 tiles) of 16 * ceil(K/32) * 20 bytes each must fit the scratch."""
+    import re
+    hdr = open(os.path.join(ROOT, "include", "mag.h")).read()
+    doc = hdr[hdr.index("mag_load_weights with MAG_FMT_F32_DENSE"):hdr.index("mag_status mag_load_weights_f32_noalloc")]
+    doc = " ".join(doc.replace("*", " ").split())
+    scratch_src = open(os.path.join(ROOT, "quantized_decode_step_gb300", "csrc", "noalloc.h")).read()
+    m = re.search(r"kNoAllocScratchBytes = (\d+)u << (\d+);", scratch_src)
+    scratch = int(m.group(1)) << int(m.group(2))
+    assert f"{scratch >> 20} MiB" in doc
+
+    def max_k(tiles_per_slab):
+        return 32 * (scratch // (16 * 20 * tiles_per_slab))
+
+    stated = [int(x.replace(",", "")) for x in re.findall(r"(\d{2,3},\d{3})", doc)]
+    assert stated == [max_k(1), max_k(128 // 16), max_k(64 // 16)], stated
+    # one more group past each limit no longer fits
+    for tiles, k in ((1, max_k(1)), (8, max_k(8)), (4, max_k(4))):
+        assert 16 * 20 * tiles * (k // 32) <= scratch < 16 * 20 * tiles * (k // 32 + 1)
