@@ -590,7 +590,7 @@ def run_configs(args, ctx_main, stream, hbm, tc) -> dict:
 
 def prefill_flops(shape, prior: int, T: int) -> float:
     """Algorithmic FLOPs of one chunk: 2 T N K over the projections, QK^T and PV over the causal key
-    ranges, and the last token's LM head (the two-term weight copy's second pass is not counted)."""
+    ranges, and the last token's LM head."""
     D, F, d = shape.hidden, shape.ffn, shape.head_dim
     per_layer = shape.qkv_rows * D + D * shape.n_heads * d + 2 * F * D + D * F
     keys = T * (prior + 1) + T * (T - 1) // 2

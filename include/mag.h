@@ -205,9 +205,10 @@ mag_status mag_decode_step_host(mag_ctx* ctx, int32_t batch, const int32_t* sess
  * output (logits, or the hidden state when vocab == 0) of the chunk's last
  * token to last_out_dev. hidden_in_dev is fp16 [n_tokens][D]; the chunk's K/V
  * are stored in the pool like mag_kv_append's (the same quantisers). The
- * projections run as tensor-core GEMMs over an exact two-term fp16 copy of
- * every W4 matrix (hi + lo = s q + m), made at load time when max_chunk > 0
- * (4 bytes per weight; mag_get_memory_stats reports it). Stream-ordered.
+ * projections run as tensor-core GEMMs that read the W4 weights the decode
+ * step reads and expand them in shared memory to fp16(s q + m), one rounding
+ * per weight (no weight copy is kept; mag_get_memory_stats reports 0 for it).
+ * Stream-ordered.
  * Errors: INVALID_ARG, CONTEXT_FULL, KV_FULL, NOT_LOADED, UNSUPPORTED (created
  * with max_chunk = 0), CUDA. */
 mag_status mag_prefill_chunk(mag_ctx* ctx, int32_t session, int32_t n_tokens, const void* hidden_in_dev,
@@ -252,7 +253,7 @@ typedef struct mag_memory_stats {
   uint64_t arena_unshared_bytes; /* sum of the arena tensors' sizes (no reuse) */
   uint64_t other_device_bytes; /* block tables, RoPE table, counters, step arguments */
   int32_t sessions_open;
-  uint64_t prefill_weight_bytes; /* exact two-term fp16 weight copies of the prefill GEMM (max_chunk > 0) */
+  uint64_t prefill_weight_bytes; /* weight copies kept for the prefill GEMM: 0 (it reads the W4 tiles) */
   uint64_t prefill_arena_bytes;  /* planned prefill activation arena (max_chunk rows) */
   /* KV pool memory: a fixed pool has it all mapped; an elastic one (MAG_FLAG_ELASTIC_POOL) maps groups of
    * pool_group_blocks blocks: the hot ones (pool_blocks_hot) stay, others come and go with demand */

@@ -153,17 +153,7 @@ struct mag_ctx {
   std::string cap_err;
   cudaStream_t cap_stream = nullptr;
   uint64_t other_bytes = 0;
-  // chunked prefill (max_chunk > 0): exact two-term fp16 weight copies, their TMA maps, planned buffers
-  struct PrefillProj {
-    __half* hi = nullptr;
-    __half* lo = nullptr;
-    int rows = 0;  // copy rows: a multiple of 128
-    alignas(64) uint8_t map_hi[128];
-    alignas(64) uint8_t map_lo[128];
-  };
-  std::vector<PrefillProj> pproj;  // [L][4]
-  uint8_t* pf_w = nullptr;
-  size_t pf_wbytes = 0;
+  // chunked prefill (max_chunk > 0): planned buffers and the activations' TMA maps (the GEMMs read the W4 tiles)
   uint8_t* pf_arena = nullptr;
   uint64_t pf_arena_bytes = 0;
   std::vector<ArenaTensor> pf_plan;
@@ -173,6 +163,8 @@ struct mag_ctx {
   __half* pf_o = nullptr;
   __half* pf_act = nullptr;
   int32_t* pf_rows = nullptr;   // [2][max_chunk]: position and session of every row (several sessions)
+  float* pf_part = nullptr;     // split-K GEMMs: partial sums of the two K halves
+  uint32_t* pf_part_cnt = nullptr;
   float* pf_last_r = nullptr;   // [MAG_MAX_BATCH][D]: the sessions' last residual rows, gathered
   alignas(64) uint8_t map_xn[128];
   alignas(64) uint8_t map_o[128];
@@ -537,9 +529,10 @@ void free_ctx(mag_ctx* c) {
   cudaFree(c->d_out_stage);
   if (c->h_ring) cudaFreeHost(c->h_ring);
   if (c->h_err) cudaFreeHost(c->h_err);
-  cudaFree(c->pf_w);
   cudaFree(c->pf_arena);
   cudaFree(c->pf_rows);
+  cudaFree(c->pf_part);
+  cudaFree(c->pf_part_cnt);
   cudaFree(c->pf_last_r);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   delete c;
@@ -573,7 +566,9 @@ mag_status check_cfg(const mag_config* g, std::string& why) {
 namespace {
 
 // ---------------------------------------------------------------- chunked prefill set-up
-// Copy rows of projection kind i: a multiple of the GEMM tile; gate-up interleaves gate and up in blocks of 64.
+// GEMM rows of projection kind i: the tile rows of its 16-row decode tiles, 8 tiles to a 128-row GEMM tile (QKV:
+// one head of d = 128 or two of 64, RoPE pairs (i, i + d/2) in canonical order; gate-up: gate and up rows
+// interleaved in blocks of 64), padded to a whole GEMM tile.
 int prefill_rows(const mag_ctx* c, int i) {
   const int t = tc_gemm_rows_multiple();
   if (i == 2) return (c->F + 63) / 64 * 128;
@@ -596,28 +591,7 @@ void build_prefill_plan(mag_ctx* c) {
 }
 
 mag_status setup_prefill(mag_ctx* c) {
-  const int Ks[4] = {c->D, c->Hq * c->d, c->D, c->F};
-  size_t total = 0;
-  std::vector<size_t> offs;
-  for (int l = 0; l < c->L; ++l)
-    for (int i = 0; i < 4; ++i) {
-      offs.push_back(total);
-      total = align256(total + (size_t)prefill_rows(c, i) * Ks[i] * 2 * 2);
-    }
-  cudaError_t e = dev_malloc(&c->pf_w, std::max<size_t>(total, 256));
-  if (e != cudaSuccess) return fail(c, MAG_ERR_OOM, "prefill weights: device allocation of %zu bytes: %s", total, cudaGetErrorString(e));
-  c->pf_wbytes = total;
-  cudaMemsetAsync(c->pf_w, 0, total, c->stream);  // padding rows stay zero
-  c->pproj.resize((size_t)c->L * 4);
-  for (int l = 0; l < c->L; ++l)
-    for (int i = 0; i < 4; ++i) {
-      auto& pp = c->pproj[(size_t)l * 4 + i];
-      pp.rows = prefill_rows(c, i);
-      pp.hi = reinterpret_cast<__half*>(c->pf_w + offs[(size_t)l * 4 + i]);
-      pp.lo = pp.hi + (size_t)pp.rows * Ks[i];
-      if (!make_tmap_2d(pp.map_hi, pp.hi, pp.rows, Ks[i]) || !make_tmap_2d(pp.map_lo, pp.lo, pp.rows, Ks[i]))
-        return fail(c, MAG_ERR_CUDA, "prefill: tensor map encoding failed (layer %d, projection %d)", l, i);
-    }
+  cudaError_t e;
   build_prefill_plan(c);
   if ((e = dev_malloc(&c->pf_arena, std::max<uint64_t>(c->pf_arena_bytes, 256))) != cudaSuccess)
     return fail(c, MAG_ERR_OOM, "prefill arena: %s", cudaGetErrorString(e));
@@ -640,15 +614,13 @@ mag_status setup_prefill(mag_ctx* c) {
       (e = dev_malloc(&c->pf_last_r, (size_t)MAG_MAX_BATCH * c->D * 4)) != cudaSuccess)
     return fail(c, MAG_ERR_OOM, "prefill row tables: %s", cudaGetErrorString(e));
   c->other_bytes += (size_t)2 * T * 4 + (size_t)MAG_MAX_BATCH * c->D * 4;
+  // GEMMs whose output blocks fill at most half the SMs split K in two, merged through a workspace
+  const size_t pf = tc_gemm_part_floats(c->n_sm), pc = (size_t)(c->n_sm / 2) * 4;
+  if ((e = dev_malloc(&c->pf_part, pf * 4)) != cudaSuccess || (e = dev_malloc(&c->pf_part_cnt, pc * 4)) != cudaSuccess)
+    return fail(c, MAG_ERR_OOM, "prefill split-K workspace: %s", cudaGetErrorString(e));
+  cudaMemsetAsync(c->pf_part_cnt, 0, pc * 4, c->stream);
+  c->other_bytes += pf * 4 + pc * 4;
   return MAG_OK;
-}
-
-// After a projection's tiles are written: its two-term copy for the prefill GEMM.
-cudaError_t refresh_prefill_copy(mag_ctx* c, int layer, int tensor) {
-  if (c->cfg.max_chunk <= 0) return cudaSuccess;
-  const Proj& p = c->proj[(size_t)layer * 4 + tensor];
-  auto& pp = c->pproj[(size_t)layer * 4 + tensor];
-  return launch_w4_tiles_to_hilo(c->stream, p.tiles, p.N, p.K, p.map, p.map_arg, pp.hi, pp.lo);
 }
 
 }  // namespace
@@ -908,12 +880,10 @@ mag_status mag_load_weights(mag_ctx* c, int32_t tensor, int32_t layer, const voi
       cudaError_t e3 = cudaFreeAsync(canon, c->stream);
       if (e2 != cudaSuccess || e3 != cudaSuccess)
         return fail(c, MAG_ERR_CUDA, "load_weights: %s", cudaGetErrorString(e2 != cudaSuccess ? e2 : e3));
-      CUDA_TRY(c, refresh_prefill_copy(c, layer, tensor));
     } else if (fmt == MAG_FMT_W4G32) {
       if (bytes != p.canon_bytes)
         return fail(c, MAG_ERR_INVALID_ARG, "load_weights: %zu bytes, expected W4G32 %zu", bytes, p.canon_bytes);
       CUDA_TRY(c, launch_w4_to_tiles(c->stream, (const uint8_t*)src, p.N, p.K, p.map, p.map_arg, p.tiles));
-      CUDA_TRY(c, refresh_prefill_copy(c, layer, tensor));
     } else {
       return fail(c, MAG_ERR_INVALID_ARG, "load_weights: projections take FP32_DENSE or W4G32");
     }
@@ -956,7 +926,6 @@ mag_status mag_load_weights_f32_noalloc(mag_ctx* c, int32_t tensor, int32_t laye
     return fail(c, MAG_ERR_INVALID_ARG, "load_weights_f32_noalloc: make the context's device %d current (not %d)",
                 c->device, dev);
   CUDA_TRY(c, load_f32_noalloc(c->stream, (const float*)src, p.N, p.K, p.map, p.map_arg, p.tiles));
-  CUDA_TRY(c, refresh_prefill_copy(c, layer, tensor));
   c->loaded[(size_t)layer * 6 + tensor] = 1;
   return MAG_OK;
 }
@@ -1378,15 +1347,34 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
   CUDA_TRY(c, launch_rows_to_resid(L, (const __half*)in, c->pf_r, T, D));
   CUDA_TRY(c, dump(0));
   for (int l = 0; l < c->L; ++l) {
-    const auto* pp = &c->pproj[(size_t)l * 4];
+    const Proj* P = &c->proj[(size_t)l * 4];
     TcGemmArgs g = {};
     g.M = T;
     g.err = c->d_err;
+    g.wait_limit = c->wait_limit;
+    // the GEMM's weights: projection i's decode tiles, their rows in the order its epilogue wants
+    auto weights = [&](TcGemmArgs& x, int i) {
+      const Proj& pr = P[i];
+      x.w = pr.tiles;
+      x.n_dtiles = pr.N / 16;
+      x.C = (pr.K + 63) / 64;
+      x.N = prefill_rows(c, i);
+      x.K = pr.K;
+      x.ksplit = tc_gemm_ksplit(x.M, x.N, x.K, c->n_sm);
+      x.part = c->pf_part;
+      x.part_cnt = c->pf_part_cnt;
+      if (pr.map == MAP_QKV) {
+        x.tpg = c->d / 16, x.gsz = c->d, x.half = c->d / 2;
+      } else if (pr.map == MAP_SWIGLU) {
+        x.tpg = 8, x.gsz = 128, x.half = 64;
+      } else {
+        x.tpg = 1, x.gsz = 16, x.half = 8;
+      }
+    };
     // RMSNorm + QKV (+ RoPE of q and k)
     CUDA_TRY(c, launch_rmsnorm_rows(L, c->pf_r, c->gamma1[l], c->cfg.rms_eps, T, D, c->pf_xn));
     TcGemmArgs gq = g;
-    gq.N = pp[0].rows;
-    gq.K = D;
+    weights(gq, 0);
     gq.n_valid = c->R;
     gq.out = c->pf_qkv;
     gq.ldo = c->R;
@@ -1396,7 +1384,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
     gq.row_pos = row_pos;
     gq.rope_cos = c->d_cos;
     gq.rope_sin = c->d_sin;
-    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_xn, pp[0].map_hi, pp[0].map_lo}, gq, EPI_QKV));
+    CUDA_TRY(c, launch_tc_gemm(L, c->map_xn, gq, EPI_QKV));
     // the chunk's k, v into the pool, then causal attention over the pool
     KvChunkArgs kc = {};
     kc.qkv = c->pf_qkv;
@@ -1422,29 +1410,26 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
     CUDA_TRY(c, launch_prefill_attention(L, pa));
     // O projection + residual
     TcGemmArgs go = g;
-    go.N = pp[1].rows;
-    go.K = HD;
+    weights(go, 1);
     go.n_valid = D;
     go.r = c->pf_r;
     go.ldr = D;
-    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_o, pp[1].map_hi, pp[1].map_lo}, go, EPI_RESID));
+    CUDA_TRY(c, launch_tc_gemm(L, c->map_o, go, EPI_RESID));
     // RMSNorm + gate-up + SwiGLU
     CUDA_TRY(c, launch_rmsnorm_rows(L, c->pf_r, c->gamma2[l], c->cfg.rms_eps, T, D, c->pf_xn));
     TcGemmArgs gg = g;
-    gg.N = pp[2].rows;
-    gg.K = D;
+    weights(gg, 2);
     gg.n_valid = c->F;
     gg.out = c->pf_act;
     gg.ldo = c->F;
-    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_xn, pp[2].map_hi, pp[2].map_lo}, gg, EPI_SWIGLU));
+    CUDA_TRY(c, launch_tc_gemm(L, c->map_xn, gg, EPI_SWIGLU));
     // down projection + residual
     TcGemmArgs gd = g;
-    gd.N = pp[3].rows;
-    gd.K = c->F;
+    weights(gd, 3);
     gd.n_valid = D;
     gd.r = c->pf_r;
     gd.ldr = D;
-    CUDA_TRY(c, launch_tc_gemm(L, TcMaps{c->map_act, pp[3].map_hi, pp[3].map_lo}, gd, EPI_RESID));
+    CUDA_TRY(c, launch_tc_gemm(L, c->map_act, gd, EPI_RESID));
     CUDA_TRY(c, dump(l + 1));
   }
   // the output rows: contiguous for one session, else each session's last row gathered
@@ -1682,7 +1667,7 @@ mag_status mag_get_memory_stats(mag_ctx* c, mag_memory_stats* s) {
   s->arena_bytes = c->arena_bytes;
   s->arena_unshared_bytes = c->arena_unshared;
   s->other_device_bytes = c->other_bytes;
-  s->prefill_weight_bytes = c->pf_wbytes;
+  s->prefill_weight_bytes = 0;  // the prefill GEMMs read the W4 tiles themselves
   s->prefill_arena_bytes = c->pf_arena_bytes;
   int open = 0;
   for (auto& x : c->sessions) open += x.open;

@@ -143,48 +143,6 @@ __global__ void w4_tiles_kernel(const uint8_t* __restrict__ src, uint8_t* __rest
   }
 }
 
-// Exact two-term fp16 copy of a tiled W4 matrix for the prefill GEMM, one thread
-// per (tile, chunk, lane): w = s q + m (exact in fp32: a product of an fp16 and
-// a 4-bit integer plus an fp16), hi = fp16(w), lo = fp16(w - hi). Canonical
-// row r goes to copy row r, except MAP_SWIGLU: copy rows 128 j .. 128 j + 63
-// hold gate rows 64 j .., the next 64 the matching up rows (so that one
-// 128-row GEMM tile carries both halves of 64 SwiGLU outputs).
-__global__ void w4_tiles_to_hilo_kernel(const uint8_t* __restrict__ tiles, int N, int K, int map, int map_arg,
-                                        __half* __restrict__ hi, __half* __restrict__ lo) {
-  const int G = (K + 31) / 32, C = (K + 63) / 64, n_mt = N / 16;
-  const int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (id >= (int64_t)n_mt * C * 32) return;
-  const int lane = (int)(id & 31), g = lane >> 2, t = lane & 3;
-  const int64_t tc = id >> 5;
-  const int mt = (int)(tc / C), c = (int)(tc - (int64_t)mt * C);
-  int rg, rg8;
-  tile_rows(map, map_arg, mt, g, rg, rg8);
-  const uint8_t* tile = tiles + tc * kTileBytes;
-  const int rows[2] = {rg, rg8};
-  for (int h = 0; h < 2; ++h) {
-    const int r = rows[h];
-    int rp = r;
-    if (map == MAP_SWIGLU) {
-      const int F = map_arg, j = r < F ? r : r - F;
-      rp = (j / 64) * 128 + (r < F ? 0 : 64) + (j % 64);
-    }
-    for (int q = 0; q < 2; ++q) {
-      const int grp = 2 * c + q;
-      if (grp >= G) continue;
-      const uint32_t w = reinterpret_cast<const uint32_t*>(tile + lane * 16)[2 * h + q];
-      const __half2 sm = reinterpret_cast<const __half2*>(tile + 512 + g * 16)[2 * h + q];
-      const float s = __low2float(sm), mn = __high2float(sm);
-      for (int e = 0; e < 8; ++e) {
-        const int k = grp * 32 + 8 * t + e;
-        if (k >= K) break;
-        const float v = __fadd_rn(__fmul_rn(s, (float)((w >> (4 * e)) & 15u)), mn);
-        const __half hv = __float2half_rn(v);
-        hi[(int64_t)rp * K + k] = hv;
-        lo[(int64_t)rp * K + k] = __float2half_rn(__fsub_rn(v, __half2float(hv)));
-      }
-    }
-  }
-}
 
 // One thread per (tile, chunk, lane, row half): 16 fp16 values of row g (or g+8).
 __global__ void f16_tiles_kernel(const __half* __restrict__ src, int N, int K, uint8_t* __restrict__ dst) {
@@ -263,13 +221,6 @@ cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, in
 }  // namespace mag
 
 namespace mag {
-cudaError_t launch_w4_tiles_to_hilo(cudaStream_t s, const uint8_t* tiles, int N, int K, int map, int map_arg,
-                                    __half* hi, __half* lo) {
-  const int64_t n = (int64_t)(N / 16) * ((K + 63) / 64) * 32;
-  if (n == 0) return cudaSuccess;
-  w4_tiles_to_hilo_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(tiles, N, K, map, map_arg, hi, lo);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_f16_to_tiles(cudaStream_t s, const __half* src, int N, int K, uint8_t* tiles) {
   const int64_t n = (int64_t)(N / 16) * ((K + 63) / 64) * 64;

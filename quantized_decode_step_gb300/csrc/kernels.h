@@ -82,18 +82,20 @@ cudaError_t launch_w4_from_tiles(cudaStream_t s, const uint8_t* tiles, int N, in
 // 2048-byte tiles [N/16][ceil(K/64)]: lane L = (g, t) of a tile holds rows
 // g and g+8 at k = 64c + 16t .. 16t+15 (32 bytes each); k >= K is zero.
 cudaError_t launch_f16_to_tiles(cudaStream_t s, const __half* src, int N, int K, uint8_t* tiles);
-// Exact two-term fp16 copy (hi + lo = s q + m) of a tiled W4 matrix for the prefill GEMM, rows
-// in canonical order except MAP_SWIGLU (gate / up interleaved in blocks of 64). hi, lo: [N][K].
-cudaError_t launch_w4_tiles_to_hilo(cudaStream_t s, const uint8_t* tiles, int N, int K, int map, int map_arg,
-                                    __half* hi, __half* lo);
-
 // ---------------------------------------------------------------- chunked prefill (tcgen05)
-// Y = X W^T over an exact two-term weight copy, 128 x 128 tiles. M: tokens, N: copy rows (a multiple
-// of 128), K. Epilogues: EPI_QKV (fp16 out, q and k rotated at position pos0 + row), EPI_RESID
-// (r[row][n] += y), EPI_SWIGLU (out[row][j] = fp16(silu(gate) up) from interleaved copy rows).
+// Y = X W^T, X fp16 [M][K] by TMA, W read from the decode path's W4 tiles and expanded in shared memory
+// (fp16(s q + m)), 128 x 128 tiles. M: tokens, N: GEMM rows (a multiple of 128: the tile rows of 8
+// consecutive decode tiles, in the order the epilogue wants). Epilogues: EPI_QKV (fp16 out, q and k
+// rotated at position pos0 + row), EPI_RESID (r[row][n] += y), EPI_SWIGLU (out[row][j] = fp16(silu(gate)
+// up) from gate and up rows interleaved in blocks of 64).
 struct TcGemmArgs {
   int32_t M, N, K;
   int32_t n_valid;  // output columns that exist (RESID: N of the matrix; SWIGLU: F)
+  const uint8_t* w;   // the projection's tiles [n_dtiles][C][640]
+  int32_t n_dtiles;   // 16-row decode tiles
+  int32_t C;          // ceil(K / 64)
+  int32_t tpg, gsz, half;  // tile-row map: decode tile j (of 8) row g / g+8 -> GEMM row
+                           // (j / tpg) gsz + 8 (j % tpg) + g (+ half)
   float* r;
   int32_t ldr;
   __half* out;
@@ -103,16 +105,18 @@ struct TcGemmArgs {
   const float* rope_cos;
   const float* rope_sin;
   uint32_t* err;
-};
-struct TcMaps {
-  const void* a;  // 128-byte tensor maps: activations [M][K], weight hi [N][K], weight lo [N][K]
-  const void* hi;
-  const void* lo;
+  uint32_t wait_limit;  // polls of a main-loop wait before it gives up (drains always use kWaitPolls)
+  int32_t ksplit;       // 1, or 2: K in halves, merged through part (fp32 partial sums) by the later half
+  float* part;          // [blocks][4][2][2][128][32] (tc_gemm_part_floats)
+  uint32_t* part_cnt;   // [blocks][4], zero between launches
 };
 // A 2-D fp16 tensor map over row-major [rows][cols] with 64 x 128 boxes and 128-byte swizzle.
 bool make_tmap_2d(void* map_out, const void* base, int64_t rows, int64_t cols);
 int tc_gemm_rows_multiple();
-cudaError_t launch_tc_gemm(const Launch& L, const TcMaps& m, const TcGemmArgs& a, int epi);
+// K split of a GEMM of M tokens x N rows x K: 2 when the output blocks fill at most half the SMs
+int tc_gemm_ksplit(int M, int N, int K, int n_sm);
+size_t tc_gemm_part_floats(int n_sm);  // workspace of a split GEMM
+cudaError_t launch_tc_gemm(const Launch& L, const void* map_a, const TcGemmArgs& a, int epi);
 cudaError_t launch_rows_to_resid(const Launch& L, const __half* x, float* r, int T, int D);
 cudaError_t launch_rmsnorm_rows(const Launch& L, const float* r, const __half* gamma, float eps, int T, int D,
                                 __half* xn);

@@ -109,7 +109,8 @@ def test_tiny_prefill_chunks_then_decode(dt):
     wl = Workload(f"tiny-prefill-kv{dt}", TINY, dt, 1, (128,), chunk=160)
     ctx = _run(wl, 21 + dt, (37, 150))
     st = ctx.memory_stats()
-    assert st["prefill_weight_bytes"] > 0 and st["prefill_arena_bytes"] > 0
+    # the prefill GEMMs read the W4 tiles themselves: no weight copy
+    assert st["prefill_weight_bytes"] == 0 and st["prefill_arena_bytes"] > 0
 
 
 def test_tiny_prefill_on_empty_cache():
