@@ -139,6 +139,11 @@ struct mag_ctx {
     int launches = 0;
   };
   StepGraph graphs[2][3][MAG_MAX_BATCH + 1];
+  // without the adaptive runtime: graphs by [verify][context bucket][batch] (attention splits by the step's
+  // longest context)
+  static constexpr int kLenBuckets = 4;
+  StepGraph len_graphs[2][kLenBuckets][MAG_MAX_BATCH + 1];
+  int step_max_len = 0;  // longest context (position + 1) among the rows of the step being launched
   int last_launches = 0;
 
   // adaptive runtime: load profile, plan in use, background capture of a new plan's graphs
@@ -423,6 +428,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
   if ((e = dump(0)) != cudaSuccess) return e;
   const PoolGeom pg = pool_geom(c);
   const int S = splits;
+  const bool kv_by_qkv = !verify && c->cfg.kv_dtype == MAG_KV_FP16 && B <= kPipeMaxBatch;
   for (int l = 0; l < c->L; ++l) {
     const Proj* P = &c->proj[(size_t)l * 4];
     {  // RMSNorm + QKV + RoPE of q and k
@@ -435,6 +441,11 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
       a.n_rot_heads = c->Hq + c->Hkv;
       a.rope_cos = c->d_cos;
       a.rope_sin = c->d_sin;
+      // FP16 pool, decode rows on the pipelined GEMV: its epilogue also stores each row's key and value
+      a.kv_store = kv_by_qkv ? 1 : 0;
+      a.n_q_heads = c->Hq;
+      a.layer = l;
+      a.pool = pg;
       MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, XSRC_RESID, EPI_QKV));
     }
     if (verify) {  // the B tokens' k and v into the pool
@@ -460,7 +471,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
       a.layer = l;
       a.pool = pg;
       a.step = c->d_args;
-      a.stored = verify;
+      a.stored = verify ? 1 : (kv_by_qkv ? 2 : 0);
       a.wide = wide;
       // more splits than one cluster holds: clusters of at most 8 (which co-schedule more readily than
       // clusters of 16), merged by the last block to finish
@@ -510,6 +521,10 @@ void free_ctx(mag_ctx* c) {
   if (c->stream) cudaStreamSynchronize(c->stream);
   if (c->cap_thread.joinable()) c->cap_thread.join();
   for (auto& gv : c->graphs)
+    for (auto& gp : gv)
+      for (auto& g : gp)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+  for (auto& gv : c->len_graphs)
     for (auto& gp : gv)
       for (auto& g : gp)
         if (g.exec) cudaGraphExecDestroy(g.exec);
@@ -1026,10 +1041,12 @@ static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs&
   if (st != MAG_OK) return st;
   a.batch = B;
   a.n_upd = 0;
+  c->step_max_len = 0;
   for (int b = 0; b < B; ++b) {
     Session& s = c->sessions[sids[b]];
     a.sess[b] = sids[b];
     a.pos[b] = s.len;
+    c->step_max_len = std::max(c->step_max_len, s.len + 1);
     if (s.len % 16 == 0) {
       int blk = c->kv.pop();
       s.table.push_back(blk);
@@ -1038,6 +1055,7 @@ static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs&
       a.upd_blk[a.n_upd] = blk;
       ++a.n_upd;
     }
+    a.blk[b] = s.table[s.len / 16];
   }
   return MAG_OK;
 }
@@ -1068,6 +1086,22 @@ static int plan_splits(const mag_ctx* c, int p, int B) {
   const int s = c->adapt.enable_adaptive ? c->adapt.plan_splits[p] : 0;
   if (s == 0) return attn_splits(c, B, plan_wide(c, p));
   return std::max(1, std::min(s, 4 * c->n_sm / (B * c->Hkv)));
+}
+
+// Attention launch shape of the step being launched: the plan's with the adaptive runtime on; otherwise by
+// the step's longest context, about 76 pool blocks per split (measured on GB300: 16 splits, one cluster, up
+// to ~19k keys; 32 at ~39k; 64 at ~78k), so that long contexts keep enough warps streaming the pool.
+struct AttnShape {
+  int splits;
+  bool wide;
+  int bucket;  // -1: the adaptive plan's graphs
+};
+static AttnShape attn_shape(const mag_ctx* c, int B) {
+  if (c->adapt.enable_adaptive) return {plan_splits(c, c->cur_plan, B), plan_wide(c, c->cur_plan), -1};
+  const int nb = (c->step_max_len + 15) / 16, def = attn_splits(c, B);
+  const int bk = nb <= 16 * 76 ? 0 : (nb <= 32 * 76 ? 1 : (nb <= 48 * 76 ? 2 : 3));
+  const int s = bk == 0 ? def : std::max(def, std::min(16 * (bk + 1), 4 * c->n_sm / (B * c->Hkv)));
+  return {s, false, bk};
 }
 
 // Capture and instantiate the step graph of (verify, plan p, batch B) on stream st: the context's
@@ -1155,14 +1189,28 @@ static void adapt_after_step(mag_ctx* c, int B, const int32_t* lens) {
 // Launches the step of B rows whose arguments were just uploaded: the captured graph of that shape
 // under the plan in use (captured on first use), or the kernels one by one under MAG_FLAG_NO_GRAPH.
 static mag_status launch_step(mag_ctx* c, int B, bool verify) {
-  const int S = plan_splits(c, c->cur_plan, B);
+  const AttnShape sh = attn_shape(c, B);
   if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
     int n = 0;
-    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify, S, plan_wide(c, c->cur_plan), c->stream));
+    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify, sh.splits, sh.wide, c->stream));
     c->last_launches = n;
     return MAG_OK;
   }
-  mag_ctx::StepGraph& g = c->graphs[verify][c->cur_plan][B];
+  mag_ctx::StepGraph& g = sh.bucket < 0 ? c->graphs[verify][c->cur_plan][B] : c->len_graphs[verify][sh.bucket][B];
+  if (!g.exec && sh.bucket >= 0) {
+    cudaGraph_t gr = nullptr;
+    int n = 0;
+    cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      e = record_step(c, B, &n, nullptr, verify, sh.splits, sh.wide, c->stream);
+      const cudaError_t e2 = cudaStreamEndCapture(c->stream, &gr);
+      if (e == cudaSuccess) e = e2;
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&g.exec, gr, 0);
+    if (gr) cudaGraphDestroy(gr);
+    if (e != cudaSuccess) return fail(c, MAG_ERR_CUDA, "step graph capture: %s", cudaGetErrorString(e));
+    g.launches = n;
+  }
   if (!g.exec) CUDA_TRY(c, capture_graph(c, verify, c->cur_plan, B, c->stream, g));
   CUDA_TRY(c, cudaGraphLaunch(g.exec, c->stream));
   c->last_launches = g.launches;
@@ -1190,8 +1238,8 @@ mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, co
   if (st != MAG_OK) return st;
   Profiler prof;
   int n = 0;
-  CUDA_TRY(c, record_step(c, B, &n, &prof, false, plan_splits(c, c->cur_plan, B), plan_wide(c, c->cur_plan),
-                          c->stream));
+  const AttnShape sh = attn_shape(c, B);
+  CUDA_TRY(c, record_step(c, B, &n, &prof, false, sh.splits, sh.wide, c->stream));
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   *n_out = (int32_t)prof.kinds.size();
@@ -1210,8 +1258,8 @@ mag_status mag_debug_step_residuals(mag_ctx* c, int32_t B, const int32_t* sids, 
   mag_status st = step_upload(c, B, sids, in, out);
   if (st != MAG_OK) return st;
   int n = 0;
-  CUDA_TRY(c, record_step(c, B, &n, nullptr, false, plan_splits(c, c->cur_plan, B), plan_wide(c, c->cur_plan),
-                          c->stream, static_cast<float*>(resid)));
+  const AttnShape sh = attn_shape(c, B);
+  CUDA_TRY(c, record_step(c, B, &n, nullptr, false, sh.splits, sh.wide, c->stream, static_cast<float*>(resid)));
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   c->last_launches = n;
@@ -1226,6 +1274,13 @@ mag_status mag_debug_set_wait_limit(mag_ctx* c, int64_t polls) {
   if (v == c->wait_limit) return MAG_OK;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   // captured graphs hold the old limit in their kernel arguments: capture again on next use
+  for (auto& gv : c->len_graphs)
+    for (auto& gp : gv)
+      for (auto& g : gp)
+        if (g.exec) {
+          cudaGraphExecDestroy(g.exec);
+          g = mag_ctx::StepGraph{};
+        }
   for (auto& gv : c->graphs)
     for (auto& gp : gv)
       for (auto& g : gp)
@@ -1500,6 +1555,7 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
     a.sess[b] = sid;
     a.pos[b] = s.len + b;
   }
+  c->step_max_len = s.len + n;
   for (int i = nb_old; i < nb_new; ++i) {
     const int blk = c->kv.pop();
     s.table.push_back(blk);
@@ -1508,6 +1564,7 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
     a.upd_blk[a.n_upd] = blk;
     ++a.n_upd;
   }
+  for (int b = 0; b < n; ++b) a.blk[b] = s.table[(s.len + b) / 16];
   a.hidden_in = (const __half*)in;
   a.out = out;
   CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));

@@ -18,6 +18,7 @@ struct StepArgs {
   int32_t upd_sess[MAG_MAX_BATCH];  // block-table writes: table[upd_sess][upd_idx] = upd_blk
   int32_t upd_idx[MAG_MAX_BATCH];
   int32_t upd_blk[MAG_MAX_BATCH];
+  int32_t blk[MAG_MAX_BATCH];       // physical pool block of row b's new token (table[sess[b]][pos[b] / 16])
 };
 
 // KV pool geometry (block-major: (layer * P + block) * block_bytes, then

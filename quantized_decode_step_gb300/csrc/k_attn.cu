@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   const int n_keys = pos + 1, new_blk = pos >> 4;
   // blocks from fresh_blk on hold keys written in this step (the row's own, or with stored keys those of
   // the session's earlier rows as well); they are mapped and fetched only after the wait
-  const int fresh_blk = a.stored ? a.step->pos[0] >> 4 : new_blk;
+  const int fresh_blk = a.stored == 1 ? a.step->pos[0] >> 4 : new_blk;
   const int n_blocks = new_blk + 1;
   const int bps = (n_blocks + S * K - 1) / (S * K);
   const int blk0 = split * bps, blk1 = min(blk0 + bps, n_blocks);
@@ -329,13 +329,13 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
     issue_block<D, DT>(ring + issued * SG::kBytes, a.pool, a.layer, phys_of(issued), gk, lane);
     cp_async_commit();
   }
+  phys_new = a.step->blk[b];  // the host's copy of table[new_blk]: no table read after the wait
   pdl_wait();
   pdl_trigger();
-  phys_new = table[new_blk];
   const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
 
   // the block that holds the new token appends its K (rotated) and V to the pool
-  if (!a.stored && blk0 <= new_blk && new_blk < blk1) {
+  if (a.stored == 0 && blk0 <= new_blk && new_blk < blk1) {
     if (tid < D) {
       s_kv[0][tid] = qkv[(int64_t)(Hq + gk) * D + tid];
       s_kv[1][tid] = qkv[(int64_t)(Hq + Hkv + gk) * D + tid];

@@ -56,6 +56,12 @@ struct GemvArgs {
   int32_t t_max;          // most tiles of one block
   uint32_t* err;          // set (bit or) when a pipeline wait gives up
   uint32_t wait_limit;    // polls of a main-loop pipeline wait before it gives up (0: at once)
+  // EPI_QKV with an FP16 pool: when kv_store is set, row b's rotated k and its v also go into the pool at
+  // (layer, pos[b]) of session sess[b] (heads n_q_heads .. n_q_heads + 2 Hkv of the output)
+  int32_t kv_store;
+  int32_t n_q_heads;
+  int32_t layer;
+  PoolGeom pool;
 };
 
 // Polls of a bounded mbarrier wait before it is declared stuck (main-loop default; drain waits always).
@@ -200,6 +206,7 @@ struct AttnArgs {
   // 0: row b appends its own token (position pos[b]) and attends to 0 .. pos[b].
   // 1: the rows are consecutive new tokens of one session (pos[b] = pos[0] + b) whose keys and values an
   //    earlier kernel stored; row b attends causally to 0 .. pos[b] and appends nothing.
+  // 2: as 0, but the QKV projection already stored row b's own key and value in the pool.
   int32_t stored;
   // 0: 4 warps per block (two blocks per SM); 1: the wide variant, 8 warps per block at head_dim 128
   // (16 at 64), one block per SM, for long contexts

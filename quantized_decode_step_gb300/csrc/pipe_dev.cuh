@@ -272,16 +272,27 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs& a, int mt, const f
       const int ih = 8 * (mt - head * tiles_per_head) + g;
       const int row = head * a.head_dim + ih, row8 = row + a.head_dim / 2;
       __half* o = a.out_h + (int64_t)tok * a.ldo;
+      __half y0, y1;
       if (head < a.n_rot_heads) {
         // round as the fp16 projection output, then rotate
         const float x0 = __half2float(__float2half_rn(lo)), x1 = __half2float(__float2half_rn(hi));
         const int pos = a.step->pos[tok], hd = a.head_dim / 2;
         const float cs = a.rope_cos[(int64_t)pos * hd + ih], sn = a.rope_sin[(int64_t)pos * hd + ih];
-        o[row] = __float2half_rn(x0 * cs - x1 * sn);
-        o[row8] = __float2half_rn(x0 * sn + x1 * cs);
+        y0 = __float2half_rn(x0 * cs - x1 * sn);
+        y1 = __float2half_rn(x0 * sn + x1 * cs);
       } else {
-        o[row] = __float2half_rn(lo);
-        o[row8] = __float2half_rn(hi);
+        y0 = __float2half_rn(lo);
+        y1 = __float2half_rn(hi);
+      }
+      o[row] = y0;
+      o[row8] = y1;
+      if (a.kv_store && head >= a.n_q_heads) {  // the token's own key (rotated) or value, into the FP16 pool
+        const int Hkv = a.pool.n_kv_heads, which = head >= a.n_q_heads + Hkv ? 1 : 0;
+        const int kvh = head - a.n_q_heads - which * Hkv, pos = a.step->pos[tok];
+        const int blk = a.step->blk[tok];
+        __half* v = reinterpret_cast<__half*>(pool_vec(a.pool, a.layer, blk, which, kvh, pos & 15));
+        v[ih] = y0;
+        v[ih + a.head_dim / 2] = y1;
       }
     }
   }
