@@ -42,8 +42,8 @@ struct Session {
 };
 
 struct GemvPlan {
-  int n_cta, stages, t_max;  // pipelined kernel (batch <= kPipeMaxBatch); n_cta = 0 otherwise
-  int ks, cpc, tpw;          // k-split kernel
+  int n_cta, stages, t_max;  // pipelined kernels (up to kPipeMaxBatch tokens; W4 above); n_cta = 0 otherwise
+  int ks, cpc, tpw;          // k-ranges (W4 above kPipeMaxBatch: windows) and their chunks; fp16 k-split tpw
   size_t smem;
 };
 
@@ -206,8 +206,10 @@ mag_status check_err(mag_ctx* c) {
 
 // Launch shape of one projection at batch B. Up to kPipeMaxBatch tokens: the
 // pipelined kernel, one block per SM over contiguous tile ranges, its per-warp
-// rings as deep as a shared-memory budget allows. Above that a k-split grid
-// whose staged activation slice fits in 64 KB of shared memory.
+// rings as deep as a shared-memory budget allows. W4 above that: k-windows whose
+// staged activations fit in 64 KB, times tile ranges, about one block per SM,
+// rings as deep as the rest of the block's shared memory allows. The fp16 LM
+// head above 4 tokens: a k-split grid of 8-warp blocks.
 constexpr size_t kPipeBudget = 200 * 1024, kSmemMax = 227 * 1024;
 
 GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
@@ -225,6 +227,33 @@ GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
     p.smem = gemv_pipe_smem_bytes(wfmt, B, n_chunks, p.stages, p.t_max);
     p.ks = 1;
     p.cpc = n_chunks;
+    return p;
+  }
+  if (kind != 4) {
+    // window: a multiple of 4 chunks whose B token rows fit in 64 KB of fp16
+    const int cw_max = std::max(4, (int)((64 * 1024) / ((size_t)B * 128)) / 4 * 4);
+    const int kw0 = (n_chunks + cw_max - 1) / cw_max;
+    // windows x tile ranges closest to one block per SM (fewest windows on a tie)
+    int best_kw = kw0, best_blocks = 0;
+    for (int kw = kw0; kw <= kw0 + 3; ++kw) {
+      const int cw = ((n_chunks + kw - 1) / kw + 3) / 4 * 4;
+      const int kw_eff = (n_chunks + cw - 1) / cw;
+      const int tr = std::max(1, std::min(n_mtiles, c->n_sm / kw_eff));
+      if (kw != kw0 && kw_eff * tr > c->n_sm) continue;  // more windows only while they fill idle SMs
+      if (kw_eff * tr > best_blocks) {
+        best_blocks = kw_eff * tr;
+        best_kw = kw_eff;
+      }
+    }
+    p.cpc = ((n_chunks + best_kw - 1) / best_kw + 3) / 4 * 4;
+    p.ks = (n_chunks + p.cpc - 1) / p.cpc;
+    p.n_cta = std::max(1, std::min(n_mtiles, c->n_sm / p.ks));
+    p.t_max = (n_mtiles + p.n_cta - 1) / p.n_cta;
+    const size_t base = gemv_batch_smem_bytes(B, p.cpc, 0, p.t_max);
+    const size_t stage = gemv_batch_stage_bytes();
+    const int fit = kSmemMax > base ? (int)((kSmemMax - base) / stage) : 0;
+    p.stages = std::max(2, std::min(gemv_batch_max_stages(), fit));
+    p.smem = gemv_batch_smem_bytes(B, p.cpc, p.stages, p.t_max);
     return p;
   }
   const int max_cpc = std::max(1, (64 * 1024) / (B * 136) - 1);
@@ -317,7 +346,7 @@ size_t gemv_partial_floats(const mag_ctx* c, int B) {
   const int nt = B > 8 ? 2 : 1;
   for (auto& ps : proj_shapes(c)) {
     GemvPlan p = plan_gemv(c, ps.kind, ps.n_mtiles, ps.K, B);
-    if (p.n_cta == 0 && p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
+    if (B > kPipeMaxBatch && p.ks > 1) mx = std::max(mx, (size_t)p.ks * ps.n_mtiles * 32 * 4 * nt);
   }
   return mx;
 }
@@ -325,7 +354,7 @@ size_t gemv_partial_floats(const mag_ctx* c, int B) {
 // Shared memory of the pipelined kernel for every projection and batch must fit one block.
 bool gemv_plans_fit(const mag_ctx* c, std::string& why) {
   for (auto& ps : proj_shapes(c))
-    for (int B = 1; B <= std::min(kPipeMaxBatch, c->B_max); ++B) {
+    for (int B = 1; B <= c->B_max; ++B) {
       const GemvPlan p = plan_gemv(c, ps.kind, ps.n_mtiles, ps.K, B);
       if (p.smem > kSmemMax) {
         char b[160];
@@ -338,7 +367,7 @@ bool gemv_plans_fit(const mag_ctx* c, std::string& why) {
   return true;
 }
 
-// Counter slots: one per block column (k-split).
+// Counter slots: one per tile (W4 k-windows) or block column (fp16 k-split).
 size_t gemv_counters(const mag_ctx* c) {
   size_t mx = 1;
   for (auto& ps : proj_shapes(c)) mx = std::max(mx, (size_t)ps.n_mtiles);

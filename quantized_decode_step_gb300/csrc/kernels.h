@@ -28,9 +28,9 @@ struct GemvArgs {
   int32_t n_mtiles;       // 16-row tiles
   int32_t K;              // reduction length
   int32_t n_chunks;       // ceil(K / 64)
-  int32_t chunks_per_cta; // k-split: k-range of one block, in chunks
-  int32_t ks;             // k-split: splits (grid.y)
-  int32_t tpw;            // k-split: tiles per warp (1, 2 or 4); a block covers 8 tpw tiles
+  int32_t chunks_per_cta; // above 4 tokens: k-range of one block, in chunks (W4: a multiple of 4)
+  int32_t ks;             // above 4 tokens: k-ranges (fp16 k-split: grid.y; W4: k-windows)
+  int32_t tpw;            // fp16 k-split: tiles per warp (1, 2 or 4); a block covers 8 tpw tiles
   int32_t batch;
   // activations: XSRC_F16 fp16 [B][ldx]; XSRC_RESID RMSNorm of the fp32 residual
   const __half* x;
@@ -47,13 +47,13 @@ struct GemvArgs {
   int32_t head_dim, n_rot_heads;  // EPI_QKV: heads below n_rot_heads get RoPE
   const float* rope_cos;
   const float* rope_sin;
-  float* partial;         // k-split: [ks][n_mtiles][32][4 * n_tiles]
-  uint32_t* counters;     // zero between launches
+  float* partial;         // fp16 k-split: [ks][n_mtiles][32][4 * n_tiles]; W4: [n_mtiles][ks][32][4 * n_tiles]
+  uint32_t* counters;     // zero between launches (fp16 k-split: per block column; W4: per tile)
   const StepArgs* step;
-  // pipelined kernel (batch <= kPipeMaxBatch): one block per SM
-  int32_t n_cta;          // blocks; block i owns tiles [i n_mtiles / n_cta, (i+1) n_mtiles / n_cta)
-  int32_t stages;         // ring slots per warp (2..8)
-  int32_t t_max;          // most tiles of one block
+  // pipelined kernels (up to 4 tokens; W4 above 4 tokens): one block per SM
+  int32_t n_cta;          // tile ranges; range i holds tiles [i n_mtiles / n_cta, (i+1) n_mtiles / n_cta)
+  int32_t stages;         // ring slots per warp (2..8; W4 above 4 tokens 2..4)
+  int32_t t_max;          // most tiles of one range
   uint32_t* err;          // set (bit or) when a pipeline wait gives up
   uint32_t wait_limit;    // polls of a main-loop pipeline wait before it gives up (0: at once)
   // EPI_QKV with an FP16 pool: when kv_store is set, row b's rotated k and its v also go into the pool at
@@ -72,7 +72,14 @@ int gemv_pipe_max_stages();
 size_t gemv_pipe_slot_bytes(int wfmt);  // ring bytes of one slot across the block's warps
 cudaError_t launch_gemv_pipe(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi);
 
+// W4 above 4 tokens (k_gemv_batch.cu): grid n_cta tile ranges x ks k-windows of chunks_per_cta chunks.
+size_t gemv_batch_smem_bytes(int batch, int cw, int stages, int t_max);
+int gemv_batch_max_stages();
+size_t gemv_batch_stage_bytes();  // ring bytes of one slot across the block's warps
+cudaError_t launch_gemv_batch(const Launch& L, const GemvArgs& a, int xsrc, int epi);
+
 size_t gemv_smem_bytes(const GemvArgs& a, int wfmt);
+// Up to 4 tokens: the pipelined kernels; above: W4 k-windows, fp16 (LM head) k-split.
 cudaError_t launch_gemv(const Launch& L, const GemvArgs& a, int wfmt, int xsrc, int epi);
 
 // Load-time repack of a W4G32 matrix [N, K] (codes [N][16G] then (scale, min)

@@ -249,9 +249,9 @@ def test_8b_agent_batch16_quantized_kv(dt):
 
 @pytest.mark.parametrize("n", [8, 6])
 def test_8b_two_layers_agent_batch_k_split(n):
-    """8 and 6 sessions of the agent batch on two layers (FP16, strict bar): the k-split GEMVs with one
-    token n-tile; at 8 the gate-up takes two tiles per warp over 2 k-ranges, and at both the LM head four
-    tiles per warp with a ragged last block."""
+    """8 and 6 sessions of the agent batch on two layers (FP16, strict bar): the W4 GEMVs with one 8-token
+    column tile, the whole K of QKV / O / gate-up staged per block and the down projection as 4 k-windows of
+    56 chunks; the fp16 LM head's k-split with four tiles per warp and a ragged last block."""
     base = agent_batch(SEED)
     wl = Workload(f"8b2L-b{n}-agent-fp16", shrink(LLAMA8B, n_layers=2), KV_FP16, n, base.prior[:n],
                   scattered_pool=True)

@@ -141,9 +141,13 @@ def test_tiny_small_batches(B):
     _run_decode(wl, 15 + B, n_steps=2)
 
 
-def test_tiny_batch16():
-    wl = Workload("tiny-b16", TINY, KV_FP16, 16, tuple(range(3, 3 + 16 * 9, 9)), scattered_pool=True)
-    _run_decode(wl, 14, n_steps=1)
+@pytest.mark.parametrize("B", [11, 16])
+def test_tiny_batch_two_token_tiles(B):
+    """11 and 16 sessions: the W4 GEMVs run two 8-token MMA column tiles (at 11 the last five columns repeat
+    the last session's row and are dropped); the 688-wide FFN's down projection runs as three k-windows
+    whose tile sums meet in global memory."""
+    wl = Workload(f"tiny-b{B}", TINY, KV_FP16, B, tuple(range(3, 3 + B * 9, 9)), scattered_pool=True)
+    _run_decode(wl, 14, n_steps=2 if B == 11 else 1)
 
 
 @pytest.mark.parametrize("dt", [KV_FP16, KV_INT8, KV_INT4])
