@@ -6,10 +6,12 @@
 // themselves ("5. Core modules" 5.1: 4-bit weights, FP16 activations): the GEMM
 // reads the decode path's 640-byte tiles (16 rows x 64 k: codes, then fp16 (scale,
 // min) pairs) and eight warps of every block expand each 128-row x 64-k slice of
-// them into the fp16 operand in shared memory, w = fp16(s q + m) with one rounding
-// (fma.rn.f16x2 of the exact code), in the 128-byte-swizzled K-major layout the
-// tensor core reads. One expanded slice serves two 128-token tiles, so the ALU
-// work is a quarter of the MMA time and the weights stream from HBM once per pair.
+// them into two fp16 operands in shared memory, hi = fp16(w) and lo = fp16(w - hi)
+// of the exact w = s q + m (so hi + lo is w to 2^-22; one fp16 term alone rounds
+// every weight, which 32 layers amplify past the parity bar), in the 128-byte-
+// swizzled K-major layout the tensor core reads; every k-step accumulates X hi^T
+// and X lo^T. One expanded slice serves two 128-token tiles, and the weights
+// stream from HBM once per pair.
 //
 // GEMM block (persistent, one per SM): a unit is 128 weight rows x up to 256
 // tokens (two 128-token tiles), K in steps of 64. Warp 0 issues the TMA loads of
