@@ -197,10 +197,15 @@ mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...) {
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // After a synchronisation: a kernel whose bounded wait gave up left a bit in the error word.
+// The arrival counters of the last-to-arrive merges (GEMV tiles, attention clusters, prefill split-K) may be
+// left part-way by a role that gave up: they start again from zero.
 mag_status check_err(mag_ctx* c) {
   const uint32_t e = *reinterpret_cast<volatile uint32_t*>(c->h_err);
   if (e == 0) return MAG_OK;
   *reinterpret_cast<volatile uint32_t*>(c->h_err) = 0;
+  cudaMemsetAsync(c->d_counters, 0, c->n_counters * 4, c->stream);
+  cudaMemsetAsync(c->attn_arrivals, 0, (size_t)c->B_max * c->Hkv * 4, c->stream);
+  if (c->pf_part_cnt) cudaMemsetAsync(c->pf_part_cnt, 0, (size_t)(c->n_sm / 2) * 4 * 4, c->stream);
   return fail(c, MAG_ERR_TIMEOUT, "a kernel's pipeline wait gave up (code 0x%x)", e);
 }
 

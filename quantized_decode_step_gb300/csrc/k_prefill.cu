@@ -247,8 +247,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int p = 0; p < nt; ++p) tma_2d(st + p * TILE_A, &map_a, kb * BK, m0 + p * BM, a_full + s);
         }
       }
-      if (!ok)  // leave no copy in flight: the last load of every slot has landed
-        for (int f = max(0, g - STAGES_A); f < g; ++f) mb_wait(a_full + f % STAGES_A, (f / STAGES_A) & 1);
+      // leave no copy in flight, also when a consumer gave up and will not wait for them: the last load of
+      // every slot has landed (at once on the normal path, where the MMA thread has waited for them)
+      for (int f = max(0, g - STAGES_A); f < g; ++f) mb_wait(a_full + f % STAGES_A, (f / STAGES_A) & 1);
     }
   } else if (warp == kLoadWarp) {
     // ---- raw W4 slices: the 8 decode tiles of a unit's weight tile at k-step kb (640 bytes each, one bulk
@@ -274,8 +275,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                      raw_full + r);
         }
       }
-      if (!ok)  // leave no copy in flight
-        for (int f = max(0, g - kRawSlots); f < g; ++f) mb_wait(raw_full + f % kRawSlots, (f / kRawSlots) & 1);
+      // leave no copy in flight, also when the expansion gave up and will not wait for them
+      for (int f = max(0, g - kRawSlots); f < g; ++f) mb_wait(raw_full + f % kRawSlots, (f / kRawSlots) & 1);
     }
   } else if (warp >= kDeqWarp0) {
     // ---- W4 expansion: this warp's decode tile (16 rows) of every 128-row x 64-k slice, two slices per pass

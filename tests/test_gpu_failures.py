@@ -5,6 +5,11 @@
   waits for the copies it has in flight within the built-in bound and returns; mag_sync reports
   MAG_ERR_TIMEOUT, and with the limit restored and the step's token dropped the context decodes on
   against the oracle. Nothing waits without a bound, so nothing can hang.
+* The prefill GEMM's waits give up the same way (every role: the activation and weight copies, the
+  expansion, the MMA thread, the epilogue). Each copy issuer waits for its own copies to land before the
+  block exits, the MMA thread for its MMAs, so the block frees its tensor memory with nothing in flight;
+  the arrival counters of the split-K merges are reset after the timeout is reported. With the limit
+  restored the same chunk, and a decode step after it, match the oracle.
 * Allocation failures injected on the host (mag_debug_fail_allocations), never a real out-of-memory:
   - mag_create failing at each of its allocations in turn (fixed and elastic pools, prefill enabled)
     returns MAG_ERR_OOM and leaves the device memory as it found it;
@@ -75,6 +80,38 @@ def test_pipeline_wait_gives_up_then_context_recovers(flags):
         ctx.sync()
         ref = oracle.forward(cfg, w, [kv], [1], x, c, s)
         _check_vs_oracle(out.cpu().numpy(), ref, f"step {step} after the timeout")
+    ctx.close()
+
+
+def test_prefill_wait_gives_up_then_context_recovers():
+    wl = Workload("tiny-prefill-timeout", TINY, KV_FP16, 1, (128,), chunk=64)
+    shape, T = wl.shape, 48
+    ctx, sids = driver.setup(wl, SEED, extra_tokens=T + 4)
+    sid, p = sids[0], wl.prior[0]
+    x = synth.hidden_f16(SEED, T, shape.hidden, tag="timeout-chunk")
+    out = torch.empty(shape.hidden, dtype=torch.float16, device="cuda")
+    ctx.set_wait_limit(0)
+    ctx.prefill_chunk(sid, T, torch.from_numpy(x).cuda(), out)
+    with pytest.raises(mag.MagError) as e:
+        ctx.sync()
+    assert e.value.status == mag.ERR_TIMEOUT and "gave up" in str(e.value)
+    ctx.sync()
+    ctx.set_wait_limit(-1)
+    ctx.session_truncate(sid, p)
+    cfg = model_cfg(shape, wl.kv_dtype)
+    kv = oracle.KV(cfg, p + T + 8)
+    kv.append(*prior_kv(shape, SEED, 0, p))
+    w = oracle_weights(shape, SEED)
+    c, s = oracle.rope_table(p + T + 8, shape.head_dim, shape.rope_base)
+    ctx.prefill_chunk(sid, T, torch.from_numpy(x).cuda(), out)
+    ctx.sync()
+    assert ctx.session_length(sid) == p + T
+    _check_vs_oracle(out.cpu().numpy(), oracle.forward(cfg, w, [kv], [T], x, c, s)[0], "the chunk after the timeout")
+    x1 = synth.hidden_f16(SEED, 1, shape.hidden, tag="timeout-after")
+    out1 = torch.empty((1, shape.hidden), dtype=torch.float16, device="cuda")
+    ctx.decode_step([sid], torch.from_numpy(x1).cuda(), out1)
+    ctx.sync()
+    _check_vs_oracle(out1.cpu().numpy(), oracle.forward(cfg, w, [kv], [1], x1, c, s), "the step after the chunk")
     ctx.close()
 
 
