@@ -978,6 +978,10 @@ cudaError_t attn_prepare() {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes<D, DT, NW>());
   if (e != cudaSuccess) return e;
+  // the largest shared-memory carveout, as the GEMVs before and after use: an SM that switches carveouts
+  // between kernels must drain and reconfigure before the next kernel's blocks can start on it
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
