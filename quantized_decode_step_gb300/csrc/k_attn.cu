@@ -226,6 +226,13 @@ __device__ __forceinline__ uint32_t pair_tokens(const uint32_t* ra, const uint32
   return __byte_perm(ra[n >> 1], rb[n >> 1], (n & 1) ? 0x7632 : 0x5410);
 }
 
+// The 8 x 8 fp16 matrix held one row pair per lane (lane 4 r + c: row r, columns 2c, 2c+1), transposed.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // 8 codes of a word as exact fp16 integers in (k0,k4) (k1,k5) (k2,k6) (k3,k7) order.
 __device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
   const __half2 k1024 = __float2half2_rn(1024.0f);
@@ -242,17 +249,11 @@ __device__ __forceinline__ uint4 u4x8_codes(uint32_t w) {
 
 constexpr int kAttnSlots = 3;  // per-warp ring depth, in (block, KV head) units
 
-// Shared-memory image of the NW warps' partial outputs, [warp][head row][t][jj][n] with the t and head
-// strides padded so that the float4 stores of a quarter-warp fall into distinct banks. n is the PV
-// n-tile, (2t + jj) the column within it: dim = (2t + jj) NV + v_slot_dim(n). It and the block's
-// merged partial o [head][dim] reuse the rings' shared memory once every warp has left its loop.
+// Shared-memory image of the NW warps' partial outputs [warp][head (8)][dim] and the block's merged partial
+// o [head][dim]; both reuse the rings' shared memory once every warp has left its loop.
 template <int D, int NW>
 struct AccGeom {
-  static constexpr int kNV = D / 8;
-  static constexpr int kTS = 2 * kNV + 4;                         // floats per t
-  static constexpr int kRow = (4 * kTS + 16 + 31) / 32 * 32 + 16;  // floats per head row, = 16 mod 32
-  static constexpr int kWarp = 8 * kRow;
-  static constexpr size_t kAccBytes = (size_t)NW * kWarp * 4;
+  static constexpr size_t kAccBytes = (size_t)NW * 8 * D * 4;
   static constexpr size_t kBytes = kAccBytes + (size_t)8 * D * 4;  // + the partial o
 };
 
@@ -354,9 +355,12 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   }
   for (; issued < kAttnSlots; ++issued) cp_async_commit();  // one group per ring slot
 
-  // query fragments: rows = the G heads of this KV head, padded to 16 with zeros
-  uint32_t qa[2 * NS][2];
-  float qsum[NS];  // INT4: per 32-dim slab, the sum of this row's query values
+  // The heads are the MMAs' 8 columns (G <= 8 of them; zero queries past G) and the block's 16 tokens, or
+  // the head's dims, the 16 rows: S^T = K Q^T and O^T += V^T P^T, so no MMA row is padding.
+  // Query B fragments: lane (gi, t) holds head gi's dims 32 s + 8 t .. + 7 of slab s (INT4: in the codes'
+  // (k0,k4) (k1,k5) (k2,k6) (k3,k7) order), the k-slots of the slab's two k-steps.
+  uint32_t qb[2 * NS][2];
+  float qsum[NS];  // INT4: per 32-dim slab, the sum of head gi's query values
   const bool hv = gi < G;
   const __half* qrow = qkv + (int64_t)(gk * G + (hv ? gi : 0)) * D;
 #pragma unroll
@@ -372,16 +376,25 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
       qsum[s] = sum;
       v = perm_k0k4(v);
     }
-    qa[2 * s][0] = v.x;
-    qa[2 * s][1] = v.y;
-    qa[2 * s + 1][0] = v.z;
-    qa[2 * s + 1][1] = v.w;
+    qb[2 * s][0] = v.x;
+    qb[2 * s][1] = v.y;
+    qb[2 * s + 1][0] = v.z;
+    qb[2 * s + 1][1] = v.w;
+  }
+  // INT4: the query sums of heads 2t and 2t+1, the columns of this lane's score fragments
+  float qs2[NS][2];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) {
+    qs2[s][0] = __shfl_sync(0xffffffffu, DT == 2 ? qsum[s] : 0.f, 8 * t);
+    qs2[s][1] = __shfl_sync(0xffffffffu, DT == 2 ? qsum[s] : 0.f, 8 * t + 4);
   }
   const float sc = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
-  float m_run = -INFINITY, l_part = 0.f;
-  float acc[NV][4];
+  // running maximum and sum of heads 2t, 2t+1; acc[m] = O^T rows g, g+8 of m-tile m (dims of slots 2m, 2m+1
+  // of lane group gi) x columns 2t, 2t+1 (heads)
+  float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+  float acc[NV / 2][4];
 #pragma unroll
-  for (int n = 0; n < NV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  for (int m = 0; m < NV / 2; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
 
   int slot_i = 0;
   for (int j = 0; j < nb; ++j) {
@@ -393,103 +406,98 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
     const uint8_t* vd = slot + SG::kData;
     const uint8_t* km = slot + 2 * SG::kData;
     const uint8_t* vm = km + SG::kMeta;
-    // ---- scores S[head][token] of the block's 16 tokens (two n-tiles of 8), the slabs in two
+    // ---- scores S^T[token][head]: rows gi, gi+8 of the block's tokens, columns 2t, 2t+1; the slabs in two
     // independent accumulation chains
-    float sfr[2][4];
+    const uint8_t* kr0 = kd + gi * SG::kDb;
+    const uint8_t* kr8 = kd + (gi + 8) * SG::kDb;
+    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (DT == 2) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint8_t* krow = kd + (gi + 8 * nt) * SG::kDb;
-      if (DT == 2) {
-        const uint8_t* kmeta0 = km + (8 * nt + 2 * t) * SG::kMb;
-#pragma unroll
-        for (int s = 0; s < NS; ++s) {
-          const uint4 kq = u4x8_codes(*reinterpret_cast<const uint32_t*>(krow + 16 * s + 4 * t));
-          float as[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_16816(as, qa[2 * s][0], 0u, qa[2 * s][1], 0u, kq.x, kq.y);
-          mma_16816(as, qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kq.z, kq.w);
-          // per (token, group): score += s * (q . codes) + m * sum(q)
-          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + 4 * s));
-          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(kmeta0 + SG::kMb + 4 * s));
-          s2[s & 1][0] = fmaf(f0.x, as[0], fmaf(f0.y, qsum[s], s2[s & 1][0]));
-          s2[s & 1][1] = fmaf(f1.x, as[1], fmaf(f1.y, qsum[s], s2[s & 1][1]));
-        }
-      } else {
-#pragma unroll
-        for (int s = 0; s < NS; ++s) {
-          uint4 kb;
-          if (DT == 0) {
-            kb = *reinterpret_cast<const uint4*>(krow + (32 * s + 8 * t) * 2);
-          } else {
-            const uint2 w = *reinterpret_cast<const uint2*>(krow + 32 * s + 8 * t);
-            i8x4_to_h2(w.x, kb.x, kb.y);
-            i8x4_to_h2(w.y, kb.z, kb.w);
-          }
-          mma_16816(s2[s & 1], qa[2 * s][0], 0u, qa[2 * s][1], 0u, kb.x, kb.y);
-          mma_16816(s2[s & 1], qa[2 * s + 1][0], 0u, qa[2 * s + 1][1], 0u, kb.z, kb.w);
-        }
+      for (int s = 0; s < NS; ++s) {
+        const uint4 k0 = u4x8_codes(*reinterpret_cast<const uint32_t*>(kr0 + 16 * s + 4 * t));
+        const uint4 k8 = u4x8_codes(*reinterpret_cast<const uint32_t*>(kr8 + 16 * s + 4 * t));
+        float as[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(as, k0.x, k8.x, k0.y, k8.y, qb[2 * s][0], qb[2 * s][1]);
+        mma_16816(as, k0.z, k8.z, k0.w, k8.w, qb[2 * s + 1][0], qb[2 * s + 1][1]);
+        // per (token, group): score += s * (codes . q) + m * sum(q)
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(km + gi * SG::kMb + 4 * s));
+        const float2 f8 = __half22float2(*reinterpret_cast<const __half2*>(km + (gi + 8) * SG::kMb + 4 * s));
+        float* acc_s = s2[s & 1];
+        acc_s[0] = fmaf(f0.x, as[0], fmaf(f0.y, qs2[s][0], acc_s[0]));
+        acc_s[1] = fmaf(f0.x, as[1], fmaf(f0.y, qs2[s][1], acc_s[1]));
+        acc_s[2] = fmaf(f8.x, as[2], fmaf(f8.y, qs2[s][0], acc_s[2]));
+        acc_s[3] = fmaf(f8.x, as[3], fmaf(f8.y, qs2[s][1], acc_s[3]));
       }
+    } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sfr[nt][e] = s2[0][e] + s2[1][e];
+      for (int s = 0; s < NS; ++s) {
+        uint4 k0, k8;
+        if (DT == 0) {
+          k0 = *reinterpret_cast<const uint4*>(kr0 + (32 * s + 8 * t) * 2);
+          k8 = *reinterpret_cast<const uint4*>(kr8 + (32 * s + 8 * t) * 2);
+        } else {
+          const uint2 w0 = *reinterpret_cast<const uint2*>(kr0 + 32 * s + 8 * t);
+          const uint2 w8 = *reinterpret_cast<const uint2*>(kr8 + 32 * s + 8 * t);
+          i8x4_to_h2(w0.x, k0.x, k0.y);
+          i8x4_to_h2(w0.y, k0.z, k0.w);
+          i8x4_to_h2(w8.x, k8.x, k8.y);
+          i8x4_to_h2(w8.y, k8.z, k8.w);
+        }
+        mma_16816(s2[s & 1], k0.x, k8.x, k0.y, k8.y, qb[2 * s][0], qb[2 * s][1]);
+        mma_16816(s2[s & 1], k0.z, k8.z, k0.w, k8.w, qb[2 * s + 1][0], qb[2 * s + 1][1]);
+      }
     }
-    // this lane's tokens: (nt, jj) -> 16 blk + 8 nt + 2 t + jj
-    float ks[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+    // e: 0 (token gi, head 2t), 1 (gi, 2t+1), 2 (gi+8, 2t), 3 (gi+8, 2t+1)
+    float sfr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sfr[e] = s2[0][e] + s2[1][e];
+    float ks[2] = {1.f, 1.f}, vsc[2] = {1.f, 1.f};  // INT8 scales of tokens gi, gi+8
     if (DT == 1) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const __half2 k2 = *reinterpret_cast<const __half2*>(km + (8 * nt + 2 * t) * 2);
-        const __half2 v2 = *reinterpret_cast<const __half2*>(vm + (8 * nt + 2 * t) * 2);
-        ks[nt][0] = __low2float(k2);
-        ks[nt][1] = __high2float(k2);
-        vsc[nt][0] = __low2float(v2);
-        vsc[nt][1] = __high2float(v2);
-      }
+      ks[0] = __half2float(*reinterpret_cast<const __half*>(km + gi * 2));
+      ks[1] = __half2float(*reinterpret_cast<const __half*>(km + (gi + 8) * 2));
+      vsc[0] = __half2float(*reinterpret_cast<const __half*>(vm + gi * 2));
+      vsc[1] = __half2float(*reinterpret_cast<const __half*>(vm + (gi + 8) * 2));
     }
-    float mx = -INFINITY;
+    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int tok = blk * 16 + 8 * nt + 2 * t + jj;
-        float v = sfr[nt][jj] * ks[nt][jj] * sc;
-        v = tok < n_keys ? v : -INFINITY;
-        sfr[nt][jj] = v;
-        mx = fmaxf(mx, v);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float corr = exp2f(m_run - m_new);
-    m_run = m_new;
-    float p[2][2];
-    float psum = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        p[nt][jj] = exp2f(sfr[nt][jj] - m_new);
-        psum += p[nt][jj];
-      }
-    l_part = l_part * corr + psum;
-#pragma unroll
-    for (int n = 0; n < NV; ++n) {
-      acc[n][0] *= corr;
-      acc[n][1] *= corr;
+    for (int e = 0; e < 4; ++e) {
+      const int tok = blk * 16 + gi + 8 * (e >> 1);
+      const float v = tok < n_keys ? sfr[e] * ks[e >> 1] * sc : -INFINITY;
+      sfr[e] = v;
+      mx[e & 1] = fmaxf(mx[e & 1], v);
     }
-    // P (times the INT8 value scale) as the A operand, split into fp16 hi + lo so the
-    // product carries no fp16 rounding of the probabilities: a0 = tokens (2t, 2t+1),
-    // a2 = tokens (8+2t, 9+2t)
-    float pv[2][2];
+    float corr[2], m_new[2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int h = 0; h < 2; ++h) {
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+      m_new[h] = fmaxf(m_run[h], mx[h]);
+      corr[h] = exp2f(m_run[h] - m_new[h]);
+      m_run[h] = m_new[h];
+    }
+    float p[4];
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) pv[nt][jj] = p[nt][jj] * vsc[nt][jj];
-    const __half2 h0 = __floats2half2_rn(pv[0][0], pv[0][1]), h2 = __floats2half2_rn(pv[1][0], pv[1][1]);
-    const float2 f0 = __half22float2(h0), f2 = __half22float2(h2);
-    const uint32_t pa0 = h2_as_u32(h0), pa2 = h2_as_u32(h2);
-    const uint32_t pl0 = h2_as_u32(__floats2half2_rn(pv[0][0] - f0.x, pv[0][1] - f0.y));
-    const uint32_t pl2 = h2_as_u32(__floats2half2_rn(pv[1][0] - f2.x, pv[1][1] - f2.y));
-    // ---- V rows of tokens 2t, 2t+1, 8+2t, 9+2t
+    for (int e = 0; e < 4; ++e) p[e] = exp2f(sfr[e] - m_new[e & 1]);
+    l_part[0] = l_part[0] * corr[0] + p[0] + p[2];
+    l_part[1] = l_part[1] * corr[1] + p[1] + p[3];
+#pragma unroll
+    for (int m = 0; m < NV / 2; ++m) {
+      acc[m][0] *= corr[0];
+      acc[m][1] *= corr[1];
+      acc[m][2] *= corr[0];
+      acc[m][3] *= corr[1];
+    }
+    // P^T (times the INT8 value scale) as the B operand, split into fp16 hi + lo so the product carries no
+    // fp16 rounding of the probabilities: the 8 x 8 tiles [token][head] of tokens 0-7 and 8-15, transposed
+    // in registers into [head][token] (b0: tokens 2t, 2t+1; b1: tokens 8+2t, 9+2t of head gi)
+    const float pv0 = p[0] * vsc[0], pv1 = p[1] * vsc[0], pv2 = p[2] * vsc[1], pv3 = p[3] * vsc[1];
+    const __half2 ht = __floats2half2_rn(pv0, pv1), hb = __floats2half2_rn(pv2, pv3);
+    const float2 ft = __half22float2(ht), fb = __half22float2(hb);
+    const uint32_t bh0 = movmatrix_trans(h2_as_u32(ht)), bh1 = movmatrix_trans(h2_as_u32(hb));
+    const uint32_t bl0 = movmatrix_trans(h2_as_u32(__floats2half2_rn(pv0 - ft.x, pv1 - ft.y)));
+    const uint32_t bl1 = movmatrix_trans(h2_as_u32(__floats2half2_rn(pv2 - fb.x, pv3 - fb.y)));
+    // ---- V rows of tokens 2t, 2t+1, 8+2t, 9+2t (lane group gi's dims)
     uint32_t v0[NW], v1[NW], v8[NW], v9[NW];
     load_v_row<D, DT>(vd + (2 * t) * SG::kDb, vm + (2 * t) * SG::kMb, gi, v0);
     load_v_row<D, DT>(vd + (2 * t + 1) * SG::kDb, vm + (2 * t + 1) * SG::kMb, gi, v1);
@@ -500,56 +508,65 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
     if (j + kAttnSlots < nb) issue_block<D, DT>(slot, a.pool, a.layer, phys_of(j + kAttnSlots), gk, lane);
     cp_async_commit();
     slot_i = slot_i + 1 == kAttnSlots ? 0 : slot_i + 1;
+    // A = V^T: row gi of m-tile m <- slot 2m, row gi+8 <- slot 2m+1; k-slots = tokens
 #pragma unroll
-    for (int n = 0; n < NV; ++n) {
-      const uint32_t b0 = pair_tokens(v0, v1, n), b1 = pair_tokens(v8, v9, n);
-      mma_16816(acc[n], pa0, 0u, pa2, 0u, b0, b1);
-      mma_16816(acc[n], pl0, 0u, pl2, 0u, b0, b1);
+    for (int m = 0; m < NV / 2; ++m) {
+      const uint32_t a0 = pair_tokens(v0, v1, 2 * m), a1 = pair_tokens(v0, v1, 2 * m + 1);
+      const uint32_t a2 = pair_tokens(v8, v9, 2 * m), a3 = pair_tokens(v8, v9, 2 * m + 1);
+      mma_16816(acc[m], a0, a1, a2, a3, bh0, bh1);
+      mma_16816(acc[m], a0, a1, a2, a3, bl0, bl1);
     }
   }
   cp_async_wait<0>();
 
   // ---- merge the NWARP warps of this block into the block's partial (m, l, o); the barrier below also
   // ends every warp's use of its ring, whose memory the merge reuses
-  float l_tot = l_part;
-  l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
-  l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-  if (hv && t == 0) {
-    s_m[warp][gi] = m_run;
-    s_l[warp][gi] = l_tot;
+  float l_tot[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float l = l_part[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    l_tot[h] = l;
   }
+  if (gi == 0)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (2 * t + h < G) {
+        s_m[warp][2 * t + h] = m_run[h];
+        s_l[warp][2 * t + h] = l_tot[h];
+      }
   __syncthreads();
-  if (hv) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int hd = 2 * t + h;
+    if (hd >= G) continue;
     // this warp's share, rescaled to the block's running maximum of the head
-    float mm = s_m[0][gi];
+    float mm = s_m[0][hd];
 #pragma unroll
-    for (int w = 1; w < NWARP; ++w) mm = fmaxf(mm, s_m[w][gi]);
-    const float e = mm == -INFINITY ? 0.f : exp2f(m_run - mm);
-    float* dst = s_acc + warp * AG::kWarp + gi * AG::kRow + t * AG::kTS;
+    for (int w = 1; w < NWARP; ++w) mm = fmaxf(mm, s_m[w][hd]);
+    const float e = mm == -INFINITY ? 0.f : exp2f(m_run[h] - mm);
+    float* dst = s_acc + (warp * 8 + hd) * D + gi * NV;
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-      for (int q = 0; q < NV / 4; ++q)
-        *reinterpret_cast<float4*>(dst + jj * NV + 4 * q) =
-            make_float4(acc[4 * q][jj] * e, acc[4 * q + 1][jj] * e, acc[4 * q + 2][jj] * e, acc[4 * q + 3][jj] * e);
-    if (warp == 0 && t == 0) {
+    for (int m = 0; m < NV / 2; ++m) {
+      dst[v_slot_dim<DT>(2 * m)] = acc[m][h] * e;
+      dst[v_slot_dim<DT>(2 * m + 1)] = acc[m][2 + h] * e;
+    }
+    if (warp == 0 && gi == 0) {
       float l = 0.f;
 #pragma unroll
-      for (int w = 0; w < NWARP; ++w) l += s_l[w][gi] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][gi] - mm));
-      s_pm[gi] = mm;  // -inf for a block without keys
-      s_pl[gi] = l;
+      for (int w = 0; w < NWARP; ++w) l += s_l[w][hd] * (mm == -INFINITY ? 0.f : exp2f(s_m[w][hd] - mm));
+      s_pm[hd] = mm;  // -inf for a block without keys
+      s_pl[hd] = l;
     }
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, dim = idx - h * D;
-    const int c = dim / NV, r = dim - c * NV;  // column 2t + jj of n-tile v_slot_dim^-1(r)
-    int n = r;
-    if (DT == 2) n = (r & 8) + ((r & 3) << 1) + ((r >> 2) & 1);
-    const int off = h * AG::kRow + (c >> 1) * AG::kTS + (c & 1) * NV + n;
     float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) sum += s_acc[w * AG::kWarp + off];
+    for (int w = 0; w < NWARP; ++w) sum += s_acc[(w * 8 + h) * D + dim];
     s_po[idx] = sum;
   }
   // ---- merge the cluster's splits through distributed shared memory: every output reads the S
