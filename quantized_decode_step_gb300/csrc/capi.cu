@@ -1,182 +1,9 @@
-// C ABI of the decode-step library: context, weights, KV block pool, arena
-// plan, CUDA-graph step and the debug hooks. See include/mag.h for the
-// contract of each call.
-#include <algorithm>
-#include <atomic>
-#include <cmath>
-#include <cstdarg>
-#include <cstdio>
-#include <cstring>
-#include <deque>
-#include <memory>
-#include <string>
-#include <thread>
-#include <vector>
+// C ABI of the decode-step library: context, weights, KV block pool, sessions, statistics and the debug
+// hooks (the decode step: step.cu; chunked prefill: prefill.cu; the verify step: verify.cu). See
+// include/mag.h for the contract of each call.
+#include "engine.h"
 
-#include "adapt.h"
-#include "alloc.h"
-#include "arena.h"
-#include "kernels.h"
-#include "kvpool.h"
-#include "noalloc.h"
-#include "mag.h"
-
-using namespace mag;
-
-namespace {
-
-constexpr int kRing = 8;
-
-struct Proj {
-  uint8_t* tiles = nullptr;  // [N/16][ceil(K/64)][640 B]
-  int N = 0, K = 0, G = 0;
-  int map = 0, map_arg = 0;  // tile row map (TileMap) and its argument
-  size_t canon_bytes = 0;    // W4G32 bytes: N * G * 20
-  size_t tile_bytes = 0;
-};
-
-struct Session {
-  bool open = false;
-  int len = 0;
-  std::vector<int32_t> table;
-};
-
-struct GemvPlan {
-  int n_cta, stages, t_max;  // pipelined kernels (up to kPipeMaxBatch tokens; W4 above); n_cta = 0 otherwise
-  int ks, cpc, tpw;          // k-ranges (W4 above kPipeMaxBatch: windows) and their chunks; fp16 k-split tpw
-  size_t smem;
-};
-
-// Event pairs around each launch of an instrumented (eager) step.
-struct Profiler {
-  std::vector<cudaEvent_t> start, stop;
-  std::vector<int> kinds;
-  cudaError_t begin(cudaStream_t s) {
-    cudaEvent_t e;
-    cudaError_t r = cudaEventCreate(&e);
-    if (r != cudaSuccess) return r;
-    start.push_back(e);
-    return cudaEventRecord(e, s);
-  }
-  cudaError_t end(cudaStream_t s, int kind) {
-    cudaEvent_t e;
-    cudaError_t r = cudaEventCreate(&e);
-    if (r != cudaSuccess) return r;
-    stop.push_back(e);
-    kinds.push_back(kind);
-    return cudaEventRecord(e, s);
-  }
-  ~Profiler() {
-    for (auto e : start) cudaEventDestroy(e);
-    for (auto e : stop) cudaEventDestroy(e);
-  }
-};
-
-}  // namespace
-
-struct mag_ctx {
-  mag_config cfg{};
-  cudaStream_t stream = nullptr;
-  bool own_stream = false;
-  int device = 0, n_sm = 0;
-  int attn_cluster_max = 1;       // largest co-scheduled attention cluster, 4-warp blocks
-  int attn_cluster_max_wide = 1;  // the same for the wide (16- or 8-warp) blocks
-  float* attn_part = nullptr;       // clusters' partial outputs when a (session, KV head) spans several
-  uint32_t* attn_arrivals = nullptr;
-  std::string err;
-  int L = 0, D = 0, Hq = 0, Hkv = 0, d = 0, F = 0, V = 0, R = 0, G = 0, B_max = 0;
-  int table_stride = 0;
-
-  // weights
-  uint8_t* wbase = nullptr;
-  size_t wbytes = 0;
-  std::vector<Proj> proj;  // [L][4]
-  std::vector<__half*> gamma1, gamma2;
-  __half* gamma_f = nullptr;
-  __half* lm_head = nullptr;
-  std::vector<uint8_t> loaded;  // [L][6] + final norm + lm head
-
-  // KV pool
-  KvPool kv;  // memory and free list (fixed, or elastic hot / cold groups)
-  int64_t block_bytes = 0;
-  int data_bytes = 0, meta_bytes = 0;
-  int32_t* d_tables = nullptr;
-  std::vector<Session> sessions;
-
-  // RoPE table
-  float* d_cos = nullptr;
-  float* d_sin = nullptr;
-
-  // activation arena (decode phase)
-  uint8_t* arena = nullptr;
-  uint64_t arena_bytes = 0, arena_unshared = 0;
-  std::vector<ArenaTensor> plan;
-  float* r = nullptr;
-  __half* qkv = nullptr;
-  __half* o = nullptr;
-  float* ss_part = nullptr;
-  __half* act = nullptr;
-  float* gemv_part = nullptr;
-
-  // counters (zero between launches) and step arguments
-  uint32_t* d_counters = nullptr;
-  uint32_t* h_err = nullptr;  // mapped pinned word: kernels set bits when a bounded wait gives up
-  uint32_t wait_limit = kWaitPolls;  // polls of a GEMV main-loop wait (mag_debug_set_wait_limit)
-  uint32_t* d_err = nullptr;
-  size_t n_counters = 0;
-  StepArgs* d_args = nullptr;
-  StepArgs* h_ring = nullptr;
-  cudaEvent_t ring_ev[kRing] = {};
-  int ring_pos = 0;
-
-  // staging for the host-buffer step
-  void* d_in_stage = nullptr;
-  void* d_out_stage = nullptr;
-
-  // captured step graphs by [verify][plan][batch]: a verify step's rows are the drafts of one session
-  struct StepGraph {
-    cudaGraphExec_t exec = nullptr;
-    int launches = 0;
-  };
-  StepGraph graphs[2][3][MAG_MAX_BATCH + 1];
-  // without the adaptive runtime: graphs by [verify][context bucket][batch] (attention splits by the step's
-  // longest context)
-  static constexpr int kLenBuckets = 4;
-  StepGraph len_graphs[2][kLenBuckets][MAG_MAX_BATCH + 1];
-  int step_max_len = 0;  // longest context (position + 1) among the rows of the step being launched
-  int last_launches = 0;
-
-  // adaptive runtime: load profile, plan in use, background capture of a new plan's graphs
-  mag_adapt_config adapt{};  // enable_adaptive = 0 until mag_set_adaptive
-  std::unique_ptr<LoadProfile> profile;
-  int cur_plan = 1;
-  int switches = 0;
-  int64_t hot_blocks = -1;
-  int pending_plan = -1;
-  std::thread cap_thread;
-  std::atomic<int> cap_state{0};  // 0 idle, 1 capturing, 2 done, 3 failed
-  std::string cap_err;
-  cudaStream_t cap_stream = nullptr;
-  uint64_t other_bytes = 0;
-  // chunked prefill (max_chunk > 0): planned buffers and the activations' TMA maps (the GEMMs read the W4 tiles)
-  uint8_t* pf_arena = nullptr;
-  uint64_t pf_arena_bytes = 0;
-  std::vector<ArenaTensor> pf_plan;
-  float* pf_r = nullptr;
-  __half* pf_xn = nullptr;
-  __half* pf_qkv = nullptr;
-  __half* pf_o = nullptr;
-  __half* pf_act = nullptr;
-  int32_t* pf_rows = nullptr;   // [2][max_chunk]: position and session of every row (several sessions)
-  float* pf_part = nullptr;     // split-K GEMMs: partial sums of the two K halves
-  uint32_t* pf_part_cnt = nullptr;
-  float* pf_last_r = nullptr;   // [MAG_MAX_BATCH][D]: the sessions' last residual rows, gathered
-  alignas(64) uint8_t map_xn[128];
-  alignas(64) uint8_t map_o[128];
-  alignas(64) uint8_t map_act[128];
-};
-
-namespace {
+namespace mag {
 
 mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...) {
   char buf[512];
@@ -187,14 +14,6 @@ mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...) {
   if (c) c->err = buf;
   return s;
 }
-
-#define CUDA_TRY(ctx, call)                                                                         \
-  do {                                                                                              \
-    cudaError_t e_ = (call);                                                                        \
-    if (e_ != cudaSuccess) return fail(ctx, MAG_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
-  } while (0)
-
-size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // After a synchronisation: a kernel whose bounded wait gave up left a bit in the error word.
 // The arrival counters of the last-to-arrive merges (GEMV tiles, attention clusters, prefill split-K) may be
@@ -215,7 +34,6 @@ mag_status check_err(mag_ctx* c) {
 // staged activations fit in 64 KB, times tile ranges, about one block per SM,
 // rings as deep as the rest of the block's shared memory allows. The fp16 LM
 // head above 4 tokens: a k-split grid of 8-warp blocks.
-constexpr size_t kPipeBudget = 200 * 1024, kSmemMax = 227 * 1024;
 
 GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
   GemvPlan p = {};
@@ -274,7 +92,7 @@ GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B) {
 
 // Splits of one (session, KV head): the blocks of one thread-block cluster, so at
 // most the largest cluster the device co-schedules (16 on a full GPU).
-int attn_splits(const mag_ctx* c, int B, bool wide = false) {
+int attn_splits(const mag_ctx* c, int B, bool wide) {
   int s = (2 * c->n_sm + B * c->Hkv - 1) / (B * c->Hkv);
   return std::max(1, std::min(s, wide ? c->attn_cluster_max_wide : c->attn_cluster_max));
 }
@@ -332,10 +150,6 @@ bool all_loaded(const mag_ctx* c) {
   return true;
 }
 
-// The decode step's projections: kind (0 QKV, 1 O, 2 gate-up, 3 down, 4 LM head), tiles, K, launch variant
-struct ProjShape {
-  int kind, n_mtiles, K, wfmt, xsrc, epi;
-};
 std::vector<ProjShape> proj_shapes(const mag_ctx* c) {
   std::vector<ProjShape> v = {{0, c->R / 16, c->D, W_W4, XSRC_RESID, EPI_QKV},
                               {1, c->D / 16, c->Hq * c->d, W_W4, XSRC_F16, EPI_RESID},
@@ -432,124 +246,6 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
   return a;
 }
 
-// Enqueue the whole decode step for batch B (captured into a graph or run eagerly).
-// The decode step's launches. With `verify` the B rows are B consecutive new tokens of one session: their
-// keys and values go into the pool in one store kernel after the QKV projection, and attention reads them
-// there (row b causally up to its own position) instead of each row appending its own.
-// `splits` is the attention split count of the plan in use; `st` the stream the launches go to (the
-// context's, or a capture stream). With `resid_dump` (eager debug steps only) the fp32 residual of the B rows
-// is copied there after the step prologue and after every layer: [L+1][B][D].
-cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool verify, int splits, bool wide,
-                        cudaStream_t st, float* resid_dump = nullptr) {
-  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !prof && !resid_dump;
-  auto dump = [&](int row) {
-    return resid_dump ? cudaMemcpyAsync(resid_dump + (size_t)row * B * c->D, c->r, (size_t)B * c->D * 4,
-                                        cudaMemcpyDeviceToDevice, st)
-                      : cudaSuccess;
-  };
-  Launch L0{st, false, n_launch};
-  Launch L{st, pdl, n_launch};
-  cudaError_t e;
-  // every launch goes through MAG_RUN, which brackets it with events when profiling
-#define MAG_RUN(kind, call)                                            \
-  do {                                                                \
-    if (prof && (e = prof->begin(st)) != cudaSuccess) return e;       \
-    if ((e = (call)) != cudaSuccess) return e;                        \
-    if (prof && (e = prof->end(st, (kind))) != cudaSuccess) return e; \
-  } while (0)
-  MAG_RUN(MAG_OP_STEP_BEGIN,
-          launch_step_begin(L0, c->d_args, c->r, c->D, c->d_tables, c->table_stride, B, c->ss_part));
-  if ((e = dump(0)) != cudaSuccess) return e;
-  const PoolGeom pg = pool_geom(c);
-  const int S = splits;
-  const bool kv_by_qkv = !verify && c->cfg.kv_dtype == MAG_KV_FP16 && B <= kPipeMaxBatch;
-  for (int l = 0; l < c->L; ++l) {
-    const Proj* P = &c->proj[(size_t)l * 4];
-    {  // RMSNorm + QKV + RoPE of q and k
-      GemvArgs a = gemv_args(c, 0, P[0].tiles, c->R / 16, c->D, B);
-      a.n_ss = l == 0 ? 1 : c->D / 16;  // the step prologue leaves one sum per token
-      a.gamma = c->gamma1[l];
-      a.out_h = c->qkv;
-      a.ldo = c->R;
-      a.head_dim = c->d;
-      a.n_rot_heads = c->Hq + c->Hkv;
-      a.rope_cos = c->d_cos;
-      a.rope_sin = c->d_sin;
-      // FP16 pool, decode rows on the pipelined GEMV: its epilogue also stores each row's key and value
-      a.kv_store = kv_by_qkv ? 1 : 0;
-      a.n_q_heads = c->Hq;
-      a.layer = l;
-      a.pool = pg;
-      MAG_RUN(MAG_OP_QKV, launch_gemv(L, a, W_W4, XSRC_RESID, EPI_QKV));
-    }
-    if (verify) {  // the B tokens' k and v into the pool
-      KvChunkArgs kc = {};
-      kc.qkv = c->qkv;
-      kc.qkv_ld = c->R;
-      kc.n_heads = c->Hq;
-      kc.n_tok = B;
-      kc.layer = l;
-      kc.pool = pg;
-      kc.step = c->d_args;
-      MAG_RUN(MAG_OP_ATTENTION, launch_kv_store_chunk(L, kc));
-    }
-    {  // KV append + attention
-      AttnArgs a = {};
-      a.qkv = c->qkv;
-      a.qkv_ld = c->R;
-      a.o = c->o;
-      a.ldo = c->Hq * c->d;
-      a.n_heads = c->Hq;
-      a.n_kv_heads = c->Hkv;
-      a.head_dim = c->d;
-      a.layer = l;
-      a.pool = pg;
-      a.step = c->d_args;
-      a.stored = verify ? 1 : (kv_by_qkv ? 2 : 0);
-      a.wide = wide;
-      // more splits than one cluster holds: clusters of at most 8 (which co-schedule more readily than
-      // clusters of 16), merged by the last block to finish
-      const int cmax = wide ? c->attn_cluster_max_wide : c->attn_cluster_max;
-      const int csz = S <= cmax ? cmax : std::min(cmax, 8);
-      a.n_groups = std::min(kAttnMaxGroups, (S + csz - 1) / csz);
-      a.n_split = std::min(csz, (S + a.n_groups - 1) / a.n_groups);
-      a.part = c->attn_part;
-      a.arrivals = c->attn_arrivals;
-      MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
-    }
-    {  // O projection + residual
-      GemvArgs a = gemv_args(c, 1, P[1].tiles, c->D / 16, c->Hq * c->d, B);
-      a.x = c->o;
-      a.ldx = c->Hq * c->d;
-      MAG_RUN(MAG_OP_O, launch_gemv(L, a, W_W4, XSRC_F16, EPI_RESID));
-    }
-    {  // RMSNorm + gate-up + SwiGLU
-      GemvArgs a = gemv_args(c, 2, P[2].tiles, c->F / 8, c->D, B);
-      a.gamma = c->gamma2[l];
-      a.out_h = c->act;
-      a.ldo = c->F;
-      MAG_RUN(MAG_OP_GATE_UP, launch_gemv(L, a, W_W4, XSRC_RESID, EPI_SWIGLU));
-    }
-    {  // down projection + residual
-      GemvArgs a = gemv_args(c, 3, P[3].tiles, c->D / 16, c->F, B);
-      a.x = c->act;
-      a.ldx = c->F;
-      MAG_RUN(MAG_OP_DOWN, launch_gemv(L, a, W_W4, XSRC_F16, EPI_RESID));
-    }
-    if ((e = dump(l + 1)) != cudaSuccess) return e;
-  }
-  if (c->V) {  // final RMSNorm + LM head
-    GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, c->D, B);
-    a.gamma = c->gamma_f;
-    a.ldo = c->V;
-    MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, XSRC_RESID, EPI_STORE_OUT));
-  } else {
-    MAG_RUN(MAG_OP_LM_HEAD, launch_final_hidden(L, c->d_args, c->r, c->D, B));
-  }
-#undef MAG_RUN
-  return cudaSuccess;
-}
-
 void free_ctx(mag_ctx* c) {
   if (!c) return;
   if (c->stream) cudaStreamSynchronize(c->stream);
@@ -610,69 +306,7 @@ mag_status check_cfg(const mag_config* g, std::string& why) {
   return MAG_OK;
 }
 
-}  // namespace
-
-namespace {
-
-// ---------------------------------------------------------------- chunked prefill set-up
-// GEMM rows of projection kind i: the tile rows of its 16-row decode tiles, 8 tiles to a 128-row GEMM tile (QKV:
-// one head of d = 128 or two of 64, RoPE pairs (i, i + d/2) in canonical order; gate-up: gate and up rows
-// interleaved in blocks of 64), padded to a whole GEMM tile.
-int prefill_rows(const mag_ctx* c, int i) {
-  const int t = tc_gemm_rows_multiple();
-  if (i == 2) return (c->F + 63) / 64 * 128;
-  const int n = i == 0 ? c->R : c->D;
-  return (n + t - 1) / t * t;
-}
-
-// Prefill activation tensors at max_chunk rows with their op lifetimes: 0 input, per layer 1 norm,
-// 2 QKV, 3 KV store + attention, 4 O, 5 norm, 6 gate-up, 7 down (one plan for every layer); 8 LM head.
-void build_prefill_plan(mag_ctx* c) {
-  const uint64_t T = c->cfg.max_chunk;
-  auto Tn = [](const char* n, uint64_t sz, int f, int l) { return ArenaTensor{n, sz, f, l, 0}; };
-  c->pf_plan.clear();
-  c->pf_plan.push_back(Tn("pf_residual", T * c->D * 4, 0, 8));
-  c->pf_plan.push_back(Tn("pf_norm", T * c->D * 2, 1, 6));
-  c->pf_plan.push_back(Tn("pf_qkv", T * c->R * 2, 2, 3));
-  c->pf_plan.push_back(Tn("pf_attn_out", T * c->Hq * c->d * 2, 3, 4));
-  c->pf_plan.push_back(Tn("pf_ffn_act", T * c->F * 2, 6, 7));
-  c->pf_arena_bytes = plan_arena(c->pf_plan, 64, (c->cfg.flags & MAG_FLAG_ARENA_NO_REUSE) != 0);
-}
-
-mag_status setup_prefill(mag_ctx* c) {
-  cudaError_t e;
-  build_prefill_plan(c);
-  if ((e = dev_malloc(&c->pf_arena, std::max<uint64_t>(c->pf_arena_bytes, 256))) != cudaSuccess)
-    return fail(c, MAG_ERR_OOM, "prefill arena: %s", cudaGetErrorString(e));
-  auto at = [&](const char* n) -> uint8_t* {
-    for (auto& t : c->pf_plan)
-      if (t.name == n) return c->pf_arena + t.offset;
-    return nullptr;
-  };
-  c->pf_r = reinterpret_cast<float*>(at("pf_residual"));
-  c->pf_xn = reinterpret_cast<__half*>(at("pf_norm"));
-  c->pf_qkv = reinterpret_cast<__half*>(at("pf_qkv"));
-  c->pf_o = reinterpret_cast<__half*>(at("pf_attn_out"));
-  c->pf_act = reinterpret_cast<__half*>(at("pf_ffn_act"));
-  const int T = c->cfg.max_chunk;
-  if (!make_tmap_2d(c->map_xn, c->pf_xn, T, c->D) || !make_tmap_2d(c->map_o, c->pf_o, T, (int64_t)c->Hq * c->d) ||
-      !make_tmap_2d(c->map_act, c->pf_act, T, c->F))
-    return fail(c, MAG_ERR_CUDA, "prefill: activation tensor maps");
-  // several sessions in one chunk: per-row positions and sessions, and the gathered last rows
-  if ((e = dev_malloc(&c->pf_rows, (size_t)2 * T * 4)) != cudaSuccess ||
-      (e = dev_malloc(&c->pf_last_r, (size_t)MAG_MAX_BATCH * c->D * 4)) != cudaSuccess)
-    return fail(c, MAG_ERR_OOM, "prefill row tables: %s", cudaGetErrorString(e));
-  c->other_bytes += (size_t)2 * T * 4 + (size_t)MAG_MAX_BATCH * c->D * 4;
-  // GEMMs whose output blocks fill at most half the SMs split K in two, merged through a workspace
-  const size_t pf = tc_gemm_part_floats(c->n_sm), pc = (size_t)(c->n_sm / 2) * 4;
-  if ((e = dev_malloc(&c->pf_part, pf * 4)) != cudaSuccess || (e = dev_malloc(&c->pf_part_cnt, pc * 4)) != cudaSuccess)
-    return fail(c, MAG_ERR_OOM, "prefill split-K workspace: %s", cudaGetErrorString(e));
-  cudaMemsetAsync(c->pf_part_cnt, 0, pc * 4, c->stream);
-  c->other_bytes += pf * 4 + pc * 4;
-  return MAG_OK;
-}
-
-}  // namespace
+}  // namespace mag
 
 // ============================================================================ API
 
@@ -1053,687 +687,6 @@ mag_status mag_kv_append(mag_ctx* c, int32_t sid, int32_t n, const void* k, cons
     }
   }
   s.len += n;
-  return MAG_OK;
-}
-
-static mag_status step_prepare(mag_ctx* c, int B, const int32_t* sids, StepArgs& a) {
-  if (B < 1 || B > c->B_max) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: batch %d not in 1..%d", B, c->B_max);
-  if (!sids) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: null session ids");
-  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "decode_step: not every weight is loaded");
-  int need = 0;
-  for (int b = 0; b < B; ++b) {
-    int s = sids[b];
-    if (s < 0 || s >= (int)c->sessions.size() || !c->sessions[s].open)
-      return fail(c, MAG_ERR_INVALID_ARG, "decode_step: session %d is not open", s);
-    for (int j = 0; j < b; ++j)
-      if (sids[j] == s) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: session %d appears twice", s);
-    if (c->sessions[s].len + 1 > c->cfg.max_context)
-      return fail(c, MAG_ERR_CONTEXT_FULL, "decode_step: session %d is at max_context", s);
-    if (c->sessions[s].len % 16 == 0) ++need;
-  }
-  mag_status st = reserve_blocks(c, "decode_step", need);
-  if (st != MAG_OK) return st;
-  a.batch = B;
-  a.n_upd = 0;
-  c->step_max_len = 0;
-  for (int b = 0; b < B; ++b) {
-    Session& s = c->sessions[sids[b]];
-    a.sess[b] = sids[b];
-    a.pos[b] = s.len;
-    c->step_max_len = std::max(c->step_max_len, s.len + 1);
-    if (s.len % 16 == 0) {
-      int blk = c->kv.pop();
-      s.table.push_back(blk);
-      a.upd_sess[a.n_upd] = sids[b];
-      a.upd_idx[a.n_upd] = s.len / 16;
-      a.upd_blk[a.n_upd] = blk;
-      ++a.n_upd;
-    }
-    a.blk[b] = s.table[s.len / 16];
-  }
-  return MAG_OK;
-}
-
-static mag_status step_upload(mag_ctx* c, int B, const int32_t* sids, const void* in, void* out) {
-  if (!in || !out) return fail(c, MAG_ERR_INVALID_ARG, "decode_step: null buffer");
-  const int slot = c->ring_pos;
-  CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
-  StepArgs& a = c->h_ring[slot];
-  memset(&a, 0, sizeof a);
-  mag_status st = step_prepare(c, B, sids, a);
-  if (st != MAG_OK) return st;
-  a.hidden_in = (const __half*)in;
-  a.out = out;
-  CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
-  CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
-  c->ring_pos = (slot + 1) % kRing;
-  return MAG_OK;
-}
-
-// Whether plan p runs the wide attention blocks.
-static bool plan_wide(const mag_ctx* c, int p) { return c->adapt.enable_adaptive && c->adapt.plan_wide[p]; }
-
-// Attention split count of plan p at batch B: the plan's count (a single-session figure), capped at about
-// 4 blocks per SM over the batch's (session, KV head) pairs; 0 = the context's default (at most one
-// cluster).
-static int plan_splits(const mag_ctx* c, int p, int B) {
-  const int s = c->adapt.enable_adaptive ? c->adapt.plan_splits[p] : 0;
-  if (s == 0) return attn_splits(c, B, plan_wide(c, p));
-  return std::max(1, std::min(s, 4 * c->n_sm / (B * c->Hkv)));
-}
-
-// Attention launch shape of the step being launched: the plan's with the adaptive runtime on; otherwise by
-// the step's longest context, about 76 pool blocks per split (measured on GB300: 16 splits, one cluster, up
-// to ~19k keys; 32 at ~39k; 64 at ~78k), so that long contexts keep enough warps streaming the pool.
-struct AttnShape {
-  int splits;
-  bool wide;
-  int bucket;  // -1: the adaptive plan's graphs
-};
-static AttnShape attn_shape(const mag_ctx* c, int B) {
-  if (c->adapt.enable_adaptive) return {plan_splits(c, c->cur_plan, B), plan_wide(c, c->cur_plan), -1};
-  const int nb = (c->step_max_len + 15) / 16, def = attn_splits(c, B);
-  const int bk = nb <= 16 * 76 ? 0 : (nb <= 32 * 76 ? 1 : (nb <= 48 * 76 ? 2 : 3));
-  const int s = bk == 0 ? def : std::max(def, std::min(16 * (bk + 1), 4 * c->n_sm / (B * c->Hkv)));
-  return {s, false, bk};
-}
-
-// Capture and instantiate the step graph of (verify, plan p, batch B) on stream st: the context's
-// stream, or the capture stream of a background switch.
-static cudaError_t capture_graph(mag_ctx* c, bool verify, int p, int B, cudaStream_t st,
-                                 mag_ctx::StepGraph& out) {
-  cudaGraph_t g = nullptr;
-  int n = 0;
-  cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
-  if (e != cudaSuccess) return e;
-  e = record_step(c, B, &n, nullptr, verify, plan_splits(c, p, B), plan_wide(c, p), st);
-  const cudaError_t e2 = cudaStreamEndCapture(st, &g);
-  if (e == cudaSuccess) e = e2;
-  if (e == cudaSuccess) e = cudaGraphInstantiate(&out.exec, g, 0);
-  if (g) cudaGraphDestroy(g);
-  if (e == cudaSuccess) out.launches = n;
-  return e;
-}
-
-// A background capture that has finished: switch to its plan, or report why it failed.
-static mag_status poll_capture(mag_ctx* c) {
-  const int s = c->cap_state.load(std::memory_order_acquire);
-  if (s != 2 && s != 3) return MAG_OK;
-  c->cap_thread.join();
-  c->cap_state.store(0);
-  const int p = c->pending_plan;
-  c->pending_plan = -1;
-  if (s == 3) return fail(c, MAG_ERR_CUDA, "capture of plan %d: %s", p, c->cap_err.c_str());
-  c->cur_plan = p;
-  ++c->switches;
-  return MAG_OK;
-}
-
-// Wait for a background capture (before the graphs or the configuration change under it).
-static mag_status finish_capture(mag_ctx* c) {
-  if (c->cap_thread.joinable()) c->cap_thread.join();
-  return poll_capture(c);
-}
-
-// Switch to plan p: at once (its graphs are captured on first use by the step), or, with async_switch,
-// after a background thread has captured p's graphs for every shape the current plan has captured.
-static void switch_plan(mag_ctx* c, int p) {
-  std::vector<std::pair<int, int>> shapes;
-  if (c->adapt.async_switch && !(c->cfg.flags & MAG_FLAG_NO_GRAPH))
-    for (int v = 0; v < 2; ++v)
-      for (int b = 1; b <= MAG_MAX_BATCH; ++b)
-        if (c->graphs[v][c->cur_plan][b].exec && !c->graphs[v][p][b].exec) shapes.emplace_back(v, b);
-  if (shapes.empty()) {
-    c->cur_plan = p;
-    ++c->switches;
-    return;
-  }
-  c->pending_plan = p;
-  c->cap_state.store(1);
-  c->cap_thread = std::thread([c, p, shapes]() {
-    cudaError_t e = cudaSetDevice(c->device);
-    for (const auto& sh : shapes) {
-      if (e != cudaSuccess) break;
-      e = capture_graph(c, sh.first != 0, p, sh.second, c->cap_stream, c->graphs[sh.first][p][sh.second]);
-    }
-    if (e != cudaSuccess) c->cap_err = cudaGetErrorString(e);
-    c->cap_state.store(e == cudaSuccess ? 2 : 3, std::memory_order_release);
-  });
-}
-
-// Offer a finished step's rows (the context length each attended) to the load profile; on a recorded
-// sample with the window full, update the hot pool target and pick the plan of the window's P90.
-static void adapt_after_step(mag_ctx* c, int B, const int32_t* lens) {
-  if (!c->adapt.enable_adaptive) return;
-  bool rec = false;
-  for (int b = 0; b < B; ++b) rec |= c->profile->observe(lens[b]);
-  if (!rec || !c->profile->full()) return;
-  const int32_t p90 = c->profile->quantile(0.9);
-  int open = 0;
-  for (const Session& s : c->sessions) open += s.open;
-  c->hot_blocks = hot_pool_blocks(p90, open, c->adapt.hot_pool_slack, 16);
-  if (c->kv.elastic() &&
-      c->kv.set_hot(c->hot_blocks, c->stream, [c](int64_t g) { return group_referenced(c, g); }) != MAG_OK)
-    fail(c, MAG_ERR_OOM, "hot pool resize (kept the old size): %s", c->kv.err.c_str());
-  if (c->adapt.force_plan >= 0 || c->pending_plan >= 0) return;
-  const int want = plan_for(p90, c->adapt.plan_short_below, c->adapt.plan_long_above);
-  if (want != c->cur_plan) switch_plan(c, want);
-}
-
-// Launches the step of B rows whose arguments were just uploaded: the captured graph of that shape
-// under the plan in use (captured on first use), or the kernels one by one under MAG_FLAG_NO_GRAPH.
-static mag_status launch_step(mag_ctx* c, int B, bool verify) {
-  const AttnShape sh = attn_shape(c, B);
-  if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
-    int n = 0;
-    CUDA_TRY(c, record_step(c, B, &n, nullptr, verify, sh.splits, sh.wide, c->stream));
-    c->last_launches = n;
-    return MAG_OK;
-  }
-  mag_ctx::StepGraph& g = sh.bucket < 0 ? c->graphs[verify][c->cur_plan][B] : c->len_graphs[verify][sh.bucket][B];
-  if (!g.exec && sh.bucket >= 0) {
-    cudaGraph_t gr = nullptr;
-    int n = 0;
-    cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
-    if (e == cudaSuccess) {
-      e = record_step(c, B, &n, nullptr, verify, sh.splits, sh.wide, c->stream);
-      const cudaError_t e2 = cudaStreamEndCapture(c->stream, &gr);
-      if (e == cudaSuccess) e = e2;
-    }
-    if (e == cudaSuccess) e = cudaGraphInstantiate(&g.exec, gr, 0);
-    if (gr) cudaGraphDestroy(gr);
-    if (e != cudaSuccess) return fail(c, MAG_ERR_CUDA, "step graph capture: %s", cudaGetErrorString(e));
-    g.launches = n;
-  }
-  if (!g.exec) CUDA_TRY(c, capture_graph(c, verify, c->cur_plan, B, c->stream, g));
-  CUDA_TRY(c, cudaGraphLaunch(g.exec, c->stream));
-  c->last_launches = g.launches;
-  return MAG_OK;
-}
-
-mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  mag_status st = poll_capture(c);
-  if (st != MAG_OK) return st;
-  st = step_upload(c, B, sids, in, out);
-  if (st != MAG_OK) return st;
-  st = launch_step(c, B, false);
-  if (st != MAG_OK) return st;
-  int32_t lens[MAG_MAX_BATCH];
-  for (int b = 0; b < B; ++b) lens[b] = ++c->sessions[sids[b]].len;
-  adapt_after_step(c, B, lens);
-  return pool_trim(c);
-}
-
-mag_status mag_debug_profile_step(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out,
-                                  int32_t* kinds, float* ms, int32_t cap, int32_t* n_out) {
-  if (!c || !n_out || cap < 0 || (cap && (!kinds || !ms))) return MAG_ERR_INVALID_ARG;
-  mag_status st = step_upload(c, B, sids, in, out);
-  if (st != MAG_OK) return st;
-  Profiler prof;
-  int n = 0;
-  const AttnShape sh = attn_shape(c, B);
-  CUDA_TRY(c, record_step(c, B, &n, &prof, false, sh.splits, sh.wide, c->stream));
-  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
-  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  *n_out = (int32_t)prof.kinds.size();
-  for (int i = 0; i < (int)prof.kinds.size() && i < cap; ++i) {
-    kinds[i] = prof.kinds[i];
-    CUDA_TRY(c, cudaEventElapsedTime(&ms[i], prof.start[i], prof.stop[i]));
-  }
-  c->last_launches = n;
-  return MAG_OK;
-}
-
-mag_status mag_debug_step_residuals(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out,
-                                    void* resid) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  if (!resid) return fail(c, MAG_ERR_INVALID_ARG, "debug_step_residuals: null residual buffer");
-  mag_status st = step_upload(c, B, sids, in, out);
-  if (st != MAG_OK) return st;
-  int n = 0;
-  const AttnShape sh = attn_shape(c, B);
-  CUDA_TRY(c, record_step(c, B, &n, nullptr, false, sh.splits, sh.wide, c->stream, static_cast<float*>(resid)));
-  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
-  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  c->last_launches = n;
-  return check_err(c);
-}
-
-mag_status mag_debug_set_wait_limit(mag_ctx* c, int64_t polls) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  mag_status st = finish_capture(c);
-  if (st != MAG_OK) return st;
-  const uint32_t v = polls < 0 ? kWaitPolls : (uint32_t)std::min<int64_t>(polls, 0xffffffffll);
-  if (v == c->wait_limit) return MAG_OK;
-  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  // captured graphs hold the old limit in their kernel arguments: capture again on next use
-  for (auto& gv : c->len_graphs)
-    for (auto& gp : gv)
-      for (auto& g : gp)
-        if (g.exec) {
-          cudaGraphExecDestroy(g.exec);
-          g = mag_ctx::StepGraph{};
-        }
-  for (auto& gv : c->graphs)
-    for (auto& gp : gv)
-      for (auto& g : gp)
-        if (g.exec) {
-          cudaGraphExecDestroy(g.exec);
-          g = mag_ctx::StepGraph{};
-        }
-  c->wait_limit = v;
-  return MAG_OK;
-}
-
-mag_status mag_decode_step_host(mag_ctx* c, int32_t B, const int32_t* sids, const void* in_host, void* out_host) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  if (!in_host || !out_host) return fail(c, MAG_ERR_INVALID_ARG, "decode_step_host: null buffer");
-  if (B < 1 || B > c->B_max) return fail(c, MAG_ERR_INVALID_ARG, "decode_step_host: batch %d", B);
-  const size_t in_b = (size_t)B * c->D * 2, out_b = (size_t)B * (c->V ? c->V : c->D) * 2;
-  CUDA_TRY(c, cudaMemcpyAsync(c->d_in_stage, in_host, in_b, cudaMemcpyHostToDevice, c->stream));
-  mag_status st = mag_decode_step(c, B, sids, c->d_in_stage, c->d_out_stage);
-  if (st != MAG_OK) return st;
-  CUDA_TRY(c, cudaMemcpyAsync(out_host, c->d_out_stage, out_b, cudaMemcpyDeviceToHost, c->stream));
-  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  return check_err(c);
-}
-
-namespace {
-
-// The chunk path of mag_prefill_chunk and mag_verify_tokens: T tokens of one session through every layer
-// (their k and v appended to the pool), then the final RMSNorm + LM head (or the final hidden state) of the
-// last out_rows tokens into out [out_rows][V or D].
-// One prefill chunk of n_seg sessions: session sids[i] appends ntok[i] tokens, the rows of the sessions
-// following each other in `in` ([sum ntok][D]); each session's tokens attend causally to its own cache.
-// Output: with all_rows (one session), every row; otherwise the last row of every session, in order.
-// With resid_dump (debug) the launches run without programmatic dependent launch and the fp32 residual of
-// the T rows is copied there after the input and after every layer: [L+1][T][D].
-mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sids, const int32_t* ntok,
-                     const void* in, void* out, bool all_rows, float* resid_dump = nullptr) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  if (c->cfg.max_chunk <= 0) return fail(c, MAG_ERR_UNSUPPORTED, "%s: created with max_chunk = 0", what);
-  if (!in || !out || !sids || !ntok) return fail(c, MAG_ERR_INVALID_ARG, "%s: null buffer", what);
-  if (n_seg < 1 || n_seg > MAG_MAX_BATCH)
-    return fail(c, MAG_ERR_INVALID_ARG, "%s: %d sessions not in 1..%d", what, n_seg, MAG_MAX_BATCH);
-  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "%s: not every weight is loaded", what);
-  int T = 0, need = 0;
-  for (int i = 0; i < n_seg; ++i) {
-    const int sid = sids[i];
-    if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
-      return fail(c, MAG_ERR_INVALID_ARG, "%s: session %d is not open", what, sid);
-    for (int j = 0; j < i; ++j)
-      if (sids[j] == sid) return fail(c, MAG_ERR_INVALID_ARG, "%s: session %d appears twice", what, sid);
-    if (ntok[i] < 1 || ntok[i] > c->cfg.max_chunk - T)
-      return fail(c, MAG_ERR_INVALID_ARG, "%s: %d + %d tokens exceed max_chunk %d", what, T, ntok[i],
-                  c->cfg.max_chunk);
-    const Session& s = c->sessions[sid];
-    if ((int64_t)s.len + ntok[i] > c->cfg.max_context)
-      return fail(c, MAG_ERR_CONTEXT_FULL, "%s: %d + %d tokens exceed max_context %d", what, s.len, ntok[i],
-                  c->cfg.max_context);
-    T += ntok[i];
-    need += (s.len + ntok[i] + 15) / 16 - (s.len + 15) / 16;
-  }
-  const int out_rows = all_rows ? T : n_seg;
-  if (all_rows && (n_seg != 1 || T > kPipeMaxBatch))
-    return fail(c, MAG_ERR_INVALID_ARG, "%s: every row's output needs one session of 1..%d tokens", what,
-                kPipeMaxBatch);
-  mag_status rs = reserve_blocks(c, what, need);
-  if (rs != MAG_OK) return rs;
-  // step arguments of the output rows' LM head (or final hidden state)
-  const int slot = c->ring_pos;
-  CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
-  StepArgs& sa = c->h_ring[slot];
-  memset(&sa, 0, sizeof sa);
-  sa.batch = out_rows;
-  sa.out = out;
-  PrefillAttnArgs pa = {};
-  pa.n_seg = n_seg;
-  RowList last = {};
-  last.n = n_seg;
-  std::vector<int32_t> rows;  // [2][T]: position and session of every row, several sessions only
-  if (n_seg > 1) rows.resize((size_t)2 * T);
-  for (int i = 0, row0 = 0; i < n_seg; row0 += ntok[i], ++i) {
-    Session& s = c->sessions[sids[i]];
-    pa.seg[i] = PfSeg{row0, ntok[i], s.len, sids[i]};
-    last.row[i] = row0 + ntok[i] - 1;
-    if (n_seg > 1)
-      for (int t = 0; t < ntok[i]; ++t) {
-        rows[row0 + t] = s.len + t;
-        rows[(size_t)T + row0 + t] = sids[i];
-      }
-    const int nb_old = (s.len + 15) / 16, nb_new = (s.len + ntok[i] + 15) / 16;
-    for (int b = nb_old; b < nb_new; ++b) s.table.push_back(c->kv.pop());
-    int32_t* row = c->d_tables + (size_t)sids[i] * c->table_stride;
-    if (nb_new > nb_old)
-      CUDA_TRY(c, cudaMemcpyAsync(row + nb_old, s.table.data() + nb_old, (size_t)(nb_new - nb_old) * 4,
-                                  cudaMemcpyHostToDevice, c->stream));
-  }
-  for (int b = 0; b < out_rows; ++b) {
-    sa.sess[b] = all_rows ? sids[0] : sids[b];
-    sa.pos[b] = all_rows ? c->sessions[sids[0]].len + b : c->sessions[sids[b]].len + ntok[b] - 1;
-  }
-  if (n_seg > 1)  // pageable source: the copy has taken the bytes when the call returns
-    CUDA_TRY(c, cudaMemcpyAsync(c->pf_rows, rows.data(), rows.size() * 4, cudaMemcpyHostToDevice, c->stream));
-  CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &sa, sizeof sa, cudaMemcpyHostToDevice, c->stream));
-  CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
-  c->ring_pos = (slot + 1) % kRing;
-  const int32_t* row_pos = n_seg > 1 ? c->pf_rows : nullptr;
-  const int32_t* row_sess = n_seg > 1 ? c->pf_rows + T : nullptr;
-  const int p0 = c->sessions[sids[0]].len;  // one session: positions p0 + row
-  int32_t* row = c->d_tables + (size_t)sids[0] * c->table_stride;
-
-  int n = 0;
-  const bool pdl = !(c->cfg.flags & MAG_FLAG_NO_PDL) && !resid_dump;
-  Launch L{c->stream, pdl, &n};
-  const int D = c->D, HD = c->Hq * c->d;
-  const PoolGeom pg = pool_geom(c);
-  auto dump = [&](int i) {
-    return resid_dump ? cudaMemcpyAsync(resid_dump + (size_t)i * T * D, c->pf_r, (size_t)T * D * 4,
-                                        cudaMemcpyDeviceToDevice, c->stream)
-                      : cudaSuccess;
-  };
-  CUDA_TRY(c, launch_rows_to_resid(L, (const __half*)in, c->pf_r, T, D));
-  CUDA_TRY(c, dump(0));
-  for (int l = 0; l < c->L; ++l) {
-    const Proj* P = &c->proj[(size_t)l * 4];
-    TcGemmArgs g = {};
-    g.M = T;
-    g.err = c->d_err;
-    g.wait_limit = c->wait_limit;
-    // the GEMM's weights: projection i's decode tiles, their rows in the order its epilogue wants
-    auto weights = [&](TcGemmArgs& x, int i) {
-      const Proj& pr = P[i];
-      x.w = pr.tiles;
-      x.n_dtiles = pr.N / 16;
-      x.C = (pr.K + 63) / 64;
-      x.N = prefill_rows(c, i);
-      x.K = pr.K;
-      x.ksplit = tc_gemm_ksplit(x.M, x.N, x.K, c->n_sm);
-      x.part = c->pf_part;
-      x.part_cnt = c->pf_part_cnt;
-      if (pr.map == MAP_QKV) {
-        x.tpg = c->d / 16, x.gsz = c->d, x.half = c->d / 2;
-      } else if (pr.map == MAP_SWIGLU) {
-        x.tpg = 8, x.gsz = 128, x.half = 64;
-      } else {
-        x.tpg = 1, x.gsz = 16, x.half = 8;
-      }
-    };
-    // RMSNorm + QKV (+ RoPE of q and k)
-    CUDA_TRY(c, launch_rmsnorm_rows(L, c->pf_r, c->gamma1[l], c->cfg.rms_eps, T, D, c->pf_xn));
-    TcGemmArgs gq = g;
-    weights(gq, 0);
-    gq.n_valid = c->R;
-    gq.out = c->pf_qkv;
-    gq.ldo = c->R;
-    gq.head_dim = c->d;
-    gq.n_rot_heads = c->Hq + c->Hkv;
-    gq.pos0 = p0;
-    gq.row_pos = row_pos;
-    gq.rope_cos = c->d_cos;
-    gq.rope_sin = c->d_sin;
-    CUDA_TRY(c, launch_tc_gemm(L, c->map_xn, gq, EPI_QKV));
-    // the chunk's k, v into the pool, then causal attention over the pool
-    KvChunkArgs kc = {};
-    kc.qkv = c->pf_qkv;
-    kc.qkv_ld = c->R;
-    kc.n_heads = c->Hq;
-    kc.n_tok = T;
-    kc.pos0 = p0;
-    kc.layer = l;
-    kc.table = row;
-    kc.pool = pg;
-    kc.row_pos = row_pos;
-    kc.row_sess = row_sess;
-    CUDA_TRY(c, launch_kv_store_chunk(L, kc));
-    pa.qkv = c->pf_qkv;
-    pa.qkv_ld = c->R;
-    pa.o = c->pf_o;
-    pa.ldo = HD;
-    pa.n_heads = c->Hq;
-    pa.n_kv_heads = c->Hkv;
-    pa.head_dim = c->d;
-    pa.layer = l;
-    pa.pool = pg;
-    CUDA_TRY(c, launch_prefill_attention(L, pa));
-    // O projection + residual
-    TcGemmArgs go = g;
-    weights(go, 1);
-    go.n_valid = D;
-    go.r = c->pf_r;
-    go.ldr = D;
-    CUDA_TRY(c, launch_tc_gemm(L, c->map_o, go, EPI_RESID));
-    // RMSNorm + gate-up + SwiGLU
-    CUDA_TRY(c, launch_rmsnorm_rows(L, c->pf_r, c->gamma2[l], c->cfg.rms_eps, T, D, c->pf_xn));
-    TcGemmArgs gg = g;
-    weights(gg, 2);
-    gg.n_valid = c->F;
-    gg.out = c->pf_act;
-    gg.ldo = c->F;
-    CUDA_TRY(c, launch_tc_gemm(L, c->map_xn, gg, EPI_SWIGLU));
-    // down projection + residual
-    TcGemmArgs gd = g;
-    weights(gd, 3);
-    gd.n_valid = D;
-    gd.r = c->pf_r;
-    gd.ldr = D;
-    CUDA_TRY(c, launch_tc_gemm(L, c->map_act, gd, EPI_RESID));
-    CUDA_TRY(c, dump(l + 1));
-  }
-  // the output rows: contiguous for one session, else each session's last row gathered
-  float* r_out = c->pf_r + (size_t)(T - out_rows) * D;
-  if (n_seg > 1) {
-    CUDA_TRY(c, launch_gather_rows(L, c->pf_r, D, last, c->pf_last_r));
-    r_out = c->pf_last_r;
-  }
-  if (c->V) {  // final RMSNorm + LM head of the output rows
-    GemvArgs a = gemv_args(c, 4, reinterpret_cast<const uint8_t*>(c->lm_head), c->V / 16, D, out_rows);
-    a.r = r_out;
-    a.ldr = D;
-    a.gamma = c->gamma_f;
-    a.ldo = c->V;
-    CUDA_TRY(c, launch_gemv(L, a, W_F16, XSRC_RESID, EPI_STORE_OUT));
-  } else {
-    CUDA_TRY(c, launch_final_hidden(L, c->d_args, r_out, D, out_rows));
-  }
-  c->last_launches = n;
-  for (int i = 0; i < n_seg; ++i) c->sessions[sids[i]].len += ntok[i];
-  return MAG_OK;
-}
-
-}  // namespace
-
-mag_status mag_prefill_chunk(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out) {
-  return run_chunk(c, "prefill_chunk", 1, &sid, &T, in, last_out, false);
-}
-
-mag_status mag_debug_prefill_residuals(mag_ctx* c, int32_t sid, int32_t T, const void* in, void* last_out,
-                                       void* resid) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  if (!resid) return fail(c, MAG_ERR_INVALID_ARG, "debug_prefill_residuals: null residual buffer");
-  mag_status st = run_chunk(c, "debug_prefill_residuals", 1, &sid, &T, in, last_out, false,
-                            static_cast<float*>(resid));
-  if (st != MAG_OK) return st;
-  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  return check_err(c);
-}
-
-mag_status mag_prefill_batch(mag_ctx* c, int32_t n_sessions, const int32_t* sids, const int32_t* n_tokens,
-                             const void* in, void* last_out) {
-  return run_chunk(c, "prefill_batch", n_sessions, sids, n_tokens, in, last_out, false);
-}
-
-// Verify step on the decode kernels: the n tokens are the n rows of a decode step of one session at
-// positions len .. len + n - 1, with their keys and values stored between the QKV projection and attention.
-static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void* in, void* out) {
-  mag_status st = poll_capture(c);
-  if (st != MAG_OK) return st;
-  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
-    return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: session %d is not open", sid);
-  if (!all_loaded(c)) return fail(c, MAG_ERR_NOT_LOADED, "verify_tokens: not every weight is loaded");
-  Session& s = c->sessions[sid];
-  if ((int64_t)s.len + n > c->cfg.max_context)
-    return fail(c, MAG_ERR_CONTEXT_FULL, "verify_tokens: %d + %d tokens exceed max_context %d", s.len, n,
-                c->cfg.max_context);
-  // n <= 16 tokens reach at most one block past the session's last one
-  const int nb_old = (s.len + 15) / 16, nb_new = (s.len + n + 15) / 16;
-  st = reserve_blocks(c, "verify_tokens", nb_new - nb_old);
-  if (st != MAG_OK) return st;
-  const int slot = c->ring_pos;
-  CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
-  StepArgs& a = c->h_ring[slot];
-  memset(&a, 0, sizeof a);
-  a.batch = n;
-  for (int b = 0; b < n; ++b) {
-    a.sess[b] = sid;
-    a.pos[b] = s.len + b;
-  }
-  c->step_max_len = s.len + n;
-  for (int i = nb_old; i < nb_new; ++i) {
-    const int blk = c->kv.pop();
-    s.table.push_back(blk);
-    a.upd_sess[a.n_upd] = sid;
-    a.upd_idx[a.n_upd] = i;
-    a.upd_blk[a.n_upd] = blk;
-    ++a.n_upd;
-  }
-  for (int b = 0; b < n; ++b) a.blk[b] = s.table[(s.len + b) / 16];
-  a.hidden_in = (const __half*)in;
-  a.out = out;
-  CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
-  CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
-  c->ring_pos = (slot + 1) % kRing;
-  st = launch_step(c, n, true);
-  if (st != MAG_OK) return st;
-  int32_t lens[MAG_MAX_BATCH];
-  for (int b = 0; b < n; ++b) lens[b] = s.len + b + 1;
-  s.len += n;
-  adapt_after_step(c, n, lens);
-  return pool_trim(c);
-}
-
-mag_status mag_verify_tokens(mag_ctx* c, int32_t sid, int32_t n_tokens, const void* hidden_in, void* out) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  if (!hidden_in || !out) return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: null buffer");
-  // up to max_batch tokens on the decode kernels (weights read once for all rows); beyond that, up to
-  // kPipeMaxBatch tokens through the prefill chunk path when the context has one
-  if (n_tokens >= 1 && n_tokens <= c->B_max) return verify_on_step(c, sid, n_tokens, hidden_in, out);
-  const int chunk_max = std::min(kPipeMaxBatch, c->cfg.max_chunk);
-  if (n_tokens >= 1 && n_tokens <= chunk_max)
-    return run_chunk(c, "verify_tokens", 1, &sid, &n_tokens, hidden_in, out, true);
-  return fail(c, MAG_ERR_INVALID_ARG, "verify_tokens: %d tokens not in 1..%d", n_tokens,
-              std::max(c->B_max, chunk_max));
-}
-
-mag_status mag_session_truncate(mag_ctx* c, int32_t sid, int32_t length) {
-  if (!c) return MAG_ERR_INVALID_ARG;
-  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
-    return fail(c, MAG_ERR_INVALID_ARG, "session_truncate: session %d is not open", sid);
-  Session& s = c->sessions[sid];
-  if (length < 0 || length > s.len)
-    return fail(c, MAG_ERR_INVALID_ARG, "session_truncate: length %d not in 0..%d", length, s.len);
-  // blocks wholly past the new length go back to the pool; the device table keeps stale entries past
-  // the length, which nothing reads, and a later append writes the new ids before they are used
-  const size_t nb = (size_t)(length + 15) / 16;
-  while (s.table.size() > nb) {
-    c->kv.push(s.table.back());
-    s.table.pop_back();
-  }
-  s.len = length;
-  return pool_trim(c);
-}
-
-void mag_adapt_defaults(mag_adapt_config* a) {
-  if (!a) return;
-  *a = mag_adapt_config{};
-  a->enable_adaptive = 1;
-  a->adaptive_window_size = 64;
-  a->adaptive_sample_rate = 4;
-  a->plan_short_below = 128;
-  a->plan_long_above = 512;
-  // measured on GB300 (8B shape, one session): 4 splits are fastest below ~128 keys, 8 to ~300, 16 above
-  a->plan_splits[0] = 4;
-  a->plan_splits[1] = 8;
-  a->plan_splits[2] = 16;
-  a->force_plan = -1;
-  a->async_switch = 0;
-  a->hot_pool_slack = 1.2f;
-}
-
-mag_status mag_set_adaptive(mag_ctx* c, const mag_adapt_config* a) {
-  if (!c || !a) return MAG_ERR_INVALID_ARG;
-  if (a->enable_adaptive) {
-    if (a->adaptive_window_size < 1 || a->adaptive_sample_rate < 1)
-      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: window %d and sample rate %d must be >= 1",
-                  a->adaptive_window_size, a->adaptive_sample_rate);
-    if (a->plan_short_below > a->plan_long_above + 1)
-      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: short_below %d above long_above %d",
-                  a->plan_short_below, a->plan_long_above);
-    for (int i = 0; i < 3; ++i) {
-      if (a->plan_splits[i] < 0 || a->plan_splits[i] > 8 * kAttnMaxGroups)
-        return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: plan %d splits %d not in 0..%d", i, a->plan_splits[i],
-                    8 * kAttnMaxGroups);
-      if (a->plan_wide[i] != 0 && a->plan_wide[i] != 1)
-        return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: plan %d wide %d not 0 or 1", i, a->plan_wide[i]);
-    }
-    if (a->force_plan < -1 || a->force_plan > 2)
-      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: force_plan %d not in -1..2", a->force_plan);
-    if (!(a->hot_pool_slack >= 1.0f && a->hot_pool_slack <= 16.0f))
-      return fail(c, MAG_ERR_INVALID_ARG, "set_adaptive: hot_pool_slack %g not in 1..16", a->hot_pool_slack);
-  }
-  mag_status st = finish_capture(c);
-  if (st != MAG_OK) return st;
-  if (a->enable_adaptive && a->async_switch && !c->cap_stream)
-    CUDA_TRY(c, cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
-  // graphs captured under other split counts are dropped; the ones that stay valid are kept
-  mag_adapt_config next = a->enable_adaptive ? *a : mag_adapt_config{};
-  for (int p = 0; p < 3; ++p) {
-    for (int b = 1; b <= MAG_MAX_BATCH; ++b) {
-      const int s_old = plan_splits(c, p, b) * 2 + plan_wide(c, p);
-      std::swap(c->adapt, next);
-      const int s_new = plan_splits(c, p, b) * 2 + plan_wide(c, p);
-      std::swap(c->adapt, next);
-      if (s_old == s_new) continue;
-      for (int v = 0; v < 2; ++v) {
-        mag_ctx::StepGraph& g = c->graphs[v][p][b];
-        if (g.exec) {
-          CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-          CUDA_TRY(c, cudaGraphExecDestroy(g.exec));
-          g = mag_ctx::StepGraph{};
-        }
-      }
-    }
-  }
-  c->adapt = next;
-  c->profile.reset();
-  if (next.enable_adaptive)
-    c->profile = std::make_unique<LoadProfile>(next.adaptive_window_size, next.adaptive_sample_rate);
-  c->hot_blocks = -1;
-  if (next.enable_adaptive && next.force_plan >= 0) {
-    if (next.force_plan != c->cur_plan) ++c->switches;
-    c->cur_plan = next.force_plan;
-  }
-  if (!next.enable_adaptive) c->cur_plan = 1;
-  return MAG_OK;
-}
-
-mag_status mag_get_profile(mag_ctx* c, mag_profile* out) {
-  if (!c || !out) return MAG_ERR_INVALID_ARG;
-  mag_status st = poll_capture(c);
-  if (st != MAG_OK) return st;
-  *out = mag_profile{};
-  out->seen = c->profile ? c->profile->seen() : 0;
-  out->recorded = c->profile ? c->profile->count() : 0;
-  out->p50 = c->profile ? c->profile->quantile(0.5) : -1;
-  out->p90 = c->profile ? c->profile->quantile(0.9) : -1;
-  out->p99 = c->profile ? c->profile->quantile(0.99) : -1;
-  out->plan = c->cur_plan;
-  out->pending_plan = c->pending_plan;
-  out->plan_splits = plan_splits(c, c->cur_plan, 1);
-  out->plan_wide = plan_wide(c, c->cur_plan);
-  out->switches = c->switches;
-  out->hot_blocks = c->hot_blocks;
   return MAG_OK;
 }
 
