@@ -48,7 +48,9 @@ typedef enum {
   MAG_ERR_NOT_LOADED = 5,   /* a step was asked for before every weight was loaded */
   MAG_ERR_CUDA = 6,         /* a CUDA runtime call failed (message says which) */
   MAG_ERR_TIMEOUT = 7,      /* a bounded device-side wait gave up */
-  MAG_ERR_UNSUPPORTED = 8   /* a shape or mode this build does not handle */
+  MAG_ERR_UNSUPPORTED = 8,  /* a shape or mode this build does not handle */
+  MAG_ERR_CORRUPT = 9       /* a device-side check found a write outside an arena tensor (MAG_FLAG_DEBUG_CANARY)
+                               or a block-table entry outside the pool; the message says which */
 } mag_status;
 
 typedef enum { MAG_KV_FP16 = 0, MAG_KV_INT8 = 1, MAG_KV_INT4 = 2 } mag_kv_dtype;
@@ -64,6 +66,15 @@ typedef enum { MAG_KV_FP16 = 0, MAG_KV_INT8 = 1, MAG_KV_INT4 = 2 } mag_kv_dtype;
  * is one group, or, with the adaptive runtime on, hot_pool_slack x the P90 need (mag_set_adaptive).
  * Free blocks go out lowest id first. pool_order_host must be NULL. */
 #define MAG_FLAG_ELASTIC_POOL ((uint64_t)8)
+/* Time every step with a pair of CUDA events around its launches (mag_get_step_stats.last_ms). */
+#define MAG_FLAG_STEP_TIMING ((uint64_t)16)
+/* Debug: 64-byte canary bands before and after every decode-arena tensor (the arena then reuses no bytes,
+ * as with MAG_FLAG_ARENA_NO_REUSE), checked by one more kernel at the end of every decode or verify step;
+ * a changed band makes the next mag_sync return MAG_ERR_CORRUPT naming the tensor, and the bands are
+ * rewritten. (Every step also checks each pool block id it reads from a block table against the pool: an
+ * id outside it is not used, the step's results are wrong, and mag_sync returns MAG_ERR_CORRUPT; the
+ * device tables are then rewritten from the host's copy.) */
+#define MAG_FLAG_DEBUG_CANARY ((uint64_t)32)
 
 /* Model shape and capacities ([Core] 5.1: the shape travels with the model;
  * [Core] 5.2: everything sized once, up front; [Magnitude] 4.3: EngineConfig). */
@@ -266,6 +277,24 @@ typedef struct mag_memory_stats {
 /* [Magnitude] 5.2 get_memory_stats: weights, pool, arena. */
 mag_status mag_get_memory_stats(mag_ctx* ctx, mag_memory_stats* out);
 
+/* Statistics of the context's steps ([Magnitude] 4.4 InferenceResult timing, per step): the last decode,
+ * verify or prefill call and the running count. last_bytes models the step's device traffic: the weights
+ * read once (packed W4, scales, norm gains, LM head), every row's KV up to the keys it attends, and the
+ * hidden states in and the logits (or hidden states) out. */
+typedef struct mag_step_stats {
+  int64_t steps;             /* decode, verify and prefill calls that launched work since create */
+  int32_t last_kind;         /* 0 decode step, 1 verify on the decode kernels, 2 the chunk path (prefill / verify) */
+  int32_t last_rows;         /* token rows of the last call (batch, drafts or chunk tokens) */
+  int32_t last_launches;     /* kernel launches of the last call */
+  int32_t last_max_keys;     /* most keys one row of the last call attends */
+  uint64_t last_bytes;       /* modelled device bytes of the last call */
+  double last_ms;            /* device time of the last call (MAG_FLAG_STEP_TIMING), else -1 */
+} mag_step_stats;
+
+/* Statistics of the last call; with MAG_FLAG_STEP_TIMING this waits for that call to finish.
+ * Errors: INVALID_ARG (null), CUDA. */
+mag_status mag_get_step_stats(mag_ctx* ctx, mag_step_stats* out);
+
 /* Message of the last error on this context (never NULL; "" if none). */
 const char* mag_last_error(mag_ctx* ctx);
 
@@ -376,6 +405,16 @@ typedef struct mag_arena_tensor {
  * n_out and the arena size into arena_bytes. */
 mag_status mag_debug_arena_plan(mag_ctx* ctx, int32_t phase, mag_arena_tensor* out, int32_t cap, int32_t* n_out,
                                 uint64_t* arena_bytes);
+
+/* Debug: write one entry of a session's block table on the device only (the host keeps its own copy), to
+ * test the block-id checks of MAG_ERR_CORRUPT. Synchronous. Errors: INVALID_ARG (session not open, index
+ * past the session's blocks), CUDA. */
+mag_status mag_debug_set_table_entry(mag_ctx* ctx, int32_t session, int32_t index, int32_t value);
+
+/* Debug: the decode activation arena's device address and size (the offsets of mag_debug_arena_plan phase
+ * 0 are relative to it; with MAG_FLAG_DEBUG_CANARY a tensor's bytes start kCanaryBand = 64 bytes into its
+ * planned slot, after its leading band). */
+mag_status mag_debug_arena(mag_ctx* ctx, void** ptr, uint64_t* bytes);
 
 /* Kernel launches of the last decode step (0 if none ran yet). */
 int32_t mag_debug_last_step_launches(mag_ctx* ctx);

@@ -16,23 +16,25 @@ LIB_PATH = os.path.join(_HERE, "libmag.so")
 _lock = threading.Lock()
 _lib = None
 
-OK, ERR_INVALID_ARG, ERR_OOM, ERR_KV_FULL, ERR_CONTEXT_FULL, ERR_NOT_LOADED, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = \
-    range(9)
-STATUS_NAMES = ["OK", "INVALID_ARG", "OOM", "KV_FULL", "CONTEXT_FULL", "NOT_LOADED", "CUDA", "TIMEOUT", "UNSUPPORTED"]
+(OK, ERR_INVALID_ARG, ERR_OOM, ERR_KV_FULL, ERR_CONTEXT_FULL, ERR_NOT_LOADED, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED,
+ ERR_CORRUPT) = range(10)
+STATUS_NAMES = ["OK", "INVALID_ARG", "OOM", "KV_FULL", "CONTEXT_FULL", "NOT_LOADED", "CUDA", "TIMEOUT", "UNSUPPORTED",
+                "CORRUPT"]
 KV_FP16, KV_INT8, KV_INT4 = 0, 1, 2
 W_QKV, W_O, W_GATE_UP, W_DOWN, NORM_ATTN, NORM_FFN, NORM_FINAL, LM_HEAD = range(8)
 FMT_F32_DENSE, FMT_W4G32, FMT_F16 = 0, 1, 2
-FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL, FLAG_ELASTIC_POOL = 1, 2, 4, 8
+FLAG_NO_GRAPH, FLAG_ARENA_NO_REUSE, FLAG_NO_PDL, FLAG_ELASTIC_POOL, FLAG_STEP_TIMING = 1, 2, 4, 8, 16
+FLAG_DEBUG_CANARY = 32
 
 EXPORTED = [
     "mag_create", "mag_destroy", "mag_load_weights", "mag_load_weights_f32_noalloc", "mag_session_open", "mag_session_close", "mag_session_length",
     "mag_session_truncate", "mag_kv_append", "mag_decode_step", "mag_decode_step_host", "mag_prefill_chunk",
     "mag_verify_tokens", "mag_prefill_batch", "mag_sync",
-    "mag_get_memory_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
+    "mag_get_memory_stats", "mag_get_step_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
     "mag_debug_last_step_launches", "mag_debug_profile_step", "mag_debug_step_residuals",
     "mag_debug_prefill_residuals", "mag_debug_set_wait_limit",
-    "mag_debug_fail_allocations",
+    "mag_debug_fail_allocations", "mag_debug_set_table_entry", "mag_debug_arena",
     "mag_adapt_defaults", "mag_set_adaptive", "mag_get_profile", "mag_profiler_create", "mag_profiler_destroy",
     "mag_profiler_observe", "mag_profiler_quantile", "mag_profiler_count", "mag_plan_for", "mag_hot_pool_blocks",
 ]
@@ -69,6 +71,12 @@ class MemoryStats(ctypes.Structure):
                 ("prefill_arena_bytes", ctypes.c_uint64), ("kv_pool_mapped_bytes", ctypes.c_uint64),
                 ("pool_blocks_mapped", ctypes.c_int32), ("pool_blocks_hot", ctypes.c_int32),
                 ("pool_group_blocks", ctypes.c_int32)]
+
+
+class StepStats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("last_kind", ctypes.c_int32), ("last_rows", ctypes.c_int32),
+                ("last_launches", ctypes.c_int32), ("last_max_keys", ctypes.c_int32),
+                ("last_bytes", ctypes.c_uint64), ("last_ms", ctypes.c_double)]
 
 
 class ArenaTensor(ctypes.Structure):
@@ -124,6 +132,7 @@ def lib():
                 "mag_prefill_batch": ([vp, i32, P32, P32, vp, vp], i32),
                 "mag_sync": ([vp], i32),
                 "mag_get_memory_stats": ([vp, ctypes.POINTER(MemoryStats)], i32),
+                "mag_get_step_stats": ([vp, ctypes.POINTER(StepStats)], i32),
                 "mag_last_error": ([vp], ctypes.c_char_p),
                 "mag_kv_bytes_per_token": ([ctypes.POINTER(Config)], u64),
                 "mag_quantize_w4g32": ([vp, i64, i64, vp, vp, vp], i32),
@@ -138,6 +147,8 @@ def lib():
                 "mag_debug_prefill_residuals": ([vp, i32, i32, vp, vp, vp], i32),
                 "mag_debug_set_wait_limit": ([vp, i64], i32),
                 "mag_debug_fail_allocations": ([i32, i32], None),
+                "mag_debug_set_table_entry": ([vp, i32, i32, i32], i32),
+                "mag_debug_arena": ([vp, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_uint64)], i32),
                 "mag_adapt_defaults": ([ctypes.POINTER(AdaptConfig)], None),
                 "mag_set_adaptive": ([vp, ctypes.POINTER(AdaptConfig)], i32),
                 "mag_get_profile": ([vp, ctypes.POINTER(Profile)], i32),
@@ -327,6 +338,11 @@ class Context:
         self._check(lib().mag_get_memory_stats(self.h, ctypes.byref(s)), "mag_get_memory_stats")
         return {n: getattr(s, n) for n, _ in MemoryStats._fields_}
 
+    def step_stats(self) -> dict:
+        s = StepStats()
+        self._check(lib().mag_get_step_stats(self.h, ctypes.byref(s)), "mag_get_step_stats")
+        return {n: getattr(s, n) for n, _ in StepStats._fields_}
+
     def debug_read_weights(self, tensor, layer, dst, nbytes):
         self._check(lib().mag_debug_read_weights(self.h, tensor, layer, _ptr(dst), nbytes), "mag_debug_read_weights")
 
@@ -338,6 +354,11 @@ class Context:
     def debug_pool(self):
         p, n = ctypes.c_void_p(), ctypes.c_uint64()
         self._check(lib().mag_debug_pool(self.h, ctypes.byref(p), ctypes.byref(n)), "mag_debug_pool")
+        return p.value, n.value
+
+    def debug_arena(self):
+        p, n = ctypes.c_void_p(), ctypes.c_uint64()
+        self._check(lib().mag_debug_arena(self.h, ctypes.byref(p), ctypes.byref(n)), "mag_debug_arena")
         return p.value, n.value
 
     def debug_arena_plan(self, phase=0):
@@ -376,6 +397,10 @@ class Context:
         ids = (ctypes.c_int32 * len(sessions))(*sessions)
         self._check(lib().mag_debug_step_residuals(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out),
                                                    _ptr(resid)), "mag_debug_step_residuals")
+
+    def debug_set_table_entry(self, sid: int, index: int, value: int):
+        """Write one block-table entry on the device only (tests of the block-id checks)."""
+        self._check(lib().mag_debug_set_table_entry(self.h, sid, index, value), "mag_debug_set_table_entry")
 
     def set_wait_limit(self, polls: int):
         """Polls of a GEMV pipeline wait before it gives up (< 0: the built-in limit; 0: at once)."""

@@ -22,6 +22,30 @@ mag_status check_err(mag_ctx* c) {
   const uint32_t e = *reinterpret_cast<volatile uint32_t*>(c->h_err);
   if (e == 0) return MAG_OK;
   *reinterpret_cast<volatile uint32_t*>(c->h_err) = 0;
+  if (e & (kErrCanary | kErrBounds)) {
+    std::string what;
+    if (e & kErrCanary) {
+      what = "a canary band changed around arena tensor(s):";
+      for (size_t i = 0; i < c->plan.size() && i < 16; ++i)
+        if (e & (1u << (kErrCanaryShift + i))) what += " " + c->plan[i].name;
+      // the bands again, for the steps after this one
+      for (const auto& t : c->plan) {
+        cudaMemsetAsync(c->arena + t.offset, kCanaryByte, c->canary_band, c->stream);
+        cudaMemsetAsync(c->arena + t.offset + t.size - c->canary_band, kCanaryByte, c->canary_band, c->stream);
+      }
+    }
+    if (e & kErrBounds) {
+      if (!what.empty()) what += "; ";
+      what += "a block-table entry outside the pool (not used; the step's results are wrong)";
+      // the device tables from the host's copy
+      for (size_t sid = 0; sid < c->sessions.size(); ++sid)
+        if (c->sessions[sid].open && !c->sessions[sid].table.empty())
+          cudaMemcpyAsync(c->d_tables + sid * c->table_stride, c->sessions[sid].table.data(),
+                          c->sessions[sid].table.size() * 4, cudaMemcpyHostToDevice, c->stream);
+    }
+    cudaStreamSynchronize(c->stream);
+    return fail(c, MAG_ERR_CORRUPT, "%s", what.c_str());
+  }
   cudaMemsetAsync(c->d_counters, 0, c->n_counters * 4, c->stream);
   cudaMemsetAsync(c->attn_arrivals, 0, (size_t)c->B_max * c->Hkv * 4, c->stream);
   if (c->pf_part_cnt) cudaMemsetAsync(c->pf_part_cnt, 0, (size_t)(c->n_sm / 2) * 4 * 4, c->stream);
@@ -210,13 +234,31 @@ void build_decode_plan(mag_ctx* c) {
   if (part) c->plan.push_back(T("gemv_partial", part * 4, 1, 6));
   c->arena_unshared = 0;
   for (auto& t : c->plan) c->arena_unshared += t.size;
-  c->arena_bytes = plan_arena(c->plan, 64, (c->cfg.flags & MAG_FLAG_ARENA_NO_REUSE) != 0);
+  // debug canaries: every tensor between two bands of its own, and no two tensors share bytes (a tensor's
+  // bytes may then not be another one's band)
+  const bool canary = (c->cfg.flags & MAG_FLAG_DEBUG_CANARY) != 0;
+  c->canary_band = canary ? kCanaryBand : 0;
+  for (auto& t : c->plan) t.size += 2 * c->canary_band;
+  c->arena_bytes = plan_arena(c->plan, 64, canary || (c->cfg.flags & MAG_FLAG_ARENA_NO_REUSE) != 0);
 }
 
 void* arena_ptr(mag_ctx* c, const char* name) {
   for (auto& t : c->plan)
-    if (t.name == name) return c->arena + t.offset;
+    if (t.name == name) return c->arena + t.offset + c->canary_band;
   return nullptr;
+}
+
+ArenaCheck arena_check_args(const mag_ctx* c) {
+  ArenaCheck a = {};
+  a.base = c->arena;
+  a.err = c->d_err;
+  for (const auto& t : c->plan) {
+    if (a.n == 16) break;
+    a.band[a.n][0] = t.offset;
+    a.band[a.n][1] = t.offset + t.size - c->canary_band;
+    ++a.n;
+  }
+  return a;
 }
 
 GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, int K, int B) {
@@ -260,6 +302,8 @@ void free_ctx(mag_ctx* c) {
         if (g.exec) cudaGraphExecDestroy(g.exec);
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
   for (auto& e : c->ring_ev)
+    if (e) cudaEventDestroy(e);
+  for (auto& e : c->ev_step)
     if (e) cudaEventDestroy(e);
   cudaFree(c->wbase);
   cudaFree(c->d_tables);
@@ -477,6 +521,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
     fail(c, MAG_ERR_OOM, "arena: %s", cudaGetErrorString(e));
     return bail(MAG_ERR_OOM);
   }
+  if (c->canary_band) cudaMemsetAsync(c->arena, kCanaryByte, c->arena_bytes, c->stream);
   c->r = (float*)arena_ptr(c, "residual");
   c->ss_part = (float*)arena_ptr(c, "sumsq_part");
   c->qkv = (__half*)arena_ptr(c, "qkv");
@@ -511,6 +556,7 @@ mag_status mag_create(const mag_config* cfg, void* cuda_stream, mag_ctx** out) {
   cudaMemsetAsync(c->attn_arrivals, 0, arrival_bytes, c->stream);
   c->other_bytes += part_bytes + arrival_bytes;
   for (auto& ev : c->ring_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  for (auto& ev : c->ev_step) cudaEventCreate(&ev);
   c->other_bytes += nc * 4 + sizeof(StepArgs) + (size_t)c->B_max * c->D * 2 + stage_out;
   if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
     fail(c, MAG_ERR_CUDA, "create: %s", cudaGetErrorString(e));
@@ -669,6 +715,7 @@ mag_status mag_kv_append(mag_ctx* c, int32_t sid, int32_t n, const void* k, cons
   a.pos0 = s.len;
   a.table = row;
   a.pool = pool_geom(c);
+  a.err = c->d_err;
   Launch L{c->stream, false, nullptr};
   // grid.x is the token count: split very long appends to respect the grid limit
   for (int t0 = 0; t0 < n; t0 += 65535) {
@@ -774,5 +821,38 @@ mag_status mag_debug_arena_plan(mag_ctx* c, int32_t phase, mag_arena_tensor* out
 }
 
 int32_t mag_debug_last_step_launches(mag_ctx* c) { return c ? c->last_launches : 0; }
+
+mag_status mag_debug_set_table_entry(mag_ctx* c, int32_t sid, int32_t idx, int32_t value) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (sid < 0 || sid >= (int)c->sessions.size() || !c->sessions[sid].open)
+    return fail(c, MAG_ERR_INVALID_ARG, "debug_set_table_entry: session %d is not open", sid);
+  if (idx < 0 || idx >= (int)c->sessions[sid].table.size())
+    return fail(c, MAG_ERR_INVALID_ARG, "debug_set_table_entry: index %d not in 0..%d", idx,
+                (int)c->sessions[sid].table.size() - 1);
+  CUDA_TRY(c, cudaMemcpyAsync(c->d_tables + (size_t)sid * c->table_stride + idx, &value, 4, cudaMemcpyHostToDevice,
+                              c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return MAG_OK;
+}
+
+mag_status mag_debug_arena(mag_ctx* c, void** p, uint64_t* bytes) {
+  if (!c || !p || !bytes) return MAG_ERR_INVALID_ARG;
+  *p = c->arena;
+  *bytes = c->arena_bytes;
+  return MAG_OK;
+}
+
+mag_status mag_get_step_stats(mag_ctx* c, mag_step_stats* out) {
+  if (!c || !out) return MAG_ERR_INVALID_ARG;
+  *out = c->stats;
+  out->last_ms = -1.0;
+  if (c->step_timed && c->stats.steps > 0) {
+    CUDA_TRY(c, cudaEventSynchronize(c->ev_step[1]));
+    float ms = 0.f;
+    CUDA_TRY(c, cudaEventElapsedTime(&ms, c->ev_step[0], c->ev_step[1]));
+    out->last_ms = ms;
+  }
+  return MAG_OK;
+}
 
 }  // extern "C"

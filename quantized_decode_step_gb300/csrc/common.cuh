@@ -6,6 +6,20 @@
 
 #define MAG_MAX_BATCH 16
 
+// Error-word bits of the device-side checks (the waits that give up use bits 2-8): a pool block id read
+// from a block table outside the pool (the id is not used), and a changed arena canary band (bit 16 + i:
+// arena tensor i).
+constexpr uint32_t kErrBounds = 2048u;
+constexpr uint32_t kErrCanary = 1024u;
+constexpr int kErrCanaryShift = 16;
+// A pool block id from a block table, checked against the pool: an id outside it becomes 0 (a valid block)
+// and sets kErrBounds.
+__device__ __forceinline__ int checked_block(int phys, int pool_blocks, uint32_t* err) {
+  if ((unsigned)phys < (unsigned)pool_blocks) return phys;
+  if (err) atomicOr(err, kErrBounds);
+  return 0;
+}
+
 // Step arguments uploaded once per decode step (one small H2D copy) and read
 // by the kernels of the captured graph, so the graph itself never changes.
 struct StepArgs {

@@ -147,6 +147,11 @@ struct mag_ctx {
   StepGraph len_graphs[2][kLenBuckets][MAG_MAX_BATCH + 1];
   int step_max_len = 0;  // longest context (position + 1) among the rows of the step being launched
   int last_launches = 0;
+  uint64_t canary_band = 0;  // MAG_FLAG_DEBUG_CANARY: bytes of each band before and after an arena tensor
+  // mag_get_step_stats: the last call's figures, and its event pair (MAG_FLAG_STEP_TIMING)
+  mag_step_stats stats{};
+  cudaEvent_t ev_step[2] = {nullptr, nullptr};
+  bool step_timed = false;
 
   // adaptive runtime: load profile, plan in use, background capture of a new plan's graphs
   mag_adapt_config adapt{};  // enable_adaptive = 0 until mag_set_adaptive
@@ -192,6 +197,7 @@ constexpr size_t kPipeBudget = 200 * 1024, kSmemMax = 227 * 1024;
 
 mag_status fail(mag_ctx* c, mag_status s, const char* fmt, ...);
 mag_status check_err(mag_ctx* c);
+ArenaCheck arena_check_args(const mag_ctx* c);  // the decode arena's canary bands
 GemvPlan plan_gemv(const mag_ctx* c, int kind, int n_mtiles, int K, int B);
 int attn_splits(const mag_ctx* c, int B, bool wide = false);
 PoolGeom pool_geom(const mag_ctx* c);
@@ -231,6 +237,10 @@ mag_status finish_capture(mag_ctx* c);
 void switch_plan(mag_ctx* c, int p);
 void adapt_after_step(mag_ctx* c, int B, const int32_t* lens);
 mag_status launch_step(mag_ctx* c, int B, bool verify);
+// statistics of a call about to launch: kind (0 decode, 1 verify step, 2 chunk path), rows, the keys each
+// row attends; records the start event with MAG_FLAG_STEP_TIMING
+mag_status stats_begin(mag_ctx* c, int kind, int rows, int out_rows, const int32_t* keys, int n_keys_rows);
+mag_status stats_end(mag_ctx* c);  // launches from last_launches; the end event
 
 // prefill.cu
 mag_status setup_prefill(mag_ctx* c);

@@ -102,6 +102,10 @@ __global__ void kv_store_kernel(const KvStoreArgs a) {
   __syncthreads();
   const int pos = a.pos0 + t;
   const int blk = a.table[pos >> 4];
+  if ((unsigned)blk >= (unsigned)a.pool.pool_blocks) {  // a table entry outside the pool: store nothing
+    if (i == 0 && a.err) atomicOr(a.err, kErrBounds);
+    return;
+  }
   store_vec(a.pool, l, blk, pos & 15, h, 0, xk, red);
   store_vec(a.pool, l, blk, pos & 15, h, 1, xv, red);
 }
@@ -320,7 +324,8 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   auto phys_of = [&](int j) {
     const int blk = blk0 + warp + NWARP * j;
     const int p = j < 32 ? __shfl_sync(0xffffffffu, phys_l, j) : table[blk];
-    return blk == new_blk ? phys_new : blk >= fresh_blk ? table[blk] : p;
+    // an id outside the pool (a corrupted table) is not used: block 0 instead, and the error word says so
+    return checked_block(blk == new_blk ? phys_new : blk >= fresh_blk ? table[blk] : p, a.pool.pool_blocks, a.err);
   };
   uint8_t* ring = smem + (size_t)warp * kAttnSlots * SG::kBytes;
   int issued = 0;
@@ -651,6 +656,10 @@ __global__ void kv_store_chunk_kernel(const KvChunkArgs a) {
   const int sess = a.row_sess ? a.row_sess[t] : (a.step ? a.step->sess[0] : -1);
   const int32_t* table = sess >= 0 ? a.pool.tables + (int64_t)sess * a.pool.table_stride : a.table;
   const int blk = table[pos >> 4];
+  if ((unsigned)blk >= (unsigned)a.pool.pool_blocks) {  // a table entry outside the pool: store nothing
+    if (i == 0 && a.err) atomicOr(a.err, kErrBounds);
+    return;
+  }
   store_vec(a.pool, a.layer, blk, pos & 15, h, 0, xk, red);
   store_vec(a.pool, a.layer, blk, pos & 15, h, 1, xv, red);
 }
@@ -782,7 +791,8 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
 #pragma unroll
       for (int pb = 0; pb < 4; ++pb) {
         const int blk = i * 4 + pb;
-        const uint8_t* kb = pool_head0 + (int64_t)(blk * 16 < n_valid ? table[blk] : 0) * a.pool.block_bytes +
+        const int pbk = blk * 16 < n_valid ? checked_block(table[blk], a.pool.pool_blocks, a.err) : 0;
+        const uint8_t* kb = pool_head0 + (int64_t)pbk * a.pool.block_bytes +
                             r0 * (2 * D) + c8 * 2;
 #pragma unroll
         for (int jj = 0; jj < 16 / kRpp; ++jj) {
@@ -812,7 +822,9 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
           continue;
         }
         float v[8];
-        dequant_unit(dt, load_unit(a.pool, a.layer, table[kp >> 4], which, gk, kp & 15, c8), v);
+        dequant_unit(dt, load_unit(a.pool, a.layer, checked_block(table[kp >> 4], a.pool.pool_blocks, a.err), which, gk,
+                                   kp & 15, c8),
+                     v);
         __half h[8], lo[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {

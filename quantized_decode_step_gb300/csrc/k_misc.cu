@@ -78,6 +78,20 @@ __global__ void step_begin_kernel(const StepArgs* __restrict__ st, float* __rest
   }
 }
 
+// Debug canaries: every 32-bit word of every arena tensor's two bands must still hold the pattern; a changed
+// band sets kErrCanary and the tensor's bit in the error word.
+__global__ void arena_check_kernel(const ArenaCheck a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int W = kCanaryBand / 4;  // words per band
+  const uint32_t pattern = (uint32_t)kCanaryByte * 0x01010101u;
+  for (int i = threadIdx.x; i < a.n * 2 * W; i += blockDim.x) {
+    const int tsr = i / (2 * W), r = i - tsr * 2 * W, side = r / W, w = r - side * W;
+    const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(a.base + a.band[tsr][side]) + w);
+    if (v != pattern) atomicOr(a.err, kErrCanary | (1u << (kErrCanaryShift + tsr)));
+  }
+}
+
 // No LM head: the output is the fp16 hidden state.
 __global__ void final_hidden_kernel(const StepArgs* __restrict__ st, const float* __restrict__ r, int D) {
   pdl_wait();
@@ -194,6 +208,11 @@ cudaError_t launch_quantize_w4g32(cudaStream_t s, const float* src, int64_t rows
 cudaError_t launch_step_begin(const Launch& L, const StepArgs* step, float* r, int D, int32_t* tables,
                               int table_stride, int batch, float* ss_part) {
   return launch_plain(L, step_begin_kernel, dim3(batch), dim3(256), step, r, D, tables, table_stride, ss_part);
+}
+
+cudaError_t launch_arena_check(const Launch& L, const ArenaCheck& a) {
+  if (a.n < 1 || a.n > 16) return cudaErrorInvalidValue;
+  return launch_plain(L, arena_check_kernel, dim3(1), dim3(256), a);
 }
 
 cudaError_t launch_final_hidden(const Launch& L, const StepArgs* step, const float* r, int D, int batch) {

@@ -146,6 +146,17 @@ cudaError_t launch_step_begin(const Launch& L, const StepArgs* step, float* r, i
                               int table_stride, int batch, float* ss_part);
 cudaError_t launch_final_hidden(const Launch& L, const StepArgs* step, const float* r, int D, int batch);
 
+// Debug canaries (MAG_FLAG_DEBUG_CANARY): 64-byte bands of kCanaryByte before and after each arena tensor.
+constexpr int kCanaryBand = 64;
+constexpr unsigned char kCanaryByte = 0xA5;
+struct ArenaCheck {
+  const uint8_t* base;
+  int32_t n;                    // tensors, at most 16
+  uint64_t band[16][2];         // byte offsets of tensor i's band before and after it
+  uint32_t* err;                // kErrCanary | 1 << (kErrCanaryShift + i) for a changed band of tensor i
+};
+cudaError_t launch_arena_check(const Launch& L, const ArenaCheck& a);
+
 // ---------------------------------------------------------------- bulk KV store
 struct KvStoreArgs {
   const __half* k;  // [L][n][Hkv][d]
@@ -154,6 +165,7 @@ struct KvStoreArgs {
   int32_t pos0;        // position of the first appended token
   const int32_t* table;  // this session's block table (device)
   PoolGeom pool;
+  uint32_t* err;         // kErrBounds when a table entry is outside the pool
 };
 cudaError_t launch_kv_store(const Launch& L, const KvStoreArgs& a);
 
@@ -171,6 +183,7 @@ struct KvChunkArgs {
   // when set (several sessions in one chunk), token t goes to session row_sess[t] at position row_pos[t]
   const int32_t* row_pos;
   const int32_t* row_sess;
+  uint32_t* err;  // kErrBounds when a table entry is outside the pool
 };
 cudaError_t launch_kv_store_chunk(const Launch& L, const KvChunkArgs& a);
 
@@ -190,6 +203,7 @@ struct PrefillAttnArgs {
   PoolGeom pool;      // block tables of the sessions in pool.tables
   int32_t n_seg;      // grid.z
   PfSeg seg[MAG_MAX_BATCH];
+  uint32_t* err;      // kErrBounds when a table entry is outside the pool
 };
 cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a);
 
@@ -218,6 +232,7 @@ struct AttnArgs {
   // 0: 4 warps per block (two blocks per SM); 1: the wide variant, 8 warps per block at head_dim 128
   // (16 at 64), one block per SM, for long contexts
   int32_t wide;
+  uint32_t* err;  // kErrBounds when a table entry is outside the pool
 };
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch);
 constexpr int kAttnMaxGroups = 8;

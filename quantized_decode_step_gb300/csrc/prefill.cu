@@ -100,6 +100,12 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
                 kPipeMaxBatch);
   mag_status rs = reserve_blocks(c, what, need);
   if (rs != MAG_OK) return rs;
+  {
+    int32_t keys[MAG_MAX_BATCH];
+    for (int i = 0; i < n_seg; ++i) keys[i] = c->sessions[sids[i]].len + ntok[i];
+    rs = stats_begin(c, 2, T, out_rows, keys, n_seg);
+    if (rs != MAG_OK) return rs;
+  }
   // step arguments of the output rows' LM head (or final hidden state)
   const int slot = c->ring_pos;
   CUDA_TRY(c, cudaEventSynchronize(c->ring_ev[slot]));
@@ -108,6 +114,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
   sa.batch = out_rows;
   sa.out = out;
   PrefillAttnArgs pa = {};
+  pa.err = c->d_err;
   pa.n_seg = n_seg;
   RowList last = {};
   last.n = n_seg;
@@ -196,6 +203,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
     CUDA_TRY(c, launch_tc_gemm(L, c->map_xn, gq, EPI_QKV));
     // the chunk's k, v into the pool, then causal attention over the pool
     KvChunkArgs kc = {};
+    kc.err = c->d_err;
     kc.qkv = c->pf_qkv;
     kc.qkv_ld = c->R;
     kc.n_heads = c->Hq;
@@ -259,7 +267,7 @@ mag_status run_chunk(mag_ctx* c, const char* what, int n_seg, const int32_t* sid
   }
   c->last_launches = n;
   for (int i = 0; i < n_seg; ++i) c->sessions[sids[i]].len += ntok[i];
-  return MAG_OK;
+  return stats_end(c);
 }
 
 }  // namespace mag

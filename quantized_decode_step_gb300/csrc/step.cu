@@ -56,6 +56,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
     }
     if (verify) {  // the B tokens' k and v into the pool
       KvChunkArgs kc = {};
+      kc.err = c->d_err;
       kc.qkv = c->qkv;
       kc.qkv_ld = c->R;
       kc.n_heads = c->Hq;
@@ -87,6 +88,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
       a.n_split = std::min(csz, (S + a.n_groups - 1) / a.n_groups);
       a.part = c->attn_part;
       a.arrivals = c->attn_arrivals;
+      a.err = c->d_err;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
     {  // O projection + residual
@@ -117,6 +119,9 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
     MAG_RUN(MAG_OP_LM_HEAD, launch_gemv(L, a, W_F16, XSRC_RESID, EPI_STORE_OUT));
   } else {
     MAG_RUN(MAG_OP_LM_HEAD, launch_final_hidden(L, c->d_args, c->r, c->D, B));
+  }
+  if (c->canary_band) {  // debug: the arena tensors' canary bands are intact
+    if ((e = launch_arena_check(L, arena_check_args(c))) != cudaSuccess) return e;
   }
 #undef MAG_RUN
   return cudaSuccess;
@@ -283,6 +288,31 @@ void adapt_after_step(mag_ctx* c, int B, const int32_t* lens) {
 
 // Launches the step of B rows whose arguments were just uploaded: the captured graph of that shape
 // under the plan in use (captured on first use), or the kernels one by one under MAG_FLAG_NO_GRAPH.
+mag_status stats_begin(mag_ctx* c, int kind, int rows, int out_rows, const int32_t* keys, int n_keys_rows) {
+  mag_step_stats& s = c->stats;
+  const uint64_t per_token = mag_kv_bytes_per_token(&c->cfg);
+  uint64_t kv = 0;
+  int most = 0;
+  for (int i = 0; i < n_keys_rows; ++i) {
+    kv += (uint64_t)keys[i] * per_token;
+    most = std::max(most, (int)keys[i]);
+  }
+  s.last_kind = kind;
+  s.last_rows = rows;
+  s.last_max_keys = most;
+  s.last_bytes = (uint64_t)c->wbytes + kv + (uint64_t)rows * c->D * 2 + (uint64_t)out_rows * (c->V ? c->V : c->D) * 2;
+  c->step_timed = (c->cfg.flags & MAG_FLAG_STEP_TIMING) != 0;
+  if (c->step_timed) CUDA_TRY(c, cudaEventRecord(c->ev_step[0], c->stream));
+  return MAG_OK;
+}
+
+mag_status stats_end(mag_ctx* c) {
+  c->stats.steps += 1;
+  c->stats.last_launches = c->last_launches;
+  if (c->step_timed) CUDA_TRY(c, cudaEventRecord(c->ev_step[1], c->stream));
+  return MAG_OK;
+}
+
 mag_status launch_step(mag_ctx* c, int B, bool verify) {
   const AttnShape sh = attn_shape(c, B);
   if (c->cfg.flags & MAG_FLAG_NO_GRAPH) {
@@ -322,10 +352,15 @@ mag_status mag_decode_step(mag_ctx* c, int32_t B, const int32_t* sids, const voi
   if (st != MAG_OK) return st;
   st = step_upload(c, B, sids, in, out);
   if (st != MAG_OK) return st;
+  int32_t lens[MAG_MAX_BATCH];
+  for (int b = 0; b < B; ++b) lens[b] = c->sessions[sids[b]].len + 1;  // the keys row b attends
+  st = stats_begin(c, 0, B, B, lens, B);
+  if (st != MAG_OK) return st;
   st = launch_step(c, B, false);
   if (st != MAG_OK) return st;
-  int32_t lens[MAG_MAX_BATCH];
-  for (int b = 0; b < B; ++b) lens[b] = ++c->sessions[sids[b]].len;
+  st = stats_end(c);
+  if (st != MAG_OK) return st;
+  for (int b = 0; b < B; ++b) ++c->sessions[sids[b]].len;
   adapt_after_step(c, B, lens);
   return pool_trim(c);
 }

@@ -44,10 +44,14 @@ static mag_status verify_on_step(mag_ctx* c, int32_t sid, int32_t n, const void*
   CUDA_TRY(c, cudaMemcpyAsync(c->d_args, &a, sizeof a, cudaMemcpyHostToDevice, c->stream));
   CUDA_TRY(c, cudaEventRecord(c->ring_ev[slot], c->stream));
   c->ring_pos = (slot + 1) % kRing;
-  st = launch_step(c, n, true);
-  if (st != MAG_OK) return st;
   int32_t lens[MAG_MAX_BATCH];
   for (int b = 0; b < n; ++b) lens[b] = s.len + b + 1;
+  st = stats_begin(c, 1, n, n, lens, n);
+  if (st != MAG_OK) return st;
+  st = launch_step(c, n, true);
+  if (st != MAG_OK) return st;
+  st = stats_end(c);
+  if (st != MAG_OK) return st;
   s.len += n;
   adapt_after_step(c, n, lens);
   return pool_trim(c);

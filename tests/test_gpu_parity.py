@@ -123,7 +123,8 @@ def test_tiny_decode_matches_oracle(dt):
     assert ctx.last_step_launches() == 1 + 5 * TINY.n_layers + 1
 
 
-@pytest.mark.parametrize("flags", [mag.FLAG_NO_GRAPH, mag.FLAG_NO_PDL, mag.FLAG_ARENA_NO_REUSE])
+@pytest.mark.parametrize("flags", [mag.FLAG_NO_GRAPH, mag.FLAG_NO_PDL, mag.FLAG_ARENA_NO_REUSE, mag.FLAG_DEBUG_CANARY,
+                                   mag.FLAG_STEP_TIMING])
 def test_tiny_decode_modes(flags):
     _run_decode(TINY_DECODE, 12, n_steps=2, flags=flags)
 

@@ -87,7 +87,7 @@ def _c_layout(struct, fields):
 
 @pytest.mark.parametrize("struct,cls", [("mag_config", "Config"), ("mag_memory_stats", "MemoryStats"),
                                         ("mag_adapt_config", "AdaptConfig"), ("mag_profile", "Profile"),
-                                        ("mag_arena_tensor", "ArenaTensor")])
+                                        ("mag_arena_tensor", "ArenaTensor"), ("mag_step_stats", "StepStats")])
 def test_binding_structs_match_the_header(struct, cls):
     """The ctypes mirrors of the header's structs have the C compiler's size and field offsets."""
     c = getattr(mag, cls)
