@@ -156,29 +156,42 @@ __device__ __forceinline__ void gemv_pipe_body(const GemvArgs& a) {
   uint32_t round = 0;
   int issued = min(NS, nf);  // fills issued so far
   if constexpr (WIN) {
+    // the current slot (as a pointer and as a 32-bit shared address) and its barrier
     const uint4* zero4 = reinterpret_cast<const uint4*>(smem + L.zero);
+    const uint32_t ring_a = smem_u32(ring), bar0_a = smem_u32(full);
+    uint32_t slot_a = ring_a, bar_a = bar0_a;
+    const uint8_t* sp = ring;
+    const uint8_t* nsrc = src + (int64_t)NS * SB;  // the fill that goes into the slot just read
+    int nleft = n - NS * SC;                        // and its pairs
     for (int f = 0; f < nf; ++f) {
       if (!dead) {
-        if (!__all_sync(0xffffffffu, mbar_wait(full + slot, round & 1, a.wait_limit))) {
-          if (lane == 0) atomicOr(a.err, 4u);
-          dead = true;
+        bool ok = mbar_try_wait_a(bar_a, round & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = mbar_wait_a(bar_a, round & 1, a.wait_limit);
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) atomicOr(a.err, 4u);
+            dead = true;
+          }
         }
       }
-      const uint8_t* sp = ring + (size_t)slot * SB;
       uint4 w[SC], smq;
 #pragma unroll
       for (int i = 0; i < SC; ++i) w[i] = *reinterpret_cast<const uint4*>(sp + i * CB + lane * 16);  // codes
       // (scale, min) of the window's groups 2t, 2t+1 (chunk t): rows g and g+8
       smq = *reinterpret_cast<const uint4*>(sp + t * CB + 512 + g * 16);
       __syncwarp();
-      if (!dead && f + NS < nf) {  // the slot is in registers: refill it
-        if (lane == 0) issue(f + NS);
+      if (!dead && nleft > 0) {  // the slot is in registers: refill it (lane 0)
+        bulk_copy_a(lane == 0, slot_a, nsrc, (uint32_t)min(SC, nleft) * CB, bar_a);
         ++issued;
       }
-      if (++slot == NS) {
-        slot = 0;
-        ++round;
-      }
+      nsrc += SB;
+      nleft -= SC;
+      const bool wrap = ++slot == NS;
+      slot = wrap ? 0 : slot;
+      round += wrap ? 1u : 0u;
+      slot_a = wrap ? ring_a : slot_a + SB;
+      bar_a = wrap ? bar0_a : bar_a + 8;
+      sp = wrap ? ring : sp + SB;
       if (dead) continue;
       // column j of the MMAs = group j of the window: lane (g, t) feeds its activations only for j == g
       float d0[4], d1[4];

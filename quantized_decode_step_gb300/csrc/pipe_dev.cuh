@@ -60,6 +60,35 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// The same on 32-bit shared-memory addresses (the window loop keeps its slot and barrier addresses in
+// registers, so that nothing is converted per use).
+__device__ __forceinline__ bool mbar_try_wait_a(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(b), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_a(uint32_t b, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait_a(b, parity)) return true;
+  return false;
+}
+// Arm the barrier for `bytes` and copy them, in the lanes where `on` is set (no branch around it).
+__device__ __forceinline__ void bulk_copy_a(bool on, uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.u32 q, %4, 0;\n\t"
+      "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %2;\n\t"
+      "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "r"((uint32_t)on)
+      : "memory");
+}
+
 // D = A * B (fp16 in, fp32 out) with a zero accumulator.
 __device__ __forceinline__ void mma_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                       uint32_t b1) {
