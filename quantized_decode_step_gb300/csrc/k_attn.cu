@@ -295,8 +295,15 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   __shared__ float s_pm[8], s_pl[8];  // this block's partial (m, l) per head
   __shared__ __half s_kv[2][D];
   __shared__ float s_red[8];
+  // inbox of the cluster merge: every rank's partial o of this rank's share of the outputs, [rank][share],
+  // and every rank's (m, l) per head
+  __shared__ __align__(16) float s_in_o[8 * D + 16];
+  __shared__ float s_in_m[16][8], s_in_l[16][8];
 
   cg::cluster_group cluster = cg::this_cluster();
+  // the first half of a split barrier: its wait (before the first store into another rank's shared memory)
+  // then only confirms that every block of the cluster has started
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int split = blockIdx.x, gk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, t = lane & 3;
   const int Hq = a.n_heads, Hkv = a.n_kv_heads, G = Hq / Hkv;
@@ -574,29 +581,31 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
     for (int w = 0; w < NWARP; ++w) sum += s_acc[(w * 8 + h) * D + dim];
     s_po[idx] = sum;
   }
-  // ---- merge the cluster's splits through distributed shared memory: every output reads the S
-  // partials (m, l, o) in one round trip
-  cluster.sync();
+  // ---- merge the cluster's splits through distributed shared memory: every rank stores its partials of
+  // each rank's share of the outputs into that rank's inbox, then combines its own share from its inbox
   const int rank = (int)cluster.block_rank();
-  const int per = (G * D + S - 1) / S;  // this rank's share of the outputs
+  const int per = (G * D + S - 1) / S;  // outputs of one rank's share
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  for (int idx = tid; idx < G * D; idx += blockDim.x) {
+    const int r = idx / per;
+    *cluster.map_shared_rank(&s_in_o[rank * per + (idx - r * per)], r) = s_po[idx];
+  }
+  if (tid < S * G) {
+    const int r = tid / G, h = tid - r * G;
+    *cluster.map_shared_rank(&s_in_m[rank][h], r) = s_pm[h];
+    *cluster.map_shared_rank(&s_in_l[rank][h], r) = s_pl[h];
+  }
+  cluster.sync();  // release / acquire: every inbox is complete
   for (int idx = rank * per + tid; idx < min((rank + 1) * per, G * D); idx += blockDim.x) {
-    const int h = idx / D;
-    float mq[16], lq[16], oq[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      mq[q] = q < S ? *cluster.map_shared_rank(&s_pm[h], q) : -INFINITY;
-      lq[q] = q < S ? *cluster.map_shared_rank(&s_pl[h], q) : 0.f;
-      oq[q] = q < S ? *cluster.map_shared_rank(&s_po[idx], q) : 0.f;
-    }
-    float mm = mq[0];
-#pragma unroll
-    for (int q = 1; q < 16; ++q) mm = fmaxf(mm, mq[q]);
+    const int h = idx / D, j = idx - rank * per;
+    float mm = -INFINITY;
+    for (int q = 0; q < S; ++q) mm = fmaxf(mm, s_in_m[q][h]);
     float l = 0.f, o = 0.f;
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float e = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mm);
-      l = fmaf(lq[q], e, l);
-      o = fmaf(oq[q], e, o);
+    for (int q = 0; q < S; ++q) {
+      const float mq = s_in_m[q][h];
+      const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
+      l = fmaf(s_in_l[q][h], e, l);
+      o = fmaf(s_in_o[q * per + j], e, o);
     }
     if (K == 1) {
       a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
@@ -636,7 +645,6 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
       if (tid == 0) a.arrivals[(int64_t)b * Hkv + gk] = 0u;  // ready for the next launch
     }
   }
-  cluster.sync();  // keep this block's shared memory alive until every rank has read it
 }
 
 // ---------------------------------------------------------------- chunked prefill
