@@ -774,6 +774,83 @@ def run_plans(args):
                       "unit": "ms per decode step", "workload": "8b decode, 1 session; contexts per KV type"}))
 
 
+def run_timeline(args):
+    """Measurement aid: the phases of one decode step of the workload (8B, batch 1, FP16 KV at 2048 by
+    default) from the step timeline (mag_debug_timeline: the step's launches made one by one with
+    programmatic dependent launch, their blocks stamping the GPU's global timer). Per launch kind, the mean
+    over the middle layers of: streaming = the median block's activations staged -> the first block of
+    the next launch entering (an SM freed); tail = first to last block of the next launch entering;
+    boundary = the last block of the next launch entering -> its median block staged (the wait on this
+    launch's completion and the next staging). Attention: entry -> after its wait, -> keys done, -> last
+    block's end. Also the step's timeline length against the graph-replayed step. Prints one JSON line."""
+    import torch
+    import quantized_decode_step_gb300 as mag
+    from quantized_decode_step_gb300 import timeline as tl
+    from synth import driver, hidden_f16
+    mag.build()
+    wl = workload_by_name(args.workload, args.seed)
+    shape = wl.shape
+    ctx, sids = driver.setup(wl, args.seed, extra_tokens=args.warmup + args.steps + 8)
+    lens = [ctx.session_length(s) for s in sids]
+    x = torch.from_numpy(hidden_f16(args.seed, wl.batch, shape.hidden, tag="x.step0")).cuda()
+    out = torch.empty((wl.batch, shape.vocab or shape.hidden), dtype=torch.float16, device="cuda")
+    for _ in range(args.warmup):
+        ctx.decode_step(sids, x, out)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        ctx.decode_step(sids, x, out)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
+    e1.record()
+    e1.synchronize()
+    graph_ms = e0.elapsed_time(e1) / args.steps
+    recs = torch.zeros((1 << 18, 4), dtype=torch.int64, device="cuda")
+    for _ in range(3):  # the last of three
+        n = ctx.timeline(sids, x, out, recs)
+        for sid, p in zip(sids, lens):
+            ctx.session_truncate(sid, p)
+    Ls = tl.launches(recs[:min(n, recs.shape[0])].cpu().numpy())
+    names = {(shape.qkv_rows // 16, shape.hidden // 64): "qkv",
+             (shape.hidden // 16, shape.n_heads * shape.head_dim // 64): "o",
+             (2 * shape.ffn // 16, shape.hidden // 64): "gate_up", (shape.hidden // 16, shape.ffn // 64): "down"}
+    kinds = []
+    for L in Ls:
+        cls, a, b, _ = L["kind"]
+        kinds.append("attention" if cls == tl.ATTN else names.get((a, b), f"gemv{a}x{b}"))
+    us = lambda v: v / 1000.0
+    per = {}
+    L_ = shape.n_layers
+    for i in range(len(Ls) - 1):
+        if i < 5 or i > len(Ls) - 7:
+            continue  # the middle layers
+        e, en = Ls[i]["ev"], Ls[i + 1]["ev"]
+        d = per.setdefault(kinds[i], {})
+        if Ls[i]["kind"][0] == tl.ATTN:
+            d.setdefault("wait_us", []).append(us(e[1][len(e[1]) // 2] - e[0][0]))
+            d.setdefault("keys_us", []).append(us(e[2][len(e[2]) // 2] - e[1][len(e[1]) // 2]))
+            d.setdefault("merge_us", []).append(us(e[3][-1] - e[2][len(e[2]) // 2]))
+            d.setdefault("to_next_ready_us", []).append(us(en[2 if Ls[i + 1]["kind"][0] == tl.GEMV else 1][len(en[0]) // 2] - e[3][-1]))
+        else:
+            ready = e[2][len(e[2]) // 2]
+            nready = en[2 if Ls[i + 1]["kind"][0] == tl.GEMV else 1]
+            d.setdefault("streaming_us", []).append(us(en[0][0] - ready))
+            d.setdefault("tail_us", []).append(us(en[0][-1] - en[0][0]))
+            d.setdefault("boundary_us", []).append(us(nready[len(nready) // 2] - en[0][-1]))
+    summary = {k: {m: round(float(np.mean(v)), 2) for m, v in d.items()} for k, d in per.items()}
+    qkv = [Ls[i]["ev"][0][0] for i in range(len(Ls)) if kinds[i] == "qkv"]
+    first = min(L["ev"][0][0] for L in Ls)
+    last = max(max(v[-1] for v in L["ev"].values()) for L in Ls)
+    print(json.dumps({"timeline": summary, "layer_us": round(float(np.mean(np.diff(qkv))) / 1000, 2),
+                      "layers": L_, "launches": len(Ls), "records": int(n), "span_ms": round((last - first) / 1e6, 4),
+                      "graph_step_ms": round(graph_ms, 4), "workload": wl.name,
+                      "note": "span_ms: first to last stamp of the timeline step (launched one by one); the LM "
+                              "head's streaming is not in span_ms (no stamp after its staging)"}))
+
+
 def run_elastic(args):
     """Measurement aid for the elastic KV pool: the 8B decode step (one FP16 session, context 2048) with a
     fixed and with an elastic pool, and the elastic pool's own costs: an append that maps a new group
@@ -852,6 +929,8 @@ def main():
                     help="measurement aid: decode step time per attention split count and context, then exit")
     ap.add_argument("--elastic", action="store_true",
                     help="measurement aid: decode step and map / release costs of the elastic KV pool, then exit")
+    ap.add_argument("--timeline", action="store_true",
+                    help="measurement aid: the phases of one decode step from the device timeline, then exit")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: the same per-layer shapes with fewer layers (not a bench configuration)")
     args = ap.parse_args()
@@ -861,6 +940,9 @@ def main():
         return
     if args.elastic:
         run_elastic(args)
+        return
+    if args.timeline:
+        run_timeline(args)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -449,6 +449,20 @@ mag_status mag_debug_profile_step(mag_ctx* ctx, int32_t batch, const int32_t* se
 mag_status mag_debug_step_residuals(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host,
                                     const void* hidden_in_dev, void* out_dev, void* resid_dev);
 
+/* Step timeline ([Magnitude] 3.1: the load profile times each operator through built-in timing hooks;
+ * here per kernel phase): one decode step like
+ * mag_decode_step, its launches made one by one (with programmatic dependent launch, as in the step graph)
+ * with a record buffer in their arguments. The GEMV and attention blocks append records of four uint64
+ * {tag, block, event, time} to recs_dev (device memory, caller-owned, room for `cap` records = 32 cap
+ * bytes): tag (1 << 60) | n_mtiles << 32 | n_chunks << 8 | batch for a GEMV, (2 << 60) | layer for
+ * attention; block = blockIdx.x | y << 20 | z << 40; time = the GPU's global timer in ns. GEMV events: 0
+ * block entry, 1 before its wait on the previous kernel (its first weight copies issued), 2 activations
+ * staged. Attention events: 0 entry, 1 after the wait, 2 keys done, 3 end. Records past cap are dropped;
+ * *n_out = the records attempted. The session lengths advance as in a step; synchronises the stream.
+ * Errors: as mag_decode_step; INVALID_ARG for a null buffer or count, cap < 0. */
+mag_status mag_debug_timeline(mag_ctx* ctx, int32_t batch, const int32_t* session_ids_host, const void* hidden_in_dev,
+                              void* out_dev, void* recs_dev, int32_t cap, int32_t* n_out);
+
 /* Failure injection for tests ([Magnitude] 5.1-5.2: the engine's error behaviour): the number of polls a
  * decode GEMV's pipeline wait (for its weight copies to land in shared memory) makes before it gives up.
  * polls < 0 restores the built-in limit (2^22); 0 makes every such wait give up at once, as if the copies

@@ -32,7 +32,7 @@ EXPORTED = [
     "mag_verify_tokens", "mag_prefill_batch", "mag_sync",
     "mag_get_memory_stats", "mag_get_step_stats", "mag_last_error", "mag_kv_bytes_per_token", "mag_quantize_w4g32",
     "mag_debug_read_weights", "mag_debug_kv_locate", "mag_debug_pool", "mag_debug_arena_plan",
-    "mag_debug_last_step_launches", "mag_debug_profile_step", "mag_debug_step_residuals",
+    "mag_debug_last_step_launches", "mag_debug_profile_step", "mag_debug_step_residuals", "mag_debug_timeline",
     "mag_debug_prefill_residuals", "mag_debug_set_wait_limit",
     "mag_debug_fail_allocations", "mag_debug_set_table_entry", "mag_debug_arena",
     "mag_adapt_defaults", "mag_set_adaptive", "mag_get_profile", "mag_profiler_create", "mag_profiler_destroy",
@@ -144,6 +144,7 @@ def lib():
                 "mag_debug_profile_step": ([vp, i32, P32, vp, vp, P32, ctypes.POINTER(ctypes.c_float), i32, P32],
                                            i32),
                 "mag_debug_step_residuals": ([vp, i32, P32, vp, vp, vp], i32),
+                "mag_debug_timeline": ([vp, i32, P32, vp, vp, vp, i32, P32], i32),
                 "mag_debug_prefill_residuals": ([vp, i32, i32, vp, vp, vp], i32),
                 "mag_debug_set_wait_limit": ([vp, i64], i32),
                 "mag_debug_fail_allocations": ([i32, i32], None),
@@ -397,6 +398,15 @@ class Context:
         ids = (ctypes.c_int32 * len(sessions))(*sessions)
         self._check(lib().mag_debug_step_residuals(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out),
                                                    _ptr(resid)), "mag_debug_step_residuals")
+
+    def timeline(self, sessions, hidden_in, out, recs):
+        """One step (launched one by one, as the graph holds it) whose GEMV and attention blocks stamp their
+        phases into recs (device uint64 [cap, 4]: tag, block, event, ns); returns the records attempted."""
+        ids = (ctypes.c_int32 * len(sessions))(*sessions)
+        n = ctypes.c_int32(0)
+        self._check(lib().mag_debug_timeline(self.h, len(sessions), ids, _ptr(hidden_in), _ptr(out), _ptr(recs),
+                                             int(recs.shape[0]), ctypes.byref(n)), "mag_debug_timeline")
+        return n.value
 
     def debug_set_table_entry(self, sid: int, index: int, value: int):
         """Write one block-table entry on the device only (tests of the block-id checks)."""

@@ -285,6 +285,7 @@ GemvArgs gemv_args(const mag_ctx* c, int kind, const uint8_t* w, int n_mtiles, i
   a.partial = c->gemv_part;
   a.counters = c->d_counters;
   a.step = c->d_args;
+  a.trace = c->trace;
   return a;
 }
 
@@ -311,6 +312,7 @@ void free_ctx(mag_ctx* c) {
   cudaFree(c->d_sin);
   cudaFree(c->arena);
   cudaFree(c->d_counters);
+  cudaFree(c->trace_n);
   cudaFree(c->attn_part);
   cudaFree(c->attn_arrivals);
   cudaFree(c->d_args);

@@ -63,6 +63,28 @@ __device__ __forceinline__ uint8_t* pool_vec(const PoolGeom& g, int layer, int b
   }
 }
 
+// Step timeline (debug aid): with rec set, kernels append records of four u64 (tag, block (x | y << 20 |
+// z << 40), event, %globaltimer in ns) at their phase boundaries; n counts the records attempted (those
+// past cap are dropped). Passed in the kernels' arguments, so that a disabled timeline costs a parameter
+// read per stamp point.
+struct TraceBuf {
+  unsigned long long* rec;
+  unsigned int* n;
+  unsigned int cap;
+};
+constexpr unsigned long long kTraceGemv = 1ull << 60, kTraceAttn = 2ull << 60;
+__device__ __forceinline__ void trace_stamp(const TraceBuf& tb, unsigned long long tag, unsigned int ev) {
+  if (!tb.rec) return;
+  const unsigned int i = atomicAdd(tb.n, 1u);
+  if (i >= tb.cap) return;
+  unsigned long long ts;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ts));
+  ulonglong2* r = reinterpret_cast<ulonglong2*>(tb.rec + 4ull * i);
+  r[0] = make_ulonglong2(tag, ((unsigned long long)blockIdx.z << 40) | ((unsigned long long)blockIdx.y << 20) |
+                                  blockIdx.x);
+  r[1] = make_ulonglong2(ev, ts);
+}
+
 // Programmatic dependent launch: wait for the producer grid's memory, and let
 // the next grid's blocks start their prologue early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

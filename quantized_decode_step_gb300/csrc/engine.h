@@ -117,6 +117,9 @@ struct mag_ctx {
   __half* qkv = nullptr;
   __half* o = nullptr;
   float* ss_part = nullptr;
+  // step timeline (mag_debug_timeline): the record buffer the next launches stamp into (rec null: off)
+  TraceBuf trace = {};
+  unsigned int* trace_n = nullptr;
   __half* act = nullptr;
   float* gemv_part = nullptr;
 

@@ -305,6 +305,8 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   // then only confirms that every block of the cluster has started
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int split = blockIdx.x, gk = blockIdx.y, b = blockIdx.z;
+  const unsigned long long ttag = kTraceAttn | (unsigned)a.layer;
+  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, t = lane & 3;
   const int Hq = a.n_heads, Hkv = a.n_kv_heads, G = Hq / Hkv;
   const int S = a.n_split;  // == cluster size
@@ -345,6 +347,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   phys_new = a.step->blk[b];  // the host's copy of table[new_blk]: no table read after the wait
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 1);
   const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
 
   // the block that holds the new token appends its K (rotated) and V to the pool
@@ -581,6 +584,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
     for (int w = 0; w < NWARP; ++w) sum += s_acc[(w * 8 + h) * D + dim];
     s_po[idx] = sum;
   }
+  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 2);
   // ---- merge the cluster's splits through distributed shared memory: every rank stores its partials of
   // each rank's share of the outputs into that rank's inbox, then combines its own share from its inbox
   const int rank = (int)cluster.block_rank();
@@ -645,6 +649,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
       if (tid == 0) a.arrivals[(int64_t)b * Hkv + gk] = 0u;  // ready for the next launch
     }
   }
+  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 3);
 }
 
 // ---------------------------------------------------------------- chunked prefill

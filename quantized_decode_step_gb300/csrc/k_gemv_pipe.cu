@@ -49,6 +49,12 @@ __device__ __forceinline__ void gemv_pipe_body(const GemvArgs& a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int C = a.n_chunks, NS = a.stages;
   const int n_cta = gridDim.x, blk = blockIdx.x;
+  // step timeline stamps (the tag is rebuilt from the arguments at each, so that nothing stays live)
+  auto stamp = [&](unsigned int ev) {
+    trace_stamp(a.trace, kTraceGemv | ((unsigned long long)a.n_mtiles << 32) | ((unsigned long long)a.n_chunks << 8) | B,
+                ev);
+  };
+  if (tid == 0) stamp(0);
   const int T0 = (int)((int64_t)blk * a.n_mtiles / n_cta), T1 = (int)((int64_t)(blk + 1) * a.n_mtiles / n_cta);
   const int T = T1 - T0, P = T * C;  // the block's (tile, chunk) pairs, tile-major
   constexpr bool win = WIN;
@@ -79,12 +85,14 @@ __device__ __forceinline__ void gemv_pipe_body(const GemvArgs& a) {
   if (tid <= kCWarps) bounds[tid] = run_lo(tid);  // read after the staging's barriers
   __syncwarp();
 
+  if (tid == 0) stamp(1);
   pdl_wait();
   pdl_trigger();
   const uint32_t xrow = C * 64 + 8, grow = 2 * C + 2;
   __half* xw = reinterpret_cast<__half*>(smem + L.x);
   float* xsw = reinterpret_cast<float*>(smem + L.xs);
   stage_x<WFMT, XSRC, B>(a, xw, xsw, reinterpret_cast<float*>(smem + L.red), xrow, grow, [] {});
+  if (tid == 0) stamp(2);
   // the rest of the ring is filled once the activations are in: their loads must not queue behind it
   if (lane == 0)
     for (int f = kPreFills; f < min(NS, nf); ++f) issue(f);

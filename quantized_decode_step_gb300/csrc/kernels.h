@@ -62,6 +62,8 @@ struct GemvArgs {
   int32_t n_q_heads;
   int32_t layer;
   PoolGeom pool;
+  TraceBuf trace;  // step timeline (debug): block stamps at entry (0), before the wait on the previous
+                   // kernel (1), activations staged (2); tag kTraceGemv | n_mtiles << 32 | n_chunks << 8 | B
 };
 
 // Polls of a bounded mbarrier wait before it is declared stuck (main-loop default; drain waits always).
@@ -233,6 +235,8 @@ struct AttnArgs {
   // (16 at 64), one block per SM, for long contexts
   int32_t wide;
   uint32_t* err;  // kErrBounds when a table entry is outside the pool
+  TraceBuf trace;  // step timeline (debug): stamps at entry (0), after the wait (1), keys done (2), end (3);
+                   // tag kTraceAttn | layer
 };
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, int batch);
 constexpr int kAttnMaxGroups = 8;

@@ -89,6 +89,7 @@ cudaError_t record_step(mag_ctx* c, int B, int* n_launch, Profiler* prof, bool v
       a.part = c->attn_part;
       a.arrivals = c->attn_arrivals;
       a.err = c->d_err;
+      a.trace = c->trace;
       MAG_RUN(MAG_OP_ATTENTION, launch_attention(L, a, B));
     }
     {  // O projection + residual
@@ -396,6 +397,36 @@ mag_status mag_debug_step_residuals(mag_ctx* c, int32_t B, const int32_t* sids, 
   CUDA_TRY(c, record_step(c, B, &n, nullptr, false, sh.splits, sh.wide, c->stream, static_cast<float*>(resid)));
   for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  c->last_launches = n;
+  return check_err(c);
+}
+
+mag_status mag_debug_timeline(mag_ctx* c, int32_t B, const int32_t* sids, const void* in, void* out, void* recs,
+                              int32_t cap, int32_t* n_out) {
+  if (!c) return MAG_ERR_INVALID_ARG;
+  if (!recs || cap < 0 || !n_out) return fail(c, MAG_ERR_INVALID_ARG, "debug_timeline: null buffer or count");
+  mag_status st = finish_capture(c);
+  if (st != MAG_OK) return st;
+  if (!c->trace_n) {
+    cudaError_t e = dev_malloc(&c->trace_n, sizeof(unsigned int));
+    if (e != cudaSuccess) return fail(c, MAG_ERR_OOM, "debug_timeline: counter: %s", cudaGetErrorString(e));
+  }
+  st = step_upload(c, B, sids, in, out);
+  if (st != MAG_OK) return st;
+  CUDA_TRY(c, cudaMemsetAsync(c->trace_n, 0, sizeof(unsigned int), c->stream));
+  c->trace = TraceBuf{static_cast<unsigned long long*>(recs), c->trace_n, (unsigned int)cap};
+  int n = 0;
+  const AttnShape sh = attn_shape(c, B);
+  // the step's launches as the graph holds them (programmatic dependent launch included), but launched
+  // one by one so that their arguments carry the record buffer
+  const cudaError_t e = record_step(c, B, &n, nullptr, false, sh.splits, sh.wide, c->stream);
+  c->trace = TraceBuf{};
+  CUDA_TRY(c, e);
+  for (int b = 0; b < B; ++b) c->sessions[sids[b]].len += 1;
+  unsigned int got = 0;
+  CUDA_TRY(c, cudaMemcpyAsync(&got, c->trace_n, sizeof got, cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  *n_out = (int32_t)std::min<unsigned int>(got, 0x7fffffffu);
   c->last_launches = n;
   return check_err(c);
 }

@@ -9,7 +9,11 @@
 * The block-id checks: a block-table entry outside the pool, written on the device only, is not used (the
   attention kernel reads block 0 instead) and the next mag_sync returns MAG_ERR_CORRUPT; the host then
   rewrites the device tables from its own copy, and the same step again matches the oracle.
+* The step timeline (mag_debug_timeline): every GEMV and attention launch of the step is there with all its
+  blocks and their events in order, and the stamped step's output is the plain step's, bit for bit.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -153,3 +157,46 @@ def test_block_id_outside_the_pool_is_not_used():
     ctx.sync()
     _check(out.cpu().numpy(), oracle.forward(cfg, w, [kv], [1], x, c, s), "the step after the report")
     ctx.close()
+
+
+@pytest.mark.parametrize("shape", [TINY, dataclasses.replace(TINY, name="tiny-2L-v512", n_layers=2, vocab=512)])
+def test_timeline(shape):
+    from quantized_decode_step_gb300 import timeline as tl
+    wl = Workload("tiny-timeline", shape, KV_FP16, 1, (37,))
+    ctx, sids = driver.setup(wl, SEED, extra_tokens=8)
+    sid, p = sids[0], wl.prior[0]
+    x = torch.from_numpy(synth.hidden_f16(SEED, 1, shape.hidden, tag="tl0")).cuda()
+    width = shape.vocab or shape.hidden
+    out1 = torch.empty((1, width), dtype=torch.float16, device="cuda")
+    out2 = torch.empty_like(out1)
+    ctx.decode_step([sid], x, out1)
+    ctx.sync()
+    ctx.session_truncate(sid, p)
+    recs = torch.zeros((4096, 4), dtype=torch.int64, device="cuda")
+    n = ctx.timeline([sid], x, out2, recs)
+    assert ctx.session_length(sid) == p + 1
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16)), "the stamps changed the step"
+    assert 0 < n <= recs.shape[0]
+    R = recs[:n].cpu().numpy()
+    Ls = tl.launches(R)
+    kinds = [L["kind"][0] for L in Ls]
+    assert kinds.count(tl.ATTN) == shape.n_layers
+    assert kinds.count(tl.GEMV) == 4 * shape.n_layers + (1 if shape.vocab else 0)
+    for L in Ls:
+        evs = (0, 1, 2) if L["kind"][0] == tl.GEMV else (0, 1, 2, 3)
+        assert all(len(L["ev"][e]) == len(L["blocks"]) for e in evs), L["kind"]
+    # a block's records in time order: its events in order, once per launch of its tag (launches of one tag
+    # are layers apart)
+    by_block = {}
+    for tag, blk, ev, t in sorted(R.tolist(), key=lambda r: (r[3], r[2])):
+        by_block.setdefault((tag, blk), []).append(ev)
+    n_of_tag = {}
+    for L in Ls:
+        n_of_tag[L["tag"]] = n_of_tag.get(L["tag"], 0) + 1
+    for (tag, blk), evs in by_block.items():
+        one = [0, 1, 2] if (tag >> 60) == tl.GEMV else [0, 1, 2, 3]
+        assert evs == one * n_of_tag[tag], (hex(tag), blk, evs)
+    rows = tl.phases(Ls)
+    assert len(rows) == len(Ls) and rows[0]["entry_first"] == 0.0
+    ctx.close()
+
