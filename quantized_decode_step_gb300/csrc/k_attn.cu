@@ -281,7 +281,7 @@ constexpr int attn_wide_warps() {
 // (session, KV head) form a thread-block cluster and merge their splits
 // through distributed shared memory. NWARP warps per block.
 template <int D, int DT, int NWARP>
-__global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(32 * NWARP, NWARP <= 4 ? 4 : (NWARP <= 8 ? 2 : 1)) attn_kernel(const AttnArgs a) {
   namespace cg = cooperative_groups;
   using SG = SlotGeom<D, DT>;
   using AG = AccGeom<D, NWARP>;
@@ -305,8 +305,9 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   // then only confirms that every block of the cluster has started
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int split = blockIdx.x, gk = blockIdx.y, b = blockIdx.z;
-  const unsigned long long ttag = kTraceAttn | (unsigned)a.layer;
-  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 0);
+  // step timeline stamps (the tag rebuilt from the arguments at each, so that nothing stays live)
+  auto stamp = [&](unsigned int ev) { trace_stamp(a.trace, kTraceAttn | (unsigned)a.layer, ev); };
+  if (threadIdx.x == 0) stamp(0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, t = lane & 3;
   const int Hq = a.n_heads, Hkv = a.n_kv_heads, G = Hq / Hkv;
   const int S = a.n_split;  // == cluster size
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
   phys_new = a.step->blk[b];  // the host's copy of table[new_blk]: no table read after the wait
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 1);
+  if (threadIdx.x == 0) stamp(1);
   const __half* qkv = a.qkv + (int64_t)b * a.qkv_ld;
 
   // the block that holds the new token appends its K (rotated) and V to the pool
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
     for (int w = 0; w < NWARP; ++w) sum += s_acc[(w * 8 + h) * D + dim];
     s_po[idx] = sum;
   }
-  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 2);
+  if (threadIdx.x == 0) stamp(2);
   // ---- merge the cluster's splits through distributed shared memory: every rank stores its partials of
   // each rank's share of the outputs into that rank's inbox, then combines its own share from its inbox
   const int rank = (int)cluster.block_rank();
@@ -649,7 +650,7 @@ __global__ void __launch_bounds__(32 * NWARP) attn_kernel(const AttnArgs a) {
       if (tid == 0) a.arrivals[(int64_t)b * Hkv + gk] = 0u;  // ready for the next launch
     }
   }
-  if (threadIdx.x == 0) trace_stamp(a.trace, ttag, 3);
+  if (threadIdx.x == 0) stamp(3);
 }
 
 // ---------------------------------------------------------------- chunked prefill
