@@ -173,6 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_batch_kernel(const GemvArgs 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int B = a.batch, C = a.n_chunks, kw = a.ks, NS = a.stages;
   const int kwi = blockIdx.x % kw, tri = blockIdx.x / kw, tr = gridDim.x / kw;
+  // step timeline stamps (the tag rebuilt from the arguments at each, so that nothing stays live)
+  auto stamp = [&](unsigned int ev) {
+    trace_stamp(a.trace, kTraceGemv | ((unsigned long long)a.n_mtiles << 32) | ((unsigned long long)a.n_chunks << 8) |
+                             (unsigned)a.batch, ev);
+  };
+  if (tid == 0) stamp(0);
   const int T0 = (int)((int64_t)tri * a.n_mtiles / tr), T1 = (int)((int64_t)(tri + 1) * a.n_mtiles / tr);
   const int c0 = kwi * a.chunks_per_cta, c1 = min(C, c0 + a.chunks_per_cta);
   const int cb = c1 - c0, spt = (cb + kSlotChunks - 1) / kSlotChunks;  // chunks and slots per tile in the window
@@ -203,11 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_batch_kernel(const GemvArgs 
   if (tid <= kWarps) bounds[tid] = run_lo(tid);  // read after the staging's barrier
   __syncwarp();
 
+  if (tid == 0) stamp(1);
   pdl_wait();
   pdl_trigger();
   __half* xw = reinterpret_cast<__half*>(smem + L.x);
   __half* xsh = reinterpret_cast<__half*>(smem + L.xs);
   stage_window<XSRC>(a, c0, c1, xw, L.xrow, xsh, L.xsrow, reinterpret_cast<float*>(smem + L.red));
+  if (tid == 0) stamp(2);
   // the rest of the ring once the activations are in: their loads must not queue behind it
   if (lane == 0)
     for (int f = kPreFills; f < min(NS, nf); ++f) issue(f);
