@@ -277,6 +277,34 @@ constexpr int attn_wide_warps() {
   return D > 64 ? 8 : ((size_t)16 * kAttnSlots * SlotGeom<D, DT>::kBytes <= 220 * 1024 ? 16 : 8);
 }
 
+// The last block of a (row, KV head) to arrive: its K parts' (m, l, o) of the G d outputs combined in part
+// order into out. Kept out of line, so that its registers do not weigh on the attention kernel's loop.
+__device__ __noinline__ void merge_parts(const float* pb, int K, int GD, __half* out) {
+  for (int idx = threadIdx.x; idx < GD; idx += blockDim.x) {
+    // all K parts in flight at once (one round trip)
+    float mq[kAttnMaxGroups], lq[kAttnMaxGroups], oq[kAttnMaxGroups];
+#pragma unroll
+    for (int q = 0; q < kAttnMaxGroups; ++q) {
+      const float* pq = pb + (int64_t)q * 3 * GD;
+      const bool v = q < K;
+      mq[q] = v ? __ldcg(pq + idx) : -INFINITY;
+      lq[q] = v ? __ldcg(pq + GD + idx) : 0.f;
+      oq[q] = v ? __ldcg(pq + 2 * GD + idx) : 0.f;
+    }
+    float mm = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kAttnMaxGroups; ++q) mm = fmaxf(mm, mq[q]);
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int q = 0; q < kAttnMaxGroups; ++q) {
+      const float e = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mm);
+      l = fmaf(lq[q], e, l);
+      o = fmaf(oq[q], e, o);
+    }
+    out[idx] = __float2half_rn(o / l);
+  }
+}
+
 // One block of the grid per (split, KV head, session); the blocks of a
 // (session, KV head) form a thread-block cluster and merge their splits
 // through distributed shared memory. NWARP warps per block.
@@ -615,7 +643,7 @@ __global__ void __launch_bounds__(32 * NWARP, NWARP <= 4 ? 4 : (NWARP <= 8 ? 2 :
     if (K == 1) {
       a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
     } else {  // this cluster's (m, l, o) of the output, for the merge of the K clusters
-      float* pp = a.part + ((((int64_t)b * Hkv + gk) * K + split / S) * 3) * G * D;
+      float* pp = a.part + ((((int64_t)b * Hkv + gk) * kAttnMaxGroups + split / S) * 3) * G * D;
       pp[idx] = mm;  // -inf when none of the cluster's splits has a key
       pp[G * D + idx] = l;
       pp[2 * G * D + idx] = o;
@@ -633,20 +661,8 @@ __global__ void __launch_bounds__(32 * NWARP, NWARP <= 4 ? 4 : (NWARP <= 8 ? 2 :
     __syncthreads();
     if (s_last) {
       __threadfence();
-      const float* pb = a.part + (((int64_t)b * Hkv + gk) * K) * 3 * G * D;
-      for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        float mm = -INFINITY;
-        for (int q = 0; q < K; ++q) mm = fmaxf(mm, __ldcg(pb + (int64_t)q * 3 * G * D + idx));
-        float l = 0.f, o = 0.f;
-        for (int q = 0; q < K; ++q) {
-          const float* pq = pb + (int64_t)q * 3 * G * D;
-          const float mq = __ldcg(pq + idx);
-          const float e = mq == -INFINITY ? 0.f : exp2f(mq - mm);
-          l = fmaf(__ldcg(pq + G * D + idx), e, l);
-          o = fmaf(__ldcg(pq + 2 * G * D + idx), e, o);
-        }
-        a.o[(int64_t)b * a.ldo + (int64_t)gk * G * D + idx] = __float2half_rn(o / l);
-      }
+      const float* pb = a.part + (((int64_t)b * Hkv + gk) * kAttnMaxGroups) * 3 * G * D;
+      merge_parts(pb, K, G * D, a.o + (int64_t)b * a.ldo + (int64_t)gk * G * D);
       if (tid == 0) a.arrivals[(int64_t)b * Hkv + gk] = 0u;  // ready for the next launch
     }
   }

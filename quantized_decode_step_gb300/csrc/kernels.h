@@ -220,7 +220,7 @@ struct AttnArgs {
   int32_t n_split;   // cluster size (<= 16)
   int32_t n_groups;  // clusters per (session, KV head), 1..kAttnMaxGroups: grid.x = n_split * n_groups
   // n_groups > 1: per (session, KV head, cluster) the cluster's (m, l, o) of the G d outputs, fp32
-  // [B][Hkv][n_groups][3][G d], and per (session, KV head) a counter of arrived blocks (zero between
+  // [B][Hkv][kAttnMaxGroups][3][G d], and per (session, KV head) a counter of arrived blocks (zero between
   // launches: the last block to arrive merges and resets it)
   float* part;
   uint32_t* arrivals;
